@@ -1,0 +1,384 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by the mathematics.
+
+Each test checks the oracle against something other than its own formula: values the
+pages print or a worked example built from the stated layout (tests/golden/), closed
+forms, invariants, brute force with plain Python loops, and special cases that reduce
+to a library routine (torch's CPU scaled_dot_product_attention, scipy's logsumexp).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import logsumexp
+
+from oracle import pck_oracle as orc
+from prefix_cached_kv_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ------------------------------------------------------------------ mlx4g32 layout
+
+def test_layout_worked_example():
+    lines = _golden_lines("mlx4g32_layout_example.txt")
+    codes = np.array([int(v) for v in lines[0].split(":")[1].split()], dtype=np.uint8)[None, :]
+    words = [int(v, 16) for v in lines[1].split(":")[1].split()]
+    assert orc.pack_codes(codes)[0].tolist() == words
+    assert np.array_equal(orc.unpack_codes(orc.pack_codes(codes), 32), codes)
+    for ln in lines[2:]:
+        kv = dict(p.split("=") for p in ln.split(":")[1].split())
+        j, w, val = int(kv["j"]), int(kv["word"]), int(kv["value"], 16)
+        c = np.zeros((1, 32), dtype=np.uint8)
+        c[0, j] = 15
+        packed = orc.pack_codes(c)[0]
+        assert packed[w] == val and packed.sum() == val
+
+
+def test_record_sizes_printed():
+    for ln in _golden_lines("mlx4g32_record_sizes.txt"):
+        kv = dict(p.split("=") for p in ln.split())
+        d = int(kv["kv_dim"])
+        assert orc.record_bytes(d) == int(kv["record_bytes"])
+        assert 2 * d == int(kv["fp16_bytes"])
+    assert round(2048 / orc.record_bytes(1024), 1) == 3.2
+
+
+def test_record_byte_order():
+    """Record = codes words, then all scales, then all biases, little-endian."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((3, 64)).astype(np.float16)
+    codes, s, b = orc.quantize_mlx4g32(x)
+    rec = orc.pack_records(codes, s, b)
+    assert rec.shape == (3, 40)
+    for r in range(3):
+        w0 = int(rec[r, 0]) | int(rec[r, 1]) << 8 | int(rec[r, 2]) << 16 | int(rec[r, 3]) << 24
+        assert w0 & 0xF == codes[r, 0] and (w0 >> 28) & 0xF == codes[r, 7]
+        assert rec[r, 32:34].tobytes() == s[r, 0].tobytes()
+        assert rec[r, 34:36].tobytes() == s[r, 1].tobytes()
+        assert rec[r, 36:38].tobytes() == b[r, 0].tobytes()
+    c2, s2, b2 = orc.unpack_records(rec, 64)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, s) and np.array_equal(b2, b)
+
+
+# ------------------------------------------------------------------ quantiser
+
+def test_quantizer_lossless_on_grid():
+    """A group already on an fp16 affine grid {b + k s} comes back exactly."""
+    rng = np.random.default_rng(2)
+    done = 0
+    while done < 50:
+        s = np.float16(2.0 ** rng.integers(-6, 2) * (1 + rng.integers(0, 64) / 64))
+        b = np.float16(rng.integers(-64, 64) / 8)
+        k = rng.integers(0, 16, size=32)
+        k[0], k[1] = 0, 15
+        x = (np.float64(b) + k * np.float64(s)).astype(np.float16)
+        if not np.array_equal(x.astype(np.float64), np.float64(b) + k * np.float64(s)):
+            continue  # this (s, b) grid is not exactly representable in fp16; draw again
+        done += 1
+        codes, sc, bi = orc.quantize_mlx4g32(x[None, :])
+        assert sc[0, 0] == s and bi[0, 0] == b
+        assert np.array_equal(codes[0], k)
+        assert np.array_equal(orc.dequantize_mlx4g32(codes, sc, bi)[0], x.astype(np.float64))
+
+
+def test_quantizer_constant_group():
+    x = np.full((2, 64), np.float16(-1.375))
+    x[1, 32:] = np.float16(7.0)
+    codes, s, b = orc.quantize_mlx4g32(x)
+    assert (codes == 0).all() and (s == 0).all()
+    assert np.array_equal(orc.dequantize_mlx4g32(codes, s, b), x.astype(np.float64))
+
+
+def test_quantizer_error_bound_and_monotone():
+    """|x - x^| <= scale/2 (+ fp32 rounding), codes monotone in x, min -> 0 and max -> 15."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((200, 128)) * np.exp(rng.standard_normal((200, 1)))).astype(np.float16)
+    codes, s, b = orc.quantize_mlx4g32(x)
+    xh = orc.dequantize_mlx4g32(codes, s, b)
+    smax = np.repeat(s.astype(np.float64), 32, axis=1)
+    err = np.abs(xh - x.astype(np.float64))
+    assert (err <= smax * 0.5 * (1 + 1e-6) + 1e-7 * np.abs(x.astype(np.float64))).all()
+    xg = x.astype(np.float64).reshape(200, 4, 32)
+    cg = codes.reshape(200, 4, 32)
+    for r in range(200):
+        for g in range(4):
+            order = np.argsort(xg[r, g], kind="stable")
+            assert (np.diff(cg[r, g][order].astype(int)) >= 0).all()
+            assert cg[r, g][np.argmin(xg[r, g])] == 0 and cg[r, g][np.argmax(xg[r, g])] == 15
+
+
+def test_quantizer_scale_is_fp16_roundtripped():
+    """Each code is the nearest point of the grid the reader sees, {b16 + c * s16 : c in 0..15}.
+
+    The page says the scale goes through fp16 before the codes are chosen; codes picked
+    against the fp32 scale would miss the nearest reader-grid point for some elements, so the
+    test also checks that such elements exist in the sample (the pin can fail)."""
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal((400, 64)) * 3).astype(np.float16)
+    codes, s, b = orc.quantize_mlx4g32(x)
+    xg = x.astype(np.float64).reshape(400, 2, 32)
+    grid = b.astype(np.float64)[:, :, None, None] + s.astype(np.float64)[:, :, None, None] * np.arange(16)
+    dist = np.abs(xg[:, :, :, None] - grid)                         # [rows, G, 32, 16]
+    best = dist.min(axis=3)
+    mine = np.take_along_axis(dist, codes.reshape(400, 2, 32, 1).astype(np.int64), axis=3)[..., 0]
+    assert (mine <= best + 1e-9 * s.astype(np.float64)[:, :, None]).all()
+    # codes chosen against the unrounded fp32 scale disagree somewhere in this sample
+    mn = xg.min(axis=2, keepdims=True)
+    s32 = ((xg.max(axis=2, keepdims=True) - mn) / 15.0)
+    alt = np.clip(np.rint((xg - b.astype(np.float64)[:, :, None]) / s32), 0, 15)
+    assert (alt != codes.reshape(400, 2, 32)).any()
+
+
+# ------------------------------------------------------------------ dense attention
+
+def _naive_attention(q, keys, vals, tau):
+    """Pure-Python brute force: explicit loops and math.exp, no max-shift."""
+    z = [tau * sum(qd * kd for qd, kd in zip(q, k)) for k in keys]
+    w = [math.exp(zi) for zi in z]
+    tot = sum(w)
+    out = [sum(w[t] * vals[t][d] for t in range(len(keys))) / tot for d in range(len(q))]
+    return out, math.log(tot)
+
+
+def test_attention_brute_force_tiny():
+    rng = np.random.default_rng(4)
+    for N in (1, 2, 3, 5, 8):
+        D = 4
+        q = rng.standard_normal((1, 1, D))
+        K = rng.standard_normal((1, N, D))
+        V = rng.standard_normal((1, N, D))
+        O, L = orc.prefix_query(q, K, V)
+        o2, l2 = _naive_attention(q[0, 0].tolist(), K[0].tolist(), V[0].tolist(), 1 / math.sqrt(D))
+        assert np.allclose(O[0, 0], o2, rtol=1e-12, atol=1e-12)
+        assert abs(L[0, 0] - l2) < 1e-12
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(5)
+    D, N = 64, 37
+    q = rng.standard_normal((1, 1, D))
+    V = rng.standard_normal((1, N, D))
+    # N = 1: output is the single value row, LSE the single scaled logit.
+    K1 = rng.standard_normal((1, 1, D))
+    O, L = orc.prefix_query(q, K1, V[:, :1])
+    assert np.allclose(O[0, 0], V[0, 0]) and np.isclose(L[0, 0], (q[0, 0] @ K1[0, 0]) / 8.0)
+    # identical keys: mean of V, LSE = tau q.k + ln N
+    K = np.repeat(K1, N, axis=1)
+    O, L = orc.prefix_query(q, K, V)
+    assert np.allclose(O[0, 0], V[0].mean(axis=0)) and np.isclose(L[0, 0], (q[0, 0] @ K1[0, 0]) / 8 + math.log(N))
+    # Q = 0: mean of V, LSE = ln N
+    Kr = rng.standard_normal((1, N, D))
+    O, L = orc.prefix_query(np.zeros_like(q), Kr, V)
+    assert np.allclose(O[0, 0], V[0].mean(axis=0)) and np.isclose(L[0, 0], math.log(N))
+
+
+def test_attention_matches_scipy_and_torch():
+    """LSE equals scipy's logsumexp of the scaled scores; O equals torch's CPU SDPA (float64)."""
+    rng = np.random.default_rng(6)
+    H, M, N, D = 3, 5, 50, 32
+    Q = rng.standard_normal((H, M, D))
+    K = rng.standard_normal((H, N, D)) * 2
+    V = rng.standard_normal((H, N, D))
+    O, L = orc.prefix_query(Q, K, V, head_map=np.arange(H))
+    for h in range(H):
+        assert np.allclose(L[h], logsumexp(Q[h] @ K[h].T / math.sqrt(D), axis=1), atol=1e-12)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None]).numpy()[0]
+    assert np.allclose(O, ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("M,S", [(1, 16), (4, 4), (3, 7), (8, 5), (512, 512)])
+def test_causal_suffix_matches_torch_mask(M, S):
+    """Bottom-right causal suffix: the mask built with torch.tril(diagonal=S-M)."""
+    rng = np.random.default_rng(7 + M)
+    H, N, D = 2, 9, 16
+    if M == 512:
+        H, N, D = 1, 33, 16
+    Q = rng.standard_normal((H, M, D))
+    K, V = rng.standard_normal((H, N, D)), rng.standard_normal((H, N, D))
+    Ks, Vs = rng.standard_normal((H, S, D)), rng.standard_normal((H, S, D))
+    O, L = orc.prefix_query(Q, K, V, np.arange(H), Ks, Vs, causal=True)
+    mask = torch.cat([torch.ones(M, N, dtype=torch.bool), torch.ones(M, S, dtype=torch.bool).tril(diagonal=S - M)], 1)
+    q = torch.from_numpy(Q)[None]
+    k = torch.from_numpy(np.concatenate([K, Ks], 1))[None]
+    v = torch.from_numpy(np.concatenate([V, Vs], 1))[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask).numpy()[0]
+    assert np.allclose(O, ref, atol=1e-11)
+    sc = (q @ k.transpose(-1, -2))[0] / math.sqrt(D)
+    lse = torch.logsumexp(sc.masked_fill(~mask, float("-inf")), dim=-1).numpy()
+    assert np.allclose(L, lse, atol=1e-11)
+    if M == S:  # standard causal: torch's own is_causal on the suffix-only part
+        O2, _ = orc.prefix_query(Q, K[:, :0], V[:, :0], np.arange(H), Ks, Vs, causal=True)
+        ref2 = torch.nn.functional.scaled_dot_product_attention(
+            q, torch.from_numpy(Ks)[None], torch.from_numpy(Vs)[None], is_causal=True).numpy()[0]
+        assert np.allclose(O2, ref2, atol=1e-11)
+
+
+def test_split_merge_equals_full():
+    """Attention over a split prefix merged through the LSE trailer equals full attention."""
+    rng = np.random.default_rng(8)
+    H, N, D = 4, 100, 64
+    Q = rng.standard_normal((H, 2, D))
+    K, V = rng.standard_normal((2, N, D)), rng.standard_normal((2, N, D))
+    hm = np.array([0, 0, 1, 1])
+    O, L = orc.prefix_query(Q, K, V, hm)
+    for t in (1, 17, 50, 99):
+        O1, L1 = orc.prefix_query(Q, K[:, :t], V[:, :t], hm)
+        O2, L2 = orc.prefix_query(Q, K[:, t:], V[:, t:], hm)
+        Om, Lm = orc.merge_partials(O1, L1, O2, L2)
+        assert np.allclose(Om, O, atol=1e-12) and np.allclose(Lm, L, atol=1e-12)
+        Om2, Lm2 = orc.merge_partials(O2, L2, O1, L1)
+        assert np.allclose(Om2, Om, atol=1e-14) and np.allclose(Lm2, Lm, atol=1e-14)
+
+
+def test_fused_suffix_equals_merge_of_parts():
+    rng = np.random.default_rng(9)
+    H_q, H_kv, N, S, D = 8, 2, 40, 16, 64
+    Q = rng.standard_normal((H_q, 1, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    Ks, Vs = rng.standard_normal((H_kv, S, D)), rng.standard_normal((H_kv, S, D))
+    hm = synth.default_head_map(H_q, H_kv)
+    O, L = orc.prefix_query(Q, K, V, hm, Ks, Vs)
+    Op, Lp = orc.prefix_query(Q, K, V, hm)
+    Os, Ls = orc.prefix_query(Q, Ks, Vs, hm)
+    Om, Lm = orc.merge_partials(Op, Lp, Os, Ls)
+    assert np.allclose(O, Om, atol=1e-12) and np.allclose(L, Lm, atol=1e-12)
+    # M=1: suffix appended to the prefix is plain dense attention over N + S keys.
+    Od, Ld = orc.prefix_query(Q, np.concatenate([K, Ks], 1), np.concatenate([V, Vs], 1), hm)
+    assert np.allclose(O, Od, atol=1e-12) and np.allclose(L, Ld, atol=1e-12)
+
+
+def test_gqa_head_map_and_permutation():
+    rng = np.random.default_rng(10)
+    H_q, H_kv, N, D = 6, 3, 20, 16
+    Q = rng.standard_normal((H_q, 2, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    hm = np.array([2, 0, 1, 1, 0, 2])
+    O, L = orc.prefix_query(Q, K, V, hm)
+    Kx, Vx = K[hm], V[hm]       # explicit per-q-head copies
+    O2, L2 = orc.prefix_query(Q, Kx, Vx, np.arange(H_q))
+    assert np.allclose(O, O2) and np.allclose(L, L2)
+    perm = rng.permutation(N)
+    O3, L3 = orc.prefix_query(Q, K[:, perm], V[:, perm], hm)
+    assert np.allclose(O, O3, atol=1e-12) and np.allclose(L, L3, atol=1e-12)
+
+
+def test_merge_with_empty_partial_is_identity():
+    O = np.arange(8.0).reshape(2, 4)
+    L = np.array([0.3, -2.0])
+    Om, Lm = orc.merge_partials(O, L, np.zeros_like(O), np.full(2, -np.inf))
+    assert np.allclose(Om, O) and np.allclose(Lm, L)
+
+
+# ------------------------------------------------------------------ block means, top-K, sparse
+
+def test_block_means_ramp_closed_form():
+    H_kv, N, D, B = 2, 203, 3, 64
+    K = np.broadcast_to(np.arange(N, dtype=np.float64)[None, :, None], (H_kv, N, D)).copy()
+    K[1] *= -2
+    km = orc.block_means(K, B)
+    assert km.shape == (2, 4, 3)
+    for b in range(4):
+        lo, hi = b * B, min(N, (b + 1) * B) - 1
+        assert np.allclose(km[0, b], (lo + hi) / 2) and np.allclose(km[1, b], -(lo + hi))
+
+
+def test_topk_tie_example():
+    lines = _golden_lines("topk_tie_example.txt")
+    scores = np.array([[float(v) for v in lines[0].split(":")[1].split()]])
+    for ln in lines[1:]:
+        k = int(ln.split()[0].split("=")[1])
+        want = [int(v) for v in ln.split(":")[1].split()]
+        assert orc.select_top_blocks(scores, k)[0].tolist() == want
+
+
+def test_sparse_covering_all_blocks_equals_dense():
+    rng = np.random.default_rng(11)
+    H_q, H_kv, N, D, B = 4, 2, 300, 32, 64
+    Q = rng.standard_normal((H_q, 1, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    Ks, Vs = rng.standard_normal((H_kv, 8, D)), rng.standard_normal((H_kv, 8, D))
+    hm = synth.default_head_map(H_q, H_kv)
+    for Kt in (5, 9):
+        O, L, idx, _ = orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs)
+        Od, Ld = orc.prefix_query(Q, K, V, hm, Ks, Vs)
+        assert (idx == np.arange(5)).all()
+        assert np.allclose(O, Od[:, 0], atol=1e-12) and np.allclose(L, Ld[:, 0], atol=1e-12)
+
+
+def test_sparse_equals_dense_over_selected_tokens():
+    rng = np.random.default_rng(12)
+    H_q, H_kv, N, D, B = 4, 1, 256, 16, 32
+    Q = rng.standard_normal((H_q, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    hm = np.zeros(H_q, dtype=np.int32)
+    O, L, idx, scores = orc.sparse_query(Q, K, V, hm, B, 3)
+    for h in range(H_q):
+        toks = np.concatenate([np.arange(b * B, (b + 1) * B) for b in idx[h]])
+        Od, Ld = orc.prefix_query(Q[h][None, None], K[:, toks], V[:, toks], np.zeros(1, dtype=int))
+        assert np.allclose(O[h], Od[0, 0]) and np.isclose(L[h], Ld[0, 0])
+        # selected blocks really are the top-3 by score
+        assert set(idx[h]) == set(np.argsort(-scores[h], kind="stable")[:3])
+
+
+def test_needle_workload_selects_needles():
+    """Sparse workload at reduced length: planted needles are exactly the selected blocks."""
+    H_q, H_kv, N, D, B, Kt = 8, 2, 8192, 256, 64, 8
+    seed = 0
+    K, V = synth.gen_kv(seed, H_kv, N, D)
+    Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+    hm = synth.default_head_map(H_q, H_kv)
+    needles = synth.needle_blocks(seed, N // B, Kt)
+    K = synth.plant_needles(K, Q, hm, needles, B)
+    scores = orc.block_scores(Q, orc.block_means(K, B), hm)
+    idx = orc.select_top_blocks(scores, Kt)
+    assert (idx == needles[None, :]).all()
+    assert (orc.topk_margin(scores, Kt) > 0.5).all()
+
+
+# ------------------------------------------------------------------ planted mistakes are caught
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Plant plausible mistakes in the oracle (on the CPU) and check a pin fails for each."""
+    import oracle.pck_oracle as mod
+    good = mod.attend_rows
+
+    def no_tau(q, k, v, tau, allowed=None):
+        return good(q, k, v, 1.0, allowed)
+
+    def drop_max(q, k, v, tau, allowed=None):
+        O, L = good(q, k, v, tau, allowed)
+        return O, L - np.max(tau * (np.asarray(q) @ np.asarray(k).T), axis=1)
+
+    for bad in (no_tau, drop_max):
+        monkeypatch.setattr(mod, "attend_rows", bad)
+        with pytest.raises(AssertionError):
+            test_attention_matches_scipy_and_torch()
+        monkeypatch.setattr(mod, "attend_rows", good)
+
+    good_q = mod.quantize_mlx4g32
+
+    def symmetric(x):
+        c, s, b = good_q(x)
+        return c, s, np.zeros_like(b)
+
+    monkeypatch.setattr(mod, "quantize_mlx4g32", symmetric)
+    with pytest.raises(AssertionError):
+        test_quantizer_lossless_on_grid()
+    monkeypatch.setattr(mod, "quantize_mlx4g32", good_q)
+
+    good_pc = mod.pack_codes
+
+    def wrong_nibble_order(codes):
+        return good_pc(codes[:, ::-1].copy())
+
+    monkeypatch.setattr(mod, "pack_codes", wrong_nibble_order)
+    with pytest.raises(AssertionError):
+        test_layout_worked_example()
