@@ -1,0 +1,181 @@
+/*
+ * pck.h -- C ABI of libpck: attention of query rows over a resident shared-prefix KV cache
+ * on one GB300 (sm_103a).
+ *
+ * The calls follow the problem statement of the ATTEND.PREFIX.* wire forms on the page
+ * "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms" (STORE / LOOKUP / QUERY /
+ * QUERY_FUSED / QUERY_SPARSE_AUTO / QUERY_SPARSE_AUTO_FUSED), with explicit M, dtypes and
+ * pointer ownership. The mlx4g32 tier follows "Shared KV Cache Serving -- Pion as LLM
+ * Memory", section "Quantized tier -- mlx4g32".
+ *
+ * Conventions for every call:
+ *  - Tensor pointers (Q, O, LSE, K, V, K_suf, V_suf, records, idx_out) are DEVICE pointers
+ *    on the context's device, caller-owned, contiguous, and must stay valid until the stream
+ *    reaches the call. head_map is a small HOST array (int32[H_q], entries in [0, H_kv));
+ *    NULL means the grouped default h / (H_q / H_kv).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default stream.
+ *  - Calls are asynchronous on `stream`. Argument, shape and slot errors are detected on the
+ *    host and returned before anything is launched. Asynchronous CUDA errors are reported as
+ *    PCK_ECUDA by pck_sync or by a later call.
+ *  - One context serialises its work: queries on one context must be issued on one stream
+ *    (they share the context's split-K workspace). Use one context per stream otherwise.
+ *  - Scores are tau * q.k with tau = 1/sqrt(D). LSE is in natural-log units of the scaled
+ *    logits: LSE = ln(sum_t exp(tau q.k_t)). O is fp32 [H_q, M, D], LSE fp32 [H_q, M].
+ *  - On a non-OK status, pck_last_error(ctx) holds a one-line reason.
+ */
+#ifndef PCK_H
+#define PCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. PCK_MISS matches the wire's +MISS / "-ERR session not found"; PCK_COLDMISS
+ * matches STATUS_COLDMISS = 0x03 of the binary lane ("Shared KV Cache Serving", section
+ * "Cold-tier state machine"): the slot was evicted by LRU and must be stored again. */
+#define PCK_OK            0
+#define PCK_MISS          1
+#define PCK_COLDMISS      3
+#define PCK_EINVAL       (-1)
+#define PCK_EUNSUPPORTED (-2)
+#define PCK_ENOMEM       (-3)
+#define PCK_ECUDA        (-4)
+
+/* Resident formats of a slot. */
+#define PCK_FMT_FP16     0  /* fp16 K/V */
+#define PCK_FMT_MLX4G32  1  /* int4, group 32, affine, fp16 scale + fp16 bias per group */
+
+/* Element types of caller tensors. */
+#define PCK_DT_F32       0
+#define PCK_DT_F16       1
+
+/* Head dimensions with kernels: 64, 128, 256. Larger H_q per kv head than 8 is split. */
+#define PCK_MAX_BATCH    64   /* descriptors per pck_query_batch call */
+#define PCK_MAX_HEADS    64   /* H_q and H_kv limit */
+
+typedef struct pck_ctx pck_ctx;
+
+typedef struct pck_info_t {
+    int64_t slots_used;       /* resident (sid, layer) slots */
+    int64_t slots_max;        /* capacity (LRU eviction beyond it) */
+    int64_t cold_entries;     /* evicted keys remembered for PCK_COLDMISS */
+    int64_t bytes_resident;   /* device bytes held by resident K/V (+ block means) */
+    int64_t queries_served;   /* query calls that launched work */
+    int64_t stores;           /* store calls that launched work */
+    int64_t evictions;        /* LRU demotions */
+} pck_info_t;
+
+/* One M=1 query of a pck_query_batch call. */
+typedef struct pck_query_desc {
+    const char *sid;          /* session id (NUL-terminated) */
+    int layer;
+    const void *Q;            /* device [H_q, D], q_dtype of the batch */
+    float *O;                 /* device [H_q, D] fp32 */
+    float *LSE;               /* device [H_q] fp32, or NULL */
+    const void *K_suf;        /* device fp16 [H_kv, S_suf, D], or NULL when S_suf == 0 */
+    const void *V_suf;
+} pck_query_desc;
+
+/* Create a context on CUDA device `device` with room for `max_slots` resident (sid, layer)
+ * slots (<= 0 selects 256, the per-worker slot table size of the pages' session cache).
+ * Allocates the split-K workspace. Returns PCK_OK and *out, or PCK_ECUDA / PCK_ENOMEM. */
+int pck_create(pck_ctx **out, int device, int max_slots);
+
+/* Free every resident slot and the workspace. Synchronises the device first. NULL is a no-op. */
+void pck_destroy(pck_ctx *ctx);
+
+/* One-line description of the last error on ctx ("" if none). Owned by ctx. */
+const char *pck_last_error(const pck_ctx *ctx);
+
+/* ATTEND.PREFIX.STORE <sid> <layer> <H> <N> <D> <K_blob> <V_blob>.
+ * K, V: device [H_kv, N, D], src_dtype F16 or F32. fmt FP16 keeps fp16 K/V resident;
+ * fmt MLX4G32 quantises both on the device (same arithmetic as pck_quantize_mlx4g32) and keeps
+ * the codes/scales/biases resident. Replaces an existing slot with the same key. The library
+ * copies K/V into its own memory: the caller may reuse K/V once the stream passes the call.
+ * D in {64, 128, 256}, H_kv <= 64, N >= 1. Errors: EINVAL, EUNSUPPORTED, ENOMEM. */
+int pck_store(pck_ctx *ctx, const char *sid, int layer, int H_kv, int N, int D, int fmt,
+              const void *K, const void *V, int src_dtype, void *stream);
+
+/* Store pre-quantised mlx4g32 records (token-major [N, rec] with rec = H_kv*D/8*4 + 2*(H_kv*D/32)*2
+ * bytes: codes words, then scales, then biases; see pck_quantize_mlx4g32) as a MLX4G32 slot. */
+int pck_store_records(pck_ctx *ctx, const char *sid, int layer, int H_kv, int N, int D,
+                      const void *K_rec, const void *V_rec, void *stream);
+
+/* ATTEND.PREFIX.LOOKUP: PCK_OK if (sid, layer) is resident, PCK_COLDMISS if it was evicted,
+ * PCK_MISS otherwise. */
+int pck_lookup(pck_ctx *ctx, const char *sid, int layer);
+
+/* Drop (sid, layer), or every layer of sid when layer < 0. Memory is released in stream order
+ * on `stream` (queued work on that stream still sees valid K/V). Returns the number dropped. */
+int pck_drop(pck_ctx *ctx, const char *sid, int layer, void *stream);
+
+/* Precompute the block means of K (fp32, [H_kv, ceil(N/B), D]) used by the sparse selector.
+ * The sparse queries build them on first use per (slot, B); this lets a caller do it at store
+ * time (e.g. before capturing a CUDA graph). Only fp16 slots. */
+int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void *stream);
+
+/* ATTEND.PREFIX.QUERY <sid> <layer> <H> <D> <top_k> <Q_blob> [<fa_window>].
+ * Q: device [H_q, M, D] of q_dtype. M == 1: split-K decode over the slot (fp16 or mlx4g32).
+ * M > 1: tiled tensor-core kernel; needs an fp16 slot and q_dtype F16.
+ * top_k: 0 or >= N (dense). fa_window: 0. Other values are PCK_EUNSUPPORTED.
+ * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
+int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
+              const void *Q, const int32_t *head_map, int top_k, int fa_window,
+              float *O, float *LSE, void *stream);
+
+/* ATTEND.PREFIX.QUERY_FUSED: prefix attention plus attention to a dense suffix
+ * K_suf/V_suf (device fp16 [H_kv, S_suf, D]), merged by online softmax in the same launch.
+ * causal != 0: query row i (of M) sees suffix keys j <= S_suf - M + i (bottom-right aligned);
+ * causal == 0: every row sees the whole suffix. The merged LSE is written if LSE != NULL. */
+int pck_query_fused(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int S_suf,
+                    int H_kv, int q_dtype, const void *Q, const void *K_suf, const void *V_suf,
+                    const int32_t *head_map, int causal, int fa_window,
+                    float *O, float *LSE, void *stream);
+
+/* ATTEND.PREFIX.QUERY_SPARSE_AUTO: M=1. Scores the slot's B-token blocks by
+ * tau * q_h . mean(K of the block), keeps the K_top best per q head (ties -> lower index,
+ * K_top clamped to ceil(N/B)), and attends only to their tokens. idx_out (device
+ * int32 [H_q, min(K_top, nblocks)], nullable) receives the selected blocks, sorted ascending.
+ * fp16 slots only. */
+int pck_query_sparse_auto(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int B,
+                          int K_top, int H_kv, int q_dtype, const void *Q,
+                          const int32_t *head_map, int fa_window,
+                          float *O, float *LSE, int32_t *idx_out, void *stream);
+
+/* ATTEND.PREFIX.QUERY_SPARSE_AUTO_FUSED: the sparse prefix plus a dense suffix (device fp16
+ * [H_kv, S_suf, D]) merged by online softmax. */
+int pck_query_sparse_auto_fused(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int B,
+                                int K_top, int H_kv, int S_suf, int q_dtype, const void *Q,
+                                const void *K_suf, const void *V_suf, const int32_t *head_map,
+                                int fa_window, float *O, float *LSE, int32_t *idx_out,
+                                void *stream);
+
+/* n independent M=1 queries of one shape (H_q, H_kv, D, S_suf, q_dtype, head_map) in ONE
+ * launch: the whole batch is split evenly over the GPU. 1 <= n <= PCK_MAX_BATCH. All slots
+ * must have the same format. */
+int pck_query_batch(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, int H_kv, int D,
+                    int S_suf, int q_dtype, const int32_t *head_map, void *stream);
+
+/* mlx4g32 quantiser (store side). X: device [rows, kv_dim] of src_dtype (F16 or F32);
+ * out_records: device [rows, rec] bytes, rec = kv_dim/2 + kv_dim/8. Per group of 32:
+ * mn/mx as fp32, s32 = (mx - mn)/15 in fp32, scale = fp16(s32) (rounded BEFORE the codes are
+ * chosen), bias = fp16(mn), code = clamp(rint((x - bias)/scale), 0, 15) in fp32, all codes 0 when
+ * scale == 0; code of element j at bits 4*(j%8) of word j/8. kv_dim % 32 == 0. Inputs must be
+ * finite and within the fp16 range. Needs no context. */
+int pck_quantize_mlx4g32(const void *X, int src_dtype, int64_t rows, int kv_dim,
+                         void *out_records, void *stream);
+
+/* Counters of ctx. */
+int pck_info(pck_ctx *ctx, pck_info_t *out);
+
+/* Synchronise `stream` and report any asynchronous CUDA error as PCK_ECUDA. */
+int pck_sync(pck_ctx *ctx, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCK_H */

@@ -1,0 +1,256 @@
+"""Thin ctypes binding of libpck (the C ABI in include/pck.h).
+
+Argument marshalling only: torch tensors provide device memory and the current stream; every
+step of the computation runs in the CUDA library. There is no fallback: if ``libpck.so`` is
+missing this module raises at import of the library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpck.so")
+
+OK, MISS, COLDMISS = 0, 1, 3
+EINVAL, EUNSUPPORTED, ENOMEM, ECUDA = -1, -2, -3, -4
+FMT_FP16, FMT_MLX4G32 = 0, 1
+DT_F32, DT_F16 = 0, 1
+MAX_BATCH = 64
+
+# Every symbol include/pck.h declares.
+EXPORTS = (
+    "pck_create", "pck_destroy", "pck_last_error", "pck_store", "pck_store_records", "pck_lookup",
+    "pck_drop", "pck_build_block_means", "pck_query", "pck_query_fused", "pck_query_sparse_auto",
+    "pck_query_sparse_auto_fused", "pck_query_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
+)
+
+
+class PckError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"pck status {code}: {msg}")
+        self.code = code
+
+
+class InfoT(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("slots_used", "slots_max", "cold_entries", "bytes_resident",
+                                              "queries_served", "stores", "evictions")]
+
+
+class QueryDesc(ctypes.Structure):
+    _fields_ = [("sid", ctypes.c_char_p), ("layer", ctypes.c_int), ("Q", ctypes.c_void_p), ("O", ctypes.c_void_p),
+                ("LSE", ctypes.c_void_p), ("K_suf", ctypes.c_void_p), ("V_suf", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpck.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i, i64, cp = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_char_p
+    sig = {
+        "pck_create": (i, [ctypes.POINTER(vp), i, i]),
+        "pck_destroy": (None, [vp]),
+        "pck_last_error": (cp, [vp]),
+        "pck_store": (i, [vp, cp, i, i, i, i, i, vp, vp, i, vp]),
+        "pck_store_records": (i, [vp, cp, i, i, i, i, vp, vp, vp]),
+        "pck_lookup": (i, [vp, cp, i]),
+        "pck_drop": (i, [vp, cp, i, vp]),
+        "pck_build_block_means": (i, [vp, cp, i, i, vp]),
+        "pck_query": (i, [vp, cp, i, i, i, i, i, vp, vp, i, i, vp, vp, vp]),
+        "pck_query_fused": (i, [vp, cp, i, i, i, i, i, i, i, vp, vp, vp, vp, i, i, vp, vp, vp]),
+        "pck_query_sparse_auto": (i, [vp, cp, i, i, i, i, i, i, i, vp, vp, i, vp, vp, vp, vp]),
+        "pck_query_sparse_auto_fused": (i, [vp, cp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp, vp]),
+        "pck_query_batch": (i, [vp, i, ctypes.POINTER(QueryDesc), i, i, i, i, i, vp, vp]),
+        "pck_quantize_mlx4g32": (i, [vp, i, i64, i, vp, vp]),
+        "pck_info": (i, [vp, ctypes.POINTER(InfoT)]),
+        "pck_sync": (i, [vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return DT_F16
+    if t.dtype == torch.float32:
+        return DT_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _hm(head_map):
+    if head_map is None:
+        return None
+    arr = (ctypes.c_int32 * len(head_map))(*[int(x) for x in head_map])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensors must be on the CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+
+
+def quantize_mlx4g32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """mlx4g32 records (uint8 [rows, kv_dim/2 + kv_dim/8]) of x ([rows, kv_dim], fp16/fp32)."""
+    lib = load_library()
+    _check_dev(x)
+    rows, kv_dim = x.shape
+    if out is None:
+        out = torch.empty((rows, kv_dim // 2 + kv_dim // 8), dtype=torch.uint8, device=x.device)
+    rc = lib.pck_quantize_mlx4g32(_ptr(x), _dt(x), rows, kv_dim, _ptr(out), _stream(stream))
+    if rc != OK:
+        raise PckError(rc, "pck_quantize_mlx4g32 rejected its arguments")
+    return out
+
+
+class Context:
+    """One libpck context (slot table + workspaces) on one device."""
+
+    def __init__(self, device: int = 0, max_slots: int = 256):
+        self.lib = load_library()
+        h = ctypes.c_void_p()
+        torch.cuda.init()
+        rc = self.lib.pck_create(ctypes.byref(h), device, max_slots)
+        if rc != OK:
+            raise PckError(rc, "pck_create failed")
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.pck_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def last_error(self) -> str:
+        return (self.lib.pck_last_error(self.h) or b"").decode()
+
+    def _rc(self, rc: int, ok=(OK,)):
+        if rc not in ok:
+            raise PckError(rc, self.last_error())
+        return rc
+
+    # ---- store / lookup / drop
+    def store(self, sid: str, layer: int, K: torch.Tensor, V: torch.Tensor, fmt: int = FMT_FP16, stream=None):
+        _check_dev(K, V)
+        H_kv, N, D = K.shape
+        return self._rc(self.lib.pck_store(self.h, sid.encode(), layer, H_kv, N, D, fmt, _ptr(K), _ptr(V), _dt(K),
+                                           _stream(stream)))
+
+    def store_records(self, sid: str, layer: int, H_kv: int, N: int, D: int, K_rec, V_rec, stream=None):
+        _check_dev(K_rec, V_rec)
+        return self._rc(self.lib.pck_store_records(self.h, sid.encode(), layer, H_kv, N, D, _ptr(K_rec), _ptr(V_rec),
+                                                   _stream(stream)))
+
+    def lookup(self, sid: str, layer: int) -> int:
+        return self.lib.pck_lookup(self.h, sid.encode(), layer)
+
+    def drop(self, sid: str, layer: int = -1, stream=None) -> int:
+        rc = self.lib.pck_drop(self.h, sid.encode(), layer, _stream(stream))
+        if rc < 0:
+            raise PckError(rc, self.last_error())
+        return rc
+
+    def build_block_means(self, sid: str, layer: int, B: int, stream=None):
+        return self._rc(self.lib.pck_build_block_means(self.h, sid.encode(), layer, B, _stream(stream)))
+
+    # ---- queries (O and LSE are allocated when not given)
+    def query(self, sid, layer, Q, head_map=None, top_k=0, fa_window=0, O=None, LSE=None, want_lse=True, stream=None):
+        _check_dev(Q)
+        H_q, M, D = Q.shape
+        O = torch.empty((H_q, M, D), dtype=torch.float32, device=Q.device) if O is None else O
+        if LSE is None and want_lse:
+            LSE = torch.empty((H_q, M), dtype=torch.float32, device=Q.device)
+        hm = _hm(head_map)
+        self._rc(self.lib.pck_query(self.h, sid.encode(), layer, H_q, D, M, _dt(Q), _ptr(Q), hm[0] if hm else None,
+                                    top_k, fa_window, _ptr(O), _ptr(LSE), _stream(stream)))
+        return O, LSE
+
+    def query_fused(self, sid, layer, Q, K_suf, V_suf, head_map=None, causal=True, fa_window=0, O=None, LSE=None,
+                    want_lse=True, stream=None):
+        _check_dev(Q, K_suf, V_suf)
+        H_q, M, D = Q.shape
+        H_kv, S_suf, _ = K_suf.shape
+        O = torch.empty((H_q, M, D), dtype=torch.float32, device=Q.device) if O is None else O
+        if LSE is None and want_lse:
+            LSE = torch.empty((H_q, M), dtype=torch.float32, device=Q.device)
+        hm = _hm(head_map)
+        self._rc(self.lib.pck_query_fused(self.h, sid.encode(), layer, H_q, D, M, S_suf, H_kv, _dt(Q), _ptr(Q),
+                                          _ptr(K_suf), _ptr(V_suf), hm[0] if hm else None, int(bool(causal)),
+                                          fa_window, _ptr(O), _ptr(LSE), _stream(stream)))
+        return O, LSE
+
+    def query_sparse_auto(self, sid, layer, Q, B, K_top, H_kv, head_map=None, K_suf=None, V_suf=None, fa_window=0,
+                          O=None, LSE=None, idx=None, stream=None):
+        _check_dev(Q, K_suf, V_suf)
+        H_q, D = Q.shape[0], Q.shape[-1]
+        O = torch.empty((H_q, D), dtype=torch.float32, device=Q.device) if O is None else O
+        LSE = torch.empty((H_q,), dtype=torch.float32, device=Q.device) if LSE is None else LSE
+        if idx is None:   # the library writes [H_q, min(K_top, n_blocks)] contiguously
+            idx = torch.empty((H_q, K_top), dtype=torch.int32, device=Q.device)
+        hm = _hm(head_map)
+        if K_suf is None:
+            rc = self.lib.pck_query_sparse_auto(self.h, sid.encode(), layer, H_q, D, B, K_top, H_kv, _dt(Q), _ptr(Q),
+                                                hm[0] if hm else None, fa_window, _ptr(O), _ptr(LSE), _ptr(idx),
+                                                _stream(stream))
+        else:
+            rc = self.lib.pck_query_sparse_auto_fused(self.h, sid.encode(), layer, H_q, D, B, K_top, H_kv,
+                                                      K_suf.shape[1], _dt(Q), _ptr(Q), _ptr(K_suf), _ptr(V_suf),
+                                                      hm[0] if hm else None, fa_window, _ptr(O), _ptr(LSE), _ptr(idx),
+                                                      _stream(stream))
+        self._rc(rc)
+        return O, LSE, idx
+
+    def query_batch(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None, stream=None):
+        """descs: list of dicts with sid, layer, Q, O, LSE (optional), K_suf/V_suf (optional)."""
+        n = len(descs)
+        arr = (QueryDesc * n)()
+        keep = []
+        for i, d in enumerate(descs):
+            sid = d["sid"].encode()
+            keep.append(sid)
+            arr[i] = QueryDesc(sid, d["layer"], d["Q"].data_ptr(), d["O"].data_ptr(),
+                               d["LSE"].data_ptr() if d.get("LSE") is not None else None,
+                               d["K_suf"].data_ptr() if d.get("K_suf") is not None else None,
+                               d["V_suf"].data_ptr() if d.get("V_suf") is not None else None)
+        hm = _hm(head_map)
+        return self._rc(self.lib.pck_query_batch(self.h, n, arr, H_q, H_kv, D, S_suf, q_dtype, hm[0] if hm else None,
+                                                 _stream(stream)))
+
+    def info(self) -> dict:
+        out = InfoT()
+        self._rc(self.lib.pck_info(self.h, ctypes.byref(out)))
+        return {n: getattr(out, n) for n, _ in InfoT._fields_}
+
+    def sync(self, stream=None):
+        return self._rc(self.lib.pck_sync(self.h, _stream(stream)))

@@ -1,0 +1,705 @@
+// pck_api.cu -- host runtime and C ABI of libpck (declared in include/pck.h).
+//
+// Slot table: resident (sid, layer) entries, the problem statement of ATTEND.PREFIX.STORE /
+// LOOKUP ("ATTEND.* and ATTEND.PREFIX.*", section "Wire forms"). When the table is full the
+// least recently used slot is released and its key kept in a bounded cold registry, so that a
+// later query answers PCK_COLDMISS instead of PCK_MISS ("Shared KV Cache Serving -- Pion as LLM
+// Memory", section "Cold-tier state machine": WARM / COLD / MISSING).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <list>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/pck.h"
+#include "pck_common.cuh"
+#include "pck_kernels.h"
+
+using namespace pck;
+
+namespace {
+
+constexpr int COLD_SLOTS = 1024;
+constexpr size_t WS_PARTIAL_BYTES = size_t(64) << 20;  // split-K partials
+constexpr int WS_COUNTERS = 1 << 16;
+constexpr int WS_SEL_BYTES = 1 << 20;                   // sparse selection lists
+constexpr size_t WS_SCORES_BYTES = size_t(16) << 20;
+
+struct Slot {
+    int fmt = 0, H_kv = 0, N = 0, D = 0, ntiles = 0;
+    uint8_t* tiles = nullptr;
+    size_t bytes = 0;
+    std::unordered_map<int, float*> kmean;  // block size -> [H_kv, nb, D] fp32
+    std::list<std::string>::iterator lru;
+};
+
+}  // namespace
+
+struct pck_ctx {
+    int device = 0;
+    int sms = 0;
+    int max_slots = 256;
+    std::string err;
+    std::unordered_map<std::string, Slot> slots;
+    std::list<std::string> lru;                 // front = most recent
+    std::deque<std::string> cold_fifo;
+    std::unordered_set<std::string> cold;
+    float* partials = nullptr;
+    int* counters = nullptr;
+    int* dev_err = nullptr;
+    uint8_t* sel = nullptr;
+    float* scores = nullptr;
+    int64_t queries = 0, stores = 0, evictions = 0;
+    int64_t bytes_resident = 0;
+    DecodeLaunchInfo dinfo[2][3];
+    bool dinfo_ok[2][3] = {{false, false, false}, {false, false, false}};
+};
+
+namespace {
+
+int fail(pck_ctx* c, int code, const char* fmt, ...) {
+    if (c) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        c->err = buf;
+    }
+    return code;
+}
+
+int cuda_fail(pck_ctx* c, cudaError_t e, const char* what) {
+    return fail(c, PCK_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::string key_of(const char* sid, int layer) {
+    std::string k(sid);
+    k.push_back('\x1f');
+    k += std::to_string(layer);
+    return k;
+}
+
+bool d_ok(int D) { return D == 64 || D == 128 || D == 256; }
+int d_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
+
+const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D) {
+    const int i = d_index(D);
+    if (!c->dinfo_ok[fmt][i]) {
+        c->dinfo[fmt][i] = decode_launch_info(fmt, D);
+        c->dinfo_ok[fmt][i] = true;
+    }
+    return c->dinfo[fmt][i];
+}
+
+void free_slot(pck_ctx* c, Slot& s, cudaStream_t st) {
+    if (s.tiles) cudaFreeAsync(s.tiles, st);
+    for (auto& kv : s.kmean) cudaFreeAsync(kv.second, st);
+    c->bytes_resident -= static_cast<int64_t>(s.bytes);
+    for (auto& kv : s.kmean) (void)kv;
+    s.tiles = nullptr;
+    s.kmean.clear();
+}
+
+void remember_cold(pck_ctx* c, const std::string& k) {
+    if (c->cold.count(k)) return;
+    c->cold.insert(k);
+    c->cold_fifo.push_back(k);
+    if (static_cast<int>(c->cold_fifo.size()) > COLD_SLOTS) {
+        c->cold.erase(c->cold_fifo.front());
+        c->cold_fifo.pop_front();
+    }
+}
+
+void forget_cold(pck_ctx* c, const std::string& k) {
+    if (!c->cold.erase(k)) return;
+    for (auto it = c->cold_fifo.begin(); it != c->cold_fifo.end(); ++it)
+        if (*it == k) { c->cold_fifo.erase(it); break; }
+}
+
+// Look up a resident slot and mark it most recently used; status PCK_OK / PCK_MISS / PCK_COLDMISS.
+int find_slot(pck_ctx* c, const char* sid, int layer, Slot** out) {
+    if (!sid) return fail(c, PCK_EINVAL, "sid is NULL");
+    const std::string k = key_of(sid, layer);
+    auto it = c->slots.find(k);
+    if (it == c->slots.end()) {
+        if (c->cold.count(k)) return fail(c, PCK_COLDMISS, "COLDMISS %s layer %d (evicted)", sid, layer);
+        return fail(c, PCK_MISS, "session not found: %s layer %d", sid, layer);
+    }
+    c->lru.splice(c->lru.begin(), c->lru, it->second.lru);
+    *out = &it->second;
+    return PCK_OK;
+}
+
+// Insert (replacing any previous slot with the key), evicting the LRU slot when full.
+Slot* put_slot(pck_ctx* c, const std::string& k, cudaStream_t st) {
+    auto it = c->slots.find(k);
+    if (it != c->slots.end()) {
+        free_slot(c, it->second, st);
+        c->lru.erase(it->second.lru);
+        c->slots.erase(it);
+    }
+    while (static_cast<int>(c->slots.size()) >= c->max_slots && !c->lru.empty()) {
+        const std::string victim = c->lru.back();
+        auto v = c->slots.find(victim);
+        free_slot(c, v->second, st);
+        c->slots.erase(v);
+        c->lru.pop_back();
+        remember_cold(c, victim);
+        ++c->evictions;
+    }
+    forget_cold(c, k);
+    c->lru.push_front(k);
+    Slot& s = c->slots[k];
+    s.lru = c->lru.begin();
+    return &s;
+}
+
+int check_async(pck_ctx* c) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(c, e, "CUDA error");
+    return PCK_OK;
+}
+
+// q heads grouped by kv head, at most GMAX per work group.
+int build_groups(pck_ctx* c, int H_q, int H_kv, const int32_t* head_map, WorkGroup* grp, int* n_groups,
+                 int8_t* hm_out, int* max_nq) {
+    if (H_q < 1 || H_kv < 1 || H_q > PCK_MAX_HEADS || H_kv > PCK_MAX_HEADS)
+        return fail(c, PCK_EINVAL, "H_q=%d H_kv=%d out of range [1, %d]", H_q, H_kv, PCK_MAX_HEADS);
+    int hm[PCK_MAX_HEADS];
+    for (int h = 0; h < H_q; ++h) {
+        if (head_map) {
+            hm[h] = head_map[h];
+        } else {
+            if (H_q % H_kv) return fail(c, PCK_EINVAL, "H_q=%d not a multiple of H_kv=%d and no head_map", H_q, H_kv);
+            hm[h] = h / (H_q / H_kv);
+        }
+        if (hm[h] < 0 || hm[h] >= H_kv) return fail(c, PCK_EINVAL, "head_map[%d]=%d outside [0, %d)", h, hm[h], H_kv);
+        if (hm_out) hm_out[h] = static_cast<int8_t>(hm[h]);
+    }
+    int n = 0, mx = 0;
+    for (int g = 0; g < H_kv; ++g) {
+        WorkGroup cur{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
+        for (int h = 0; h < H_q; ++h) {
+            if (hm[h] != g) continue;
+            cur.qh[cur.nq++] = static_cast<int8_t>(h);
+            if (cur.nq == GMAX) {
+                if (n == MAX_GROUPS) return fail(c, PCK_EUNSUPPORTED, "too many work groups");
+                grp[n++] = cur;
+                mx = GMAX;
+                cur = WorkGroup{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
+            }
+        }
+        if (cur.nq) {
+            if (n == MAX_GROUPS) return fail(c, PCK_EUNSUPPORTED, "too many work groups");
+            mx = std::max(mx, cur.nq);
+            grp[n++] = cur;
+        }
+    }
+    *n_groups = n;
+    if (max_nq) *max_nq = mx;
+    return PCK_OK;
+}
+
+struct DescIn {
+    Slot* slot;
+    const void* Q;
+    float* O;
+    float* LSE;
+    const void* Ksuf;
+    const void* Vsuf;
+};
+
+// Plan and launch one decode over n descriptors (dense), or one sparse descriptor.
+int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f16, const WorkGroup* grp,
+               int n_groups, const DescIn* dsc, int n, int sparse, int tiles_per_block, int sel_max,
+               const int* sel_blocks, const uint8_t* sel_mask, cudaStream_t st) {
+    static thread_local DecodeParams p;   // ~6 KB, built on the host and copied into the launch
+    std::memset(&p, 0, sizeof p);
+    p.n_desc = n;
+    p.n_groups = n_groups;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.S_suf = S_suf;
+    p.q_f16 = q_f16;
+    p.sparse = sparse;
+    p.tiles_per_block = tiles_per_block;
+    p.sel_max = sel_max;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    for (int g = 0; g < n_groups; ++g) p.grp[g] = grp[g];
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        DecodeDesc& d = p.desc[i];
+        d.kv = dsc[i].slot->tiles;
+        d.Q = dsc[i].Q;
+        d.O = dsc[i].O;
+        d.LSE = dsc[i].LSE;
+        d.Ksuf = static_cast<const __half*>(dsc[i].Ksuf);
+        d.Vsuf = static_cast<const __half*>(dsc[i].Vsuf);
+        d.N = dsc[i].slot->N;
+        d.ntiles = dsc[i].slot->ntiles;
+        d.vtiles = sparse ? sel_max * tiles_per_block : d.ntiles;
+        d.sel_blocks = sel_blocks;
+        d.sel_mask = sel_mask;
+        d.tile_off = static_cast<int>(total);
+        total += static_cast<int64_t>(n_groups) * d.vtiles;
+    }
+    if (total >= (int64_t(1) << 30)) return fail(c, PCK_EUNSUPPORTED, "too many tiles in one launch");
+    const DecodeLaunchInfo& li = dinfo(c, fmt, D);
+    const int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS;
+    int64_t tpw = (total + max_warps - 1) / max_warps;
+    if (tpw < 2) tpw = 2;
+    const int64_t n_workers = (total + tpw - 1) / tpw;
+    const int n_items = n * n_groups;
+    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
+    const int64_t slots = n_workers + n_items + static_cast<int64_t>(n_items) * n_suf;
+    const size_t need = static_cast<size_t>(slots) * GMAX * (D + 2) * sizeof(float);
+    if (need > WS_PARTIAL_BYTES) return fail(c, PCK_EUNSUPPORTED, "split-K workspace too small (%zu B needed)", need);
+    if (n_items > WS_COUNTERS) return fail(c, PCK_EUNSUPPORTED, "too many work items");
+    p.total_tiles = static_cast<int>(total);
+    p.tpw = static_cast<int>(tpw);
+    p.n_workers = static_cast<int>(n_workers);
+    p.n_suf = n_suf;
+    p.partials = c->partials;
+    p.counters = c->counters;
+    p.err = c->dev_err;
+    const int64_t warps = n_workers + static_cast<int64_t>(n_items) * n_suf;
+    const int n_ctas = static_cast<int>((warps + DECODE_WARPS - 1) / DECODE_WARPS);
+    cudaError_t e = launch_decode(fmt, D, p, n_ctas, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
+    ++c->queries;
+    return PCK_OK;
+}
+
+bool dtype_ok(int dt) { return dt == PCK_DT_F32 || dt == PCK_DT_F16; }
+
+}  // namespace
+
+extern "C" {
+
+int pck_create(pck_ctx** out, int device, int max_slots) {
+    if (!out) return PCK_EINVAL;
+    *out = nullptr;
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return PCK_ECUDA;
+    pck_ctx* c = new pck_ctx();
+    c->device = device;
+    c->max_slots = max_slots > 0 ? max_slots : 256;
+    cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, device);
+    if (c->sms <= 0) c->sms = 1;
+    if (cudaMalloc(&c->partials, WS_PARTIAL_BYTES) != cudaSuccess ||
+        cudaMalloc(&c->counters, WS_COUNTERS * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&c->dev_err, sizeof(int)) != cudaSuccess || cudaMalloc(&c->sel, WS_SEL_BYTES) != cudaSuccess ||
+        cudaMalloc(&c->scores, WS_SCORES_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        pck_destroy(c);
+        return PCK_ENOMEM;
+    }
+    cudaMemset(c->counters, 0, WS_COUNTERS * sizeof(int));
+    cudaMemset(c->dev_err, 0, sizeof(int));
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        pck_destroy(c);
+        return PCK_ECUDA;
+    }
+    *out = c;
+    return PCK_OK;
+}
+
+void pck_destroy(pck_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    cudaDeviceSynchronize();
+    for (auto& kv : c->slots) free_slot(c, kv.second, nullptr);
+    cudaDeviceSynchronize();
+    cudaFree(c->partials);
+    cudaFree(c->counters);
+    cudaFree(c->dev_err);
+    cudaFree(c->sel);
+    cudaFree(c->scores);
+    delete c;
+}
+
+const char* pck_last_error(const pck_ctx* c) { return c ? c->err.c_str() : "no context"; }
+
+int pck_store(pck_ctx* c, const char* sid, int layer, int H_kv, int N, int D, int fmt, const void* K, const void* V,
+              int src_dtype, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!sid || !K || !V) return fail(c, PCK_EINVAL, "NULL sid/K/V");
+    if (H_kv < 1 || H_kv > PCK_MAX_HEADS || N < 1) return fail(c, PCK_EINVAL, "bad H_kv=%d or N=%d", H_kv, N);
+    if (!d_ok(D)) return fail(c, PCK_EUNSUPPORTED, "D=%d (kernels exist for 64, 128, 256)", D);
+    if (fmt != PCK_FMT_FP16 && fmt != PCK_FMT_MLX4G32) return fail(c, PCK_EINVAL, "fmt=%d", fmt);
+    if (!dtype_ok(src_dtype)) return fail(c, PCK_EINVAL, "src_dtype=%d", src_dtype);
+    if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) & 15)
+        return fail(c, PCK_EINVAL, "K/V must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int ntiles = (N + TILE_TOK - 1) / TILE_TOK;
+    const size_t bytes = static_cast<size_t>(H_kv) * ntiles * tile_bytes(fmt, D);
+    uint8_t* tiles = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&tiles), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate %zu bytes for the slot", bytes);
+    }
+    cudaError_t e;
+    const int f16 = src_dtype == PCK_DT_F16;
+    if (fmt == PCK_FMT_FP16) {
+        e = launch_relayout_fp16(K, V, f16, H_kv, N, D, ntiles, tiles, st, c->sms);
+    } else {
+        const int64_t rows = static_cast<int64_t>(H_kv) * N;   // head rows [H_kv * N, D]
+        const size_t rec = static_cast<size_t>(D / 2 + D / 8);
+        uint8_t* recs = nullptr;
+        if (cudaMallocAsync(reinterpret_cast<void**>(&recs), 2 * rec * rows, st) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeAsync(tiles, st);
+            return fail(c, PCK_ENOMEM, "cannot allocate the quantiser staging buffer");
+        }
+        e = launch_quantize(K, f16, rows, D, recs, st, c->sms);
+        if (e == cudaSuccess) e = launch_quantize(V, f16, rows, D, recs + rec * rows, st, c->sms);
+        if (e == cudaSuccess) e = launch_relayout_mlx4(recs, recs + rec * rows, 1, H_kv, N, D, ntiles, tiles, st, c->sms);
+        cudaFreeAsync(recs, st);
+    }
+    if (e != cudaSuccess) {
+        cudaFreeAsync(tiles, st);
+        return cuda_fail(c, e, "store launch");
+    }
+    Slot* s = put_slot(c, key_of(sid, layer), st);
+    s->fmt = fmt;
+    s->H_kv = H_kv;
+    s->N = N;
+    s->D = D;
+    s->ntiles = ntiles;
+    s->tiles = tiles;
+    s->bytes = bytes;
+    c->bytes_resident += static_cast<int64_t>(bytes);
+    ++c->stores;
+    return PCK_OK;
+}
+
+int pck_store_records(pck_ctx* c, const char* sid, int layer, int H_kv, int N, int D, const void* K_rec,
+                      const void* V_rec, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!sid || !K_rec || !V_rec) return fail(c, PCK_EINVAL, "NULL sid/records");
+    if (H_kv < 1 || H_kv > PCK_MAX_HEADS || N < 1) return fail(c, PCK_EINVAL, "bad H_kv=%d or N=%d", H_kv, N);
+    if (!d_ok(D)) return fail(c, PCK_EUNSUPPORTED, "D=%d (kernels exist for 64, 128, 256)", D);
+    if ((reinterpret_cast<uintptr_t>(K_rec) | reinterpret_cast<uintptr_t>(V_rec)) & 3)
+        return fail(c, PCK_EINVAL, "records must be 4-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int ntiles = (N + TILE_TOK - 1) / TILE_TOK;
+    const size_t bytes = static_cast<size_t>(H_kv) * ntiles * tile_bytes(PCK_FMT_MLX4G32, D);
+    uint8_t* tiles = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&tiles), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate %zu bytes for the slot", bytes);
+    }
+    cudaError_t e = launch_relayout_mlx4(K_rec, V_rec, 0, H_kv, N, D, ntiles, tiles, st, c->sms);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(tiles, st);
+        return cuda_fail(c, e, "store_records launch");
+    }
+    Slot* s = put_slot(c, key_of(sid, layer), st);
+    s->fmt = PCK_FMT_MLX4G32;
+    s->H_kv = H_kv;
+    s->N = N;
+    s->D = D;
+    s->ntiles = ntiles;
+    s->tiles = tiles;
+    s->bytes = bytes;
+    c->bytes_resident += static_cast<int64_t>(bytes);
+    ++c->stores;
+    return PCK_OK;
+}
+
+int pck_lookup(pck_ctx* c, const char* sid, int layer) {
+    if (!c) return PCK_EINVAL;
+    if (!sid) return fail(c, PCK_EINVAL, "sid is NULL");
+    const std::string k = key_of(sid, layer);
+    if (c->slots.count(k)) return PCK_OK;
+    return c->cold.count(k) ? PCK_COLDMISS : PCK_MISS;
+}
+
+int pck_drop(pck_ctx* c, const char* sid, int layer, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!sid) return fail(c, PCK_EINVAL, "sid is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dropped = 0;
+    std::vector<std::string> keys;
+    if (layer >= 0) {
+        keys.push_back(key_of(sid, layer));
+    } else {
+        const std::string prefix = std::string(sid) + '\x1f';
+        for (auto& kv : c->slots)
+            if (kv.first.compare(0, prefix.size(), prefix) == 0) keys.push_back(kv.first);
+    }
+    for (auto& k : keys) {
+        auto it = c->slots.find(k);
+        if (it == c->slots.end()) continue;
+        free_slot(c, it->second, st);
+        c->lru.erase(it->second.lru);
+        c->slots.erase(it);
+        ++dropped;
+    }
+    return dropped;
+}
+
+int pck_build_block_means(pck_ctx* c, const char* sid, int layer, int B, void* stream) {
+    if (!c) return PCK_EINVAL;
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "block means are built for fp16 slots only");
+    if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
+    if (s->kmean.count(B)) return PCK_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nb = (s->N + B - 1) / B;
+    float* km = nullptr;
+    const size_t bytes = static_cast<size_t>(s->H_kv) * nb * s->D * sizeof(float);
+    if (cudaMallocAsync(reinterpret_cast<void**>(&km), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate block means");
+    }
+    cudaError_t e = launch_block_means(s->tiles, s->H_kv, s->N, s->D, s->ntiles, B, km, st, c->sms);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(km, st);
+        return cuda_fail(c, e, "block means launch");
+    }
+    s->kmean[B] = km;
+    s->bytes += bytes;
+    c->bytes_resident += static_cast<int64_t>(bytes);
+    return PCK_OK;
+}
+
+static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, int M, int S_suf, int H_kv_arg,
+                        int q_dtype, const void* Q, const void* K_suf, const void* V_suf, const int32_t* head_map,
+                        int causal, int fa_window, float* O, float* LSE, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
+    if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
+    if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
+    if (M < 1) return fail(c, PCK_EINVAL, "M=%d", M);
+    if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
+    if (S_suf > 0 && (!K_suf || !V_suf)) return fail(c, PCK_EINVAL, "S_suf=%d with NULL K_suf/V_suf", S_suf);
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (D != s->D) return fail(c, PCK_EINVAL, "D=%d but the slot holds D=%d", D, s->D);
+    if (H_kv_arg > 0 && H_kv_arg != s->H_kv)
+        return fail(c, PCK_EINVAL, "H_kv=%d but the slot holds H_kv=%d", H_kv_arg, s->H_kv);
+    WorkGroup grp[MAX_GROUPS];
+    int n_groups = 0;
+    rc = build_groups(c, H_q, s->H_kv, head_map, grp, &n_groups, nullptr, nullptr);
+    if (rc != PCK_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M == 1) {
+        DescIn d{s, Q, O, LSE, K_suf, V_suf};
+        rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0,
+                        nullptr, nullptr, st);
+        if (rc != PCK_OK) return rc;
+        return check_async(c);
+    }
+    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs an fp16 slot");
+    if (q_dtype != PCK_DT_F16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs fp16 Q");
+    if (!prefill_supported(D)) return fail(c, PCK_EUNSUPPORTED, "M>1 kernel not available for D=%d", D);
+    PrefillParams pp{};
+    pp.Q = static_cast<const __half*>(Q);
+    pp.kv = s->tiles;
+    pp.Ksuf = static_cast<const __half*>(K_suf);
+    pp.Vsuf = static_cast<const __half*>(V_suf);
+    pp.O = O;
+    pp.LSE = LSE;
+    pp.H_q = H_q;
+    pp.H_kv = s->H_kv;
+    pp.M = M;
+    pp.N = s->N;
+    pp.ntiles = s->ntiles;
+    pp.S_suf = S_suf;
+    pp.causal = causal;
+    pp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    pp.partials = c->partials;
+    pp.counters = c->counters;
+    pp.err = c->dev_err;
+    for (int h = 0; h < H_q; ++h)
+        pp.head_map[h] = head_map ? static_cast<int8_t>(head_map[h]) : static_cast<int8_t>(h / (H_q / s->H_kv));
+    cudaError_t e = launch_prefill(pp, st, c->sms, D);
+    if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
+    ++c->queries;
+    return check_async(c);
+}
+
+int pck_query(pck_ctx* c, const char* sid, int layer, int H_q, int D, int M, int q_dtype, const void* Q,
+              const int32_t* head_map, int top_k, int fa_window, float* O, float* LSE, void* stream) {
+    if (!c) return PCK_EINVAL;
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (top_k != 0 && top_k < s->N)
+        return fail(c, PCK_EUNSUPPORTED, "top_k=%d < N=%d (only 0 or >= N, i.e. dense, is defined)", top_k, s->N);
+    return query_common(c, sid, layer, H_q, D, M, 0, 0, q_dtype, Q, nullptr, nullptr, head_map, 1, fa_window, O, LSE,
+                        stream);
+}
+
+int pck_query_fused(pck_ctx* c, const char* sid, int layer, int H_q, int D, int M, int S_suf, int H_kv, int q_dtype,
+                    const void* Q, const void* K_suf, const void* V_suf, const int32_t* head_map, int causal,
+                    int fa_window, float* O, float* LSE, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (H_kv < 1) return fail(c, PCK_EINVAL, "H_kv=%d", H_kv);
+    return query_common(c, sid, layer, H_q, D, M, S_suf, H_kv, q_dtype, Q, K_suf, V_suf, head_map, causal, fa_window,
+                        O, LSE, stream);
+}
+
+static int sparse_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
+                         int S_suf, int q_dtype, const void* Q, const void* K_suf, const void* V_suf,
+                         const int32_t* head_map, int fa_window, float* O, float* LSE, int32_t* idx_out,
+                         void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
+    if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
+    if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
+    if (K_top < 1) return fail(c, PCK_EINVAL, "K_top=%d", K_top);
+    if (S_suf < 0 || (S_suf > 0 && (!K_suf || !V_suf))) return fail(c, PCK_EINVAL, "bad suffix arguments");
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (D != s->D) return fail(c, PCK_EINVAL, "D=%d but the slot holds D=%d", D, s->D);
+    if (H_kv != s->H_kv) return fail(c, PCK_EINVAL, "H_kv=%d but the slot holds H_kv=%d", H_kv, s->H_kv);
+    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "sparse queries need an fp16 slot");
+    if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
+    const int nb = (s->N + B - 1) / B;
+    const int K_eff = std::min(K_top, nb);
+    if (K_eff > 64) return fail(c, PCK_EUNSUPPORTED, "K_top=%d (at most 64)", K_top);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = pck_build_block_means(c, sid, layer, B, stream);
+    if (rc != PCK_OK) return rc;
+    static thread_local SelectParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    int n_groups = 0, max_nq = 0;
+    rc = build_groups(c, H_q, s->H_kv, head_map, sp.grp, &n_groups, sp.head_map, &max_nq);
+    if (rc != PCK_OK) return rc;
+    const int sel_max = max_nq * K_eff;
+    if (static_cast<size_t>(n_groups) * sel_max * (sizeof(int) + 1) > WS_SEL_BYTES)
+        return fail(c, PCK_EUNSUPPORTED, "selection lists too large");
+    if (static_cast<size_t>(H_q) * nb * sizeof(float) > WS_SCORES_BYTES)
+        return fail(c, PCK_EUNSUPPORTED, "too many blocks for the score workspace");
+    int* sel_blocks = reinterpret_cast<int*>(c->sel);
+    uint8_t* sel_mask = c->sel + static_cast<size_t>(n_groups) * sel_max * sizeof(int);
+    sp.kmean = s->kmean[B];
+    sp.Q = Q;
+    sp.q_f16 = q_dtype == PCK_DT_F16;
+    sp.H_q = H_q;
+    sp.H_kv = s->H_kv;
+    sp.D = D;
+    sp.nb = nb;
+    sp.K_top = K_top;
+    sp.K_eff = K_eff;
+    sp.sel_max = sel_max;
+    sp.n_groups = n_groups;
+    sp.tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    sp.scores = c->scores;
+    sp.idx_out = idx_out;
+    sp.sel_blocks = sel_blocks;
+    sp.sel_mask = sel_mask;
+    cudaError_t e = launch_select(sp, st, c->sms);
+    if (e != cudaSuccess) return cuda_fail(c, e, "selector launch");
+    DescIn d{s, Q, O, LSE, K_suf, V_suf};
+    rc = run_decode(c, PCK_FMT_FP16, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, sp.grp, n_groups, &d, 1, 1, B / 16,
+                    sel_max, sel_blocks, sel_mask, st);
+    if (rc != PCK_OK) return rc;
+    return check_async(c);
+}
+
+int pck_query_sparse_auto(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
+                          int q_dtype, const void* Q, const int32_t* head_map, int fa_window, float* O, float* LSE,
+                          int32_t* idx_out, void* stream) {
+    return sparse_common(c, sid, layer, H_q, D, B, K_top, H_kv, 0, q_dtype, Q, nullptr, nullptr, head_map, fa_window, O,
+                         LSE, idx_out, stream);
+}
+
+int pck_query_sparse_auto_fused(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
+                                int S_suf, int q_dtype, const void* Q, const void* K_suf, const void* V_suf,
+                                const int32_t* head_map, int fa_window, float* O, float* LSE, int32_t* idx_out,
+                                void* stream) {
+    return sparse_common(c, sid, layer, H_q, D, B, K_top, H_kv, S_suf, q_dtype, Q, K_suf, V_suf, head_map, fa_window,
+                         O, LSE, idx_out, stream);
+}
+
+int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int H_kv, int D, int S_suf, int q_dtype,
+                    const int32_t* head_map, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (n < 1 || n > PCK_MAX_BATCH || !descs) return fail(c, PCK_EINVAL, "n=%d (1..%d) or NULL descs", n, PCK_MAX_BATCH);
+    if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
+    if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
+    DescIn ds[PCK_MAX_BATCH];
+    int fmt = -1;
+    for (int i = 0; i < n; ++i) {
+        Slot* s = nullptr;
+        int rc = find_slot(c, descs[i].sid, descs[i].layer, &s);
+        if (rc != PCK_OK) return rc;
+        if (s->D != D || s->H_kv != H_kv)
+            return fail(c, PCK_EINVAL, "descriptor %d: slot shape (H_kv=%d, D=%d) differs from the batch", i, s->H_kv, s->D);
+        if (fmt >= 0 && s->fmt != fmt) return fail(c, PCK_EINVAL, "descriptor %d: mixed slot formats", i);
+        fmt = s->fmt;
+        if (!descs[i].Q || !descs[i].O) return fail(c, PCK_EINVAL, "descriptor %d: NULL Q or O", i);
+        if (S_suf > 0 && (!descs[i].K_suf || !descs[i].V_suf))
+            return fail(c, PCK_EINVAL, "descriptor %d: NULL suffix", i);
+        ds[i] = DescIn{s, descs[i].Q, descs[i].O, descs[i].LSE, descs[i].K_suf, descs[i].V_suf};
+    }
+    WorkGroup grp[MAX_GROUPS];
+    int n_groups = 0;
+    int rc = build_groups(c, H_q, H_kv, head_map, grp, &n_groups, nullptr, nullptr);
+    if (rc != PCK_OK) return rc;
+    rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0, nullptr, nullptr,
+                    static_cast<cudaStream_t>(stream));
+    if (rc != PCK_OK) return rc;
+    return check_async(c);
+}
+
+int pck_quantize_mlx4g32(const void* X, int src_dtype, int64_t rows, int kv_dim, void* out_records, void* stream) {
+    if (!X || !out_records || rows < 0 || kv_dim < 32 || kv_dim % 32) return PCK_EINVAL;
+    if (!dtype_ok(src_dtype)) return PCK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(X) & 15) return PCK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(out_records) & 3) return PCK_EINVAL;
+    if (rows == 0) return PCK_OK;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = launch_quantize(X, src_dtype == PCK_DT_F16, rows, kv_dim, out_records,
+                                    static_cast<cudaStream_t>(stream), sms > 0 ? sms : 1);
+    return e == cudaSuccess ? PCK_OK : PCK_ECUDA;
+}
+
+int pck_info(pck_ctx* c, pck_info_t* out) {
+    if (!c || !out) return PCK_EINVAL;
+    out->slots_used = static_cast<int64_t>(c->slots.size());
+    out->slots_max = c->max_slots;
+    out->cold_entries = static_cast<int64_t>(c->cold.size());
+    out->bytes_resident = c->bytes_resident;
+    out->queries_served = c->queries;
+    out->stores = c->stores;
+    out->evictions = c->evictions;
+    return PCK_OK;
+}
+
+int pck_sync(pck_ctx* c, void* stream) {
+    if (!c) return PCK_EINVAL;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(c, e, "stream synchronize");
+    int herr = 0;
+    e = cudaMemcpy(&herr, c->dev_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "error word read");
+    if (herr) {
+        cudaMemset(c->dev_err, 0, sizeof(int));
+        cudaMemset(c->counters, 0, WS_COUNTERS * sizeof(int));
+        cudaDeviceSynchronize();
+        return fail(c, PCK_ECUDA, "a device wait gave up (code %d); results of the affected calls are invalid", herr);
+    }
+    return PCK_OK;
+}
+
+}  // extern "C"

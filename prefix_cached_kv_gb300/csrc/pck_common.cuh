@@ -1,0 +1,183 @@
+// pck_common.cuh -- shared device helpers, resident tile layout and launch parameter blocks.
+//
+// Resident layout of a slot (one (sid, layer) of the ATTEND.PREFIX.STORE problem statement,
+// "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms"): per kv head g, the N prefix tokens are
+// cut into 16-token tiles; tile j of head g sits at  base + (g * ntiles + j) * tile_bytes.
+// Inside a tile the data is stored in the register-fragment order of the warp MMA
+// m16n8k16 (f16 in, f32 accumulate) so that every lane reads its fragments with 16-byte
+// shared-memory loads and no shuffles:
+//
+//   FP16 tile (64*D bytes):     [K part 32*D B][V part 32*D B]
+//     K part, 16-B chunk s (one 16-wide k-step of d) for lane l at (s*32 + l)*16:
+//        u32 r = nb*2 + hi  (nb: token n-block 0/1, hi: d offset +8)  holds
+//        half2( K[t][d0], K[t][d0+1] ),  t = 8*nb + l/4,  d0 = 16*s + 8*hi + 2*(l%4)
+//     V part, chunk c for lane l at (c*32 + l)*16:
+//        u32 r = jj*2 + hi  (j = 2c + jj: 8-wide n-block of d)  holds
+//        half2( V[t0][d], V[t0+1][d] ),  d = 8*j + l/4,  t0 = 8*hi + 2*(l%4)
+//
+//   MLX4G32 tile (20*D bytes):  [K codes 8*D B][K sb 2*D B][V codes 8*D B][V sb 2*D B]
+//     codes: lane l owns D/16 u32 words; word i at ((i/4)*32 + l)*16 + (i%4)*4.
+//       K word i: nb = i / (D/32), group gq = i % (D/32) (k-steps s0 = 2gq, s1 = 2gq+1),
+//         t = 8*nb + l/4, q = l%4; nibble n (bits 4n..4n+3):
+//           n0 = c[t][16s0+2q]  n4 = c[t][16s0+2q+1]  n1 = c[t][16s0+8+2q]  n5 = c[t][16s0+9+2q]
+//           n2 = c[t][16s1+2q]  n6 = c[t][16s1+2q+1]  n3 = c[t][16s1+8+2q]  n7 = c[t][16s1+9+2q]
+//       V word i: n-blocks j0 = 2i, j1 = 2i+1, d0 = 8*j0 + l/4, d1 = 8*j1 + l/4:
+//           n0 = c[2q][d0]  n4 = c[2q+1][d0]  n1 = c[8+2q][d0]  n5 = c[9+2q][d0]
+//           n2 = c[2q][d1]  n6 = c[2q+1][d1]  n3 = c[8+2q][d1]  n7 = c[9+2q][d1]
+//       so (w & 0x000F000F), (w & 0x00F000F0), ((w>>8) & 0x000F000F), ((w>>8) & 0x00F000F0),
+//       each OR 0x64006400, are four half2 registers (1024 + c) or (1024 + 16c).
+//     sb: [q 0..3][slot 0..3][group 0..D/32) half2(scale, bias), slot -> token {2q, 2q+1, 8+2q, 9+2q}.
+//
+// The codes, scales and biases are the bytes of the mlx4g32 records ("Shared KV Cache Serving --
+// Pion as LLM Memory", section "Quantized tier -- mlx4g32"), only permuted.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pck {
+
+constexpr int FMT_FP16 = 0;
+constexpr int FMT_I4 = 1;
+constexpr int TILE_TOK = 16;       // tokens per resident tile
+constexpr int GMAX = 8;            // q heads per work item (MMA rows 0-7 hi, 8-15 lo)
+constexpr int MAX_DESC = 64;       // descriptors per launch
+constexpr int MAX_GROUPS = 64;     // work groups (kv head x q-head batch)
+constexpr int DECODE_WARPS = 4;    // warps per CTA (each an independent worker)
+
+__host__ __device__ constexpr int tile_bytes(int fmt, int D) { return fmt == FMT_FP16 ? 64 * D : 20 * D; }
+
+// ------------------------------------------------------------------ launch parameter blocks
+
+struct DecodeDesc {
+    const uint8_t* kv;      // resident tiles of this slot: [H_kv][ntiles][tile_bytes]
+    const void* Q;          // [H_q, D] (q_f16 ? half : float)
+    float* O;               // [H_q, D]
+    float* LSE;             // [H_q] or nullptr
+    const __half* Ksuf;     // [H_kv, S_suf, D] or nullptr
+    const __half* Vsuf;
+    const int* sel_blocks;  // sparse: [n_groups][sel_max] block ids (-1 = empty), or nullptr
+    const uint8_t* sel_mask;// sparse: [n_groups][sel_max] bit h = local q head h selected it
+    int N;                  // prefix tokens
+    int ntiles;             // ceil(N / 16)
+    int vtiles;             // tiles of one item's sequence (ntiles, or sel_max * tiles/block)
+    int tile_off;           // first global tile of this descriptor's items
+};
+
+struct WorkGroup {
+    int g;                  // kv head
+    int nq;                 // q heads (<= GMAX)
+    int8_t qh[GMAX];        // the q heads, local order
+};
+
+struct DecodeParams {
+    DecodeDesc desc[MAX_DESC];
+    WorkGroup grp[MAX_GROUPS];
+    int n_desc, n_groups, H_q, H_kv, S_suf, q_f16;
+    int total_tiles;        // sum over items of vtiles
+    int tpw;                // tiles per prefix worker
+    int n_workers;          // prefix workers (warps)
+    int n_suf;              // suffix pieces per item (ceil(S_suf / 16))
+    int sparse;             // 1: item sequences come from sel_blocks
+    int tiles_per_block;    // sparse: B / 16
+    int sel_max;            // sparse: entries per group in sel_blocks
+    float scale_log2;       // tau * log2(e)
+    float* partials;        // workspace: [slots][GMAX][D + 2]
+    int* counters;          // workspace: [n_items]
+    int* err;               // device error word (bounded waits that gave up)
+};
+
+// ------------------------------------------------------------------ small PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~2^22 polls (well over a second with the
+// back-off) and returns false, so that a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < (1u << 22); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it > 64) __nanosleep(64);
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completing on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// x -> (hi, lo) fp16 pair with hi + lo == x to ~22 bits; packs two values per register.
+__device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    __half2 h = __floats2half2_rn(x0, x1);
+    float2 hf = __half22float2(h);
+    __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = h2_as_u32(h);
+    lo = h2_as_u32(l);
+}
+
+// Four 4-bit codes pairs of one word -> half2 registers holding exact (c, c) or (16c, 16c).
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+    const uint32_t magic = 0x64006400u;   // fp16 1024.0 in both halves
+    uint32_t w8 = w >> 8;
+    uint32_t r0, r1, r2, r3;
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r0) : "r"(w), "r"(0x000F000Fu), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r1) : "r"(w), "r"(0x00F000F0u), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r2) : "r"(w8), "r"(0x000F000Fu), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r3) : "r"(w8), "r"(0x00F000F0u), "r"(magic));
+    const __half2 k1024 = u32_as_h2(magic);
+    p0 = h2_as_u32(__hsub2(u32_as_h2(r0), k1024));
+    p1 = h2_as_u32(__hsub2(u32_as_h2(r1), k1024));
+    p2 = h2_as_u32(__hsub2(u32_as_h2(r2), k1024));
+    p3 = h2_as_u32(__hsub2(u32_as_h2(r3), k1024));
+}
+
+__device__ __forceinline__ void set_err(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+}  // namespace pck

@@ -1,0 +1,617 @@
+// pck_decode.cu -- M=1 attention over a resident prefix: split-K ("stream-K") decode with the
+// dense suffix and the online-softmax merge fused into the same launch.
+//
+// Follows "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms": QUERY (M=1), QUERY_FUSED
+// (prefix + dense suffix + merge in one dispatch), QUERY_SPARSE_AUTO(_FUSED) (attention
+// restricted to selected blocks), with GQA through head_map; and "Shared KV Cache Serving --
+// Pion as LLM Memory", section "Wire-protocol details" (LSE of each row for the merge).
+//
+// Work decomposition. A work item is (query descriptor, kv head, <= 8 q heads of that kv head).
+// Every item is a sequence of 16-token resident tiles (the prefix, or the tiles of the selected
+// blocks). All items' tiles are concatenated and cut into equal contiguous ranges, one per warp
+// ("worker"), so the whole GPU streams the same number of bytes per warp whatever the shapes.
+// A worker keeps a private ring of shared-memory stages filled by 1-D TMA bulk copies
+// (cp.async.bulk, mbarrier completion) and computes, per tile, S = q K^T and O += P V with the
+// warp MMA m16n8k16 (fp16 operands, fp32 accumulation): the NT q heads of the item are the MMA
+// rows (hi part in rows 0-7, lo part in rows 8-15 -- q and P are split in two fp16 halves to
+// keep fp32 accuracy), tokens / head dims the columns. mlx4g32 codes enter the MMA as exact
+// fp16 integers; the per-group affine terms are applied to the fp32 scores
+// (z = s * sum_d q_d c_d + b * sum_d q_d) and, for V, through P' = p * s and sum_t p_t b_t.
+// Each worker writes an (m, l, o) partial per item piece; the last piece to finish (atomic
+// ticket, no waiting) merges all pieces of the item plus the dense suffix pieces:
+//   m = max m_k, l = sum l_k 2^(m_k - m), O = sum o_k 2^(m_k - m) / l, LSE = (m + log2 l) ln 2.
+// Softmax runs in base 2 on log2(e)-prescaled scores; the running max is only moved when a
+// tile's max exceeds it by more than 8 (so stored weights stay <= 256), which keeps the
+// rescale of the accumulators off the common path and does not change the result.
+#include <math.h>
+
+#include "pck_common.cuh"
+#include "pck_kernels.h"
+
+namespace pck {
+
+template <int FMT, int D>
+struct DCfg {
+    static constexpr int KS = D / 16;       // 16-wide k-steps over d
+    static constexpr int NG = D / 32;       // mlx4g32 groups per head
+    static constexpr int NBV = D / 8;       // PV n-blocks over d
+    static constexpr int TB = tile_bytes(FMT, D);
+    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 2 : 1));
+    static constexpr int STAGE = TPS * TB;
+    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : 4;
+    static constexpr bool QSMEM = D > 128;  // q fragments live in shared memory (register budget)
+    static constexpr int QSMEM_BYTES = QSMEM ? KS * 32 * 16 : 0;
+    static constexpr int RING = NSTAGE * STAGE;
+    static constexpr int SMEM = DECODE_WARPS * (RING + QSMEM_BYTES) + DECODE_WARPS * NSTAGE * 8;
+};
+
+constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
+constexpr float LN2 = 0.69314718055994530942f;
+
+template <int D>
+struct QAStore {
+    static constexpr int KS = D / 16;
+    uint32_t r[D > 128 ? 1 : KS][4];
+};
+
+template <int FMT, int D>
+struct WState {
+    using C = DCfg<FMT, D>;
+    QAStore<D> qa;
+    float qsum[C::NG];
+    float oacc[C::NBV][4];
+    float bacc[C::NG];
+    float m_ref;
+    float l_part;
+};
+
+template <int D>
+__device__ __forceinline__ void get_qa(const QAStore<D>& qa, const uint32_t* qsm, int s, int lane, uint32_t (&a)[4]) {
+    if constexpr (D > 128) {
+        uint4 v = *reinterpret_cast<const uint4*>(qsm + (s * 32 + lane) * 4);
+        a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+    } else {
+        a[0] = qa.r[s][0]; a[1] = qa.r[s][1]; a[2] = qa.r[s][2]; a[3] = qa.r[s][3];
+    }
+}
+
+__device__ __forceinline__ float ld_q(const void* Q, int q_f16, int idx) {
+    return q_f16 ? __half2float(reinterpret_cast<const __half*>(Q)[idx]) : reinterpret_cast<const float*>(Q)[idx];
+}
+
+// Build the MMA A fragments of the item's q heads (rows l/4: hi, rows l/4+8: lo), prescaled by
+// tau*log2(e); for the mlx4g32 tier, d offsets 8..15 of every k-step are divided by 16 (those B
+// registers hold 16 * code).
+template <int FMT, int D>
+__device__ __forceinline__ void start_item(WState<FMT, D>& st, uint32_t* qsm, const DecodeParams& p,
+                                           const DecodeDesc& ds, const WorkGroup& wg, int lane) {
+    using C = DCfg<FMT, D>;
+    const int q = lane & 3, h = lane >> 2;
+    const int qh = h < wg.nq ? wg.qh[h] : -1;
+    float gs[C::NG];
+#pragma unroll
+    for (int g = 0; g < C::NG; ++g) gs[g] = 0.f;
+#pragma unroll
+    for (int s = 0; s < C::KS; ++s) {
+        uint32_t a[4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int d0 = 16 * s + 8 * r + 2 * q;
+            float x0 = 0.f, x1 = 0.f;
+            if (qh >= 0) {
+                x0 = ld_q(ds.Q, p.q_f16, qh * D + d0) * p.scale_log2;
+                x1 = ld_q(ds.Q, p.q_f16, qh * D + d0 + 1) * p.scale_log2;
+            }
+            gs[s / 2] += x0 + x1;
+            const float f = (FMT == FMT_I4 && r == 1) ? 0.0625f : 1.0f;
+            split_hi_lo(x0 * f, x1 * f, a[2 * r], a[2 * r + 1]);
+        }
+        if constexpr (C::QSMEM) {
+            *reinterpret_cast<uint4*>(qsm + (s * 32 + lane) * 4) = make_uint4(a[0], a[1], a[2], a[3]);
+        } else {
+            st.qa.r[s][0] = a[0]; st.qa.r[s][1] = a[1]; st.qa.r[s][2] = a[2]; st.qa.r[s][3] = a[3];
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < C::NG; ++g) {
+        float v = gs[g];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        st.qsum[g] = v;
+        st.bacc[g] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < C::NBV; ++j) st.oacc[j][0] = st.oacc[j][1] = st.oacc[j][2] = st.oacc[j][3] = 0.f;
+    st.m_ref = -INFINITY;
+    st.l_part = 0.f;
+    __syncwarp();
+}
+
+// Online softmax on this lane's 4 scores (tokens 2q, 2q+1, 8+2q, 9+2q of the tile; head l/4).
+template <int FMT, int D>
+__device__ __forceinline__ void softmax_update(WState<FMT, D>& st, float (&z)[4], float (&pr)[4]) {
+    using C = DCfg<FMT, D>;
+    float mt = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const bool need = mt > st.m_ref + RESCALE_THRESHOLD;   // false when mt == -inf
+    if (__any_sync(0xffffffffu, need)) {
+        const float mnew = need ? mt : st.m_ref;
+        const float alpha = need ? exp2f(st.m_ref - mnew) : 1.0f;   // exp2(-inf) = 0 on the first tile
+#pragma unroll
+        for (int j = 0; j < C::NBV; ++j) {
+            st.oacc[j][0] *= alpha; st.oacc[j][1] *= alpha; st.oacc[j][2] *= alpha; st.oacc[j][3] *= alpha;
+        }
+#pragma unroll
+        for (int g = 0; g < C::NG; ++g) st.bacc[g] *= alpha;
+        st.l_part *= alpha;
+        st.m_ref = mnew;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pr[k] = (z[k] == -INFINITY) ? 0.f : exp2f(z[k] - st.m_ref);
+    st.l_part += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+}
+
+__device__ __forceinline__ void mask_scores(float (&z)[4], int lane, int valid, bool head_ok) {
+    const int q = lane & 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int t = (k & 1) + 2 * q + ((k >> 1) << 3);
+        if (!head_ok || t >= valid) z[k] = -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------------- fp16 tile (fetch functors)
+
+struct SmemFp16Tile {
+    const uint8_t* kp;
+    const uint8_t* vp;
+    int lane;
+    __device__ __forceinline__ uint4 k(int s) const { return *reinterpret_cast<const uint4*>(kp + (s * 32 + lane) * 16); }
+    __device__ __forceinline__ uint4 v(int c) const { return *reinterpret_cast<const uint4*>(vp + (c * 32 + lane) * 16); }
+};
+
+// Dense suffix K_suf/V_suf [S_suf, D] of one kv head, natural layout, read straight from global.
+template <int D>
+struct GlobalSuffixTile {
+    const __half* Kg;   // kv head base [S_suf, D]
+    const __half* Vg;
+    int t0, S, lane;
+    __device__ __forceinline__ uint32_t kw(int t, int d) const {
+        return t < S ? __ldg(reinterpret_cast<const uint32_t*>(Kg + (size_t)t * D + d)) : 0u;
+    }
+    __device__ __forceinline__ uint32_t vw(int t, int d) const {
+        const unsigned short a = t < S ? __ldg(reinterpret_cast<const unsigned short*>(Vg + (size_t)t * D + d)) : 0;
+        const unsigned short b = t + 1 < S ? __ldg(reinterpret_cast<const unsigned short*>(Vg + (size_t)(t + 1) * D + d)) : 0;
+        return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+    }
+    __device__ __forceinline__ uint4 k(int s) const {
+        const int q = lane & 3, l4 = lane >> 2;
+        const int d0 = 16 * s + 2 * q;
+        return make_uint4(kw(t0 + l4, d0), kw(t0 + l4, d0 + 8), kw(t0 + 8 + l4, d0), kw(t0 + 8 + l4, d0 + 8));
+    }
+    __device__ __forceinline__ uint4 v(int c) const {
+        const int q = lane & 3, l4 = lane >> 2;
+        const int dA = 8 * (2 * c) + l4, dB = 8 * (2 * c + 1) + l4;
+        return make_uint4(vw(t0 + 2 * q, dA), vw(t0 + 8 + 2 * q, dA), vw(t0 + 2 * q, dB), vw(t0 + 8 + 2 * q, dB));
+    }
+};
+
+template <int FMT, int D, typename Tile>
+__device__ __forceinline__ void tile_fp16(WState<FMT, D>& st, const uint32_t* qsm, const Tile& tl, int lane, int valid,
+                                          bool head_ok) {
+    using C = DCfg<FMT, D>;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < C::KS; ++s) {
+        uint32_t a[4];
+        get_qa<D>(st.qa, qsm, s, lane, a);
+        const uint4 kb = tl.k(s);
+        mma16816(acc0, a, kb.x, kb.y);
+        mma16816(acc1, a, kb.z, kb.w);
+    }
+    float z[4] = {acc0[0] + acc0[2], acc0[1] + acc0[3], acc1[0] + acc1[2], acc1[1] + acc1[3]};
+    mask_scores(z, lane, valid, head_ok);
+    float pr[4];
+    softmax_update<FMT, D>(st, z, pr);
+    uint32_t a[4];
+    split_hi_lo(pr[0], pr[1], a[0], a[1]);
+    split_hi_lo(pr[2], pr[3], a[2], a[3]);
+#pragma unroll
+    for (int c = 0; c < C::KS; ++c) {
+        const uint4 vb = tl.v(c);
+        mma16816(st.oacc[2 * c], a, vb.x, vb.y);
+        mma16816(st.oacc[2 * c + 1], a, vb.z, vb.w);
+    }
+}
+
+// ---------------------------------------------------------------- mlx4g32 tile (shared memory)
+
+template <int D>
+__device__ __forceinline__ void tile_i4(WState<FMT_I4, D>& st, const uint32_t* qsm, const uint8_t* tile, int lane,
+                                        int valid, bool head_ok) {
+    using C = DCfg<FMT_I4, D>;
+    constexpr int NG = C::NG;
+    const int q = lane & 3;
+    const uint8_t* kc = tile;
+    const uint32_t* ksb = reinterpret_cast<const uint32_t*>(tile + 8 * D) + q * 4 * NG;
+    const uint8_t* vc = tile + 10 * D;
+    const uint32_t* vsb = reinterpret_cast<const uint32_t*>(tile + 18 * D) + q * 4 * NG;
+    uint32_t kw[D / 16];
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(kc + (c * 32 + lane) * 16);
+        kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
+    }
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            uint32_t b00, b01, b10, b11;
+            unpack_word(kw[nb * NG + g], b00, b01, b10, b11);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t a[4];
+            get_qa<D>(st.qa, qsm, 2 * g, lane, a);
+            mma16816(acc, a, b00, b01);
+            get_qa<D>(st.qa, qsm, 2 * g + 1, lane, a);
+            mma16816(acc, a, b10, b11);
+            const float2 sb0 = __half22float2(u32_as_h2(ksb[(2 * nb) * NG + g]));
+            const float2 sb1 = __half22float2(u32_as_h2(ksb[(2 * nb + 1) * NG + g]));
+            z[2 * nb] = fmaf(sb0.x, acc[0] + acc[2], fmaf(sb0.y, st.qsum[g], z[2 * nb]));
+            z[2 * nb + 1] = fmaf(sb1.x, acc[1] + acc[3], fmaf(sb1.y, st.qsum[g], z[2 * nb + 1]));
+        }
+    }
+    mask_scores(z, lane, valid, head_ok);
+    float pr[4];
+    softmax_update<FMT_I4, D>(st, z, pr);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const float2 s0 = __half22float2(u32_as_h2(vsb[0 * NG + g]));
+        const float2 s1 = __half22float2(u32_as_h2(vsb[1 * NG + g]));
+        const float2 s2 = __half22float2(u32_as_h2(vsb[2 * NG + g]));
+        const float2 s3 = __half22float2(u32_as_h2(vsb[3 * NG + g]));
+        st.bacc[g] = fmaf(pr[0], s0.y, fmaf(pr[1], s1.y, fmaf(pr[2], s2.y, fmaf(pr[3], s3.y, st.bacc[g]))));
+        uint32_t a[4];
+        split_hi_lo(pr[0] * s0.x, pr[1] * s1.x, a[0], a[1]);
+        split_hi_lo(pr[2] * s2.x * 0.0625f, pr[3] * s3.x * 0.0625f, a[2], a[3]);
+#pragma unroll
+        for (int ww = 0; ww < 2; ++ww) {
+            const int i = 2 * g + ww;          // V word: n-blocks 2i, 2i+1
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vc + ((i >> 2) * 32 + lane) * 16 + (i & 3) * 4);
+            uint32_t p0, p1, p2, p3;
+            unpack_word(w, p0, p1, p2, p3);
+            mma16816(st.oacc[2 * i], a, p0, p1);
+            mma16816(st.oacc[2 * i + 1], a, p2, p3);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- pieces, tickets and the merge
+
+__device__ __forceinline__ int item_pieces(const DecodeParams& p, int item) {
+    const int d = item / p.n_groups, grp = item - d * p.n_groups;
+    const int s = p.desc[d].tile_off + grp * p.desc[d].vtiles;
+    const int e = s + p.desc[d].vtiles;
+    return (e - 1) / p.tpw - s / p.tpw + 1;
+}
+
+template <int D>
+__device__ void combine_item(const DecodeParams& p, int item, int lane) {
+    const int d = item / p.n_groups, grp = item - d * p.n_groups;
+    const DecodeDesc& ds = p.desc[d];
+    const WorkGroup& wg = p.grp[grp];
+    const int s = ds.tile_off + grp * ds.vtiles, e = s + ds.vtiles;
+    const int w0 = s / p.tpw, w1 = (e - 1) / p.tpw;
+    const int n_items = p.n_desc * p.n_groups;
+    const int npref = w1 - w0 + 1;
+    const int npieces = npref + p.n_suf;
+    constexpr int PSTR = GMAX * (D + 2);
+    for (int h = 0; h < wg.nq; ++h) {
+        float M = -INFINITY;
+        for (int k = 0; k < npieces; ++k) {
+            const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
+            M = fmaxf(M, __ldcg(p.partials + (size_t)slot * PSTR + h * (D + 2)));
+        }
+        float L = 0.f;
+        float o[D / 32];
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) o[i] = 0.f;
+        for (int k = 0; k < npieces; ++k) {
+            const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
+            const float* ph = p.partials + (size_t)slot * PSTR + h * (D + 2);
+            const float mk = __ldcg(ph);
+            const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+            L = fmaf(wk, __ldcg(ph + 1), L);
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) o[i] = fmaf(wk, __ldcg(ph + 2 + lane + 32 * i), o[i]);
+        }
+        const int qh = wg.qh[h];
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) ds.O[(size_t)qh * D + lane + 32 * i] = o[i] * inv;
+        if (lane == 0 && ds.LSE) ds.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+    }
+}
+
+template <int FMT, int D>
+__device__ void finish_piece(WState<FMT, D>& st, const DecodeParams& p, int item, int slot, int lane) {
+    using C = DCfg<FMT, D>;
+    const int q = lane & 3, h = lane >> 2;
+    const int grp = item % p.n_groups;
+    float l = st.l_part;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    float bs[C::NG];
+#pragma unroll
+    for (int g = 0; g < C::NG; ++g) {
+        float v = st.bacc[g];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        bs[g] = FMT == FMT_I4 ? v : 0.f;
+    }
+    float* ph = p.partials + (size_t)slot * GMAX * (D + 2) + h * (D + 2);
+    if (h < p.grp[grp].nq) {
+        if (q == 0) { ph[0] = st.m_ref; ph[1] = l; }
+#pragma unroll
+        for (int j = 0; j < C::NBV; ++j) {
+            const int dd = 8 * j + 2 * q;
+            const float b = bs[j / 4];
+            ph[2 + dd] = st.oacc[j][0] + st.oacc[j][2] + b;
+            ph[3 + dd] = st.oacc[j][1] + st.oacc[j][3] + b;
+        }
+    }
+    __threadfence();
+    __syncwarp();
+    int prev = 0;
+    if (lane == 0) prev = atomicAdd(p.counters + item, 1);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == item_pieces(p, item) + p.n_suf - 1) {
+        __threadfence();
+        combine_item<D>(p, item, lane);
+        if (lane == 0) p.counters[item] = 0;   // ready for the next launch
+    }
+}
+
+// ---------------------------------------------------------------- tile cursor over a worker range
+
+struct Cursor {
+    int t, t_end, d, grp, item_start, item_end;
+};
+
+struct Chunk {
+    int item, d, grp;
+    int tile;     // first real tile (within the kv head) of the chunk
+    int nreal;    // tiles to copy and compute (0: nothing, e.g. an empty sparse slot)
+    int slot_blk; // sparse: index of the block in the group's selection list
+    bool last;    // last chunk of this worker's piece of the item
+    const uint8_t* src;
+};
+
+__device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
+    int d = 0;
+    while (d + 1 < p.n_desc && p.desc[d + 1].tile_off <= c.t) ++d;
+    const int vt = p.desc[d].vtiles;
+    const int grp = (c.t - p.desc[d].tile_off) / vt;
+    c.d = d;
+    c.grp = grp;
+    c.item_start = p.desc[d].tile_off + grp * vt;
+    c.item_end = c.item_start + vt;
+}
+
+template <int TPS, int TB>
+__device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Chunk& ch) {
+    if (c.t >= c.t_end) return false;
+    if (c.t >= c.item_end) {
+        if (++c.grp == p.n_groups) { c.grp = 0; ++c.d; }
+        c.item_start = p.desc[c.d].tile_off + c.grp * p.desc[c.d].vtiles;
+        c.item_end = c.item_start + p.desc[c.d].vtiles;
+    }
+    const DecodeDesc& ds = p.desc[c.d];
+    const int local = c.t - c.item_start;
+    const int lim = min(c.t_end, c.item_end) - c.t;
+    int n;
+    if (!p.sparse) {
+        n = min(TPS, lim);
+        ch.tile = local;
+        ch.nreal = n;
+        ch.slot_blk = 0;
+    } else {
+        const int bs = local / p.tiles_per_block, within = local - bs * p.tiles_per_block;
+        n = min(TPS, min(lim, p.tiles_per_block - within));
+        const int blk = ds.sel_blocks[c.grp * p.sel_max + bs];
+        ch.slot_blk = bs;
+        if (blk < 0) {
+            ch.tile = 0;
+            ch.nreal = 0;
+        } else {
+            ch.tile = blk * p.tiles_per_block + within;
+            ch.nreal = max(0, min(n, ds.ntiles - ch.tile));
+        }
+    }
+    ch.item = c.d * p.n_groups + c.grp;
+    ch.d = c.d;
+    ch.grp = c.grp;
+    ch.src = ds.kv + ((size_t)p.grp[c.grp].g * ds.ntiles + ch.tile) * TB;
+    c.t += n;
+    ch.last = (c.t == c.item_end) || (c.t == c.t_end);
+    return true;
+}
+
+// ---------------------------------------------------------------- workers
+
+template <int FMT, int D>
+__device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars, uint32_t* qsm) {
+    using C = DCfg<FMT, D>;
+    Cursor cons;
+    cons.t = w * p.tpw;
+    cons.t_end = min(p.total_tiles, cons.t + p.tpw);
+    if (cons.t >= cons.t_end) return;
+    cursor_seek(p, cons);
+    Cursor prod = cons;
+
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t bar_s = smem_u32(bars);
+    if (lane == 0) {
+        for (int s = 0; s < C::NSTAGE; ++s) mbar_init(bar_s + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    auto issue = [&](const Chunk& c, int s) {
+        if (lane == 0) {
+            if (c.nreal > 0) {
+                mbar_arrive_expect_tx(bar_s + 8 * s, c.nreal * C::TB);
+                bulk_g2s(ring_s + s * C::STAGE, c.src, c.nreal * C::TB, bar_s + 8 * s);
+            } else {
+                mbar_arrive(bar_s + 8 * s);
+            }
+        }
+    };
+
+    int inflight = 0;
+    for (int s = 0; s < C::NSTAGE; ++s) {
+        Chunk c;
+        if (!cursor_next<C::TPS, C::TB>(p, prod, c)) break;
+        issue(c, s);
+        ++inflight;
+    }
+
+    WState<FMT, D> st;
+    int cur_item = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    Chunk c;
+    while (cursor_next<C::TPS, C::TB>(p, cons, c)) {
+        const DecodeDesc& ds = p.desc[c.d];
+        const WorkGroup& wg = p.grp[c.grp];
+        if (c.item != cur_item) {
+            cur_item = c.item;
+            start_item<FMT, D>(st, qsm, p, ds, wg, lane);
+        }
+        if (!mbar_wait_bounded(bar_s + 8 * stage, (phase >> stage) & 1u)) {
+            set_err(p.err, 1);
+            for (int k = 1; k < inflight; ++k) {   // let the other copies land before leaving
+                const int s2 = (stage + k) % C::NSTAGE;
+                mbar_wait_bounded(bar_s + 8 * s2, (phase >> s2) & 1u);
+            }
+            return;
+        }
+        --inflight;
+        bool head_ok = (lane >> 2) < wg.nq;
+        if (p.sparse && c.nreal > 0) {
+            const uint8_t m = ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
+            head_ok = head_ok && ((m >> (lane >> 2)) & 1u);
+        }
+        const uint8_t* sbuf = ring + stage * C::STAGE;
+        for (int k = 0; k < c.nreal; ++k) {
+            const int valid = ds.N - (c.tile + k) * TILE_TOK;
+            const uint8_t* tile = sbuf + k * C::TB;
+            if constexpr (FMT == FMT_FP16) {
+                SmemFp16Tile tl{tile, tile + 32 * D, lane};
+                tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
+            } else {
+                tile_i4<D>(st, qsm, tile, lane, valid, head_ok);
+            }
+        }
+        phase ^= 1u << stage;
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();   // our reads of this stage precede the next copy into it
+        Chunk nc;
+        if (cursor_next<C::TPS, C::TB>(p, prod, nc)) {
+            issue(nc, stage);
+            ++inflight;
+        }
+        stage = stage + 1 == C::NSTAGE ? 0 : stage + 1;
+        if (c.last) {
+            finish_piece<FMT, D>(st, p, cur_item, w + cur_item, lane);
+            cur_item = -1;
+        }
+    }
+}
+
+template <int FMT, int D>
+__device__ void suffix_worker(const DecodeParams& p, int sidx, int lane, uint32_t* qsm) {
+    const int n_items = p.n_desc * p.n_groups;
+    const int item = sidx / p.n_suf, k = sidx - item * p.n_suf;
+    if (item >= n_items) return;
+    const int d = item / p.n_groups, grp = item - d * p.n_groups;
+    const DecodeDesc& ds = p.desc[d];
+    const WorkGroup& wg = p.grp[grp];
+    // The suffix is fp16 whatever the prefix format: fp16-style q fragments (no 1/16 factor).
+    WState<FMT_FP16, D> st;
+    start_item<FMT_FP16, D>(st, qsm, p, ds, wg, lane);
+    const int t0 = 16 * k;
+    GlobalSuffixTile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
+    tile_fp16<FMT_FP16, D>(st, qsm, tl, lane, p.S_suf - t0, (lane >> 2) < wg.nq);
+    finish_piece<FMT_FP16, D>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
+}
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(DECODE_WARPS * 32) decode_kernel(const __grid_constant__ DecodeParams p) {
+    using C = DCfg<FMT, D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * DECODE_WARPS + warp;
+    uint8_t* ring = smem + warp * C::RING;
+    uint32_t* qsm = reinterpret_cast<uint32_t*>(smem + DECODE_WARPS * C::RING + warp * C::QSMEM_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * (C::RING + C::QSMEM_BYTES)) + warp * C::NSTAGE;
+    if (gw < p.n_workers) {
+        prefix_worker<FMT, D>(p, gw, lane, ring, bars, qsm);
+    } else if (p.n_suf > 0) {
+        suffix_worker<FMT, D>(p, gw - p.n_workers, lane, qsm);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int FMT, int D>
+static cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) {
+    using C = DCfg<FMT, D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FMT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    decode_kernel<FMT, D><<<n_ctas, DECODE_WARPS * 32, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int FMT, int D>
+static DecodeLaunchInfo info_t() {
+    using C = DCfg<FMT, D>;
+    DecodeLaunchInfo i{C::STAGE, C::NSTAGE, C::SMEM, 0};
+    int n = 0;
+    cudaFuncSetAttribute(decode_kernel<FMT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FMT, D>, DECODE_WARPS * 32, C::SMEM) != cudaSuccess)
+        n = 1;
+    i.ctas_per_sm = n > 0 ? n : 1;
+    return i;
+}
+
+DecodeLaunchInfo decode_launch_info(int fmt, int D) {
+    if (fmt == FMT_FP16) {
+        if (D == 64) return info_t<FMT_FP16, 64>();
+        if (D == 128) return info_t<FMT_FP16, 128>();
+        return info_t<FMT_FP16, 256>();
+    }
+    if (D == 64) return info_t<FMT_I4, 64>();
+    if (D == 128) return info_t<FMT_I4, 128>();
+    return info_t<FMT_I4, 256>();
+}
+
+cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st) {
+    if (fmt == FMT_FP16) {
+        if (D == 64) return launch_t<FMT_FP16, 64>(p, n_ctas, st);
+        if (D == 128) return launch_t<FMT_FP16, 128>(p, n_ctas, st);
+        if (D == 256) return launch_t<FMT_FP16, 256>(p, n_ctas, st);
+    } else {
+        if (D == 64) return launch_t<FMT_I4, 64>(p, n_ctas, st);
+        if (D == 128) return launch_t<FMT_I4, 128>(p, n_ctas, st);
+        if (D == 256) return launch_t<FMT_I4, 256>(p, n_ctas, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pck

@@ -1,0 +1,66 @@
+// pck_kernels.h -- host-side declarations of the kernel launchers (internal to libpck).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pck_common.cuh"
+
+namespace pck {
+
+constexpr int PCK_MAXH = 64;
+
+// store side
+cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim, void* out, cudaStream_t st, int sms);
+cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
+                                 void* out, cudaStream_t st, int sms);
+cudaError_t launch_relayout_mlx4(const void* Krec, const void* Vrec, int head_rows, int H_kv, int N, int D, int ntiles,
+                                 void* out, cudaStream_t st, int sms);
+
+// M=1 split-K decode (dense or sparse item sequences), fused suffix and merge
+struct DecodeLaunchInfo {
+    int stage_bytes;
+    int nstage;
+    int smem_bytes;
+    int ctas_per_sm;
+};
+DecodeLaunchInfo decode_launch_info(int fmt, int D);
+cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);
+
+// sparse selector
+cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int ntiles, int B, float* kmean,
+                               cudaStream_t st, int sms);
+struct SelectParams {
+    const float* kmean;      // [H_kv, nb, D]
+    const void* Q;           // [H_q, D]
+    int q_f16;
+    int H_q, H_kv, D, nb, K_top, K_eff, sel_max, n_groups;
+    float tau;
+    float* scores;           // workspace [H_q, nb]
+    int* idx_out;            // [H_q, K_eff] or nullptr
+    int* sel_blocks;         // [n_groups, sel_max]
+    uint8_t* sel_mask;       // [n_groups, sel_max]
+    int8_t head_map[PCK_MAXH];
+    WorkGroup grp[MAX_GROUPS];
+};
+cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
+
+// batched-Q tensor-core prefill (tcgen05)
+struct PrefillParams {
+    const __half* Q;          // [H_q, M, D]
+    const uint8_t* kv;        // resident fp16 tiles of the slot
+    const __half* Ksuf;       // [H_kv, S_suf, D] or nullptr
+    const __half* Vsuf;
+    float* O;                 // [H_q, M, D]
+    float* LSE;               // [H_q, M] or nullptr
+    int8_t head_map[PCK_MAXH];
+    int H_q, H_kv, M, N, ntiles, S_suf, causal;
+    float scale_log2;
+    float* partials;          // split-N workspace
+    int* counters;
+    int* err;
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st, int sms, int D);
+bool prefill_supported(int D);
+
+}  // namespace pck

@@ -1,0 +1,153 @@
+// pck_sparse.cu -- block-mean top-K selector feeding the sparse (gather) decode.
+//
+// "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms" / QUERY_SPARSE_AUTO: the block means of K
+// (block size B) are kept per slot; each q head's blocks are scored against its query and the
+// K_top best are kept ("GQA-aware": a kv head's gather reads the union of its q heads' blocks
+// once, each q head attending only to its own). Ties go to the lower block index; the
+// selected indices are reported sorted ascending.
+#include <math.h>
+
+#include "pck_common.cuh"
+#include "pck_kernels.h"
+
+namespace pck {
+
+// K_mean[g, b, d] = mean over the tokens of block b of K[g, t, d] (fp32 sum of fp16 values),
+// read from the resident fp16 tiles (fragment-ordered; see pck_common.cuh).
+__global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int D, int ntiles, int B,
+                                   float* __restrict__ kmean) {
+    const int b = blockIdx.x, g = blockIdx.y, nb = gridDim.x;
+    const int t0 = b * B, t1 = min(N, t0 + B);
+    const size_t tb = (size_t)64 * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const int s = d >> 4, hi = (d >> 3) & 1, q = (d >> 1) & 3, e = d & 1;
+        float acc = 0.f;
+        for (int t = t0; t < t1; ++t) {
+            const int j = t >> 4, tt = t & 15, nbk = tt >> 3, l4 = tt & 7;
+            const int lane = 4 * l4 + q, r = nbk * 2 + hi;
+            const uint8_t* tile = tiles + ((size_t)g * ntiles + j) * tb;
+            const __half v = *reinterpret_cast<const __half*>(tile + (s * 32 + lane) * 16 + r * 4 + e * 2);
+            acc += __half2float(v);
+        }
+        kmean[((size_t)g * nb + b) * D + d] = acc / static_cast<float>(t1 - t0);
+    }
+}
+
+// score[h, b] = tau * q_h . K_mean[head_map[h], b]; one warp per (kv head, block).
+__global__ void block_scores_kernel(const __grid_constant__ SelectParams p) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= p.H_kv * p.nb) return;
+    const int g = warp / p.nb, b = warp - g * p.nb;
+    const float* km = p.kmean + ((size_t)g * p.nb + b) * p.D;
+    float kv[8];
+    const int per = p.D / 32;
+    for (int i = 0; i < per; ++i) kv[i] = km[lane + 32 * i];
+    for (int h = 0; h < p.H_q; ++h) {
+        if (p.head_map[h] != g) continue;
+        float acc = 0.f;
+        for (int i = 0; i < per; ++i) {
+            const int d = lane + 32 * i;
+            const float qv = p.q_f16 ? __half2float(reinterpret_cast<const __half*>(p.Q)[h * p.D + d])
+                                     : reinterpret_cast<const float*>(p.Q)[h * p.D + d];
+            acc = fmaf(qv, kv[i], acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) p.scores[(size_t)h * p.nb + b] = p.tau * acc;
+    }
+}
+
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+// One CTA per work group: warp w selects the top-K of the group's w-th q head, then warp 0
+// merges the heads' selections into the group's sorted union (with per-head masks).
+__global__ void select_kernel(const __grid_constant__ SelectParams p) {
+    __shared__ int picks[GMAX][64];
+    const int grp = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WorkGroup& wg = p.grp[grp];
+    const int K = p.K_eff;
+    if (warp < wg.nq) {
+        const int h = wg.qh[warp];
+        const float* sc = p.scores + (size_t)h * p.nb;
+        float prev_s = INFINITY;
+        int prev_i = -1;
+        for (int r = 0; r < K; ++r) {
+            float bs = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int b = lane; b < p.nb; b += 32) {
+                const float s = sc[b];
+                if (better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
+                    bs = s;
+                    bi = b;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (oi != 0x7fffffff && (bi == 0x7fffffff || better(os, oi, bs, bi))) {
+                    bs = os;
+                    bi = oi;
+                }
+            }
+            prev_s = bs;
+            prev_i = bi;
+            if (lane == 0) picks[warp][r] = bi;
+        }
+        __syncwarp();
+        if (lane == 0) {   // ascending order
+            for (int i = 1; i < K; ++i) {
+                const int v = picks[warp][i];
+                int j = i - 1;
+                while (j >= 0 && picks[warp][j] > v) { picks[warp][j + 1] = picks[warp][j]; --j; }
+                picks[warp][j + 1] = v;
+            }
+            if (p.idx_out)
+                for (int i = 0; i < K; ++i) p.idx_out[(size_t)h * K + i] = picks[warp][i];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int* out_b = p.sel_blocks + (size_t)grp * p.sel_max;
+        uint8_t* out_m = p.sel_mask + (size_t)grp * p.sel_max;
+        int pos[GMAX];
+        for (int w = 0; w < wg.nq; ++w) pos[w] = 0;
+        int n = 0;
+        while (true) {   // k-way merge of the sorted per-head lists
+            int best = 0x7fffffff;
+            for (int w = 0; w < wg.nq; ++w)
+                if (pos[w] < K && picks[w][pos[w]] < best) best = picks[w][pos[w]];
+            if (best == 0x7fffffff) break;
+            uint8_t m = 0;
+            for (int w = 0; w < wg.nq; ++w)
+                if (pos[w] < K && picks[w][pos[w]] == best) { m |= uint8_t(1u << w); ++pos[w]; }
+            out_b[n] = best;
+            out_m[n] = m;
+            ++n;
+        }
+        for (; n < p.sel_max; ++n) { out_b[n] = -1; out_m[n] = 0; }
+    }
+}
+
+cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int ntiles, int B, float* kmean,
+                               cudaStream_t st, int sms) {
+    (void)sms;
+    const int nb = (N + B - 1) / B;
+    dim3 grid(nb, H_kv);
+    block_means_kernel<<<grid, D < 128 ? D : 128, 0, st>>>(static_cast<const uint8_t*>(tiles), N, D, ntiles, B, kmean);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
+    (void)sms;
+    const int warps = p.H_kv * p.nb;
+    block_scores_kernel<<<(warps + 7) / 8, 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    select_kernel<<<p.n_groups, GMAX * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pck

@@ -1,0 +1,270 @@
+// pck_store.cu -- store side: mlx4g32 quantiser and the re-layout of K/V into resident tiles.
+//
+// Quantiser: "Shared KV Cache Serving -- Pion as LLM Memory", section "Quantized tier --
+// mlx4g32" (int4, group 32, affine, fp16 scale and bias, the scale rounded to fp16 before the
+// codes are chosen; per token [u32 codes x D/8][f16 scales x D/32][f16 biases x D/32], element j
+// of a group at bits 4*(j%8)).
+#include "pck_common.cuh"
+#include "pck_kernels.h"
+
+namespace pck {
+
+// ------------------------------------------------------------------ quantiser
+
+template <typename SrcT>
+__device__ __forceinline__ void load8(const SrcT* p, float (&x)[8]);
+
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* p, float (&x)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&x)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// One thread per output code word (8 consecutive elements); a group of 32 is 4 adjacent lanes.
+template <typename SrcT>
+__global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __restrict__ X, int64_t rows,
+                                                                int kv_dim, uint8_t* __restrict__ out) {
+    const int wpr = kv_dim / 8;                 // words per row
+    const int64_t total = rows * wpr;           // multiple of 4; a warp never splits a group
+    const int rec = kv_dim / 2 + kv_dim / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t wi0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // Every lane of a warp runs the same number of iterations (total is padded by the grid),
+    // so the group shuffles below always see their 4 partners.
+    int64_t iters = (total + stride - 1) / stride;
+    for (int64_t it = 0; it < iters; ++it) {
+        int64_t wi = wi0 + it * stride;
+        bool live = wi < total;
+        float x[8];
+        if (live) {
+            load8<SrcT>(X + wi * 8, x);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = 0.f;
+        }
+        float mn = x[0], mx = x[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) { mn = fminf(mn, x[k]); mx = fmaxf(mx, x[k]); }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+        const __half s16 = __float2half_rn(s32);     // round-trip through fp16 first
+        const __half b16 = __float2half_rn(mn);
+        const float sf = __half2float(s16), bf = __half2float(b16);
+        uint32_t w = 0;
+        if (sf != 0.0f) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float t = __fdiv_rn(__fsub_rn(x[k], bf), sf);
+                float c = fminf(fmaxf(rintf(t), 0.0f), 15.0f);
+                w |= static_cast<uint32_t>(c) << (4 * k);
+            }
+        }
+        if (live) {
+            const int64_t row = wi / wpr;
+            const int word = static_cast<int>(wi - row * wpr);
+            uint8_t* r = out + row * rec;
+            reinterpret_cast<uint32_t*>(r)[word] = w;
+            if ((word & 3) == 0) {
+                reinterpret_cast<__half*>(r + kv_dim / 2)[word >> 2] = s16;
+                reinterpret_cast<__half*>(r + kv_dim / 2 + kv_dim / 16)[word >> 2] = b16;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ fp16 re-layout
+
+// One thread per output u32 of a tile (tile = 16 * D u32: K part 8*D, V part 8*D).
+template <typename SrcT>
+__global__ void __launch_bounds__(256) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
+                                                            int H_kv, int N, int D, int ntiles,
+                                                            uint32_t* __restrict__ out) {
+    const int words_tile = 16 * D;
+    const int64_t total = (int64_t)H_kv * ntiles * words_tile;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tileg = i / words_tile;          // g * ntiles + j
+        const int w = static_cast<int>(i - tileg * words_tile);
+        const int g = static_cast<int>(tileg / ntiles);
+        const int j = static_cast<int>(tileg - (int64_t)g * ntiles);
+        const bool isV = w >= 8 * D;
+        const int wl = isV ? w - 8 * D : w;            // word within part
+        const int chunk = wl / 128, lane = (wl / 4) & 31, r = wl & 3;
+        const int q = lane & 3, l4 = lane >> 2;
+        int t0, t1, d0, d1;
+        if (!isV) {
+            const int nb = r >> 1, hi = r & 1;
+            t0 = t1 = 8 * nb + l4;
+            d0 = 16 * chunk + 8 * hi + 2 * q;
+            d1 = d0 + 1;
+        } else {
+            const int jj = r >> 1, hi = r & 1;
+            d0 = d1 = 8 * (2 * chunk + jj) + l4;
+            t0 = 8 * hi + 2 * q;
+            t1 = t0 + 1;
+        }
+        const SrcT* src = isV ? V : K;
+        const int tok0 = j * TILE_TOK + t0, tok1 = j * TILE_TOK + t1;
+        float v0 = tok0 < N ? static_cast<float>(src[((int64_t)g * N + tok0) * D + d0]) : 0.f;
+        float v1 = tok1 < N ? static_cast<float>(src[((int64_t)g * N + tok1) * D + d1]) : 0.f;
+        out[i] = h2_as_u32(__floats2half2_rn(v0, v1));
+    }
+}
+
+// ------------------------------------------------------------------ mlx4g32 re-layout
+
+struct RecSrc {
+    const uint8_t* base;
+    int head_rows;   // 1: rows are (g, t) with kv_dim = D; 0: rows are tokens with kv_dim = H_kv * D
+    int H_kv, N, D;
+};
+
+__device__ __forceinline__ const uint8_t* rec_row(const RecSrc& s, int g, int t, int& kvr, int& goff) {
+    if (s.head_rows) {
+        kvr = s.D;
+        goff = 0;
+        return s.base + ((int64_t)g * s.N + t) * (s.D / 2 + s.D / 8);
+    }
+    kvr = s.H_kv * s.D;
+    goff = g * s.D;
+    return s.base + (int64_t)t * (kvr / 2 + kvr / 8);
+}
+
+__device__ __forceinline__ uint32_t rec_code(const RecSrc& s, int g, int t, int d) {
+    if (t >= s.N) return 0;
+    int kvr, goff;
+    const uint8_t* r = rec_row(s, g, t, kvr, goff);
+    const int e = goff + d;
+    uint32_t w = reinterpret_cast<const uint32_t*>(r)[e >> 3];
+    return (w >> (4 * (e & 7))) & 0xFu;
+}
+
+__device__ __forceinline__ uint32_t rec_sb(const RecSrc& s, int g, int t, int gi) {
+    if (t >= s.N) return 0;
+    int kvr, goff;
+    const uint8_t* r = rec_row(s, g, t, kvr, goff);
+    const int e = goff / 32 + gi;
+    const uint16_t sc = reinterpret_cast<const uint16_t*>(r + kvr / 2)[e];
+    const uint16_t bi = reinterpret_cast<const uint16_t*>(r + kvr / 2 + kvr / 16)[e];
+    return static_cast<uint32_t>(sc) | (static_cast<uint32_t>(bi) << 16);
+}
+
+// One thread per output u32 of a tile (5 * D u32: K codes 2D, K sb D/2, V codes 2D, V sb D/2).
+__global__ void __launch_bounds__(256) relayout_mlx4_kernel(RecSrc ks, RecSrc vs, int ntiles, uint32_t* __restrict__ out) {
+    const int D = ks.D;
+    const int words_tile = 5 * D;
+    const int64_t total = (int64_t)ks.H_kv * ntiles * words_tile;
+    const int ng = D / 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tileg = i / words_tile;
+        int w = static_cast<int>(i - tileg * words_tile);
+        const int g = static_cast<int>(tileg / ntiles);
+        const int j = static_cast<int>(tileg - (int64_t)g * ntiles);
+        const int tb = j * TILE_TOK;
+        bool isV = false;
+        if (w >= 2 * D + D / 2) { isV = true; w -= 2 * D + D / 2; }
+        const RecSrc& s = isV ? vs : ks;
+        uint32_t val = 0;
+        if (w < 2 * D) {                                 // codes word
+            const int chunk = w / 128, lane = (w / 4) & 31, iw = chunk * 4 + (w & 3);
+            const int q = lane & 3, l4 = lane >> 2;
+            uint32_t nib[8];
+            if (!isV) {
+                const int nb = iw / ng, gq = iw % ng, s0 = 2 * gq, s1 = 2 * gq + 1;
+                const int t = tb + 8 * nb + l4;
+                nib[0] = rec_code(s, g, t, 16 * s0 + 2 * q);
+                nib[4] = rec_code(s, g, t, 16 * s0 + 2 * q + 1);
+                nib[1] = rec_code(s, g, t, 16 * s0 + 8 + 2 * q);
+                nib[5] = rec_code(s, g, t, 16 * s0 + 9 + 2 * q);
+                nib[2] = rec_code(s, g, t, 16 * s1 + 2 * q);
+                nib[6] = rec_code(s, g, t, 16 * s1 + 2 * q + 1);
+                nib[3] = rec_code(s, g, t, 16 * s1 + 8 + 2 * q);
+                nib[7] = rec_code(s, g, t, 16 * s1 + 9 + 2 * q);
+            } else {
+                const int d0 = 8 * (2 * iw) + l4, d1 = 8 * (2 * iw + 1) + l4;
+                nib[0] = rec_code(s, g, tb + 2 * q, d0);
+                nib[4] = rec_code(s, g, tb + 2 * q + 1, d0);
+                nib[1] = rec_code(s, g, tb + 8 + 2 * q, d0);
+                nib[5] = rec_code(s, g, tb + 9 + 2 * q, d0);
+                nib[2] = rec_code(s, g, tb + 2 * q, d1);
+                nib[6] = rec_code(s, g, tb + 2 * q + 1, d1);
+                nib[3] = rec_code(s, g, tb + 8 + 2 * q, d1);
+                nib[7] = rec_code(s, g, tb + 9 + 2 * q, d1);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) val |= nib[k] << (4 * k);
+        } else {                                         // scale/bias word
+            const int e = w - 2 * D;                     // [q][slot][group]
+            const int gi = e % ng, slot = (e / ng) & 3, q = e / (4 * ng);
+            const int toff = (slot & 1) + 2 * q + ((slot >> 1) ? 8 : 0);
+            val = rec_sb(s, g, tb + toff, gi);
+        }
+        out[i] = val;
+    }
+}
+
+// ------------------------------------------------------------------ host launchers
+
+static int grid_for(int64_t work, int threads, int sms) {
+    int64_t b = (work + threads - 1) / threads;
+    int64_t cap = (int64_t)sms * 16;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return static_cast<int>(b);
+}
+
+cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim, void* out, cudaStream_t st, int sms) {
+    int64_t total = rows * (kv_dim / 8);
+    int threads = 256;
+    int blocks = grid_for(total, threads, sms);
+    if (src_f16)
+        quantize_mlx4g32_kernel<__half><<<blocks, threads, 0, st>>>(static_cast<const __half*>(X), rows, kv_dim,
+                                                                     static_cast<uint8_t*>(out));
+    else
+        quantize_mlx4g32_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float*>(X), rows, kv_dim,
+                                                                    static_cast<uint8_t*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
+                                 void* out, cudaStream_t st, int sms) {
+    int64_t total = (int64_t)H_kv * ntiles * 16 * D;
+    int blocks = grid_for(total, 256, sms);
+    if (src_f16)
+        relayout_fp16_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half*>(K), static_cast<const __half*>(V),
+                                                             H_kv, N, D, ntiles, static_cast<uint32_t*>(out));
+    else
+        relayout_fp16_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(K), static_cast<const float*>(V),
+                                                            H_kv, N, D, ntiles, static_cast<uint32_t*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_relayout_mlx4(const void* Krec, const void* Vrec, int head_rows, int H_kv, int N, int D, int ntiles,
+                                 void* out, cudaStream_t st, int sms) {
+    RecSrc ks{static_cast<const uint8_t*>(Krec), head_rows, H_kv, N, D};
+    RecSrc vs{static_cast<const uint8_t*>(Vrec), head_rows, H_kv, N, D};
+    int64_t total = (int64_t)H_kv * ntiles * 5 * D;
+    int blocks = grid_for(total, 256, sms);
+    relayout_mlx4_kernel<<<blocks, 256, 0, st>>>(ks, vs, ntiles, static_cast<uint32_t*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace pck

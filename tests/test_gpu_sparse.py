@@ -1,0 +1,89 @@
+"""Block-mean top-K sparse attention on the GPU vs the oracle: selected blocks bit-exact (except
+near-ties of the oracle's scores), outputs within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import pck_oracle as orc
+from prefix_cached_kv_gb300 import synth
+from tests.gpu_util import TIE_EPS, assert_close_o_lse, ctx_factory, dev, host, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    need_gpu()
+    c = ctx_factory()
+    yield c
+    c.close()
+
+
+def _check_idx(idx, scores, K_top):
+    ok_rows = orc.topk_margin(scores, K_top) >= TIE_EPS
+    want = orc.select_top_blocks(scores, K_top)
+    assert np.array_equal(idx[ok_rows], want[ok_rows])
+    assert (np.diff(idx, axis=1) > 0).all()          # strictly ascending everywhere
+    return want
+
+
+@pytest.mark.parametrize("H_q,H_kv,N,D,B,K_top,S", [
+    (8, 2, 1000, 64, 64, 3, 0),
+    (8, 2, 1000, 64, 64, 3, 7),
+    (4, 4, 777, 256, 32, 5, 16),
+    (6, 2, 4096, 128, 64, 8, 32),
+    (8, 1, 100, 64, 16, 2, 0),
+])
+def test_sparse_matches_oracle(ctx, H_q, H_kv, N, D, B, K_top, S):
+    seed = N + D + K_top
+    K, V = synth.gen_kv(seed, H_kv, N, D)
+    Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+    hm = synth.default_head_map(H_q, H_kv)
+    sid = f"sp{seed}"
+    ctx.store(sid, 0, dev(K), dev(V))
+    Ks = Vs = None
+    if S:
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+    O, L, idx = ctx.query_sparse_auto(sid, 0, dev(Q), B, K_top, H_kv, K_suf=dev(Ks) if S else None,
+                                      V_suf=dev(Vs) if S else None)
+    O_ref, L_ref, idx_ref, scores = orc.sparse_query(Q, K, V, hm, B, K_top, Ks, Vs)
+    k_eff = min(K_top, (N + B - 1) // B)
+    idx = host(idx).reshape(-1)[: H_q * k_eff].reshape(H_q, k_eff)
+    _check_idx(idx, scores, K_top)
+    near = orc.topk_margin(scores, K_top) < TIE_EPS
+    assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], "sparse")
+    ctx.drop(sid)
+
+
+def test_sparse_covering_all_blocks_equals_dense(ctx):
+    H_q, H_kv, N, D, B = 8, 2, 300, 64, 64
+    K, V = synth.gen_kv(21, H_kv, N, D)
+    Q = synth.gen_q(21, H_q, 1, D)
+    ctx.store("spall", 0, dev(K), dev(V))
+    O, L, idx = ctx.query_sparse_auto("spall", 0, dev(Q[:, 0]), B, 5, H_kv)
+    Od, Ld = ctx.query("spall", 0, dev(Q))
+    assert (host(idx).reshape(-1)[: H_q * 5].reshape(H_q, 5) == np.arange(5)).all()
+    O_ref, L_ref = orc.prefix_query(Q, K, V, synth.default_head_map(H_q, H_kv))
+    assert_close_o_lse(host(O), host(L), O_ref[:, 0], L_ref[:, 0], "sparse-all")
+    assert_close_o_lse(host(Od), host(Ld), O_ref, L_ref, "dense")
+
+
+def test_sparse_needle_workload_full(ctx):
+    """Sparse long-context workload: N=65,536, D=256, H_q=8, H_kv=2, B=64, K_top=8, S_suf=32, with
+    eight seeded needle blocks pulled toward the query (+3 sigma along the GQA-group direction)."""
+    w = synth.WORKLOADS["sparse_topk_64k"]
+    H_q, H_kv, N, D, B, Kt, S = w["H_q"], w["H_kv"], w["N"], w["D"], w["B"], w["K_top"], w["S_suf"]
+    K, V = synth.gen_kv(0, H_kv, N, D)
+    Q = synth.gen_q(0, H_q, 1, D)[:, 0]
+    hm = synth.default_head_map(H_q, H_kv)
+    needles = synth.needle_blocks(0, N // B, Kt)
+    K = synth.plant_needles(K, Q, hm, needles, B)
+    Ks, Vs = synth.gen_suffix(0, H_kv, S, D)
+    ctx.store("needle", 0, dev(K), dev(V))
+    O, L, idx = ctx.query_sparse_auto("needle", 0, dev(Q), B, Kt, H_kv, K_suf=dev(Ks), V_suf=dev(Vs))
+    O_ref, L_ref, idx_ref, scores = orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs)
+    idx = host(idx)
+    assert (idx_ref == needles[None]).all()
+    assert np.array_equal(idx, idx_ref)
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, "needle")
+    ctx.drop("needle")
