@@ -247,6 +247,29 @@ class Context:
         return self._rc(self.lib.pck_query_batch(self.h, n, arr, H_q, H_kv, D, S_suf, q_dtype, hm[0] if hm else None,
                                                  _stream(stream)))
 
+    def batch_caller(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None):
+        """Prebuild the descriptor array of a pck_query_batch call; returns a no-argument callable
+        that issues the call on the current stream (cheap enough to capture in a CUDA graph)."""
+        n = len(descs)
+        arr = (QueryDesc * n)()
+        keep = []
+        for i, d in enumerate(descs):
+            sid = d["sid"].encode()
+            keep.append(sid)
+            arr[i] = QueryDesc(sid, d["layer"], d["Q"].data_ptr(), d["O"].data_ptr(),
+                               d["LSE"].data_ptr() if d.get("LSE") is not None else None,
+                               d["K_suf"].data_ptr() if d.get("K_suf") is not None else None,
+                               d["V_suf"].data_ptr() if d.get("V_suf") is not None else None)
+        hm = _hm(head_map)
+        fn, h = self.lib.pck_query_batch, self.h
+
+        def call():
+            rc = fn(h, n, arr, H_q, H_kv, D, S_suf, q_dtype, hm[0] if hm else None, _stream(None))
+            if rc != OK:
+                raise PckError(rc, self.last_error())
+        call._keep = (arr, keep, hm)
+        return call
+
     def info(self) -> dict:
         out = InfoT()
         self._rc(self.lib.pck_info(self.h, ctypes.byref(out)))

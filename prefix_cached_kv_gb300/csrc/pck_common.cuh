@@ -2,18 +2,20 @@
 //
 // Resident layout of a slot (one (sid, layer) of the ATTEND.PREFIX.STORE problem statement,
 // "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms"): per kv head g, the N prefix tokens are
-// cut into 16-token tiles; tile j of head g sits at  base + (g * ntiles + j) * tile_bytes.
-// Inside a tile the data is stored in the register-fragment order of the warp MMA
-// m16n8k16 (f16 in, f32 accumulate) so that every lane reads its fragments with 16-byte
-// shared-memory loads and no shuffles:
+// cut into 16-token tiles (the last one zero-padded).
 //
-//   FP16 tile (64*D bytes):     [K part 32*D B][V part 32*D B]
-//     K part, 16-B chunk s (one 16-wide k-step of d) for lane l at (s*32 + l)*16:
-//        u32 r = nb*2 + hi  (nb: token n-block 0/1, hi: d offset +8)  holds
-//        half2( K[t][d0], K[t][d0+1] ),  t = 8*nb + l/4,  d0 = 16*s + 8*hi + 2*(l%4)
-//     V part, chunk c for lane l at (c*32 + l)*16:
-//        u32 r = jj*2 + hi  (j = 2c + jj: 8-wide n-block of d)  holds
-//        half2( V[t0][d], V[t0+1][d] ),  d = 8*j + l/4,  t0 = 8*hi + 2*(l%4)
+//   FP16 slot: per kv head g, at base + g * ntiles * 64*D:
+//     K region (ntiles * 32*D bytes): 8x8 "core matrices" of 8 tokens x 8 d (16 B per token row),
+//        core (T, c) for token group T = t/8 and d chunk c = d/8 at (T * D/8 + c) * 128,
+//        element (t, d) at row t%8 (16 B apart), halfword d%8.
+//     V region (ntiles * 32*D bytes, right after K): per 16-token tile j, V transposed in core
+//        matrices of 8 d x 8 tokens, core (dg, tc) for d group dg = d/8 and token chunk
+//        tc = (t%16)/8 at j*32*D + (dg*2 + tc) * 128, element at row d%8, halfword t%8.
+//     These are the no-swizzle K-major operand layouts of the tcgen05 MMA (S = Q K^T reads a
+//     key block of any length with one descriptor, LBO = 128 B, SBO = 16*D B; O += P V reads
+//     one 16-key tile per MMA, LBO = 128 B, SBO = 256 B), and word `lane` of a core matrix is
+//     exactly the m16n8k16 B-fragment register of that lane, so the warp-MMA decode reads
+//     its fragments with conflict-free 32-bit loads.
 //
 //   MLX4G32 tile (20*D bytes):  [K codes 8*D B][K sb 2*D B][V codes 8*D B][V sb 2*D B]
 //     codes: lane l owns D/16 u32 words; word i at ((i/4)*32 + l)*16 + (i%4)*4.
@@ -47,6 +49,8 @@ constexpr int MAX_GROUPS = 64;     // work groups (kv head x q-head batch)
 constexpr int DECODE_WARPS = 4;    // warps per CTA (each an independent worker)
 
 __host__ __device__ constexpr int tile_bytes(int fmt, int D) { return fmt == FMT_FP16 ? 64 * D : 20 * D; }
+// fp16 slots: bytes of one kv head's K region (the V region follows it).
+__host__ __device__ inline size_t fp16_region_bytes(int ntiles, int D) { return (size_t)ntiles * 32 * D; }
 
 // ------------------------------------------------------------------ launch parameter blocks
 

@@ -163,12 +163,26 @@ __device__ __forceinline__ void mask_scores(float (&z)[4], int lane, int valid, 
 
 // ---------------------------------------------------------------- fp16 tile (fetch functors)
 
+// One 16-token tile of an fp16 slot in shared memory: kp -> its K part (2 token groups x D/8
+// d chunks of 128-B core matrices), vp -> its V part (D/8 d groups x 2 token chunks).
+// Word `lane` of a core matrix is that lane's m16n8k16 B-fragment register.
+template <int D>
 struct SmemFp16Tile {
     const uint8_t* kp;
     const uint8_t* vp;
     int lane;
-    __device__ __forceinline__ uint4 k(int s) const { return *reinterpret_cast<const uint4*>(kp + (s * 32 + lane) * 16); }
-    __device__ __forceinline__ uint4 v(int c) const { return *reinterpret_cast<const uint4*>(vp + (c * 32 + lane) * 16); }
+    __device__ __forceinline__ uint32_t kw(int nb, int c) const {
+        return *reinterpret_cast<const uint32_t*>(kp + ((nb * (D / 8) + c) * 32 + lane) * 4);
+    }
+    __device__ __forceinline__ uint32_t vw(int j, int tc) const {
+        return *reinterpret_cast<const uint32_t*>(vp + ((j * 2 + tc) * 32 + lane) * 4);
+    }
+    __device__ __forceinline__ uint4 k(int s) const {
+        return make_uint4(kw(0, 2 * s), kw(0, 2 * s + 1), kw(1, 2 * s), kw(1, 2 * s + 1));
+    }
+    __device__ __forceinline__ uint4 v(int c) const {
+        return make_uint4(vw(2 * c, 0), vw(2 * c, 1), vw(2 * c + 1, 0), vw(2 * c + 1, 1));
+    }
 };
 
 // Dense suffix K_suf/V_suf [S_suf, D] of one kv head, natural layout, read straight from global.
@@ -385,7 +399,8 @@ struct Chunk {
     int nreal;    // tiles to copy and compute (0: nothing, e.g. an empty sparse slot)
     int slot_blk; // sparse: index of the block in the group's selection list
     bool last;    // last chunk of this worker's piece of the item
-    const uint8_t* src;
+    const uint8_t* src;   // mlx4g32: the tiles; fp16: the K region part
+    const uint8_t* src2;  // fp16: the V region part
 };
 
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
@@ -399,7 +414,7 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
     c.item_end = c.item_start + vt;
 }
 
-template <int TPS, int TB>
+template <int FMT, int D, int TPS, int TB>
 __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Chunk& ch) {
     if (c.t >= c.t_end) return false;
     if (c.t >= c.item_end) {
@@ -432,7 +447,15 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
     ch.item = c.d * p.n_groups + c.grp;
     ch.d = c.d;
     ch.grp = c.grp;
-    ch.src = ds.kv + ((size_t)p.grp[c.grp].g * ds.ntiles + ch.tile) * TB;
+    if constexpr (FMT == FMT_FP16) {
+        const size_t reg = fp16_region_bytes(ds.ntiles, D);
+        const uint8_t* base = ds.kv + (size_t)p.grp[c.grp].g * 2 * reg;
+        ch.src = base + (size_t)ch.tile * 32 * D;
+        ch.src2 = base + reg + (size_t)ch.tile * 32 * D;
+    } else {
+        ch.src = ds.kv + ((size_t)p.grp[c.grp].g * ds.ntiles + ch.tile) * TB;
+        ch.src2 = nullptr;
+    }
     c.t += n;
     ch.last = (c.t == c.item_end) || (c.t == c.t_end);
     return true;
@@ -462,7 +485,13 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         if (lane == 0) {
             if (c.nreal > 0) {
                 mbar_arrive_expect_tx(bar_s + 8 * s, c.nreal * C::TB);
-                bulk_g2s(ring_s + s * C::STAGE, c.src, c.nreal * C::TB, bar_s + 8 * s);
+                if constexpr (FMT == FMT_FP16) {
+                    const uint32_t half = c.nreal * 32 * D;
+                    bulk_g2s(ring_s + s * C::STAGE, c.src, half, bar_s + 8 * s);
+                    bulk_g2s(ring_s + s * C::STAGE + C::STAGE / 2, c.src2, half, bar_s + 8 * s);
+                } else {
+                    bulk_g2s(ring_s + s * C::STAGE, c.src, c.nreal * C::TB, bar_s + 8 * s);
+                }
             } else {
                 mbar_arrive(bar_s + 8 * s);
             }
@@ -472,7 +501,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     int inflight = 0;
     for (int s = 0; s < C::NSTAGE; ++s) {
         Chunk c;
-        if (!cursor_next<C::TPS, C::TB>(p, prod, c)) break;
+        if (!cursor_next<FMT, D, C::TPS, C::TB>(p, prod, c)) break;
         issue(c, s);
         ++inflight;
     }
@@ -482,7 +511,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     int stage = 0;
     uint32_t phase = 0;
     Chunk c;
-    while (cursor_next<C::TPS, C::TB>(p, cons, c)) {
+    while (cursor_next<FMT, D, C::TPS, C::TB>(p, cons, c)) {
         const DecodeDesc& ds = p.desc[c.d];
         const WorkGroup& wg = p.grp[c.grp];
         if (c.item != cur_item) {
@@ -506,19 +535,18 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {
             const int valid = ds.N - (c.tile + k) * TILE_TOK;
-            const uint8_t* tile = sbuf + k * C::TB;
             if constexpr (FMT == FMT_FP16) {
-                SmemFp16Tile tl{tile, tile + 32 * D, lane};
+                SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
                 tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
             } else {
-                tile_i4<D>(st, qsm, tile, lane, valid, head_ok);
+                tile_i4<D>(st, qsm, sbuf + k * C::TB, lane, valid, head_ok);
             }
         }
         phase ^= 1u << stage;
         __syncwarp();
         if (lane == 0) fence_proxy_async_smem();   // our reads of this stage precede the next copy into it
         Chunk nc;
-        if (cursor_next<C::TPS, C::TB>(p, prod, nc)) {
+        if (cursor_next<FMT, D, C::TPS, C::TB>(p, prod, nc)) {
             issue(nc, stage);
             ++inflight;
         }

@@ -13,21 +13,17 @@
 namespace pck {
 
 // K_mean[g, b, d] = mean over the tokens of block b of K[g, t, d] (fp32 sum of fp16 values),
-// read from the resident fp16 tiles (fragment-ordered; see pck_common.cuh).
+// read from the K region of the resident fp16 slot (see pck_common.cuh).
 __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int D, int ntiles, int B,
                                    float* __restrict__ kmean) {
     const int b = blockIdx.x, g = blockIdx.y, nb = gridDim.x;
     const int t0 = b * B, t1 = min(N, t0 + B);
-    const size_t tb = (size_t)64 * D;
+    const uint8_t* kreg = tiles + (size_t)g * 2 * fp16_region_bytes(ntiles, D);
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const int s = d >> 4, hi = (d >> 3) & 1, q = (d >> 1) & 3, e = d & 1;
         float acc = 0.f;
         for (int t = t0; t < t1; ++t) {
-            const int j = t >> 4, tt = t & 15, nbk = tt >> 3, l4 = tt & 7;
-            const int lane = 4 * l4 + q, r = nbk * 2 + hi;
-            const uint8_t* tile = tiles + ((size_t)g * ntiles + j) * tb;
-            const __half v = *reinterpret_cast<const __half*>(tile + (s * 32 + lane) * 16 + r * 4 + e * 2);
-            acc += __half2float(v);
+            const size_t off = ((size_t)(t >> 3) * (D / 8) + (d >> 3)) * 128 + (t & 7) * 16 + (d & 7) * 2;
+            acc += __half2float(*reinterpret_cast<const __half*>(kreg + off));
         }
         kmean[((size_t)g * nb + b) * D + d] = acc / static_cast<float>(t1 - t0);
     }

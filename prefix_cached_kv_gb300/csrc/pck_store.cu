@@ -91,39 +91,41 @@ __global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __res
 
 // ------------------------------------------------------------------ fp16 re-layout
 
-// One thread per output u32 of a tile (tile = 16 * D u32: K part 8*D, V part 8*D).
+// One thread per output u32 of a kv head's regions (K region 8*D*ntiles u32, then V region).
 template <typename SrcT>
 __global__ void __launch_bounds__(256) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
                                                             int H_kv, int N, int D, int ntiles,
                                                             uint32_t* __restrict__ out) {
-    const int words_tile = 16 * D;
-    const int64_t total = (int64_t)H_kv * ntiles * words_tile;
+    const int64_t region = (int64_t)ntiles * 8 * D;           // u32 per region
+    const int64_t total = (int64_t)H_kv * 2 * region;
+    const int cpt = D / 8;                                    // d chunks (K) / d groups (V)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tileg = i / words_tile;          // g * ntiles + j
-        const int w = static_cast<int>(i - tileg * words_tile);
-        const int g = static_cast<int>(tileg / ntiles);
-        const int j = static_cast<int>(tileg - (int64_t)g * ntiles);
-        const bool isV = w >= 8 * D;
-        const int wl = isV ? w - 8 * D : w;            // word within part
-        const int chunk = wl / 128, lane = (wl / 4) & 31, r = wl & 3;
-        const int q = lane & 3, l4 = lane >> 2;
+        const int g = static_cast<int>(i / (2 * region));
+        const int64_t w = i - (int64_t)g * 2 * region;
+        const bool isV = w >= region;
+        const int64_t wl = isV ? w - region : w;
+        const int64_t ci = wl >> 5;                           // core matrix index
+        const int wi = static_cast<int>(wl & 31);             // word within the core (= lane)
+        const int r = wi >> 2, e = 2 * (wi & 3);
         int t0, t1, d0, d1;
         if (!isV) {
-            const int nb = r >> 1, hi = r & 1;
-            t0 = t1 = 8 * nb + l4;
-            d0 = 16 * chunk + 8 * hi + 2 * q;
+            const int64_t T = ci / cpt;
+            const int c = static_cast<int>(ci - T * cpt);
+            t0 = t1 = static_cast<int>(8 * T + r);
+            d0 = 8 * c + e;
             d1 = d0 + 1;
         } else {
-            const int jj = r >> 1, hi = r & 1;
-            d0 = d1 = 8 * (2 * chunk + jj) + l4;
-            t0 = 8 * hi + 2 * q;
+            const int64_t j = ci / (2 * cpt);
+            const int cc = static_cast<int>(ci - j * 2 * cpt);
+            const int dg = cc >> 1, tc = cc & 1;
+            d0 = d1 = 8 * dg + r;
+            t0 = static_cast<int>(16 * j + 8 * tc + e);
             t1 = t0 + 1;
         }
         const SrcT* src = isV ? V : K;
-        const int tok0 = j * TILE_TOK + t0, tok1 = j * TILE_TOK + t1;
-        float v0 = tok0 < N ? static_cast<float>(src[((int64_t)g * N + tok0) * D + d0]) : 0.f;
-        float v1 = tok1 < N ? static_cast<float>(src[((int64_t)g * N + tok1) * D + d1]) : 0.f;
+        float v0 = t0 < N ? static_cast<float>(src[((int64_t)g * N + t0) * D + d0]) : 0.f;
+        float v1 = t1 < N ? static_cast<float>(src[((int64_t)g * N + t1) * D + d1]) : 0.f;
         out[i] = h2_as_u32(__floats2half2_rn(v0, v1));
     }
 }
