@@ -168,6 +168,25 @@ int pck_query_batch(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, i
 int pck_quantize_mlx4g32(const void *X, int src_dtype, int64_t rows, int kv_dim,
                          void *out_records, void *stream);
 
+/* Attention of M=1 queries over mlx4g32 records the caller holds, allocating nothing.
+ * The pages have no counterpart: it exists for callers that cannot allocate device memory at
+ * call time (code running under another framework's allocator budget, a request path that must
+ * not touch the allocator, or a process without a pck context). It runs the same kernels as
+ * pck_store_records + pck_query_fused (M=1), with all scratch in device arrays compiled into
+ * libpck (PCK_NOALLOC_SCRATCH_BYTES per GPU, held from library load until process exit).
+ * K_rec, V_rec: device token-major records [N, rec] as in pck_store_records. Q: device [H_q, D];
+ * O: device fp32 [H_q, D]; LSE: device fp32 [H_q] or NULL; K_suf/V_suf: device fp16
+ * [H_kv, S_suf, D] or NULL when S_suf == 0. Limits: H_kv * ceil(N/16) * 20*D bytes of resident
+ * tiles <= 16 MiB, D in {64, 128, 256}; larger inputs return PCK_EUNSUPPORTED before any
+ * launch. The first call on a device looks up the scratch addresses: make it before any stream
+ * capture. All calls share the scratch: calls that overlap on the GPU (other streams or host
+ * threads) race and must be serialised by the caller. Returns PCK_OK, PCK_EINVAL,
+ * PCK_EUNSUPPORTED or PCK_ECUDA (no context, so no pck_last_error text). */
+#define PCK_NOALLOC_SCRATCH_BYTES ((16u << 20) + (8u << 20) + 4096u * 4u + 256u)
+int pck_attend_records_noalloc(int H_kv, int N, int D, const void *K_rec, const void *V_rec, int H_q,
+                               int q_dtype, const void *Q, const int32_t *head_map, int S_suf,
+                               const void *K_suf, const void *V_suf, float *O, float *LSE, void *stream);
+
 /* Counters of ctx. */
 int pck_info(pck_ctx *ctx, pck_info_t *out);
 

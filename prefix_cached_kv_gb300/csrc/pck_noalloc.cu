@@ -1,0 +1,167 @@
+// pck_noalloc.cu -- M=1 attention over caller-held mlx4g32 records that allocates nothing.
+//
+// Some callers cannot allocate device memory when they need an answer: code that runs inside
+// another framework's memory budget (its caching allocator owns the device heap), a serving
+// loop that is forbidden to touch the allocator on the request path, or a process that has
+// not created a pck context at all. For them, pck_attend_records_noalloc runs the same two
+// kernels as a store + fused query (records -> resident tiles, then the split-K decode with
+// the suffix merge), but every scratch byte it needs lives in the file-scope device arrays
+// below instead of memory from cudaMalloc. The caller passes only inputs and outputs.
+//
+// Cost of that choice: every GPU that loads libpck holds these arrays (PCK_NOALLOC_SCRATCH_BYTES
+// in total) until the process exits, and all calls share them, so calls that overlap on the
+// GPU (two streams, or two host threads) race and must be serialised by the caller.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "../../include/pck.h"
+#include "pck_common.cuh"
+#include "pck_kernels.h"
+
+namespace {
+
+using namespace pck;
+
+constexpr size_t NA_TILE_BYTES = size_t(16) << 20;      // resident tiles of one query's slot
+constexpr size_t NA_PARTIAL_BYTES = size_t(8) << 20;    // split-K partials
+constexpr int NA_COUNTERS = 4096;                       // per-item tickets
+constexpr int NA_MAX_DEVICES = 64;
+
+static __device__ __align__(256) uint8_t g_na_tiles[NA_TILE_BYTES];
+static __device__ __align__(256) float g_na_partials[NA_PARTIAL_BYTES / sizeof(float)];
+static __device__ __align__(256) int g_na_counters[NA_COUNTERS];
+static __device__ __align__(256) int g_na_err[64];
+
+struct NaPtrs {
+    bool ready = false;
+    uint8_t* tiles = nullptr;
+    float* partials = nullptr;
+    int* counters = nullptr;
+    int* err = nullptr;
+    int sms = 0;
+};
+NaPtrs g_na[NA_MAX_DEVICES];
+
+// Device addresses of the scratch arrays on the current device (host code must not pass the
+// symbols themselves: in host code they are host-side stand-ins).
+int na_setup(int dev) {
+    NaPtrs& p = g_na[dev];
+    if (p.ready) return PCK_OK;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.tiles), g_na_tiles) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.partials), g_na_partials) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.counters), g_na_counters) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.err), g_na_err) != cudaSuccess) {
+        cudaGetLastError();
+        return PCK_ECUDA;
+    }
+    if (cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || p.sms <= 0) {
+        cudaGetLastError();
+        return PCK_ECUDA;
+    }
+    p.ready = true;
+    return PCK_OK;
+}
+
+}  // namespace
+
+extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_rec, const void* V_rec, int H_q,
+                                          int q_dtype, const void* Q, const int32_t* head_map, int S_suf,
+                                          const void* K_suf, const void* V_suf, float* O, float* LSE,
+                                          void* stream) {
+    using namespace pck;
+    if (!K_rec || !V_rec || !Q || !O) return PCK_EINVAL;
+    if (H_kv < 1 || H_kv > PCK_MAX_HEADS || H_q < 1 || H_q > PCK_MAX_HEADS || N < 1 || S_suf < 0) return PCK_EINVAL;
+    if (D != 64 && D != 128 && D != 256) return PCK_EUNSUPPORTED;
+    if (q_dtype != PCK_DT_F32 && q_dtype != PCK_DT_F16) return PCK_EINVAL;
+    if (S_suf > 0 && (!K_suf || !V_suf)) return PCK_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(K_rec) | reinterpret_cast<uintptr_t>(V_rec)) & 3) return PCK_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES) return PCK_ECUDA;
+    int rc = na_setup(dev);
+    if (rc != PCK_OK) return rc;
+    const NaPtrs& sp = g_na[dev];
+
+    // q heads grouped by kv head, at most GMAX per group
+    int hm[PCK_MAX_HEADS];
+    for (int h = 0; h < H_q; ++h) {
+        if (head_map) {
+            hm[h] = head_map[h];
+        } else {
+            if (H_q % H_kv) return PCK_EINVAL;
+            hm[h] = h / (H_q / H_kv);
+        }
+        if (hm[h] < 0 || hm[h] >= H_kv) return PCK_EINVAL;
+    }
+    static thread_local DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    int n_groups = 0;
+    for (int g = 0; g < H_kv; ++g) {
+        WorkGroup cur{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
+        for (int h = 0; h < H_q; ++h) {
+            if (hm[h] != g) continue;
+            cur.qh[cur.nq++] = static_cast<int8_t>(h);
+            if (cur.nq == GMAX) {
+                p.grp[n_groups++] = cur;
+                cur = WorkGroup{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
+            }
+        }
+        if (cur.nq) p.grp[n_groups++] = cur;
+    }
+
+    // size limits of the static scratch
+    const int ntiles = (N + TILE_TOK - 1) / TILE_TOK;
+    const size_t tiles_bytes = static_cast<size_t>(H_kv) * ntiles * tile_bytes(FMT_I4, D);
+    if (tiles_bytes > NA_TILE_BYTES) return PCK_EUNSUPPORTED;
+    if (n_groups > NA_COUNTERS) return PCK_EUNSUPPORTED;
+    const int64_t total = static_cast<int64_t>(n_groups) * ntiles;
+    const DecodeLaunchInfo li = decode_launch_info(FMT_I4, D);
+    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
+    const size_t slot_bytes = static_cast<size_t>(GMAX) * (D + 2) * sizeof(float);
+    const int64_t max_slots = static_cast<int64_t>(NA_PARTIAL_BYTES / slot_bytes);
+    int64_t max_warps = static_cast<int64_t>(sp.sms) * li.ctas_per_sm * DECODE_WARPS;
+    const int64_t fixed = n_groups + static_cast<int64_t>(n_groups) * n_suf;   // item + suffix slots
+    if (fixed >= max_slots) return PCK_EUNSUPPORTED;
+    if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;
+    int64_t tpw = (total + max_warps - 1) / max_warps;
+    if (tpw < 2) tpw = 2;
+    const int64_t n_workers = (total + tpw - 1) / tpw;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // tickets must start at zero; the error word too
+    if (cudaMemsetAsync(sp.counters, 0, sizeof(int) * n_groups, st) != cudaSuccess) return PCK_ECUDA;
+    if (cudaMemsetAsync(sp.err, 0, sizeof(int), st) != cudaSuccess) return PCK_ECUDA;
+    if (launch_relayout_mlx4(K_rec, V_rec, 0, H_kv, N, D, ntiles, sp.tiles, st, sp.sms) != cudaSuccess)
+        return PCK_ECUDA;
+
+    p.n_desc = 1;
+    p.n_groups = n_groups;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.S_suf = S_suf;
+    p.q_f16 = q_dtype == PCK_DT_F16;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    DecodeDesc& d = p.desc[0];
+    d.kv = sp.tiles;
+    d.Q = Q;
+    d.O = O;
+    d.LSE = LSE;
+    d.Ksuf = static_cast<const __half*>(K_suf);
+    d.Vsuf = static_cast<const __half*>(V_suf);
+    d.N = N;
+    d.ntiles = ntiles;
+    d.vtiles = ntiles;
+    d.tile_off = 0;
+    p.total_tiles = static_cast<int>(total);
+    p.tpw = static_cast<int>(tpw);
+    p.n_workers = static_cast<int>(n_workers);
+    p.n_suf = n_suf;
+    p.partials = sp.partials;
+    p.counters = sp.counters;
+    p.err = sp.err;
+    const int64_t warps = n_workers + static_cast<int64_t>(n_groups) * n_suf;
+    const int n_ctas = static_cast<int>((warps + DECODE_WARPS - 1) / DECODE_WARPS);
+    if (launch_decode(FMT_I4, D, p, n_ctas, st) != cudaSuccess) return PCK_ECUDA;
+    return PCK_OK;
+}
