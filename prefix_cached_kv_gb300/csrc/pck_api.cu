@@ -33,6 +33,7 @@ constexpr size_t WS_PARTIAL_BYTES = size_t(64) << 20;  // split-K partials
 constexpr int WS_COUNTERS = 1 << 16;
 constexpr int WS_SEL_BYTES = 1 << 20;                   // sparse selection lists
 constexpr size_t WS_SCORES_BYTES = size_t(16) << 20;
+constexpr size_t WS_SUFFIX_BYTES = size_t(32) << 20;    // batched-Q suffix staged in the slot layout
 
 struct Slot {
     int fmt = 0, H_kv = 0, N = 0, D = 0, ntiles = 0;
@@ -58,6 +59,7 @@ struct pck_ctx {
     int* dev_err = nullptr;
     uint8_t* sel = nullptr;
     float* scores = nullptr;
+    uint8_t* suf_ws = nullptr;
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
     DecodeLaunchInfo dinfo[2][3];
@@ -299,7 +301,8 @@ int pck_create(pck_ctx** out, int device, int max_slots) {
     if (cudaMalloc(&c->partials, WS_PARTIAL_BYTES) != cudaSuccess ||
         cudaMalloc(&c->counters, WS_COUNTERS * sizeof(int)) != cudaSuccess ||
         cudaMalloc(&c->dev_err, sizeof(int)) != cudaSuccess || cudaMalloc(&c->sel, WS_SEL_BYTES) != cudaSuccess ||
-        cudaMalloc(&c->scores, WS_SCORES_BYTES) != cudaSuccess) {
+        cudaMalloc(&c->scores, WS_SCORES_BYTES) != cudaSuccess ||
+        cudaMalloc(&c->suf_ws, WS_SUFFIX_BYTES) != cudaSuccess) {
         cudaGetLastError();
         pck_destroy(c);
         return PCK_ENOMEM;
@@ -325,6 +328,7 @@ void pck_destroy(pck_ctx* c) {
     cudaFree(c->dev_err);
     cudaFree(c->sel);
     cudaFree(c->scores);
+    cudaFree(c->suf_ws);
     delete c;
 }
 
@@ -506,12 +510,19 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     }
     if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs an fp16 slot");
     if (q_dtype != PCK_DT_F16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs fp16 Q");
+    if (reinterpret_cast<uintptr_t>(Q) & 15) return fail(c, PCK_EINVAL, "Q must be 16-byte aligned");
     if (!prefill_supported(D)) return fail(c, PCK_EUNSUPPORTED, "M>1 kernel not available for D=%d", D);
+    if (S_suf > 0 && static_cast<size_t>(s->H_kv) * 2 * fp16_region_bytes((S_suf + TILE_TOK - 1) / TILE_TOK, D) >
+                         WS_SUFFIX_BYTES)
+        return fail(c, PCK_EUNSUPPORTED, "suffix of %d tokens exceeds the staging workspace", S_suf);
+    const int suf_ntiles = (S_suf + TILE_TOK - 1) / TILE_TOK;
+    if (S_suf > 0) {   // stage the suffix in the resident layout (the MMA operand layout)
+        cudaError_t e = launch_relayout_fp16(K_suf, V_suf, 1, s->H_kv, S_suf, D, suf_ntiles, c->suf_ws, st, c->sms);
+        if (e != cudaSuccess) return cuda_fail(c, e, "suffix staging launch");
+    }
     PrefillParams pp{};
     pp.Q = static_cast<const __half*>(Q);
     pp.kv = s->tiles;
-    pp.Ksuf = static_cast<const __half*>(K_suf);
-    pp.Vsuf = static_cast<const __half*>(V_suf);
     pp.O = O;
     pp.LSE = LSE;
     pp.H_q = H_q;
@@ -522,12 +533,8 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     pp.S_suf = S_suf;
     pp.causal = causal;
     pp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    pp.partials = c->partials;
-    pp.counters = c->counters;
     pp.err = c->dev_err;
-    for (int h = 0; h < H_q; ++h)
-        pp.head_map[h] = head_map ? static_cast<int8_t>(head_map[h]) : static_cast<int8_t>(h / (H_q / s->H_kv));
-    cudaError_t e = launch_prefill(pp, st, c->sms, D);
+    cudaError_t e = launch_prefill(pp, grp, n_groups, S_suf > 0 ? c->suf_ws : nullptr, suf_ntiles, st, D);
     if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
     ++c->queries;
     return check_async(c);

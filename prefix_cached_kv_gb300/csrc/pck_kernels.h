@@ -48,19 +48,16 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
 // batched-Q tensor-core prefill (tcgen05)
 struct PrefillParams {
     const __half* Q;          // [H_q, M, D]
-    const uint8_t* kv;        // resident fp16 tiles of the slot
-    const __half* Ksuf;       // [H_kv, S_suf, D] or nullptr
-    const __half* Vsuf;
+    const uint8_t* kv;        // resident fp16 slot
     float* O;                 // [H_q, M, D]
     float* LSE;               // [H_q, M] or nullptr
-    int8_t head_map[PCK_MAXH];
     int H_q, H_kv, M, N, ntiles, S_suf, causal;
     float scale_log2;
-    float* partials;          // split-N workspace
-    int* counters;
     int* err;
 };
-cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st, int sms, int D);
+// suf_tiles: the suffix [H_kv, S_suf, D] re-laid out like a resident fp16 slot of suf_ntiles tiles
+cudaError_t launch_prefill(const PrefillParams& p, const WorkGroup* grp, int n_groups, const void* suf_tiles,
+                           int suf_ntiles, cudaStream_t st, int D);
 bool prefill_supported(int D);
 
 }  // namespace pck

@@ -1,14 +1,440 @@
-// pck_prefill.cu -- batched-Q (M > 1) prefix attention on the tensor cores (tcgen05).
+// pck_prefill.cu -- batched-Q (M > 1) prefix attention on the 5th-generation tensor cores.
+//
+// "Shared KV Cache Serving -- Pion as LLM Memory", section "Wire-protocol details": the
+// batched-Q form of ATTEND.PREFIX.QUERY takes Q (H, M, D) and returns O plus one LSE per row;
+// "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms" / QUERY_FUSED: the prefix attention is
+// merged with a dense suffix (here causal, bottom-right aligned: row i sees suffix keys
+// j <= S_suf - M + i) in the same dispatch.
+//
+// One CTA owns 128 query rows of one kv head (the rows of its GQA q heads are packed:
+// row = local head * M + i) and walks all of that kv head's keys, prefix then suffix, in blocks
+// of up to 128 keys:
+//   * warp 5 (one lane) streams each key block's K and V with two cp.async.bulk copies into a
+//     2-stage shared-memory ring (the resident fp16 layout already is the operand layout);
+//   * warp 4 (one lane) issues tcgen05.mma (kind::f16, M=128, fp32 accumulators in TMEM):
+//     S = Q K^T (N = keys of the block, K-steps over d), then O += P V (one 16-key step per
+//     resident tile, N = D); completion goes to mbarriers through tcgen05.commit;
+//   * warps 0-3 (thread = row = TMEM lane) read S with tcgen05.ld, apply the causal / length
+//     mask, keep the running max m (base 2, tau*log2(e)-prescaled) and sum l, write
+//     P = 2^(s - m) as fp16 to shared memory in the A-operand layout, and finally read O,
+//     divide by l and write O and LSE = (m + log2 l) ln 2.
+// The running max is only moved when a block's max exceeds it by more than 8; O (in TMEM) is
+// then rescaled in place by the softmax warps, while no MMA touches it (the S-block commit
+// implies the previous P V has completed). Every wait is bounded: a stuck pipeline sets the
+// device error word and the CTA still releases its tensor memory.
+#include <math.h>
+
 #include "pck_common.cuh"
 #include "pck_kernels.h"
 
 namespace pck {
 
-bool prefill_supported(int D) { (void)D; return false; }
+namespace {
 
-cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t st, int sms, int D) {
-    (void)p; (void)st; (void)sms; (void)D;
-    return cudaErrorNotSupported;
+constexpr int PF_ROWS = 128;          // query rows per CTA (MMA M)
+constexpr int PF_BLOCK = 128;         // keys per block (MMA N of S = Q K^T)
+constexpr int PF_THREADS = 192;       // 4 softmax warps + MMA warp + producer warp
+constexpr float PF_THRESH = 8.0f;     // lazy-rescale threshold (log2 units)
+constexpr float PF_LN2 = 0.69314718055994530942f;
+
+template <int D>
+struct PCfg {
+    static constexpr int Q_BYTES = PF_ROWS * D * 2;
+    static constexpr int KV_BYTES = PF_BLOCK * D * 2;        // K (or V) of one block
+    static constexpr int P_BYTES = PF_ROWS * PF_BLOCK * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K0 = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V0 = OFF_K0 + KV_BYTES;
+    static constexpr int OFF_K1 = OFF_V0 + KV_BYTES;
+    static constexpr int OFF_V1 = OFF_K1 + KV_BYTES;
+    static constexpr int OFF_P = OFF_V1 + KV_BYTES;
+    static constexpr int OFF_BAR = OFF_P + P_BYTES;           // 8 mbarriers + tmem slot
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;         // + alignment slack
+    static constexpr int S_COL = 0;                           // TMEM columns of S
+    static constexpr int O_COL = PF_BLOCK;                    // TMEM columns of O
+    static constexpr int TMEM_COLS = 256;
+};
+
+// ---------------------------------------------------------------- tcgen05 wrappers
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    // shared-memory matrix descriptor, no swizzle, K-major core matrices of 8 rows x 16 B
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;            // descriptor version for this architecture
+    return d;                                        // base offset 0, layout type 0 (no swizzle)
+}
+
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+    // kind::f16: D f32, A/B f16, both K-major, no negation / sparsity
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+        ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- work description
+
+struct PfTask {
+    int grp;        // work group (kv head + its q heads)
+    int row0;       // first packed row of the CTA
+};
+
+struct PfParams {
+    PrefillParams a;
+    WorkGroup grp[MAX_GROUPS];
+    int n_groups;
+    int n_tasks;
+    int task_off[MAX_GROUPS + 1];   // prefix sums of row tiles per group
+    const uint8_t* suf_tiles;       // suffix in the resident fp16 layout (or nullptr)
+    int suf_ntiles;
+};
+
+// Key block b of the task's key sequence: prefix blocks first, then suffix blocks.
+struct KeyBlock {
+    const uint8_t* k;
+    const uint8_t* v;
+    int ntile;       // resident 16-key tiles in the block
+    int key0;        // first key index (within prefix or suffix)
+    int is_suf;
+};
+
+__device__ __forceinline__ KeyBlock key_block(const PfParams& P, int g, int b, int nbp, int D) {
+    KeyBlock kb;
+    const int tiles_per_block = PF_BLOCK / TILE_TOK;
+    if (b < nbp) {
+        const size_t reg = fp16_region_bytes(P.a.ntiles, D);
+        const uint8_t* base = P.a.kv + (size_t)g * 2 * reg;
+        const int t0 = b * tiles_per_block;
+        kb.ntile = min(tiles_per_block, P.a.ntiles - t0);
+        kb.k = base + (size_t)t0 * 32 * D;
+        kb.v = base + reg + (size_t)t0 * 32 * D;
+        kb.key0 = t0 * TILE_TOK;
+        kb.is_suf = 0;
+    } else {
+        const int bs = b - nbp;
+        const size_t reg = fp16_region_bytes(P.suf_ntiles, D);
+        const uint8_t* base = P.suf_tiles + (size_t)g * 2 * reg;
+        const int t0 = bs * tiles_per_block;
+        kb.ntile = min(tiles_per_block, P.suf_ntiles - t0);
+        kb.k = base + (size_t)t0 * 32 * D;
+        kb.v = base + reg + (size_t)t0 * 32 * D;
+        kb.key0 = t0 * TILE_TOK;
+        kb.is_suf = 1;
+    }
+    return kb;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_constant__ PfParams P) {
+    using C = PCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar = s_base + C::OFF_BAR;   // [0,1] full, [2,3] empty, [4] s_full, [5] p_full, [6] o_done, [7] final
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 64);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- which rows
+    const int task = blockIdx.x;
+    int grp = 0;
+    while (grp + 1 < P.n_groups && P.task_off[grp + 1] <= task) ++grp;
+    const WorkGroup& wg = P.grp[grp];
+    const int g = wg.g;
+    const int M = P.a.M;
+    const int rows_total = wg.nq * M;
+    const int row0 = (task - P.task_off[grp]) * PF_ROWS;
+    const int N = P.a.N, S = P.a.S_suf;
+    const int nbp = (N + PF_BLOCK - 1) / PF_BLOCK;
+    // suffix blocks needed by the last row of the tile (causal) or all of them
+    int nbs = 0;
+    if (S > 0) {
+        int kmax = S;   // keys [0, kmax) of the suffix may be visible to some row of the tile
+        if (P.a.causal) {
+            const int last = min(rows_total, row0 + PF_ROWS) - 1;
+            // rows are (local head, i): the largest i in the tile is M-1 if the tile crosses
+            // the end of a head's rows, else that of its last row
+            const int imax = (row0 / M != last / M) ? M - 1 : last % M;
+            kmax = max(0, min(S, S - M + imax + 1));
+        }
+        nbs = (kmax + PF_BLOCK - 1) / PF_BLOCK;
+    }
+    const int nblocks = nbp + nbs;
+
+    // ---- setup: barriers, TMEM, Q tile
+    if (tid == 0) {
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 8, 1);
+        mbar_init(bar + 16, 1);
+        mbar_init(bar + 24, 1);
+        mbar_init(bar + 32, 1);
+        mbar_init(bar + 40, 128);
+        mbar_init(bar + 48, 1);
+        mbar_init(bar + 56, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(C::TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid < PF_ROWS) {   // Q row -> core-matrix layout (zeros for rows past the end)
+        const int r = row0 + tid;
+        uint8_t* qs = smem + C::OFF_Q;
+        const int R = tid >> 3, rr = tid & 7;
+        if (r < rows_total) {
+            const int h = wg.qh[r / M], i = r % M;
+            const uint4* src = reinterpret_cast<const uint4*>(P.a.Q + ((size_t)h * M + i) * D);
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c)
+                *reinterpret_cast<uint4*>(qs + (R * (D / 8) + c) * 128 + rr * 16) = __ldg(src + c);
+        } else {
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c)
+                *reinterpret_cast<uint4*>(qs + (R * (D / 8) + c) * 128 + rr * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int b = 0; b < nblocks && !failed; ++b) {
+                const int st = b & 1;
+                if (b >= 2 && !mbar_wait_bounded(bar + 16 + 8 * st, ((b >> 1) - 1) & 1)) { failed = true; break; }
+                const KeyBlock kb = key_block(P, g, b, nbp, D);
+                const uint32_t bytes = kb.ntile * 32 * D;
+                mbar_arrive_expect_tx(bar + 8 * st, 2 * bytes);
+                bulk_g2s(s_base + (st ? C::OFF_K1 : C::OFF_K0), kb.k, bytes, bar + 8 * st);
+                bulk_g2s(s_base + (st ? C::OFF_V1 : C::OFF_V0), kb.v, bytes, bar + 8 * st);
+            }
+            if (failed) set_err(P.a.err, 2);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t s_tm = tmem + C::S_COL, o_tm = tmem + C::O_COL;
+            int prev_ntile = 0;
+            for (int b = 0; b <= nblocks && !failed; ++b) {
+                if (b < nblocks) {
+                    const int st = b & 1;
+                    if (!mbar_wait_bounded(bar + 8 * st, (b >> 1) & 1)) { failed = true; break; }
+                }
+                if (b > 0) {   // O += P(b-1) V(b-1) once the softmax has written P(b-1)
+                    if (!mbar_wait_bounded(bar + 40, (b - 1) & 1)) { failed = true; break; }
+                    tc_fence_after();
+                    const int pst = (b - 1) & 1;
+                    const uint32_t v_s = s_base + (pst ? C::OFF_V1 : C::OFF_V0);
+                    const uint32_t idesc = idesc_f16(PF_ROWS, D);
+                    for (int u = 0; u < prev_ntile; ++u) {
+                        const uint64_t a = sdesc(s_base + C::OFF_P + u * 256, 128, 16 * 128);
+                        const uint64_t bd = sdesc(v_s + u * 32 * D, 128, 256);
+                        umma_f16(o_tm, a, bd, idesc, (b - 1 > 0 || u > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar + 16 + 8 * pst);   // K/V stage free once these complete
+                    if (b == nblocks) umma_commit(bar + 48);   // O final
+                }
+                if (b < nblocks) {   // S = Q K(b)^T
+                    const int st = b & 1;
+                    const KeyBlock kb = key_block(P, g, b, nbp, D);
+                    const uint32_t k_s = s_base + (st ? C::OFF_K1 : C::OFF_K0);
+                    const uint32_t idesc = idesc_f16(PF_ROWS, kb.ntile * TILE_TOK);
+                    for (int s = 0; s < D / 16; ++s) {
+                        const uint64_t a = sdesc(s_base + C::OFF_Q + s * 256, 128, 16 * D);
+                        const uint64_t bd = sdesc(k_s + s * 256, 128, 16 * D);
+                        umma_f16(s_tm, a, bd, idesc, s > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar + 32);
+                    prev_ntile = kb.ntile;
+                }
+            }
+            if (failed) set_err(P.a.err, 3);
+            // drain: make sure no MMA is still writing TMEM when the CTA releases it
+            umma_commit(bar + 56);
+            mbar_wait_bounded(bar + 56, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps (row = tid)
+        const int r = row0 + tid;
+        const bool row_ok = r < rows_total;
+        const int i = row_ok ? r % M : 0;
+        const int suf_lim = P.a.causal ? (S - M + i) : (S - 1);   // last visible suffix key
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t s_tm = tmem + C::S_COL + lane_base, o_tm = tmem + C::O_COL + lane_base;
+        const float sc = P.a.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        uint8_t* ps = smem + C::OFF_P;
+        const int R = tid >> 3, rr = tid & 7;
+        for (int b = 0; b < nblocks; ++b) {
+            // warp-uniform outcome: the tcgen05.ld below must be executed by the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + 32, b & 1))) { failed = true; break; }
+            tc_fence_after();
+            const KeyBlock kb = key_block(P, g, b, nbp, D);
+            const int lim = kb.is_suf ? min(kb.key0 + kb.ntile * TILE_TOK, suf_lim + 1) : min(kb.key0 + kb.ntile * TILE_TOK, N);
+            const int nvalid = row_ok ? max(0, lim - kb.key0) : 0;   // keys [key0, key0 + nvalid) visible
+            const int ncols = kb.ntile * TILE_TOK;
+            float bmax = -INFINITY;
+            for (int c0 = 0; c0 < ncols; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(s_tm + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < nvalid) bmax = fmaxf(bmax, __uint_as_float(v[j]));
+            }
+            const float mb = bmax * sc;
+            const bool need = mb > m + PF_THRESH;
+            if (__any_sync(0xffffffffu, need)) {
+                const float mnew = need ? mb : m;
+                const float alpha = need ? exp2f(m - mnew) : 1.0f;
+                if (b > 0) {
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(o_tm + c0, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                        tmem_st32(o_tm + c0, v);
+                    }
+                }
+                l *= alpha;
+                m = mnew;
+            }
+            for (int c0 = 0; c0 < PF_BLOCK; c0 += 32) {
+                uint32_t pk[16];
+                if (c0 < ncols) {
+                    uint32_t v[32];
+                    tmem_ld32(s_tm + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float p0 = (c0 + j < nvalid) ? exp2f(__uint_as_float(v[j]) * sc - m) : 0.f;
+                        const float p1 = (c0 + j + 1 < nvalid) ? exp2f(__uint_as_float(v[j + 1]) * sc - m) : 0.f;
+                        const __half2 h = __floats2half2_rn(p0, p1);
+                        const float2 hf = __half22float2(h);
+                        l += hf.x + hf.y;   // normaliser of the probabilities actually used
+                        pk[j >> 1] = h2_as_u32(h);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {   // 8 keys (16 B) per core-matrix row
+                    const int kc = (c0 >> 3) + q;
+                    *reinterpret_cast<uint4*>(ps + (R * 16 + kc) * 128 + rr * 16) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar + 40);
+        }
+        if (failed) {
+            set_err(P.a.err, 4);
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + 48, 0))) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            float* orow = row_ok ? P.a.O + ((size_t)wg.qh[r / M] * M + i) * D : nullptr;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(o_tm + c0, v);
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(orow + c0 + j) =
+                            make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
+                                        __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+                }
+            }
+            if (row_ok && P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
+        } else {
+            set_err(P.a.err, 5);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+bool prefill_supported(int D) { return D == 64 || D == 128; }
+
+template <int D>
+static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
+    using C = PCfg<D>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    prefill_kernel<D><<<P.n_tasks, PF_THREADS, C::SMEM, st>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_groups, const void* suf_tiles,
+                           int suf_ntiles, cudaStream_t st, int D) {
+    static thread_local PfParams P;
+    P.a = a;
+    P.n_groups = n_groups;
+    int off = 0;
+    for (int i = 0; i < n_groups; ++i) {
+        P.grp[i] = grp[i];
+        P.task_off[i] = off;
+        off += (grp[i].nq * a.M + PF_ROWS - 1) / PF_ROWS;
+    }
+    P.task_off[n_groups] = off;
+    P.n_tasks = off;
+    P.suf_tiles = static_cast<const uint8_t*>(suf_tiles);
+    P.suf_ntiles = suf_ntiles;
+    if (off == 0) return cudaSuccess;
+    if (D == 64) return launch_prefill_t<64>(P, st);
+    if (D == 128) return launch_prefill_t<128>(P, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pck
