@@ -213,8 +213,8 @@ def run_main(args, ctx, torch, pk):
     achieved = ALG_BYTES_STEP / (ms_step * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm"], 4), "traffic": traffic_from_profiles("decode_mlx4g32_gqa"),
-            "kernel": "decode_kernel<mlx4g32, D=64>", "algorithmic_bytes_per_launch": ALG_BYTES_STEP,
-            "duration": "per-launch time of back-to-back graph-replayed launches (one launch per step)",
+            "kernel": "decode_kernel<mlx4g32, D=64> + merge_kernel", "algorithmic_bytes_per_launch": ALG_BYTES_STEP,
+            "duration": "per-step time of back-to-back graph-replayed steps (decode + merge, PDL-chained)",
             "peak_source": f"{pk['src']} hbm_gbs"}
     e2e = run_e2e(args, ctx, torch, sets)
     return ms_step, steps, clocks, roof, e2e
@@ -541,7 +541,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--rows", default="all", choices=["all", "main"])
+    ap.add_argument("--rows", default="all",
+                    help="all | comma list of main,fp16,sparse,prefill,cartridge (main = the headline line)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -554,17 +555,26 @@ def main():
     from prefix_cached_kv_gb300 import binding
     pk = peaks()
     ctx = binding.Context(torch.cuda.current_device())
-    ms_step, steps, clocks, roof, e2e = run_main(args, ctx, torch, pk)
-    for r in range(ROTATE):
-        ctx.drop(f"bench{r}")
+    want = {"main", "fp16", "sparse", "prefill", "cartridge"} if args.rows == "all" else set(args.rows.split(","))
+    ms_step = steps = clocks = roof = e2e = None
+    if "main" in want:
+        ms_step, steps, clocks, roof, e2e = run_main(args, ctx, torch, pk)
+        for r in range(ROTATE):
+            ctx.drop(f"bench{r}")
     rows = {}
-    if args.rows == "all":
+    if "fp16" in want:
         rows["A0_A2_fp16_m1"] = row_fp16_m1(ctx, torch, pk)
+    if "sparse" in want:
         rows["A6_A7_sparse"] = row_sparse(ctx, torch, pk)
+    if "prefill" in want:
         rows["A4_A5_batched_q"] = row_prefill(ctx, torch, pk)
+    if "cartridge" in want:
         rows["A1_A3_cartridge"] = row_cartridge(ctx, torch, pk)
     ctx.close()
     if rank() != 0:
+        return
+    if ms_step is None:   # rows only (profiling runs): no headline line
+        print(json.dumps({"rows": rows}), flush=True)
         return
     ws = world()
     value = ws * KV_BYTES_STEP / (ms_step * 1e-3) / 1e9
@@ -576,7 +586,7 @@ def main():
                        "l2": f"rotate {ROTATE} distinct 84 MB prefix sets (336 MB > L2)",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": steps, "rows": rows}
+            "gpu_launches": 2 * steps, "rows": rows}
     print(json.dumps(line), flush=True)
 
 

@@ -62,8 +62,8 @@ struct pck_ctx {
     uint8_t* suf_ws = nullptr;
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
-    DecodeLaunchInfo dinfo[2][3];
-    bool dinfo_ok[2][3] = {{false, false, false}, {false, false, false}};
+    DecodeLaunchInfo dinfo[2][6];
+    bool dinfo_ok[2][6] = {};
 };
 
 namespace {
@@ -94,10 +94,10 @@ std::string key_of(const char* sid, int layer) {
 bool d_ok(int D) { return D == 64 || D == 128 || D == 256; }
 int d_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
 
-const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D) {
-    const int i = d_index(D);
+const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D, int ncb) {
+    const int i = d_index(D) + 3 * (ncb - 1);
     if (!c->dinfo_ok[fmt][i]) {
-        c->dinfo[fmt][i] = decode_launch_info(fmt, D);
+        c->dinfo[fmt][i] = decode_launch_info(fmt, D, ncb);
         c->dinfo_ok[fmt][i] = true;
     }
     return c->dinfo[fmt][i];
@@ -256,7 +256,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
         total += static_cast<int64_t>(n_groups) * d.vtiles;
     }
     if (total >= (int64_t(1) << 30)) return fail(c, PCK_EUNSUPPORTED, "too many tiles in one launch");
-    const DecodeLaunchInfo& li = dinfo(c, fmt, D);
+    const DecodeLaunchInfo& li = dinfo(c, fmt, D, fmt == PCK_FMT_MLX4G32 ? decode_ncb(p) : 1);
     const int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS;
     int64_t tpw = (total + max_warps - 1) / max_warps;
     if (tpw < 2) tpw = 2;
@@ -264,7 +264,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     const int n_items = n * n_groups;
     const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
     const int64_t slots = n_workers + n_items + static_cast<int64_t>(n_items) * n_suf;
-    const size_t need = static_cast<size_t>(slots) * GMAX * (D + 2) * sizeof(float);
+    const size_t need = static_cast<size_t>(slots) * GMAX * partial_stride(D) * sizeof(float);
     if (need > WS_PARTIAL_BYTES) return fail(c, PCK_EUNSUPPORTED, "split-K workspace too small (%zu B needed)", need);
     if (n_items > WS_COUNTERS) return fail(c, PCK_EUNSUPPORTED, "too many work items");
     p.total_tiles = static_cast<int>(total);
@@ -485,6 +485,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
                         int causal, int fa_window, float* O, float* LSE, void* stream) {
     if (!c) return PCK_EINVAL;
     if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
+    if (reinterpret_cast<uintptr_t>(O) & 15) return fail(c, PCK_EINVAL, "O must be 16-byte aligned");
     if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
     if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
     if (M < 1) return fail(c, PCK_EINVAL, "M=%d", M);
@@ -567,6 +568,7 @@ static int sparse_common(pck_ctx* c, const char* sid, int layer, int H_q, int D,
                          void* stream) {
     if (!c) return PCK_EINVAL;
     if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
+    if (reinterpret_cast<uintptr_t>(O) & 15) return fail(c, PCK_EINVAL, "O must be 16-byte aligned");
     if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
     if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
     if (K_top < 1) return fail(c, PCK_EINVAL, "K_top=%d", K_top);
@@ -653,6 +655,8 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
         if (fmt >= 0 && s->fmt != fmt) return fail(c, PCK_EINVAL, "descriptor %d: mixed slot formats", i);
         fmt = s->fmt;
         if (!descs[i].Q || !descs[i].O) return fail(c, PCK_EINVAL, "descriptor %d: NULL Q or O", i);
+        if (reinterpret_cast<uintptr_t>(descs[i].O) & 15)
+            return fail(c, PCK_EINVAL, "descriptor %d: O must be 16-byte aligned", i);
         if (S_suf > 0 && (!descs[i].K_suf || !descs[i].V_suf))
             return fail(c, PCK_EINVAL, "descriptor %d: NULL suffix", i);
         ds[i] = DescIn{s, descs[i].Q, descs[i].O, descs[i].LSE, descs[i].K_suf, descs[i].V_suf};

@@ -18,17 +18,17 @@
 //     its fragments with conflict-free 32-bit loads.
 //
 //   MLX4G32 tile (20*D bytes):  [K codes 8*D B][K sb 2*D B][V codes 8*D B][V sb 2*D B]
-//     codes: lane l owns D/16 u32 words; word i at ((i/4)*32 + l)*16 + (i%4)*4.
-//       K word i: nb = i / (D/32), group gq = i % (D/32) (k-steps s0 = 2gq, s1 = 2gq+1),
-//         t = 8*nb + l/4, q = l%4; nibble n (bits 4n..4n+3):
-//           n0 = c[t][16s0+2q]  n4 = c[t][16s0+2q+1]  n1 = c[t][16s0+8+2q]  n5 = c[t][16s0+9+2q]
-//           n2 = c[t][16s1+2q]  n6 = c[t][16s1+2q+1]  n3 = c[t][16s1+8+2q]  n7 = c[t][16s1+9+2q]
-//       V word i: n-blocks j0 = 2i, j1 = 2i+1, d0 = 8*j0 + l/4, d1 = 8*j1 + l/4:
+//     codes: lane l owns D/16 u32 words; word i at ((i/4)*32 + l)*16 + (i%4)*4; t = l/4, q = l%4.
+//       K word s (k-step s, d = 16s..16s+15) is the lane's m16n8k16 A fragment with the 16
+//       tokens of the tile as rows; nibble n (bits 4n..4n+3):
+//           n0 = c[t][16s+2q]    n4 = c[t][16s+2q+1]    n1 = c[t+8][16s+2q]    n5 = c[t+8][16s+2q+1]
+//           n2 = c[t][16s+8+2q]  n6 = c[t][16s+9+2q]    n3 = c[t+8][16s+8+2q]  n7 = c[t+8][16s+9+2q]
+//       V word i: the B fragments of d n-blocks j0 = 2i, j1 = 2i+1 (d0 = 8*j0 + t, d1 = 8*j1 + t):
 //           n0 = c[2q][d0]  n4 = c[2q+1][d0]  n1 = c[8+2q][d0]  n5 = c[9+2q][d0]
 //           n2 = c[2q][d1]  n6 = c[2q+1][d1]  n3 = c[8+2q][d1]  n7 = c[9+2q][d1]
-//       so (w & 0x000F000F), (w & 0x00F000F0), ((w>>8) & 0x000F000F), ((w>>8) & 0x00F000F0),
-//       each OR 0x64006400, are four half2 registers (1024 + c) or (1024 + 16c).
-//     sb: [q 0..3][slot 0..3][group 0..D/32) half2(scale, bias), slot -> token {2q, 2q+1, 8+2q, 9+2q}.
+//       so (w & 0x000F000F), (w & 0x00F000F0), ((w>>8) & 0x000F000F), ((w>>8) & 0x00F000F0) are
+//       four half2 registers holding the codes as exact fp16 subnormals c * 2^-24 or 16c * 2^-24.
+//     sb: [token 0..15][group 0..D/32) half2(scale, bias).
 //
 // The codes, scales and biases are the bytes of the mlx4g32 records ("Shared KV Cache Serving --
 // Pion as LLM Memory", section "Quantized tier -- mlx4g32"), only permuted.
@@ -49,6 +49,9 @@ constexpr int MAX_GROUPS = 64;     // work groups (kv head x q-head batch)
 constexpr int DECODE_WARPS = 4;    // warps per CTA (each an independent worker)
 
 __host__ __device__ constexpr int tile_bytes(int fmt, int D) { return fmt == FMT_FP16 ? 64 * D : 20 * D; }
+// Split-K partial of one q head: [m, l, pad, pad, o[0..D)] -- o starts 16-byte aligned.
+__host__ __device__ constexpr int partial_stride(int D) { return D + 4; }
+constexpr int PARTIAL_O = 4;   // float offset of o inside a head's partial
 // fp16 slots: bytes of one kv head's K region (the V region follows it).
 __host__ __device__ inline size_t fp16_region_bytes(int ntiles, int D) { return (size_t)ntiles * 32 * D; }
 
@@ -87,7 +90,7 @@ struct DecodeParams {
     int tiles_per_block;    // sparse: B / 16
     int sel_max;            // sparse: entries per group in sel_blocks
     float scale_log2;       // tau * log2(e)
-    float* partials;        // workspace: [slots][GMAX][D + 2]
+    float* partials;        // workspace: [slots][GMAX][partial_stride(D)]
     int* counters;          // workspace: [n_items]
     int* err;               // device error word (bounded waits that gave up)
 };
@@ -164,20 +167,40 @@ __device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t& hi, ui
     lo = h2_as_u32(l);
 }
 
-// Four 4-bit codes pairs of one word -> half2 registers holding exact (c, c) or (16c, 16c).
+// The eight 4-bit codes of one word -> four half2 registers holding the codes as exact fp16
+// subnormals: (w & 0x000F000F) is half2(c0 * 2^-24, c4 * 2^-24), (w & 0x00F000F0) is
+// half2(16 c1 * 2^-24, 16 c5 * 2^-24), and the same on w >> 8 for c2, c6 / c3, c7. The tensor
+// cores multiply subnormal fp16 inputs exactly; the 2^24 (or 2^20) goes into a later fp32 scale.
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
-    const uint32_t magic = 0x64006400u;   // fp16 1024.0 in both halves
-    uint32_t w8 = w >> 8;
-    uint32_t r0, r1, r2, r3;
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r0) : "r"(w), "r"(0x000F000Fu), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r1) : "r"(w), "r"(0x00F000F0u), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r2) : "r"(w8), "r"(0x000F000Fu), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r3) : "r"(w8), "r"(0x00F000F0u), "r"(magic));
-    const __half2 k1024 = u32_as_h2(magic);
-    p0 = h2_as_u32(__hsub2(u32_as_h2(r0), k1024));
-    p1 = h2_as_u32(__hsub2(u32_as_h2(r1), k1024));
-    p2 = h2_as_u32(__hsub2(u32_as_h2(r2), k1024));
-    p3 = h2_as_u32(__hsub2(u32_as_h2(r3), k1024));
+    const uint32_t w8 = w >> 8;
+    p0 = w & 0x000F000Fu;
+    p1 = w & 0x00F000F0u;
+    p2 = w8 & 0x000F000Fu;
+    p3 = w8 & 0x00F000F0u;
+}
+
+// Transpose an 8x8 matrix of 16-bit values held in the m8n8 fragment layout (lane l: row l/4,
+// columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// x -> half2(fp16(x), fp16(x - fp16(x))): the hi and lo fp16 parts of x in one register.
+__device__ __forceinline__ uint32_t pack_hilo(float x) {
+    const __half h = __float2half_rn(x);
+    const __half l = __float2half_rn(x - __half2float(h));
+    return static_cast<uint32_t>(__half_as_ushort(h)) | (static_cast<uint32_t>(__half_as_ushort(l)) << 16);
+}
+
+// 2^x with the hardware approximation (MUFU.EX2: ~2 ulp, flushes subnormal results to 0);
+// used on base-2 scores that are <= 0 after the max subtraction, where its error is far below
+// the 2e-3 / 1e-3 output tolerances.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void set_err(int* err, int code) {

@@ -11,12 +11,17 @@
 // blocks). All items' tiles are concatenated and cut into equal contiguous ranges, one per warp
 // ("worker"), so the whole GPU streams the same number of bytes per warp whatever the shapes.
 // A worker keeps a private ring of shared-memory stages filled by 1-D TMA bulk copies
-// (cp.async.bulk, mbarrier completion) and computes, per tile, S = q K^T and O += P V with the
-// warp MMA m16n8k16 (fp16 operands, fp32 accumulation): the NT q heads of the item are the MMA
-// rows (hi part in rows 0-7, lo part in rows 8-15 -- q and P are split in two fp16 halves to
-// keep fp32 accuracy), tokens / head dims the columns. mlx4g32 codes enter the MMA as exact
-// fp16 integers; the per-group affine terms are applied to the fp32 scores
-// (z = s * sum_d q_d c_d + b * sum_d q_d) and, for V, through P' = p * s and sum_t p_t b_t.
+// (cp.async.bulk, mbarrier completion) and computes each tile with the warp MMA m16n8k16
+// (fp16 operands, fp32 accumulation); q and P are split into fp16 hi + lo halves so that the
+// products keep fp32 accuracy.
+//   fp16 slots: S = q K^T with the q heads as MMA rows (hi in rows 0-7, lo in rows 8-15).
+//   mlx4g32 slots: S^T = K q^T with the 16 tokens of the tile as MMA rows and the q heads as
+//     columns (head h, hi / lo in columns 2h, 2h+1), so that every row and column carries data
+//     and every lane owns (2 tokens, 1 head) in the softmax. The codes enter the MMA as exact
+//     fp16 subnormals (c * 2^-24, one AND per register); the per-group affine terms are applied
+//     to the fp32 scores, z = 2^24 s * S + b * sum_d q_d, and for V through P' = p * s and
+//     sum_t p_t b_t. P' moves from the score layout into the A operand of O += P' V with one
+//     movmatrix.trans per 8 tokens.
 // Each worker writes an (m, l, o) partial per item piece; the last piece to finish (atomic
 // ticket, no waiting) merges all pieces of the item plus the dense suffix pieces:
 //   m = max m_k, l = sum l_k 2^(m_k - m), O = sum o_k 2^(m_k - m) / l, LSE = (m + log2 l) ln 2.
@@ -24,6 +29,8 @@
 // tile's max exceeds it by more than 8 (so stored weights stay <= 256), which keeps the
 // rescale of the accumulators off the common path and does not change the result.
 #include <math.h>
+
+#include <type_traits>
 
 #include "pck_common.cuh"
 #include "pck_kernels.h"
@@ -36,9 +43,9 @@ struct DCfg {
     static constexpr int NG = D / 32;       // mlx4g32 groups per head
     static constexpr int NBV = D / 8;       // PV n-blocks over d
     static constexpr int TB = tile_bytes(FMT, D);
-    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 2 : 1));
+    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 2 : 1);
     static constexpr int STAGE = TPS * TB;
-    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : 4;
+    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : (D == 256 ? 2 : 4);
     static constexpr bool QSMEM = D > 128;  // q fragments live in shared memory (register budget)
     static constexpr int QSMEM_BYTES = QSMEM ? KS * 32 * 16 : 0;
     static constexpr int RING = NSTAGE * STAGE;
@@ -148,7 +155,7 @@ __device__ __forceinline__ void softmax_update(WState<FMT, D>& st, float (&z)[4]
         st.m_ref = mnew;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) pr[k] = (z[k] == -INFINITY) ? 0.f : exp2f(z[k] - st.m_ref);
+    for (int k = 0; k < 4; ++k) pr[k] = (z[k] == -INFINITY) ? 0.f : ex2_approx(z[k] - st.m_ref);
     st.l_part += (pr[0] + pr[1]) + (pr[2] + pr[3]);
 }
 
@@ -239,64 +246,254 @@ __device__ __forceinline__ void tile_fp16(WState<FMT, D>& st, const uint32_t* qs
     }
 }
 
-// ---------------------------------------------------------------- mlx4g32 tile (shared memory)
+// ---------------------------------------------------------------- mlx4g32 path (S^T orientation)
 
-template <int D>
-__device__ __forceinline__ void tile_i4(WState<FMT_I4, D>& st, const uint32_t* qsm, const uint8_t* tile, int lane,
-                                        int valid, bool head_ok) {
-    using C = DCfg<FMT_I4, D>;
-    constexpr int NG = C::NG;
-    const int q = lane & 3;
-    const uint8_t* kc = tile;
-    const uint32_t* ksb = reinterpret_cast<const uint32_t*>(tile + 8 * D) + q * 4 * NG;
-    const uint8_t* vc = tile + 10 * D;
-    const uint32_t* vsb = reinterpret_cast<const uint32_t*>(tile + 18 * D) + q * 4 * NG;
-    uint32_t kw[D / 16];
+// Lane l: tokens t = l/4 and t + 8 of each tile, head q = l%4 of each column block cb (heads
+// cb*4 .. cb*4+3 of the item); B fragments of q: column n = l/4 = (head hl = n/2, part = n%2).
+template <int D, int NCB>
+struct I4State {
+    static constexpr int KS = D / 16, NG = D / 32, NBV = D / 8;
+    uint32_t qb[NCB][KS][2];   // B fragments of the item's q (tau*log2e prescaled), hi or lo part
+    float qs[NCB][NG];         // sum over the group's d of the lane's head q (prescaled)
+    float oacc[NBV][4];        // O rows l/4 (block 0) in [0..1], rows 8 + l/4 (block 1) in [2..3]
+    float bacc[NCB][NG];       // sum_t p_t * bias_t of the lane's head, per group
+    float m_ref[NCB];
+    float l_part[NCB];
+};
+
+template <int D, int NCB>
+__device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeParams& p, const DecodeDesc& ds,
+                                              const WorkGroup& wg, int lane) {
+    using S = I4State<D, NCB>;
+    const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(kc + (c * 32 + lane) * 16);
-        kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
+    for (int cb = 0; cb < NCB; ++cb) {
+        const int h = cb * 4 + hl;
+        const int qh = h < wg.nq ? wg.qh[h] : -1;
+        float gsum[S::NG];
+#pragma unroll
+        for (int g = 0; g < S::NG; ++g) gsum[g] = 0.f;
+#pragma unroll
+        for (int s = 0; s < S::KS; ++s) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int d0 = 16 * s + 8 * r + 2 * q;
+                float x0 = 0.f, x1 = 0.f;
+                if (qh >= 0) {
+                    x0 = ld_q(ds.Q, p.q_f16, qh * D + d0) * p.scale_log2;
+                    x1 = ld_q(ds.Q, p.q_f16, qh * D + d0 + 1) * p.scale_log2;
+                }
+                gsum[s >> 1] += x0 + x1;
+                uint32_t hi, lo;
+                split_hi_lo(x0, x1, hi, lo);
+                st.qb[cb][s][r] = part ? lo : hi;
+            }
+        }
+        // gsum: this lane's 8 of the group's 32 d of head hl; the 4 lanes q = 0..3 of a column
+        // hold all 32, and lane 8*h' (column 2h') holds head h' -> the lane's S^T head q.
+#pragma unroll
+        for (int g = 0; g < S::NG; ++g) {
+            float v = gsum[g];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            st.qs[cb][g] = __shfl_sync(0xffffffffu, v, 8 * q);
+            st.bacc[cb][g] = 0.f;
+        }
+        st.m_ref[cb] = -INFINITY;
+        st.l_part[cb] = 0.f;
     }
-    float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+    for (int j = 0; j < S::NBV; ++j) st.oacc[j][0] = st.oacc[j][1] = st.oacc[j][2] = st.oacc[j][3] = 0.f;
+    __syncwarp();
+}
+
+// NT (1 or 2) consecutive 16-token tiles of a kv head: scores of all NT*16 tokens, one online
+// softmax step, then O += P' V for each tile.
+template <int D, int NCB, int NT>
+__device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile0, int lane, int valid0,
+                                        uint32_t head_mask, int nq) {
+    using S = I4State<D, NCB>;
+    constexpr int NG = S::NG, KS = S::KS, TB = 20 * D;
+    const int q = lane & 3, t0 = lane >> 2;
+    uint32_t kw[NT][KS], vw[NT][KS];
+    uint32_t ks0[NT][NG], ks1[NT][NG], vs0[NT][NG], vs1[NT][NG];   // (scale, bias) of tokens t0, t0+8
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            uint32_t b00, b01, b10, b11;
-            unpack_word(kw[nb * NG + g], b00, b01, b10, b11);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t a[4];
-            get_qa<D>(st.qa, qsm, 2 * g, lane, a);
-            mma16816(acc, a, b00, b01);
-            get_qa<D>(st.qa, qsm, 2 * g + 1, lane, a);
-            mma16816(acc, a, b10, b11);
-            const float2 sb0 = __half22float2(u32_as_h2(ksb[(2 * nb) * NG + g]));
-            const float2 sb1 = __half22float2(u32_as_h2(ksb[(2 * nb + 1) * NG + g]));
-            z[2 * nb] = fmaf(sb0.x, acc[0] + acc[2], fmaf(sb0.y, st.qsum[g], z[2 * nb]));
-            z[2 * nb + 1] = fmaf(sb1.x, acc[1] + acc[3], fmaf(sb1.y, st.qsum[g], z[2 * nb + 1]));
+    for (int x = 0; x < NT; ++x) {
+        const uint8_t* tile = tile0 + x * TB;
+        const uint32_t* ksb = reinterpret_cast<const uint32_t*>(tile + 8 * D);
+        const uint32_t* vsb = reinterpret_cast<const uint32_t*>(tile + 18 * D);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {   // 16-byte loads: consecutive lanes, consecutive 16 B
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + (c * 32 + lane) * 16);
+            kw[x][4 * c] = v.x; kw[x][4 * c + 1] = v.y; kw[x][4 * c + 2] = v.z; kw[x][4 * c + 3] = v.w;
+            const uint4 u = *reinterpret_cast<const uint4*>(tile + 10 * D + (c * 32 + lane) * 16);
+            vw[x][4 * c] = u.x; vw[x][4 * c + 1] = u.y; vw[x][4 * c + 2] = u.z; vw[x][4 * c + 3] = u.w;
+        }
+#pragma unroll
+        for (int g = 0; g < NG; g += 2) {
+            const uint2 a = *reinterpret_cast<const uint2*>(ksb + t0 * NG + g);
+            const uint2 b = *reinterpret_cast<const uint2*>(ksb + (t0 + 8) * NG + g);
+            const uint2 c = *reinterpret_cast<const uint2*>(vsb + t0 * NG + g);
+            const uint2 d = *reinterpret_cast<const uint2*>(vsb + (t0 + 8) * NG + g);
+            ks0[x][g] = a.x; ks0[x][g + 1] = a.y; ks1[x][g] = b.x; ks1[x][g + 1] = b.y;
+            vs0[x][g] = c.x; vs0[x][g + 1] = c.y; vs1[x][g] = d.x; vs1[x][g + 1] = d.y;
         }
     }
-    mask_scores(z, lane, valid, head_ok);
-    float pr[4];
-    softmax_update<FMT_I4, D>(st, z, pr);
+    // ---- scores: z[x][cb][0] token 16x + t0, z[x][cb][1] token 16x + t0 + 8 (head q of block cb)
+    float z[NT][NCB][2];
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
-        const float2 s0 = __half22float2(u32_as_h2(vsb[0 * NG + g]));
-        const float2 s1 = __half22float2(u32_as_h2(vsb[1 * NG + g]));
-        const float2 s2 = __half22float2(u32_as_h2(vsb[2 * NG + g]));
-        const float2 s3 = __half22float2(u32_as_h2(vsb[3 * NG + g]));
-        st.bacc[g] = fmaf(pr[0], s0.y, fmaf(pr[1], s1.y, fmaf(pr[2], s2.y, fmaf(pr[3], s3.y, st.bacc[g]))));
-        uint32_t a[4];
-        split_hi_lo(pr[0] * s0.x, pr[1] * s1.x, a[0], a[1]);
-        split_hi_lo(pr[2] * s2.x * 0.0625f, pr[3] * s3.x * 0.0625f, a[2], a[3]);
+    for (int x = 0; x < NT; ++x) {
+        float zs0[NCB], zs1[NCB], zb0[NCB], zb1[NCB];
 #pragma unroll
-        for (int ww = 0; ww < 2; ++ww) {
-            const int i = 2 * g + ww;          // V word: n-blocks 2i, 2i+1
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(vc + ((i >> 2) * 32 + lane) * 16 + (i & 3) * 4);
-            uint32_t p0, p1, p2, p3;
-            unpack_word(w, p0, p1, p2, p3);
-            mma16816(st.oacc[2 * i], a, p0, p1);
-            mma16816(st.oacc[2 * i + 1], a, p2, p3);
+        for (int cb = 0; cb < NCB; ++cb) zs0[cb] = zs1[cb] = zb0[cb] = zb1[cb] = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            float acc[NCB][4];
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
+#pragma unroll
+            for (int ss = 0; ss < 2; ++ss) {
+                const int s = 2 * g + ss;
+                uint32_t a[4];
+                unpack_word(kw[x][s], a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
+            }
+            const float2 sb0 = __half22float2(u32_as_h2(ks0[x][g]));
+            const float2 sb1 = __half22float2(u32_as_h2(ks1[x][g]));
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+                zs0[cb] = fmaf(sb0.x, acc[cb][0] + acc[cb][1], zs0[cb]);
+                zs1[cb] = fmaf(sb1.x, acc[cb][2] + acc[cb][3], zs1[cb]);
+                zb0[cb] = fmaf(sb0.y, st.qs[cb][g], zb0[cb]);
+                zb1[cb] = fmaf(sb1.y, st.qs[cb][g], zb1[cb]);
+            }
+        }
+        const int va = valid0 - 16 * x;
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+            const int h = cb * 4 + q;
+            const bool hok = h < nq && ((head_mask >> h) & 1u);
+            float z0 = fmaf(zs0[cb], 16777216.0f, zb0[cb]);     // 2^24: codes entered as c * 2^-24
+            float z1 = fmaf(zs1[cb], 1048576.0f, zb1[cb]);      // 2^20: rows t0+8 hold 16 c * 2^-24
+            z[x][cb][0] = (hok && t0 < va) ? z0 : -INFINITY;
+            z[x][cb][1] = (hok && t0 + 8 < va) ? z1 : -INFINITY;
+        }
+    }
+    // ---- online softmax step over the NT*16 tokens (lanes with the same q share a head)
+    bool need_any = false;
+    float mt[NCB];
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        float m = fmaxf(z[0][cb][0], z[0][cb][1]);
+#pragma unroll
+        for (int x = 1; x < NT; ++x) m = fmaxf(m, fmaxf(z[x][cb][0], z[x][cb][1]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        mt[cb] = m;
+        need_any |= m > st.m_ref[cb] + RESCALE_THRESHOLD;
+    }
+    if (__any_sync(0xffffffffu, need_any)) {
+        float alpha_row[NCB];
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+            const bool need = mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;
+            const float mnew = need ? mt[cb] : st.m_ref[cb];
+            const float alpha = need ? exp2f(st.m_ref[cb] - mnew) : 1.0f;   // head q's factor
+            st.l_part[cb] *= alpha;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) st.bacc[cb][g] *= alpha;
+            st.m_ref[cb] = mnew;
+            alpha_row[cb] = __shfl_sync(0xffffffffu, alpha, lane >> 3);    // factor of O row head l/8
+        }
+#pragma unroll
+        for (int j = 0; j < S::NBV; ++j) {
+            st.oacc[j][0] *= alpha_row[0];
+            st.oacc[j][1] *= alpha_row[0];
+            if constexpr (NCB == 2) {
+                st.oacc[j][2] *= alpha_row[1];
+                st.oacc[j][3] *= alpha_row[1];
+            }
+        }
+    }
+    float pr[NT][NCB][2];
+#pragma unroll
+    for (int x = 0; x < NT; ++x)
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+#pragma unroll
+            for (int y = 0; y < 2; ++y)
+                pr[x][cb][y] = z[x][cb][y] == -INFINITY ? 0.f : ex2_approx(z[x][cb][y] - st.m_ref[cb]);
+            st.l_part[cb] += pr[x][cb][0] + pr[x][cb][1];
+        }
+    // ---- O += P' V per tile and group of 32 d (P' = p * scale of the token's group)
+#pragma unroll
+    for (int x = 0; x < NT; ++x) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const float2 sv0 = __half22float2(u32_as_h2(vs0[x][g]));
+            const float2 sv1 = __half22float2(u32_as_h2(vs1[x][g]));
+            uint32_t a[4];
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+                st.bacc[cb][g] = fmaf(pr[x][cb][0], sv0.y, fmaf(pr[x][cb][1], sv1.y, st.bacc[cb][g]));
+                a[cb] = movmatrix_trans(pack_hilo(pr[x][cb][0] * sv0.x));
+                a[2 + cb] = movmatrix_trans(pack_hilo(pr[x][cb][1] * sv1.x * 0.0625f));   // V regs of t+8 hold 16 c
+            }
+            if constexpr (NCB == 1) { a[1] = 0u; a[3] = 0u; }
+#pragma unroll
+            for (int ww = 0; ww < 2; ++ww) {
+                const int i = 2 * g + ww;          // V word: n-blocks 2i, 2i+1
+                uint32_t b0, b1, b2, b3;
+                unpack_word(vw[x][i], b0, b1, b2, b3);
+                mma16816(st.oacc[2 * i], a, b0, b1);
+                mma16816(st.oacc[2 * i + 1], a, b2, b3);
+            }
+        }
+    }
+}
+
+// Partial of the item piece: for every head h of the item, [m, l, o[0..D)] with o already in
+// real units (2^24 and the V biases applied).
+template <int D, int NCB>
+__device__ __forceinline__ void write_partial_i4(I4State<D, NCB>& st, float* P, int nq, int lane) {
+    using S = I4State<D, NCB>;
+    const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        float l = st.l_part[cb];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        float bsum[S::NG];
+#pragma unroll
+        for (int g = 0; g < S::NG; ++g) {
+            float v = st.bacc[cb][g];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            bsum[g] = __shfl_sync(0xffffffffu, v, hl);   // bias sums of head hl (held by lane hl)
+        }
+        const int hq = cb * 4 + q;
+        if (lane < 4 && hq < nq) {
+            float* ph = P + hq * partial_stride(D);
+            ph[0] = st.m_ref[cb];
+            ph[1] = l;
+        }
+        const int h = cb * 4 + hl;
+#pragma unroll
+        for (int j = 0; j < S::NBV; ++j) {
+            const float c0 = cb == 0 ? st.oacc[j][0] : st.oacc[j][2];
+            const float c1 = cb == 0 ? st.oacc[j][1] : st.oacc[j][3];
+            const float o0 = c0 + __shfl_xor_sync(0xffffffffu, c0, 4);   // hi row + lo row
+            const float o1 = c1 + __shfl_xor_sync(0xffffffffu, c1, 4);
+            if (part == 0 && h < nq) {
+                const int dd = 8 * j + 2 * q;
+                const float b = bsum[j / 4];
+                P[h * partial_stride(D) + PARTIAL_O + dd] = fmaf(o0, 16777216.0f, b);
+                P[h * partial_stride(D) + PARTIAL_O + 1 + dd] = fmaf(o1, 16777216.0f, b);
+            }
         }
     }
 }
@@ -310,8 +507,10 @@ __device__ __forceinline__ int item_pieces(const DecodeParams& p, int item) {
     return (e - 1) / p.tpw - s / p.tpw + 1;
 }
 
+// Merge of one (item, q head): lanes over pieces for the max and the normaliser, then lanes
+// over d with the pieces' weights broadcast by shuffles. Partials are read through L2 (__ldcg).
 template <int D>
-__device__ void combine_item(const DecodeParams& p, int item, int lane) {
+__device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane) {
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
     const DecodeDesc& ds = p.desc[d];
     const WorkGroup& wg = p.grp[grp];
@@ -320,71 +519,124 @@ __device__ void combine_item(const DecodeParams& p, int item, int lane) {
     const int n_items = p.n_desc * p.n_groups;
     const int npref = w1 - w0 + 1;
     const int npieces = npref + p.n_suf;
-    constexpr int PSTR = GMAX * (D + 2);
-    for (int h = 0; h < wg.nq; ++h) {
-        float M = -INFINITY;
-        for (int k = 0; k < npieces; ++k) {
-            const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
-            M = fmaxf(M, __ldcg(p.partials + (size_t)slot * PSTR + h * (D + 2)));
-        }
-        float L = 0.f;
-        float o[D / 32];
+    constexpr int PSTR = GMAX * partial_stride(D);
+    auto piece = [&](int k) -> const float* {
+        const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
+        return p.partials + (size_t)slot * PSTR + h * partial_stride(D);
+    };
+    float M = -INFINITY;
+    for (int k = lane; k < npieces; k += 32) M = fmaxf(M, __ldcg(piece(k)));
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) o[i] = 0.f;
-        for (int k = 0; k < npieces; ++k) {
-            const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
-            const float* ph = p.partials + (size_t)slot * PSTR + h * (D + 2);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // weights and normaliser: lanes over pieces
+    float L = 0.f;
+    // o: a warp step covers PPS pieces, each read by D/4 lanes as float4 (lane -> piece
+    // k0 + lane / (D/4), d = 4 * (lane % (D/4))); D = 256 uses two float4 per lane.
+    constexpr int LPP = D / 4 > 32 ? 32 : D / 4;      // lanes per piece
+    constexpr int PPS = 32 / LPP;                     // pieces per warp step
+    constexpr int V4 = D / 4 / LPP;                   // float4 per lane per piece
+    const int sub = lane / LPP, dl = lane % LPP;
+    float4 acc[V4];
+#pragma unroll
+    for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < npieces; c += 32) {
+        float wk = 0.f;
+        if (c + lane < npieces) {
+            const float* ph = piece(c + lane);
             const float mk = __ldcg(ph);
-            const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+            wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
             L = fmaf(wk, __ldcg(ph + 1), L);
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) o[i] = fmaf(wk, __ldcg(ph + 2 + lane + 32 * i), o[i]);
         }
-        const int qh = wg.qh[h];
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        const int nk = min(32, npieces - c);
+        constexpr int BATCH = 16 / PPS > 0 ? 16 / PPS : 1;   // warp steps whose loads are in flight together
+        for (int j0 = 0; j0 < nk; j0 += BATCH * PPS) {
+            float4 xs[BATCH][V4];
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) ds.O[(size_t)qh * D + lane + 32 * i] = o[i] * inv;
-        if (lane == 0 && ds.LSE) ds.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+            for (int b = 0; b < BATCH; ++b) {
+                const int jj = j0 + b * PPS + sub;
+                if (jj < nk) {
+                    const float4* ph = reinterpret_cast<const float4*>(piece(c + jj) + PARTIAL_O) + dl;
+#pragma unroll
+                    for (int v = 0; v < V4; ++v) xs[b][v] = __ldcg(ph + v * LPP);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V4; ++v) xs[b][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const float w = __shfl_sync(0xffffffffu, wk, (j0 + b * PPS + sub) & 31);
+#pragma unroll
+                for (int v = 0; v < V4; ++v) {
+                    acc[v].x = fmaf(w, xs[b][v].x, acc[v].x);
+                    acc[v].y = fmaf(w, xs[b][v].y, acc[v].y);
+                    acc[v].z = fmaf(w, xs[b][v].z, acc[v].z);
+                    acc[v].w = fmaf(w, xs[b][v].w, acc[v].w);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
+#pragma unroll
+    for (int x = LPP; x < 32; x <<= 1) {   // sum the pieces' partial sums across lane groups
+#pragma unroll
+        for (int v = 0; v < V4; ++v) {
+            acc[v].x += __shfl_xor_sync(0xffffffffu, acc[v].x, x);
+            acc[v].y += __shfl_xor_sync(0xffffffffu, acc[v].y, x);
+            acc[v].z += __shfl_xor_sync(0xffffffffu, acc[v].z, x);
+            acc[v].w += __shfl_xor_sync(0xffffffffu, acc[v].w, x);
+        }
+    }
+    const int qh = wg.qh[h];
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    if (sub == 0) {
+#pragma unroll
+        for (int v = 0; v < V4; ++v)
+            reinterpret_cast<float4*>(ds.O + (size_t)qh * D)[dl + v * LPP] =
+                make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+    }
+    if (lane == 0 && ds.LSE) ds.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+}
+
+// Second kernel of a decode: one warp per (item, q head). Launched with programmatic dependent
+// launch; it waits for the decode grid (partials complete and visible) before reading.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ DecodeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int n_pairs = p.n_desc * p.n_groups * GMAX;
+    for (int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < n_pairs; wi += (gridDim.x * blockDim.x) >> 5) {
+        const int item = wi / GMAX, h = wi - item * GMAX;
+        if (h >= p.grp[item % p.n_groups].nq) continue;
+        merge_item_head<D>(p, item, h, lane);
     }
 }
 
-template <int FMT, int D>
-__device__ void finish_piece(WState<FMT, D>& st, const DecodeParams& p, int item, int slot, int lane) {
-    using C = DCfg<FMT, D>;
+template <int D>
+__device__ void finish_piece(WState<FMT_FP16, D>& st, const DecodeParams& p, int item, int slot, int lane) {
+    using C = DCfg<FMT_FP16, D>;
     const int q = lane & 3, h = lane >> 2;
     const int grp = item % p.n_groups;
     float l = st.l_part;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    float bs[C::NG];
-#pragma unroll
-    for (int g = 0; g < C::NG; ++g) {
-        float v = st.bacc[g];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        bs[g] = FMT == FMT_I4 ? v : 0.f;
-    }
-    float* ph = p.partials + (size_t)slot * GMAX * (D + 2) + h * (D + 2);
+    float* ph = p.partials + (size_t)slot * GMAX * partial_stride(D) + h * partial_stride(D);
     if (h < p.grp[grp].nq) {
         if (q == 0) { ph[0] = st.m_ref; ph[1] = l; }
 #pragma unroll
         for (int j = 0; j < C::NBV; ++j) {
             const int dd = 8 * j + 2 * q;
-            const float b = bs[j / 4];
-            ph[2 + dd] = st.oacc[j][0] + st.oacc[j][2] + b;
-            ph[3 + dd] = st.oacc[j][1] + st.oacc[j][3] + b;
+            ph[PARTIAL_O + dd] = st.oacc[j][0] + st.oacc[j][2];
+            ph[PARTIAL_O + 1 + dd] = st.oacc[j][1] + st.oacc[j][3];
         }
     }
-    __threadfence();
-    __syncwarp();
-    int prev = 0;
-    if (lane == 0) prev = atomicAdd(p.counters + item, 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev == item_pieces(p, item) + p.n_suf - 1) {
-        __threadfence();
-        combine_item<D>(p, item, lane);
-        if (lane == 0) p.counters[item] = 0;   // ready for the next launch
-    }
+}
+
+template <int D, int NCB>
+__device__ void finish_piece_i4(I4State<D, NCB>& st, const DecodeParams& p, int item, int slot, int lane) {
+    const int grp = item % p.n_groups;
+    write_partial_i4<D, NCB>(st, p.partials + (size_t)slot * GMAX * partial_stride(D), p.grp[grp].nq, lane);
 }
 
 // ---------------------------------------------------------------- tile cursor over a worker range
@@ -463,9 +715,10 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
 
 // ---------------------------------------------------------------- workers
 
-template <int FMT, int D>
+template <int FMT, int D, int NCB>
 __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars, uint32_t* qsm) {
     using C = DCfg<FMT, D>;
+    using StateT = std::conditional_t<FMT == FMT_FP16, WState<FMT_FP16, D>, I4State<D, NCB>>;
     Cursor cons;
     cons.t = w * p.tpw;
     cons.t_end = min(p.total_tiles, cons.t + p.tpw);
@@ -506,7 +759,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         ++inflight;
     }
 
-    WState<FMT, D> st;
+    StateT st;
     int cur_item = -1;
     int stage = 0;
     uint32_t phase = 0;
@@ -516,7 +769,8 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         const WorkGroup& wg = p.grp[c.grp];
         if (c.item != cur_item) {
             cur_item = c.item;
-            start_item<FMT, D>(st, qsm, p, ds, wg, lane);
+            if constexpr (FMT == FMT_FP16) start_item<FMT_FP16, D>(st, qsm, p, ds, wg, lane);
+            else start_item_i4<D, NCB>(st, p, ds, wg, lane);
         }
         if (!mbar_wait_bounded(bar_s + 8 * stage, (phase >> stage) & 1u)) {
             set_err(p.err, 1);
@@ -527,11 +781,9 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
             return;
         }
         --inflight;
-        bool head_ok = (lane >> 2) < wg.nq;
-        if (p.sparse && c.nreal > 0) {
-            const uint8_t m = ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
-            head_ok = head_ok && ((m >> (lane >> 2)) & 1u);
-        }
+        uint32_t head_mask = 0xFFu;   // bit h: local q head h attends to this chunk's tokens
+        if (p.sparse && c.nreal > 0) head_mask = ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
+        const bool head_ok = (lane >> 2) < wg.nq && ((head_mask >> (lane >> 2)) & 1u);
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {
             const int valid = ds.N - (c.tile + k) * TILE_TOK;
@@ -539,7 +791,12 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
                 SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
                 tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
             } else {
-                tile_i4<D>(st, qsm, sbuf + k * C::TB, lane, valid, head_ok);
+                if (k + 1 < c.nreal) {   // two tiles per softmax step
+                    tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                    ++k;
+                } else {
+                    tile_i4<D, NCB, 1>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                }
             }
         }
         phase ^= 1u << stage;
@@ -552,7 +809,8 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         }
         stage = stage + 1 == C::NSTAGE ? 0 : stage + 1;
         if (c.last) {
-            finish_piece<FMT, D>(st, p, cur_item, w + cur_item, lane);
+            if constexpr (FMT == FMT_FP16) finish_piece<D>(st, p, cur_item, w + cur_item, lane);
+            else finish_piece_i4<D, NCB>(st, p, cur_item, w + cur_item, lane);
             cur_item = -1;
         }
     }
@@ -572,10 +830,10 @@ __device__ void suffix_worker(const DecodeParams& p, int sidx, int lane, uint32_
     const int t0 = 16 * k;
     GlobalSuffixTile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
     tile_fp16<FMT_FP16, D>(st, qsm, tl, lane, p.S_suf - t0, (lane >> 2) < wg.nq);
-    finish_piece<FMT_FP16, D>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
+    finish_piece<D>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
 }
 
-template <int FMT, int D>
+template <int FMT, int D, int NCB>
 __global__ void __launch_bounds__(DECODE_WARPS * 32) decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<FMT, D>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -585,7 +843,7 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32) decode_kernel(const __grid_
     uint32_t* qsm = reinterpret_cast<uint32_t*>(smem + DECODE_WARPS * C::RING + warp * C::QSMEM_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * (C::RING + C::QSMEM_BYTES)) + warp * C::NSTAGE;
     if (gw < p.n_workers) {
-        prefix_worker<FMT, D>(p, gw, lane, ring, bars, qsm);
+        prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars, qsm);
     } else if (p.n_suf > 0) {
         suffix_worker<FMT, D>(p, gw - p.n_workers, lane, qsm);
     }
@@ -593,51 +851,85 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32) decode_kernel(const __grid_
 
 // ---------------------------------------------------------------- host side
 
-template <int FMT, int D>
+template <int FMT, int D, int NCB>
 static cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) {
     using C = DCfg<FMT, D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FMT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<FMT, D, NCB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    decode_kernel<FMT, D><<<n_ctas, DECODE_WARPS * 32, C::SMEM, st>>>(p);
-    return cudaGetLastError();
+    decode_kernel<FMT, D, NCB><<<n_ctas, DECODE_WARPS * 32, C::SMEM, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the merge of the partials, overlapping its launch with the decode's tail
+    const int pairs = p.n_desc * p.n_groups * GMAX;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((pairs + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p);
 }
 
-template <int FMT, int D>
+template <int FMT, int D, int NCB>
 static DecodeLaunchInfo info_t() {
     using C = DCfg<FMT, D>;
     DecodeLaunchInfo i{C::STAGE, C::NSTAGE, C::SMEM, 0};
     int n = 0;
-    cudaFuncSetAttribute(decode_kernel<FMT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FMT, D>, DECODE_WARPS * 32, C::SMEM) != cudaSuccess)
+    cudaFuncSetAttribute(decode_kernel<FMT, D, NCB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<FMT, D, NCB>, DECODE_WARPS * 32, C::SMEM) !=
+        cudaSuccess)
         n = 1;
     i.ctas_per_sm = n > 0 ? n : 1;
     return i;
 }
 
-DecodeLaunchInfo decode_launch_info(int fmt, int D) {
+// ncb: 4-head column blocks of the mlx4g32 kernel (1 when every work group has <= 4 q heads).
+DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb) {
     if (fmt == FMT_FP16) {
-        if (D == 64) return info_t<FMT_FP16, 64>();
-        if (D == 128) return info_t<FMT_FP16, 128>();
-        return info_t<FMT_FP16, 256>();
+        if (D == 64) return info_t<FMT_FP16, 64, 1>();
+        if (D == 128) return info_t<FMT_FP16, 128, 1>();
+        return info_t<FMT_FP16, 256, 1>();
     }
-    if (D == 64) return info_t<FMT_I4, 64>();
-    if (D == 128) return info_t<FMT_I4, 128>();
-    return info_t<FMT_I4, 256>();
+    if (ncb == 1) {
+        if (D == 64) return info_t<FMT_I4, 64, 1>();
+        if (D == 128) return info_t<FMT_I4, 128, 1>();
+        return info_t<FMT_I4, 256, 1>();
+    }
+    if (D == 64) return info_t<FMT_I4, 64, 2>();
+    if (D == 128) return info_t<FMT_I4, 128, 2>();
+    return info_t<FMT_I4, 256, 2>();
+}
+
+int decode_ncb(const DecodeParams& p) {
+    int mx = 0;
+    for (int i = 0; i < p.n_groups; ++i) mx = p.grp[i].nq > mx ? p.grp[i].nq : mx;
+    return mx > 4 ? 2 : 1;
 }
 
 cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st) {
     if (fmt == FMT_FP16) {
-        if (D == 64) return launch_t<FMT_FP16, 64>(p, n_ctas, st);
-        if (D == 128) return launch_t<FMT_FP16, 128>(p, n_ctas, st);
-        if (D == 256) return launch_t<FMT_FP16, 256>(p, n_ctas, st);
+        if (D == 64) return launch_t<FMT_FP16, 64, 1>(p, n_ctas, st);
+        if (D == 128) return launch_t<FMT_FP16, 128, 1>(p, n_ctas, st);
+        if (D == 256) return launch_t<FMT_FP16, 256, 1>(p, n_ctas, st);
+        return cudaErrorInvalidValue;
+    }
+    if (decode_ncb(p) == 1) {
+        if (D == 64) return launch_t<FMT_I4, 64, 1>(p, n_ctas, st);
+        if (D == 128) return launch_t<FMT_I4, 128, 1>(p, n_ctas, st);
+        if (D == 256) return launch_t<FMT_I4, 256, 1>(p, n_ctas, st);
     } else {
-        if (D == 64) return launch_t<FMT_I4, 64>(p, n_ctas, st);
-        if (D == 128) return launch_t<FMT_I4, 128>(p, n_ctas, st);
-        if (D == 256) return launch_t<FMT_I4, 256>(p, n_ctas, st);
+        if (D == 64) return launch_t<FMT_I4, 64, 2>(p, n_ctas, st);
+        if (D == 128) return launch_t<FMT_I4, 128, 2>(p, n_ctas, st);
+        if (D == 256) return launch_t<FMT_I4, 256, 2>(p, n_ctas, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -24,7 +24,8 @@ struct DecodeLaunchInfo {
     int smem_bytes;
     int ctas_per_sm;
 };
-DecodeLaunchInfo decode_launch_info(int fmt, int D);
+DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb);
+int decode_ncb(const DecodeParams& p);   // 4-head column blocks the mlx4g32 kernel needs for p
 cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);
 
 // sparse selector

@@ -72,6 +72,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
                                           void* stream) {
     using namespace pck;
     if (!K_rec || !V_rec || !Q || !O) return PCK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(O) & 15) return PCK_EINVAL;
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || H_q < 1 || H_q > PCK_MAX_HEADS || N < 1 || S_suf < 0) return PCK_EINVAL;
     if (D != 64 && D != 128 && D != 256) return PCK_EUNSUPPORTED;
     if (q_dtype != PCK_DT_F32 && q_dtype != PCK_DT_F16) return PCK_EINVAL;
@@ -116,9 +117,11 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     if (tiles_bytes > NA_TILE_BYTES) return PCK_EUNSUPPORTED;
     if (n_groups > NA_COUNTERS) return PCK_EUNSUPPORTED;
     const int64_t total = static_cast<int64_t>(n_groups) * ntiles;
-    const DecodeLaunchInfo li = decode_launch_info(FMT_I4, D);
+    int max_nq = 0;
+    for (int i = 0; i < n_groups; ++i) max_nq = p.grp[i].nq > max_nq ? p.grp[i].nq : max_nq;
+    const DecodeLaunchInfo li = decode_launch_info(FMT_I4, D, max_nq > 4 ? 2 : 1);
     const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
-    const size_t slot_bytes = static_cast<size_t>(GMAX) * (D + 2) * sizeof(float);
+    const size_t slot_bytes = static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float);
     const int64_t max_slots = static_cast<int64_t>(NA_PARTIAL_BYTES / slot_bytes);
     int64_t max_warps = static_cast<int64_t>(sp.sms) * li.ctas_per_sm * DECODE_WARPS;
     const int64_t fixed = n_groups + static_cast<int64_t>(n_groups) * n_suf;   // item + suffix slots

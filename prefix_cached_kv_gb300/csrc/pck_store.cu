@@ -189,17 +189,16 @@ __global__ void __launch_bounds__(256) relayout_mlx4_kernel(RecSrc ks, RecSrc vs
             const int chunk = w / 128, lane = (w / 4) & 31, iw = chunk * 4 + (w & 3);
             const int q = lane & 3, l4 = lane >> 2;
             uint32_t nib[8];
-            if (!isV) {
-                const int nb = iw / ng, gq = iw % ng, s0 = 2 * gq, s1 = 2 * gq + 1;
-                const int t = tb + 8 * nb + l4;
-                nib[0] = rec_code(s, g, t, 16 * s0 + 2 * q);
-                nib[4] = rec_code(s, g, t, 16 * s0 + 2 * q + 1);
-                nib[1] = rec_code(s, g, t, 16 * s0 + 8 + 2 * q);
-                nib[5] = rec_code(s, g, t, 16 * s0 + 9 + 2 * q);
-                nib[2] = rec_code(s, g, t, 16 * s1 + 2 * q);
-                nib[6] = rec_code(s, g, t, 16 * s1 + 2 * q + 1);
-                nib[3] = rec_code(s, g, t, 16 * s1 + 8 + 2 * q);
-                nib[7] = rec_code(s, g, t, 16 * s1 + 9 + 2 * q);
+            if (!isV) {   // K word iw = k-step s: the A fragment (tokens l4 and l4+8, d 16s + ...)
+                const int s16 = 16 * iw;
+                nib[0] = rec_code(s, g, tb + l4, s16 + 2 * q);
+                nib[4] = rec_code(s, g, tb + l4, s16 + 2 * q + 1);
+                nib[1] = rec_code(s, g, tb + 8 + l4, s16 + 2 * q);
+                nib[5] = rec_code(s, g, tb + 8 + l4, s16 + 2 * q + 1);
+                nib[2] = rec_code(s, g, tb + l4, s16 + 8 + 2 * q);
+                nib[6] = rec_code(s, g, tb + l4, s16 + 9 + 2 * q);
+                nib[3] = rec_code(s, g, tb + 8 + l4, s16 + 8 + 2 * q);
+                nib[7] = rec_code(s, g, tb + 8 + l4, s16 + 9 + 2 * q);
             } else {
                 const int d0 = 8 * (2 * iw) + l4, d1 = 8 * (2 * iw + 1) + l4;
                 nib[0] = rec_code(s, g, tb + 2 * q, d0);
@@ -213,11 +212,10 @@ __global__ void __launch_bounds__(256) relayout_mlx4_kernel(RecSrc ks, RecSrc vs
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) val |= nib[k] << (4 * k);
-        } else {                                         // scale/bias word
-            const int e = w - 2 * D;                     // [q][slot][group]
-            const int gi = e % ng, slot = (e / ng) & 3, q = e / (4 * ng);
-            const int toff = (slot & 1) + 2 * q + ((slot >> 1) ? 8 : 0);
-            val = rec_sb(s, g, tb + toff, gi);
+        } else {                                         // scale/bias word, [token][group]
+            const int e = w - 2 * D;
+            const int gi = e % ng, t = e / ng;
+            val = rec_sb(s, g, tb + t, gi);
         }
         out[i] = val;
     }
