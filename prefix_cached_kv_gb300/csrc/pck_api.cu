@@ -259,6 +259,10 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     const DecodeLaunchInfo& li = dinfo(c, fmt, D, fmt == PCK_FMT_MLX4G32 ? decode_ncb(p) : 1);
     const int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS;
     int64_t tpw = (total + max_warps - 1) / max_warps;
+    // at most ~32 prefix pieces per item, so that the merge stays short
+    int vmax = 1;
+    for (int i = 0; i < n; ++i) vmax = std::max(vmax, p.desc[i].vtiles);
+    tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);
     if (tpw < 2) tpw = 2;
     const int64_t n_workers = (total + tpw - 1) / tpw;
     const int n_items = n * n_groups;
@@ -535,7 +539,8 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     pp.causal = causal;
     pp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     pp.err = c->dev_err;
-    cudaError_t e = launch_prefill(pp, grp, n_groups, S_suf > 0 ? c->suf_ws : nullptr, suf_ntiles, st, D);
+    cudaError_t e = launch_prefill(pp, grp, n_groups, S_suf > 0 ? c->suf_ws : nullptr, suf_ntiles, c->partials,
+                                   WS_PARTIAL_BYTES, c->sms, st, D);
     if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
     ++c->queries;
     return check_async(c);

@@ -57,8 +57,10 @@ struct PrefillParams {
     int* err;
 };
 // suf_tiles: the suffix [H_kv, S_suf, D] re-laid out like a resident fp16 slot of suf_ntiles tiles
+// partials: split-K workspace (partial_bytes); the launch splits each row tile's keys over CTAs
+// when that fills the GPU better, and merges the partials with a second (PDL-chained) kernel.
 cudaError_t launch_prefill(const PrefillParams& p, const WorkGroup* grp, int n_groups, const void* suf_tiles,
-                           int suf_ntiles, cudaStream_t st, int D);
+                           int suf_ntiles, float* partials, size_t partial_bytes, int sms, cudaStream_t st, int D);
 bool prefill_supported(int D);
 
 }  // namespace pck

@@ -32,11 +32,13 @@ namespace pck {
 namespace {
 
 constexpr int PF_ROWS = 128;          // query rows per CTA (MMA M)
-constexpr int PF_BLOCK = 128;         // keys per block (MMA N of S = Q K^T)
+constexpr int PF_BLOCK = 64;          // keys per block (MMA N of S = Q K^T)
 constexpr int PF_THREADS = 192;       // 4 softmax warps + MMA warp + producer warp
 constexpr float PF_THRESH = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr float PF_LN2 = 0.69314718055994530942f;
 
+// Shared memory of one CTA, sized so that two CTAs fit on an SM (one's softmax overlaps the
+// other's MMAs): Q tile, a 2-stage K/V ring of 64-key blocks, the P tile, barriers.
 template <int D>
 struct PCfg {
     static constexpr int Q_BYTES = PF_ROWS * D * 2;
@@ -49,9 +51,9 @@ struct PCfg {
     static constexpr int OFF_V1 = OFF_K1 + KV_BYTES;
     static constexpr int OFF_P = OFF_V1 + KV_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;           // 8 mbarriers + tmem slot
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;         // + alignment slack
-    static constexpr int S_COL = 0;                           // TMEM columns of S
-    static constexpr int O_COL = PF_BLOCK;                    // TMEM columns of O
+    static constexpr int SMEM = OFF_BAR + 128 + 128;          // + alignment slack (128 B)
+    static constexpr int S_COL = 0;                           // TMEM columns of S (64)
+    static constexpr int O_COL = 128;                         // TMEM columns of O (D)
     static constexpr int TMEM_COLS = 256;
 };
 
@@ -123,10 +125,12 @@ struct PfParams {
     PrefillParams a;
     WorkGroup grp[MAX_GROUPS];
     int n_groups;
-    int n_tasks;
+    int n_tiles;                    // row tiles over all groups
+    int n_split;                    // key-range splits per row tile (CTAs = n_tiles * n_split)
     int task_off[MAX_GROUPS + 1];   // prefix sums of row tiles per group
     const uint8_t* suf_tiles;       // suffix in the resident fp16 layout (or nullptr)
     int suf_ntiles;
+    float* partials;                // n_split > 1: [tile][split][row][partial_stride(D)]
 };
 
 // Key block b of the task's key sequence: prefix blocks first, then suffix blocks.
@@ -170,14 +174,15 @@ template <int D>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_constant__ PfParams P) {
     using C = PCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t s_base = smem_u32(smem);
     const uint32_t bar = s_base + C::OFF_BAR;   // [0,1] full, [2,3] empty, [4] s_full, [5] p_full, [6] o_done, [7] final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 64);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- which rows
-    const int task = blockIdx.x;
+    const int task = blockIdx.x / P.n_split;       // row tile
+    const int split = blockIdx.x - task * P.n_split;
     int grp = 0;
     while (grp + 1 < P.n_groups && P.task_off[grp + 1] <= task) ++grp;
     const WorkGroup& wg = P.grp[grp];
@@ -201,6 +206,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         nbs = (kmax + PF_BLOCK - 1) / PF_BLOCK;
     }
     const int nblocks = nbp + nbs;
+    // this CTA's contiguous share of the key blocks (n_split <= nbp, so it is never empty)
+    const int kb0 = static_cast<int>((static_cast<int64_t>(nblocks) * split) / P.n_split);
+    const int kb1 = static_cast<int>((static_cast<int64_t>(nblocks) * (split + 1)) / P.n_split);
+    const int nbl = kb1 - kb0;
 
     // ---- setup: barriers, TMEM, Q tile
     if (tid == 0) {
@@ -245,10 +254,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     if (warp == 5) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            for (int b = 0; b < nblocks && !failed; ++b) {
-                const int st = b & 1;
-                if (b >= 2 && !mbar_wait_bounded(bar + 16 + 8 * st, ((b >> 1) - 1) & 1)) { failed = true; break; }
-                const KeyBlock kb = key_block(P, g, b, nbp, D);
+            for (int bi = 0; bi < nbl && !failed; ++bi) {
+                const int st = bi & 1;
+                if (bi >= 2 && !mbar_wait_bounded(bar + 16 + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
+                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
                 const uint32_t bytes = kb.ntile * 32 * D;
                 mbar_arrive_expect_tx(bar + 8 * st, 2 * bytes);
                 bulk_g2s(s_base + (st ? C::OFF_K1 : C::OFF_K0), kb.k, bytes, bar + 8 * st);
@@ -261,34 +270,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         if (lane == 0) {
             const uint32_t s_tm = tmem + C::S_COL, o_tm = tmem + C::O_COL;
             int prev_ntile = 0;
-            for (int b = 0; b <= nblocks && !failed; ++b) {
-                if (b < nblocks) {
-                    const int st = b & 1;
-                    if (!mbar_wait_bounded(bar + 8 * st, (b >> 1) & 1)) { failed = true; break; }
+            for (int bi = 0; bi <= nbl && !failed; ++bi) {
+                if (bi < nbl) {
+                    const int st = bi & 1;
+                    if (!mbar_wait_bounded(bar + 8 * st, (bi >> 1) & 1)) { failed = true; break; }
                 }
-                if (b > 0) {   // O += P(b-1) V(b-1) once the softmax has written P(b-1)
-                    if (!mbar_wait_bounded(bar + 40, (b - 1) & 1)) { failed = true; break; }
+                if (bi > 0) {   // O += P(bi-1) V(bi-1) once the softmax has written P(bi-1)
+                    if (!mbar_wait_bounded(bar + 40, (bi - 1) & 1)) { failed = true; break; }
                     tc_fence_after();
-                    const int pst = (b - 1) & 1;
+                    const int pst = (bi - 1) & 1;
                     const uint32_t v_s = s_base + (pst ? C::OFF_V1 : C::OFF_V0);
                     const uint32_t idesc = idesc_f16(PF_ROWS, D);
                     for (int u = 0; u < prev_ntile; ++u) {
-                        const uint64_t a = sdesc(s_base + C::OFF_P + u * 256, 128, 16 * 128);
+                        const uint64_t a = sdesc(s_base + C::OFF_P + u * 256, 128, (PF_BLOCK / 8) * 128);
                         const uint64_t bd = sdesc(v_s + u * 32 * D, 128, 256);
-                        umma_f16(o_tm, a, bd, idesc, (b - 1 > 0 || u > 0) ? 1u : 0u);
+                        umma_f16(o_tm, a, bd, idesc, (bi - 1 > 0 || u > 0) ? 1u : 0u);
                     }
                     umma_commit(bar + 16 + 8 * pst);   // K/V stage free once these complete
-                    if (b == nblocks) umma_commit(bar + 48);   // O final
+                    if (bi == nbl) umma_commit(bar + 48);   // O final
                 }
-                if (b < nblocks) {   // S = Q K(b)^T
-                    const int st = b & 1;
-                    const KeyBlock kb = key_block(P, g, b, nbp, D);
+                if (bi < nbl) {   // S = Q K(b)^T
+                    const int st = bi & 1;
+                    const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
                     const uint32_t k_s = s_base + (st ? C::OFF_K1 : C::OFF_K0);
                     const uint32_t idesc = idesc_f16(PF_ROWS, kb.ntile * TILE_TOK);
-                    for (int s = 0; s < D / 16; ++s) {
-                        const uint64_t a = sdesc(s_base + C::OFF_Q + s * 256, 128, 16 * D);
-                        const uint64_t bd = sdesc(k_s + s * 256, 128, 16 * D);
-                        umma_f16(s_tm, a, bd, idesc, s > 0 ? 1u : 0u);
+                    for (int s2 = 0; s2 < D / 16; ++s2) {
+                        const uint64_t a = sdesc(s_base + C::OFF_Q + s2 * 256, 128, 16 * D);
+                        const uint64_t bd = sdesc(k_s + s2 * 256, 128, 16 * D);
+                        umma_f16(s_tm, a, bd, idesc, s2 > 0 ? 1u : 0u);
                     }
                     umma_commit(bar + 32);
                     prev_ntile = kb.ntile;
@@ -311,11 +320,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         float m = -INFINITY, l = 0.f;
         uint8_t* ps = smem + C::OFF_P;
         const int R = tid >> 3, rr = tid & 7;
-        for (int b = 0; b < nblocks; ++b) {
+        for (int bi = 0; bi < nbl; ++bi) {
             // warp-uniform outcome: the tcgen05.ld below must be executed by the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + 32, b & 1))) { failed = true; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + 32, bi & 1))) { failed = true; break; }
             tc_fence_after();
-            const KeyBlock kb = key_block(P, g, b, nbp, D);
+            const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
             const int lim = kb.is_suf ? min(kb.key0 + kb.ntile * TILE_TOK, suf_lim + 1) : min(kb.key0 + kb.ntile * TILE_TOK, N);
             const int nvalid = row_ok ? max(0, lim - kb.key0) : 0;   // keys [key0, key0 + nvalid) visible
             const int ncols = kb.ntile * TILE_TOK;
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             if (__any_sync(0xffffffffu, need)) {
                 const float mnew = need ? mb : m;
                 const float alpha = need ? exp2f(m - mnew) : 1.0f;
-                if (b > 0) {
+                if (bi > 0) {
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t v[32];
                         tmem_ld32(o_tm + c0, v);
@@ -351,8 +360,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                     tmem_ld32(s_tm + c0, v);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float p0 = (c0 + j < nvalid) ? exp2f(__uint_as_float(v[j]) * sc - m) : 0.f;
-                        const float p1 = (c0 + j + 1 < nvalid) ? exp2f(__uint_as_float(v[j + 1]) * sc - m) : 0.f;
+                        const float p0 = (c0 + j < nvalid) ? ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m)) : 0.f;
+                        const float p1 = (c0 + j + 1 < nvalid) ? ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m)) : 0.f;
                         const __half2 h = __floats2half2_rn(p0, p1);
                         const float2 hf = __half22float2(h);
                         l += hf.x + hf.y;   // normaliser of the probabilities actually used
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {   // 8 keys (16 B) per core-matrix row
                     const int kc = (c0 >> 3) + q;
-                    *reinterpret_cast<uint4*>(ps + (R * 16 + kc) * 128 + rr * 16) =
+                    *reinterpret_cast<uint4*>(ps + (R * (PF_BLOCK / 8) + kc) * 128 + rr * 16) =
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
@@ -377,20 +386,37 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             set_err(P.a.err, 4);
         } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + 48, 0))) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.0f / l : 0.f;
-            float* orow = row_ok ? P.a.O + ((size_t)wg.qh[r / M] * M + i) * D : nullptr;
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(o_tm + c0, v);
-                if (row_ok) {
+            if (P.n_split == 1) {
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+                float* orow = row_ok ? P.a.O + ((size_t)wg.qh[r / M] * M + i) * D : nullptr;
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(o_tm + c0, v);
+                    if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(orow + c0 + j) =
-                            make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
-                                        __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(orow + c0 + j) =
+                                make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
+                                            __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+                    }
+                }
+                if (row_ok && P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
+            } else {   // partial [m, l, -, -, o unnormalised] of this key range, merged later
+                float* prow = P.partials +
+                              ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * partial_stride(D);
+                if (row_ok) { prow[0] = m; prow[1] = l; }
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(o_tm + c0, v);
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(prow + PARTIAL_O + c0 + j) =
+                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                    }
                 }
             }
-            if (row_ok && P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
         } else {
             set_err(P.a.err, 5);
         }
@@ -399,6 +425,50 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// Merge of the key-range partials of each row: one warp per row, lanes over d (float4).
+template <int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PfParams P) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int rows = P.n_tiles * PF_ROWS;
+    constexpr int LPP = D / 4;   // lanes holding the row's d (D <= 128)
+    for (int R = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; R < rows; R += (gridDim.x * blockDim.x) >> 5) {
+        const int tile = R / PF_ROWS, rr = R - tile * PF_ROWS;
+        int grp = 0;
+        while (grp + 1 < P.n_groups && P.task_off[grp + 1] <= tile) ++grp;
+        const WorkGroup& wg = P.grp[grp];
+        const int M = P.a.M;
+        const int r = (tile - P.task_off[grp]) * PF_ROWS + rr;
+        if (r >= wg.nq * M) continue;
+        const float* base = P.partials + ((size_t)tile * P.n_split * PF_ROWS + rr) * partial_stride(D);
+        const size_t sstride = (size_t)PF_ROWS * partial_stride(D);
+        float ms = -INFINITY, ls = 0.f;
+        if (lane < P.n_split) { ms = __ldcg(base + lane * sstride); ls = __ldcg(base + lane * sstride + 1); }
+        float Mx = ms;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+        const float w = (lane < P.n_split && ms != -INFINITY) ? exp2f(ms - Mx) : 0.f;
+        float L = w * ls;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < P.n_split; ++sp) {
+            const float ws = __shfl_sync(0xffffffffu, w, sp);
+            if (lane < LPP) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(base + sp * sstride + PARTIAL_O) + lane);
+                acc.x = fmaf(ws, x.x, acc.x); acc.y = fmaf(ws, x.y, acc.y);
+                acc.z = fmaf(ws, x.z, acc.z); acc.w = fmaf(ws, x.w, acc.w);
+            }
+        }
+        const int h = wg.qh[r / M], i = r % M;
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        if (lane < LPP)
+            reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = L > 0.f ? (Mx + log2f(L)) * PF_LN2 : -INFINITY;
+    }
 }
 
 bool prefill_supported(int D) { return D == 64 || D == 128; }
@@ -412,12 +482,24 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    prefill_kernel<D><<<P.n_tasks, PF_THREADS, C::SMEM, st>>>(P);
-    return cudaGetLastError();
+    prefill_kernel<D><<<P.n_tiles * P.n_split, PF_THREADS, C::SMEM, st>>>(P);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || P.n_split == 1) return e;
+    cudaLaunchConfig_t cfg = {};
+    const int rows = P.n_tiles * PF_ROWS;
+    cfg.gridDim = dim3((rows + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr2[1];
+    attr2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr2[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, P);
 }
 
 cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_groups, const void* suf_tiles,
-                           int suf_ntiles, cudaStream_t st, int D) {
+                           int suf_ntiles, float* partials, size_t partial_bytes, int sms, cudaStream_t st, int D) {
     static thread_local PfParams P;
     P.a = a;
     P.n_groups = n_groups;
@@ -428,10 +510,19 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
         off += (grp[i].nq * a.M + PF_ROWS - 1) / PF_ROWS;
     }
     P.task_off[n_groups] = off;
-    P.n_tasks = off;
+    P.n_tiles = off;
     P.suf_tiles = static_cast<const uint8_t*>(suf_tiles);
     P.suf_ntiles = suf_ntiles;
+    P.partials = partials;
     if (off == 0) return cudaSuccess;
+    // key-range splits: enough CTAs for two per SM, never more splits than prefix blocks
+    const int nbp = (a.N + PF_BLOCK - 1) / PF_BLOCK;
+    int ns = (2 * sms) / off;
+    if (ns < 1) ns = 1;
+    if (ns > nbp) ns = nbp;
+    if (ns > 32) ns = 32;
+    while (ns > 1 && static_cast<size_t>(off) * ns * PF_ROWS * partial_stride(D) * sizeof(float) > partial_bytes) --ns;
+    P.n_split = ns;
     if (D == 64) return launch_prefill_t<64>(P, st);
     if (D == 128) return launch_prefill_t<128>(P, st);
     return cudaErrorInvalidValue;

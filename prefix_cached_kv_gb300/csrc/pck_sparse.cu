@@ -67,16 +67,35 @@ __global__ void select_kernel(const __grid_constant__ SelectParams p) {
     if (warp < wg.nq) {
         const int h = wg.qh[warp];
         const float* sc = p.scores + (size_t)h * p.nb;
+        constexpr int RPL = 32;                 // scores held in registers per lane (nb <= 1024)
+        float reg[RPL];
+        const bool in_regs = p.nb <= 32 * RPL;
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) reg[i] = (lane + 32 * i < p.nb) ? sc[lane + 32 * i] : -INFINITY;
+        }
         float prev_s = INFINITY;
         int prev_i = -1;
         for (int r = 0; r < K; ++r) {
             float bs = -INFINITY;
             int bi = 0x7fffffff;
-            for (int b = lane; b < p.nb; b += 32) {
-                const float s = sc[b];
-                if (better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
-                    bs = s;
-                    bi = b;
+            if (in_regs) {
+#pragma unroll
+                for (int i = 0; i < RPL; ++i) {
+                    const int b = lane + 32 * i;
+                    const float s = reg[i];
+                    if (b < p.nb && better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
+                        bs = s;
+                        bi = b;
+                    }
+                }
+            } else {
+                for (int b = lane; b < p.nb; b += 32) {
+                    const float s = sc[b];
+                    if (better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
+                        bs = s;
+                        bi = b;
+                    }
                 }
             }
 #pragma unroll

@@ -34,56 +34,88 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// One thread per output code word (8 consecutive elements); a group of 32 is 4 adjacent lanes.
+// Codes of one word (8 elements) given its group's fp16 scale and bias, bit-exact with
+// clamp(rint(fp32(fp32(x - bias) / scale)), 0, 15):
+//   the quotient is first taken as a * RN(1/scale), which is within 2^-17 of the exact quotient
+//   for |a/scale| <= 17 (two roundings of 2^-24 relative each); rint of it can only differ from
+//   rint of the correctly rounded quotient when the value lies within 2^-16 of a half-integer,
+//   and exactly those elements are redone with the IEEE division. Values far outside [0, 15]
+//   clamp to the same code either way.
+__device__ __forceinline__ uint32_t codes_of(const float (&x)[8], float sf, float bf, float rcp) {
+    uint32_t w = 0;
+    if (sf != 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float a = __fsub_rn(x[k], bf);
+            const float tp = __fmul_rn(a, rcp);
+            float c = rintf(tp);
+            if (fabsf(tp - c) > 0.5f - 1.52587890625e-05f) c = rintf(__fdiv_rn(a, sf));   // near a tie
+            c = fminf(fmaxf(c, 0.0f), 15.0f);
+            w |= static_cast<uint32_t>(c) << (4 * k);
+        }
+    }
+    return w;
+}
+
+// One thread per pair of output code words (16 consecutive elements, 32 B of fp16 input); a group
+// of 32 elements is 2 adjacent lanes. Each iteration handles two pairs (at p and p + stride) so
+// that four 16-byte loads per thread are in flight.
 template <typename SrcT>
 __global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __restrict__ X, int64_t rows,
                                                                 int kv_dim, uint8_t* __restrict__ out) {
     const int wpr = kv_dim / 8;                 // words per row
-    const int64_t total = rows * wpr;           // multiple of 4; a warp never splits a group
+    const int64_t total = rows * wpr / 2;       // word pairs; even per group, a warp never splits one
     const int rec = kv_dim / 2 + kv_dim / 8;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t wi0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // Every lane of a warp runs the same number of iterations (total is padded by the grid),
-    // so the group shuffles below always see their 4 partners.
-    int64_t iters = (total + stride - 1) / stride;
+    const int64_t pi0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // Every lane of a warp runs the same number of iterations, so the group shuffle below always
+    // sees its partner (the 2 lanes of a group are both live or both idle).
+    const int64_t iters = (total + 2 * stride - 1) / (2 * stride);
     for (int64_t it = 0; it < iters; ++it) {
-        int64_t wi = wi0 + it * stride;
-        bool live = wi < total;
-        float x[8];
-        if (live) {
-            load8<SrcT>(X + wi * 8, x);
-        } else {
+        int64_t pi[2];
+        bool live[2];
+        float x[2][2][8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = 0.f;
-        }
-        float mn = x[0], mx = x[0];
+        for (int u = 0; u < 2; ++u) {
+            pi[u] = pi0 + (2 * it + u) * stride;
+            live[u] = pi[u] < total;
 #pragma unroll
-        for (int k = 1; k < 8; ++k) { mn = fminf(mn, x[k]); mx = fmaxf(mx, x[k]); }
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-        const __half s16 = __float2half_rn(s32);     // round-trip through fp16 first
-        const __half b16 = __float2half_rn(mn);
-        const float sf = __half2float(s16), bf = __half2float(b16);
-        uint32_t w = 0;
-        if (sf != 0.0f) {
+            for (int h = 0; h < 2; ++h) {
+                if (live[u]) {
+                    load8<SrcT>(X + (pi[u] * 2 + h) * 8, x[u][h]);
+                } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float t = __fdiv_rn(__fsub_rn(x[k], bf), sf);
-                float c = fminf(fmaxf(rintf(t), 0.0f), 15.0f);
-                w |= static_cast<uint32_t>(c) << (4 * k);
+                    for (int k = 0; k < 8; ++k) x[u][h][k] = 0.f;
+                }
             }
         }
-        if (live) {
-            const int64_t row = wi / wpr;
-            const int word = static_cast<int>(wi - row * wpr);
-            uint8_t* r = out + row * rec;
-            reinterpret_cast<uint32_t*>(r)[word] = w;
-            if ((word & 3) == 0) {
-                reinterpret_cast<__half*>(r + kv_dim / 2)[word >> 2] = s16;
-                reinterpret_cast<__half*>(r + kv_dim / 2 + kv_dim / 16)[word >> 2] = b16;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            float mn = x[u][0][0], mx = x[u][0][0];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) { mn = fminf(mn, x[u][h][k]); mx = fmaxf(mx, x[u][h][k]); }
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+            const __half s16 = __float2half_rn(s32);     // round-trip through fp16 first
+            const __half b16 = __float2half_rn(mn);
+            const float sf = __half2float(s16), bf = __half2float(b16);
+            const float rcp = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+            const uint32_t w0 = codes_of(x[u][0], sf, bf, rcp);
+            const uint32_t w1 = codes_of(x[u][1], sf, bf, rcp);
+            if (live[u]) {
+                const int64_t wi = pi[u] * 2;
+                const int64_t row = wi / wpr;
+                const int word = static_cast<int>(wi - row * wpr);
+                uint8_t* r = out + row * rec;
+                reinterpret_cast<uint32_t*>(r)[word] = w0;        // records are only 4-byte aligned
+                reinterpret_cast<uint32_t*>(r)[word + 1] = w1;
+                if ((word & 3) == 0) {
+                    reinterpret_cast<__half*>(r + kv_dim / 2)[word >> 2] = s16;
+                    reinterpret_cast<__half*>(r + kv_dim / 2 + kv_dim / 16)[word >> 2] = b16;
+                }
             }
         }
     }
@@ -232,7 +264,7 @@ static int grid_for(int64_t work, int threads, int sms) {
 }
 
 cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim, void* out, cudaStream_t st, int sms) {
-    int64_t total = rows * (kv_dim / 8);
+    int64_t total = rows * (kv_dim / 16);   // word pairs
     int threads = 256;
     int blocks = grid_for(total, threads, sms);
     if (src_f16)
