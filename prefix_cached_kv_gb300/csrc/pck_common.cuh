@@ -23,9 +23,9 @@
 //       tokens of the tile as rows; nibble n (bits 4n..4n+3):
 //           n0 = c[t][16s+2q]    n4 = c[t][16s+2q+1]    n1 = c[t+8][16s+2q]    n5 = c[t+8][16s+2q+1]
 //           n2 = c[t][16s+8+2q]  n6 = c[t][16s+9+2q]    n3 = c[t+8][16s+8+2q]  n7 = c[t+8][16s+9+2q]
-//       V word i: the B fragments of d n-blocks j0 = 2i, j1 = 2i+1 (d0 = 8*j0 + t, d1 = 8*j1 + t):
-//           n0 = c[2q][d0]  n4 = c[2q+1][d0]  n1 = c[8+2q][d0]  n5 = c[9+2q][d0]
-//           n2 = c[2q][d1]  n6 = c[2q+1][d1]  n3 = c[8+2q][d1]  n7 = c[9+2q][d1]
+//       V word i (m-tile i, d = 16i + t): the lane's A fragment of O^T = V^T P'^T, d as rows:
+//           n0 = c[2q][d]    n4 = c[2q+1][d]    n1 = c[2q][d+8]    n5 = c[2q+1][d+8]
+//           n2 = c[8+2q][d]  n6 = c[9+2q][d]    n3 = c[8+2q][d+8]  n7 = c[9+2q][d+8]
 //       so (w & 0x000F000F), (w & 0x00F000F0), ((w>>8) & 0x000F000F), ((w>>8) & 0x00F000F0) are
 //       four half2 registers holding the codes as exact fp16 subnormals c * 2^-24 or 16c * 2^-24.
 //     sb: [token 0..15][group 0..D/32) half2(scale, bias).

@@ -43,9 +43,9 @@ struct DCfg {
     static constexpr int NG = D / 32;       // mlx4g32 groups per head
     static constexpr int NBV = D / 8;       // PV n-blocks over d
     static constexpr int TB = tile_bytes(FMT, D);
-    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 2 : 1);
+    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 2 : 1));
     static constexpr int STAGE = TPS * TB;
-    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : (D == 256 ? 2 : 4);
+    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : 2;
     static constexpr bool QSMEM = D > 128;  // q fragments live in shared memory (register budget)
     static constexpr int QSMEM_BYTES = QSMEM ? KS * 32 * 16 : 0;
     static constexpr int RING = NSTAGE * STAGE;
@@ -255,7 +255,8 @@ struct I4State {
     static constexpr int KS = D / 16, NG = D / 32, NBV = D / 8;
     uint32_t qb[NCB][KS][2];   // B fragments of the item's q (tau*log2e prescaled), hi or lo part
     float qs[NCB][NG];         // sum over the group's d of the lane's head q (prescaled)
-    float oacc[NBV][4];        // O rows l/4 (block 0) in [0..1], rows 8 + l/4 (block 1) in [2..3]
+    float oacc[NCB][KS][4];    // O^T m-tile mt: d = 16mt + l/4 in [0..1], d + 8 in [2..3]; columns
+                               // 2q, 2q+1 = (hi, lo) of head cb*4 + q
     float bacc[NCB][NG];       // sum_t p_t * bias_t of the lane's head, per group
     float m_ref[NCB];
     float l_part[NCB];
@@ -301,9 +302,9 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
         }
         st.m_ref[cb] = -INFINITY;
         st.l_part[cb] = 0.f;
-    }
 #pragma unroll
-    for (int j = 0; j < S::NBV; ++j) st.oacc[j][0] = st.oacc[j][1] = st.oacc[j][2] = st.oacc[j][3] = 0.f;
+        for (int mt = 0; mt < S::KS; ++mt) st.oacc[cb][mt][0] = st.oacc[cb][mt][1] = st.oacc[cb][mt][2] = st.oacc[cb][mt][3] = 0.f;
+    }
     __syncwarp();
 }
 
@@ -395,7 +396,6 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
         need_any |= m > st.m_ref[cb] + RESCALE_THRESHOLD;
     }
     if (__any_sync(0xffffffffu, need_any)) {
-        float alpha_row[NCB];
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
             const bool need = mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;
@@ -405,15 +405,10 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
 #pragma unroll
             for (int g = 0; g < NG; ++g) st.bacc[cb][g] *= alpha;
             st.m_ref[cb] = mnew;
-            alpha_row[cb] = __shfl_sync(0xffffffffu, alpha, lane >> 3);    // factor of O row head l/8
-        }
 #pragma unroll
-        for (int j = 0; j < S::NBV; ++j) {
-            st.oacc[j][0] *= alpha_row[0];
-            st.oacc[j][1] *= alpha_row[0];
-            if constexpr (NCB == 2) {
-                st.oacc[j][2] *= alpha_row[1];
-                st.oacc[j][3] *= alpha_row[1];
+            for (int m2 = 0; m2 < KS; ++m2) {   // O^T columns of this lane are head q's
+                st.oacc[cb][m2][0] *= alpha; st.oacc[cb][m2][1] *= alpha;
+                st.oacc[cb][m2][2] *= alpha; st.oacc[cb][m2][3] *= alpha;
             }
         }
     }
@@ -427,28 +422,28 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
                 pr[x][cb][y] = z[x][cb][y] == -INFINITY ? 0.f : ex2_approx(z[x][cb][y] - st.m_ref[cb]);
             st.l_part[cb] += pr[x][cb][0] + pr[x][cb][1];
         }
-    // ---- O += P' V per tile and group of 32 d (P' = p * scale of the token's group)
+    // ---- O^T += V^T P'^T per tile and group of 32 d (P' = p * scale of the token's group):
+    //      A = V codes (d as rows), B = P' of the 16 tokens x (head, hi/lo) columns
 #pragma unroll
     for (int x = 0; x < NT; ++x) {
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
             const float2 sv0 = __half22float2(u32_as_h2(vs0[x][g]));
             const float2 sv1 = __half22float2(u32_as_h2(vs1[x][g]));
-            uint32_t a[4];
+            uint32_t b[NCB][2];
 #pragma unroll
             for (int cb = 0; cb < NCB; ++cb) {
                 st.bacc[cb][g] = fmaf(pr[x][cb][0], sv0.y, fmaf(pr[x][cb][1], sv1.y, st.bacc[cb][g]));
-                a[cb] = movmatrix_trans(pack_hilo(pr[x][cb][0] * sv0.x));
-                a[2 + cb] = movmatrix_trans(pack_hilo(pr[x][cb][1] * sv1.x * 0.0625f));   // V regs of t+8 hold 16 c
+                b[cb][0] = movmatrix_trans(pack_hilo(pr[x][cb][0] * sv0.x));   // tokens 0..7
+                b[cb][1] = movmatrix_trans(pack_hilo(pr[x][cb][1] * sv1.x));   // tokens 8..15
             }
-            if constexpr (NCB == 1) { a[1] = 0u; a[3] = 0u; }
 #pragma unroll
             for (int ww = 0; ww < 2; ++ww) {
-                const int i = 2 * g + ww;          // V word: n-blocks 2i, 2i+1
-                uint32_t b0, b1, b2, b3;
-                unpack_word(vw[x][i], b0, b1, b2, b3);
-                mma16816(st.oacc[2 * i], a, b0, b1);
-                mma16816(st.oacc[2 * i + 1], a, b2, b3);
+                const int m2 = 2 * g + ww;          // m-tile of 16 d
+                uint32_t a[4];
+                unpack_word(vw[x][m2], a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int cb = 0; cb < NCB; ++cb) mma16816(st.oacc[cb][m2], a, b[cb][0], b[cb][1]);
             }
         }
     }
@@ -459,9 +454,10 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
 template <int D, int NCB>
 __device__ __forceinline__ void write_partial_i4(I4State<D, NCB>& st, float* P, int nq, int lane) {
     using S = I4State<D, NCB>;
-    const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
+    const int q = lane & 3, l4 = lane >> 2;
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
+        const int hq = cb * 4 + q;   // this lane's head for l, bias and the O^T columns
         float l = st.l_part[cb];
         l += __shfl_xor_sync(0xffffffffu, l, 4);
         l += __shfl_xor_sync(0xffffffffu, l, 8);
@@ -473,26 +469,21 @@ __device__ __forceinline__ void write_partial_i4(I4State<D, NCB>& st, float* P, 
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             v += __shfl_xor_sync(0xffffffffu, v, 8);
             v += __shfl_xor_sync(0xffffffffu, v, 16);
-            bsum[g] = __shfl_sync(0xffffffffu, v, hl);   // bias sums of head hl (held by lane hl)
+            bsum[g] = v;
         }
-        const int hq = cb * 4 + q;
-        if (lane < 4 && hq < nq) {
+        if (hq < nq) {
             float* ph = P + hq * partial_stride(D);
-            ph[0] = st.m_ref[cb];
-            ph[1] = l;
-        }
-        const int h = cb * 4 + hl;
+            if (lane < 4) {
+                ph[0] = st.m_ref[cb];
+                ph[1] = l;
+            }
 #pragma unroll
-        for (int j = 0; j < S::NBV; ++j) {
-            const float c0 = cb == 0 ? st.oacc[j][0] : st.oacc[j][2];
-            const float c1 = cb == 0 ? st.oacc[j][1] : st.oacc[j][3];
-            const float o0 = c0 + __shfl_xor_sync(0xffffffffu, c0, 4);   // hi row + lo row
-            const float o1 = c1 + __shfl_xor_sync(0xffffffffu, c1, 4);
-            if (part == 0 && h < nq) {
-                const int dd = 8 * j + 2 * q;
-                const float b = bsum[j / 4];
-                P[h * partial_stride(D) + PARTIAL_O + dd] = fmaf(o0, 16777216.0f, b);
-                P[h * partial_stride(D) + PARTIAL_O + 1 + dd] = fmaf(o1, 16777216.0f, b);
+            for (int m2 = 0; m2 < S::KS; ++m2) {
+                const float b = bsum[m2 / 2];
+                const int d = 16 * m2 + l4;
+                // columns 2q (hi) and 2q+1 (lo) hold the same head; rows d+8 carry 16 c
+                ph[PARTIAL_O + d] = fmaf(st.oacc[cb][m2][0] + st.oacc[cb][m2][1], 16777216.0f, b);
+                ph[PARTIAL_O + d + 8] = fmaf(st.oacc[cb][m2][2] + st.oacc[cb][m2][3], 1048576.0f, b);
             }
         }
     }

@@ -101,6 +101,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -328,13 +342,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             const int lim = kb.is_suf ? min(kb.key0 + kb.ntile * TILE_TOK, suf_lim + 1) : min(kb.key0 + kb.ntile * TILE_TOK, N);
             const int nvalid = row_ok ? max(0, lim - kb.key0) : 0;   // keys [key0, key0 + nvalid) visible
             const int ncols = kb.ntile * TILE_TOK;
+            // one pass over S: both 32-column loads in flight, one wait
+            uint32_t v[PF_BLOCK];
+            tmem_ld32_nowait(s_tm, v);
+            if (ncols > 32) tmem_ld32_nowait(s_tm + 32, v + 32);
+            tmem_wait_ld();
+            const bool full = nvalid == PF_BLOCK;   // every key of the block visible to this row
             float bmax = -INFINITY;
-            for (int c0 = 0; c0 < ncols; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(s_tm + c0, v);
+            if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < nvalid) bmax = fmaxf(bmax, __uint_as_float(v[j]));
+                for (int j = 0; j < PF_BLOCK; ++j) bmax = fmaxf(bmax, __uint_as_float(v[j]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < PF_BLOCK; ++j)
+                    if (j < nvalid) bmax = fmaxf(bmax, __uint_as_float(v[j]));
             }
             const float mb = bmax * sc;
             const bool need = mb > m + PF_THRESH;
@@ -343,41 +364,40 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                 const float alpha = need ? exp2f(m - mnew) : 1.0f;
                 if (bi > 0) {
                     for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(o_tm + c0, v);
+                        uint32_t o[32];
+                        tmem_ld32(o_tm + c0, o);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-                        tmem_st32(o_tm + c0, v);
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(o_tm + c0, o);
                     }
                 }
                 l *= alpha;
                 m = mnew;
             }
-            for (int c0 = 0; c0 < PF_BLOCK; c0 += 32) {
-                uint32_t pk[16];
-                if (c0 < ncols) {
-                    uint32_t v[32];
-                    tmem_ld32(s_tm + c0, v);
+            uint32_t pk[PF_BLOCK / 2];
+            float lsum = 0.f;
+            if (full) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float p0 = (c0 + j < nvalid) ? ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m)) : 0.f;
-                        const float p1 = (c0 + j + 1 < nvalid) ? ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m)) : 0.f;
-                        const __half2 h = __floats2half2_rn(p0, p1);
-                        const float2 hf = __half22float2(h);
-                        l += hf.x + hf.y;   // normaliser of the probabilities actually used
-                        pk[j >> 1] = h2_as_u32(h);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+                for (int j = 0; j < PF_BLOCK; j += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m));
+                    lsum += p0 + p1;
+                    pk[j >> 1] = h2_as_u32(__floats2half2_rn(p0, p1));
                 }
+            } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {   // 8 keys (16 B) per core-matrix row
-                    const int kc = (c0 >> 3) + q;
-                    *reinterpret_cast<uint4*>(ps + (R * (PF_BLOCK / 8) + kc) * 128 + rr * 16) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int j = 0; j < PF_BLOCK; j += 2) {
+                    const float p0 = j < nvalid ? ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m)) : 0.f;
+                    const float p1 = j + 1 < nvalid ? ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m)) : 0.f;
+                    lsum += p0 + p1;
+                    pk[j >> 1] = h2_as_u32(__floats2half2_rn(p0, p1));
                 }
             }
+            l += lsum;
+#pragma unroll
+            for (int kc = 0; kc < PF_BLOCK / 8; ++kc)   // 8 keys (16 B) per core-matrix row
+                *reinterpret_cast<uint4*>(ps + (R * (PF_BLOCK / 8) + kc) * 128 + rr * 16) =
+                    make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar + 40);

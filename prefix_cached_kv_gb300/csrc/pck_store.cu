@@ -231,16 +231,16 @@ __global__ void __launch_bounds__(256) relayout_mlx4_kernel(RecSrc ks, RecSrc vs
                 nib[6] = rec_code(s, g, tb + l4, s16 + 9 + 2 * q);
                 nib[3] = rec_code(s, g, tb + 8 + l4, s16 + 8 + 2 * q);
                 nib[7] = rec_code(s, g, tb + 8 + l4, s16 + 9 + 2 * q);
-            } else {
-                const int d0 = 8 * (2 * iw) + l4, d1 = 8 * (2 * iw + 1) + l4;
-                nib[0] = rec_code(s, g, tb + 2 * q, d0);
-                nib[4] = rec_code(s, g, tb + 2 * q + 1, d0);
-                nib[1] = rec_code(s, g, tb + 8 + 2 * q, d0);
-                nib[5] = rec_code(s, g, tb + 9 + 2 * q, d0);
-                nib[2] = rec_code(s, g, tb + 2 * q, d1);
-                nib[6] = rec_code(s, g, tb + 2 * q + 1, d1);
-                nib[3] = rec_code(s, g, tb + 8 + 2 * q, d1);
-                nib[7] = rec_code(s, g, tb + 9 + 2 * q, d1);
+            } else {   // V word iw = m-tile of d (16*iw ..): the A fragment of O^T = V^T P'^T
+                const int d = 16 * iw + l4;
+                nib[0] = rec_code(s, g, tb + 2 * q, d);
+                nib[4] = rec_code(s, g, tb + 2 * q + 1, d);
+                nib[1] = rec_code(s, g, tb + 2 * q, d + 8);
+                nib[5] = rec_code(s, g, tb + 2 * q + 1, d + 8);
+                nib[2] = rec_code(s, g, tb + 8 + 2 * q, d);
+                nib[6] = rec_code(s, g, tb + 9 + 2 * q, d);
+                nib[3] = rec_code(s, g, tb + 8 + 2 * q, d + 8);
+                nib[7] = rec_code(s, g, tb + 9 + 2 * q, d + 8);
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) val |= nib[k] << (4 * k);
