@@ -257,7 +257,10 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     }
     if (total >= (int64_t(1) << 30)) return fail(c, PCK_EUNSUPPORTED, "too many tiles in one launch");
     const DecodeLaunchInfo& li = dinfo(c, fmt, D, fmt == PCK_FMT_MLX4G32 ? decode_ncb(p) : 1);
-    const int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS;
+    const int n_suf_warps = n * n_groups * ((S_suf + TILE_TOK - 1) / TILE_TOK);
+    // prefix workers and suffix warps together stay within one wave of resident warps
+    int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS - n_suf_warps;
+    if (max_warps < 1) max_warps = 1;
     int64_t tpw = (total + max_warps - 1) / max_warps;
     // at most ~32 prefix pieces per item, so that the merge stays short
     int vmax = 1;

@@ -123,7 +123,8 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
     const size_t slot_bytes = static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float);
     const int64_t max_slots = static_cast<int64_t>(NA_PARTIAL_BYTES / slot_bytes);
-    int64_t max_warps = static_cast<int64_t>(sp.sms) * li.ctas_per_sm * DECODE_WARPS;
+    int64_t max_warps = static_cast<int64_t>(sp.sms) * li.ctas_per_sm * DECODE_WARPS - n_groups * n_suf;
+    if (max_warps < 1) max_warps = 1;
     const int64_t fixed = n_groups + static_cast<int64_t>(n_groups) * n_suf;   // item + suffix slots
     if (fixed >= max_slots) return PCK_EUNSUPPORTED;
     if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;

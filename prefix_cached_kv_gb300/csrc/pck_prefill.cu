@@ -38,21 +38,22 @@ constexpr float PF_THRESH = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr float PF_LN2 = 0.69314718055994530942f;
 
 // Shared memory of one CTA, sized so that two CTAs fit on an SM (one's softmax overlaps the
-// other's MMAs): Q tile, a 2-stage K/V ring of 64-key blocks, the P tile, barriers.
+// other's MMAs): the Q tile and a 2-stage K/V ring of 64-key blocks. Tensor memory: two S
+// buffers (64 fp32 columns each; P of a block is written back over the first 32 columns of its
+// S buffer as packed fp16) and O (D columns).
 template <int D>
 struct PCfg {
     static constexpr int Q_BYTES = PF_ROWS * D * 2;
     static constexpr int KV_BYTES = PF_BLOCK * D * 2;        // K (or V) of one block
-    static constexpr int P_BYTES = PF_ROWS * PF_BLOCK * 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K0 = OFF_Q + Q_BYTES;
     static constexpr int OFF_V0 = OFF_K0 + KV_BYTES;
     static constexpr int OFF_K1 = OFF_V0 + KV_BYTES;
     static constexpr int OFF_V1 = OFF_K1 + KV_BYTES;
-    static constexpr int OFF_P = OFF_V1 + KV_BYTES;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;           // 8 mbarriers + tmem slot
+    static constexpr int OFF_BAR = OFF_V1 + KV_BYTES;         // 14 mbarriers + tmem slot
     static constexpr int SMEM = OFF_BAR + 128 + 128;          // + alignment slack (128 B)
-    static constexpr int S_COL = 0;                           // TMEM columns of S (64)
+    static constexpr int S_COL0 = 0;                          // TMEM columns of the S buffers
+    static constexpr int S_COL1 = PF_BLOCK;
     static constexpr int O_COL = 128;                         // TMEM columns of O (D)
     static constexpr int TMEM_COLS = 256;
 };
@@ -79,6 +80,14 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b
         "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
         ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// D (TMEM) += A (TMEM: row = lane, K packed two fp16 per 32-bit column) * B (shared memory)
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+        ::"r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -190,8 +199,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t bar = s_base + C::OFF_BAR;   // [0,1] full, [2,3] empty, [4] s_full, [5] p_full, [6] o_done, [7] final
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 64);
+    // mbarriers (8 B each): +0/+8 K full, +16/+24 V full, +32/+40 K free, +48/+56 V free (per
+    // stage), +64/+72 S full (per S buffer), +80 P ready (128 arrivals), +88 P.V done,
+    // +96 O final, +104 drain. K and V are released separately: K(b) once S(b) is done,
+    // V(b) once P(b).V(b) is done, so K(b+2) streams in while P.V(b) still runs.
+    const uint32_t bar = s_base + C::OFF_BAR;
+    constexpr int B_KF = 0, B_VF = 16, B_KE = 32, B_VE = 48, B_SF = 64, B_PR = 80, B_PV = 88, B_OF = 96, B_DR = 104;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 112);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- which rows
@@ -227,14 +241,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
 
     // ---- setup: barriers, TMEM, Q tile
     if (tid == 0) {
-        mbar_init(bar + 0, 1);
-        mbar_init(bar + 8, 1);
-        mbar_init(bar + 16, 1);
-        mbar_init(bar + 24, 1);
-        mbar_init(bar + 32, 1);
-        mbar_init(bar + 40, 128);
-        mbar_init(bar + 48, 1);
-        mbar_init(bar + 56, 1);
+        for (int k = 0; k < 14; ++k) mbar_init(bar + 8 * k, 8 * k == B_PR ? 128 : 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -270,57 +277,64 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         if (lane == 0) {
             for (int bi = 0; bi < nbl && !failed; ++bi) {
                 const int st = bi & 1;
-                if (bi >= 2 && !mbar_wait_bounded(bar + 16 + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
                 const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
                 const uint32_t bytes = kb.ntile * 32 * D;
-                mbar_arrive_expect_tx(bar + 8 * st, 2 * bytes);
-                bulk_g2s(s_base + (st ? C::OFF_K1 : C::OFF_K0), kb.k, bytes, bar + 8 * st);
-                bulk_g2s(s_base + (st ? C::OFF_V1 : C::OFF_V0), kb.v, bytes, bar + 8 * st);
+                if (bi >= 2 && !mbar_wait_bounded(bar + B_KE + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
+                mbar_arrive_expect_tx(bar + B_KF + 8 * st, bytes);
+                bulk_g2s(s_base + (st ? C::OFF_K1 : C::OFF_K0), kb.k, bytes, bar + B_KF + 8 * st);
+                if (bi >= 2 && !mbar_wait_bounded(bar + B_VE + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
+                mbar_arrive_expect_tx(bar + B_VF + 8 * st, bytes);
+                bulk_g2s(s_base + (st ? C::OFF_V1 : C::OFF_V0), kb.v, bytes, bar + B_VF + 8 * st);
             }
             if (failed) set_err(P.a.err, 2);
         }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
+        // S(b) = Q K(b)^T into S buffer b%2; after the softmax has written P(b) over it,
+        // O += P(b) V(b) with P read from tensor memory; S(b+2) reuses the buffer right after
+        // (the MMAs of one thread execute in issue order), so S(b+1) overlaps softmax(b).
         if (lane == 0) {
-            const uint32_t s_tm = tmem + C::S_COL, o_tm = tmem + C::O_COL;
-            int prev_ntile = 0;
-            for (int bi = 0; bi <= nbl && !failed; ++bi) {
-                if (bi < nbl) {
-                    const int st = bi & 1;
-                    if (!mbar_wait_bounded(bar + 8 * st, (bi >> 1) & 1)) { failed = true; break; }
+            const uint32_t o_tm = tmem + C::O_COL;
+            auto issue_S = [&](int bi) -> bool {
+                const int st = bi & 1;
+                if (!mbar_wait_bounded(bar + B_KF + 8 * st, (bi >> 1) & 1)) return false;
+                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
+                const uint32_t k_s = s_base + (st ? C::OFF_K1 : C::OFF_K0);
+                const uint32_t s_tm = tmem + (st ? C::S_COL1 : C::S_COL0);
+                const uint32_t idesc = idesc_f16(PF_ROWS, kb.ntile * TILE_TOK);
+                for (int s2 = 0; s2 < D / 16; ++s2) {
+                    const uint64_t a = sdesc(s_base + C::OFF_Q + s2 * 256, 128, 16 * D);
+                    const uint64_t bd = sdesc(k_s + s2 * 256, 128, 16 * D);
+                    umma_f16(s_tm, a, bd, idesc, s2 > 0 ? 1u : 0u);
                 }
-                if (bi > 0) {   // O += P(bi-1) V(bi-1) once the softmax has written P(bi-1)
-                    if (!mbar_wait_bounded(bar + 40, (bi - 1) & 1)) { failed = true; break; }
-                    tc_fence_after();
-                    const int pst = (bi - 1) & 1;
-                    const uint32_t v_s = s_base + (pst ? C::OFF_V1 : C::OFF_V0);
-                    const uint32_t idesc = idesc_f16(PF_ROWS, D);
-                    for (int u = 0; u < prev_ntile; ++u) {
-                        const uint64_t a = sdesc(s_base + C::OFF_P + u * 256, 128, (PF_BLOCK / 8) * 128);
-                        const uint64_t bd = sdesc(v_s + u * 32 * D, 128, 256);
-                        umma_f16(o_tm, a, bd, idesc, (bi - 1 > 0 || u > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar + 16 + 8 * pst);   // K/V stage free once these complete
-                    if (bi == nbl) umma_commit(bar + 48);   // O final
+                umma_commit(bar + B_SF + 8 * st);   // S ready for the softmax
+                umma_commit(bar + B_KE + 8 * st);   // K stage free
+                return true;
+            };
+            if (nbl > 0 && !issue_S(0)) failed = true;
+            if (!failed && nbl > 1 && !issue_S(1)) failed = true;
+            for (int bi = 0; bi < nbl && !failed; ++bi) {
+                if (!mbar_wait_bounded(bar + B_PR, bi & 1)) { failed = true; break; }   // P(bi) written
+                const int st = bi & 1;
+                if (!mbar_wait_bounded(bar + B_VF + 8 * st, (bi >> 1) & 1)) { failed = true; break; }
+                tc_fence_after();
+                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
+                const uint32_t v_s = s_base + (st ? C::OFF_V1 : C::OFF_V0);
+                const uint32_t p_tm = tmem + (st ? C::S_COL1 : C::S_COL0);
+                const uint32_t idesc = idesc_f16(PF_ROWS, D);
+                for (int u = 0; u < kb.ntile; ++u) {   // 16 keys (8 TMEM columns of P) per step
+                    const uint64_t bd = sdesc(v_s + u * 32 * D, 128, 256);
+                    umma_f16_ts(o_tm, p_tm + 8 * u, bd, idesc, (bi > 0 || u > 0) ? 1u : 0u);
                 }
-                if (bi < nbl) {   // S = Q K(b)^T
-                    const int st = bi & 1;
-                    const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
-                    const uint32_t k_s = s_base + (st ? C::OFF_K1 : C::OFF_K0);
-                    const uint32_t idesc = idesc_f16(PF_ROWS, kb.ntile * TILE_TOK);
-                    for (int s2 = 0; s2 < D / 16; ++s2) {
-                        const uint64_t a = sdesc(s_base + C::OFF_Q + s2 * 256, 128, 16 * D);
-                        const uint64_t bd = sdesc(k_s + s2 * 256, 128, 16 * D);
-                        umma_f16(s_tm, a, bd, idesc, s2 > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar + 32);
-                    prev_ntile = kb.ntile;
-                }
+                umma_commit(bar + B_VE + 8 * st);   // V stage free once these complete
+                umma_commit(bar + B_PV);            // P.V of block bi done
+                if (bi + 2 < nbl && !issue_S(bi + 2)) { failed = true; break; }
             }
+            umma_commit(bar + B_OF);                // O final (all earlier MMAs)
             if (failed) set_err(P.a.err, 3);
             // drain: make sure no MMA is still writing TMEM when the CTA releases it
-            umma_commit(bar + 56);
-            mbar_wait_bounded(bar + 56, 0);
+            umma_commit(bar + B_DR);
+            mbar_wait_bounded(bar + B_DR, 0);
         }
     } else {
         // ------------------------------------------------------------ softmax warps (row = tid)
@@ -329,14 +343,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         const int i = row_ok ? r % M : 0;
         const int suf_lim = P.a.causal ? (S - M + i) : (S - 1);   // last visible suffix key
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t s_tm = tmem + C::S_COL + lane_base, o_tm = tmem + C::O_COL + lane_base;
+        const uint32_t o_tm = tmem + C::O_COL + lane_base;
         const float sc = P.a.scale_log2;
         float m = -INFINITY, l = 0.f;
-        uint8_t* ps = smem + C::OFF_P;
-        const int R = tid >> 3, rr = tid & 7;
         for (int bi = 0; bi < nbl; ++bi) {
+            const int st = bi & 1;
+            const uint32_t s_tm = tmem + (st ? C::S_COL1 : C::S_COL0) + lane_base;
             // warp-uniform outcome: the tcgen05.ld below must be executed by the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + 32, bi & 1))) { failed = true; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_SF + 8 * st, (bi >> 1) & 1))) { failed = true; break; }
             tc_fence_after();
             const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
             const int lim = kb.is_suf ? min(kb.key0 + kb.ntile * TILE_TOK, suf_lim + 1) : min(kb.key0 + kb.ntile * TILE_TOK, N);
@@ -362,7 +376,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             if (__any_sync(0xffffffffu, need)) {
                 const float mnew = need ? mb : m;
                 const float alpha = need ? exp2f(m - mnew) : 1.0f;
-                if (bi > 0) {
+                if (bi > 0) {   // O must be quiet: wait for P.V of the previous block
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_PV, (bi - 1) & 1))) { failed = true; break; }
+                    tc_fence_after();
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
                         tmem_ld32(o_tm + c0, o);
@@ -394,17 +410,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                 }
             }
             l += lsum;
-#pragma unroll
-            for (int kc = 0; kc < PF_BLOCK / 8; ++kc)   // 8 keys (16 B) per core-matrix row
-                *reinterpret_cast<uint4*>(ps + (R * (PF_BLOCK / 8) + kc) * 128 + rr * 16) =
-                    make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-            fence_proxy_async_smem();
+            tmem_st32(s_tm, pk);   // P(bi) over the first 32 columns of its S buffer
             tc_fence_before();
-            mbar_arrive(bar + 40);
+            mbar_arrive(bar + B_PR);
         }
         if (failed) {
             set_err(P.a.err, 4);
-        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + 48, 0))) {
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_OF, 0))) {
             tc_fence_after();
             if (P.n_split == 1) {
                 const float inv = l > 0.f ? 1.0f / l : 0.f;
