@@ -7,21 +7,21 @@
 // j <= S_suf - M + i) in the same dispatch.
 //
 // One CTA owns 128 query rows of one kv head (the rows of its GQA q heads are packed:
-// row = local head * M + i) and walks all of that kv head's keys, prefix then suffix, in blocks
-// of up to 128 keys:
-//   * warp 5 (one lane) streams each key block's K and V with two cp.async.bulk copies into a
-//     2-stage shared-memory ring (the resident fp16 layout already is the operand layout);
-//   * warp 4 (one lane) issues tcgen05.mma (kind::f16, M=128, fp32 accumulators in TMEM):
-//     S = Q K^T (N = keys of the block, K-steps over d), then O += P V (one 16-key step per
-//     resident tile, N = D); completion goes to mbarriers through tcgen05.commit;
-//   * warps 0-3 (thread = row = TMEM lane) read S with tcgen05.ld, apply the causal / length
-//     mask, keep the running max m (base 2, tau*log2(e)-prescaled) and sum l, write
-//     P = 2^(s - m) as fp16 to shared memory in the A-operand layout, and finally read O,
-//     divide by l and write O and LSE = (m + log2 l) ln 2.
-// The running max is only moved when a block's max exceeds it by more than 8; O (in TMEM) is
-// then rescaled in place by the softmax warps, while no MMA touches it (the S-block commit
-// implies the previous P V has completed). Every wait is bounded: a stuck pipeline sets the
-// device error word and the CTA still releases its tensor memory.
+// row = local head * M + i) and walks a contiguous range of that kv head's key blocks (64 keys;
+// prefix then suffix); two CTAs share an SM, so one's softmax runs while the other's MMAs do:
+//   * warp 5 (one lane) streams each block's K and V with cp.async.bulk into 2-stage K and V
+//     rings (the resident fp16 layout already is the MMA operand layout);
+//   * warp 4 issues tcgen05.mma (kind::f16, M=128, fp32 accumulators in TMEM) from one
+//     elected lane: S = Q K^T into one of two S buffers (N = keys of the block, K-steps over
+//     d), then O += P V with P read back from TMEM; S(b+1) runs while the softmax works on S(b);
+//   * warps 0-3 (thread = row = TMEM lane) are the softmax: read S with tcgen05.ld, apply the
+//     causal / length mask, write P = 2^(s - m) as packed fp16 over S and keep the running sum
+//     l (fp32 pairs through the packed f32x2 instructions), and finally read O and write O / l
+//     and LSE = (m + log2 l) ln 2 (or the partial of the key range, merged by a second kernel).
+// The running max m (base 2, tau*log2(e)-prescaled) is only moved when a 32-key chunk's sum
+// exceeds 2^15 (which also bounds every P by 2^15, inside fp16): then O (in TMEM, once P.V of
+// the previous block is done), l and the chunk are rescaled. Every wait is bounded: a stuck
+// pipeline sets the device error word and the CTA still releases its tensor memory.
 #include <math.h>
 
 #include "pck_common.cuh"
@@ -34,27 +34,24 @@ namespace {
 constexpr int PF_ROWS = 128;          // query rows per CTA (MMA M)
 constexpr int PF_BLOCK = 64;          // keys per block (MMA N of S = Q K^T)
 constexpr int PF_THREADS = 192;       // 4 softmax warps + MMA warp + producer warp
-constexpr float PF_THRESH = 8.0f;     // lazy-rescale threshold (log2 units)
+constexpr int PF_MMA_WARP = 4, PF_LOAD_WARP = 5;
+constexpr int PF_ST = 2;              // K and V stages
 constexpr float PF_LN2 = 0.69314718055994530942f;
 
-// Shared memory of one CTA, sized so that two CTAs fit on an SM (one's softmax overlaps the
-// other's MMAs): the Q tile and a 2-stage K/V ring of 64-key blocks. Tensor memory: two S
-// buffers (64 fp32 columns each; P of a block is written back over the first 32 columns of its
-// S buffer as packed fp16) and O (D columns).
+// Shared memory of one CTA, sized so that two CTAs fit on an SM: the Q tile and 2-stage K and
+// V rings of 64-key blocks. Tensor memory: two S buffers (64 fp32 columns each; P of a block is
+// written back over the first 32 columns of its buffer as packed fp16) and O (D columns).
 template <int D>
 struct PCfg {
     static constexpr int Q_BYTES = PF_ROWS * D * 2;
-    static constexpr int KV_BYTES = PF_BLOCK * D * 2;        // K (or V) of one block
+    static constexpr int KV_BYTES = PF_BLOCK * D * 2;         // K (or V) of one block
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K0 = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V0 = OFF_K0 + KV_BYTES;
-    static constexpr int OFF_K1 = OFF_V0 + KV_BYTES;
-    static constexpr int OFF_V1 = OFF_K1 + KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V1 + KV_BYTES;         // 14 mbarriers + tmem slot
-    static constexpr int SMEM = OFF_BAR + 128 + 128;          // + alignment slack (128 B)
-    static constexpr int S_COL0 = 0;                          // TMEM columns of the S buffers
-    static constexpr int S_COL1 = PF_BLOCK;
-    static constexpr int O_COL = 128;                         // TMEM columns of O (D)
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + PF_ST * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + PF_ST * KV_BYTES;   // mbarriers + tmem slot
+    static constexpr int SMEM = OFF_BAR + 256 + 128;           // + alignment slack (128 B)
+    static constexpr int S_COL0 = 0, S_COL1 = PF_BLOCK;        // TMEM columns of the S buffers
+    static constexpr int O_COL = 2 * PF_BLOCK;                 // TMEM columns of O (D)
     static constexpr int TMEM_COLS = 256;
 };
 
@@ -75,23 +72,29 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// MMA (A and B from shared memory; or A from TMEM: row = lane, K packed two fp16 per 32-bit
+// column) and commit, issued by one elected lane of a converged warp. The issuing warp runs
+// its whole loop in step, so the descriptors stay warp-uniform values; computing them in
+// lane-divergent code made each MMA issue cost about a hundred cycles.
+__device__ __forceinline__ void umma_f16_elect(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+        "{ .reg .pred p, e; .reg .b32 rx; elect.sync rx|e, 0xffffffff; setp.ne.u32 p, %4, 0; "
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
         ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
-// D (TMEM) += A (TMEM: row = lane, K packed two fp16 per 32-bit column) * B (shared memory)
-__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void umma_f16_ts_elect(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+        "{ .reg .pred p, e; .reg .b32 rx; elect.sync rx|e, 0xffffffff; setp.ne.u32 p, %4, 0; "
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
         ::"r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{ .reg .pred e; .reg .b32 rx; elect.sync rx|e, 0xffffffff; "
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
+        ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -124,17 +127,71 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
         ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16-column load, waited
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- softmax arithmetic
+
+// two fp32 lanes in one 64-bit register (the packed f32x2 instructions of this architecture)
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t x;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    return x;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t x, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// P of one 32-key chunk of a row: p_j = 2^(s_j sc - m) for the nv visible keys (0 for the
+// rest), packed as fp16 pairs into pk; returns the fp32 sum of the p_j.
+template <bool FULL>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&v)[32], int nv, uint64_t sc2, float m, uint32_t (&pk)[16]) {
+    const uint64_t nm2 = f2_pack(-m, -m);
+    uint64_t acc0 = 0, acc1 = 0;   // (0.f, 0.f)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), sc2, nm2), x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (!FULL) {
+            p0 = 2 * j < nv ? p0 : 0.f;
+            p1 = 2 * j + 1 < nv ? p1 : 0.f;
+        }
+        if (j & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+        else acc0 = f2_add(acc0, f2_pack(p0, p1));
+        pk[j] = h2_as_u32(__floats2half2_rn(p0, p1));
+    }
+    float a, b, c, d;
+    f2_unpack(acc0, a, b);
+    f2_unpack(acc1, c, d);
+    return (a + b) + (c + d);
 }
 
 // ---------------------------------------------------------------- work description
@@ -199,13 +256,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t s_base = smem_u32(smem);
-    // mbarriers (8 B each): +0/+8 K full, +16/+24 V full, +32/+40 K free, +48/+56 V free (per
-    // stage), +64/+72 S full (per S buffer), +80 P ready (128 arrivals), +88 P.V done,
-    // +96 O final, +104 drain. K and V are released separately: K(b) once S(b) is done,
-    // V(b) once P(b).V(b) is done, so K(b+2) streams in while P.V(b) still runs.
+    // mbarriers (8 B each): K full / K free and V full / V free per stage, S full and P ready
+    // (128 arrivals) per S buffer, P.V done, O final, drain. K(b) is released once S(b) is done,
+    // V(b) once P(b).V is. No party can get a whole phase ahead of a waiter: the softmax arrives
+    // P(b+2) only after S(b+2), which the issuer starts after it has seen P(b); the producer
+    // refills a stage only after the issuer's commit for its previous contents.
     const uint32_t bar = s_base + C::OFF_BAR;
-    constexpr int B_KF = 0, B_VF = 16, B_KE = 32, B_VE = 48, B_SF = 64, B_PR = 80, B_PV = 88, B_OF = 96, B_DR = 104;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 112);
+    constexpr int B_KF = 0, B_KE = 16, B_VF = 32, B_VE = 48, B_SF = 64, B_PR = 80, B_PV = 96, B_OF = 104,
+                  B_DR = 112, N_BAR = 15;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * N_BAR);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- which rows
@@ -241,7 +300,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
 
     // ---- setup: barriers, TMEM, Q tile
     if (tid == 0) {
-        for (int k = 0; k < 14; ++k) mbar_init(bar + 8 * k, 8 * k == B_PR ? 128 : 1);
+        for (int k = 0; k < N_BAR; ++k) mbar_init(bar + 8 * k, (8 * k == B_PR || 8 * k == B_PR + 8) ? 128 : 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -272,70 +331,76 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     bool failed = false;
 
-    if (warp == 5) {
+    if (warp == PF_LOAD_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            for (int bi = 0; bi < nbl && !failed; ++bi) {
-                const int st = bi & 1;
-                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
+            for (int j = 0; j < nbl && !failed; ++j) {
+                const KeyBlock kb = key_block(P, g, kb0 + j, nbp, D);
                 const uint32_t bytes = kb.ntile * 32 * D;
-                if (bi >= 2 && !mbar_wait_bounded(bar + B_KE + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
+                const int st = j % PF_ST;
+                if (j >= PF_ST && !mbar_wait_bounded(bar + B_KE + 8 * st, (j / PF_ST - 1) & 1)) { failed = true; break; }
                 mbar_arrive_expect_tx(bar + B_KF + 8 * st, bytes);
-                bulk_g2s(s_base + (st ? C::OFF_K1 : C::OFF_K0), kb.k, bytes, bar + B_KF + 8 * st);
-                if (bi >= 2 && !mbar_wait_bounded(bar + B_VE + 8 * st, ((bi >> 1) - 1) & 1)) { failed = true; break; }
+                bulk_g2s(s_base + C::OFF_K + st * C::KV_BYTES, kb.k, bytes, bar + B_KF + 8 * st);
+                if (j >= PF_ST && !mbar_wait_bounded(bar + B_VE + 8 * st, (j / PF_ST - 1) & 1)) { failed = true; break; }
                 mbar_arrive_expect_tx(bar + B_VF + 8 * st, bytes);
-                bulk_g2s(s_base + (st ? C::OFF_V1 : C::OFF_V0), kb.v, bytes, bar + B_VF + 8 * st);
+                bulk_g2s(s_base + C::OFF_V + st * C::KV_BYTES, kb.v, bytes, bar + B_VF + 8 * st);
             }
             if (failed) set_err(P.a.err, 2);
         }
-    } else if (warp == 4) {
+    } else if (warp == PF_MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         // S(b) = Q K(b)^T into S buffer b%2; after the softmax has written P(b) over it,
         // O += P(b) V(b) with P read from tensor memory; S(b+2) reuses the buffer right after
-        // (the MMAs of one thread execute in issue order), so S(b+1) overlaps softmax(b).
-        if (lane == 0) {
-            const uint32_t o_tm = tmem + C::O_COL;
-            auto issue_S = [&](int bi) -> bool {
-                const int st = bi & 1;
-                if (!mbar_wait_bounded(bar + B_KF + 8 * st, (bi >> 1) & 1)) return false;
-                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
-                const uint32_t k_s = s_base + (st ? C::OFF_K1 : C::OFF_K0);
-                const uint32_t s_tm = tmem + (st ? C::S_COL1 : C::S_COL0);
-                const uint32_t idesc = idesc_f16(PF_ROWS, kb.ntile * TILE_TOK);
-                for (int s2 = 0; s2 < D / 16; ++s2) {
-                    const uint64_t a = sdesc(s_base + C::OFF_Q + s2 * 256, 128, 16 * D);
-                    const uint64_t bd = sdesc(k_s + s2 * 256, 128, 16 * D);
-                    umma_f16(s_tm, a, bd, idesc, s2 > 0 ? 1u : 0u);
-                }
-                umma_commit(bar + B_SF + 8 * st);   // S ready for the softmax
-                umma_commit(bar + B_KE + 8 * st);   // K stage free
-                return true;
-            };
-            if (nbl > 0 && !issue_S(0)) failed = true;
-            if (!failed && nbl > 1 && !issue_S(1)) failed = true;
-            for (int bi = 0; bi < nbl && !failed; ++bi) {
-                if (!mbar_wait_bounded(bar + B_PR, bi & 1)) { failed = true; break; }   // P(bi) written
-                const int st = bi & 1;
-                if (!mbar_wait_bounded(bar + B_VF + 8 * st, (bi >> 1) & 1)) { failed = true; break; }
-                tc_fence_after();
-                const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
-                const uint32_t v_s = s_base + (st ? C::OFF_V1 : C::OFF_V0);
-                const uint32_t p_tm = tmem + (st ? C::S_COL1 : C::S_COL0);
-                const uint32_t idesc = idesc_f16(PF_ROWS, D);
-                for (int u = 0; u < kb.ntile; ++u) {   // 16 keys (8 TMEM columns of P) per step
-                    const uint64_t bd = sdesc(v_s + u * 32 * D, 128, 256);
-                    umma_f16_ts(o_tm, p_tm + 8 * u, bd, idesc, (bi > 0 || u > 0) ? 1u : 0u);
-                }
-                umma_commit(bar + B_VE + 8 * st);   // V stage free once these complete
-                umma_commit(bar + B_PV);            // P.V of block bi done
-                if (bi + 2 < nbl && !issue_S(bi + 2)) { failed = true; break; }
+        // (the MMAs of one thread execute in issue order), so S(b+1) overlaps softmax(b). The
+        // whole warp walks the loop; lane 0 (elected) issues. Descriptors are built once and
+        // advanced by adds (the start address field counts 16-byte units).
+        const uint32_t o_tm = tmem + C::O_COL;
+        const uint64_t q_desc = sdesc(s_base + C::OFF_Q, 128, 16 * D);
+        const uint64_t k_desc = sdesc(s_base + C::OFF_K, 128, 16 * D);
+        const uint64_t v_desc = sdesc(s_base + C::OFF_V, 128, 256);
+        const uint32_t idesc_pv = idesc_f16(PF_ROWS, D);
+        constexpr int TPB = PF_BLOCK / TILE_TOK;
+        auto ntile_of = [&](int bi) -> int {
+            const int b = kb0 + bi;
+            return b < nbp ? min(TPB, P.a.ntiles - b * TPB) : min(TPB, P.suf_ntiles - (b - nbp) * TPB);
+        };
+        auto issue_S = [&](int bi) -> bool {
+            const int st = bi % PF_ST;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_KF + 8 * st, (bi / PF_ST) & 1))) return false;
+            const uint32_t idesc = idesc_f16(PF_ROWS, ntile_of(bi) * TILE_TOK);
+            const uint64_t kd = k_desc + static_cast<uint64_t>((st * C::KV_BYTES) >> 4);
+            const uint32_t s_tm = tmem + ((bi & 1) ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+            for (int s2 = 0; s2 < D / 16; ++s2) umma_f16_elect(s_tm, q_desc + 16 * s2, kd + 16 * s2, idesc, s2 > 0 ? 1u : 0u);
+            umma_commit_elect(bar + B_SF + 8 * (bi & 1));   // S ready for the softmax
+            umma_commit_elect(bar + B_KE + 8 * st);         // K stage free
+            return true;
+        };
+        if (nbl > 0 && !issue_S(0)) failed = true;
+        if (!failed && nbl > 1 && !issue_S(1)) failed = true;
+        for (int bi = 0; bi < nbl && !failed; ++bi) {
+            const int st = bi % PF_ST;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_PR + 8 * (bi & 1), (bi >> 1) & 1) &&   // P(bi) written
+                                             mbar_wait_bounded(bar + B_VF + 8 * st, (bi / PF_ST) & 1))) {
+                failed = true;
+                break;
             }
-            umma_commit(bar + B_OF);                // O final (all earlier MMAs)
-            if (failed) set_err(P.a.err, 3);
-            // drain: make sure no MMA is still writing TMEM when the CTA releases it
-            umma_commit(bar + B_DR);
-            mbar_wait_bounded(bar + B_DR, 0);
+            tc_fence_after();
+            const int nt = ntile_of(bi);
+            const uint64_t vd = v_desc + static_cast<uint64_t>((st * C::KV_BYTES) >> 4);
+            const uint32_t p_tm = tmem + ((bi & 1) ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+            for (int u = 0; u < TPB; ++u)   // 16 keys (8 TMEM columns of P) per step
+                if (u < nt) umma_f16_ts_elect(o_tm, p_tm + 8 * u, vd + ((u * 32 * D) >> 4), idesc_pv, (bi > 0 || u > 0) ? 1u : 0u);
+            umma_commit_elect(bar + B_VE + 8 * st);   // V stage free once these complete
+            umma_commit_elect(bar + B_PV);            // P.V of block bi done
+            if (bi + 2 < nbl && !issue_S(bi + 2)) { failed = true; break; }
         }
+        umma_commit_elect(bar + B_OF);                // O final (all earlier MMAs)
+        if (failed && lane == 0) set_err(P.a.err, 3);
+        // drain: make sure no MMA is still writing TMEM when the CTA releases it
+        umma_commit_elect(bar + B_DR);
+        __all_sync(0xffffffffu, mbar_wait_bounded(bar + B_DR, 0));
     } else {
         // ------------------------------------------------------------ softmax warps (row = tid)
         const int r = row0 + tid;
@@ -345,74 +410,79 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t o_tm = tmem + C::O_COL + lane_base;
         const float sc = P.a.scale_log2;
+        const uint64_t sc2 = f2_pack(sc, sc);
         float m = -INFINITY, l = 0.f;
         for (int bi = 0; bi < nbl; ++bi) {
-            const int st = bi & 1;
-            const uint32_t s_tm = tmem + (st ? C::S_COL1 : C::S_COL0) + lane_base;
+            const uint32_t s_tm = tmem + ((bi & 1) ? C::S_COL1 : C::S_COL0) + lane_base;
             // warp-uniform outcome: the tcgen05.ld below must be executed by the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_SF + 8 * st, (bi >> 1) & 1))) { failed = true; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_SF + 8 * (bi & 1), (bi >> 1) & 1))) { failed = true; break; }
             tc_fence_after();
             const KeyBlock kb = key_block(P, g, kb0 + bi, nbp, D);
-            const int lim = kb.is_suf ? min(kb.key0 + kb.ntile * TILE_TOK, suf_lim + 1) : min(kb.key0 + kb.ntile * TILE_TOK, N);
-            const int nvalid = row_ok ? max(0, lim - kb.key0) : 0;   // keys [key0, key0 + nvalid) visible
             const int ncols = kb.ntile * TILE_TOK;
-            // one pass over S: both 32-column loads in flight, one wait
-            uint32_t v[PF_BLOCK];
-            tmem_ld32_nowait(s_tm, v);
-            if (ncols > 32) tmem_ld32_nowait(s_tm + 32, v + 32);
+            const int lim = kb.is_suf ? min(kb.key0 + ncols, suf_lim + 1) : min(kb.key0 + ncols, N);
+            const int nvalid = row_ok ? max(0, lim - kb.key0) : 0;   // keys [key0, key0 + nvalid) visible
+            const int nch = (ncols + 31) >> 5;
+            uint32_t v[PF_BLOCK / 32][32];
+#pragma unroll
+            for (int c = 0; c < PF_BLOCK / 32; ++c)
+                if (c < nch) tmem_ld32_nowait(s_tm + 32 * c, v[c]);
             tmem_wait_ld();
-            const bool full = nvalid == PF_BLOCK;   // every key of the block visible to this row
-            float bmax = -INFINITY;
-            if (full) {
+            float lsum = 0.f;   // this block's sum at the current m
 #pragma unroll
-                for (int j = 0; j < PF_BLOCK; ++j) bmax = fmaxf(bmax, __uint_as_float(v[j]));
-            } else {
+            for (int c = 0; c < PF_BLOCK / 32; ++c) {
+                if (c >= nch) break;
+                const int nv = nvalid - 32 * c;   // visible keys of this chunk (<= 0 .. >= 32)
+                uint32_t pk[16];
+                float cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
+                // A sum <= 2^15 bounds every p_j by 2^15: they fit fp16 and m may stay. Otherwise
+                // (or on the first chunk, where m = -inf and the sum is infinite) move m to the
+                // chunk's max, rescale what was summed or written with the old m, and redo.
+                const bool need = !(cs <= 32768.f);
+                if (__any_sync(0xffffffffu, need)) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < PF_BLOCK; ++j)
-                    if (j < nvalid) bmax = fmaxf(bmax, __uint_as_float(v[j]));
-            }
-            const float mb = bmax * sc;
-            const bool need = mb > m + PF_THRESH;
-            if (__any_sync(0xffffffffu, need)) {
-                const float mnew = need ? mb : m;
-                const float alpha = need ? exp2f(m - mnew) : 1.0f;
-                if (bi > 0) {   // O must be quiet: wait for P.V of the previous block
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_PV, (bi - 1) & 1))) { failed = true; break; }
-                    tc_fence_after();
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(o_tm + c0, o);
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nv) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(v[c][j]));
+                    const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+                    const float mnew = need ? fmaxf(m, cm) : m;
+                    const float alpha = need ? exp2f(m - mnew) : 1.0f;
+                    if (bi > 0) {   // O must be quiet: wait for P.V of the previous block
+                        if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_PV, (bi - 1) & 1))) { failed = true; break; }
+                        tc_fence_after();
+                        for (int c0 = 0; c0 < D; c0 += 16) {
+                            uint32_t o[16];
+                            tmem_ld16(o_tm + c0, o);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        tmem_st32(o_tm + c0, o);
+                            for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                            tmem_st16_nowait(o_tm + c0, o);
+                        }
                     }
-                }
-                l *= alpha;
-                m = mnew;
-            }
-            uint32_t pk[PF_BLOCK / 2];
-            float lsum = 0.f;
-            if (full) {
+                    if (c > 0) {    // P of the earlier chunks, written over columns [0, 16c)
+                        tmem_wait_st();
+                        const __half2 a2 = __float2half2_rn(alpha);
+                        for (int c1 = 0; c1 < c; ++c1) {
+                            uint32_t q[16];
+                            tmem_ld16(s_tm + 16 * c1, q);
 #pragma unroll
-                for (int j = 0; j < PF_BLOCK; j += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m));
-                    lsum += p0 + p1;
-                    pk[j >> 1] = h2_as_u32(__floats2half2_rn(p0, p1));
+                            for (int j = 0; j < 16; ++j) q[j] = h2_as_u32(__hmul2(u32_as_h2(q[j]), a2));
+                            tmem_st16_nowait(s_tm + 16 * c1, q);
+                        }
+                    }
+                    tmem_wait_st();
+                    lsum *= alpha;
+                    l *= alpha;
+                    m = mnew;
+                    cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < PF_BLOCK; j += 2) {
-                    const float p0 = j < nvalid ? ex2_approx(fmaf(__uint_as_float(v[j]), sc, -m)) : 0.f;
-                    const float p1 = j + 1 < nvalid ? ex2_approx(fmaf(__uint_as_float(v[j + 1]), sc, -m)) : 0.f;
-                    lsum += p0 + p1;
-                    pk[j >> 1] = h2_as_u32(__floats2half2_rn(p0, p1));
-                }
+                lsum += cs;
+                // P of this chunk's 32 keys over columns [16c, 16c + 16): S there was read already
+                tmem_st16_nowait(s_tm + 16 * c, pk);
             }
+            if (failed) break;
+            tmem_wait_st();
             l += lsum;
-            tmem_st32(s_tm, pk);   // P(bi) over the first 32 columns of its S buffer
             tc_fence_before();
-            mbar_arrive(bar + B_PR);
+            mbar_arrive(bar + B_PR + 8 * (bi & 1));
         }
         if (failed) {
             set_err(P.a.err, 4);
@@ -434,8 +504,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                 }
                 if (row_ok && P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
             } else {   // partial [m, l, -, -, o unnormalised] of this key range, merged later
-                float* prow = P.partials +
-                              ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * partial_stride(D);
+                float* prow = P.partials + ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * partial_stride(D);
                 if (row_ok) { prow[0] = m; prow[1] = l; }
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t v[32];
