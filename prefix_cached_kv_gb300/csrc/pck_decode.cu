@@ -498,8 +498,11 @@ __device__ __forceinline__ int item_pieces(const DecodeParams& p, int item) {
     return (e - 1) / p.tpw - s / p.tpw + 1;
 }
 
-// Merge of one (item, q head): lanes over pieces for the max and the normaliser, then lanes
-// over d with the pieces' weights broadcast by shuffles. Partials are read through L2 (__ldcg).
+// Merge of one (item, q head). Pieces are taken in batches of BP (BP * D / 4 float4 of o per
+// batch, 16 per lane); all of a batch's loads (m and l of the lane's piece, and every o) are
+// issued before any is used, so a batch costs one L2 round trip. Batches are combined with an
+// online rescale; within a batch the weights 2^(m_k - M) are broadcast by shuffles. Partials are
+// read through L2 (__ldcg).
 template <int D>
 __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane) {
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
@@ -515,55 +518,59 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
         const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
         return p.partials + (size_t)slot * PSTR + h * partial_stride(D);
     };
-    float M = -INFINITY;
-    for (int k = lane; k < npieces; k += 32) M = fmaxf(M, __ldcg(piece(k)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    // weights and normaliser: lanes over pieces
-    float L = 0.f;
-    // o: a warp step covers PPS pieces, each read by D/4 lanes as float4 (lane -> piece
-    // k0 + lane / (D/4), d = 4 * (lane % (D/4))); D = 256 uses two float4 per lane.
-    constexpr int LPP = D / 4 > 32 ? 32 : D / 4;      // lanes per piece
-    constexpr int PPS = 32 / LPP;                     // pieces per warp step
-    constexpr int V4 = D / 4 / LPP;                   // float4 per lane per piece
+    constexpr int LPP = D / 4 > 32 ? 32 : D / 4;   // lanes per piece (one float4 of d each)
+    constexpr int PPS = 32 / LPP;                  // pieces per warp-wide load
+    constexpr int V4 = D / 4 / LPP;                // float4 per lane per piece
+    constexpr int NB = 16 / V4;                    // warp-wide loads per batch
+    constexpr int BP = NB * PPS;                   // pieces per batch (32, 16, 8 for D = 64, 128, 256)
     const int sub = lane / LPP, dl = lane % LPP;
+    float M = -INFINITY, L = 0.f;                  // L: this lane's share (lanes over pieces)
     float4 acc[V4];
 #pragma unroll
     for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < npieces; c += 32) {
-        float wk = 0.f;
-        if (c + lane < npieces) {
-            const float* ph = piece(c + lane);
-            const float mk = __ldcg(ph);
-            wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
-            L = fmaf(wk, __ldcg(ph + 1), L);
+    for (int c = 0; c < npieces; c += BP) {
+        const int nk = min(BP, npieces - c);
+        float mk = -INFINITY, lk = 0.f;
+        if (lane < nk) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(piece(c + lane)));
+            mk = ml.x;
+            lk = ml.y;
         }
-        const int nk = min(32, npieces - c);
-        constexpr int BATCH = 16 / PPS > 0 ? 16 / PPS : 1;   // warp steps whose loads are in flight together
-        for (int j0 = 0; j0 < nk; j0 += BATCH * PPS) {
-            float4 xs[BATCH][V4];
+        float4 xs[NB][V4];
 #pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                const int jj = j0 + b * PPS + sub;
-                if (jj < nk) {
-                    const float4* ph = reinterpret_cast<const float4*>(piece(c + jj) + PARTIAL_O) + dl;
+        for (int b = 0; b < NB; ++b) {
+            const int jj = b * PPS + sub;
+            if (jj < nk) {
+                const float4* ph = reinterpret_cast<const float4*>(piece(c + jj) + PARTIAL_O) + dl;
 #pragma unroll
-                    for (int v = 0; v < V4; ++v) xs[b][v] = __ldcg(ph + v * LPP);
-                } else {
+                for (int v = 0; v < V4; ++v) xs[b][v] = __ldcg(ph + v * LPP);
+            } else {
 #pragma unroll
-                    for (int v = 0; v < V4; ++v) xs[b][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                for (int v = 0; v < V4; ++v) xs[b][v] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        }
+        float Mb = mk;
 #pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                const float w = __shfl_sync(0xffffffffu, wk, (j0 + b * PPS + sub) & 31);
+        for (int o = 16; o > 0; o >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+        const float Mn = fmaxf(M, Mb);
+        if (Mn != -INFINITY) {
+            const float r = M == -INFINITY ? 0.f : exp2f(M - Mn);   // rescale of earlier batches
+            L *= r;
 #pragma unroll
-                for (int v = 0; v < V4; ++v) {
-                    acc[v].x = fmaf(w, xs[b][v].x, acc[v].x);
-                    acc[v].y = fmaf(w, xs[b][v].y, acc[v].y);
-                    acc[v].z = fmaf(w, xs[b][v].z, acc[v].z);
-                    acc[v].w = fmaf(w, xs[b][v].w, acc[v].w);
-                }
+            for (int v = 0; v < V4; ++v) { acc[v].x *= r; acc[v].y *= r; acc[v].z *= r; acc[v].w *= r; }
+            M = Mn;
+        }
+        const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+        L = fmaf(wk, lk, L);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float w = __shfl_sync(0xffffffffu, wk, (b * PPS + sub) & 31);
+#pragma unroll
+            for (int v = 0; v < V4; ++v) {
+                acc[v].x = fmaf(w, xs[b][v].x, acc[v].x);
+                acc[v].y = fmaf(w, xs[b][v].y, acc[v].y);
+                acc[v].z = fmaf(w, xs[b][v].z, acc[v].z);
+                acc[v].w = fmaf(w, xs[b][v].w, acc[v].w);
             }
         }
     }
