@@ -488,35 +488,35 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             set_err(P.a.err, 4);
         } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_OF, 0))) {
             tc_fence_after();
-            if (P.n_split == 1) {
-                const float inv = l > 0.f ? 1.0f / l : 0.f;
-                float* orow = row_ok ? P.a.O + ((size_t)wg.qh[r / M] * M + i) * D : nullptr;
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(o_tm + c0, v);
-                    if (row_ok) {
+            // The row goes out through shared memory (the Q, K and V buffers are idle now that
+            // every MMA has completed): the thread writes it there (a 132- or 68-word row
+            // stride, so a quarter-warp's float4 stores hit 32 different banks) and sends it with
+            // one bulk copy, instead of strided float4 stores to global memory.
+            const bool fin = P.n_split == 1;
+            const float inv = fin ? (l > 0.f ? 1.0f / l : 0.f) : 1.0f;
+            constexpr int RS = partial_stride(D);   // floats per staged row
+            float* srow = reinterpret_cast<float*>(smem) + (size_t)tid * RS;
+            srow[0] = m;
+            srow[1] = l;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(o_tm + c0, v);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(orow + c0 + j) =
-                                make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
-                                            __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
-                    }
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(srow + PARTIAL_O + c0 + j) =
+                        make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
+                                    __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+            }
+            if (row_ok) {
+                fence_proxy_async_smem();   // this thread's writes, before its own bulk copy reads them
+                if (fin) {   // O row, and LSE
+                    bulk_s2g(P.a.O + ((size_t)wg.qh[r / M] * M + i) * D, smem_u32(srow + PARTIAL_O), D * 4);
+                    if (P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
+                } else {     // partial [m, l, -, -, o unnormalised] of this key range, merged later
+                    bulk_s2g(P.partials + ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * RS, smem_u32(srow),
+                             RS * 4);
                 }
-                if (row_ok && P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
-            } else {   // partial [m, l, -, -, o unnormalised] of this key range, merged later
-                float* prow = P.partials + ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * partial_stride(D);
-                if (row_ok) { prow[0] = m; prow[1] = l; }
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(o_tm + c0, v);
-                    if (row_ok) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(prow + PARTIAL_O + c0 + j) =
-                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                    }
-                }
+                bulk_s2g_wait();
             }
         } else {
             set_err(P.a.err, 5);
@@ -528,9 +528,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
 }
 
-// Merge of the key-range partials of each row: one warp per row, lanes over d (float4).
+// Merge of the key-range partials of each row: one warp per row, lanes over d (float4). Small
+// per-warp state (4 splits per batch) keeps 48 warps on an SM, so many rows' loads are in flight.
 template <int D>
-__global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PfParams P) {
+__global__ void __launch_bounds__(256, 6) prefill_merge_kernel(const __grid_constant__ PfParams P) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int rows = P.n_tiles * PF_ROWS;
@@ -545,22 +546,44 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
         if (r >= wg.nq * M) continue;
         const float* base = P.partials + ((size_t)tile * P.n_split * PF_ROWS + rr) * partial_stride(D);
         const size_t sstride = (size_t)PF_ROWS * partial_stride(D);
-        float ms = -INFINITY, ls = 0.f;
-        if (lane < P.n_split) { ms = __ldcg(base + lane * sstride); ls = __ldcg(base + lane * sstride + 1); }
-        float Mx = ms;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-        const float w = (lane < P.n_split && ms != -INFINITY) ? exp2f(ms - Mx) : 0.f;
-        float L = w * ls;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        // splits in batches of 4: a batch's (m, l) and o loads are all issued before any is used
+        constexpr int NBS = 4;
+        float Mx = -INFINITY, L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 0; sp < P.n_split; ++sp) {
-            const float ws = __shfl_sync(0xffffffffu, w, sp);
-            if (lane < LPP) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(base + sp * sstride + PARTIAL_O) + lane);
-                acc.x = fmaf(ws, x.x, acc.x); acc.y = fmaf(ws, x.y, acc.y);
-                acc.z = fmaf(ws, x.z, acc.z); acc.w = fmaf(ws, x.w, acc.w);
+        for (int c = 0; c < P.n_split; c += NBS) {
+            const int nk = min(NBS, P.n_split - c);
+            float ms = -INFINITY, ls = 0.f;
+            if (lane < nk) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + (c + lane) * sstride));
+                ms = ml.x;
+                ls = ml.y;
+            }
+            float4 xs[NBS];
+#pragma unroll
+            for (int k = 0; k < NBS; ++k)
+                xs[k] = (k < nk && lane < LPP)
+                            ? __ldcg(reinterpret_cast<const float4*>(base + (c + k) * sstride + PARTIAL_O) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            float Mb = ms;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+            const float Mn = fmaxf(Mx, Mb);
+            if (Mn != -INFINITY) {
+                const float rs = Mx == -INFINITY ? 0.f : exp2f(Mx - Mn);   // rescale of earlier batches
+                L *= rs;
+                acc.x *= rs; acc.y *= rs; acc.z *= rs; acc.w *= rs;
+                Mx = Mn;
+            }
+            const float w = ms == -INFINITY ? 0.f : exp2f(ms - Mx);
+            float Lb = w * ls;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Lb += __shfl_xor_sync(0xffffffffu, Lb, o);
+            L += Lb;
+#pragma unroll
+            for (int k = 0; k < NBS; ++k) {
+                const float ws = __shfl_sync(0xffffffffu, w, k);
+                acc.x = fmaf(ws, xs[k].x, acc.x); acc.y = fmaf(ws, xs[k].y, acc.y);
+                acc.z = fmaf(ws, xs[k].z, acc.z); acc.w = fmaf(ws, xs[k].w, acc.w);
             }
         }
         const int h = wg.qh[r / M], i = r % M;
@@ -583,18 +606,23 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    prefill_kernel<D><<<P.n_tiles * P.n_split, PF_THREADS, C::SMEM, st>>>(P);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || P.n_split == 1) return e;
+    // The merge is launched programmatically (PDL) and waits for the attention grid as a whole.
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.n_tiles * P.n_split);
+    cfg.blockDim = dim3(PF_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, P);
+    if (e != cudaSuccess || P.n_split == 1) return e;
     const int rows = P.n_tiles * PF_ROWS;
     cfg.gridDim = dim3((rows + 7) / 8);
     cfg.blockDim = dim3(256);
-    cfg.stream = st;
-    cudaLaunchAttribute attr2[1];
-    attr2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr2[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr2;
+    cfg.dynamicSmemBytes = 0;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, P);
 }
