@@ -11,7 +11,8 @@
  * Conventions for every call:
  *  - Tensor pointers (Q, O, LSE, K, V, K_suf, V_suf, records, idx_out) are DEVICE pointers
  *    on the context's device, caller-owned, contiguous, and must stay valid until the stream
- *    reaches the call. O, K, V and Q must be 16-byte aligned (PCK_EINVAL otherwise). head_map is a small HOST array (int32[H_q], entries in [0, H_kv));
+ *    reaches the call. O, K, V and Q must be 16-byte aligned, and K_suf / V_suf too when M > 1
+ *    (PCK_EINVAL otherwise). head_map is a small HOST array (int32[H_q], entries in [0, H_kv));
  *    NULL means the grouped default h / (H_q / H_kv).
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default stream.
  *  - Calls are asynchronous on `stream`. Argument, shape and slot errors are detected on the

@@ -519,6 +519,8 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs an fp16 slot");
     if (q_dtype != PCK_DT_F16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs fp16 Q");
     if (reinterpret_cast<uintptr_t>(Q) & 15) return fail(c, PCK_EINVAL, "Q must be 16-byte aligned");
+    if (S_suf > 0 && ((reinterpret_cast<uintptr_t>(K_suf) | reinterpret_cast<uintptr_t>(V_suf)) & 15))
+        return fail(c, PCK_EINVAL, "K_suf/V_suf must be 16-byte aligned when M > 1");
     if (!prefill_supported(D)) return fail(c, PCK_EUNSUPPORTED, "M>1 kernel not available for D=%d", D);
     if (S_suf > 0 && static_cast<size_t>(s->H_kv) * 2 * fp16_region_bytes((S_suf + TILE_TOK - 1) / TILE_TOK, D) >
                          WS_SUFFIX_BYTES)

@@ -123,42 +123,51 @@ __global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __res
 
 // ------------------------------------------------------------------ fp16 re-layout
 
-// One thread per output u32 of a kv head's regions (K region 8*D*ntiles u32, then V region).
+// One CTA per (16-token tile j, kv head g). K and V rows t0..t0+15 are loaded coalesced into
+// shared memory (zeros past N; rows padded by 16 bytes so the column reads below spread over
+// the banks), then the tile's two 32*D-byte pieces of the resident layout are written with
+// consecutive 16-byte stores: the K piece as core matrices [token group][d chunk] (16 bytes =
+// 8 consecutive d of one token), the V piece as core matrices [d group][key chunk] (16 bytes =
+// 8 consecutive keys of one d).
 template <typename SrcT>
-__global__ void __launch_bounds__(256) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
-                                                            int H_kv, int N, int D, int ntiles,
-                                                            uint32_t* __restrict__ out) {
-    const int64_t region = (int64_t)ntiles * 8 * D;           // u32 per region
-    const int64_t total = (int64_t)H_kv * 2 * region;
-    const int cpt = D / 8;                                    // d chunks (K) / d groups (V)
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int g = static_cast<int>(i / (2 * region));
-        const int64_t w = i - (int64_t)g * 2 * region;
-        const bool isV = w >= region;
-        const int64_t wl = isV ? w - region : w;
-        const int64_t ci = wl >> 5;                           // core matrix index
-        const int wi = static_cast<int>(wl & 31);             // word within the core (= lane)
-        const int r = wi >> 2, e = 2 * (wi & 3);
-        int t0, t1, d0, d1;
-        if (!isV) {
-            const int64_t T = ci / cpt;
-            const int c = static_cast<int>(ci - T * cpt);
-            t0 = t1 = static_cast<int>(8 * T + r);
-            d0 = 8 * c + e;
-            d1 = d0 + 1;
+__global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
+                                                            int N, int D, int ntiles, uint4* __restrict__ out) {
+    constexpr int MAXD = 256;
+    __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
+    const int j = blockIdx.x, g = blockIdx.y;
+    const int t0 = j * TILE_TOK;
+    for (int x = 0; x < 2; ++x) {
+        const SrcT* src = (x ? V : K) + (int64_t)g * N * D;
+        if constexpr (sizeof(SrcT) == 2) {
+            for (int q = threadIdx.x; q < TILE_TOK * D / 8; q += blockDim.x) {
+                const int tok = q / (D / 8), c = q - tok * (D / 8);
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                if (t0 + tok < N) val = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(t0 + tok) * D + 8 * c));
+                *reinterpret_cast<uint4*>(&sm[x][tok][8 * c]) = val;
+            }
         } else {
-            const int64_t j = ci / (2 * cpt);
-            const int cc = static_cast<int>(ci - j * 2 * cpt);
-            const int dg = cc >> 1, tc = cc & 1;
-            d0 = d1 = 8 * dg + r;
-            t0 = static_cast<int>(16 * j + 8 * tc + e);
-            t1 = t0 + 1;
+            for (int q = threadIdx.x; q < TILE_TOK * D; q += blockDim.x) {
+                const int tok = q / D, d = q - tok * D;
+                sm[x][tok][d] = __float2half_rn(t0 + tok < N ? static_cast<float>(src[(int64_t)(t0 + tok) * D + d]) : 0.f);
+            }
         }
-        const SrcT* src = isV ? V : K;
-        float v0 = t0 < N ? static_cast<float>(src[((int64_t)g * N + t0) * D + d0]) : 0.f;
-        float v1 = t1 < N ? static_cast<float>(src[((int64_t)g * N + t1) * D + d1]) : 0.f;
-        out[i] = h2_as_u32(__floats2half2_rn(v0, v1));
+    }
+    __syncthreads();
+    const int64_t piece = 2 * D;                              // uint4 per tile piece (32 * D bytes)
+    uint4* kout = out + ((int64_t)g * 2 * ntiles + j) * piece;
+    uint4* vout = out + ((int64_t)g * 2 * ntiles + ntiles + j) * piece;
+    const int cpt = D / 8;                                    // d chunks (K) / d groups (V)
+    for (int u = threadIdx.x; u < piece; u += blockDim.x) {
+        const int core = u >> 3, row = u & 7;
+        const int T = core / cpt, c = core - T * cpt;         // K core: token group T, d chunk c
+        kout[u] = *reinterpret_cast<const uint4*>(&sm[0][8 * T + row][8 * c]);
+        const int dg = core >> 1, tc = core & 1, d = 8 * dg + row;   // V core: d group, key chunk
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k][d])) |
+                   (static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k + 1][d])) << 16);
+        vout[u] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -278,14 +287,15 @@ cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim
 
 cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
                                  void* out, cudaStream_t st, int sms) {
-    int64_t total = (int64_t)H_kv * ntiles * 16 * D;
-    int blocks = grid_for(total, 256, sms);
+    (void)sms;
+    if (D > 256 || D % 8 != 0) return cudaErrorInvalidValue;
+    const dim3 grid(ntiles, H_kv);
     if (src_f16)
-        relayout_fp16_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half*>(K), static_cast<const __half*>(V),
-                                                             H_kv, N, D, ntiles, static_cast<uint32_t*>(out));
+        relayout_fp16_kernel<__half><<<grid, 128, 0, st>>>(static_cast<const __half*>(K), static_cast<const __half*>(V),
+                                                           N, D, ntiles, static_cast<uint4*>(out));
     else
-        relayout_fp16_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(K), static_cast<const float*>(V),
-                                                            H_kv, N, D, ntiles, static_cast<uint32_t*>(out));
+        relayout_fp16_kernel<float><<<grid, 128, 0, st>>>(static_cast<const float*>(K), static_cast<const float*>(V),
+                                                          N, D, ntiles, static_cast<uint4*>(out));
     return cudaGetLastError();
 }
 
