@@ -334,7 +334,7 @@ def row_sparse(ctx, torch, pk, reps=10):
     return {"workload": "sparse_topk_64k", "us_per_call_back_to_back": round(ms * 1e3, 2),
             "alg_bytes_per_call": alg, "gbs": round(alg / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(alg / (ms * 1e-3) / 1e9 / pk["hbm"], 4), "needles_selected": ok,
-            "launches_per_call": 3}
+            "launches_per_call": 4}
 
 
 def row_cartridge(ctx, torch, pk, reps=10):

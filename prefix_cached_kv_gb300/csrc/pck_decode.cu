@@ -498,9 +498,9 @@ __device__ __forceinline__ int item_pieces(const DecodeParams& p, int item) {
     return (e - 1) / p.tpw - s / p.tpw + 1;
 }
 
-// Merge of one (item, q head). Pieces are taken in batches of BP (BP * D / 4 float4 of o per
-// batch, 16 per lane); all of a batch's loads (m and l of the lane's piece, and every o) are
-// issued before any is used, so a batch costs one L2 round trip. Batches are combined with an
+// Merge of one (item, q head). Pieces are taken in batches of BP (16 float4 of o per lane, 32
+// at D = 256, where few items mean few warps); all of a batch's loads (m and l of the lane's
+// piece, and every o) are issued before any is used, so a batch costs one L2 round trip. Batches are combined with an
 // online rescale; within a batch the weights 2^(m_k - M) are broadcast by shuffles. Partials are
 // read through L2 (__ldcg).
 template <int D>
@@ -521,8 +521,8 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
     constexpr int LPP = D / 4 > 32 ? 32 : D / 4;   // lanes per piece (one float4 of d each)
     constexpr int PPS = 32 / LPP;                  // pieces per warp-wide load
     constexpr int V4 = D / 4 / LPP;                // float4 per lane per piece
-    constexpr int NB = 16 / V4;                    // warp-wide loads per batch
-    constexpr int BP = NB * PPS;                   // pieces per batch (32, 16, 8 for D = 64, 128, 256)
+    constexpr int NB = D == 256 ? 16 : 16 / V4;    // warp-wide loads per batch
+    constexpr int BP = NB * PPS;                   // pieces per batch (32, 16, 16 for D = 64, 128, 256)
     const int sub = lane / LPP, dl = lane % LPP;
     float M = -INFINITY, L = 0.f;                  // L: this lane's share (lanes over pieces)
     float4 acc[V4];

@@ -57,10 +57,72 @@ __device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
     return sa > sb || (sa == sb && ia < ib);
 }
 
+// Top-K of one q head's nb <= 1024 scores held 32 per lane (block b = lane + 32 i), when
+// K <= 32: every lane finds its best element; the K-th best of those 32 lane bests, T, bounds
+// the answer (the K lane bests ranked 0..K-1 are all at least T, so the K-th best score is too),
+// so the top K are among the elements at least as good as T. When there are at most 32 of them
+// they are gathered and each one's rank among them is its place; otherwise (many ties) the
+// caller falls back to K rounds of arg-max. Order: higher score first, ties to the lower index.
+__device__ __forceinline__ bool topk_by_threshold(const float (&reg)[32], int nb, int K, int lane, float* cs, int* ci,
+                                                  int* picks) {
+    constexpr int NONE = 0x7fffffff;
+    float lb = -INFINITY;
+    int li = NONE;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int b = lane + 32 * i;
+        if (b < nb && (li == NONE || better(reg[i], b, lb, li))) { lb = reg[i]; li = b; }
+    }
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float os = __shfl_sync(0xffffffffu, lb, j);
+        const int oi = __shfl_sync(0xffffffffu, li, j);
+        if (oi != NONE && (li == NONE || better(os, oi, lb, li))) ++rank;
+    }
+    const unsigned at = __ballot_sync(0xffffffffu, li != NONE && rank == K - 1);
+    if (at == 0u) return false;
+    const int src = __ffs(at) - 1;
+    const float Ts = __shfl_sync(0xffffffffu, lb, src);
+    const int Ti = __shfl_sync(0xffffffffu, li, src);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int b = lane + 32 * i;
+        cnt += (b < nb && (b == Ti || better(reg[i], b, Ts, Ti))) ? 1 : 0;
+    }
+    int pre = cnt;   // inclusive scan over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += x;
+    }
+    const int C = __shfl_sync(0xffffffffu, pre, 31);
+    if (C > 32) return false;
+    int pos = pre - cnt;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int b = lane + 32 * i;
+        if (b < nb && (b == Ti || better(reg[i], b, Ts, Ti))) { cs[pos] = reg[i]; ci[pos] = b; ++pos; }
+    }
+    __syncwarp();
+    if (lane < C) {
+        const float s = cs[lane];
+        const int b = ci[lane];
+        int r = 0;
+        for (int k = 0; k < C; ++k) r += better(cs[k], ci[k], s, b) ? 1 : 0;
+        if (r < K) picks[r] = b;
+    }
+    __syncwarp();
+    return true;
+}
+
 // One CTA per work group: warp w selects the top-K of the group's w-th q head, then warp 0
 // merges the heads' selections into the group's sorted union (with per-head masks).
 __global__ void select_kernel(const __grid_constant__ SelectParams p) {
     __shared__ int picks[GMAX][64];
+    __shared__ float cand_s[GMAX][32];
+    __shared__ int cand_i[GMAX][32];
     const int grp = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WorkGroup& wg = p.grp[grp];
     const int K = p.K_eff;
@@ -74,9 +136,10 @@ __global__ void select_kernel(const __grid_constant__ SelectParams p) {
 #pragma unroll
             for (int i = 0; i < RPL; ++i) reg[i] = (lane + 32 * i < p.nb) ? sc[lane + 32 * i] : -INFINITY;
         }
+        const bool fast = in_regs && K <= 32 && topk_by_threshold(reg, p.nb, K, lane, cand_s[warp], cand_i[warp], picks[warp]);
         float prev_s = INFINITY;
         int prev_i = -1;
-        for (int r = 0; r < K; ++r) {
+        for (int r = 0; r < (fast ? 0 : K); ++r) {
             float bs = -INFINITY;
             int bi = 0x7fffffff;
             if (in_regs) {
