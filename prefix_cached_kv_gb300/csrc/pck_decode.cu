@@ -308,7 +308,7 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
     __syncwarp();
 }
 
-// NT (1 or 2) consecutive 16-token tiles of a kv head: scores of all NT*16 tokens, one online
+// NT (1, 2 or 4) consecutive 16-token tiles of a kv head: scores of all NT*16 tokens, one online
 // softmax step, then O += P' V for each tile.
 template <int D, int NCB, int NT>
 __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile0, int lane, int valid0,
@@ -789,7 +789,10 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
                 SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
                 tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
             } else {
-                if (k + 1 < c.nreal) {   // two tiles per softmax step
+                if (D == 64 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
+                    tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                    k += 3;
+                } else if (k + 1 < c.nreal) {   // two tiles per softmax step
                     tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
                     ++k;
                 } else {
