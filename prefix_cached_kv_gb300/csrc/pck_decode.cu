@@ -43,7 +43,7 @@ struct DCfg {
     static constexpr int NG = D / 32;       // mlx4g32 groups per head
     static constexpr int NBV = D / 8;       // PV n-blocks over d
     static constexpr int TB = tile_bytes(FMT, D);
-    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 2 : 1));
+    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 4 : 1));
     static constexpr int STAGE = TPS * TB;
     static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : 2;
     static constexpr bool QSMEM = D > 128;  // q fragments live in shared memory (register budget)
@@ -789,7 +789,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
                 SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
                 tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
             } else {
-                if (D == 64 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
+                if (D <= 128 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
                     tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
                     k += 3;
                 } else if (k + 1 < c.nreal) {   // two tiles per softmax step
