@@ -840,6 +840,9 @@ template <int FMT, int D, int NCB>
 __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<FMT, D>;
     extern __shared__ __align__(128) uint8_t smem[];
+    // the merge kernel (launched after this one with programmatic dependence) may be scheduled as
+    // this grid's CTAs retire; it still waits for the whole grid before reading any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * DECODE_WARPS + warp;
     uint8_t* ring = smem + warp * C::RING;

@@ -266,6 +266,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                   B_DR = 112, N_BAR = 15;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * N_BAR);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the merge kernel (programmatic dependence) may be scheduled as this grid's CTAs retire; it
+    // still waits for the whole grid before reading any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- which rows
     const int task = blockIdx.x / P.n_split;       // row tile
