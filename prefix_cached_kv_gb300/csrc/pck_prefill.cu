@@ -598,6 +598,63 @@ __global__ void __launch_bounds__(256, 6) prefill_merge_kernel(const __grid_cons
     }
 }
 
+// The same merge when there are at most 4 splits (the usual case): a warp takes 4 consecutive
+// rows of a tile and issues all of their loads (16 o float4 per lane, and lane 4q + k's (m, l)
+// of row q, split k) before reducing any, so the whole merge is about one L2 round trip.
+template <int D>
+__global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_constant__ PfParams P) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    constexpr int LPP = D / 4;   // lanes holding a row's d (D <= 128)
+    const int R0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4;
+    if (R0 >= P.n_tiles * PF_ROWS) return;
+    const int tile = R0 / PF_ROWS, rr0 = R0 - tile * PF_ROWS;
+    int grp = 0;
+    while (grp + 1 < P.n_groups && P.task_off[grp + 1] <= tile) ++grp;
+    const WorkGroup& wg = P.grp[grp];
+    const int M = P.a.M, ns = P.n_split;
+    const size_t sstride = (size_t)PF_ROWS * partial_stride(D);
+    const float* base = P.partials + ((size_t)tile * ns * PF_ROWS + rr0) * partial_stride(D);
+    const int mq = lane >> 2, mk = lane & 3;   // this lane's (row, split) for m and l
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < 16 && mk < ns) ml = __ldcg(reinterpret_cast<const float2*>(base + mq * partial_stride(D) + mk * sstride));
+    float4 xs[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            xs[q][k] = (k < ns && lane < LPP)
+                           ? __ldcg(reinterpret_cast<const float4*>(base + q * partial_stride(D) + k * sstride + PARTIAL_O) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    // per row: max and normaliser over the lanes 4q .. 4q + 3
+    float Mx = ml.x;
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 1));
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 2));
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
+    float L = w * ml.y;
+    L += __shfl_xor_sync(0xffffffffu, L, 1);
+    L += __shfl_xor_sync(0xffffffffu, L, 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, 4 * q + k);
+            acc.x = fmaf(wk, xs[q][k].x, acc.x); acc.y = fmaf(wk, xs[q][k].y, acc.y);
+            acc.z = fmaf(wk, xs[q][k].z, acc.z); acc.w = fmaf(wk, xs[q][k].w, acc.w);
+        }
+        const float Lq = __shfl_sync(0xffffffffu, L, 4 * q), Mq = __shfl_sync(0xffffffffu, Mx, 4 * q);
+        const int r = (tile - P.task_off[grp]) * PF_ROWS + rr0 + q;
+        if (r >= wg.nq * M) continue;
+        const int h = wg.qh[r / M], i = r % M;
+        const float inv = Lq > 0.f ? 1.0f / Lq : 0.f;
+        if (lane < LPP)
+            reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lq > 0.f ? (Mq + log2f(Lq)) * PF_LN2 : -INFINITY;
+    }
+}
+
 bool prefill_supported(int D) { return D == 64 || D == 128; }
 
 template <int D>
@@ -623,10 +680,14 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
     cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, P);
     if (e != cudaSuccess || P.n_split == 1) return e;
     const int rows = P.n_tiles * PF_ROWS;
-    cfg.gridDim = dim3((rows + 7) / 8);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.numAttrs = 1;
+    if (P.n_split <= 4) {   // 4 rows per warp
+        cfg.gridDim = dim3((rows + 31) / 32);
+        return cudaLaunchKernelEx(&cfg, prefill_merge4_kernel<D>, P);
+    }
+    cfg.gridDim = dim3((rows + 7) / 8);
     return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, P);
 }
 
