@@ -87,3 +87,40 @@ def test_sparse_needle_workload_full(ctx):
     assert np.array_equal(idx, idx_ref)
     assert_close_o_lse(host(O), host(L), O_ref, L_ref, "needle")
     ctx.drop("needle")
+
+
+def test_sparse_exact_ties_pick_lowest_indices(ctx):
+    """Every block has the same mean (K is the same vector at every token, so the block means are
+    bit-identical), so every score ties: each head must select blocks 0..K_top-1 (ties go to the
+    lower block index), and attend uniformly over their tokens."""
+    H_q, H_kv, N, D, B, Kt = 4, 1, 4096, 64, 64, 8
+    rng = np.random.default_rng(5)
+    row = rng.standard_normal(D).astype(np.float16)
+    K = np.broadcast_to(row, (H_kv, N, D)).copy()
+    _, V = synth.gen_kv(5, H_kv, N, D)
+    Q = synth.gen_q(5, H_q, 1, D)[:, 0]
+    hm = synth.default_head_map(H_q, H_kv)
+    ctx.store("ties", 0, dev(K), dev(V))
+    O, L, idx = ctx.query_sparse_auto("ties", 0, dev(Q), B, Kt, H_kv)
+    idx = host(idx).reshape(-1)[: H_q * Kt].reshape(H_q, Kt)
+    assert (idx == np.arange(Kt)[None]).all()
+    O_ref, L_ref, idx_ref, _ = orc.sparse_query(Q, K, V, hm, B, Kt)
+    assert (idx_ref == np.arange(Kt)[None]).all()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, "sparse-ties")
+    ctx.drop("ties")
+
+
+def test_sparse_more_blocks_than_registers(ctx):
+    """2500 blocks per head (more than the selector keeps in registers): scores read from memory."""
+    H_q, H_kv, N, D, B, Kt = 4, 2, 40000, 64, 16, 6
+    K, V = synth.gen_kv(77, H_kv, N, D)
+    Q = synth.gen_q(77, H_q, 1, D)[:, 0]
+    hm = synth.default_head_map(H_q, H_kv)
+    ctx.store("manyb", 0, dev(K), dev(V))
+    O, L, idx = ctx.query_sparse_auto("manyb", 0, dev(Q), B, Kt, H_kv)
+    O_ref, L_ref, idx_ref, scores = orc.sparse_query(Q, K, V, hm, B, Kt)
+    idx = host(idx).reshape(-1)[: H_q * Kt].reshape(H_q, Kt)
+    _check_idx(idx, scores, Kt)
+    near = orc.topk_margin(scores, Kt) < TIE_EPS
+    assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], "sparse-many")
+    ctx.drop("manyb")
