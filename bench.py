@@ -252,8 +252,7 @@ def run_e2e(args, ctx, torch, sets):
     for k in range(n_steps):
         step(k)
     dt = max_over_ranks((time.perf_counter() - t0) * 1e3)
-    ws = world()
-    return {"value": round(ws * KV_BYTES_STEP * n_steps / (dt * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(job_throughput(KV_BYTES_STEP * n_steps, dt) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(dt / n_steps, 4),
             "steps": n_steps, "path": "pinned host Q + suffix -> device, pck_query_batch, O + LSE -> pinned host, "
                                       "stream synchronize, every step"}
@@ -499,41 +498,9 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ distributed plumbing
 
-def world():
-    return int(os.environ.get("WORLD_SIZE", "1"))
-
-
-def rank():
-    return int(os.environ.get("RANK", "0"))
-
-
-_PG = False
-
-
-def dist_init():
-    global _PG
-    if world() > 1 and not _PG:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        dist.init_process_group("nccl")
-        _PG = True
-
-
-def barrier():
-    if _PG:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x):
-    if not _PG:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+from prefix_cached_kv_gb300.replicas import barrier, max_over_ranks, rank, world   # noqa: E402
+from prefix_cached_kv_gb300.replicas import init as dist_init   # noqa: E402
+from prefix_cached_kv_gb300.replicas import job_throughput   # noqa: E402
 
 
 def main():
@@ -578,7 +545,7 @@ def main():
         print(json.dumps({"rows": rows}), flush=True)
         return
     ws = world()
-    value = ws * KV_BYTES_STEP / (ms_step * 1e-3) / 1e9
+    value = job_throughput(KV_BYTES_STEP, ms_step, ws) / 1e9
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u4/f16 in, f32 accumulate", "data": "synthetic",
