@@ -58,11 +58,12 @@ __device__ __forceinline__ uint32_t codes_of(const float (&x)[8], float sf, floa
 }
 
 // One thread per pair of output code words (16 consecutive elements, 32 B of fp16 input); a group
-// of 32 elements is 2 adjacent lanes. Each iteration handles two pairs (at p and p + stride) so
-// that four 16-byte loads per thread are in flight.
+// of 32 elements is 2 adjacent lanes. One pair per iteration with a register budget for six
+// 256-thread CTAs per SM: more warps hide the load latency better than more loads per thread
+// (measured: 107 us against 119 us for two pairs per iteration at four CTAs, 256 MB of input).
 template <typename SrcT>
-__global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __restrict__ X, int64_t rows,
-                                                                int kv_dim, uint8_t* __restrict__ out) {
+__global__ void __launch_bounds__(256, 6) quantize_mlx4g32_kernel(const SrcT* __restrict__ X, int64_t rows,
+                                                                   int kv_dim, uint8_t* __restrict__ out) {
     const int wpr = kv_dim / 8;                 // words per row
     const int64_t total = rows * wpr / 2;       // word pairs; even per group, a warp never splits one
     const int rec = kv_dim / 2 + kv_dim / 8;
@@ -70,52 +71,44 @@ __global__ void __launch_bounds__(256) quantize_mlx4g32_kernel(const SrcT* __res
     const int64_t pi0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     // Every lane of a warp runs the same number of iterations, so the group shuffle below always
     // sees its partner (the 2 lanes of a group are both live or both idle).
-    const int64_t iters = (total + 2 * stride - 1) / (2 * stride);
+    const int64_t iters = (total + stride - 1) / stride;
     for (int64_t it = 0; it < iters; ++it) {
-        int64_t pi[2];
-        bool live[2];
-        float x[2][2][8];
+        const int64_t pi = pi0 + it * stride;
+        const bool live = pi < total;
+        float x[2][8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            pi[u] = pi0 + (2 * it + u) * stride;
-            live[u] = pi[u] < total;
+        for (int h = 0; h < 2; ++h) {
+            if (live) {
+                load8<SrcT>(X + (pi * 2 + h) * 8, x[h]);
+            } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (live[u]) {
-                    load8<SrcT>(X + (pi[u] * 2 + h) * 8, x[u][h]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[u][h][k] = 0.f;
-                }
+                for (int k = 0; k < 8; ++k) x[h][k] = 0.f;
             }
         }
+        float mn = x[0][0], mx = x[0][0];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float mn = x[u][0][0], mx = x[u][0][0];
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) { mn = fminf(mn, x[u][h][k]); mx = fmaxf(mx, x[u][h][k]); }
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-            const __half s16 = __float2half_rn(s32);     // round-trip through fp16 first
-            const __half b16 = __float2half_rn(mn);
-            const float sf = __half2float(s16), bf = __half2float(b16);
-            const float rcp = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
-            const uint32_t w0 = codes_of(x[u][0], sf, bf, rcp);
-            const uint32_t w1 = codes_of(x[u][1], sf, bf, rcp);
-            if (live[u]) {
-                const int64_t wi = pi[u] * 2;
-                const int64_t row = wi / wpr;
-                const int word = static_cast<int>(wi - row * wpr);
-                uint8_t* r = out + row * rec;
-                reinterpret_cast<uint32_t*>(r)[word] = w0;        // records are only 4-byte aligned
-                reinterpret_cast<uint32_t*>(r)[word + 1] = w1;
-                if ((word & 3) == 0) {
-                    reinterpret_cast<__half*>(r + kv_dim / 2)[word >> 2] = s16;
-                    reinterpret_cast<__half*>(r + kv_dim / 2 + kv_dim / 16)[word >> 2] = b16;
-                }
+            for (int k = 0; k < 8; ++k) { mn = fminf(mn, x[h][k]); mx = fmaxf(mx, x[h][k]); }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+        const __half s16 = __float2half_rn(s32);     // round-trip through fp16 first
+        const __half b16 = __float2half_rn(mn);
+        const float sf = __half2float(s16), bf = __half2float(b16);
+        const float rcp = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+        const uint32_t w0 = codes_of(x[0], sf, bf, rcp);
+        const uint32_t w1 = codes_of(x[1], sf, bf, rcp);
+        if (live) {
+            const int64_t wi = pi * 2;
+            const int64_t row = wi / wpr;
+            const int word = static_cast<int>(wi - row * wpr);
+            uint8_t* r = out + row * rec;
+            reinterpret_cast<uint32_t*>(r)[word] = w0;        // records are only 4-byte aligned
+            reinterpret_cast<uint32_t*>(r)[word + 1] = w1;
+            if ((word & 3) == 0) {
+                reinterpret_cast<__half*>(r + kv_dim / 2)[word >> 2] = s16;
+                reinterpret_cast<__half*>(r + kv_dim / 2 + kv_dim / 16)[word >> 2] = b16;
             }
         }
     }
