@@ -138,24 +138,37 @@ class Timer:
 
 
 def setup_decode_sets(ctx, torch, seed=0):
-    """ROTATE distinct sets of 16 mlx4g32 layers + per-layer Q, suffix, outputs (device)."""
+    """ROTATE distinct sets of 16 mlx4g32 layers + per-layer Q, suffix, outputs (device). A set's
+    per-layer inputs (Q, K_suf, V_suf) are views into one device buffer and its outputs (O, then
+    LSE) into another, the way a serving loop keeps one step's inputs together: the end-to-end
+    path then moves each step's inputs and results with one copy each way."""
     H_q, H_kv, N, D, L, S = W["H_q"], W["H_kv"], W["N"], W["D"], W["layers"], W["S_suf"]
     from prefix_cached_kv_gb300 import synth
-    sets = []
+    q_b, s_b, o_b, l_b = H_q * D * 4, H_kv * S * D * 2, H_q * D * 4, H_q * 4
+    per_in = q_b + 2 * s_b
+    sets, arenas = [], []
     for r in range(ROTATE):
+        din = torch.empty(L * per_in, dtype=torch.uint8, device="cuda")
+        dout = torch.empty(L * (o_b + l_b), dtype=torch.uint8, device="cuda")
         descs = []
         for layer in range(L):
             K, V = synth.torch_gen_kv_device(seed + 101 * r, H_kv, N, D, "cuda", col_scale=True, layer=layer)
             ctx.store(f"bench{r}", layer, K, V, fmt=1)
             g = torch.Generator(device="cuda").manual_seed(1000 * r + layer)
-            Q = torch.randn((H_q, D), generator=g, device="cuda")
-            Ks = torch.randn((H_kv, S, D), generator=g, device="cuda").half()
-            Vs = torch.randn((H_kv, S, D), generator=g, device="cuda").half()
-            descs.append(dict(sid=f"bench{r}", layer=layer, Q=Q, O=torch.empty((H_q, D), device="cuda"),
-                              LSE=torch.empty((H_q,), device="cuda"), K_suf=Ks, V_suf=Vs))
+            base = layer * per_in
+            Q = din[base:base + q_b].view(torch.float32).view(H_q, D)
+            Ks = din[base + q_b:base + q_b + s_b].view(torch.float16).view(H_kv, S, D)
+            Vs = din[base + q_b + s_b:base + per_in].view(torch.float16).view(H_kv, S, D)
+            Q.copy_(torch.randn((H_q, D), generator=g, device="cuda"))
+            Ks.copy_(torch.randn((H_kv, S, D), generator=g, device="cuda").half())
+            Vs.copy_(torch.randn((H_kv, S, D), generator=g, device="cuda").half())
+            O = dout[layer * o_b:(layer + 1) * o_b].view(torch.float32).view(H_q, D)
+            LSE = dout[L * o_b + layer * l_b:L * o_b + (layer + 1) * l_b].view(torch.float32)
+            descs.append(dict(sid=f"bench{r}", layer=layer, Q=Q, O=O, LSE=LSE, K_suf=Ks, V_suf=Vs))
         sets.append(descs)
+        arenas.append((din, dout))
     torch.cuda.synchronize()
-    return sets
+    return sets, arenas
 
 
 def graph_of(torch, fn):
@@ -183,7 +196,7 @@ def time_replays(torch, g, n):
 
 
 def run_main(args, ctx, torch, pk):
-    sets = setup_decode_sets(ctx, torch)
+    sets, arenas = setup_decode_sets(ctx, torch)
     H_q, H_kv, D, S = W["H_q"], W["H_kv"], W["D"], W["S_suf"]
     callers = [ctx.batch_caller(sets[r], H_q, H_kv, D, S_suf=S) for r in range(ROTATE)]
     for c in callers:          # eager warm-up (first launch sets kernel attributes)
@@ -216,31 +229,24 @@ def run_main(args, ctx, torch, pk):
             "kernel": "decode_kernel<mlx4g32, D=64> + merge_kernel", "algorithmic_bytes_per_launch": ALG_BYTES_STEP,
             "duration": "per-step time of back-to-back graph-replayed steps (decode + merge, PDL-chained)",
             "peak_source": f"{pk['src']} hbm_gbs"}
-    e2e = run_e2e(args, ctx, torch, sets)
+    e2e = run_e2e(args, ctx, torch, sets, arenas)
     return ms_step, steps, clocks, roof, e2e
 
 
-def run_e2e(args, ctx, torch, sets):
+def run_e2e(args, ctx, torch, sets, arenas):
     H_q, H_kv, D, S = W["H_q"], W["H_kv"], W["D"], W["S_suf"]
-    hosts = []
-    for descs in sets:
-        hin = [dict(Q=d["Q"].cpu().pin_memory(), K_suf=d["K_suf"].cpu().pin_memory(),
-                    V_suf=d["V_suf"].cpu().pin_memory(), O=torch.empty_like(d["O"], device="cpu").pin_memory(),
-                    LSE=torch.empty_like(d["LSE"], device="cpu").pin_memory()) for d in descs]
-        hosts.append(hin)
-    h2d = sum(h["Q"].numel() * 4 + h["K_suf"].numel() * 2 + h["V_suf"].numel() * 2 for h in hosts[0])
-    d2h = sum(h["O"].numel() * 4 + h["LSE"].numel() * 4 for h in hosts[0])
+    # pinned host copies of each set's input and output buffers
+    hosts = [(din.cpu().pin_memory(), torch.empty(dout.shape, dtype=dout.dtype).pin_memory()) for din, dout in arenas]
+    h2d = arenas[0][0].numel()
+    d2h = arenas[0][1].numel()
+    # the batched query through the binding's prebuilt call (the descriptor array is built once)
+    calls = [ctx.batch_caller(sets[r], H_q, H_kv, D, S_suf=S) for r in range(ROTATE)]
 
     def step(k):
-        descs, hin = sets[k % ROTATE], hosts[k % ROTATE]
-        for d, h in zip(descs, hin):
-            d["Q"].copy_(h["Q"], non_blocking=True)
-            d["K_suf"].copy_(h["K_suf"], non_blocking=True)
-            d["V_suf"].copy_(h["V_suf"], non_blocking=True)
-        ctx.query_batch(descs, H_q, H_kv, D, S_suf=S)
-        for d, h in zip(descs, hin):
-            h["O"].copy_(d["O"], non_blocking=True)
-            h["LSE"].copy_(d["LSE"], non_blocking=True)
+        (din, dout), (hin, hout) = arenas[k % ROTATE], hosts[k % ROTATE]
+        din.copy_(hin, non_blocking=True)
+        calls[k % ROTATE]()
+        hout.copy_(dout, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     n_steps = min(args.steps, 400)
@@ -254,8 +260,9 @@ def run_e2e(args, ctx, torch, sets):
     dt = max_over_ranks((time.perf_counter() - t0) * 1e3)
     return {"value": round(job_throughput(KV_BYTES_STEP * n_steps, dt) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(dt / n_steps, 4),
-            "steps": n_steps, "path": "pinned host Q + suffix -> device, pck_query_batch, O + LSE -> pinned host, "
-                                      "stream synchronize, every step"}
+            "steps": n_steps, "path": "pinned host Q + suffix of the 16 layers -> device (one copy), "
+                                      "pck_query_batch (prebuilt descriptors), O + LSE -> pinned host (one copy), stream synchronize, "
+                                      "every step"}
 
 
 # ------------------------------------------------------------------ other rows of the hot path
