@@ -120,7 +120,8 @@ int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void 
 
 /* ATTEND.PREFIX.QUERY <sid> <layer> <H> <D> <top_k> <Q_blob> [<fa_window>].
  * Q: device [H_q, M, D] of q_dtype. M == 1: split-K decode over the slot (fp16 or mlx4g32).
- * M > 1: tiled tensor-core kernel; needs an fp16 slot and q_dtype F16.
+ * M > 1: tiled tensor-core kernel; needs an fp16 slot, q_dtype F16 and D in {64, 128}
+ * (PCK_EUNSUPPORTED otherwise).
  * top_k: 0 or >= N (dense). fa_window: 0. Other values are PCK_EUNSUPPORTED.
  * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
 int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
