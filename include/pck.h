@@ -80,6 +80,18 @@ typedef struct pck_query_desc {
     const void *V_suf;
 } pck_query_desc;
 
+/* One M=1 query of a pck_query_sparse_batch call. */
+typedef struct pck_sparse_desc {
+    const char *sid;          /* session id (NUL-terminated) */
+    int layer;
+    const void *Q;            /* device [H_q, D], q_dtype of the batch */
+    float *O;                 /* device [H_q, D] fp32 */
+    float *LSE;               /* device [H_q] fp32, or NULL */
+    const void *K_suf;        /* device fp16 [H_kv, S_suf, D], or NULL when S_suf == 0 */
+    const void *V_suf;
+    int32_t *idx_out;         /* device [H_q, min(K_top, nb)] selected blocks (ascending), or NULL */
+} pck_sparse_desc;
+
 /* Create a context on CUDA device `device` with room for `max_slots` resident (sid, layer)
  * slots (<= 0 selects 256, the per-worker slot table size of the pages' session cache).
  * Allocates the split-K workspace. Returns PCK_OK and *out, or PCK_ECUDA / PCK_ENOMEM. */
@@ -160,6 +172,18 @@ int pck_query_sparse_auto_fused(pck_ctx *ctx, const char *sid, int layer, int H_
  * must have the same format. */
 int pck_query_batch(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, int H_kv, int D,
                     int S_suf, int q_dtype, const int32_t *head_map, void *stream);
+
+/* n independent ATTEND.PREFIX.QUERY_SPARSE_AUTO(_FUSED) queries (page "ATTEND.* and
+ * ATTEND.PREFIX.*", section "Wire forms"; batching them is this library's addition, as for
+ * pck_query_batch) of one shape (H_q, H_kv, D, B, K_top, S_suf, q_dtype, head_map) over fp16
+ * slots of the same N: the block scores and top-K of all of them run in one selector launch and
+ * their gathers (+ suffixes) in one split-K decode. Each query is as pck_query_sparse_auto_fused
+ * (S_suf > 0) or pck_query_sparse_auto (S_suf == 0) would compute it alone.
+ * 1 <= n <= PCK_MAX_BATCH. Errors: EINVAL, EUNSUPPORTED (slots of different N, B not a multiple
+ * of 16, K_top > 64, fa_window), MISS / COLDMISS for an absent slot. */
+int pck_query_sparse_batch(pck_ctx *ctx, int n, const pck_sparse_desc *descs, int H_q, int H_kv, int D,
+                           int B, int K_top, int S_suf, int q_dtype, const int32_t *head_map,
+                           void *stream);
 
 /* mlx4g32 quantiser (store side). X: device [rows, kv_dim] of src_dtype (F16 or F32);
  * out_records: device [rows, rec] bytes, rec = kv_dim/2 + kv_dim/8. Per group of 32:

@@ -24,7 +24,7 @@ MAX_BATCH = 64
 EXPORTS = (
     "pck_create", "pck_destroy", "pck_last_error", "pck_store", "pck_store_records", "pck_lookup",
     "pck_drop", "pck_build_block_means", "pck_query", "pck_query_fused", "pck_query_sparse_auto",
-    "pck_query_sparse_auto_fused", "pck_query_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
+    "pck_query_sparse_auto_fused", "pck_query_batch", "pck_query_sparse_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
     "pck_attend_records_noalloc",
 )
 
@@ -43,6 +43,12 @@ class InfoT(ctypes.Structure):
 class QueryDesc(ctypes.Structure):
     _fields_ = [("sid", ctypes.c_char_p), ("layer", ctypes.c_int), ("Q", ctypes.c_void_p), ("O", ctypes.c_void_p),
                 ("LSE", ctypes.c_void_p), ("K_suf", ctypes.c_void_p), ("V_suf", ctypes.c_void_p)]
+
+
+class SparseDesc(ctypes.Structure):
+    _fields_ = [("sid", ctypes.c_char_p), ("layer", ctypes.c_int), ("Q", ctypes.c_void_p), ("O", ctypes.c_void_p),
+                ("LSE", ctypes.c_void_p), ("K_suf", ctypes.c_void_p), ("V_suf", ctypes.c_void_p),
+                ("idx_out", ctypes.c_void_p)]
 
 
 _lib = None
@@ -71,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pck_query_sparse_auto": (i, [vp, cp, i, i, i, i, i, i, i, vp, vp, i, vp, vp, vp, vp]),
         "pck_query_sparse_auto_fused": (i, [vp, cp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp, vp]),
         "pck_query_batch": (i, [vp, i, ctypes.POINTER(QueryDesc), i, i, i, i, i, vp, vp]),
+        "pck_query_sparse_batch": (i, [vp, i, ctypes.POINTER(SparseDesc), i, i, i, i, i, i, i, vp, vp]),
         "pck_quantize_mlx4g32": (i, [vp, i, i64, i, vp, vp]),
         "pck_info": (i, [vp, ctypes.POINTER(InfoT)]),
         "pck_sync": (i, [vp, vp]),
@@ -232,6 +239,33 @@ class Context:
                                                       _stream(stream))
         self._rc(rc)
         return O, LSE, idx
+
+    def sparse_batch_caller(self, descs, H_q, H_kv, D, B, K_top, S_suf=0, q_dtype=DT_F32, head_map=None):
+        """Prebuild a pck_query_sparse_batch call over descs (dicts with sid, layer, Q, O, and
+        optionally LSE, K_suf, V_suf, idx); returns a no-argument callable issuing it on the
+        current stream (cheap enough to capture in a CUDA graph)."""
+        n = len(descs)
+        arr = (SparseDesc * n)()
+        keep = []
+        opt = lambda d, k: d[k].data_ptr() if d.get(k) is not None else None
+        for i, d in enumerate(descs):
+            sid = d["sid"].encode()
+            keep.append(sid)
+            arr[i] = SparseDesc(sid, d["layer"], d["Q"].data_ptr(), d["O"].data_ptr(), opt(d, "LSE"), opt(d, "K_suf"),
+                                opt(d, "V_suf"), opt(d, "idx"))
+        hm = _hm(head_map)
+        fn, h = self.lib.pck_query_sparse_batch, self.h
+
+        def call():
+            rc = fn(h, n, arr, H_q, H_kv, D, B, K_top, S_suf, q_dtype, hm[0] if hm else None, _stream(None))
+            if rc != OK:
+                raise PckError(rc, self.last_error())
+        call._keep = (arr, keep, hm)
+        return call
+
+    def query_sparse_batch(self, descs, H_q, H_kv, D, B, K_top, S_suf=0, q_dtype=DT_F32, head_map=None):
+        """n sparse queries in one selector launch and one gather decode (see sparse_batch_caller)."""
+        self.sparse_batch_caller(descs, H_q, H_kv, D, B, K_top, S_suf, q_dtype, head_map)()
 
     def query_batch(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None, stream=None):
         """descs: list of dicts with sid, layer, Q, O, LSE (optional), K_suf/V_suf (optional)."""

@@ -219,12 +219,13 @@ struct DescIn {
     float* LSE;
     const void* Ksuf;
     const void* Vsuf;
+    const int* sel_blocks = nullptr;     // sparse: the query's [n_groups, sel_max] block lists
+    const uint8_t* sel_mask = nullptr;   // sparse: per-block q-head masks
 };
 
 // Plan and launch one decode over n descriptors (dense), or one sparse descriptor.
 int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f16, const WorkGroup* grp,
-               int n_groups, const DescIn* dsc, int n, int sparse, int tiles_per_block, int sel_max,
-               const int* sel_blocks, const uint8_t* sel_mask, cudaStream_t st) {
+               int n_groups, const DescIn* dsc, int n, int sparse, int tiles_per_block, int sel_max, cudaStream_t st) {
     static thread_local DecodeParams p;   // ~6 KB, built on the host and copied into the launch
     std::memset(&p, 0, sizeof p);
     p.n_desc = n;
@@ -250,8 +251,8 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
         d.N = dsc[i].slot->N;
         d.ntiles = dsc[i].slot->ntiles;
         d.vtiles = sparse ? sel_max * tiles_per_block : d.ntiles;
-        d.sel_blocks = sel_blocks;
-        d.sel_mask = sel_mask;
+        d.sel_blocks = dsc[i].sel_blocks;
+        d.sel_mask = dsc[i].sel_mask;
         d.tile_off = static_cast<int>(total);
         total += static_cast<int64_t>(n_groups) * d.vtiles;
     }
@@ -511,8 +512,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M == 1) {
         DescIn d{s, Q, O, LSE, K_suf, V_suf};
-        rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0,
-                        nullptr, nullptr, st);
+        rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0, st);
         if (rc != PCK_OK) return rc;
         return check_async(c);
     }
@@ -572,63 +572,89 @@ int pck_query_fused(pck_ctx* c, const char* sid, int layer, int H_q, int D, int 
                         O, LSE, stream);
 }
 
-static int sparse_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
-                         int S_suf, int q_dtype, const void* Q, const void* K_suf, const void* V_suf,
-                         const int32_t* head_map, int fa_window, float* O, float* LSE, int32_t* idx_out,
-                         void* stream) {
+// One sparse query: its slot, Q, outputs, suffix and (optional) index output.
+struct SparseIn {
+    const char* sid;
+    int layer;
+    const void* Q;
+    float* O;
+    float* LSE;
+    const void* K_suf;
+    const void* V_suf;
+    int32_t* idx_out;
+};
+
+// n sparse queries of the same shapes (slots with the same N): block scoring and top-K for all of
+// them in one selector launch, then one split-K gather decode (+ merge) over all of them.
+static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int B, int K_top, int H_kv, int S_suf,
+                      int q_dtype, const int32_t* head_map, int fa_window, void* stream) {
     if (!c) return PCK_EINVAL;
-    if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
-    if (reinterpret_cast<uintptr_t>(O) & 15) return fail(c, PCK_EINVAL, "O must be 16-byte aligned");
+    if (n < 1 || n > MAX_DESC) return fail(c, PCK_EINVAL, "n=%d (1..%d queries per call)", n, MAX_DESC);
     if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
     if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
     if (K_top < 1) return fail(c, PCK_EINVAL, "K_top=%d", K_top);
-    if (S_suf < 0 || (S_suf > 0 && (!K_suf || !V_suf))) return fail(c, PCK_EINVAL, "bad suffix arguments");
-    Slot* s = nullptr;
-    int rc = find_slot(c, sid, layer, &s);
-    if (rc != PCK_OK) return rc;
-    if (D != s->D) return fail(c, PCK_EINVAL, "D=%d but the slot holds D=%d", D, s->D);
-    if (H_kv != s->H_kv) return fail(c, PCK_EINVAL, "H_kv=%d but the slot holds H_kv=%d", H_kv, s->H_kv);
-    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "sparse queries need an fp16 slot");
+    if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
     if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
-    const int nb = (s->N + B - 1) / B;
+    Slot* slots[MAX_DESC];
+    for (int i = 0; i < n; ++i) {
+        if (!q[i].Q || !q[i].O) return fail(c, PCK_EINVAL, "query %d: NULL Q or O", i);
+        if (reinterpret_cast<uintptr_t>(q[i].O) & 15) return fail(c, PCK_EINVAL, "query %d: O must be 16-byte aligned", i);
+        if (S_suf > 0 && (!q[i].K_suf || !q[i].V_suf)) return fail(c, PCK_EINVAL, "query %d: bad suffix arguments", i);
+        int rc = find_slot(c, q[i].sid, q[i].layer, &slots[i]);
+        if (rc != PCK_OK) return rc;
+        const Slot* s = slots[i];
+        if (D != s->D) return fail(c, PCK_EINVAL, "query %d: D=%d but the slot holds D=%d", i, D, s->D);
+        if (H_kv != s->H_kv) return fail(c, PCK_EINVAL, "query %d: H_kv=%d but the slot holds H_kv=%d", i, H_kv, s->H_kv);
+        if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "sparse queries need an fp16 slot");
+        if (s->N != slots[0]->N) return fail(c, PCK_EUNSUPPORTED, "query %d: N=%d differs from N=%d", i, s->N, slots[0]->N);
+    }
+    const int nb = (slots[0]->N + B - 1) / B;
     const int K_eff = std::min(K_top, nb);
     if (K_eff > 64) return fail(c, PCK_EUNSUPPORTED, "K_top=%d (at most 64)", K_top);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    rc = pck_build_block_means(c, sid, layer, B, stream);
-    if (rc != PCK_OK) return rc;
+    for (int i = 0; i < n; ++i) {   // cached per (slot, B): only the first query of a slot builds them
+        int rc = pck_build_block_means(c, q[i].sid, q[i].layer, B, stream);
+        if (rc != PCK_OK) return rc;
+    }
     static thread_local SelectParams sp;
     std::memset(&sp, 0, sizeof sp);
     int n_groups = 0, max_nq = 0;
-    rc = build_groups(c, H_q, s->H_kv, head_map, sp.grp, &n_groups, sp.head_map, &max_nq);
+    int rc = build_groups(c, H_q, H_kv, head_map, sp.grp, &n_groups, sp.head_map, &max_nq);
     if (rc != PCK_OK) return rc;
     const int sel_max = max_nq * K_eff;
-    if (static_cast<size_t>(n_groups) * sel_max * (sizeof(int) + 1) > WS_SEL_BYTES)
+    const size_t lists = static_cast<size_t>(n_groups) * sel_max;   // entries per query
+    if (static_cast<size_t>(n) * lists * (sizeof(int) + 1) > WS_SEL_BYTES)
         return fail(c, PCK_EUNSUPPORTED, "selection lists too large");
-    if (static_cast<size_t>(H_q) * nb * sizeof(float) > WS_SCORES_BYTES)
+    if (static_cast<size_t>(n) * H_q * nb * sizeof(float) > WS_SCORES_BYTES)
         return fail(c, PCK_EUNSUPPORTED, "too many blocks for the score workspace");
     int* sel_blocks = reinterpret_cast<int*>(c->sel);
-    uint8_t* sel_mask = c->sel + static_cast<size_t>(n_groups) * sel_max * sizeof(int);
-    sp.kmean = s->kmean[B];
-    sp.Q = Q;
+    uint8_t* sel_mask = c->sel + static_cast<size_t>(n) * lists * sizeof(int);
     sp.q_f16 = q_dtype == PCK_DT_F16;
     sp.H_q = H_q;
-    sp.H_kv = s->H_kv;
+    sp.H_kv = H_kv;
     sp.D = D;
     sp.nb = nb;
     sp.K_top = K_top;
     sp.K_eff = K_eff;
     sp.sel_max = sel_max;
     sp.n_groups = n_groups;
+    sp.n_sess = n;
     sp.tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
-    sp.scores = c->scores;
-    sp.idx_out = idx_out;
-    sp.sel_blocks = sel_blocks;
-    sp.sel_mask = sel_mask;
+    static thread_local DescIn d[MAX_DESC];
+    for (int i = 0; i < n; ++i) {
+        SelSession& ss = sp.sess[i];
+        ss.kmean = slots[i]->kmean[B];
+        ss.Q = q[i].Q;
+        ss.scores = c->scores + static_cast<size_t>(i) * H_q * nb;
+        ss.idx_out = q[i].idx_out;
+        ss.sel_blocks = sel_blocks + i * lists;
+        ss.sel_mask = sel_mask + i * lists;
+        d[i] = DescIn{slots[i], q[i].Q, q[i].O, q[i].LSE, q[i].K_suf, q[i].V_suf, ss.sel_blocks, ss.sel_mask};
+    }
     cudaError_t e = launch_select(sp, st, c->sms);
     if (e != cudaSuccess) return cuda_fail(c, e, "selector launch");
-    DescIn d{s, Q, O, LSE, K_suf, V_suf};
-    rc = run_decode(c, PCK_FMT_FP16, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, sp.grp, n_groups, &d, 1, 1, B / 16,
-                    sel_max, sel_blocks, sel_mask, st);
+    rc = run_decode(c, PCK_FMT_FP16, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, sp.grp, n_groups, d, n, 1, B / 16,
+                    sel_max, st);
     if (rc != PCK_OK) return rc;
     return check_async(c);
 }
@@ -636,16 +662,27 @@ static int sparse_common(pck_ctx* c, const char* sid, int layer, int H_q, int D,
 int pck_query_sparse_auto(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
                           int q_dtype, const void* Q, const int32_t* head_map, int fa_window, float* O, float* LSE,
                           int32_t* idx_out, void* stream) {
-    return sparse_common(c, sid, layer, H_q, D, B, K_top, H_kv, 0, q_dtype, Q, nullptr, nullptr, head_map, fa_window, O,
-                         LSE, idx_out, stream);
+    const SparseIn q{sid, layer, Q, O, LSE, nullptr, nullptr, idx_out};
+    return sparse_run(c, 1, &q, H_q, D, B, K_top, H_kv, 0, q_dtype, head_map, fa_window, stream);
 }
 
 int pck_query_sparse_auto_fused(pck_ctx* c, const char* sid, int layer, int H_q, int D, int B, int K_top, int H_kv,
                                 int S_suf, int q_dtype, const void* Q, const void* K_suf, const void* V_suf,
                                 const int32_t* head_map, int fa_window, float* O, float* LSE, int32_t* idx_out,
                                 void* stream) {
-    return sparse_common(c, sid, layer, H_q, D, B, K_top, H_kv, S_suf, q_dtype, Q, K_suf, V_suf, head_map, fa_window,
-                         O, LSE, idx_out, stream);
+    const SparseIn q{sid, layer, Q, O, LSE, K_suf, V_suf, idx_out};
+    return sparse_run(c, 1, &q, H_q, D, B, K_top, H_kv, S_suf, q_dtype, head_map, fa_window, stream);
+}
+
+int pck_query_sparse_batch(pck_ctx* c, int n, const pck_sparse_desc* descs, int H_q, int H_kv, int D, int B,
+                           int K_top, int S_suf, int q_dtype, const int32_t* head_map, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (n < 1 || n > PCK_MAX_BATCH || !descs) return fail(c, PCK_EINVAL, "n=%d (1..%d) or NULL descs", n, PCK_MAX_BATCH);
+    SparseIn q[PCK_MAX_BATCH];
+    for (int i = 0; i < n; ++i)
+        q[i] = SparseIn{descs[i].sid, descs[i].layer, descs[i].Q, descs[i].O, descs[i].LSE,
+                        S_suf > 0 ? descs[i].K_suf : nullptr, S_suf > 0 ? descs[i].V_suf : nullptr, descs[i].idx_out};
+    return sparse_run(c, n, q, H_q, D, B, K_top, H_kv, S_suf, q_dtype, head_map, 0, stream);
 }
 
 int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int H_kv, int D, int S_suf, int q_dtype,
@@ -675,7 +712,7 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
     int n_groups = 0;
     int rc = build_groups(c, H_q, H_kv, head_map, grp, &n_groups, nullptr, nullptr);
     if (rc != PCK_OK) return rc;
-    rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0, nullptr, nullptr,
+    rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0,
                     static_cast<cudaStream_t>(stream));
     if (rc != PCK_OK) return rc;
     return check_async(c);

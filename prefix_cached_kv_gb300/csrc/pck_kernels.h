@@ -31,18 +31,23 @@ cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cud
 // sparse selector
 cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int ntiles, int B, float* kmean,
                                cudaStream_t st, int sms);
-struct SelectParams {
+// One session of a selector launch (a query against one slot).
+struct SelSession {
     const float* kmean;      // [H_kv, nb, D]
     const void* Q;           // [H_q, D]
-    int q_f16;
-    int H_q, H_kv, D, nb, K_top, K_eff, sel_max, n_groups;
-    float tau;
     float* scores;           // workspace [H_q, nb]
     int* idx_out;            // [H_q, K_eff] or nullptr
     int* sel_blocks;         // [n_groups, sel_max]
     uint8_t* sel_mask;       // [n_groups, sel_max]
+};
+// Block scoring + top-K selection for n_sess sessions of the same shapes (one launch each).
+struct SelectParams {
+    int q_f16;
+    int H_q, H_kv, D, nb, K_top, K_eff, sel_max, n_groups, n_sess;
+    float tau;
     int8_t head_map[PCK_MAXH];
     WorkGroup grp[MAX_GROUPS];
+    SelSession sess[MAX_DESC];
 };
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
 

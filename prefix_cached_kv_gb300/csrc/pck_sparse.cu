@@ -29,12 +29,15 @@ __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int
     }
 }
 
-// score[h, b] = tau * q_h . K_mean[head_map[h], b]; one warp per (kv head, block).
+// score[h, b] = tau * q_h . K_mean[head_map[h], b]; one warp per (session, kv head, block).
 __global__ void block_scores_kernel(const __grid_constant__ SelectParams p) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= p.H_kv * p.nb) return;
-    const int g = warp / p.nb, b = warp - g * p.nb;
-    const float* km = p.kmean + ((size_t)g * p.nb + b) * p.D;
+    const int per_sess = p.H_kv * p.nb;
+    if (warp >= p.n_sess * per_sess) return;
+    const int si = warp / per_sess, wl = warp - si * per_sess;
+    const SelSession& ss = p.sess[si];
+    const int g = wl / p.nb, b = wl - g * p.nb;
+    const float* km = ss.kmean + ((size_t)g * p.nb + b) * p.D;
     float kv[8];
     const int per = p.D / 32;
     for (int i = 0; i < per; ++i) kv[i] = km[lane + 32 * i];
@@ -43,13 +46,13 @@ __global__ void block_scores_kernel(const __grid_constant__ SelectParams p) {
         float acc = 0.f;
         for (int i = 0; i < per; ++i) {
             const int d = lane + 32 * i;
-            const float qv = p.q_f16 ? __half2float(reinterpret_cast<const __half*>(p.Q)[h * p.D + d])
-                                     : reinterpret_cast<const float*>(p.Q)[h * p.D + d];
+            const float qv = p.q_f16 ? __half2float(reinterpret_cast<const __half*>(ss.Q)[h * p.D + d])
+                                     : reinterpret_cast<const float*>(ss.Q)[h * p.D + d];
             acc = fmaf(qv, kv[i], acc);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) p.scores[(size_t)h * p.nb + b] = p.tau * acc;
+        if (lane == 0) ss.scores[(size_t)h * p.nb + b] = p.tau * acc;
     }
 }
 
@@ -117,18 +120,19 @@ __device__ __forceinline__ bool topk_by_threshold(const float (&reg)[32], int nb
     return true;
 }
 
-// One CTA per work group: warp w selects the top-K of the group's w-th q head, then warp 0
-// merges the heads' selections into the group's sorted union (with per-head masks).
+// One CTA per (work group, session): warp w selects the top-K of the group's w-th q head, then
+// thread 0 merges the heads' selections into the group's sorted union (with per-head masks).
 __global__ void select_kernel(const __grid_constant__ SelectParams p) {
     __shared__ int picks[GMAX][64];
     __shared__ float cand_s[GMAX][32];
     __shared__ int cand_i[GMAX][32];
     const int grp = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const SelSession& ss = p.sess[blockIdx.y];
     const WorkGroup& wg = p.grp[grp];
     const int K = p.K_eff;
     if (warp < wg.nq) {
         const int h = wg.qh[warp];
-        const float* sc = p.scores + (size_t)h * p.nb;
+        const float* sc = ss.scores + (size_t)h * p.nb;
         constexpr int RPL = 32;                 // scores held in registers per lane (nb <= 1024)
         float reg[RPL];
         const bool in_regs = p.nb <= 32 * RPL;
@@ -182,14 +186,14 @@ __global__ void select_kernel(const __grid_constant__ SelectParams p) {
                 while (j >= 0 && picks[warp][j] > v) { picks[warp][j + 1] = picks[warp][j]; --j; }
                 picks[warp][j + 1] = v;
             }
-            if (p.idx_out)
-                for (int i = 0; i < K; ++i) p.idx_out[(size_t)h * K + i] = picks[warp][i];
+            if (ss.idx_out)
+                for (int i = 0; i < K; ++i) ss.idx_out[(size_t)h * K + i] = picks[warp][i];
         }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int* out_b = p.sel_blocks + (size_t)grp * p.sel_max;
-        uint8_t* out_m = p.sel_mask + (size_t)grp * p.sel_max;
+        int* out_b = ss.sel_blocks + (size_t)grp * p.sel_max;
+        uint8_t* out_m = ss.sel_mask + (size_t)grp * p.sel_max;
         int pos[GMAX];
         for (int w = 0; w < wg.nq; ++w) pos[w] = 0;
         int n = 0;
@@ -220,11 +224,11 @@ cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int nt
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
     (void)sms;
-    const int warps = p.H_kv * p.nb;
-    block_scores_kernel<<<(warps + 7) / 8, 256, 0, st>>>(p);
+    const int64_t warps = static_cast<int64_t>(p.n_sess) * p.H_kv * p.nb;
+    block_scores_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    select_kernel<<<p.n_groups, GMAX * 32, 0, st>>>(p);
+    select_kernel<<<dim3(p.n_groups, p.n_sess), GMAX * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -124,3 +124,51 @@ def test_sparse_more_blocks_than_registers(ctx):
     near = orc.topk_margin(scores, Kt) < TIE_EPS
     assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], "sparse-many")
     ctx.drop("manyb")
+
+
+def test_sparse_batch_matches_single_calls_and_oracle(ctx):
+    """pck_query_sparse_batch over 3 sessions (own data, own suffix): every query selects what its
+    own single call selects, and its outputs match the oracle."""
+    H_q, H_kv, N, D, B, Kt, S = 8, 2, 3000, 128, 64, 5, 24
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs, singles = [], [], []
+    for r in range(3):
+        seed = 300 + r
+        K, V = synth.gen_kv(seed, H_kv, N, D)
+        Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        sid = f"spb{r}"
+        ctx.store(sid, 0, dev(K), dev(V))
+        O1, L1, i1 = ctx.query_sparse_auto(sid, 0, dev(Q), B, Kt, H_kv, K_suf=dev(Ks), V_suf=dev(Vs))
+        singles.append(host(i1).reshape(-1)[: H_q * Kt].reshape(H_q, Kt))
+        d = dict(sid=sid, layer=0, Q=dev(Q), O=torch.empty((H_q, D), device="cuda"),
+                 LSE=torch.empty((H_q,), device="cuda"), K_suf=dev(Ks), V_suf=dev(Vs),
+                 idx=torch.empty((H_q, Kt), dtype=torch.int32, device="cuda"))
+        descs.append(d)
+        refs.append(orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs))
+    ctx.query_sparse_batch(descs, H_q, H_kv, D, B, Kt, S_suf=S)
+    ctx.sync()
+    for r, (d, (O_ref, L_ref, idx_ref, scores)) in enumerate(zip(descs, refs)):
+        idx = host(d["idx"])
+        assert np.array_equal(idx, singles[r])
+        _check_idx(idx, scores, Kt)
+        near = orc.topk_margin(scores, Kt) < TIE_EPS
+        assert_close_o_lse(host(d["O"])[~near], host(d["LSE"])[~near], O_ref[~near], L_ref[~near], f"batch {r}")
+    for r in range(3):
+        ctx.drop(f"spb{r}")
+
+
+def test_sparse_batch_rejects_slots_of_different_lengths(ctx):
+    from prefix_cached_kv_gb300 import binding
+    H_q, H_kv, D = 4, 1, 64
+    descs = []
+    for r, N in enumerate((512, 640)):
+        K, V = synth.gen_kv(r, H_kv, N, D)
+        ctx.store(f"spn{r}", 0, dev(K), dev(V))
+        descs.append(dict(sid=f"spn{r}", layer=0, Q=dev(synth.gen_q(r, H_q, 1, D)[:, 0]),
+                          O=torch.empty((H_q, D), device="cuda")))
+    with pytest.raises(binding.PckError) as e:
+        ctx.query_sparse_batch(descs, H_q, H_kv, D, 64, 2)
+    assert e.value.code == binding.EUNSUPPORTED
+    for r in range(2):
+        ctx.drop(f"spn{r}")
