@@ -641,7 +641,19 @@ __device__ void finish_piece_i4(I4State<D, NCB>& st, const DecodeParams& p, int 
 
 struct Cursor {
     int t, t_end, d, grp, item_start, item_end;
+    int sel_blk, sel_msk;   // sparse, lists of <= 32 blocks: lane l holds entry l of the item's list
 };
+
+// Sparse queries whose selection lists fit a warp keep the current item's list in registers
+// (one entry per lane, read by shuffles), so a chunk does not wait on a global load for its block.
+__device__ __forceinline__ void cursor_load_sel(const DecodeParams& p, Cursor& c) {
+    if (!p.sparse || p.sel_max > 32) return;
+    const int lane = threadIdx.x & 31;
+    const DecodeDesc& ds = p.desc[c.d];
+    const int base = c.grp * p.sel_max;
+    c.sel_blk = lane < p.sel_max ? ds.sel_blocks[base + lane] : -1;
+    c.sel_msk = lane < p.sel_max ? ds.sel_mask[base + lane] : 0;
+}
 
 struct Chunk {
     int item, d, grp;
@@ -662,6 +674,7 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
     c.grp = grp;
     c.item_start = p.desc[d].tile_off + grp * vt;
     c.item_end = c.item_start + vt;
+    cursor_load_sel(p, c);
 }
 
 template <int FMT, int D, int TPS, int TB>
@@ -671,6 +684,7 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
         if (++c.grp == p.n_groups) { c.grp = 0; ++c.d; }
         c.item_start = p.desc[c.d].tile_off + c.grp * p.desc[c.d].vtiles;
         c.item_end = c.item_start + p.desc[c.d].vtiles;
+        cursor_load_sel(p, c);
     }
     const DecodeDesc& ds = p.desc[c.d];
     const int local = c.t - c.item_start;
@@ -684,7 +698,7 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
     } else {
         const int bs = local / p.tiles_per_block, within = local - bs * p.tiles_per_block;
         n = min(TPS, min(lim, p.tiles_per_block - within));
-        const int blk = ds.sel_blocks[c.grp * p.sel_max + bs];
+        const int blk = p.sel_max <= 32 ? __shfl_sync(0xffffffffu, c.sel_blk, bs) : ds.sel_blocks[c.grp * p.sel_max + bs];
         ch.slot_blk = bs;
         if (blk < 0) {
             ch.tile = 0;
@@ -780,7 +794,9 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         }
         --inflight;
         uint32_t head_mask = 0xFFu;   // bit h: local q head h attends to this chunk's tokens
-        if (p.sparse && c.nreal > 0) head_mask = ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
+        if (p.sparse && c.nreal > 0)
+            head_mask = p.sel_max <= 32 ? __shfl_sync(0xffffffffu, cons.sel_msk, c.slot_blk)
+                                        : ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
         const bool head_ok = (lane >> 2) < wg.nq && ((head_mask >> (lane >> 2)) & 1u);
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {

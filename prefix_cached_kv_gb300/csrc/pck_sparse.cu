@@ -29,30 +29,45 @@ __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int
     }
 }
 
-// score[h, b] = tau * q_h . K_mean[head_map[h], b]; one warp per (session, kv head, block).
+// score[h, b] = tau * q_h . K_mean[head_map[h], b]; one warp per (session, kv head, 4 consecutive
+// blocks): the 4 blocks' means are loaded together (32 loads per lane in flight at D = 256), then
+// each q head of the kv head is read once and dotted with all 4.
+constexpr int SCORE_BPW = 4;
 __global__ void block_scores_kernel(const __grid_constant__ SelectParams p) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int per_sess = p.H_kv * p.nb;
+    const int nbw = (p.nb + SCORE_BPW - 1) / SCORE_BPW;   // warps per (session, kv head)
+    const int per_sess = p.H_kv * nbw;
     if (warp >= p.n_sess * per_sess) return;
     const int si = warp / per_sess, wl = warp - si * per_sess;
     const SelSession& ss = p.sess[si];
-    const int g = wl / p.nb, b = wl - g * p.nb;
-    const float* km = ss.kmean + ((size_t)g * p.nb + b) * p.D;
-    float kv[8];
-    const int per = p.D / 32;
-    for (int i = 0; i < per; ++i) kv[i] = km[lane + 32 * i];
+    const int g = wl / nbw, b0 = (wl - g * nbw) * SCORE_BPW;
+    const int per = p.D / 32;   // <= 8
+    float kv[SCORE_BPW][8];
+#pragma unroll
+    for (int j = 0; j < SCORE_BPW; ++j) {
+        const float* km = ss.kmean + ((size_t)g * p.nb + min(b0 + j, p.nb - 1)) * p.D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kv[j][i] = i < per ? km[lane + 32 * i] : 0.f;
+    }
     for (int h = 0; h < p.H_q; ++h) {
         if (p.head_map[h] != g) continue;
-        float acc = 0.f;
-        for (int i = 0; i < per; ++i) {
+        float qv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             const int d = lane + 32 * i;
-            const float qv = p.q_f16 ? __half2float(reinterpret_cast<const __half*>(ss.Q)[h * p.D + d])
-                                     : reinterpret_cast<const float*>(ss.Q)[h * p.D + d];
-            acc = fmaf(qv, kv[i], acc);
+            qv[i] = i >= per ? 0.f
+                             : (p.q_f16 ? __half2float(reinterpret_cast<const __half*>(ss.Q)[h * p.D + d])
+                                        : reinterpret_cast<const float*>(ss.Q)[h * p.D + d]);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) ss.scores[(size_t)h * p.nb + b] = p.tau * acc;
+        for (int j = 0; j < SCORE_BPW; ++j) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = fmaf(qv[i], kv[j][i], acc);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0 && b0 + j < p.nb) ss.scores[(size_t)h * p.nb + b0 + j] = p.tau * acc;
+        }
     }
 }
 
@@ -224,7 +239,7 @@ cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int nt
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
     (void)sms;
-    const int64_t warps = static_cast<int64_t>(p.n_sess) * p.H_kv * p.nb;
+    const int64_t warps = static_cast<int64_t>(p.n_sess) * p.H_kv * ((p.nb + SCORE_BPW - 1) / SCORE_BPW);
     block_scores_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
