@@ -696,8 +696,12 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
         ch.nreal = n;
         ch.slot_blk = 0;
     } else {
-        const int bs = local / p.tiles_per_block, within = local - bs * p.tiles_per_block;
-        n = min(TPS, min(lim, p.tiles_per_block - within));
+        // The item's virtual tiles visit its selection list slot by slot, tile by tile (slot
+        // local % sel_max, tile local / sel_max of that block): the list's real blocks come
+        // first and its empty slots last, so this spreads the real tiles evenly over the
+        // workers' contiguous ranges. One tile per chunk.
+        const int bs = local % p.sel_max, within = local / p.sel_max;
+        n = 1;
         const int blk = p.sel_max <= 32 ? __shfl_sync(0xffffffffu, c.sel_blk, bs) : ds.sel_blocks[c.grp * p.sel_max + bs];
         ch.slot_blk = bs;
         if (blk < 0) {
