@@ -225,7 +225,8 @@ struct DescIn {
 
 // Plan and launch one decode over n descriptors (dense), or one sparse descriptor.
 int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f16, const WorkGroup* grp,
-               int n_groups, const DescIn* dsc, int n, int sparse, int tiles_per_block, int sel_max, cudaStream_t st) {
+               int n_groups, const DescIn* dsc, int n, int sparse, int tiles_per_block, int sel_max, const int* item_base,
+               cudaStream_t st) {
     static thread_local DecodeParams p;   // ~6 KB, built on the host and copied into the launch
     std::memset(&p, 0, sizeof p);
     p.n_desc = n;
@@ -237,6 +238,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     p.sparse = sparse;
     p.tiles_per_block = tiles_per_block;
     p.sel_max = sel_max;
+    p.item_base = item_base;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     for (int g = 0; g < n_groups; ++g) p.grp[g] = grp[g];
     int64_t total = 0;
@@ -268,7 +270,9 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     for (int i = 0; i < n; ++i) vmax = std::max(vmax, p.desc[i].vtiles);
     tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);
     if (tpw < 2) tpw = 2;
-    const int64_t n_workers = (total + tpw - 1) / tpw;
+    // sparse: total bounds the units (every list full); the selector's real count is split over
+    // all the resident prefix warps on the device
+    const int64_t n_workers = sparse ? std::min<int64_t>(max_warps, total) : (total + tpw - 1) / tpw;
     const int n_items = n * n_groups;
     const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
     const int64_t slots = n_workers + n_items + static_cast<int64_t>(n_items) * n_suf;
@@ -277,6 +281,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     if (n_items > WS_COUNTERS) return fail(c, PCK_EUNSUPPORTED, "too many work items");
     p.total_tiles = static_cast<int>(total);
     p.tpw = static_cast<int>(tpw);
+    p.max_units = static_cast<int>(total);
     p.n_workers = static_cast<int>(n_workers);
     p.n_suf = n_suf;
     p.partials = c->partials;
@@ -512,7 +517,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M == 1) {
         DescIn d{s, Q, O, LSE, K_suf, V_suf};
-        rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0, st);
+        rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0, nullptr, st);
         if (rc != PCK_OK) return rc;
         return check_async(c);
     }
@@ -595,10 +600,12 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     if (K_top < 1) return fail(c, PCK_EINVAL, "K_top=%d", K_top);
     if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
     if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
+    if (D != 64 && D != 128 && D != 256) return fail(c, PCK_EUNSUPPORTED, "D=%d (sparse queries take 64, 128 or 256)", D);
     Slot* slots[MAX_DESC];
     for (int i = 0; i < n; ++i) {
         if (!q[i].Q || !q[i].O) return fail(c, PCK_EINVAL, "query %d: NULL Q or O", i);
-        if (reinterpret_cast<uintptr_t>(q[i].O) & 15) return fail(c, PCK_EINVAL, "query %d: O must be 16-byte aligned", i);
+        if ((reinterpret_cast<uintptr_t>(q[i].O) | reinterpret_cast<uintptr_t>(q[i].Q)) & 15)
+            return fail(c, PCK_EINVAL, "query %d: Q and O must be 16-byte aligned", i);
         if (S_suf > 0 && (!q[i].K_suf || !q[i].V_suf)) return fail(c, PCK_EINVAL, "query %d: bad suffix arguments", i);
         int rc = find_slot(c, q[i].sid, q[i].layer, &slots[i]);
         if (rc != PCK_OK) return rc;
@@ -623,12 +630,18 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     if (rc != PCK_OK) return rc;
     const int sel_max = max_nq * K_eff;
     const size_t lists = static_cast<size_t>(n_groups) * sel_max;   // entries per query
-    if (static_cast<size_t>(n) * lists * (sizeof(int) + 1) > WS_SEL_BYTES)
+    const int n_items = n * n_groups;
+    // selection workspace: block lists, q-head masks, then the items' unit counts and offsets
+    const size_t cnt_off = (static_cast<size_t>(n) * lists * (sizeof(int) + 1) + 15) & ~size_t(15);
+    const size_t base_off = cnt_off + static_cast<size_t>(n_items) * sizeof(int);
+    if (base_off + static_cast<size_t>(n_items + 1) * sizeof(int) > WS_SEL_BYTES)
         return fail(c, PCK_EUNSUPPORTED, "selection lists too large");
     if (static_cast<size_t>(n) * H_q * nb * sizeof(float) > WS_SCORES_BYTES)
         return fail(c, PCK_EUNSUPPORTED, "too many blocks for the score workspace");
     int* sel_blocks = reinterpret_cast<int*>(c->sel);
     uint8_t* sel_mask = c->sel + static_cast<size_t>(n) * lists * sizeof(int);
+    int* item_cnt = reinterpret_cast<int*>(c->sel + cnt_off);
+    int* item_base = reinterpret_cast<int*>(c->sel + base_off);
     sp.q_f16 = q_dtype == PCK_DT_F16;
     sp.H_q = H_q;
     sp.H_kv = H_kv;
@@ -640,6 +653,11 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     sp.n_groups = n_groups;
     sp.n_sess = n;
     sp.tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    sp.tpb = B / 16;
+    sp.ntiles = slots[0]->ntiles;
+    sp.item_cnt = item_cnt;
+    sp.item_base = item_base;
+    sp.done = reinterpret_cast<unsigned*>(c->counters + (WS_COUNTERS - 1));
     static thread_local DescIn d[MAX_DESC];
     for (int i = 0; i < n; ++i) {
         SelSession& ss = sp.sess[i];
@@ -654,7 +672,7 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     cudaError_t e = launch_select(sp, st, c->sms);
     if (e != cudaSuccess) return cuda_fail(c, e, "selector launch");
     rc = run_decode(c, PCK_FMT_FP16, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, sp.grp, n_groups, d, n, 1, B / 16,
-                    sel_max, st);
+                    sel_max, item_base, st);
     if (rc != PCK_OK) return rc;
     return check_async(c);
 }
@@ -702,8 +720,8 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
         if (fmt >= 0 && s->fmt != fmt) return fail(c, PCK_EINVAL, "descriptor %d: mixed slot formats", i);
         fmt = s->fmt;
         if (!descs[i].Q || !descs[i].O) return fail(c, PCK_EINVAL, "descriptor %d: NULL Q or O", i);
-        if (reinterpret_cast<uintptr_t>(descs[i].O) & 15)
-            return fail(c, PCK_EINVAL, "descriptor %d: O must be 16-byte aligned", i);
+        if ((reinterpret_cast<uintptr_t>(descs[i].O) | reinterpret_cast<uintptr_t>(descs[i].Q)) & 15)
+            return fail(c, PCK_EINVAL, "descriptor %d: Q and O must be 16-byte aligned", i);
         if (S_suf > 0 && (!descs[i].K_suf || !descs[i].V_suf))
             return fail(c, PCK_EINVAL, "descriptor %d: NULL suffix", i);
         ds[i] = DescIn{s, descs[i].Q, descs[i].O, descs[i].LSE, descs[i].K_suf, descs[i].V_suf};
@@ -712,7 +730,7 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
     int n_groups = 0;
     int rc = build_groups(c, H_q, H_kv, head_map, grp, &n_groups, nullptr, nullptr);
     if (rc != PCK_OK) return rc;
-    rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0,
+    rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0, nullptr,
                     static_cast<cudaStream_t>(stream));
     if (rc != PCK_OK) return rc;
     return check_async(c);

@@ -82,13 +82,16 @@ struct DecodeParams {
     DecodeDesc desc[MAX_DESC];
     WorkGroup grp[MAX_GROUPS];
     int n_desc, n_groups, H_q, H_kv, S_suf, q_f16;
-    int total_tiles;        // sum over items of vtiles
-    int tpw;                // tiles per prefix worker
+    int total_tiles;        // dense: sum over items of vtiles
+    int tpw;                // dense: tiles per prefix worker
     int n_workers;          // prefix workers (warps)
     int n_suf;              // suffix pieces per item (ceil(S_suf / 16))
     int sparse;             // 1: item sequences come from sel_blocks
     int tiles_per_block;    // sparse: B / 16
     int sel_max;            // sparse: entries per group in sel_blocks
+    int max_units;          // sparse: upper bound of the units of one launch (clamps item_base)
+    const int* item_base;   // sparse: [n_items + 1] first unit (selected tile) of each item, written
+                            // by the selector; the workers split [0, item_base[n_items]) evenly
     float scale_log2;       // tau * log2(e)
     float* partials;        // workspace: [slots][GMAX][partial_stride(D)]
     int* counters;          // workspace: [n_items]

@@ -98,17 +98,23 @@ __device__ __forceinline__ void start_item(WState<FMT, D>& st, uint32_t* qsm, co
     float gs[C::NG];
 #pragma unroll
     for (int g = 0; g < C::NG; ++g) gs[g] = 0.f;
+    // every load first (one round trip), then the splits and the fragment stores
+    float2 xq[C::KS][2];
+#pragma unroll
+    for (int s = 0; s < C::KS; ++s)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int d0 = 16 * s + 8 * r + 2 * q;
+            if (qh < 0) xq[s][r] = make_float2(0.f, 0.f);
+            else if (p.q_f16) xq[s][r] = __half22float2(__ldg(reinterpret_cast<const __half2*>(reinterpret_cast<const __half*>(ds.Q) + qh * D + d0)));
+            else xq[s][r] = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(ds.Q) + qh * D + d0));
+        }
 #pragma unroll
     for (int s = 0; s < C::KS; ++s) {
         uint32_t a[4];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const int d0 = 16 * s + 8 * r + 2 * q;
-            float x0 = 0.f, x1 = 0.f;
-            if (qh >= 0) {
-                x0 = ld_q(ds.Q, p.q_f16, qh * D + d0) * p.scale_log2;
-                x1 = ld_q(ds.Q, p.q_f16, qh * D + d0 + 1) * p.scale_log2;
-            }
+            const float x0 = xq[s][r].x * p.scale_log2, x1 = xq[s][r].y * p.scale_log2;
             gs[s / 2] += x0 + x1;
             const float f = (FMT == FMT_I4 && r == 1) ? 0.0625f : 1.0f;
             split_hi_lo(x0 * f, x1 * f, a[2 * r], a[2 * r + 1]);
@@ -491,11 +497,29 @@ __device__ __forceinline__ void write_partial_i4(I4State<D, NCB>& st, float* P, 
 
 // ---------------------------------------------------------------- pieces, tickets and the merge
 
-__device__ __forceinline__ int item_pieces(const DecodeParams& p, int item) {
+// Units per prefix worker: host-computed when dense; for a sparse launch, the selector's total
+// split over all the prefix workers.
+__device__ __forceinline__ int worker_units(const DecodeParams& p, int total) {
+    return p.sparse ? max(1, (total + p.n_workers - 1) / p.n_workers) : p.tpw;
+}
+
+// The item's units [s, e) and the first prefix worker w0 whose range meets them; the pieces of
+// the item are those of workers w0 .. w0 + npref - 1 (npref = 0 when the item has no units).
+__device__ __forceinline__ void item_range(const DecodeParams& p, int item, int& w0, int& npref) {
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
-    const int s = p.desc[d].tile_off + grp * p.desc[d].vtiles;
-    const int e = s + p.desc[d].vtiles;
-    return (e - 1) / p.tpw - s / p.tpw + 1;
+    int s, e, tpw;
+    if (p.sparse) {
+        const int n_items = p.n_desc * p.n_groups;
+        s = min(max(__ldcg(p.item_base + item), 0), p.max_units);
+        e = min(max(__ldcg(p.item_base + item + 1), s), p.max_units);
+        tpw = worker_units(p, min(max(__ldcg(p.item_base + n_items), 0), p.max_units));
+    } else {
+        s = p.desc[d].tile_off + grp * p.desc[d].vtiles;
+        e = s + p.desc[d].vtiles;
+        tpw = p.tpw;
+    }
+    w0 = s / tpw;
+    npref = e > s ? (e - 1) / tpw - w0 + 1 : 0;
 }
 
 // Merge of one (item, q head). Pieces are taken in batches of BP (16 float4 of o per lane, 32
@@ -508,10 +532,9 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
     const DecodeDesc& ds = p.desc[d];
     const WorkGroup& wg = p.grp[grp];
-    const int s = ds.tile_off + grp * ds.vtiles, e = s + ds.vtiles;
-    const int w0 = s / p.tpw, w1 = (e - 1) / p.tpw;
+    int w0, npref;
+    item_range(p, item, w0, npref);
     const int n_items = p.n_desc * p.n_groups;
-    const int npref = w1 - w0 + 1;
     const int npieces = npref + p.n_suf;
     constexpr int PSTR = GMAX * partial_stride(D);
     auto piece = [&](int k) -> const float* {
@@ -639,89 +662,174 @@ __device__ void finish_piece_i4(I4State<D, NCB>& st, const DecodeParams& p, int 
 
 // ---------------------------------------------------------------- tile cursor over a worker range
 
+// A worker walks a contiguous range of units. Dense: a unit is one of the item's resident tiles
+// (items laid end to end, host-computed ranges). Sparse: a unit is one tile of a block that the
+// item's selection list holds, in list order; the selector wrote each item's first unit
+// (item_base), and the workers split [0, total) evenly on the device. The cursor keeps what a
+// chunk needs of the current item in registers, so a chunk reads no launch parameter.
 struct Cursor {
-    int t, t_end, d, grp, item_start, item_end;
-    int sel_blk, sel_msk;   // sparse, lists of <= 32 blocks: lane l holds entry l of the item's list
+    int t, t_end;            // current unit, end of the worker's range
+    int item, d, grp;        // current item (= d * n_groups + grp)
+    int item_start, item_end;
+    int ntiles, N, nq;
+    const uint8_t* kbase;    // fp16: K region of the item's kv head; mlx4g32: the kv head's tiles
+    size_t vofs;             // fp16: bytes from the K region to the V region
+    int sel_blk, sel_msk;    // sparse, lists of <= 32 blocks: lane l holds entry l of the item's list
+    int win, win_lo;         // sparse: lane l holds item_base[win_lo + l]
 };
-
-// Sparse queries whose selection lists fit a warp keep the current item's list in registers
-// (one entry per lane, read by shuffles), so a chunk does not wait on a global load for its block.
-__device__ __forceinline__ void cursor_load_sel(const DecodeParams& p, Cursor& c) {
-    if (!p.sparse || p.sel_max > 32) return;
-    const int lane = threadIdx.x & 31;
-    const DecodeDesc& ds = p.desc[c.d];
-    const int base = c.grp * p.sel_max;
-    c.sel_blk = lane < p.sel_max ? ds.sel_blocks[base + lane] : -1;
-    c.sel_msk = lane < p.sel_max ? ds.sel_mask[base + lane] : 0;
-}
 
 struct Chunk {
     int item, d, grp;
     int tile;     // first real tile (within the kv head) of the chunk
-    int nreal;    // tiles to copy and compute (0: nothing, e.g. an empty sparse slot)
-    int slot_blk; // sparse: index of the block in the group's selection list
+    int nreal;    // tiles to copy and compute
+    int valid;    // tokens of the prefix from the chunk's first token on
+    int nq;       // q heads of the item
+    uint32_t mask;// bit h: local q head h attends to this chunk's tokens
     bool last;    // last chunk of this worker's piece of the item
     const uint8_t* src;   // mlx4g32: the tiles; fp16: the K region part
     const uint8_t* src2;  // fp16: the V region part
 };
 
+__device__ __forceinline__ int units_total(const DecodeParams& p) {
+    const int n_items = p.n_desc * p.n_groups;
+    return min(max(__ldcg(p.item_base + n_items), 0), p.max_units);
+}
+
+// item_base[i], clamped into [0, max_units] (read from the lane window, reloaded when i leaves it)
+__device__ __forceinline__ int cursor_base(const DecodeParams& p, Cursor& c, int i) {
+    const int n_items = p.n_desc * p.n_groups;
+    if (i - c.win_lo > 31 || i < c.win_lo) {
+        const int lane = threadIdx.x & 31;
+        c.win_lo = i;
+        c.win = min(max(__ldcg(p.item_base + min(i + lane, n_items)), 0), p.max_units);
+    }
+    return __shfl_sync(0xffffffffu, c.win, i - c.win_lo);
+}
+
+template <int FMT, int D>
+__device__ __forceinline__ void cursor_set_item(const DecodeParams& p, Cursor& c) {
+    const DecodeDesc& ds = p.desc[c.d];
+    const WorkGroup& wg = p.grp[c.grp];
+    c.ntiles = ds.ntiles;
+    c.N = ds.N;
+    c.nq = wg.nq;
+    if constexpr (FMT == FMT_FP16) {
+        c.vofs = fp16_region_bytes(ds.ntiles, D);
+        c.kbase = ds.kv + (size_t)wg.g * 2 * c.vofs;
+    } else {
+        c.vofs = 0;
+        c.kbase = ds.kv + (size_t)wg.g * ds.ntiles * tile_bytes(FMT_I4, D);
+    }
+    if (FMT == FMT_FP16 && p.sparse && p.sel_max <= 32) {
+        const int lane = threadIdx.x & 31;
+        const int base = c.grp * p.sel_max;
+        c.sel_blk = lane < p.sel_max ? ds.sel_blocks[base + lane] : -1;
+        c.sel_msk = lane < p.sel_max ? ds.sel_mask[base + lane] : 0;
+    }
+}
+
+// Sparse: make `i` (or the first non-empty item after it) the current item; units >= t exist.
+template <int FMT, int D>
+__device__ __forceinline__ void cursor_enter_sparse(const DecodeParams& p, Cursor& c, int i) {
+    const int n_items = p.n_desc * p.n_groups;
+    int e = cursor_base(p, c, i + 1);
+    while (e <= c.t && i + 1 < n_items) {   // skip items that end at or before t (empty ones)
+        ++i;
+        e = cursor_base(p, c, i + 1);
+    }
+    c.item = i;
+    c.item_start = cursor_base(p, c, i);
+    c.item_end = e;
+    c.d = i / p.n_groups;
+    c.grp = i - c.d * p.n_groups;
+    cursor_set_item<FMT, D>(p, c);
+}
+
+// Position a cursor at unit t (the first of worker w's range).
+template <int FMT, int D>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
-    int d = 0;
-    while (d + 1 < p.n_desc && p.desc[d + 1].tile_off <= c.t) ++d;
-    const int vt = p.desc[d].vtiles;
-    const int grp = (c.t - p.desc[d].tile_off) / vt;
-    c.d = d;
-    c.grp = grp;
-    c.item_start = p.desc[d].tile_off + grp * vt;
-    c.item_end = c.item_start + vt;
-    cursor_load_sel(p, c);
+    if (FMT != FMT_FP16 || !p.sparse) {
+        int d = 0;
+        while (d + 1 < p.n_desc && p.desc[d + 1].tile_off <= c.t) ++d;
+        const int vt = p.desc[d].vtiles;
+        const int grp = (c.t - p.desc[d].tile_off) / vt;
+        c.d = d;
+        c.grp = grp;
+        c.item = d * p.n_groups + grp;
+        c.item_start = p.desc[d].tile_off + grp * vt;
+        c.item_end = c.item_start + vt;
+        cursor_set_item<FMT, D>(p, c);
+        return;
+    }
+    // the largest item i with item_base[i] <= t: a 32-way search over item_base
+    const int n_items = p.n_desc * p.n_groups;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = n_items;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = lo + lane * step;
+        const bool ok = idx < hi && min(max(__ldcg(p.item_base + idx), 0), p.max_units) <= c.t;
+        const unsigned b = __ballot_sync(0xffffffffu, ok);   // a prefix of the lanes (lane 0 always)
+        const int k = 31 - __clz(b | 1u);
+        lo += k * step;
+        hi = min(hi, lo + step);
+    }
+    c.win_lo = -64;   // empty window
+    cursor_enter_sparse<FMT, D>(p, c, lo);
 }
 
 template <int FMT, int D, int TPS, int TB>
 __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Chunk& ch) {
     if (c.t >= c.t_end) return false;
+    constexpr bool CAN_SPARSE = FMT == FMT_FP16;   // sparse launches hold fp16 slots
     if (c.t >= c.item_end) {
-        if (++c.grp == p.n_groups) { c.grp = 0; ++c.d; }
-        c.item_start = p.desc[c.d].tile_off + c.grp * p.desc[c.d].vtiles;
-        c.item_end = c.item_start + p.desc[c.d].vtiles;
-        cursor_load_sel(p, c);
+        if (!CAN_SPARSE || !p.sparse) {
+            if (++c.grp == p.n_groups) { c.grp = 0; ++c.d; }
+            c.item = c.d * p.n_groups + c.grp;
+            c.item_start = p.desc[c.d].tile_off + c.grp * p.desc[c.d].vtiles;
+            c.item_end = c.item_start + p.desc[c.d].vtiles;
+            cursor_set_item<FMT, D>(p, c);
+        } else {
+            cursor_enter_sparse<FMT, D>(p, c, c.item + 1);
+        }
     }
-    const DecodeDesc& ds = p.desc[c.d];
     const int local = c.t - c.item_start;
     const int lim = min(c.t_end, c.item_end) - c.t;
     int n;
-    if (!p.sparse) {
+    if (!CAN_SPARSE || !p.sparse) {
         n = min(TPS, lim);
         ch.tile = local;
         ch.nreal = n;
-        ch.slot_blk = 0;
+        ch.mask = 0xFFu;
     } else {
-        // The item's virtual tiles visit its selection list slot by slot, tile by tile (slot
-        // local % sel_max, tile local / sel_max of that block): the list's real blocks come
-        // first and its empty slots last, so this spreads the real tiles evenly over the
-        // workers' contiguous ranges. One tile per chunk.
-        const int bs = local % p.sel_max, within = local / p.sel_max;
+        // unit `local` of the item: tile `local % tpb` of the block in list slot `local / tpb`
+        // (every slot before the item's last holds a whole block; the last may be the ragged end)
+        const int slot = min(max(local / p.tiles_per_block, 0), p.sel_max - 1);
+        const int within = local - (local / p.tiles_per_block) * p.tiles_per_block;
         n = 1;
-        const int blk = p.sel_max <= 32 ? __shfl_sync(0xffffffffu, c.sel_blk, bs) : ds.sel_blocks[c.grp * p.sel_max + bs];
-        ch.slot_blk = bs;
-        if (blk < 0) {
-            ch.tile = 0;
-            ch.nreal = 0;
+        int blk, msk;
+        if (p.sel_max <= 32) {
+            blk = __shfl_sync(0xffffffffu, c.sel_blk, slot & 31);
+            msk = __shfl_sync(0xffffffffu, c.sel_msk, slot & 31);
         } else {
-            ch.tile = blk * p.tiles_per_block + within;
-            ch.nreal = max(0, min(n, ds.ntiles - ch.tile));
+            const DecodeDesc& ds = p.desc[c.d];
+            blk = ds.sel_blocks[c.grp * p.sel_max + slot];
+            msk = ds.sel_mask[c.grp * p.sel_max + slot];
         }
+        ch.tile = max(blk, 0) * p.tiles_per_block + within;
+        ch.nreal = blk >= 0 && within >= 0 && ch.tile < c.ntiles ? 1 : 0;
+        ch.mask = static_cast<uint32_t>(msk);
     }
-    ch.item = c.d * p.n_groups + c.grp;
+    ch.item = c.item;
     ch.d = c.d;
     ch.grp = c.grp;
+    ch.nq = c.nq;
+    ch.valid = c.N - ch.tile * TILE_TOK;
     if constexpr (FMT == FMT_FP16) {
-        const size_t reg = fp16_region_bytes(ds.ntiles, D);
-        const uint8_t* base = ds.kv + (size_t)p.grp[c.grp].g * 2 * reg;
-        ch.src = base + (size_t)ch.tile * 32 * D;
-        ch.src2 = base + reg + (size_t)ch.tile * 32 * D;
+        ch.src = c.kbase + (size_t)ch.tile * 32 * D;
+        ch.src2 = c.kbase + c.vofs + (size_t)ch.tile * 32 * D;
     } else {
-        ch.src = ds.kv + ((size_t)p.grp[c.grp].g * ds.ntiles + ch.tile) * TB;
+        ch.src = c.kbase + (size_t)ch.tile * TB;
         ch.src2 = nullptr;
     }
     c.t += n;
@@ -736,10 +844,12 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     using C = DCfg<FMT, D>;
     using StateT = std::conditional_t<FMT == FMT_FP16, WState<FMT_FP16, D>, I4State<D, NCB>>;
     Cursor cons;
-    cons.t = w * p.tpw;
-    cons.t_end = min(p.total_tiles, cons.t + p.tpw);
+    const int total = FMT == FMT_FP16 && p.sparse ? units_total(p) : p.total_tiles;
+    const int tpw = worker_units(p, total);
+    cons.t = w * tpw;
+    cons.t_end = min(total, cons.t + tpw);
     if (cons.t >= cons.t_end) return;
-    cursor_seek(p, cons);
+    cursor_seek<FMT, D>(p, cons);
     Cursor prod = cons;
 
     const uint32_t ring_s = smem_u32(ring);
@@ -781,12 +891,10 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     uint32_t phase = 0;
     Chunk c;
     while (cursor_next<FMT, D, C::TPS, C::TB>(p, cons, c)) {
-        const DecodeDesc& ds = p.desc[c.d];
-        const WorkGroup& wg = p.grp[c.grp];
         if (c.item != cur_item) {
             cur_item = c.item;
-            if constexpr (FMT == FMT_FP16) start_item<FMT_FP16, D>(st, qsm, p, ds, wg, lane);
-            else start_item_i4<D, NCB>(st, p, ds, wg, lane);
+            if constexpr (FMT == FMT_FP16) start_item<FMT_FP16, D>(st, qsm, p, p.desc[c.d], p.grp[c.grp], lane);
+            else start_item_i4<D, NCB>(st, p, p.desc[c.d], p.grp[c.grp], lane);
         }
         if (!mbar_wait_bounded(bar_s + 8 * stage, (phase >> stage) & 1u)) {
             set_err(p.err, 1);
@@ -797,26 +905,23 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
             return;
         }
         --inflight;
-        uint32_t head_mask = 0xFFu;   // bit h: local q head h attends to this chunk's tokens
-        if (p.sparse && c.nreal > 0)
-            head_mask = p.sel_max <= 32 ? __shfl_sync(0xffffffffu, cons.sel_msk, c.slot_blk)
-                                        : ds.sel_mask[c.grp * p.sel_max + c.slot_blk];
-        const bool head_ok = (lane >> 2) < wg.nq && ((head_mask >> (lane >> 2)) & 1u);
+        const uint32_t head_mask = c.mask;   // bit h: local q head h attends to this chunk's tokens
+        const bool head_ok = (lane >> 2) < c.nq && ((head_mask >> (lane >> 2)) & 1u);
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {
-            const int valid = ds.N - (c.tile + k) * TILE_TOK;
+            const int valid = c.valid - k * TILE_TOK;
             if constexpr (FMT == FMT_FP16) {
                 SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
                 tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
             } else {
                 if (D <= 128 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
-                    tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                    tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
                     k += 3;
                 } else if (k + 1 < c.nreal) {   // two tiles per softmax step
-                    tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                    tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
                     ++k;
                 } else {
-                    tile_i4<D, NCB, 1>(st, sbuf + k * C::TB, lane, valid, head_mask, wg.nq);
+                    tile_i4<D, NCB, 1>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
                 }
             }
         }

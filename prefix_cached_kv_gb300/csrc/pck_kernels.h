@@ -44,7 +44,12 @@ struct SelSession {
 struct SelectParams {
     int q_f16;
     int H_q, H_kv, D, nb, K_top, K_eff, sel_max, n_groups, n_sess;
+    int tpb;                 // 16-token tiles per block (B / 16)
+    int ntiles;              // tiles of the slots (ceil(N / 16))
     float tau;
+    int* item_cnt;           // [n_sess * n_groups] selected tiles of each (session, group) item
+    int* item_base;          // [n_sess * n_groups + 1] exclusive prefix of item_cnt (the decode's units)
+    unsigned* done;          // select CTAs finished (the last one writes item_base and resets it)
     int8_t head_map[PCK_MAXH];
     WorkGroup grp[MAX_GROUPS];
     SelSession sess[MAX_DESC];

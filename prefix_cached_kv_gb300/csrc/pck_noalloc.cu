@@ -72,7 +72,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
                                           void* stream) {
     using namespace pck;
     if (!K_rec || !V_rec || !Q || !O) return PCK_EINVAL;
-    if (reinterpret_cast<uintptr_t>(O) & 15) return PCK_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(Q)) & 15) return PCK_EINVAL;
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || H_q < 1 || H_q > PCK_MAX_HEADS || N < 1 || S_suf < 0) return PCK_EINVAL;
     if (D != 64 && D != 128 && D != 256) return PCK_EUNSUPPORTED;
     if (q_dtype != PCK_DT_F32 && q_dtype != PCK_DT_F16) return PCK_EINVAL;
