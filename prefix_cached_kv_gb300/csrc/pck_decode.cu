@@ -968,6 +968,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __gr
     // the merge kernel (launched after this one with programmatic dependence) may be scheduled as
     // this grid's CTAs retire; it still waits for the whole grid before reading any partial
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid may itself be launched early (programmatic dependence on the previous kernel of
+    // the stream, e.g. the sparse selector): nothing is read before that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * DECODE_WARPS + warp;
     uint8_t* ring = smem + warp * C::RING;
@@ -992,8 +995,17 @@ static cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    decode_kernel<FMT, D, NCB><<<n_ctas, DECODE_WARPS * 32, C::SMEM, st>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3(n_ctas);
+    dc.blockDim = dim3(DECODE_WARPS * 32);
+    dc.dynamicSmemBytes = C::SMEM;
+    dc.stream = st;
+    dc.attrs = pdl;
+    dc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&dc, decode_kernel<FMT, D, NCB>, p);
     if (e != cudaSuccess) return e;
     // the merge of the partials, overlapping its launch with the decode's tail
     const int pairs = p.n_desc * p.n_groups * GMAX;

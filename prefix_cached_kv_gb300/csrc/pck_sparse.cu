@@ -29,36 +29,27 @@ __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int
     }
 }
 
-// score[h, b] = tau * q_h . K_mean[head_map[h], b]. One warp per (session, kv head, 8 consecutive
-// blocks): the 8 blocks' means (8 KB at D = 256) are read with 16-byte loads that are all in
-// flight together, then dotted with the kv head's q heads, 4 at a time. The 8 x 4 per-lane dot
-// products are summed over the lanes by a reduce-scatter (31 shuffles for 32 sums), after which
-// lane l holds block l / 4 and head l % 4 of the batch.
-constexpr int SCORE_BPW = 8;
+// ---------------------------------------------------------------- block scoring
+
+// The selector is one launch. A CTA scores a slab of SCORE_BPC consecutive blocks of one
+// (session, kv head): one bulk copy brings the slab's block means (64 KB at D = 256) into shared
+// memory, then each warp dots 8 blocks with the kv head's q heads, 4 at a time, and sums the
+// 8 x 4 per-lane products over the lanes by a reduce-scatter (31 shuffles for 32 sums; lane l
+// ends with block l / 4, head l % 4): score[h, b] = tau * q_h . K_mean[head_map[h], b].
+// The last CTA of a (session, kv head) to finish its slab then selects for that kv head's work
+// groups (below), and the one that completes the last item writes the items' unit offsets.
+constexpr int SEL_WARPS = 4;                           // warps per CTA (q heads taken in turn when selecting)
+constexpr int SCORE_BPW = 8;                           // blocks per warp
+constexpr int SCORE_BPC = SEL_WARPS * SCORE_BPW;       // blocks per CTA
 
 template <int D>
-__global__ void __launch_bounds__(128) block_scores_kernel(const __grid_constant__ SelectParams p) {
+__device__ __forceinline__ void score_blocks(const SelectParams& p, const SelSession& ss, int g, int b0, int nbl,
+                                             const float* kslab, int lane) {
     constexpr int F4 = D / 4;                  // float4 per block mean
     constexpr int L4 = SCORE_BPW * F4 / 32;    // float4 per lane (16, 8, 4 for D = 256, 128, 64)
     constexpr int QN = F4 >= 32 ? F4 / 32 : 1; // float4 of one q head per lane
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    // the select launch that follows counts its finished CTAs from zero
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.done = 0u;
-    const int nbw = (p.nb + SCORE_BPW - 1) / SCORE_BPW;   // warps per (session, kv head)
-    const int per_sess = p.H_kv * nbw;
-    if (warp >= p.n_sess * per_sess) return;
-    const int si = warp / per_sess, wl = warp - si * per_sess;
-    const SelSession& ss = p.sess[si];
-    const int g = wl / nbw, b0 = (wl - g * nbw) * SCORE_BPW;
-    const int nbl = min(SCORE_BPW, p.nb - b0);
     // float4 e = lane + 32 k of the warp's blocks: block e / F4, float4 e % F4 of that block
-    const float4* km = reinterpret_cast<const float4*>(ss.kmean + ((size_t)g * p.nb + b0) * D);
-    float4 kv[L4];
-#pragma unroll
-    for (int k = 0; k < L4; ++k) {
-        const int e = lane + 32 * k;
-        kv[k] = e / F4 < nbl ? __ldg(km + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const float4* km = reinterpret_cast<const float4*>(kslab);
     const int hb = lane + 32 < p.H_q ? p.head_map[lane + 32] : -1;
     const int ha = lane < p.H_q ? p.head_map[lane] : -1;
     uint64_t heads = (static_cast<uint64_t>(__ballot_sync(0xffffffffu, hb == g)) << 32) |
@@ -93,13 +84,15 @@ __global__ void __launch_bounds__(128) block_scores_kernel(const __grid_constant
         for (int v = 0; v < 32; ++v) acc[v] = 0.f;
 #pragma unroll
         for (int k = 0; k < L4; ++k) {
+            const int e = lane + 32 * k;
+            const float4 kv = e / F4 < nbl ? km[e] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float4 q = qv[j][F4 >= 32 ? k % QN : 0];
-                float x = kv[k].x * q.x;
-                x = fmaf(kv[k].y, q.y, x);
-                x = fmaf(kv[k].z, q.z, x);
-                x = fmaf(kv[k].w, q.w, x);
+                float x = kv.x * q.x;
+                x = fmaf(kv.y, q.y, x);
+                x = fmaf(kv.z, q.z, x);
+                x = fmaf(kv.w, q.w, x);
                 if constexpr (F4 >= 32) {
                     acc[(k / (F4 / 32)) * 4 + j] += x;
                 } else {   // D = 64: lanes 0-15 hold block 2k, lanes 16-31 block 2k + 1
@@ -125,205 +118,280 @@ __global__ void __launch_bounds__(128) block_scores_kernel(const __grid_constant
     }
 }
 
-__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
-    return sa > sb || (sa == sb && ia < ib);
+// Selection order: higher score first, ties to the lower block index. A score and its block
+// become one 64-bit key whose unsigned order is that order (the float's bits made monotone,
+// then the block index inverted), so every comparison below is a branch-free integer compare.
+// Key 0 stands for "no block".
+__device__ __forceinline__ uint64_t score_key(float s, int b) {
+    const uint32_t u = __float_as_uint(s == 0.f ? 0.f : s);   // -0 ties with +0
+    const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<uint64_t>(o) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(b));
+}
+__device__ __forceinline__ int key_block(uint64_t k) { return static_cast<int>(~static_cast<uint32_t>(k)); }
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
+    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v), src);
+    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl64_xor(uint64_t v, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t max32(const uint64_t (&k)[32]) {   // a depth-5 tree
+    uint64_t t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = umax64(k[2 * i], k[2 * i + 1]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = umax64(t[2 * i], t[2 * i + 1]);
+    return t[0];
 }
 
-// Top-K of one q head's nb <= 1024 scores held 32 per lane (block b = lane + 32 i), when
-// K <= 32: every lane finds its best element; the K-th best of those 32 lane bests, T, bounds
-// the answer (the K lane bests ranked 0..K-1 are all at least T, so the K-th best score is too),
-// so the top K are among the elements at least as good as T. When there are at most 32 of them
-// they are gathered and each one's rank among them is its place; otherwise (many ties) the
-// caller falls back to K rounds of arg-max. Order: higher score first, ties to the lower index.
-__device__ __forceinline__ bool topk_by_threshold(const float (&reg)[32], int nb, int K, int lane, float* cs, int* ci,
+// Top-K of one q head's keys held 32 per lane, when K <= 32: every lane takes its best key;
+// the K-th best of those 32 lane bests, T, bounds the answer (the K lane bests ranked 0..K-1
+// are all >= T, so the K-th best key is too), so the top K are among the keys >= T. When
+// there are at most 32 of them they are gathered and each one's rank among them is its place;
+// otherwise (many ties) the caller falls back to K rounds of arg-max. picks[r] = r-th best.
+__device__ __forceinline__ bool topk_by_threshold(const uint64_t (&key)[32], int K, int lane, uint64_t* cand,
                                                   int* picks) {
-    constexpr int NONE = 0x7fffffff;
-    float lb = -INFINITY;
-    int li = NONE;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int b = lane + 32 * i;
-        if (b < nb && (li == NONE || better(reg[i], b, lb, li))) { lb = reg[i]; li = b; }
-    }
+    const uint64_t m = max32(key);
     int rank = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float os = __shfl_sync(0xffffffffu, lb, j);
-        const int oi = __shfl_sync(0xffffffffu, li, j);
-        if (oi != NONE && (li == NONE || better(os, oi, lb, li))) ++rank;
-    }
-    const unsigned at = __ballot_sync(0xffffffffu, li != NONE && rank == K - 1);
+    for (int j = 0; j < 32; ++j) rank += shfl64(m, j) > m ? 1 : 0;
+    const unsigned at = __ballot_sync(0xffffffffu, m != 0 && rank == K - 1);
     if (at == 0u) return false;
-    const int src = __ffs(at) - 1;
-    const float Ts = __shfl_sync(0xffffffffu, lb, src);
-    const int Ti = __shfl_sync(0xffffffffu, li, src);
+    const uint64_t T = shfl64(m, __ffs(at) - 1);
     int cnt = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int b = lane + 32 * i;
-        cnt += (b < nb && (b == Ti || better(reg[i], b, Ts, Ti))) ? 1 : 0;
-    }
+    for (int i = 0; i < 32; ++i) cnt += key[i] >= T ? 1 : 0;
     int pre = cnt;   // inclusive scan over lanes
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int x = __shfl_up_sync(0xffffffffu, pre, o);
-        if (lane >= o) pre += x;
+        pre += lane >= o ? x : 0;
     }
     const int C = __shfl_sync(0xffffffffu, pre, 31);
     if (C > 32) return false;
     int pos = pre - cnt;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const int b = lane + 32 * i;
-        if (b < nb && (b == Ti || better(reg[i], b, Ts, Ti))) { cs[pos] = reg[i]; ci[pos] = b; ++pos; }
+        if (key[i] >= T) cand[pos] = key[i];
+        pos += key[i] >= T ? 1 : 0;
     }
     __syncwarp();
     if (lane < C) {
-        const float s = cs[lane];
-        const int b = ci[lane];
+        const uint64_t k = cand[lane];
         int r = 0;
-        for (int k = 0; k < C; ++k) r += better(cs[k], ci[k], s, b) ? 1 : 0;
-        if (r < K) picks[r] = b;
+        for (int j = 0; j < C; ++j) r += cand[j] > k ? 1 : 0;
+        if (r < K) picks[r] = key_block(k);
     }
     __syncwarp();
     return true;
 }
 
-// One CTA per (work group, session): warp w selects the top-K of the group's w-th q head and
-// sorts it ascending; then the CTA forms the group's sorted union of blocks, with a mask of the
-// q heads that chose each, and the number of resident tiles the union covers (the item's units
-// in the gather decode). The last CTA of the launch to finish turns the items' counts into
-// their exclusive prefix (item_base), from which the decode's workers split the units evenly.
-__global__ void __launch_bounds__(GMAX * 32) select_kernel(const __grid_constant__ SelectParams p) {
-    __shared__ int picks[GMAX][64];
-    __shared__ int sorted[GMAX][64];
-    __shared__ float cand_s[GMAX][32];
-    __shared__ int cand_i[GMAX][32];
-    __shared__ uint8_t first[GMAX * 64];
-    __shared__ int s_cnt, s_last;
-    __shared__ int s_scan[GMAX * 32];
-    const int grp = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SelSession& ss = p.sess[blockIdx.y];
+struct SelShared {
+    int picks[GMAX][64];
+    int sorted[GMAX][64];
+    uint64_t cand[GMAX][32];
+    uint8_t first[GMAX * 64];
+    int scan[64];
+    int cnt, last, nuniq;
+};
+
+// Selection for work group `grp` of session si, by a whole CTA (SEL_WARPS warps): warp w takes
+// the top-K of the group's q heads w, w + SEL_WARPS, ... and sorts each ascending; then the CTA forms the group's
+// sorted union of blocks, with a mask of the q heads that chose each, and the number of
+// resident tiles the union covers (the item's units in the gather decode). The CTA that
+// completes the last item of the launch turns the items' counts into their exclusive prefix
+// (item_base), from which the decode's workers split the units evenly.
+__device__ void select_group(const SelectParams& p, int si, int grp, SelShared& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const SelSession& ss = p.sess[si];
     const WorkGroup& wg = p.grp[grp];
     const int K = p.K_eff;
-    if (threadIdx.x == 0) s_cnt = 0;
-    if (warp < wg.nq) {
-        const int h = wg.qh[warp];
+    if (threadIdx.x == 0) { sm.cnt = 0; sm.nuniq = 0; }
+    for (int hw = warp; hw < wg.nq; hw += SEL_WARPS) {
+        const int h = wg.qh[hw];
         const float* sc = ss.scores + (size_t)h * p.nb;
-        constexpr int RPL = 32;                 // scores held in registers per lane (nb <= 1024)
-        float reg[RPL];
+        constexpr int RPL = 32;                 // keys held in registers per lane (nb <= 1024)
+        uint64_t key[RPL];
         const bool in_regs = p.nb <= 32 * RPL;
         if (in_regs) {
 #pragma unroll
-            for (int i = 0; i < RPL; ++i) reg[i] = (lane + 32 * i < p.nb) ? sc[lane + 32 * i] : -INFINITY;
+            for (int i = 0; i < RPL; ++i) {
+                const int b = lane + 32 * i;
+                key[i] = b < p.nb ? score_key(__ldcg(sc + b), b) : 0ull;
+            }
         }
-        const bool fast = in_regs && K <= 32 && topk_by_threshold(reg, p.nb, K, lane, cand_s[warp], cand_i[warp], picks[warp]);
-        float prev_s = INFINITY;
-        int prev_i = -1;
+        const bool fast = in_regs && K <= 32 && topk_by_threshold(key, K, lane, sm.cand[hw], sm.picks[hw]);
+        uint64_t prev = ~0ull;   // K rounds of arg-max below the previous pick
         for (int r = 0; r < (fast ? 0 : K); ++r) {
-            float bs = -INFINITY;
-            int bi = 0x7fffffff;
+            uint64_t best = 0;
             if (in_regs) {
+                uint64_t below[RPL];
 #pragma unroll
-                for (int i = 0; i < RPL; ++i) {
-                    const int b = lane + 32 * i;
-                    const float s = reg[i];
-                    if (b < p.nb && better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
-                        bs = s;
-                        bi = b;
-                    }
-                }
+                for (int i = 0; i < RPL; ++i) below[i] = key[i] < prev ? key[i] : 0ull;
+                best = max32(below);
             } else {
                 for (int b = lane; b < p.nb; b += 32) {
-                    const float s = sc[b];
-                    if (better(prev_s, prev_i, s, b) && (bi == 0x7fffffff || better(s, b, bs, bi))) {
-                        bs = s;
-                        bi = b;
-                    }
+                    const uint64_t k = score_key(__ldcg(sc + b), b);
+                    best = umax64(best, k < prev ? k : 0ull);
                 }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (oi != 0x7fffffff && (bi == 0x7fffffff || better(os, oi, bs, bi))) {
-                    bs = os;
-                    bi = oi;
-                }
-            }
-            prev_s = bs;
-            prev_i = bi;
-            if (lane == 0) picks[warp][r] = bi;
+            for (int o = 16; o > 0; o >>= 1) best = umax64(best, shfl64_xor(best, o));
+            prev = best;
+            if (lane == 0) sm.picks[hw][r] = key_block(best);
         }
         __syncwarp();
         // ascending order: a pick's place is the number of (distinct) picks below it
         for (int k = lane; k < K; k += 32) {
-            const int v = picks[warp][k];
+            const int v = sm.picks[hw][k];
             int r = 0;
-            for (int j = 0; j < K; ++j) r += picks[warp][j] < v ? 1 : 0;
-            sorted[warp][r] = v;
+            for (int j = 0; j < K; ++j) r += sm.picks[hw][j] < v ? 1 : 0;
+            sm.sorted[hw][r] = v;
             if (ss.idx_out) ss.idx_out[(size_t)h * K + r] = v;
         }
     }
     __syncthreads();
-    // union: entry e = (head w, place k); the first head holding a block represents it
-    const int ne = wg.nq * K;
-    for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-        const int w = e / K, b = sorted[w][e - w * K];
-        bool f = true;
-        for (int w2 = 0; w2 < w; ++w2)
-            for (int k = 0; k < K; ++k) f = f && sorted[w2][k] != b;
-        first[e] = f ? 1 : 0;
+    // union: entry (w, k) = head w's k-th smallest pick; the first head holding a block stands
+    // for it. Lists are padded to 64 entries (index w * 64 + k, no divisions).
+    const int nq = wg.nq;
+    int nfirst = 0;
+    for (int e = threadIdx.x; e < nq * 64; e += blockDim.x) {
+        const int w = e >> 6, k = e & 63;
+        bool f = false;
+        if (k < K) {
+            const int b = sm.sorted[w][k];
+            f = true;
+            for (int w2 = 0; w2 < w; ++w2)
+                for (int k2 = 0; k2 < K; ++k2) f = f && sm.sorted[w2][k2] != b;
+        }
+        sm.first[e] = f ? 1 : 0;
+        nfirst += f ? 1 : 0;
     }
+    if (nfirst) atomicAdd(&sm.nuniq, nfirst);
     __syncthreads();
+    const int nuniq = sm.nuniq;
     int* out_b = ss.sel_blocks + (size_t)grp * p.sel_max;
     uint8_t* out_m = ss.sel_mask + (size_t)grp * p.sel_max;
-    int nuniq = 0;
-    for (int e = 0; e < ne; ++e) nuniq += first[e];
-    for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-        if (!first[e]) continue;
-        const int w = e / K, b = sorted[w][e - w * K];
-        int rank = 0;
-        for (int e2 = 0; e2 < ne; ++e2) rank += (first[e2] && sorted[e2 / K][e2 % K] < b) ? 1 : 0;
-        uint8_t m = 0;
-        for (int w2 = 0; w2 < wg.nq; ++w2)
-            for (int k = 0; k < K; ++k)
-                if (sorted[w2][k] == b) m |= uint8_t(1u << w2);
+    for (int e = threadIdx.x; e < nq * 64; e += blockDim.x) {
+        if (!sm.first[e]) continue;
+        const int b = sm.sorted[e >> 6][e & 63];
+        int rank = 0;   // distinct blocks below b
+        uint32_t m = 0;
+        for (int w2 = 0; w2 < nq; ++w2)
+            for (int k2 = 0; k2 < K; ++k2) {
+                const int v = sm.sorted[w2][k2];
+                rank += (sm.first[w2 * 64 + k2] && v < b) ? 1 : 0;
+                m |= (v == b ? 1u : 0u) << w2;
+            }
         out_b[rank] = b;
-        out_m[rank] = m;
-        atomicAdd(&s_cnt, min(p.tpb, p.ntiles - b * p.tpb));
+        out_m[rank] = static_cast<uint8_t>(m);
+        atomicAdd(&sm.cnt, min(p.tpb, p.ntiles - b * p.tpb));
     }
     for (int n = nuniq + threadIdx.x; n < p.sel_max; n += blockDim.x) { out_b[n] = -1; out_m[n] = 0; }
     __syncthreads();
     const int n_items = p.n_sess * p.n_groups;
     if (threadIdx.x == 0) {
-        p.item_cnt[blockIdx.y * p.n_groups + grp] = s_cnt;
+        p.item_cnt[si * p.n_groups + grp] = sm.cnt;
         __threadfence();
         const unsigned old = atomicAdd(p.done, 1u);
-        s_last = old == static_cast<unsigned>(n_items) - 1u;
+        sm.last = old == static_cast<unsigned>(n_items) - 1u;
     }
     __syncthreads();
-    if (!s_last) return;
+    if (!sm.last) return;
     __threadfence();
-    // last CTA: exclusive prefix of the counts (a contiguous chunk per thread, then a block scan)
+    // last item: exclusive prefix of the counts (a contiguous chunk per thread, then a block scan)
     const int nt = blockDim.x, per = (n_items + nt - 1) / nt;
     const int i0 = min(n_items, (int)threadIdx.x * per), i1 = min(n_items, i0 + per);
     int sum = 0;
     for (int i = i0; i < i1; ++i) sum += __ldcg(p.item_cnt + i);
-    s_scan[threadIdx.x] = sum;
+    int x = sum;   // inclusive scan over the warp, then over the warps' totals
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.scan[warp] = x;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int t = 0; t < nt; ++t) { const int x = s_scan[t]; s_scan[t] = run; run += x; }
-        p.item_base[n_items] = run;
-        *p.done = 0u;
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int t = lane < nw ? sm.scan[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) sm.scan[32 + lane] = t;   // inclusive warp totals
+        if (lane == nw - 1) {
+            p.item_base[n_items] = t;
+            *p.done = 0u;   // ready for the next launch
+        }
     }
     __syncthreads();
-    int run = s_scan[threadIdx.x];
+    int run = x - sum + (warp > 0 ? sm.scan[32 + warp - 1] : 0);
     for (int i = i0; i < i1; ++i) {
         p.item_base[i] = run;
         run += __ldcg(p.item_cnt + i);
     }
+}
+
+// One CTA per (session, kv head, slab of SCORE_BPC blocks); SEL_WARPS warps.
+template <int D>
+__global__ void __launch_bounds__(SEL_WARPS * 32, 4) select_kernel(const __grid_constant__ SelectParams p) {
+    extern __shared__ __align__(128) uint8_t dsm[];   // the slab's block means, [SCORE_BPC][D] fp32
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ SelShared sm;
+    __shared__ int s_go;
+    // the caller's inputs (and, for a first query, the block means) come from earlier kernels
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbc = (p.nb + SCORE_BPC - 1) / SCORE_BPC;   // slabs per (session, kv head)
+    const int per_sess = p.H_kv * nbc;
+    const int si = blockIdx.x / per_sess, r = blockIdx.x - si * per_sess;
+    const int g = r / nbc, b0 = (r - g * nbc) * SCORE_BPC;
+    const int nbl = min(SCORE_BPC, p.nb - b0);
+    const SelSession& ss = p.sess[si];
+    const float* kslab = reinterpret_cast<const float*>(dsm);
+    const uint32_t bar_s = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bar_s, 1);
+        fence_mbar_init();
+        const uint32_t bytes = static_cast<uint32_t>(nbl) * D * 4;
+        mbar_arrive_expect_tx(bar_s, bytes);
+        bulk_g2s(smem_u32(dsm), ss.kmean + ((size_t)g * p.nb + b0) * D, bytes, bar_s);
+        s_go = mbar_wait_bounded(bar_s, 0) ? 1 : 0;
+        if (!s_go) {
+            set_err(p.err, 6);
+            mbar_wait_bounded(bar_s, 0);   // let the copy land before the CTA leaves
+        }
+    }
+    __syncthreads();
+    if (s_go) {
+        const int wb0 = warp * SCORE_BPW;
+        if (wb0 < nbl) score_blocks<D>(p, ss, g, b0 + wb0, min(SCORE_BPW, nbl - wb0), kslab + (size_t)wb0 * D, lane);
+    }
+    __syncthreads();
+    // the decode grid may launch once every CTA got here; it waits for this grid's completion
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        __threadfence();   // this CTA's scores, before its count
+        const unsigned old = atomicAdd(p.gcount + si * p.H_kv + g, 1u);
+        s_go = old == static_cast<unsigned>(nbc) - 1u;
+        if (s_go) p.gcount[si * p.H_kv + g] = 0u;   // ready for the next launch
+    }
+    __syncthreads();
+    if (!s_go) return;
+    __threadfence();   // every slab of (si, g) is scored and visible
+    for (int gi = 0; gi < p.n_groups; ++gi)
+        if (p.grp[gi].g == g) {
+            select_group(p, si, gi, sm);
+            __syncthreads();
+        }
 }
 
 cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int ntiles, int B, float* kmean,
@@ -337,16 +405,31 @@ cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int nt
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
     (void)sms;
-    const int64_t warps = static_cast<int64_t>(p.n_sess) * p.H_kv * ((p.nb + SCORE_BPW - 1) / SCORE_BPW);
-    const unsigned ctas = static_cast<unsigned>((warps + 3) / 4);
-    if (p.D == 64) block_scores_kernel<64><<<ctas, 128, 0, st>>>(p);
-    else if (p.D == 128) block_scores_kernel<128><<<ctas, 128, 0, st>>>(p);
-    else if (p.D == 256) block_scores_kernel<256><<<ctas, 128, 0, st>>>(p);
-    else return cudaErrorInvalidValue;
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    select_kernel<<<dim3(p.n_groups, p.n_sess), GMAX * 32, 0, st>>>(p);
-    return cudaGetLastError();
+    const unsigned ctas = static_cast<unsigned>(p.n_sess * p.H_kv * ((p.nb + SCORE_BPC - 1) / SCORE_BPC));
+    const size_t smem = static_cast<size_t>(SCORE_BPC) * p.D * sizeof(float);
+    void (*kern)(SelectParams) = p.D == 64 ? select_kernel<64> : p.D == 128 ? select_kernel<128>
+                               : p.D == 256 ? select_kernel<256> : nullptr;
+    if (!kern) return cudaErrorInvalidValue;
+    static bool attr_set[3] = {false, false, false};
+    const int ai = p.D == 64 ? 0 : p.D == 128 ? 1 : 2;
+    if (!attr_set[ai]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set[ai] = true;
+    }
+    // programmatic dependent launch: the launch overlaps the previous kernel's tail; the kernel
+    // waits for that kernel's completion before reading anything
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t sc = {};
+    sc.gridDim = dim3(ctas);
+    sc.blockDim = dim3(SEL_WARPS * 32);
+    sc.dynamicSmemBytes = smem;
+    sc.stream = st;
+    sc.attrs = pdl;
+    sc.numAttrs = 1;
+    return cudaLaunchKernelEx(&sc, kern, p);
 }
 
 }  // namespace pck
