@@ -657,9 +657,7 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     sp.ntiles = slots[0]->ntiles;
     sp.item_cnt = item_cnt;
     sp.item_base = item_base;
-    // counters workspace: [0, n * H_kv) slab counts per (session, kv head), last word: items done
-    sp.done = reinterpret_cast<unsigned*>(c->counters + (WS_COUNTERS - 1));
-    sp.gcount = reinterpret_cast<unsigned*>(c->counters);
+    sp.done = reinterpret_cast<unsigned*>(c->counters + (WS_COUNTERS - 1));   // items selected so far
     sp.err = c->dev_err;
     static thread_local DescIn d[MAX_DESC];
     for (int i = 0; i < n; ++i) {

@@ -50,7 +50,6 @@ struct SelectParams {
     int* item_cnt;           // [n_sess * n_groups] selected tiles of each (session, group) item
     int* item_base;          // [n_sess * n_groups + 1] exclusive prefix of item_cnt (the decode's units)
     unsigned* done;          // items selected so far (the last one writes item_base and resets it)
-    unsigned* gcount;        // [n_sess * H_kv] slabs scored per (session, kv head); reset by the last
     int* err;                // device error word
     int8_t head_map[PCK_MAXH];
     WorkGroup grp[MAX_GROUPS];

@@ -7,6 +7,8 @@
 // selected indices are reported sorted ascending.
 #include <math.h>
 
+#include <algorithm>
+
 #include "pck_common.cuh"
 #include "pck_kernels.h"
 
@@ -207,7 +209,7 @@ struct SelShared {
 // resident tiles the union covers (the item's units in the gather decode). The CTA that
 // completes the last item of the launch turns the items' counts into their exclusive prefix
 // (item_base), from which the decode's workers split the units evenly.
-__device__ void select_group(const SelectParams& p, int si, int grp, SelShared& sm) {
+__device__ __forceinline__ void select_group(const SelectParams& p, int si, int grp, SelShared& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SelSession& ss = p.sess[si];
     const WorkGroup& wg = p.grp[grp];
@@ -340,12 +342,13 @@ __device__ void select_group(const SelectParams& p, int si, int grp, SelShared& 
     }
 }
 
-// One CTA per (session, kv head, slab of SCORE_BPC blocks); SEL_WARPS warps.
+// Scoring: one CTA of SEL_WARPS warps per slab (session, kv head, SCORE_BPC blocks): one bulk
+// copy brings the slab's block means into shared memory, each warp scores 8 blocks. No atomics:
+// a CTA leaves as soon as its scores are stored.
 template <int D>
-__global__ void __launch_bounds__(SEL_WARPS * 32, 4) select_kernel(const __grid_constant__ SelectParams p) {
+__global__ void __launch_bounds__(SEL_WARPS * 32, 4) score_kernel(const __grid_constant__ SelectParams p) {
     extern __shared__ __align__(128) uint8_t dsm[];   // the slab's block means, [SCORE_BPC][D] fp32
     __shared__ __align__(8) uint64_t bar;
-    __shared__ SelShared sm;
     __shared__ int s_go;
     // the caller's inputs (and, for a first query, the block means) come from earlier kernels
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -355,15 +358,13 @@ __global__ void __launch_bounds__(SEL_WARPS * 32, 4) select_kernel(const __grid_
     const int si = blockIdx.x / per_sess, r = blockIdx.x - si * per_sess;
     const int g = r / nbc, b0 = (r - g * nbc) * SCORE_BPC;
     const int nbl = min(SCORE_BPC, p.nb - b0);
-    const SelSession& ss = p.sess[si];
-    const float* kslab = reinterpret_cast<const float*>(dsm);
     const uint32_t bar_s = smem_u32(&bar);
     if (threadIdx.x == 0) {
         mbar_init(bar_s, 1);
         fence_mbar_init();
         const uint32_t bytes = static_cast<uint32_t>(nbl) * D * 4;
         mbar_arrive_expect_tx(bar_s, bytes);
-        bulk_g2s(smem_u32(dsm), ss.kmean + ((size_t)g * p.nb + b0) * D, bytes, bar_s);
+        bulk_g2s(smem_u32(dsm), p.sess[si].kmean + ((size_t)g * p.nb + b0) * D, bytes, bar_s);
         s_go = mbar_wait_bounded(bar_s, 0) ? 1 : 0;
         if (!s_go) {
             set_err(p.err, 6);
@@ -371,27 +372,21 @@ __global__ void __launch_bounds__(SEL_WARPS * 32, 4) select_kernel(const __grid_
         }
     }
     __syncthreads();
-    if (s_go) {
-        const int wb0 = warp * SCORE_BPW;
-        if (wb0 < nbl) score_blocks<D>(p, ss, g, b0 + wb0, min(SCORE_BPW, nbl - wb0), kslab + (size_t)wb0 * D, lane);
-    }
-    __syncthreads();
-    // the decode grid may launch once every CTA got here; it waits for this grid's completion
+    // the select grid may launch once every CTA got here; it waits for this grid's completion
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) {
-        __threadfence();   // this CTA's scores, before its count
-        const unsigned old = atomicAdd(p.gcount + si * p.H_kv + g, 1u);
-        s_go = old == static_cast<unsigned>(nbc) - 1u;
-        if (s_go) p.gcount[si * p.H_kv + g] = 0u;   // ready for the next launch
-    }
-    __syncthreads();
-    if (!s_go) return;
-    __threadfence();   // every slab of (si, g) is scored and visible
-    for (int gi = 0; gi < p.n_groups; ++gi)
-        if (p.grp[gi].g == g) {
-            select_group(p, si, gi, sm);
-            __syncthreads();
-        }
+    const int wb0 = warp * SCORE_BPW;
+    if (s_go && wb0 < nbl)
+        score_blocks<D>(p, p.sess[si], g, b0 + wb0, min(SCORE_BPW, nbl - wb0),
+                        reinterpret_cast<const float*>(dsm) + (size_t)wb0 * D, lane);
+}
+
+// Selection: one CTA per (work group, session), after the scoring grid has completed.
+__global__ void __launch_bounds__(SEL_WARPS * 32) select_kernel(const __grid_constant__ SelectParams p) {
+    __shared__ SelShared sm;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // every score is stored and visible
+    // the decode grid may launch now; it waits for this grid's completion
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    select_group(p, blockIdx.y, blockIdx.x, sm);
 }
 
 cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int ntiles, int B, float* kmean,
@@ -405,10 +400,10 @@ cudaError_t launch_block_means(const void* tiles, int H_kv, int N, int D, int nt
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
     (void)sms;
-    const unsigned ctas = static_cast<unsigned>(p.n_sess * p.H_kv * ((p.nb + SCORE_BPC - 1) / SCORE_BPC));
+    const int n_slabs = p.n_sess * p.H_kv * ((p.nb + SCORE_BPC - 1) / SCORE_BPC);
     const size_t smem = static_cast<size_t>(SCORE_BPC) * p.D * sizeof(float);
-    void (*kern)(SelectParams) = p.D == 64 ? select_kernel<64> : p.D == 128 ? select_kernel<128>
-                               : p.D == 256 ? select_kernel<256> : nullptr;
+    void (*kern)(SelectParams) = p.D == 64 ? score_kernel<64> : p.D == 128 ? score_kernel<128>
+                               : p.D == 256 ? score_kernel<256> : nullptr;
     if (!kern) return cudaErrorInvalidValue;
     static bool attr_set[3] = {false, false, false};
     const int ai = p.D == 64 ? 0 : p.D == 128 ? 1 : 2;
@@ -417,19 +412,27 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms) {
         if (e != cudaSuccess) return e;
         attr_set[ai] = true;
     }
-    // programmatic dependent launch: the launch overlaps the previous kernel's tail; the kernel
-    // waits for that kernel's completion before reading anything
+    // programmatic dependent launches: each grid's launch overlaps the previous kernel's tail,
+    // and each kernel waits for that kernel's completion before reading anything
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t sc = {};
-    sc.gridDim = dim3(ctas);
+    sc.gridDim = dim3(static_cast<unsigned>(n_slabs));
     sc.blockDim = dim3(SEL_WARPS * 32);
     sc.dynamicSmemBytes = smem;
     sc.stream = st;
     sc.attrs = pdl;
     sc.numAttrs = 1;
-    return cudaLaunchKernelEx(&sc, kern, p);
+    cudaError_t e = cudaLaunchKernelEx(&sc, kern, p);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t sl = {};
+    sl.gridDim = dim3(p.n_groups, p.n_sess);
+    sl.blockDim = dim3(SEL_WARPS * 32);
+    sl.stream = st;
+    sl.attrs = pdl;
+    sl.numAttrs = 1;
+    return cudaLaunchKernelEx(&sl, select_kernel, p);
 }
 
 }  // namespace pck
