@@ -259,7 +259,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
         total += static_cast<int64_t>(n_groups) * d.vtiles;
     }
     if (total >= (int64_t(1) << 30)) return fail(c, PCK_EUNSUPPORTED, "too many tiles in one launch");
-    const DecodeLaunchInfo& li = dinfo(c, fmt, D, fmt == PCK_FMT_MLX4G32 ? decode_ncb(p) : 1);
+    const DecodeLaunchInfo& li = dinfo(c, fmt, D, decode_ncb(p));
     const int n_suf_warps = n * n_groups * ((S_suf + TILE_TOK - 1) / TILE_TOK);
     // prefix workers and suffix warps together stay within one wave of resident warps
     int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS - n_suf_warps;

@@ -45,162 +45,93 @@ struct DCfg {
     static constexpr int TB = tile_bytes(FMT, D);
     static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 4 : 1));
     static constexpr int STAGE = TPS * TB;
-    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D == 256 ? 2 : 3) : 2;
-    static constexpr bool QSMEM = D > 128;  // q fragments live in shared memory (register budget)
-    static constexpr int QSMEM_BYTES = QSMEM ? KS * 32 * 16 : 0;
+    static constexpr int NSTAGE = FMT == FMT_FP16 ? 3 : 2;
     static constexpr int RING = NSTAGE * STAGE;
-    static constexpr int SMEM = DECODE_WARPS * (RING + QSMEM_BYTES) + DECODE_WARPS * NSTAGE * 8;
+    static constexpr int SMEM = DECODE_WARPS * RING + DECODE_WARPS * NSTAGE * 8;
 };
 
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 constexpr float LN2 = 0.69314718055994530942f;
 
-template <int D>
-struct QAStore {
+// ---------------------------------------------------------------- fp16 path (S^T orientation)
+
+// Lane l: tokens t = l/4 and t + 8 of each tile, head q = l%4 of each column block cb (heads
+// cb*4 .. cb*4+3 of the item); B fragments of q: column n = l/4 = (head n/2, hi or lo part n%2).
+template <int D, int NCB>
+struct F16State {
     static constexpr int KS = D / 16;
-    uint32_t r[D > 128 ? 1 : KS][4];
+    uint32_t qb[NCB][KS][2];   // B fragments of the item's q (tau*log2e prescaled), hi or lo part
+    float oacc[NCB][KS][4];    // O^T m-tile mt: d = 16mt + l/4 in [0..1], d + 8 in [2..3]; columns
+                               // 2q, 2q+1 = (hi, lo) of head cb*4 + q
+    float m_ref[NCB];
+    float l_part[NCB];
 };
 
-template <int FMT, int D>
-struct WState {
-    using C = DCfg<FMT, D>;
-    QAStore<D> qa;
-    float qsum[C::NG];
-    float oacc[C::NBV][4];
-    float bacc[C::NG];
-    float m_ref;
-    float l_part;
-};
-
-template <int D>
-__device__ __forceinline__ void get_qa(const QAStore<D>& qa, const uint32_t* qsm, int s, int lane, uint32_t (&a)[4]) {
-    if constexpr (D > 128) {
-        uint4 v = *reinterpret_cast<const uint4*>(qsm + (s * 32 + lane) * 4);
-        a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-    } else {
-        a[0] = qa.r[s][0]; a[1] = qa.r[s][1]; a[2] = qa.r[s][2]; a[3] = qa.r[s][3];
-    }
-}
-
-__device__ __forceinline__ float ld_q(const void* Q, int q_f16, int idx) {
-    return q_f16 ? __half2float(reinterpret_cast<const __half*>(Q)[idx]) : reinterpret_cast<const float*>(Q)[idx];
-}
-
-// Build the MMA A fragments of the item's q heads (rows l/4: hi, rows l/4+8: lo), prescaled by
-// tau*log2(e); for the mlx4g32 tier, d offsets 8..15 of every k-step are divided by 16 (those B
-// registers hold 16 * code).
-template <int FMT, int D>
-__device__ __forceinline__ void start_item(WState<FMT, D>& st, uint32_t* qsm, const DecodeParams& p,
-                                           const DecodeDesc& ds, const WorkGroup& wg, int lane) {
-    using C = DCfg<FMT, D>;
-    const int q = lane & 3, h = lane >> 2;
-    const int qh = h < wg.nq ? wg.qh[h] : -1;
-    float gs[C::NG];
+// The item's q fragments: every load first (one round trip), then the hi / lo splits.
+template <int D, int NCB>
+__device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const DecodeParams& p, const DecodeDesc& ds,
+                                               const WorkGroup& wg, int lane) {
+    constexpr int KS = D / 16;
+    const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
+    float2 xq[NCB][KS][2];
 #pragma unroll
-    for (int g = 0; g < C::NG; ++g) gs[g] = 0.f;
-    // every load first (one round trip), then the splits and the fragment stores
-    float2 xq[C::KS][2];
+    for (int cb = 0; cb < NCB; ++cb) {
+        const int h = cb * 4 + hl;
+        const int qh = h < wg.nq ? wg.qh[h] : -1;
 #pragma unroll
-    for (int s = 0; s < C::KS; ++s)
+        for (int s = 0; s < KS; ++s)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int d0 = 16 * s + 8 * r + 2 * q;
-            if (qh < 0) xq[s][r] = make_float2(0.f, 0.f);
-            else if (p.q_f16) xq[s][r] = __half22float2(__ldg(reinterpret_cast<const __half2*>(reinterpret_cast<const __half*>(ds.Q) + qh * D + d0)));
-            else xq[s][r] = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(ds.Q) + qh * D + d0));
-        }
-#pragma unroll
-    for (int s = 0; s < C::KS; ++s) {
-        uint32_t a[4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float x0 = xq[s][r].x * p.scale_log2, x1 = xq[s][r].y * p.scale_log2;
-            gs[s / 2] += x0 + x1;
-            const float f = (FMT == FMT_I4 && r == 1) ? 0.0625f : 1.0f;
-            split_hi_lo(x0 * f, x1 * f, a[2 * r], a[2 * r + 1]);
-        }
-        if constexpr (C::QSMEM) {
-            *reinterpret_cast<uint4*>(qsm + (s * 32 + lane) * 4) = make_uint4(a[0], a[1], a[2], a[3]);
-        } else {
-            st.qa.r[s][0] = a[0]; st.qa.r[s][1] = a[1]; st.qa.r[s][2] = a[2]; st.qa.r[s][3] = a[3];
-        }
+            for (int r = 0; r < 2; ++r) {
+                const int d0 = 16 * s + 8 * r + 2 * q;
+                if (qh < 0) xq[cb][s][r] = make_float2(0.f, 0.f);
+                else if (p.q_f16) xq[cb][s][r] = __half22float2(__ldg(reinterpret_cast<const __half2*>(reinterpret_cast<const __half*>(ds.Q) + qh * D + d0)));
+                else xq[cb][s][r] = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(ds.Q) + qh * D + d0));
+            }
     }
 #pragma unroll
-    for (int g = 0; g < C::NG; ++g) {
-        float v = gs[g];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        st.qsum[g] = v;
-        st.bacc[g] = 0.f;
-    }
+    for (int cb = 0; cb < NCB; ++cb) {
 #pragma unroll
-    for (int j = 0; j < C::NBV; ++j) st.oacc[j][0] = st.oacc[j][1] = st.oacc[j][2] = st.oacc[j][3] = 0.f;
-    st.m_ref = -INFINITY;
-    st.l_part = 0.f;
+        for (int s = 0; s < KS; ++s)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                uint32_t hi, lo;
+                split_hi_lo(xq[cb][s][r].x * p.scale_log2, xq[cb][s][r].y * p.scale_log2, hi, lo);
+                st.qb[cb][s][r] = part ? lo : hi;
+            }
+        st.m_ref[cb] = -INFINITY;
+        st.l_part[cb] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) st.oacc[cb][mt][0] = st.oacc[cb][mt][1] = st.oacc[cb][mt][2] = st.oacc[cb][mt][3] = 0.f;
+    }
     __syncwarp();
 }
 
-// Online softmax on this lane's 4 scores (tokens 2q, 2q+1, 8+2q, 9+2q of the tile; head l/4).
-template <int FMT, int D>
-__device__ __forceinline__ void softmax_update(WState<FMT, D>& st, float (&z)[4], float (&pr)[4]) {
-    using C = DCfg<FMT, D>;
-    float mt = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-    const bool need = mt > st.m_ref + RESCALE_THRESHOLD;   // false when mt == -inf
-    if (__any_sync(0xffffffffu, need)) {
-        const float mnew = need ? mt : st.m_ref;
-        const float alpha = need ? exp2f(st.m_ref - mnew) : 1.0f;   // exp2(-inf) = 0 on the first tile
-#pragma unroll
-        for (int j = 0; j < C::NBV; ++j) {
-            st.oacc[j][0] *= alpha; st.oacc[j][1] *= alpha; st.oacc[j][2] *= alpha; st.oacc[j][3] *= alpha;
-        }
-#pragma unroll
-        for (int g = 0; g < C::NG; ++g) st.bacc[g] *= alpha;
-        st.l_part *= alpha;
-        st.m_ref = mnew;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) pr[k] = (z[k] == -INFINITY) ? 0.f : ex2_approx(z[k] - st.m_ref);
-    st.l_part += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 
-__device__ __forceinline__ void mask_scores(float (&z)[4], int lane, int valid, bool head_ok) {
-    const int q = lane & 3;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int t = (k & 1) + 2 * q + ((k >> 1) << 3);
-        if (!head_ok || t >= valid) z[k] = -INFINITY;
-    }
-}
-
-// ---------------------------------------------------------------- fp16 tile (fetch functors)
-
-// One 16-token tile of an fp16 slot in shared memory: kp -> its K part (2 token groups x D/8
-// d chunks of 128-B core matrices), vp -> its V part (D/8 d groups x 2 token chunks).
-// Word `lane` of a core matrix is that lane's m16n8k16 B-fragment register.
+// One 16-token tile of an fp16 slot in shared memory (resident layout). K part: 2 token groups
+// x D/8 d chunks of 128-B core matrices, [8 tokens][8 d] each; V part: D/8 d groups x 2 token
+// chunks, [8 d][8 tokens] each. One ldmatrix.x4 gives the A fragment of a k-step of K (tokens x
+// 16 d) or of an m-tile of V^T (16 d x tokens).
 template <int D>
-struct SmemFp16Tile {
-    const uint8_t* kp;
-    const uint8_t* vp;
+struct SmemF16Tile {
+    uint32_t kp, vp;   // shared-memory addresses of the K and V parts
     int lane;
-    __device__ __forceinline__ uint32_t kw(int nb, int c) const {
-        return *reinterpret_cast<const uint32_t*>(kp + ((nb * (D / 8) + c) * 32 + lane) * 4);
+    __device__ __forceinline__ void ka(int s, uint32_t (&a)[4]) const {
+        const int j = lane >> 3;   // core matrix j: token group j & 1, d chunk 2s + (j >> 1)
+        ldsm_x4(kp + ((j & 1) * (D / 8) + 2 * s + (j >> 1)) * 128 + (lane & 7) * 16, a);
     }
-    __device__ __forceinline__ uint32_t vw(int j, int tc) const {
-        return *reinterpret_cast<const uint32_t*>(vp + ((j * 2 + tc) * 32 + lane) * 4);
-    }
-    __device__ __forceinline__ uint4 k(int s) const {
-        return make_uint4(kw(0, 2 * s), kw(0, 2 * s + 1), kw(1, 2 * s), kw(1, 2 * s + 1));
-    }
-    __device__ __forceinline__ uint4 v(int c) const {
-        return make_uint4(vw(2 * c, 0), vw(2 * c, 1), vw(2 * c + 1, 0), vw(2 * c + 1, 1));
+    __device__ __forceinline__ void va(int mt, uint32_t (&a)[4]) const {
+        const int j = lane >> 3;   // core matrix j: d group 2mt + (j & 1), token chunk j >> 1
+        ldsm_x4(vp + ((2 * mt + (j & 1)) * 2 + (j >> 1)) * 128 + (lane & 7) * 16, a);
     }
 };
 
 // Dense suffix K_suf/V_suf [S_suf, D] of one kv head, natural layout, read straight from global.
 template <int D>
-struct GlobalSuffixTile {
+struct GlobalF16Tile {
     const __half* Kg;   // kv head base [S_suf, D]
     const __half* Vg;
     int t0, S, lane;
@@ -212,43 +143,106 @@ struct GlobalSuffixTile {
         const unsigned short b = t + 1 < S ? __ldg(reinterpret_cast<const unsigned short*>(Vg + (size_t)(t + 1) * D + d)) : 0;
         return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
     }
-    __device__ __forceinline__ uint4 k(int s) const {
-        const int q = lane & 3, l4 = lane >> 2;
-        const int d0 = 16 * s + 2 * q;
-        return make_uint4(kw(t0 + l4, d0), kw(t0 + l4, d0 + 8), kw(t0 + 8 + l4, d0), kw(t0 + 8 + l4, d0 + 8));
+    __device__ __forceinline__ void ka(int s, uint32_t (&a)[4]) const {   // rows: tokens, k: d
+        const int g = lane >> 2, d = 16 * s + 2 * (lane & 3), t = t0 + g;
+        a[0] = kw(t, d); a[1] = kw(t + 8, d); a[2] = kw(t, d + 8); a[3] = kw(t + 8, d + 8);
     }
-    __device__ __forceinline__ uint4 v(int c) const {
-        const int q = lane & 3, l4 = lane >> 2;
-        const int dA = 8 * (2 * c) + l4, dB = 8 * (2 * c + 1) + l4;
-        return make_uint4(vw(t0 + 2 * q, dA), vw(t0 + 8 + 2 * q, dA), vw(t0 + 2 * q, dB), vw(t0 + 8 + 2 * q, dB));
+    __device__ __forceinline__ void va(int mt, uint32_t (&a)[4]) const {  // rows: d, k: tokens
+        const int dd = 16 * mt + (lane >> 2), t = t0 + 2 * (lane & 3);
+        a[0] = vw(t, dd); a[1] = vw(t, dd + 8); a[2] = vw(t + 8, dd); a[3] = vw(t + 8, dd + 8);
     }
 };
 
-template <int FMT, int D, typename Tile>
-__device__ __forceinline__ void tile_fp16(WState<FMT, D>& st, const uint32_t* qsm, const Tile& tl, int lane, int valid,
-                                          bool head_ok) {
-    using C = DCfg<FMT, D>;
-    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+// One 16-token tile: S^T = K q^T (fp32 scores of 2 tokens x 1 head per lane), one online-softmax
+// step, then O^T += V^T P^T with P (hi / lo fp16 parts) moved into B fragments by movmatrix.
+template <int D, int NCB, typename Src>
+__device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, int lane, int valid,
+                                         uint32_t head_mask, int nq) {
+    constexpr int KS = D / 16;
+    const int q = lane & 3, t0 = lane >> 2;
+    float acc[NCB][4];
 #pragma unroll
-    for (int s = 0; s < C::KS; ++s) {
+    for (int cb = 0; cb < NCB; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
         uint32_t a[4];
-        get_qa<D>(st.qa, qsm, s, lane, a);
-        const uint4 kb = tl.k(s);
-        mma16816(acc0, a, kb.x, kb.y);
-        mma16816(acc1, a, kb.z, kb.w);
-    }
-    float z[4] = {acc0[0] + acc0[2], acc0[1] + acc0[3], acc1[0] + acc1[2], acc1[1] + acc1[3]};
-    mask_scores(z, lane, valid, head_ok);
-    float pr[4];
-    softmax_update<FMT, D>(st, z, pr);
-    uint32_t a[4];
-    split_hi_lo(pr[0], pr[1], a[0], a[1]);
-    split_hi_lo(pr[2], pr[3], a[2], a[3]);
+        src.ka(s, a);
 #pragma unroll
-    for (int c = 0; c < C::KS; ++c) {
-        const uint4 vb = tl.v(c);
-        mma16816(st.oacc[2 * c], a, vb.x, vb.y);
-        mma16816(st.oacc[2 * c + 1], a, vb.z, vb.w);
+        for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
+    }
+    float z[NCB][2];
+    bool need_any = false;
+    float mt[NCB];
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        const int h = cb * 4 + q;
+        const bool hok = h < nq && ((head_mask >> h) & 1u);
+        z[cb][0] = (hok && t0 < valid) ? acc[cb][0] + acc[cb][1] : -INFINITY;       // hi + lo columns
+        z[cb][1] = (hok && t0 + 8 < valid) ? acc[cb][2] + acc[cb][3] : -INFINITY;
+        float m = fmaxf(z[cb][0], z[cb][1]);   // lanes with the same q share a head
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        mt[cb] = m;
+        need_any |= m > st.m_ref[cb] + RESCALE_THRESHOLD;   // false when m == -inf
+    }
+    if (__any_sync(0xffffffffu, need_any)) {
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+            const bool need = mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;
+            const float mnew = need ? mt[cb] : st.m_ref[cb];
+            const float alpha = need ? exp2f(st.m_ref[cb] - mnew) : 1.0f;   // exp2(-inf) = 0 on the first tile
+            st.l_part[cb] *= alpha;
+            st.m_ref[cb] = mnew;
+#pragma unroll
+            for (int m2 = 0; m2 < KS; ++m2) {   // O^T columns of this lane are head q's
+                st.oacc[cb][m2][0] *= alpha; st.oacc[cb][m2][1] *= alpha;
+                st.oacc[cb][m2][2] *= alpha; st.oacc[cb][m2][3] *= alpha;
+            }
+        }
+    }
+    uint32_t b[NCB][2];
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        const float p0 = z[cb][0] == -INFINITY ? 0.f : ex2_approx(z[cb][0] - st.m_ref[cb]);
+        const float p1 = z[cb][1] == -INFINITY ? 0.f : ex2_approx(z[cb][1] - st.m_ref[cb]);
+        st.l_part[cb] += p0 + p1;
+        b[cb][0] = movmatrix_trans(pack_hilo(p0));   // tokens 0..7 as the k rows of B
+        b[cb][1] = movmatrix_trans(pack_hilo(p1));   // tokens 8..15
+    }
+#pragma unroll
+    for (int m2 = 0; m2 < KS; ++m2) {
+        uint32_t a[4];
+        src.va(m2, a);
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) mma16816(st.oacc[cb][m2], a, b[cb][0], b[cb][1]);
+    }
+}
+
+// Partial of the item piece: for every head h of the item, [m, l, o[0..D)].
+template <int D, int NCB>
+__device__ __forceinline__ void write_partial_f16(F16State<D, NCB>& st, float* P, int nq, int lane) {
+    constexpr int KS = D / 16;
+    const int q = lane & 3, l4 = lane >> 2;
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        const int hq = cb * 4 + q;
+        float l = st.l_part[cb];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (hq < nq) {
+            float* ph = P + hq * partial_stride(D);
+            if (lane < 4) {
+                ph[0] = st.m_ref[cb];
+                ph[1] = l;
+            }
+#pragma unroll
+            for (int m2 = 0; m2 < KS; ++m2) {   // columns 2q (hi) and 2q+1 (lo) hold the same head
+                ph[PARTIAL_O + 16 * m2 + l4] = st.oacc[cb][m2][0] + st.oacc[cb][m2][1];
+                ph[PARTIAL_O + 16 * m2 + l4 + 8] = st.oacc[cb][m2][2] + st.oacc[cb][m2][3];
+            }
+        }
     }
 }
 
@@ -280,16 +274,21 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
         float gsum[S::NG];
 #pragma unroll
         for (int g = 0; g < S::NG; ++g) gsum[g] = 0.f;
+        float2 xq[S::KS][2];   // every load first (one round trip)
+#pragma unroll
+        for (int s = 0; s < S::KS; ++s)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int d0 = 16 * s + 8 * r + 2 * q;
+                if (qh < 0) xq[s][r] = make_float2(0.f, 0.f);
+                else if (p.q_f16) xq[s][r] = __half22float2(__ldg(reinterpret_cast<const __half2*>(reinterpret_cast<const __half*>(ds.Q) + qh * D + d0)));
+                else xq[s][r] = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(ds.Q) + qh * D + d0));
+            }
 #pragma unroll
         for (int s = 0; s < S::KS; ++s) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int d0 = 16 * s + 8 * r + 2 * q;
-                float x0 = 0.f, x1 = 0.f;
-                if (qh >= 0) {
-                    x0 = ld_q(ds.Q, p.q_f16, qh * D + d0) * p.scale_log2;
-                    x1 = ld_q(ds.Q, p.q_f16, qh * D + d0 + 1) * p.scale_log2;
-                }
+                const float x0 = xq[s][r].x * p.scale_log2, x1 = xq[s][r].y * p.scale_log2;
                 gsum[s >> 1] += x0 + x1;
                 uint32_t hi, lo;
                 split_hi_lo(x0, x1, hi, lo);
@@ -634,24 +633,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     }
 }
 
-template <int D>
-__device__ void finish_piece(WState<FMT_FP16, D>& st, const DecodeParams& p, int item, int slot, int lane) {
-    using C = DCfg<FMT_FP16, D>;
-    const int q = lane & 3, h = lane >> 2;
-    const int grp = item % p.n_groups;
-    float l = st.l_part;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    float* ph = p.partials + (size_t)slot * GMAX * partial_stride(D) + h * partial_stride(D);
-    if (h < p.grp[grp].nq) {
-        if (q == 0) { ph[0] = st.m_ref; ph[1] = l; }
-#pragma unroll
-        for (int j = 0; j < C::NBV; ++j) {
-            const int dd = 8 * j + 2 * q;
-            ph[PARTIAL_O + dd] = st.oacc[j][0] + st.oacc[j][2];
-            ph[PARTIAL_O + 1 + dd] = st.oacc[j][1] + st.oacc[j][3];
-        }
-    }
+template <int D, int NCB>
+__device__ void finish_piece_f16(F16State<D, NCB>& st, const DecodeParams& p, int item, int slot, int lane) {
+    write_partial_f16<D, NCB>(st, p.partials + (size_t)slot * GMAX * partial_stride(D), p.grp[item % p.n_groups].nq, lane);
 }
 
 template <int D, int NCB>
@@ -761,11 +745,12 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
         cursor_set_item<FMT, D>(p, c);
         return;
     }
-    // the largest item i with item_base[i] <= t: a 32-way search over item_base
+    // the largest item i with item_base[i] <= t: a 32-way search over item_base; its last step
+    // loads item_base[lo .. lo + 31], which then serves as the cursor's window
     const int n_items = p.n_desc * p.n_groups;
     const int lane = threadIdx.x & 31;
     int lo = 0, hi = n_items;
-    while (hi - lo > 1) {
+    while (hi - lo > 31) {
         const int step = (hi - lo + 31) / 32;
         const int idx = lo + lane * step;
         const bool ok = idx < hi && min(max(__ldcg(p.item_base + idx), 0), p.max_units) <= c.t;
@@ -774,8 +759,10 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, Cursor& c) {
         lo += k * step;
         hi = min(hi, lo + step);
     }
-    c.win_lo = -64;   // empty window
-    cursor_enter_sparse<FMT, D>(p, c, lo);
+    c.win_lo = lo;
+    c.win = min(max(__ldcg(p.item_base + min(lo + lane, n_items)), 0), p.max_units);
+    const unsigned b = __ballot_sync(0xffffffffu, lo + lane < hi && c.win <= c.t);
+    cursor_enter_sparse<FMT, D>(p, c, lo + 31 - __clz(b | 1u));
 }
 
 template <int FMT, int D, int TPS, int TB>
@@ -840,9 +827,9 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
 // ---------------------------------------------------------------- workers
 
 template <int FMT, int D, int NCB>
-__device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars, uint32_t* qsm) {
+__device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars) {
     using C = DCfg<FMT, D>;
-    using StateT = std::conditional_t<FMT == FMT_FP16, WState<FMT_FP16, D>, I4State<D, NCB>>;
+    using StateT = std::conditional_t<FMT == FMT_FP16, F16State<D, NCB>, I4State<D, NCB>>;
     Cursor cons;
     const int total = FMT == FMT_FP16 && p.sparse ? units_total(p) : p.total_tiles;
     const int tpw = worker_units(p, total);
@@ -893,7 +880,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     while (cursor_next<FMT, D, C::TPS, C::TB>(p, cons, c)) {
         if (c.item != cur_item) {
             cur_item = c.item;
-            if constexpr (FMT == FMT_FP16) start_item<FMT_FP16, D>(st, qsm, p, p.desc[c.d], p.grp[c.grp], lane);
+            if constexpr (FMT == FMT_FP16) start_item_f16<D, NCB>(st, p, p.desc[c.d], p.grp[c.grp], lane);
             else start_item_i4<D, NCB>(st, p, p.desc[c.d], p.grp[c.grp], lane);
         }
         if (!mbar_wait_bounded(bar_s + 8 * stage, (phase >> stage) & 1u)) {
@@ -906,13 +893,13 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         }
         --inflight;
         const uint32_t head_mask = c.mask;   // bit h: local q head h attends to this chunk's tokens
-        const bool head_ok = (lane >> 2) < c.nq && ((head_mask >> (lane >> 2)) & 1u);
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {
             const int valid = c.valid - k * TILE_TOK;
             if constexpr (FMT == FMT_FP16) {
-                SmemFp16Tile<D> tl{sbuf + k * 32 * D, sbuf + C::STAGE / 2 + k * 32 * D, lane};
-                tile_fp16<FMT, D>(st, qsm, tl, lane, valid, head_ok);
+                const uint32_t sb = smem_u32(sbuf);
+                SmemF16Tile<D> tl{sb + k * 32 * D, sb + C::STAGE / 2 + k * 32 * D, lane};
+                tile_f16<D, NCB>(st, tl, lane, valid, head_mask, c.nq);
             } else {
                 if (D <= 128 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
                     tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
@@ -935,15 +922,15 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         }
         stage = stage + 1 == C::NSTAGE ? 0 : stage + 1;
         if (c.last) {
-            if constexpr (FMT == FMT_FP16) finish_piece<D>(st, p, cur_item, w + cur_item, lane);
+            if constexpr (FMT == FMT_FP16) finish_piece_f16<D, NCB>(st, p, cur_item, w + cur_item, lane);
             else finish_piece_i4<D, NCB>(st, p, cur_item, w + cur_item, lane);
             cur_item = -1;
         }
     }
 }
 
-template <int FMT, int D>
-__device__ void suffix_worker(const DecodeParams& p, int sidx, int lane, uint32_t* qsm) {
+template <int D, int NCB>
+__device__ void suffix_worker(const DecodeParams& p, int sidx, int lane) {
     const int n_items = p.n_desc * p.n_groups;
     const int item = sidx / p.n_suf, k = sidx - item * p.n_suf;
     if (item >= n_items) return;
@@ -951,12 +938,12 @@ __device__ void suffix_worker(const DecodeParams& p, int sidx, int lane, uint32_
     const DecodeDesc& ds = p.desc[d];
     const WorkGroup& wg = p.grp[grp];
     // The suffix is fp16 whatever the prefix format: fp16-style q fragments (no 1/16 factor).
-    WState<FMT_FP16, D> st;
-    start_item<FMT_FP16, D>(st, qsm, p, ds, wg, lane);
+    F16State<D, NCB> st;
+    start_item_f16<D, NCB>(st, p, ds, wg, lane);
     const int t0 = 16 * k;
-    GlobalSuffixTile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
-    tile_fp16<FMT_FP16, D>(st, qsm, tl, lane, p.S_suf - t0, (lane >> 2) < wg.nq);
-    finish_piece<D>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
+    GlobalF16Tile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
+    tile_f16<D, NCB>(st, tl, lane, p.S_suf - t0, 0xFFFFFFFFu, wg.nq);
+    finish_piece_f16<D, NCB>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
 }
 
 template <int FMT, int D, int NCB>
@@ -972,14 +959,15 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __gr
     // the stream, e.g. the sparse selector): nothing is read before that kernel has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * DECODE_WARPS + warp;
+    // worker ids go round the CTAs first, so that the prefix workers (and the suffix warps after
+    // them) spread evenly over the SMs however many of them have work
+    const int gw = warp * gridDim.x + blockIdx.x;
     uint8_t* ring = smem + warp * C::RING;
-    uint32_t* qsm = reinterpret_cast<uint32_t*>(smem + DECODE_WARPS * C::RING + warp * C::QSMEM_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * (C::RING + C::QSMEM_BYTES)) + warp * C::NSTAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * C::RING) + warp * C::NSTAGE;
     if (gw < p.n_workers) {
-        prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars, qsm);
+        prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars);
     } else if (p.n_suf > 0) {
-        suffix_worker<FMT, D>(p, gw - p.n_workers, lane, qsm);
+        suffix_worker<D, NCB>(p, gw - p.n_workers, lane);
     }
 }
 
@@ -1038,9 +1026,14 @@ static DecodeLaunchInfo info_t() {
 // ncb: 4-head column blocks of the mlx4g32 kernel (1 when every work group has <= 4 q heads).
 DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb) {
     if (fmt == FMT_FP16) {
-        if (D == 64) return info_t<FMT_FP16, 64, 1>();
-        if (D == 128) return info_t<FMT_FP16, 128, 1>();
-        return info_t<FMT_FP16, 256, 1>();
+        if (ncb == 1) {
+            if (D == 64) return info_t<FMT_FP16, 64, 1>();
+            if (D == 128) return info_t<FMT_FP16, 128, 1>();
+            return info_t<FMT_FP16, 256, 1>();
+        }
+        if (D == 64) return info_t<FMT_FP16, 64, 2>();
+        if (D == 128) return info_t<FMT_FP16, 128, 2>();
+        return info_t<FMT_FP16, 256, 2>();
     }
     if (ncb == 1) {
         if (D == 64) return info_t<FMT_I4, 64, 1>();
@@ -1060,9 +1053,15 @@ int decode_ncb(const DecodeParams& p) {
 
 cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st) {
     if (fmt == FMT_FP16) {
-        if (D == 64) return launch_t<FMT_FP16, 64, 1>(p, n_ctas, st);
-        if (D == 128) return launch_t<FMT_FP16, 128, 1>(p, n_ctas, st);
-        if (D == 256) return launch_t<FMT_FP16, 256, 1>(p, n_ctas, st);
+        if (decode_ncb(p) == 1) {
+            if (D == 64) return launch_t<FMT_FP16, 64, 1>(p, n_ctas, st);
+            if (D == 128) return launch_t<FMT_FP16, 128, 1>(p, n_ctas, st);
+            if (D == 256) return launch_t<FMT_FP16, 256, 1>(p, n_ctas, st);
+        } else {
+            if (D == 64) return launch_t<FMT_FP16, 64, 2>(p, n_ctas, st);
+            if (D == 128) return launch_t<FMT_FP16, 128, 2>(p, n_ctas, st);
+            if (D == 256) return launch_t<FMT_FP16, 256, 2>(p, n_ctas, st);
+        }
         return cudaErrorInvalidValue;
     }
     if (decode_ncb(p) == 1) {
