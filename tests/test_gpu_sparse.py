@@ -172,3 +172,33 @@ def test_sparse_batch_rejects_slots_of_different_lengths(ctx):
     assert e.value.code == binding.EUNSUPPORTED
     for r in range(2):
         ctx.drop(f"spn{r}")
+
+
+def test_sparse_batch_many_sessions_uneven_items(ctx):
+    """24 sessions x 2 kv heads = 48 work items (more than one 32-item window): the device-side
+    split of the selected tiles over the workers (a 32-way search over the items' unit offsets,
+    then a window of them per worker), with a ragged last block and a suffix, against the oracle
+    per session."""
+    H_q, H_kv, N, D, B, Kt, S = 8, 2, 1500, 64, 64, 4, 8
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs = [], []
+    for r in range(24):
+        seed = 900 + r
+        K, V = synth.gen_kv(seed, H_kv, N, D)
+        Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        sid = f"spm{r}"
+        ctx.store(sid, 0, dev(K), dev(V))
+        descs.append(dict(sid=sid, layer=0, Q=dev(Q), O=torch.empty((H_q, D), device="cuda"),
+                          LSE=torch.empty((H_q,), device="cuda"), K_suf=dev(Ks), V_suf=dev(Vs),
+                          idx=torch.empty((H_q, Kt), dtype=torch.int32, device="cuda")))
+        refs.append(orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs))
+    for _ in range(2):   # twice: the launch-to-launch counters must come back to zero
+        ctx.query_sparse_batch(descs, H_q, H_kv, D, B, Kt, S_suf=S)
+        ctx.sync()
+        for r, (d, (O_ref, L_ref, idx_ref, scores)) in enumerate(zip(descs, refs)):
+            _check_idx(host(d["idx"]), scores, Kt)
+            near = orc.topk_margin(scores, Kt) < TIE_EPS
+            assert_close_o_lse(host(d["O"])[~near], host(d["LSE"])[~near], O_ref[~near], L_ref[~near], f"session {r}")
+    for r in range(24):
+        ctx.drop(f"spm{r}")
