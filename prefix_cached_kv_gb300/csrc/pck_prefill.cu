@@ -336,17 +336,38 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
 
     if (warp == PF_LOAD_WARP) {
         // ------------------------------------------------------------ producer
+        // One lane feeds both rings without blocking on either: K(j) needs S(j-2) done and V(j)
+        // needs P(j-2).V done, and whichever stage frees first is refilled first (V never runs
+        // ahead of K). Idle polls back off and are bounded like every other wait.
         if (lane == 0) {
-            for (int j = 0; j < nbl && !failed; ++j) {
-                const KeyBlock kb = key_block(P, g, kb0 + j, nbp, D);
-                const uint32_t bytes = kb.ntile * 32 * D;
-                const int st = j % PF_ST;
-                if (j >= PF_ST && !mbar_wait_bounded(bar + B_KE + 8 * st, (j / PF_ST - 1) & 1)) { failed = true; break; }
-                mbar_arrive_expect_tx(bar + B_KF + 8 * st, bytes);
-                bulk_g2s(s_base + C::OFF_K + st * C::KV_BYTES, kb.k, bytes, bar + B_KF + 8 * st);
-                if (j >= PF_ST && !mbar_wait_bounded(bar + B_VE + 8 * st, (j / PF_ST - 1) & 1)) { failed = true; break; }
-                mbar_arrive_expect_tx(bar + B_VF + 8 * st, bytes);
-                bulk_g2s(s_base + C::OFF_V + st * C::KV_BYTES, kb.v, bytes, bar + B_VF + 8 * st);
+            int jk = 0, jv = 0;
+            uint32_t idle = 0;
+            while (jv < nbl) {
+                bool moved = false;
+                if (jk < nbl && (jk < PF_ST || mbar_try_wait(bar + B_KE + 8 * (jk % PF_ST), (jk / PF_ST - 1) & 1))) {
+                    const KeyBlock kb = key_block(P, g, kb0 + jk, nbp, D);
+                    const uint32_t bytes = kb.ntile * 32 * D;
+                    const int st = jk % PF_ST;
+                    mbar_arrive_expect_tx(bar + B_KF + 8 * st, bytes);
+                    bulk_g2s(s_base + C::OFF_K + st * C::KV_BYTES, kb.k, bytes, bar + B_KF + 8 * st);
+                    ++jk;
+                    moved = true;
+                }
+                if (jv < jk && (jv < PF_ST || mbar_try_wait(bar + B_VE + 8 * (jv % PF_ST), (jv / PF_ST - 1) & 1))) {
+                    const KeyBlock kb = key_block(P, g, kb0 + jv, nbp, D);
+                    const uint32_t bytes = kb.ntile * 32 * D;
+                    const int st = jv % PF_ST;
+                    mbar_arrive_expect_tx(bar + B_VF + 8 * st, bytes);
+                    bulk_g2s(s_base + C::OFF_V + st * C::KV_BYTES, kb.v, bytes, bar + B_VF + 8 * st);
+                    ++jv;
+                    moved = true;
+                }
+                if (moved) {
+                    idle = 0;
+                } else {
+                    if (++idle > (1u << 22)) { failed = true; break; }
+                    if (idle > 64) __nanosleep(64);
+                }
             }
             if (failed) set_err(P.a.err, 2);
         }
