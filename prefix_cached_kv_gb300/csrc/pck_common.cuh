@@ -206,6 +206,17 @@ __device__ __forceinline__ uint32_t pack_hilo(float x) {
     return static_cast<uint32_t>(__half_as_ushort(h)) | (static_cast<uint32_t>(__half_as_ushort(l)) << 16);
 }
 
+// pack_hilo of two values at once (bit-identical): a = half2(fp16(x0), fp16(x0 - fp16(x0))),
+// b = the same for x1; the hi parts and the lo parts each take one paired conversion.
+__device__ __forceinline__ void pack_hilo2(float x0, float x1, uint32_t& a, uint32_t& b) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    const uint32_t hu = h2_as_u32(h), lu = h2_as_u32(l);
+    a = __byte_perm(hu, lu, 0x5410);   // (hi0, lo0)
+    b = __byte_perm(hu, lu, 0x7632);   // (hi1, lo1)
+}
+
 // 2^x with the hardware approximation (MUFU.EX2: ~2 ulp, flushes subnormal results to 0);
 // used on base-2 scores that are <= 0 after the max subtraction, where its error is far below
 // the 2e-3 / 1e-3 output tolerances.

@@ -207,8 +207,10 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
         const float p0 = z[cb][0] == -INFINITY ? 0.f : ex2_approx(z[cb][0] - st.m_ref[cb]);
         const float p1 = z[cb][1] == -INFINITY ? 0.f : ex2_approx(z[cb][1] - st.m_ref[cb]);
         st.l_part[cb] += p0 + p1;
-        b[cb][0] = movmatrix_trans(pack_hilo(p0));   // tokens 0..7 as the k rows of B
-        b[cb][1] = movmatrix_trans(pack_hilo(p1));   // tokens 8..15
+        uint32_t h0, h1;
+        pack_hilo2(p0, p1, h0, h1);
+        b[cb][0] = movmatrix_trans(h0);   // tokens 0..7 as the k rows of B
+        b[cb][1] = movmatrix_trans(h1);   // tokens 8..15
     }
 #pragma unroll
     for (int m2 = 0; m2 < KS; ++m2) {
@@ -439,8 +441,10 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
 #pragma unroll
             for (int cb = 0; cb < NCB; ++cb) {
                 st.bacc[cb][g] = fmaf(pr[x][cb][0], sv0.y, fmaf(pr[x][cb][1], sv1.y, st.bacc[cb][g]));
-                b[cb][0] = movmatrix_trans(pack_hilo(pr[x][cb][0] * sv0.x));   // tokens 0..7
-                b[cb][1] = movmatrix_trans(pack_hilo(pr[x][cb][1] * sv1.x));   // tokens 8..15
+                uint32_t h0, h1;
+                pack_hilo2(pr[x][cb][0] * sv0.x, pr[x][cb][1] * sv1.x, h0, h1);
+                b[cb][0] = movmatrix_trans(h0);   // tokens 0..7
+                b[cb][1] = movmatrix_trans(h1);   // tokens 8..15
             }
 #pragma unroll
             for (int ww = 0; ww < 2; ++ww) {
