@@ -264,7 +264,8 @@ class Context:
         return call
 
     def query_sparse_batch(self, descs, H_q, H_kv, D, B, K_top, S_suf=0, q_dtype=DT_F32, head_map=None):
-        """n sparse queries in one selector launch and one gather decode (see sparse_batch_caller)."""
+        """n sparse queries in one scoring, one selection and one gather-decode launch (plus its
+        merge); see sparse_batch_caller."""
         self.sparse_batch_caller(descs, H_q, H_kv, D, B, K_top, S_suf, q_dtype, head_map)()
 
     def query_batch(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None, stream=None):

@@ -589,8 +589,9 @@ struct SparseIn {
     int32_t* idx_out;
 };
 
-// n sparse queries of the same shapes (slots with the same N): block scoring and top-K for all of
-// them in one selector launch, then one split-K gather decode (+ merge) over all of them.
+// n sparse queries of the same shapes (slots with the same N): block scoring of all of them in one
+// launch, their top-K selections in one launch, then one split-K gather decode (+ merge) over the
+// selected tiles of all of them.
 static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int B, int K_top, int H_kv, int S_suf,
                       int q_dtype, const int32_t* head_map, int fa_window, void* stream) {
     if (!c) return PCK_EINVAL;

@@ -9,21 +9,22 @@
 // Work decomposition. A work item is (query descriptor, kv head, <= 8 q heads of that kv head).
 // Every item is a sequence of 16-token resident tiles (the prefix, or the tiles of the selected
 // blocks). All items' tiles are concatenated and cut into equal contiguous ranges, one per warp
-// ("worker"), so the whole GPU streams the same number of bytes per warp whatever the shapes.
-// A worker keeps a private ring of shared-memory stages filled by 1-D TMA bulk copies
-// (cp.async.bulk, mbarrier completion) and computes each tile with the warp MMA m16n8k16
-// (fp16 operands, fp32 accumulation); q and P are split into fp16 hi + lo halves so that the
-// products keep fp32 accuracy.
-//   fp16 slots: S = q K^T with the q heads as MMA rows (hi in rows 0-7, lo in rows 8-15).
-//   mlx4g32 slots: S^T = K q^T with the 16 tokens of the tile as MMA rows and the q heads as
-//     columns (head h, hi / lo in columns 2h, 2h+1), so that every row and column carries data
-//     and every lane owns (2 tokens, 1 head) in the softmax. The codes enter the MMA as exact
-//     fp16 subnormals (c * 2^-24, one AND per register); the per-group affine terms are applied
-//     to the fp32 scores, z = 2^24 s * S + b * sum_d q_d, and for V through P' = p * s and
-//     sum_t p_t b_t. P' moves from the score layout into the A operand of O += P' V with one
-//     movmatrix.trans per 8 tokens.
-// Each worker writes an (m, l, o) partial per item piece; the last piece to finish (atomic
-// ticket, no waiting) merges all pieces of the item plus the dense suffix pieces:
+// ("worker"), so the whole GPU streams the same number of bytes per warp whatever the shapes;
+// for sparse items the selector writes the items' tile counts and the workers split them on the
+// device. A worker keeps a private ring of shared-memory stages filled by 1-D TMA bulk copies
+// (cp.async.bulk, mbarrier completion) and computes each tile with the warp MMA m16n8k16 (fp16
+// operands, fp32 accumulation); q and P are split into fp16 hi + lo halves so that the products
+// keep fp32 accuracy. Both tiers compute S^T = K q^T with the 16 tokens of the tile as MMA rows
+// and the q heads as columns (head h, hi / lo in columns 2h, 2h+1), so that every lane owns
+// (2 tokens, 1 head) in the softmax, and O^T += V^T P^T with d as the MMA rows; P moves from the
+// score layout into the B operand with one movmatrix.trans per 8 tokens.
+//   fp16 slots: the K and V^T A-fragments come straight from the resident core-matrix layout
+//     with one ldmatrix.x4 per 16 d (K) or per 16 rows of d (V^T); q stays in registers.
+//   mlx4g32 slots: the codes enter the MMA as exact fp16 subnormals (c * 2^-24, one AND per
+//     register); the per-group affine terms are applied to the fp32 scores,
+//     z = 2^24 s * S + b * sum_d q_d, and for V through P' = p * s and sum_t p_t b_t.
+// Each worker writes an (m, l, o) partial per item piece; a second kernel (programmatic
+// dependent launch) merges each (item, q head) from its pieces and the dense suffix pieces:
 //   m = max m_k, l = sum l_k 2^(m_k - m), O = sum o_k 2^(m_k - m) / l, LSE = (m + log2 l) ln 2.
 // Softmax runs in base 2 on log2(e)-prescaled scores; the running max is only moved when a
 // tile's max exceeds it by more than 8 (so stored weights stay <= 256), which keeps the

@@ -5,6 +5,12 @@
 // K_top best are kept ("GQA-aware": a kv head's gather reads the union of its q heads' blocks
 // once, each q head attending only to its own). Ties go to the lower block index; the
 // selected indices are reported sorted ascending.
+//
+// Two kernels: score_kernel streams the block means through shared memory and writes every
+// (q head, block) score; select_kernel (programmatic dependent launch) takes each q head's top-K,
+// forms each work group's union of blocks with per-head masks, counts the resident tiles of the
+// union (the gather decode's units) and, in the CTA that completes the last item, writes the
+// items' unit offsets, from which the decode's workers split the selected tiles evenly.
 #include <math.h>
 
 #include <algorithm>
