@@ -172,14 +172,26 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
         for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
     }
     float z[NCB][2];
+#pragma unroll
+    for (int cb = 0; cb < NCB; ++cb) {
+        z[cb][0] = acc[cb][0] + acc[cb][1];   // hi + lo columns
+        z[cb][1] = acc[cb][2] + acc[cb][3];
+    }
+    // masks (warp-uniform test): tokens past the end, heads the tile does not serve
+    const uint32_t heads = nq >= 32 ? 0xFFFFFFFFu : ((1u << nq) - 1u);
+    if (valid < 16 || (head_mask & heads) != heads || nq < 4 * NCB) {
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+            const int h = cb * 4 + q;
+            const bool hok = h < nq && ((head_mask >> h) & 1u);
+            if (!(hok && t0 < valid)) z[cb][0] = -INFINITY;
+            if (!(hok && t0 + 8 < valid)) z[cb][1] = -INFINITY;
+        }
+    }
     bool need_any = false;
     float mt[NCB];
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
-        const int h = cb * 4 + q;
-        const bool hok = h < nq && ((head_mask >> h) & 1u);
-        z[cb][0] = (hok && t0 < valid) ? acc[cb][0] + acc[cb][1] : -INFINITY;       // hi + lo columns
-        z[cb][1] = (hok && t0 + 8 < valid) ? acc[cb][2] + acc[cb][3] : -INFINITY;
         float m = fmaxf(z[cb][0], z[cb][1]);   // lanes with the same q share a head
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
@@ -205,8 +217,10 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
     uint32_t b[NCB][2];
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
-        const float p0 = z[cb][0] == -INFINITY ? 0.f : ex2_approx(z[cb][0] - st.m_ref[cb]);
-        const float p1 = z[cb][1] == -INFINITY ? 0.f : ex2_approx(z[cb][1] - st.m_ref[cb]);
+        // ex2(-inf) = +0; a head whose m_ref is still -inf has only -inf scores
+        const float ms = st.m_ref[cb] == -INFINITY ? 0.f : st.m_ref[cb];
+        const float p0 = ex2_approx(z[cb][0] - ms);
+        const float p1 = ex2_approx(z[cb][1] - ms);
         st.l_part[cb] += p0 + p1;
         uint32_t h0, h1;
         pack_hilo2(p0, p1, h0, h1);
@@ -378,15 +392,25 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
                 zb1[cb] = fmaf(sb1.y, st.qs[cb][g], zb1[cb]);
             }
         }
-        const int va = valid0 - 16 * x;
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
-            const int h = cb * 4 + q;
-            const bool hok = h < nq && ((head_mask >> h) & 1u);
-            float z0 = fmaf(zs0[cb], 16777216.0f, zb0[cb]);     // 2^24: codes entered as c * 2^-24
-            float z1 = fmaf(zs1[cb], 1048576.0f, zb1[cb]);      // 2^20: rows t0+8 hold 16 c * 2^-24
-            z[x][cb][0] = (hok && t0 < va) ? z0 : -INFINITY;
-            z[x][cb][1] = (hok && t0 + 8 < va) ? z1 : -INFINITY;
+            z[x][cb][0] = fmaf(zs0[cb], 16777216.0f, zb0[cb]);     // 2^24: codes entered as c * 2^-24
+            z[x][cb][1] = fmaf(zs1[cb], 1048576.0f, zb1[cb]);      // 2^20: rows t0+8 hold 16 c * 2^-24
+        }
+    }
+    // masks (warp-uniform test): tokens past the end of the prefix, heads the chunk does not serve
+    const uint32_t heads = nq >= 32 ? 0xFFFFFFFFu : ((1u << nq) - 1u);
+    if (valid0 < 16 * NT || (head_mask & heads) != heads || nq < 4 * NCB) {
+#pragma unroll
+        for (int x = 0; x < NT; ++x) {
+            const int va = valid0 - 16 * x;
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+                const int h = cb * 4 + q;
+                const bool hok = h < nq && ((head_mask >> h) & 1u);
+                if (!(hok && t0 < va)) z[x][cb][0] = -INFINITY;
+                if (!(hok && t0 + 8 < va)) z[x][cb][1] = -INFINITY;
+            }
         }
     }
     // ---- online softmax step over the NT*16 tokens (lanes with the same q share a head)
@@ -425,9 +449,11 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
     for (int x = 0; x < NT; ++x)
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
+            // ex2(-inf) = +0; a head whose m_ref is still -inf has only -inf scores (any finite
+            // one would have moved it), so 0 stands in for it there
+            const float ms = st.m_ref[cb] == -INFINITY ? 0.f : st.m_ref[cb];
 #pragma unroll
-            for (int y = 0; y < 2; ++y)
-                pr[x][cb][y] = z[x][cb][y] == -INFINITY ? 0.f : ex2_approx(z[x][cb][y] - st.m_ref[cb]);
+            for (int y = 0; y < 2; ++y) pr[x][cb][y] = ex2_approx(z[x][cb][y] - ms);
             st.l_part[cb] += pr[x][cb][0] + pr[x][cb][1];
         }
     // ---- O^T += V^T P'^T per tile and group of 32 d (P' = p * scale of the token's group):
