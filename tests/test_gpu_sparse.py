@@ -33,6 +33,9 @@ def _check_idx(idx, scores, K_top):
     (4, 4, 777, 256, 32, 5, 16),
     (6, 2, 4096, 128, 64, 8, 32),
     (8, 1, 100, 64, 16, 2, 0),
+    (8, 2, 4096, 64, 64, 40, 0),      # K_top > 32: arg-max rounds; union lists longer than 32
+    (4, 1, 8192, 128, 64, 64, 16),    # the largest K_top
+    (2, 1, 1, 64, 16, 1, 0),          # a one-token prefix: one block
 ])
 def test_sparse_matches_oracle(ctx, H_q, H_kv, N, D, B, K_top, S):
     seed = N + D + K_top
