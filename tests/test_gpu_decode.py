@@ -41,6 +41,8 @@ CASES = [
     (6, 3, 1, 64, 0, 0),            # N = 1
     (6, 3, 1, 64, 0, 1),
     (16, 2, 333, 128, 33, 1),       # GQA 8
+    (16, 2, 333, 128, 33, 0),       # GQA 8, fp16 (two 4-head column blocks)
+    (16, 2, 600, 256, 20, 0),       # GQA 8, fp16, D = 256
     (24, 2, 100, 64, 1, 0),         # GQA 12 -> two work groups per kv head
     (1, 1, 4097, 64, 0, 1),
 ]
