@@ -26,7 +26,7 @@ What each function follows (page title, section):
   forms" (the server keeps block means of K per slot, scores blocks against Q
   and keeps K_top blocks of size B, GQA-aware).
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 
 * Quantiser: mn/mx are the group's min/max as fp32; s32 = fp32(mx-mn)/15 in fp32;
   s16 = fp16(s32); b16 = fp16(mn); code = clamp(rint_half_even(fp32(fp32(x - b16) /
