@@ -39,13 +39,12 @@ __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int
 
 // ---------------------------------------------------------------- block scoring
 
-// The selector is one launch. A CTA scores a slab of SCORE_BPC consecutive blocks of one
-// (session, kv head): one bulk copy brings the slab's block means (64 KB at D = 256) into shared
-// memory, then each warp dots 8 blocks with the kv head's q heads, 4 at a time, and sums the
-// 8 x 4 per-lane products over the lanes by a reduce-scatter (31 shuffles for 32 sums; lane l
-// ends with block l / 4, head l % 4): score[h, b] = tau * q_h . K_mean[head_map[h], b].
-// The last CTA of a (session, kv head) to finish its slab then selects for that kv head's work
-// groups (below), and the one that completes the last item writes the items' unit offsets.
+// A scoring CTA takes a slab of SCORE_BPC consecutive blocks of one (session, kv head): one bulk
+// copy brings the slab's block means (32 KB at D = 256) into shared memory, then each warp dots 8
+// blocks with the kv head's q heads, 4 at a time, and sums the 8 x 4 per-lane products over the
+// lanes by a reduce-scatter (31 shuffles for 32 sums; lane l ends with block l / 4, head l % 4):
+// score[h, b] = tau * q_h . K_mean[head_map[h], b]. A kv head that no q head maps to scores
+// nothing. The selection runs in its own grid (select_kernel, below).
 constexpr int SEL_WARPS = 4;                           // warps per CTA (q heads taken in turn when selecting)
 constexpr int SCORE_BPW = 8;                           // blocks per warp
 constexpr int SCORE_BPC = SEL_WARPS * SCORE_BPW;       // blocks per CTA

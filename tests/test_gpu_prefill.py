@@ -27,6 +27,10 @@ CASES = [
     (6, 2, 1000, 96, 200, 128, False),
     (2, 2, 33, 200, 17, 64, True),      # M > S_suf: early rows see no suffix
     (8, 8, 17, 16, 16, 128, True),
+    (12, 1, 200, 50, 30, 64, True),     # GQA 12: two work groups on one kv head, 600 + 0 rows
+    (2, 1, 1, 2, 3, 128, True),         # N = 1, M = 2: one partial key block, two suffix rows
+    (1, 1, 4133, 16, 8, 64, True),      # one row tile: 32 key-range splits over 65 blocks (ragged)
+    (4, 1, 500, 129, 0, 128, True),     # 516 rows: four full row tiles and one of 4 rows
 ]
 
 
@@ -64,3 +68,21 @@ def test_prefill_batched_q_workload_layer(ctx):
     ctx.sync()
     assert_close_o_lse(host(O), host(L), O_ref, L_ref, "batched-Q layer")
     ctx.drop("pfcfg")
+
+
+@pytest.mark.parametrize("H_q,H_kv,hm", [
+    (6, 3, [2, 0, 1, 1, 0, 2]),         # q heads of a kv head not adjacent
+    (4, 2, [0, 0, 0, 0]),               # kv head 1 has no q heads
+])
+def test_prefill_custom_head_map(ctx, H_q, H_kv, hm):
+    N, M, S, D = 300, 70, 40, 64
+    hm = np.array(hm, dtype=np.int32)
+    K, V = synth.gen_kv(21, H_kv, N, D)
+    Q = synth.gen_q(21, H_q, M, D, dtype=np.float16)
+    Ks, Vs = synth.gen_suffix(21, H_kv, S, D)
+    ctx.store("pfhm", 0, dev(K), dev(V))
+    O, L = ctx.query_fused("pfhm", 0, dev(Q), dev(Ks), dev(Vs), head_map=hm, causal=True)
+    O_ref, L_ref = orc.prefix_query(Q, K, V, hm, Ks, Vs, causal=True)
+    ctx.sync()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"batched-Q head_map {hm.tolist()}")
+    ctx.drop("pfhm")

@@ -36,6 +36,7 @@ def _check_idx(idx, scores, K_top):
     (8, 2, 4096, 64, 64, 40, 0),      # K_top > 32: arg-max rounds; union lists longer than 32
     (4, 1, 8192, 128, 64, 64, 16),    # the largest K_top
     (2, 1, 1, 64, 16, 1, 0),          # a one-token prefix: one block
+    (12, 1, 2000, 64, 64, 4, 5),      # GQA 12: two work groups (two unions) on one kv head
 ])
 def test_sparse_matches_oracle(ctx, H_q, H_kv, N, D, B, K_top, S):
     seed = N + D + K_top
@@ -205,3 +206,23 @@ def test_sparse_batch_many_sessions_uneven_items(ctx):
             assert_close_o_lse(host(d["O"])[~near], host(d["LSE"])[~near], O_ref[~near], L_ref[~near], f"session {r}")
     for r in range(24):
         ctx.drop(f"spm{r}")
+
+
+@pytest.mark.parametrize("H_q,H_kv,hm", [
+    (6, 3, [2, 0, 1, 1, 0, 2]),         # q heads of a kv head not adjacent
+    (4, 2, [1, 1, 1, 1]),               # kv head 0 has no q heads: nothing scored or selected there
+])
+def test_sparse_custom_head_map(ctx, H_q, H_kv, hm):
+    N, D, B, K_top, S = 1500, 128, 64, 4, 9
+    hm = np.array(hm, dtype=np.int32)
+    K, V = synth.gen_kv(23, H_kv, N, D)
+    Q = synth.gen_q(23, H_q, 1, D)[:, 0]
+    Ks, Vs = synth.gen_suffix(23, H_kv, S, D)
+    ctx.store("sphm", 0, dev(K), dev(V))
+    O, L, idx = ctx.query_sparse_auto("sphm", 0, dev(Q), B, K_top, H_kv, head_map=hm, K_suf=dev(Ks), V_suf=dev(Vs))
+    O_ref, L_ref, idx_ref, scores = orc.sparse_query(Q, K, V, hm, B, K_top, Ks, Vs)
+    idx = host(idx).reshape(-1)[: H_q * K_top].reshape(H_q, K_top)
+    _check_idx(idx, scores, K_top)
+    near = orc.topk_margin(scores, K_top) < TIE_EPS
+    assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], f"sparse head_map {hm.tolist()}")
+    ctx.drop("sphm")
