@@ -188,20 +188,23 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
             if (!(hok && t0 + 8 < valid)) z[cb][1] = -INFINITY;
         }
     }
+    // Rescale test on each lane's own maximum: the head's maximum over its 8 lanes passes the
+    // threshold exactly when one of the lanes' maxima does, so the cross-lane maximum is only
+    // formed when some head rescales.
     bool need_any = false;
     float mt[NCB];
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
-        float m = fmaxf(z[cb][0], z[cb][1]);   // lanes with the same q share a head
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        mt[cb] = m;
-        need_any |= m > st.m_ref[cb] + RESCALE_THRESHOLD;   // false when m == -inf
+        mt[cb] = fmaxf(z[cb][0], z[cb][1]);
+        need_any |= mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;   // false when the maximum is -inf
     }
     if (__any_sync(0xffffffffu, need_any)) {
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
+            float m = mt[cb];                   // lanes with the same q share a head
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            mt[cb] = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
             const bool need = mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;
             const float mnew = need ? mt[cb] : st.m_ref[cb];
             const float alpha = need ? exp2f(st.m_ref[cb] - mnew) : 1.0f;   // exp2(-inf) = 0 on the first tile
@@ -414,6 +417,8 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
         }
     }
     // ---- online softmax step over the NT*16 tokens (lanes with the same q share a head)
+    // (the rescale test runs on each lane's own maximum; the cross-lane maximum only when some
+    //  head rescales, as in tile_f16)
     bool need_any = false;
     float mt[NCB];
 #pragma unroll
@@ -421,15 +426,16 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
         float m = fmaxf(z[0][cb][0], z[0][cb][1]);
 #pragma unroll
         for (int x = 1; x < NT; ++x) m = fmaxf(m, fmaxf(z[x][cb][0], z[x][cb][1]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         mt[cb] = m;
         need_any |= m > st.m_ref[cb] + RESCALE_THRESHOLD;
     }
     if (__any_sync(0xffffffffu, need_any)) {
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
+            float m = mt[cb];
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            mt[cb] = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
             const bool need = mt[cb] > st.m_ref[cb] + RESCALE_THRESHOLD;
             const float mnew = need ? mt[cb] : st.m_ref[cb];
             const float alpha = need ? exp2f(st.m_ref[cb] - mnew) : 1.0f;   // head q's factor
