@@ -564,12 +564,10 @@ __device__ __forceinline__ void item_range(const DecodeParams& p, int item, int&
 // online rescale; within a batch the weights 2^(m_k - M) are broadcast by shuffles. Partials are
 // read through L2 (__ldcg).
 template <int D>
-__device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane) {
+__device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane, int w0, int npref) {
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
     const DecodeDesc& ds = p.desc[d];
     const WorkGroup& wg = p.grp[grp];
-    int w0, npref;
-    item_range(p, item, w0, npref);
     const int n_items = p.n_desc * p.n_groups;
     const int npieces = npref + p.n_suf;
     constexpr int PSTR = GMAX * partial_stride(D);
@@ -656,18 +654,23 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
     if (lane == 0 && ds.LSE) ds.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
 }
 
-// Second kernel of a decode: one warp per (item, q head). Launched with programmatic dependent
-// launch; it waits for the decode grid (partials complete and visible) before reading.
+// Second kernel of a decode: one warp per (item, q head) slot, GMAX slots per item (the grid
+// covers them all). Launched with programmatic dependent launch; it waits for the decode grid
+// (partials complete and visible) before reading them. A dense launch's piece range depends on
+// launch parameters only and is found before that wait; a sparse one's comes from the unit
+// offsets the selection grid wrote, so after it.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ DecodeParams p) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    const int n_pairs = p.n_desc * p.n_groups * GMAX;
-    for (int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < n_pairs; wi += (gridDim.x * blockDim.x) >> 5) {
-        const int item = wi / GMAX, h = wi - item * GMAX;
-        if (h >= p.grp[item % p.n_groups].nq) continue;
-        merge_item_head<D>(p, item, h, lane);
-    }
+    const int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int item = wi / GMAX, h = wi - item * GMAX;
+    const bool live = wi < p.n_desc * p.n_groups * GMAX && h < p.grp[item % p.n_groups].nq;   // warp-uniform
+    int w0 = 0, npref = 0;
+    if (live && !p.sparse) item_range(p, item, w0, npref);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!live) return;
+    if (p.sparse) item_range(p, item, w0, npref);
+    merge_item_head<D>(p, item, h, lane, w0, npref);
 }
 
 template <int D, int NCB>
