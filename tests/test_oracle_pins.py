@@ -290,6 +290,34 @@ def test_block_means_ramp_closed_form():
         assert np.allclose(km[0, b], (lo + hi) / 2) and np.allclose(km[1, b], -(lo + hi))
 
 
+def test_block_scores_closed_form():
+    """score[h, b] = tau * q_h . K_mean[head_map[h], b]: unit queries against known block means,
+    through a head map that is neither the identity nor the grouped default."""
+    D = 16
+    tau = 1.0 / np.sqrt(D)
+    km = np.zeros((2, 3, D))
+    km[0, :, 3] = [1.0, 2.0, 4.0]        # kv head 0: d = 3 carries 1, 2, 4
+    km[1, :, 5] = [-8.0, 0.5, 16.0]      # kv head 1: d = 5 carries -8, 0.5, 16
+    Q = np.zeros((3, D))
+    Q[0, 3] = 2.0                        # head 0 -> kv head 1, but probes d = 3: all zero
+    Q[1, 5] = 3.0                        # head 1 -> kv head 1, probes d = 5
+    Q[2, 3] = -1.0                       # head 2 -> kv head 0, probes d = 3
+    sc = orc.block_scores(Q, km, np.array([1, 1, 0]))
+    assert sc.shape == (3, 3)
+    assert np.allclose(sc[0], 0.0)
+    assert np.allclose(sc[1], tau * 3.0 * np.array([-8.0, 0.5, 16.0]))
+    assert np.allclose(sc[2], -tau * np.array([1.0, 2.0, 4.0]))
+
+
+def test_topk_margin_worked_example():
+    """Gap between the K-th and (K+1)-th largest score of a row, by hand: scores 5, 1, 3, 3."""
+    s = np.array([[5.0, 1.0, 3.0, 3.0]])
+    assert orc.topk_margin(s, 1)[0] == 2.0      # 5 vs 3
+    assert orc.topk_margin(s, 2)[0] == 0.0      # 3 vs 3: a tie at the cut
+    assert orc.topk_margin(s, 3)[0] == 2.0      # 3 vs 1
+    assert np.isinf(orc.topk_margin(s, 4)[0])   # every block kept: no cut
+
+
 def test_topk_tie_example():
     lines = _golden_lines("topk_tie_example.txt")
     scores = np.array([[float(v) for v in lines[0].split(":")[1].split()]])
@@ -382,3 +410,41 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     monkeypatch.setattr(mod, "pack_codes", wrong_nibble_order)
     with pytest.raises(AssertionError):
         test_layout_worked_example()
+    monkeypatch.setattr(mod, "pack_codes", good_pc)
+
+    good_bs = mod.block_scores
+
+    def scores_no_tau(Q, K_mean, head_map):
+        return good_bs(Q, K_mean, head_map) * np.sqrt(np.shape(Q)[-1])
+
+    def scores_ignore_map(Q, K_mean, head_map):
+        return good_bs(Q, K_mean, np.arange(np.shape(Q)[0]) % K_mean.shape[0])
+
+    for bad in (scores_no_tau, scores_ignore_map):
+        monkeypatch.setattr(mod, "block_scores", bad)
+        with pytest.raises(AssertionError):
+            test_block_scores_closed_form()
+        monkeypatch.setattr(mod, "block_scores", good_bs)
+
+    good_tm = mod.topk_margin
+
+    def margin_off_by_one(scores, K_top):
+        return good_tm(scores, K_top + 1)
+
+    monkeypatch.setattr(mod, "topk_margin", margin_off_by_one)
+    with pytest.raises(AssertionError):
+        test_topk_margin_worked_example()
+    monkeypatch.setattr(mod, "topk_margin", good_tm)
+
+    good_bm = mod.block_means
+
+    def means_over_full_blocks(K, B):
+        K = np.asarray(K, dtype=np.float64)
+        nb = (K.shape[1] + B - 1) // B
+        pad = np.zeros((K.shape[0], nb * B - K.shape[1], K.shape[2]))
+        return np.concatenate([K, pad], axis=1).reshape(K.shape[0], nb, B, K.shape[2]).mean(axis=2)
+
+    monkeypatch.setattr(mod, "block_means", means_over_full_blocks)
+    with pytest.raises(AssertionError):
+        test_block_means_ramp_closed_form()
+    monkeypatch.setattr(mod, "block_means", good_bm)
