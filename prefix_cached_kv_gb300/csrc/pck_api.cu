@@ -14,7 +14,6 @@
 #include <cstring>
 #include <deque>
 #include <list>
-#include <mutex>
 #include <string>
 #include <unordered_map>
 #include <unordered_set>
@@ -107,7 +106,6 @@ void free_slot(pck_ctx* c, Slot& s, cudaStream_t st) {
     if (s.tiles) cudaFreeAsync(s.tiles, st);
     for (auto& kv : s.kmean) cudaFreeAsync(kv.second, st);
     c->bytes_resident -= static_cast<int64_t>(s.bytes);
-    for (auto& kv : s.kmean) (void)kv;
     s.tiles = nullptr;
     s.kmean.clear();
 }
