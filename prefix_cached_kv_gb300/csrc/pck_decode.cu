@@ -987,8 +987,9 @@ __device__ void suffix_worker(const DecodeParams& p, int sidx, int lane) {
 }
 
 template <int FMT, int D, int NCB>
-// An explicit minimum of one CTA per SM lets ptxas give the int4 kernels more registers (109
-// instead of 90 at D=64); measured faster than the higher occupancy the default budget allows.
+// An explicit minimum of one CTA per SM lifts ptxas's register budget for the int4 kernels (118
+// registers at D=64, four CTAs per SM); fewer warps with more registers each measured faster than
+// the higher occupancy of a tighter budget.
 __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<FMT, D>;
     extern __shared__ __align__(128) uint8_t smem[];
