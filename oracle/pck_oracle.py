@@ -163,6 +163,17 @@ def attend_rows(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, tau: f
     return O, LSE
 
 
+def suffix_allowed(M: int, N: int, S: int, causal: bool) -> np.ndarray:
+    """[M, N + S] key mask of the fused forms: every row sees the N prefix keys; with causal, row
+    i (0-based, of M) sees suffix keys j <= S - M + i (bottom-right alignment), else all S."""
+    allowed = np.ones((M, N + S), dtype=bool)
+    if S and causal:
+        for i in range(M):
+            jmax = S - M + i
+            allowed[i, N + max(jmax + 1, 0):] = False
+    return allowed
+
+
 def prefix_query(Q, K, V, head_map=None, K_suf=None, V_suf=None, causal: bool = True):
     """Attention of Q [H_q, M, D] over the prefix K/V [H_kv, N, D] (+ optional suffix [H_kv, S, D]).
 
@@ -179,11 +190,7 @@ def prefix_query(Q, K, V, head_map=None, K_suf=None, V_suf=None, causal: bool = 
     S = 0 if K_suf is None else K_suf.shape[1]
     O = np.zeros((H_q, M, D))
     LSE = np.zeros((H_q, M))
-    allowed = np.ones((M, N + S), dtype=bool)
-    if S and causal:
-        for i in range(M):
-            jmax = S - M + i
-            allowed[i, N + max(jmax + 1, 0):] = False
+    allowed = suffix_allowed(M, N, S, causal)
     for h in range(H_q):
         g = int(head_map[h])
         keys = np.asarray(K[g], dtype=np.float64)

@@ -448,3 +448,27 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_block_means_ramp_closed_form()
     monkeypatch.setattr(mod, "block_means", good_bm)
+
+    good_mask = mod.suffix_allowed
+
+    def top_left_causal(M, N, S, causal):
+        allowed = np.ones((M, N + S), dtype=bool)
+        if S and causal:
+            for i in range(M):
+                allowed[i, N + i + 1:] = False
+        return allowed
+
+    def causal_one_short(M, N, S, causal):
+        allowed = good_mask(M, N, S, causal)
+        if S and causal:
+            for i in range(M):
+                j = S - M + i
+                if 0 <= j < S:
+                    allowed[i, N + j] = False
+        return allowed
+
+    for bad in (top_left_causal, causal_one_short):
+        monkeypatch.setattr(mod, "suffix_allowed", bad)
+        with pytest.raises(AssertionError):
+            test_causal_suffix_matches_torch_mask(3, 7)
+        monkeypatch.setattr(mod, "suffix_allowed", good_mask)
