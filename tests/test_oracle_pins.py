@@ -402,6 +402,32 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         test_quantizer_lossless_on_grid()
     monkeypatch.setattr(mod, "quantize_mlx4g32", good_q)
 
+    def groups_and_params(x):
+        """x as [rows, groups, 32] float64, with the correct fp16 scales and biases."""
+        xg = np.asarray(x).astype(np.float64).reshape(np.shape(x)[0], -1, 32)
+        _, s16, b16 = good_q(x)
+        return xg, s16, b16
+
+    def fp32_scale_codes(x):
+        xg, s16, b16 = groups_and_params(x)
+        s32 = (xg.max(axis=2) - xg.min(axis=2)) / 15.0
+        c = np.clip(np.rint((xg - b16.astype(np.float64)[:, :, None]) / s32[:, :, None]), 0, 15)
+        return c.astype(np.uint8).reshape(np.shape(x)), s16, b16
+
+    def truncated_codes(x):
+        xg, s16, b16 = groups_and_params(x)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            t = (xg - b16.astype(np.float64)[:, :, None]) / s16.astype(np.float64)[:, :, None]
+        c = np.where((s16 == 0)[:, :, None], 0, np.clip(np.floor(np.nan_to_num(t)), 0, 15))
+        return c.astype(np.uint8).reshape(np.shape(x)), s16, b16
+
+    for bad, pin in ((fp32_scale_codes, test_quantizer_scale_is_fp16_roundtripped),
+                     (truncated_codes, test_quantizer_error_bound_and_monotone)):
+        monkeypatch.setattr(mod, "quantize_mlx4g32", bad)
+        with pytest.raises(AssertionError):
+            pin()
+        monkeypatch.setattr(mod, "quantize_mlx4g32", good_q)
+
     good_pc = mod.pack_codes
 
     def wrong_nibble_order(codes):
