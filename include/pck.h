@@ -190,7 +190,7 @@ int pck_query_sparse_batch(pck_ctx *ctx, int n, const pck_sparse_desc *descs, in
  * out_records: device [rows, rec] bytes, rec = kv_dim/2 + kv_dim/8. Per group of 32:
  * mn/mx as fp32, s32 = (mx - mn)/15 in fp32, scale = fp16(s32) (rounded BEFORE the codes are
  * chosen), bias = fp16(mn), code = clamp(rint((x - bias)/scale), 0, 15) in fp32, all codes 0 when
- * scale == 0; code of element j at bits 4*(j%8) of word j/8. kv_dim % 32 == 0. Inputs must be
+ * scale == 0; code j fills bits 4*(j%8) .. 4*(j%8)+3 of word j/8. kv_dim % 32 == 0. Inputs must be
  * finite and within the fp16 range. Needs no context. */
 int pck_quantize_mlx4g32(const void *X, int src_dtype, int64_t rows, int kv_dim,
                          void *out_records, void *stream);

@@ -10,11 +10,11 @@ What each function follows (page title, section):
 
 * mlx4g32 record layout and quantiser -- "Shared KV Cache Serving -- Pion as LLM
   Memory", section "Quantized tier -- mlx4g32"; the same text is on "V.* -- the
-  V-store", section "The mlx4g32 tier": int4 codes, groups of 32, affine with an
-  fp16 scale and an fp16 bias per group; per token the record is
-  ``[u32 x D/8 codes][f16 x D/32 scales][f16 x D/32 biases]`` with element j of a
-  group at bits ``4*(j%8)``; the scale is rounded to fp16 *before* the codes are
-  chosen.
+  V-store", section "The mlx4g32 tier": 4-bit codes in groups of 32 values, each
+  group affine with its own fp16 scale and fp16 bias. A token's record holds D/8
+  32-bit code words, then D/32 fp16 scales, then D/32 fp16 biases; the code of a
+  group's j-th value fills the four bits from ``4*(j mod 8)`` of its word. The scale
+  is rounded to fp16 first, and the codes are picked against that rounded scale.
 * Attention over the resident prefix -- "ATTEND.* and ATTEND.PREFIX.*", section
   "Wire forms" (QUERY, QUERY_FUSED, QUERY_SPARSE_AUTO(_FUSED)), and "Shared KV
   Cache Serving", section "Stage 2: ATTEND.PREFIX.*" (agreement is judged against
@@ -83,7 +83,7 @@ def quantize_mlx4g32(x) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
 
 
 def pack_codes(codes: np.ndarray) -> np.ndarray:
-    """uint8 codes [rows, kv_dim] -> uint32 words [rows, kv_dim/8]; element j at bits 4*(j%8) of word j//8."""
+    """uint8 codes [rows, kv_dim] -> uint32 words [rows, kv_dim/8]; code j fills bits 4*(j%8) .. 4*(j%8)+3 of word j//8."""
     rows, kv_dim = codes.shape
     words = np.zeros((rows, kv_dim // 8), dtype=np.uint32)
     for j in range(kv_dim):

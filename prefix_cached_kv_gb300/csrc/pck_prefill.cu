@@ -1,7 +1,8 @@
 // pck_prefill.cu -- batched-Q (M > 1) prefix attention on the 5th-generation tensor cores.
 //
-// "Shared KV Cache Serving -- Pion as LLM Memory", section "Wire-protocol details": the
-// batched-Q form of ATTEND.PREFIX.QUERY takes Q (H, M, D) and returns O plus one LSE per row;
+// "Shared KV Cache Serving -- Pion as LLM Memory", section "Wire-protocol details":
+// ATTEND.PREFIX.QUERY with M query rows per head, Q of shape (H, M, D), answers with O and an
+// LSE for every row;
 // "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms" / QUERY_FUSED: the prefix attention is
 // merged with a dense suffix (here causal, bottom-right aligned: row i sees suffix keys
 // j <= S_suf - M + i) in the same dispatch.

@@ -1,9 +1,9 @@
 // pck_store.cu -- store side: mlx4g32 quantiser and the re-layout of K/V into resident tiles.
 //
 // Quantiser: "Shared KV Cache Serving -- Pion as LLM Memory", section "Quantized tier --
-// mlx4g32" (int4, group 32, affine, fp16 scale and bias, the scale rounded to fp16 before the
-// codes are chosen; per token [u32 codes x D/8][f16 scales x D/32][f16 biases x D/32], element j
-// of a group at bits 4*(j%8)).
+// mlx4g32": 4-bit codes in groups of 32, affine with an fp16 scale and bias per group, codes
+// picked against the fp16-rounded scale. A token's record is D/8 code words, D/32 fp16 scales,
+// D/32 fp16 biases; a group's j-th code fills bits 4*(j mod 8) onward of its word.
 #include "pck_common.cuh"
 #include "pck_kernels.h"
 

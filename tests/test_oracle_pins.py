@@ -117,7 +117,7 @@ def test_quantizer_error_bound_and_monotone():
 def test_quantizer_scale_is_fp16_roundtripped():
     """Each code is the nearest point of the grid the reader sees, {b16 + c * s16 : c in 0..15}.
 
-    The page says the scale goes through fp16 before the codes are chosen; codes picked
+    The page has the scale rounded to fp16 ahead of code selection; codes picked
     against the fp32 scale would miss the nearest reader-grid point for some elements, so the
     test also checks that such elements exist in the sample (the pin can fail)."""
     rng = np.random.default_rng(13)
