@@ -214,7 +214,7 @@ struct PfParams {
     float* partials;                // n_split > 1: [tile][split][row][partial_stride(D)]
 };
 
-// Key block b of the task's key sequence: prefix blocks first, then suffix blocks.
+// Key block b of a work unit's key sequence (row tile x key range): prefix blocks, then suffix.
 struct KeyBlock {
     const uint8_t* k;
     const uint8_t* v;
