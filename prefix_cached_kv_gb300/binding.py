@@ -116,22 +116,73 @@ def _hm(head_map):
     return ctypes.cast(arr, ctypes.c_void_p), arr
 
 
-def _check_dev(*ts):
-    for t in ts:
-        if t is not None:
-            if not t.is_cuda:
-                raise ValueError("tensors must be on the CUDA device")
-            if not t.is_contiguous():
-                raise ValueError("tensors must be contiguous")
+def _spec(t, name, dtype=None, numel=None, at_least=None, nbytes=None):
+    """What the library will read or write through t: its dtype (one or a tuple), an exact element
+    count, a minimum element count, or a minimum size in bytes."""
+    return (t, name, dtype, numel, at_least, nbytes)
+
+
+def _check_all(*specs):
+    """Check caller tensors before their pointers reach the library, which trusts the sizes the
+    call implies: dtypes and sizes of every tensor first, then contiguity, then the device."""
+    live = [sp for sp in specs if sp[0] is not None]
+    for t, name, dtype, numel, at_least, nbytes in live:
+        if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if numel is not None and t.numel() != numel:
+            raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+        if at_least is not None and t.numel() < at_least:
+            raise ValueError(f"{name}: {t.numel()} elements, at least {at_least} needed")
+        if nbytes is not None and t.numel() * t.element_size() < nbytes:
+            raise ValueError(f"{name}: {t.numel() * t.element_size()} bytes, at least {nbytes} needed")
+    for t, name, *_ in live:
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous")
+    for t, name, *_ in live:
+        if not t.is_cuda:
+            raise ValueError(f"{name}: must be on the CUDA device")
+
+
+_FP = (torch.float16, torch.float32)
+
+
+def _check_suffix(K_suf, V_suf, D, H_kv=None):
+    if K_suf is None and V_suf is None:
+        return
+    if K_suf is None or V_suf is None or K_suf.dim() != 3 or V_suf.shape != K_suf.shape:
+        raise ValueError("K_suf and V_suf must both be given, [H_kv, S_suf, D] of one shape")
+    if K_suf.shape[2] != D or (H_kv is not None and K_suf.shape[0] != H_kv):
+        raise ValueError(f"suffix shape {tuple(K_suf.shape)} does not match H_kv={H_kv}, D={D}")
+
+
+def _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, sparse=False):
+    """Descriptor tensors of a batched call: Q [H_q, D] of q_dtype, O (fp32) and LSE (fp32) of at
+    least H_q * D and H_q elements, the suffix [H_kv, S_suf, D] fp16, idx int32 (sparse)."""
+    qt = {DT_F32: torch.float32, DT_F16: torch.float16}.get(q_dtype)
+    if qt is None:
+        raise ValueError(f"q_dtype={q_dtype}")
+    specs = []
+    for i, d in enumerate(descs):
+        specs += [_spec(d["Q"], f"descs[{i}].Q", qt, numel=H_q * D),
+                  _spec(d["O"], f"descs[{i}].O", torch.float32, at_least=H_q * D),
+                  _spec(d.get("LSE"), f"descs[{i}].LSE", torch.float32, at_least=H_q)]
+        if S_suf > 0:
+            for k in ("K_suf", "V_suf"):
+                specs.append(_spec(d.get(k), f"descs[{i}].{k}", torch.float16, numel=H_kv * S_suf * D))
+        if sparse:
+            specs.append(_spec(d.get("idx"), f"descs[{i}].idx", torch.int32, at_least=H_q))
+    _check_all(*specs)
 
 
 def quantize_mlx4g32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """mlx4g32 records (uint8 [rows, kv_dim/2 + kv_dim/8]) of x ([rows, kv_dim], fp16/fp32)."""
     lib = load_library()
-    _check_dev(x)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, kv_dim]")
     rows, kv_dim = x.shape
     if out is None:
         out = torch.empty((rows, kv_dim // 2 + kv_dim // 8), dtype=torch.uint8, device=x.device)
+    _check_all(_spec(x, "x", _FP), _spec(out, "out", nbytes=rows * (kv_dim // 2 + kv_dim // 8)))
     rc = lib.pck_quantize_mlx4g32(_ptr(x), _dt(x), rows, kv_dim, _ptr(out), _stream(stream))
     if rc != OK:
         raise PckError(rc, "pck_quantize_mlx4g32 rejected its arguments")
@@ -171,13 +222,16 @@ class Context:
 
     # ---- store / lookup / drop
     def store(self, sid: str, layer: int, K: torch.Tensor, V: torch.Tensor, fmt: int = FMT_FP16, stream=None):
-        _check_dev(K, V)
+        if K.dim() != 3 or V.shape != K.shape or V.dtype != K.dtype:
+            raise ValueError("K and V must be [H_kv, N, D] tensors of one shape and dtype")
+        _check_all(_spec(K, "K", _FP), _spec(V, "V", _FP))
         H_kv, N, D = K.shape
         return self._rc(self.lib.pck_store(self.h, sid.encode(), layer, H_kv, N, D, fmt, _ptr(K), _ptr(V), _dt(K),
                                            _stream(stream)))
 
     def store_records(self, sid: str, layer: int, H_kv: int, N: int, D: int, K_rec, V_rec, stream=None):
-        _check_dev(K_rec, V_rec)
+        rec = N * (H_kv * D // 2 + H_kv * D // 8)
+        _check_all(_spec(K_rec, "K_rec", nbytes=rec), _spec(V_rec, "V_rec", nbytes=rec))
         return self._rc(self.lib.pck_store_records(self.h, sid.encode(), layer, H_kv, N, D, _ptr(K_rec), _ptr(V_rec),
                                                    _stream(stream)))
 
@@ -195,11 +249,14 @@ class Context:
 
     # ---- queries (O and LSE are allocated when not given)
     def query(self, sid, layer, Q, head_map=None, top_k=0, fa_window=0, O=None, LSE=None, want_lse=True, stream=None):
-        _check_dev(Q)
+        if Q.dim() != 3:
+            raise ValueError("Q must be [H_q, M, D]")
         H_q, M, D = Q.shape
         O = torch.empty((H_q, M, D), dtype=torch.float32, device=Q.device) if O is None else O
         if LSE is None and want_lse:
             LSE = torch.empty((H_q, M), dtype=torch.float32, device=Q.device)
+        _check_all(_spec(Q, "Q", _FP), _spec(O, "O", torch.float32, at_least=H_q * M * D),
+                   _spec(LSE, "LSE", torch.float32, at_least=H_q * M))
         hm = _hm(head_map)
         self._rc(self.lib.pck_query(self.h, sid.encode(), layer, H_q, D, M, _dt(Q), _ptr(Q), hm[0] if hm else None,
                                     top_k, fa_window, _ptr(O), _ptr(LSE), _stream(stream)))
@@ -207,12 +264,19 @@ class Context:
 
     def query_fused(self, sid, layer, Q, K_suf, V_suf, head_map=None, causal=True, fa_window=0, O=None, LSE=None,
                     want_lse=True, stream=None):
-        _check_dev(Q, K_suf, V_suf)
+        if Q.dim() != 3:
+            raise ValueError("Q must be [H_q, M, D]")
         H_q, M, D = Q.shape
+        if K_suf is None:
+            raise ValueError("query_fused needs K_suf and V_suf")
+        _check_suffix(K_suf, V_suf, D)
         H_kv, S_suf, _ = K_suf.shape
         O = torch.empty((H_q, M, D), dtype=torch.float32, device=Q.device) if O is None else O
         if LSE is None and want_lse:
             LSE = torch.empty((H_q, M), dtype=torch.float32, device=Q.device)
+        _check_all(_spec(Q, "Q", _FP), _spec(K_suf, "K_suf", torch.float16), _spec(V_suf, "V_suf", torch.float16),
+                   _spec(O, "O", torch.float32, at_least=H_q * M * D),
+                   _spec(LSE, "LSE", torch.float32, at_least=H_q * M))
         hm = _hm(head_map)
         self._rc(self.lib.pck_query_fused(self.h, sid.encode(), layer, H_q, D, M, S_suf, H_kv, _dt(Q), _ptr(Q),
                                           _ptr(K_suf), _ptr(V_suf), hm[0] if hm else None, int(bool(causal)),
@@ -221,12 +285,15 @@ class Context:
 
     def query_sparse_auto(self, sid, layer, Q, B, K_top, H_kv, head_map=None, K_suf=None, V_suf=None, fa_window=0,
                           O=None, LSE=None, idx=None, stream=None):
-        _check_dev(Q, K_suf, V_suf)
         H_q, D = Q.shape[0], Q.shape[-1]
+        _check_suffix(K_suf, V_suf, D, H_kv)
         O = torch.empty((H_q, D), dtype=torch.float32, device=Q.device) if O is None else O
         LSE = torch.empty((H_q,), dtype=torch.float32, device=Q.device) if LSE is None else LSE
         if idx is None:   # the library writes [H_q, min(K_top, n_blocks)] contiguously
             idx = torch.empty((H_q, K_top), dtype=torch.int32, device=Q.device)
+        _check_all(_spec(Q, "Q", _FP, numel=H_q * D), _spec(K_suf, "K_suf", torch.float16),
+                   _spec(V_suf, "V_suf", torch.float16), _spec(O, "O", torch.float32, at_least=H_q * D),
+                   _spec(LSE, "LSE", torch.float32, at_least=H_q), _spec(idx, "idx", torch.int32, at_least=H_q))
         hm = _hm(head_map)
         if K_suf is None:
             rc = self.lib.pck_query_sparse_auto(self.h, sid.encode(), layer, H_q, D, B, K_top, H_kv, _dt(Q), _ptr(Q),
@@ -244,6 +311,7 @@ class Context:
         """Prebuild a pck_query_sparse_batch call over descs (dicts with sid, layer, Q, O, and
         optionally LSE, K_suf, V_suf, idx); returns a no-argument callable issuing it on the
         current stream (cheap enough to capture in a CUDA graph)."""
+        _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, sparse=True)
         n = len(descs)
         arr = (SparseDesc * n)()
         keep = []
@@ -270,6 +338,7 @@ class Context:
 
     def query_batch(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None, stream=None):
         """descs: list of dicts with sid, layer, Q, O, LSE (optional), K_suf/V_suf (optional)."""
+        _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype)
         n = len(descs)
         arr = (QueryDesc * n)()
         keep = []
@@ -287,6 +356,7 @@ class Context:
     def batch_caller(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None):
         """Prebuild the descriptor array of a pck_query_batch call; returns a no-argument callable
         that issues the call on the current stream (cheap enough to capture in a CUDA graph)."""
+        _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype)
         n = len(descs)
         arr = (QueryDesc * n)()
         keep = []
