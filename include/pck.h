@@ -217,7 +217,12 @@ int pck_attend_records_noalloc(int H_kv, int N, int D, const void *K_rec, const 
 /* Counters of ctx. */
 int pck_info(pck_ctx *ctx, pck_info_t *out);
 
-/* Synchronise `stream` and report any asynchronous CUDA error as PCK_ECUDA. */
+/* Synchronise `stream` and report any asynchronous CUDA error as PCK_ECUDA. Also PCK_ECUDA when
+ * a kernel's bounded wait gave up since the last check (a TMA stage or pipeline barrier that
+ * never completed). The kernel then skipped the rest of its work, so the affected results are
+ * invalid. pck_last_error names the code: 1 decode ring stage, 2 prefill producer, 3 prefill
+ * MMA warp, 4 prefill softmax, 5 prefill final O, 6 sparse scoring copy. The error word and
+ * the selector's counters are then reset, so the context stays usable. */
 int pck_sync(pck_ctx *ctx, void *stream);
 
 #ifdef __cplusplus
