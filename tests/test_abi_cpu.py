@@ -49,3 +49,36 @@ def test_binding_loads_and_sets_signatures(lib_path):
 def test_header_compiles_as_c():
     r = subprocess.run(["gcc", "-fsyntax-only", "-Wall", "-Werror", "-x", "c", HEADER], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_noalloc_rejects_bad_arguments_before_any_device_call(lib_path):
+    """pck_attend_records_noalloc checks its arguments before its first CUDA call. Every case
+    below breaks exactly one rule and must be refused with that rule's code. The pointer values
+    are never dereferenced: a case that slipped through would stop at the device query, which
+    has no device here (PCK_ECUDA) and fails the test. Skipped where a GPU is present, where the
+    GPU tests cover this entry point with real buffers."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("covered with real buffers by the GPU tests")
+    from prefix_cached_kv_gb300 import binding
+    lib = binding.load_library(lib_path)
+    P = ctypes.c_void_p(1 << 20)          # 16-byte aligned stand-ins, never read
+    P2 = ctypes.c_void_p((1 << 20) + 2)   # not 4-byte aligned
+    P4 = ctypes.c_void_p((1 << 20) + 4)   # 4- but not 16-byte aligned
+    good = dict(H_kv=2, N=64, D=64, K=P, V=P, H_q=4, qdt=binding.DT_F32, Q=P, S=0, Ks=None, Vs=None, O=P, L=P)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return lib.pck_attend_records_noalloc(a["H_kv"], a["N"], a["D"], a["K"], a["V"], a["H_q"], a["qdt"],
+                                              a["Q"], None, a["S"], a["Ks"], a["Vs"], a["O"], a["L"], None)
+
+    cases = [
+        (dict(K=None), binding.EINVAL), (dict(Q=None), binding.EINVAL), (dict(O=None), binding.EINVAL),
+        (dict(O=P4), binding.EINVAL), (dict(Q=P4), binding.EINVAL),
+        (dict(H_kv=0), binding.EINVAL), (dict(H_q=65), binding.EINVAL), (dict(N=0), binding.EINVAL),
+        (dict(S=-1), binding.EINVAL), (dict(D=96), binding.EUNSUPPORTED), (dict(qdt=7), binding.EINVAL),
+        (dict(S=4), binding.EINVAL), (dict(S=4, Ks=P), binding.EINVAL), (dict(K=P2), binding.EINVAL),
+    ]
+    for kw, want in cases:
+        assert call(**kw) == want, kw
+    assert call() == binding.ECUDA        # well-formed: the next step is the device query
