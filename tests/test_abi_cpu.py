@@ -82,3 +82,16 @@ def test_noalloc_rejects_bad_arguments_before_any_device_call(lib_path):
     for kw, want in cases:
         assert call(**kw) == want, kw
     assert call() == binding.ECUDA        # well-formed: the next step is the device query
+
+
+def test_quantizer_rejects_bad_arguments_before_any_device_call(lib_path):
+    """pck_quantize_mlx4g32 refuses malformed calls, and returns at once for zero rows, before it
+    touches the device; no case below launches anything, so the stand-in pointers are never used."""
+    from prefix_cached_kv_gb300 import binding
+    lib = binding.load_library(lib_path)
+    P, P8, P2 = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 8), ctypes.c_void_p((1 << 20) + 2)
+    q = lambda X=P, dt=binding.DT_F16, rows=4, kv=64, out=P: lib.pck_quantize_mlx4g32(X, dt, rows, kv, out, None)
+    for kw in (dict(X=None), dict(out=None), dict(rows=-1), dict(kv=16), dict(kv=48), dict(dt=5), dict(X=P8),
+               dict(out=P2)):
+        assert q(**kw) == binding.EINVAL, kw
+    assert q(rows=0) == binding.OK
