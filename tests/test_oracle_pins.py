@@ -67,6 +67,22 @@ def test_record_byte_order():
     assert np.array_equal(c2, codes) and np.array_equal(s2, s) and np.array_equal(b2, b)
 
 
+def test_records_to_heads_lossless_roundtrip():
+    """Token-major records [N, H_kv*D] back to [H_kv, N, D]: on a lossless grid (scale 1/8, a bias
+    of g + t/8 per kv head g and token t, codes (d + t) mod 16 so every group spans 0..15) every
+    value names its own (g, t, d), so the round trip must return K exactly."""
+    H_kv, N, D = 3, 5, 64
+    g = np.arange(H_kv)[:, None, None]
+    t = np.arange(N)[None, :, None]
+    d = np.arange(D)[None, None, :]
+    K = (g + t / 8.0 + ((d + t) % 16) / 8.0).astype(np.float16)
+    assert np.array_equal(K.astype(np.float64), g + t / 8.0 + ((d + t) % 16) / 8.0)   # exact in fp16
+    tok = K.transpose(1, 0, 2).reshape(N, H_kv * D)          # the pages' token-major row layout
+    back = orc.records_to_heads(orc.quantize_records(tok), H_kv, D)
+    assert back.shape == (H_kv, N, D)
+    assert np.array_equal(back, K.astype(np.float64))
+
+
 # ------------------------------------------------------------------ quantiser
 
 def test_quantizer_lossless_on_grid():
@@ -498,3 +514,14 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         with pytest.raises(AssertionError):
             test_causal_suffix_matches_torch_mask(3, 7)
         monkeypatch.setattr(mod, "suffix_allowed", good_mask)
+
+    good_rh = mod.records_to_heads
+
+    def heads_as_token_blocks(rec, H_kv, D):
+        x = mod.dequantize_mlx4g32(*mod.unpack_records(rec, H_kv * D))
+        return x.reshape(H_kv, rec.shape[0], D).copy()     # reads the rows as head-major blocks
+
+    monkeypatch.setattr(mod, "records_to_heads", heads_as_token_blocks)
+    with pytest.raises(AssertionError):
+        test_records_to_heads_lossless_roundtrip()
+    monkeypatch.setattr(mod, "records_to_heads", good_rh)
