@@ -132,8 +132,8 @@ int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void 
 
 /* ATTEND.PREFIX.QUERY <sid> <layer> <H> <D> <top_k> <Q_blob> [<fa_window>].
  * Q: device [H_q, M, D] of q_dtype. M == 1: split-K decode over the slot (fp16 or mlx4g32).
- * M > 1: tiled tensor-core kernel; needs an fp16 slot, q_dtype F16 and D in {64, 128}
- * (PCK_EUNSUPPORTED otherwise).
+ * M > 1: tiled tensor-core kernel; needs an fp16 slot and q_dtype F16 (PCK_EUNSUPPORTED
+ * otherwise).
  * top_k: 0 or >= N (dense). fa_window: 0. Other values are PCK_EUNSUPPORTED.
  * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
 int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
@@ -199,20 +199,30 @@ int pck_quantize_mlx4g32(const void *X, int src_dtype, int64_t rows, int kv_dim,
  * The pages have no counterpart: it exists for callers that cannot allocate device memory at
  * call time (code running under another framework's allocator budget, a request path that must
  * not touch the allocator, or a process without a pck context). It runs the same kernels as
- * pck_store_records + pck_query_fused (M=1), with all scratch in device arrays compiled into
- * libpck (PCK_NOALLOC_SCRATCH_BYTES per GPU, held from library load until process exit).
+ * pck_store_records + pck_query_fused (M=1), with the same split of the work, but all scratch
+ * lives in device arrays compiled into libpck (PCK_NOALLOC_SCRATCH_BYTES per GPU, held from
+ * library load until process exit).
  * K_rec, V_rec: device token-major records [N, rec] as in pck_store_records. Q: device [H_q, D];
  * O: device fp32 [H_q, D]; LSE: device fp32 [H_q] or NULL; K_suf/V_suf: device fp16
  * [H_kv, S_suf, D] or NULL when S_suf == 0. Limits: H_kv * ceil(N/16) * 20*D bytes of resident
  * tiles <= 16 MiB, D in {64, 128, 256}; larger inputs return PCK_EUNSUPPORTED before any
- * launch. The first call on a device looks up the scratch addresses: make it before any stream
- * capture. All calls share the scratch: calls that overlap on the GPU (other streams or host
- * threads) race and must be serialised by the caller. Returns PCK_OK, PCK_EINVAL,
- * PCK_EUNSUPPORTED or PCK_ECUDA (no context, so no pck_last_error text). */
-#define PCK_NOALLOC_SCRATCH_BYTES ((16u << 20) + (8u << 20) + 4096u * 4u + 256u)
+ * launch. The first call on a device (or the first pck_noalloc_status there) looks up the
+ * scratch addresses and the kernels' occupancy: make it before any stream capture. All calls
+ * share the scratch: calls that overlap on the GPU (other streams or host threads) race and
+ * must be serialised by the caller. Returns PCK_OK, PCK_EINVAL, PCK_EUNSUPPORTED or PCK_ECUDA
+ * (no context, so no pck_last_error text). A kernel-side failure (see pck_sync's codes) shows
+ * only in pck_noalloc_status. */
+#define PCK_NOALLOC_SCRATCH_BYTES ((16u << 20) + (16u << 20) + 64u * 4u)
 int pck_attend_records_noalloc(int H_kv, int N, int D, const void *K_rec, const void *V_rec, int H_q,
                                int q_dtype, const void *Q, const int32_t *head_map, int S_suf,
                                const void *K_suf, const void *V_suf, float *O, float *LSE, void *stream);
+
+/* Status of the pck_attend_records_noalloc calls made on the current device since the last
+ * status call. Synchronises `stream`, reads the scratch's device error word and clears it.
+ * PCK_OK: no kernel reported an error. PCK_ECUDA: a CUDA error, or some call's kernels set a
+ * device error code (written to *code when code != NULL; the codes are pck_sync's): at least
+ * one of those calls wrote invalid results. Callers that use the results should check it. */
+int pck_noalloc_status(void *stream, int *code);
 
 /* Counters of ctx. */
 int pck_info(pck_ctx *ctx, pck_info_t *out);
@@ -221,8 +231,11 @@ int pck_info(pck_ctx *ctx, pck_info_t *out);
  * a kernel's bounded wait gave up since the last check (a TMA stage or pipeline barrier that
  * never completed). The kernel then skipped the rest of its work, so the affected results are
  * invalid. pck_last_error names the code: 1 decode ring stage, 2 prefill producer, 3 prefill
- * MMA warp, 4 prefill softmax, 5 prefill final O, 6 sparse scoring copy. The error word and
- * the selector's counters are then reset, so the context stays usable. */
+ * MMA warp, 4 prefill softmax, 5 prefill final O, 6 sparse scoring copy, 7 an fp32 Q element
+ * of an M=1 query with |q| * log2(e) / sqrt(D) >= 65504 (or not finite): the M=1 kernels
+ * carry q * log2(e) / sqrt(D) as an fp16 hi + lo pair, so |q| < 65504 * sqrt(D) / log2(e)
+ * (e.g. 363,000 at D = 64) is the valid range. The error word and the selector's counters
+ * are then reset, so the context stays usable. */
 int pck_sync(pck_ctx *ctx, void *stream);
 
 #ifdef __cplusplus

@@ -25,7 +25,7 @@ EXPORTS = (
     "pck_create", "pck_destroy", "pck_last_error", "pck_store", "pck_store_records", "pck_lookup",
     "pck_drop", "pck_build_block_means", "pck_query", "pck_query_fused", "pck_query_sparse_auto",
     "pck_query_sparse_auto_fused", "pck_query_batch", "pck_query_sparse_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
-    "pck_attend_records_noalloc",
+    "pck_attend_records_noalloc", "pck_noalloc_status",
 )
 
 
@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pck_info": (i, [vp, ctypes.POINTER(InfoT)]),
         "pck_sync": (i, [vp, vp]),
         "pck_attend_records_noalloc": (i, [i, i, i, vp, vp, i, i, vp, vp, i, vp, vp, vp, vp, vp]),
+        "pck_noalloc_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

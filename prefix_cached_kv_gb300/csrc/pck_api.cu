@@ -258,35 +258,24 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     }
     if (total >= (int64_t(1) << 30)) return fail(c, PCK_EUNSUPPORTED, "too many tiles in one launch");
     const DecodeLaunchInfo& li = dinfo(c, fmt, D, decode_ncb(p));
-    const int n_suf_warps = n * n_groups * ((S_suf + TILE_TOK - 1) / TILE_TOK);
-    // prefix workers and suffix warps together stay within one wave of resident warps
-    int64_t max_warps = static_cast<int64_t>(c->sms) * li.ctas_per_sm * DECODE_WARPS - n_suf_warps;
-    if (max_warps < 1) max_warps = 1;
-    int64_t tpw = (total + max_warps - 1) / max_warps;
-    // at most ~32 prefix pieces per item, so that the merge stays short
     int vmax = 1;
     for (int i = 0; i < n; ++i) vmax = std::max(vmax, p.desc[i].vtiles);
-    tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);
-    if (tpw < 2) tpw = 2;
-    // sparse: total bounds the units (every list full); the selector's real count is split over
-    // all the resident prefix warps on the device
-    const int64_t n_workers = sparse ? std::min<int64_t>(max_warps, total) : (total + tpw - 1) / tpw;
     const int n_items = n * n_groups;
-    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
-    const int64_t slots = n_workers + n_items + static_cast<int64_t>(n_items) * n_suf;
-    const size_t need = static_cast<size_t>(slots) * GMAX * partial_stride(D) * sizeof(float);
-    if (need > WS_PARTIAL_BYTES) return fail(c, PCK_EUNSUPPORTED, "split-K workspace too small (%zu B needed)", need);
     if (n_items > WS_COUNTERS) return fail(c, PCK_EUNSUPPORTED, "too many work items");
+    const int64_t max_slots =
+        static_cast<int64_t>(WS_PARTIAL_BYTES / (static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float)));
+    DecodePlan plan;
+    if (!plan_decode(total, vmax, n_items, S_suf, sparse != 0, c->sms, li.ctas_per_sm, max_slots, &plan))
+        return fail(c, PCK_EUNSUPPORTED, "split-K workspace too small for %d items", n_items);
     p.total_tiles = static_cast<int>(total);
-    p.tpw = static_cast<int>(tpw);
+    p.tpw = plan.tpw;
     p.max_units = static_cast<int>(total);
-    p.n_workers = static_cast<int>(n_workers);
-    p.n_suf = n_suf;
+    p.n_workers = plan.n_workers;
+    p.n_suf = plan.n_suf;
     p.partials = c->partials;
     p.counters = c->counters;
     p.err = c->dev_err;
-    const int64_t warps = n_workers + static_cast<int64_t>(n_items) * n_suf;
-    const int n_ctas = static_cast<int>((warps + DECODE_WARPS - 1) / DECODE_WARPS);
+    const int n_ctas = plan.n_ctas;
     cudaError_t e = launch_decode(fmt, D, p, n_ctas, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
     ++c->queries;

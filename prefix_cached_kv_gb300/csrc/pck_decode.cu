@@ -31,6 +31,7 @@
 // rescale of the accumulators off the common path and does not change the result.
 #include <math.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "pck_common.cuh"
@@ -53,6 +54,10 @@ struct DCfg {
 
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 constexpr float LN2 = 0.69314718055994530942f;
+// q enters the MMAs as an fp16 hi + lo pair of q * tau * log2(e): the hi part is finite only for
+// magnitudes below the largest fp16, so a larger (or non-finite) element of Q is reported through
+// the device error word (code 7) instead of silently turning the scores into infinities.
+constexpr float Q_LIMIT = 65504.0f;
 
 // ---------------------------------------------------------------- fp16 path (S^T orientation)
 
@@ -89,14 +94,17 @@ __device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const Decod
                 else xq[cb][s][r] = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(ds.Q) + qh * D + d0));
             }
     }
+    bool bad = false;   // a q element whose prescaled value has no finite fp16 hi part
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
 #pragma unroll
         for (int s = 0; s < KS; ++s)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
+                const float x0 = xq[cb][s][r].x * p.scale_log2, x1 = xq[cb][s][r].y * p.scale_log2;
+                bad |= !(fabsf(x0) < Q_LIMIT) || !(fabsf(x1) < Q_LIMIT);
                 uint32_t hi, lo;
-                split_hi_lo(xq[cb][s][r].x * p.scale_log2, xq[cb][s][r].y * p.scale_log2, hi, lo);
+                split_hi_lo(x0, x1, hi, lo);
                 st.qb[cb][s][r] = part ? lo : hi;
             }
         st.m_ref[cb] = -INFINITY;
@@ -104,7 +112,7 @@ __device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const Decod
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) st.oacc[cb][mt][0] = st.oacc[cb][mt][1] = st.oacc[cb][mt][2] = st.oacc[cb][mt][3] = 0.f;
     }
-    __syncwarp();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_err(p.err, 7);
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -287,6 +295,7 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
                                               const WorkGroup& wg, int lane) {
     using S = I4State<D, NCB>;
     const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
+    bool bad = false;   // a q element whose prescaled value has no finite fp16 hi part
 #pragma unroll
     for (int cb = 0; cb < NCB; ++cb) {
         const int h = cb * 4 + hl;
@@ -309,6 +318,7 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const float x0 = xq[s][r].x * p.scale_log2, x1 = xq[s][r].y * p.scale_log2;
+                bad |= !(fabsf(x0) < Q_LIMIT) || !(fabsf(x1) < Q_LIMIT);
                 gsum[s >> 1] += x0 + x1;
                 uint32_t hi, lo;
                 split_hi_lo(x0, x1, hi, lo);
@@ -330,7 +340,7 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
 #pragma unroll
         for (int mt = 0; mt < S::KS; ++mt) st.oacc[cb][mt][0] = st.oacc[cb][mt][1] = st.oacc[cb][mt][2] = st.oacc[cb][mt][3] = 0.f;
     }
-    __syncwarp();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_err(p.err, 7);
 }
 
 // NT (1, 2 or 4) consecutive 16-token tiles of a kv head: scores of all NT*16 tokens, one online
@@ -1084,6 +1094,28 @@ DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb) {
     if (D == 64) return info_t<FMT_I4, 64, 2>();
     if (D == 128) return info_t<FMT_I4, 128, 2>();
     return info_t<FMT_I4, 256, 2>();
+}
+
+bool plan_decode(int64_t total, int vmax, int n_items, int S_suf, bool sparse, int sms, int ctas_per_sm,
+                 int64_t max_slots, DecodePlan* out) {
+    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
+    const int64_t n_suf_warps = static_cast<int64_t>(n_items) * n_suf;
+    const int64_t fixed = n_items + n_suf_warps;            // item slots + suffix piece slots
+    if (fixed >= max_slots) return false;
+    // prefix workers and suffix warps together stay within one wave of resident warps
+    int64_t max_warps = static_cast<int64_t>(sms) * ctas_per_sm * DECODE_WARPS - n_suf_warps;
+    if (max_warps < 1) max_warps = 1;
+    if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;
+    int64_t tpw = (total + max_warps - 1) / max_warps;
+    tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);         // at most ~32 prefix pieces per item
+    if (tpw < 2) tpw = 2;
+    const int64_t n_workers = sparse ? std::min<int64_t>(max_warps, total) : (total + tpw - 1) / tpw;
+    out->tpw = static_cast<int>(tpw);
+    out->n_workers = static_cast<int>(n_workers);
+    out->n_suf = n_suf;
+    out->n_ctas = static_cast<int>((n_workers + n_suf_warps + DECODE_WARPS - 1) / DECODE_WARPS);
+    out->slots = n_workers + fixed;
+    return true;
 }
 
 int decode_ncb(const DecodeParams& p) {

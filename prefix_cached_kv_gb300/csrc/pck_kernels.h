@@ -25,6 +25,23 @@ struct DecodeLaunchInfo {
     int ctas_per_sm;
 };
 DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb);
+// How one decode launch splits its work. Dense: `total` units (16-token tiles) over items of at
+// most `vmax` units each are cut into ranges of tpw units, one per prefix worker (a warp), with
+// at least ceil(vmax / 32) units per range so that an item has at most ~32 pieces to merge, and at
+// most one wave of resident warps (ctas_per_sm CTAs of DECODE_WARPS warps on each of `sms` SMs)
+// together with the items' suffix warps. Sparse: `total` bounds the units, and every resident
+// prefix warp takes a share on the device. The partial slots the launch writes (one per prefix
+// worker, per item, and per suffix piece) must fit `max_slots`; ranges grow until they do.
+struct DecodePlan {
+    int tpw;              // dense: units per prefix worker
+    int n_workers;        // prefix workers
+    int n_suf;            // suffix pieces per item (ceil(S_suf / 16))
+    int n_ctas;           // CTAs of the launch
+    int64_t slots;        // partial slots written
+};
+// false when the launch cannot fit (the item and suffix slots alone exceed max_slots).
+bool plan_decode(int64_t total, int vmax, int n_items, int S_suf, bool sparse, int sms, int ctas_per_sm,
+                 int64_t max_slots, DecodePlan* out);
 int decode_ncb(const DecodeParams& p);   // 4-head column blocks the mlx4g32 kernel needs for p
 cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);
 

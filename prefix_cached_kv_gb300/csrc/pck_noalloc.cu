@@ -5,16 +5,21 @@
 // loop that is forbidden to touch the allocator on the request path, or a process that has
 // not created a pck context at all. For them, pck_attend_records_noalloc runs the same two
 // kernels as a store + fused query (records -> resident tiles, then the split-K decode with
-// the suffix merge), but every scratch byte it needs lives in the file-scope device arrays
-// below instead of memory from cudaMalloc. The caller passes only inputs and outputs.
+// the suffix merge), planned by the same split as the context path, but every scratch byte it
+// needs lives in the file-scope device arrays below instead of memory from cudaMalloc. The
+// caller passes only inputs and outputs.
 //
 // Cost of that choice: every GPU that loads libpck holds these arrays (PCK_NOALLOC_SCRATCH_BYTES
 // in total) until the process exits, and all calls share them, so calls that overlap on the
 // GPU (two streams, or two host threads) race and must be serialised by the caller.
+//
+// The kernels' device error codes (a bounded wait that gave up, a Q element out of range) land
+// in the scratch's error word, which keeps them until pck_noalloc_status reads and clears it.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/pck.h"
 #include "pck_common.cuh"
@@ -25,43 +30,52 @@ namespace {
 using namespace pck;
 
 constexpr size_t NA_TILE_BYTES = size_t(16) << 20;      // resident tiles of one query's slot
-constexpr size_t NA_PARTIAL_BYTES = size_t(8) << 20;    // split-K partials
-constexpr int NA_COUNTERS = 4096;                       // per-item tickets
+constexpr size_t NA_PARTIAL_BYTES = size_t(16) << 20;   // split-K partials
 constexpr int NA_MAX_DEVICES = 64;
 
 static __device__ __align__(256) uint8_t g_na_tiles[NA_TILE_BYTES];
 static __device__ __align__(256) float g_na_partials[NA_PARTIAL_BYTES / sizeof(float)];
-static __device__ __align__(256) int g_na_counters[NA_COUNTERS];
 static __device__ __align__(256) int g_na_err[64];
 
-struct NaPtrs {
-    bool ready = false;
+static_assert(NA_TILE_BYTES + NA_PARTIAL_BYTES + 64 * sizeof(int) == PCK_NOALLOC_SCRATCH_BYTES,
+              "the header states the scratch size");
+
+// Per device: the scratch arrays' device addresses (host code must not pass the symbols
+// themselves: in host code they are host-side stand-ins), the SM count and the decode
+// kernels' occupancy, found once with the device current.
+struct NaDevice {
+    std::once_flag once;
+    int rc = PCK_ECUDA;
     uint8_t* tiles = nullptr;
     float* partials = nullptr;
-    int* counters = nullptr;
     int* err = nullptr;
     int sms = 0;
+    int ctas_per_sm[3][2] = {};   // [D = 64, 128, 256][column blocks 1, 2]
 };
-NaPtrs g_na[NA_MAX_DEVICES];
+NaDevice g_na[NA_MAX_DEVICES];
 
-// Device addresses of the scratch arrays on the current device (host code must not pass the
-// symbols themselves: in host code they are host-side stand-ins).
-int na_setup(int dev) {
-    NaPtrs& p = g_na[dev];
-    if (p.ready) return PCK_OK;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.tiles), g_na_tiles) != cudaSuccess ||
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.partials), g_na_partials) != cudaSuccess ||
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.counters), g_na_counters) != cudaSuccess ||
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&p.err), g_na_err) != cudaSuccess) {
+void na_setup_once(NaDevice& s, int dev) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.tiles), g_na_tiles) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&s.partials), g_na_partials) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_na_err) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s.sms <= 0) {
         cudaGetLastError();
-        return PCK_ECUDA;
+        s.rc = PCK_ECUDA;
+        return;
     }
-    if (cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || p.sms <= 0) {
-        cudaGetLastError();
-        return PCK_ECUDA;
-    }
-    p.ready = true;
-    return PCK_OK;
+    const int Ds[3] = {64, 128, 256};
+    for (int i = 0; i < 3; ++i)
+        for (int ncb = 1; ncb <= 2; ++ncb) s.ctas_per_sm[i][ncb - 1] = decode_launch_info(FMT_I4, Ds[i], ncb).ctas_per_sm;
+    s.rc = cudaGetLastError() == cudaSuccess ? PCK_OK : PCK_ECUDA;
+}
+
+// The current device's scratch, set up on first use (thread-safe: one set-up per device).
+NaDevice* na_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES) return nullptr;
+    NaDevice& s = g_na[dev];
+    std::call_once(s.once, [&s, dev] { na_setup_once(s, dev); });
+    return s.rc == PCK_OK ? &s : nullptr;
 }
 
 }  // namespace
@@ -78,13 +92,8 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     if (q_dtype != PCK_DT_F32 && q_dtype != PCK_DT_F16) return PCK_EINVAL;
     if (S_suf > 0 && (!K_suf || !V_suf)) return PCK_EINVAL;
     if ((reinterpret_cast<uintptr_t>(K_rec) | reinterpret_cast<uintptr_t>(V_rec)) & 3) return PCK_EINVAL;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES) return PCK_ECUDA;
-    int rc = na_setup(dev);
-    if (rc != PCK_OK) return rc;
-    const NaPtrs& sp = g_na[dev];
 
-    // q heads grouped by kv head, at most GMAX per group
+    // q heads grouped by kv head, at most GMAX per group (host-only work before any CUDA call)
     int hm[PCK_MAX_HEADS];
     for (int h = 0; h < H_q; ++h) {
         if (head_map) {
@@ -97,7 +106,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     }
     static thread_local DecodeParams p;
     std::memset(&p, 0, sizeof p);
-    int n_groups = 0;
+    int n_groups = 0, max_nq = 0;
     for (int g = 0; g < H_kv; ++g) {
         WorkGroup cur{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
         for (int h = 0; h < H_q; ++h) {
@@ -110,33 +119,26 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
         }
         if (cur.nq) p.grp[n_groups++] = cur;
     }
+    for (int i = 0; i < n_groups; ++i) max_nq = p.grp[i].nq > max_nq ? p.grp[i].nq : max_nq;
 
-    // size limits of the static scratch
+    // size limit of the static tile scratch
     const int ntiles = (N + TILE_TOK - 1) / TILE_TOK;
     const size_t tiles_bytes = static_cast<size_t>(H_kv) * ntiles * tile_bytes(FMT_I4, D);
     if (tiles_bytes > NA_TILE_BYTES) return PCK_EUNSUPPORTED;
-    if (n_groups > NA_COUNTERS) return PCK_EUNSUPPORTED;
+
+    NaDevice* sp = na_device();
+    if (!sp) return PCK_ECUDA;
+    const int ncb = max_nq > 4 ? 2 : 1;
+    const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
     const int64_t total = static_cast<int64_t>(n_groups) * ntiles;
-    int max_nq = 0;
-    for (int i = 0; i < n_groups; ++i) max_nq = p.grp[i].nq > max_nq ? p.grp[i].nq : max_nq;
-    const DecodeLaunchInfo li = decode_launch_info(FMT_I4, D, max_nq > 4 ? 2 : 1);
-    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
-    const size_t slot_bytes = static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float);
-    const int64_t max_slots = static_cast<int64_t>(NA_PARTIAL_BYTES / slot_bytes);
-    int64_t max_warps = static_cast<int64_t>(sp.sms) * li.ctas_per_sm * DECODE_WARPS - n_groups * n_suf;
-    if (max_warps < 1) max_warps = 1;
-    const int64_t fixed = n_groups + static_cast<int64_t>(n_groups) * n_suf;   // item + suffix slots
-    if (fixed >= max_slots) return PCK_EUNSUPPORTED;
-    if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;
-    int64_t tpw = (total + max_warps - 1) / max_warps;
-    if (tpw < 2) tpw = 2;
-    const int64_t n_workers = (total + tpw - 1) / tpw;
+    const int64_t max_slots =
+        static_cast<int64_t>(NA_PARTIAL_BYTES / (static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float)));
+    DecodePlan plan;
+    if (!plan_decode(total, ntiles, n_groups, S_suf, false, sp->sms, sp->ctas_per_sm[di][ncb - 1], max_slots, &plan))
+        return PCK_EUNSUPPORTED;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // tickets must start at zero; the error word too
-    if (cudaMemsetAsync(sp.counters, 0, sizeof(int) * n_groups, st) != cudaSuccess) return PCK_ECUDA;
-    if (cudaMemsetAsync(sp.err, 0, sizeof(int), st) != cudaSuccess) return PCK_ECUDA;
-    if (launch_relayout_mlx4(K_rec, V_rec, 0, H_kv, N, D, ntiles, sp.tiles, st, sp.sms) != cudaSuccess)
+    if (launch_relayout_mlx4(K_rec, V_rec, 0, H_kv, N, D, ntiles, sp->tiles, st, sp->sms) != cudaSuccess)
         return PCK_ECUDA;
 
     p.n_desc = 1;
@@ -147,7 +149,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     p.q_f16 = q_dtype == PCK_DT_F16;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     DecodeDesc& d = p.desc[0];
-    d.kv = sp.tiles;
+    d.kv = sp->tiles;
     d.Q = Q;
     d.O = O;
     d.LSE = LSE;
@@ -158,14 +160,35 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     d.vtiles = ntiles;
     d.tile_off = 0;
     p.total_tiles = static_cast<int>(total);
-    p.tpw = static_cast<int>(tpw);
-    p.n_workers = static_cast<int>(n_workers);
-    p.n_suf = n_suf;
-    p.partials = sp.partials;
-    p.counters = sp.counters;
-    p.err = sp.err;
-    const int64_t warps = n_workers + static_cast<int64_t>(n_groups) * n_suf;
-    const int n_ctas = static_cast<int>((warps + DECODE_WARPS - 1) / DECODE_WARPS);
-    if (launch_decode(FMT_I4, D, p, n_ctas, st) != cudaSuccess) return PCK_ECUDA;
+    p.tpw = plan.tpw;
+    p.max_units = static_cast<int>(total);
+    p.n_workers = plan.n_workers;
+    p.n_suf = plan.n_suf;
+    p.partials = sp->partials;
+    p.counters = nullptr;   // the dense decode takes no tickets
+    p.err = sp->err;
+    if (launch_decode(FMT_I4, D, p, plan.n_ctas, st) != cudaSuccess) return PCK_ECUDA;
     return PCK_OK;
+}
+
+extern "C" int pck_noalloc_status(void* stream, int* code) {
+    using namespace pck;
+    if (code) *code = 0;
+    NaDevice* sp = na_device();
+    if (!sp) return PCK_ECUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PCK_ECUDA;
+    }
+    int h = 0;
+    if (cudaMemcpy(&h, sp->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return PCK_ECUDA;
+    }
+    if (code) *code = h;
+    if (h == 0) return PCK_OK;
+    if (cudaMemset(sp->err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+    }
+    return PCK_ECUDA;
 }

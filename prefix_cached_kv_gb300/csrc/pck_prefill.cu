@@ -9,16 +9,21 @@
 //
 // One CTA owns 128 query rows of one kv head (the rows of its GQA q heads are packed:
 // row = local head * M + i) and walks a contiguous range of that kv head's key blocks (64 keys;
-// prefix then suffix); two CTAs share an SM, so one's softmax runs while the other's MMAs do:
+// prefix then suffix); at D <= 128 two CTAs share an SM, so one's softmax runs while the other's
+// MMAs do (at D = 256 the tile needs 512 TMEM columns and 192 KB of shared memory, one CTA per
+// SM, and the next block's S = Q K^T overlaps the softmax instead):
 //   * warp 5 (one lane) streams each block's K and V with cp.async.bulk into 2-stage K and V
 //     rings (the resident fp16 layout already is the MMA operand layout);
 //   * warp 4 issues tcgen05.mma (kind::f16, M=128, fp32 accumulators in TMEM) from one
 //     elected lane: S = Q K^T into one of two S buffers (N = keys of the block, K-steps over
 //     d), then O += P V with P read back from TMEM; S(b+1) runs while the softmax works on S(b);
 //   * warps 0-3 (thread = row = TMEM lane) are the softmax: read S with tcgen05.ld, apply the
-//     causal / length mask, write P = 2^(s - m) as packed fp16 over S and keep the running sum
-//     l (fp32 pairs through the packed f32x2 instructions), and finally read O and write O / l
-//     and LSE = (m + log2 l) ln 2 (or the partial of the key range, merged by a second kernel).
+//     causal / length mask, write P = 2^(s - m) as packed fp16 over S and keep two running sums
+//     (fp32 pairs through the packed f32x2 instructions): l_r of the fp16-rounded P, the
+//     weights P.V actually multiplies, and l_x of the unrounded p; finally read O and write
+//     O / l_r (a convex combination of the V rows whatever the rounding of P, so a large common
+//     offset of V cancels exactly) and LSE = (m + log2 l_x) ln 2, or the partial of the key
+//     range (merged by a second kernel).
 // The running max m (base 2, tau*log2(e)-prescaled) is only moved when a 32-key chunk's sum
 // exceeds 2^15 (which also bounds every P by 2^15, inside fp16): then O (in TMEM, once P.V of
 // the previous block is done), l and the chunk are rescaled. Every wait is bounded: a stuck
@@ -39,8 +44,8 @@ constexpr int PF_MMA_WARP = 4, PF_LOAD_WARP = 5;
 constexpr int PF_ST = 2;              // K and V stages
 constexpr float PF_LN2 = 0.69314718055994530942f;
 
-// Shared memory of one CTA, sized so that two CTAs fit on an SM: the Q tile and 2-stage K and
-// V rings of 64-key blocks. Tensor memory: two S buffers (64 fp32 columns each; P of a block is
+// Shared memory of one CTA: the Q tile and 2-stage K and V rings of 64-key blocks (two CTAs fit
+// on an SM up to D = 128). Tensor memory: two S buffers (64 fp32 columns each; P of a block is
 // written back over the first 32 columns of its buffer as packed fp16) and O (D columns).
 template <int D>
 struct PCfg {
@@ -53,7 +58,8 @@ struct PCfg {
     static constexpr int SMEM = OFF_BAR + 256 + 128;           // + alignment slack (128 B)
     static constexpr int S_COL0 = 0, S_COL1 = PF_BLOCK;        // TMEM columns of the S buffers
     static constexpr int O_COL = 2 * PF_BLOCK;                 // TMEM columns of O (D)
-    static constexpr int TMEM_COLS = 256;
+    static constexpr int TMEM_COLS = O_COL + D <= 256 ? 256 : 512;   // a power of two
+    static constexpr int CTAS_PER_SM = TMEM_COLS == 256 ? 2 : 1;     // TMEM holds 512 columns per SM
 };
 
 // ---------------------------------------------------------------- tcgen05 wrappers
@@ -171,11 +177,11 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 
 // P of one 32-key chunk of a row: p_j = 2^(s_j sc - m) for the nv visible keys (0 for the
-// rest), packed as fp16 pairs into pk; returns the fp32 sum of the p_j.
+// rest), packed as fp16 pairs into pk; returns (sum of the fp16-rounded p_j, sum of the fp32 p_j).
 template <bool FULL>
-__device__ __forceinline__ float chunk_exp(const uint32_t (&v)[32], int nv, uint64_t sc2, float m, uint32_t (&pk)[16]) {
+__device__ __forceinline__ float2 chunk_exp(const uint32_t (&v)[32], int nv, uint64_t sc2, float m, uint32_t (&pk)[16]) {
     const uint64_t nm2 = f2_pack(-m, -m);
-    uint64_t acc0 = 0, acc1 = 0;   // (0.f, 0.f)
+    uint64_t ax0 = 0, ax1 = 0, ar0 = 0, ar1 = 0;   // (0.f, 0.f)
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         float x0, x1;
@@ -185,13 +191,37 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&v)[32], int nv, uint
             p0 = 2 * j < nv ? p0 : 0.f;
             p1 = 2 * j + 1 < nv ? p1 : 0.f;
         }
-        if (j & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-        else acc0 = f2_add(acc0, f2_pack(p0, p1));
-        pk[j] = h2_as_u32(__floats2half2_rn(p0, p1));
+        const __half2 h = __floats2half2_rn(p0, p1);
+        const float2 r = __half22float2(h);
+        if (j & 1) {
+            ax1 = f2_add(ax1, f2_pack(p0, p1));
+            ar1 = f2_add(ar1, f2_pack(r.x, r.y));
+        } else {
+            ax0 = f2_add(ax0, f2_pack(p0, p1));
+            ar0 = f2_add(ar0, f2_pack(r.x, r.y));
+        }
+        pk[j] = h2_as_u32(h);
+    }
+    float a, b, c, d, e, f, g, k;
+    f2_unpack(ax0, a, b);
+    f2_unpack(ax1, c, d);
+    f2_unpack(ar0, e, f);
+    f2_unpack(ar1, g, k);
+    return make_float2((e + f) + (g + k), (a + b) + (c + d));
+}
+
+// Sum of the 32 fp16 values packed in q.
+__device__ __forceinline__ float half_sum32(const uint32_t (&q)[16]) {
+    uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float2 r = __half22float2(u32_as_h2(q[j]));
+        if (j & 1) a1 = f2_add(a1, f2_pack(r.x, r.y));
+        else a0 = f2_add(a0, f2_pack(r.x, r.y));
     }
     float a, b, c, d;
-    f2_unpack(acc0, a, b);
-    f2_unpack(acc1, c, d);
+    f2_unpack(a0, a, b);
+    f2_unpack(a1, c, d);
     return (a + b) + (c + d);
 }
 
@@ -436,7 +466,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         const uint32_t o_tm = tmem + C::O_COL + lane_base;
         const float sc = P.a.scale_log2;
         const uint64_t sc2 = f2_pack(sc, sc);
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, lr = 0.f, lx = 0.f;   // running max; sums of rounded / exact P
         for (int bi = 0; bi < nbl; ++bi) {
             const uint32_t s_tm = tmem + ((bi & 1) ? C::S_COL1 : C::S_COL0) + lane_base;
             // warp-uniform outcome: the tcgen05.ld below must be executed by the whole warp
@@ -452,17 +482,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             for (int c = 0; c < PF_BLOCK / 32; ++c)
                 if (c < nch) tmem_ld32_nowait(s_tm + 32 * c, v[c]);
             tmem_wait_ld();
-            float lsum = 0.f;   // this block's sum at the current m
+            float br = 0.f, bx = 0.f;   // this block's sums (rounded, exact) at the current m
 #pragma unroll
             for (int c = 0; c < PF_BLOCK / 32; ++c) {
                 if (c >= nch) break;
                 const int nv = nvalid - 32 * c;   // visible keys of this chunk (<= 0 .. >= 32)
                 uint32_t pk[16];
-                float cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
+                float2 cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
                 // A sum <= 2^15 bounds every p_j by 2^15: they fit fp16 and m may stay. Otherwise
                 // (or on the first chunk, where m = -inf and the sum is infinite) move m to the
                 // chunk's max, rescale what was summed or written with the old m, and redo.
-                const bool need = !(cs <= 32768.f);
+                const bool need = !(cs.y <= 32768.f);
                 if (__any_sync(0xffffffffu, need)) {
                     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -485,27 +515,32 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                     if (c > 0) {    // P of the earlier chunks, written over columns [0, 16c)
                         tmem_wait_st();
                         const __half2 a2 = __float2half2_rn(alpha);
+                        br = 0.f;   // the rounded sum of what is stored after the rescale
                         for (int c1 = 0; c1 < c; ++c1) {
                             uint32_t q[16];
                             tmem_ld16(s_tm + 16 * c1, q);
 #pragma unroll
                             for (int j = 0; j < 16; ++j) q[j] = h2_as_u32(__hmul2(u32_as_h2(q[j]), a2));
+                            br += half_sum32(q);
                             tmem_st16_nowait(s_tm + 16 * c1, q);
                         }
                     }
                     tmem_wait_st();
-                    lsum *= alpha;
-                    l *= alpha;
+                    bx *= alpha;
+                    lr *= alpha;
+                    lx *= alpha;
                     m = mnew;
                     cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
                 }
-                lsum += cs;
+                br += cs.x;
+                bx += cs.y;
                 // P of this chunk's 32 keys over columns [16c, 16c + 16): S there was read already
                 tmem_st16_nowait(s_tm + 16 * c, pk);
             }
             if (failed) break;
             tmem_wait_st();
-            l += lsum;
+            lr += br;
+            lx += bx;
             tc_fence_before();
             mbar_arrive(bar + B_PR + 8 * (bi & 1));
         }
@@ -514,15 +549,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         } else if (__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_OF, 0))) {
             tc_fence_after();
             // The row goes out through shared memory (the Q, K and V buffers are idle now that
-            // every MMA has completed): the thread writes it there (a 132- or 68-word row
+            // every MMA has completed): the thread writes it there (a D + 4-word row
             // stride, so a quarter-warp's float4 stores hit 32 different banks) and sends it with
             // one bulk copy, instead of strided float4 stores to global memory.
             const bool fin = P.n_split == 1;
-            const float inv = fin ? (l > 0.f ? 1.0f / l : 0.f) : 1.0f;
+            const float inv = fin ? (lr > 0.f ? 1.0f / lr : 0.f) : 1.0f;
             constexpr int RS = partial_stride(D);   // floats per staged row
             float* srow = reinterpret_cast<float*>(smem) + (size_t)tid * RS;
             srow[0] = m;
-            srow[1] = l;
+            srow[1] = lr;
+            srow[2] = lx;
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(o_tm + c0, v);
@@ -536,8 +572,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                 fence_proxy_async_smem();   // this thread's writes, before its own bulk copy reads them
                 if (fin) {   // O row, and LSE
                     bulk_s2g(P.a.O + ((size_t)wg.qh[r / M] * M + i) * D, smem_u32(srow + PARTIAL_O), D * 4);
-                    if (P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(l)) * PF_LN2;
-                } else {     // partial [m, l, -, -, o unnormalised] of this key range, merged later
+                    if (P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(lx)) * PF_LN2;
+                } else {     // partial [m, l_r, l_x, -, o unnormalised] of this key range, merged later
                     bulk_s2g(P.partials + ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * RS, smem_u32(srow),
                              RS * 4);
                 }
@@ -553,14 +589,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
 }
 
-// Merge of the key-range partials of each row: one warp per row, lanes over d (float4). Small
-// per-warp state (4 splits per batch) keeps 48 warps on an SM, so many rows' loads are in flight.
+// Merge of the key-range partials of each row: one warp per row, lanes over d (float4; two of
+// them per lane at D = 256). O is normalised by the merged sum of the rounded P, the LSE comes
+// from the merged sum of the exact p (the two sums of the attention kernel). Small per-warp state
+// (4 splits per batch) keeps many warps on an SM, so many rows' loads are in flight.
 template <int D>
-__global__ void __launch_bounds__(256, 6) prefill_merge_kernel(const __grid_constant__ PfParams P) {
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PfParams P) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int rows = P.n_tiles * PF_ROWS;
-    constexpr int LPP = D / 4;   // lanes holding the row's d (D <= 128)
+    constexpr int LPP = D / 4 < 32 ? D / 4 : 32;   // lanes holding the row's d
+    constexpr int V4 = D / 4 / LPP;                  // float4 of d per lane
     for (int R = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; R < rows; R += (gridDim.x * blockDim.x) >> 5) {
         const int tile = R / PF_ROWS, rr = R - tile * PF_ROWS;
         int grp = 0;
@@ -571,63 +610,77 @@ __global__ void __launch_bounds__(256, 6) prefill_merge_kernel(const __grid_cons
         if (r >= wg.nq * M) continue;
         const float* base = P.partials + ((size_t)tile * P.n_split * PF_ROWS + rr) * partial_stride(D);
         const size_t sstride = (size_t)PF_ROWS * partial_stride(D);
-        // splits in batches of 4: a batch's (m, l) and o loads are all issued before any is used
+        // splits in batches of 4: a batch's (m, l_r, l_x) and o loads are all issued before any is used
         constexpr int NBS = 4;
-        float Mx = -INFINITY, L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Mx = -INFINITY, Lr = 0.f, Lx = 0.f;
+        float4 acc[V4];
+#pragma unroll
+        for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c = 0; c < P.n_split; c += NBS) {
             const int nk = min(NBS, P.n_split - c);
-            float ms = -INFINITY, ls = 0.f;
-            if (lane < nk) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + (c + lane) * sstride));
-                ms = ml.x;
-                ls = ml.y;
-            }
-            float4 xs[NBS];
+            float4 ml = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            if (lane < nk) ml = __ldcg(reinterpret_cast<const float4*>(base + (c + lane) * sstride));
+            float4 xs[NBS][V4];
 #pragma unroll
             for (int k = 0; k < NBS; ++k)
-                xs[k] = (k < nk && lane < LPP)
-                            ? __ldcg(reinterpret_cast<const float4*>(base + (c + k) * sstride + PARTIAL_O) + lane)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            float Mb = ms;
+#pragma unroll
+                for (int v = 0; v < V4; ++v)
+                    xs[k][v] = (k < nk && lane < LPP)
+                                   ? __ldcg(reinterpret_cast<const float4*>(base + (c + k) * sstride + PARTIAL_O) + lane + v * LPP)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            float Mb = ml.x;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
             const float Mn = fmaxf(Mx, Mb);
             if (Mn != -INFINITY) {
                 const float rs = Mx == -INFINITY ? 0.f : exp2f(Mx - Mn);   // rescale of earlier batches
-                L *= rs;
-                acc.x *= rs; acc.y *= rs; acc.z *= rs; acc.w *= rs;
+                Lr *= rs;
+                Lx *= rs;
+#pragma unroll
+                for (int v = 0; v < V4; ++v) { acc[v].x *= rs; acc[v].y *= rs; acc[v].z *= rs; acc[v].w *= rs; }
                 Mx = Mn;
             }
-            const float w = ms == -INFINITY ? 0.f : exp2f(ms - Mx);
-            float Lb = w * ls;
+            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
+            float Br = w * ml.y, Bx = w * ml.z;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Lb += __shfl_xor_sync(0xffffffffu, Lb, o);
-            L += Lb;
+            for (int o = 16; o > 0; o >>= 1) {
+                Br += __shfl_xor_sync(0xffffffffu, Br, o);
+                Bx += __shfl_xor_sync(0xffffffffu, Bx, o);
+            }
+            Lr += Br;
+            Lx += Bx;
 #pragma unroll
             for (int k = 0; k < NBS; ++k) {
                 const float ws = __shfl_sync(0xffffffffu, w, k);
-                acc.x = fmaf(ws, xs[k].x, acc.x); acc.y = fmaf(ws, xs[k].y, acc.y);
-                acc.z = fmaf(ws, xs[k].z, acc.z); acc.w = fmaf(ws, xs[k].w, acc.w);
+#pragma unroll
+                for (int v = 0; v < V4; ++v) {
+                    acc[v].x = fmaf(ws, xs[k][v].x, acc[v].x); acc[v].y = fmaf(ws, xs[k][v].y, acc[v].y);
+                    acc[v].z = fmaf(ws, xs[k][v].z, acc[v].z); acc[v].w = fmaf(ws, xs[k][v].w, acc[v].w);
+                }
             }
         }
         const int h = wg.qh[r / M], i = r % M;
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
-        if (lane < LPP)
-            reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = L > 0.f ? (Mx + log2f(L)) * PF_LN2 : -INFINITY;
+        const float inv = Lr > 0.f ? 1.0f / Lr : 0.f;
+        if (lane < LPP) {
+#pragma unroll
+            for (int v = 0; v < V4; ++v)
+                reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane + v * LPP] =
+                    make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+        }
+        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lx > 0.f ? (Mx + log2f(Lx)) * PF_LN2 : -INFINITY;
     }
 }
 
-// The same merge when there are at most 4 splits (the usual case): a warp takes 4 consecutive
-// rows of a tile and issues all of their loads (16 o float4 per lane, and lane 4q + k's (m, l)
-// of row q, split k) before reducing any, so the whole merge is about one L2 round trip.
+// The same merge when there are at most 4 splits (the usual case) and D <= 128: a warp takes 4
+// consecutive rows of a tile and issues all of their loads (16 o float4 per lane, and lane
+// 4q + k's (m, l_r, l_x) of row q, split k) before reducing any, so the whole merge is about one
+// L2 round trip.
 template <int D>
 __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_constant__ PfParams P) {
+    static_assert(D <= 128, "four rows per warp hold D / 4 <= 32 lanes of o");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    constexpr int LPP = D / 4;   // lanes holding a row's d (D <= 128)
+    constexpr int LPP = D / 4;   // lanes holding a row's d
     const int R0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4;
     if (R0 >= P.n_tiles * PF_ROWS) return;
     const int tile = R0 / PF_ROWS, rr0 = R0 - tile * PF_ROWS;
@@ -637,9 +690,9 @@ __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_con
     const int M = P.a.M, ns = P.n_split;
     const size_t sstride = (size_t)PF_ROWS * partial_stride(D);
     const float* base = P.partials + ((size_t)tile * ns * PF_ROWS + rr0) * partial_stride(D);
-    const int mq = lane >> 2, mk = lane & 3;   // this lane's (row, split) for m and l
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < 16 && mk < ns) ml = __ldcg(reinterpret_cast<const float2*>(base + mq * partial_stride(D) + mk * sstride));
+    const int mq = lane >> 2, mk = lane & 3;   // this lane's (row, split) for m, l_r and l_x
+    float4 ml = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    if (lane < 16 && mk < ns) ml = __ldcg(reinterpret_cast<const float4*>(base + mq * partial_stride(D) + mk * sstride));
     float4 xs[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -648,14 +701,16 @@ __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_con
             xs[q][k] = (k < ns && lane < LPP)
                            ? __ldcg(reinterpret_cast<const float4*>(base + q * partial_stride(D) + k * sstride + PARTIAL_O) + lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    // per row: max and normaliser over the lanes 4q .. 4q + 3
+    // per row: max and the two sums over the lanes 4q .. 4q + 3
     float Mx = ml.x;
     Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 1));
     Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 2));
     const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
-    float L = w * ml.y;
-    L += __shfl_xor_sync(0xffffffffu, L, 1);
-    L += __shfl_xor_sync(0xffffffffu, L, 2);
+    float Lr = w * ml.y, Lx = w * ml.z;
+    Lr += __shfl_xor_sync(0xffffffffu, Lr, 1);
+    Lr += __shfl_xor_sync(0xffffffffu, Lr, 2);
+    Lx += __shfl_xor_sync(0xffffffffu, Lx, 1);
+    Lx += __shfl_xor_sync(0xffffffffu, Lx, 2);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -665,23 +720,25 @@ __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_con
             acc.x = fmaf(wk, xs[q][k].x, acc.x); acc.y = fmaf(wk, xs[q][k].y, acc.y);
             acc.z = fmaf(wk, xs[q][k].z, acc.z); acc.w = fmaf(wk, xs[q][k].w, acc.w);
         }
-        const float Lq = __shfl_sync(0xffffffffu, L, 4 * q), Mq = __shfl_sync(0xffffffffu, Mx, 4 * q);
+        const float Lrq = __shfl_sync(0xffffffffu, Lr, 4 * q), Lxq = __shfl_sync(0xffffffffu, Lx, 4 * q);
+        const float Mq = __shfl_sync(0xffffffffu, Mx, 4 * q);
         const int r = (tile - P.task_off[grp]) * PF_ROWS + rr0 + q;
         if (r >= wg.nq * M) continue;
         const int h = wg.qh[r / M], i = r % M;
-        const float inv = Lq > 0.f ? 1.0f / Lq : 0.f;
+        const float inv = Lrq > 0.f ? 1.0f / Lrq : 0.f;
         if (lane < LPP)
             reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lq > 0.f ? (Mq + log2f(Lq)) * PF_LN2 : -INFINITY;
+        if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lxq > 0.f ? (Mq + log2f(Lxq)) * PF_LN2 : -INFINITY;
     }
 }
 
-bool prefill_supported(int D) { return D == 64 || D == 128; }
+bool prefill_supported(int D) { return D == 64 || D == 128 || D == 256; }
 
 template <int D>
 static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
     using C = PCfg<D>;
+    static_assert(C::CTAS_PER_SM * (C::SMEM + 1024) <= 233472, "the CTAs of an SM must fit its shared memory");
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -705,9 +762,11 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.numAttrs = 1;
-    if (P.n_split <= 4) {   // 4 rows per warp
-        cfg.gridDim = dim3((rows + 31) / 32);
-        return cudaLaunchKernelEx(&cfg, prefill_merge4_kernel<D>, P);
+    if constexpr (D <= 128) {
+        if (P.n_split <= 4) {   // 4 rows per warp
+            cfg.gridDim = dim3((rows + 31) / 32);
+            return cudaLaunchKernelEx(&cfg, prefill_merge4_kernel<D>, P);
+        }
     }
     cfg.gridDim = dim3((rows + 7) / 8);
     return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, P);
@@ -730,9 +789,11 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
     P.suf_ntiles = suf_ntiles;
     P.partials = partials;
     if (off == 0) return cudaSuccess;
-    // key-range splits: enough CTAs for two per SM, never more splits than prefix blocks
+    // key-range splits: enough CTAs to fill the SMs (two per SM up to D = 128, one at D = 256),
+    // never more splits than prefix blocks
     const int nbp = (a.N + PF_BLOCK - 1) / PF_BLOCK;
-    int ns = (2 * sms) / off;
+    const int per_sm = D == 256 ? PCfg<256>::CTAS_PER_SM : PCfg<128>::CTAS_PER_SM;
+    int ns = (per_sm * sms) / off;
     if (ns < 1) ns = 1;
     if (ns > nbp) ns = nbp;
     if (ns > 32) ns = 32;
@@ -740,6 +801,7 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
     P.n_split = ns;
     if (D == 64) return launch_prefill_t<64>(P, st);
     if (D == 128) return launch_prefill_t<128>(P, st);
+    if (D == 256) return launch_prefill_t<256>(P, st);
     return cudaErrorInvalidValue;
 }
 

@@ -85,6 +85,78 @@ def plant_needles(K: np.ndarray, Q: np.ndarray, head_map: np.ndarray, blocks: np
     return K2.astype(np.float16)
 
 
+STRESS_KINDS = ("q30", "q100", "monotone", "dominant_prefix", "dominant_suffix", "bias_scale")
+
+
+def gen_stress(kind: str, seed: int, H_q: int, H_kv: int, N: int, D: int, M: int = 1, S: int = 0,
+               rise: float = 0.75, q_dtype=np.float32):
+    """Inputs that push the online softmax and the number formats to their edges.
+
+    Returns (Q [H_q, M, D] q_dtype, K, V [H_kv, N, D] fp16, K_suf, V_suf [H_kv, S, D] fp16 or None).
+    Scores are only shaped through the inputs; nothing here computes attention.
+
+    * ``q30`` / ``q100``: the standard recipe with Q multiplied by 30 or 100, so scaled logits
+      reach the hundreds.
+    * ``monotone``: every q head is ``8 e + 0.25 n`` for one shared unit vector e, and key t
+      (prefix, then the suffix continuing the sequence) is ``c t e + 0.25 n``; c is chosen so that
+      tau * q.k grows by about ``rise`` log2 units per token, so the running maximum moves all
+      along the sequence.
+    * ``dominant_prefix`` / ``dominant_suffix``: the same e construction with flat keys, except one
+      key (a seeded prefix token, or a seeded suffix token) that gets ``b e`` added, b chosen so
+      that its score exceeds the others by about 60 natural-log units.
+    * ``bias_scale``: the standard recipe, except that in every kv head the first 32 dimensions of
+      K and V are ``+60 + 0.02 n`` and the next 32 (when D > 32) are ``-8 + 0.004 n``: groups with
+      a large bias and a tiny fp16 scale once quantised.
+    """
+    if kind not in STRESS_KINDS:
+        raise ValueError(kind)
+    r = lambda k, shape: rng(seed, 100 + k).standard_normal(shape, dtype=np.float32)
+    if kind in ("q30", "q100", "bias_scale"):
+        K, V = gen_kv(seed, H_kv, N, D)
+        Q = gen_q(seed, H_q, M, D).astype(np.float32)
+        Ks = Vs = None
+        if S:
+            Ks, Vs = gen_suffix(seed, H_kv, S, D)
+        if kind != "bias_scale":
+            Q = Q * np.float32(30.0 if kind == "q30" else 100.0)
+        else:
+            def shift(X):
+                X = X.astype(np.float32)
+                X[..., :32] = 60.0 + 0.02 * r(1 + X.shape[1], X[..., :32].shape)
+                if X.shape[2] > 32:
+                    X[..., 32:64] = -8.0 + 0.004 * r(2 + X.shape[1], X[..., 32:64].shape)
+                return X.astype(np.float16)
+            K, V = shift(K), shift(V)
+            if S:
+                Ks, Vs = shift(Ks), shift(Vs)
+        return Q.astype(q_dtype), K, V, Ks, Vs
+    e = r(3, (D,))
+    e = (e / np.linalg.norm(e)).astype(np.float32)
+    tau = 1.0 / np.sqrt(D)
+    qa = 8.0
+    Q = (qa * e[None, None, :] + 0.25 * r(4, (H_q, M, D))).astype(np.float32)
+    T = N + S
+    Kall = 0.25 * r(5, (H_kv, T, D))
+    Vall = r(6, (H_kv, T, D))
+    if kind == "monotone":
+        c = rise / np.log2(np.e) / (tau * qa)          # key growth per token along e
+        Kall = Kall + (c * np.arange(T, dtype=np.float32))[None, :, None] * e[None, None, :]
+    else:
+        b = 60.0 / (tau * qa)
+        pick = rng(seed, 107)
+        t_star = int(pick.integers(0, N)) if kind == "dominant_prefix" else N + int(pick.integers(0, max(S, 1)))
+        if kind == "dominant_suffix" and S == 0:
+            raise ValueError("dominant_suffix needs S > 0")
+        Kall[:, t_star, :] += b * e[None, :]
+    Kall = Kall.astype(np.float16)
+    Vall = Vall.astype(np.float16)
+    K, V = np.ascontiguousarray(Kall[:, :N]), np.ascontiguousarray(Vall[:, :N])
+    Ks = Vs = None
+    if S:
+        Ks, Vs = np.ascontiguousarray(Kall[:, N:]), np.ascontiguousarray(Vall[:, N:])
+    return Q.astype(q_dtype), K, V, Ks, Vs
+
+
 # Workload table: the five shapes the pages' measurements are quoted on.
 WORKLOADS = {
     "prefix_m1_fp16": dict(H_q=8, H_kv=8, N=2048, D=128, M=1, layers=1, fmt="fp16", S_suf=0),

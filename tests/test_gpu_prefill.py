@@ -31,6 +31,13 @@ CASES = [
     (2, 1, 1, 2, 3, 128, True),         # N = 1, M = 2: one partial key block, two suffix rows
     (1, 1, 4133, 16, 8, 64, True),      # one row tile: 32 key-range splits over 65 blocks (ragged)
     (4, 1, 500, 129, 0, 128, True),     # 516 rows: four full row tiles and one of 4 rows
+    # D = 256: 512 TMEM columns, one CTA per SM, the general merge (two float4 of d per lane)
+    (4, 2, 300, 130, 40, 256, True),
+    (3, 1, 256, 128, 128, 256, True),
+    (6, 2, 1000, 96, 200, 256, False),
+    (2, 1, 1, 2, 3, 256, True),
+    (1, 1, 4133, 16, 8, 256, True),     # 32 key-range splits
+    (12, 1, 200, 50, 30, 256, True),    # GQA 12
 ]
 
 
