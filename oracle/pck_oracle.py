@@ -25,6 +25,14 @@ What each function follows (page title, section):
 * Block-mean top-K selection -- "ATTEND.* and ATTEND.PREFIX.*", section "Wire
   forms" (the server keeps block means of K per slot, scores blocks against Q
   and keeps K_top blocks of size B, GQA-aware).
+* Sparse attention over caller-chosen tokens -- "ATTEND.* and ATTEND.PREFIX.*",
+  command table, QUERY_SPARSE (per-head indices and counts, at most K_sparse_max
+  of them, supplied by the caller, e.g. a learned router).
+* Dequantise-and-transpose of stored records -- "Shared KV Cache Serving -- Pion
+  as LLM Memory", sections "KV.PREFIX.WARM" and "Cold-tier state machine" (the
+  records come back as fp32 and are turned from token-major [N, H*D] into the
+  attention layout [H, N, D]); "V.* -- the V-store", V.FETCH RANGE (dequantised
+  fp32 values).
 
 Readings taken where the pages are silent:
 
@@ -38,6 +46,10 @@ Readings taken where the pages are silent:
 * Top-K is per query head; ties go to the lower block index; K_top is clamped to the
   number of blocks; the selected indices are returned sorted ascending. The last
   block may be partial; its mean is over the tokens it has.
+* QUERY_SPARSE indices are prefix token positions; q head h attends to the first
+  counts[h] entries of its row of indices (kv head head_map[h]).
+* The dequantised values are fp32: the exact s*c + b rounded once to fp32. An fp16
+  output is that fp32 value rounded to fp16.
 """
 from __future__ import annotations
 
@@ -137,6 +149,13 @@ def records_to_heads(rec: np.ndarray, H_kv: int, D: int) -> np.ndarray:
     """Dequantised token-major records [N, H_kv*D] -> float64 [H_kv, N, D]."""
     x = dequantize_mlx4g32(*unpack_records(rec, H_kv * D))
     return x.reshape(rec.shape[0], H_kv, D).transpose(1, 0, 2).copy()
+
+
+def warm_heads(rec: np.ndarray, H_kv: int, D: int, dtype=np.float32) -> np.ndarray:
+    """The WARM / FETCH RANGE form of stored records: [H_kv, N, D] in fp32 (each exact
+    dequantised value rounded once to fp32), or fp16 (that fp32 value rounded to fp16)."""
+    x32 = records_to_heads(rec, H_kv, D).astype(np.float32)
+    return x32 if np.dtype(dtype) == np.float32 else x32.astype(np.float16)
 
 
 # ----------------------------------------------------------------------------------
@@ -282,3 +301,27 @@ def sparse_query(Q, K, V, head_map, B: int, K_top: int, K_suf=None, V_suf=None):
         o, l = attend_rows(Q[h:h + 1], keys, vals, tau)
         O[h], LSE[h] = o[0], l[0]
     return O, LSE, idx, scores
+
+
+def sparse_query_indices(Q, K, V, indices, counts, head_map=None):
+    """M=1 attention of each q head over the prefix tokens a caller chose for it.
+
+    Q [H_q, D] (or [H_q, 1, D]); K, V [H_kv, N, D]; indices [H_q, K_sparse_max] token
+    positions; counts [H_q]: head h attends to tokens indices[h, :counts[h]] of kv head
+    head_map[h] (default h // (H_q / H_kv)). Returns (O [H_q, D], LSE [H_q]).
+    """
+    Q = np.asarray(Q, dtype=np.float64).reshape(np.shape(Q)[0], -1)
+    H_q, D = Q.shape
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if head_map is None:
+        head_map = np.arange(H_q) // (H_q // K.shape[0])
+    tau = 1.0 / math.sqrt(D)
+    O = np.zeros((H_q, D))
+    LSE = np.zeros(H_q)
+    for h in range(H_q):
+        g = int(head_map[h])
+        toks = np.asarray(indices[h][:int(counts[h])], dtype=np.int64)
+        o, l = attend_rows(Q[h:h + 1], K[g, toks], V[g, toks], tau)
+        O[h], LSE[h] = o[0], l[0]
+    return O, LSE

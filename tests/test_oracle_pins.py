@@ -387,6 +387,74 @@ def test_needle_workload_selects_needles():
     assert (orc.topk_margin(scores, Kt) > 0.5).all()
 
 
+def test_sparse_indices_hand_worked_two_heads():
+    """Two heads, D = 2 (tau = 1/sqrt(2)), by hand. Head 0 picks tokens {0, 2} of kv head 0 with
+    q = (sqrt(2) ln 3, 0): scores 0 and ln 3, weights 1/4 and 3/4, LSE = ln 4. Head 1 picks
+    token {1} of kv head 1 alone: O is that value row, LSE its score."""
+    Q = np.array([[math.sqrt(2) * math.log(3), 0.0], [0.5, -1.0]])
+    K = np.array([[[0.0, 5.0], [7.0, 7.0], [1.0, -2.0]],
+                  [[9.0, 9.0], [2.0, 4.0], [-3.0, 3.0]]])
+    V = np.array([[[4.0, 0.0], [100.0, 100.0], [0.0, 8.0]],
+                  [[50.0, 50.0], [-1.0, 2.0], [60.0, 60.0]]])
+    idx = np.array([[0, 2], [1, 0]])
+    cnt = np.array([2, 1])
+    O, L = orc.sparse_query_indices(Q, K, V, idx, cnt, head_map=np.array([0, 1]))
+    assert np.allclose(O[0], [1.0, 6.0]) and math.isclose(L[0], math.log(4.0))
+    assert np.allclose(O[1], [-1.0, 2.0])
+    assert math.isclose(L[1], (0.5 * 2.0 - 1.0 * 4.0) / math.sqrt(2))
+
+
+def test_sparse_indices_all_tokens_equal_dense():
+    rng = np.random.default_rng(13)
+    H_q, H_kv, N, D = 6, 2, 50, 16
+    Q = rng.standard_normal((H_q, 1, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    idx = np.tile(np.arange(N), (H_q, 1))
+    O, L = orc.sparse_query_indices(Q, K, V, idx, np.full(H_q, N))
+    Od, Ld = orc.prefix_query(Q, K, V)
+    assert np.allclose(O, Od[:, 0], atol=1e-12) and np.allclose(L, Ld[:, 0], atol=1e-12)
+
+
+def test_sparse_indices_of_selected_blocks_equal_auto():
+    """The tokens of the blocks the block-mean selector picks, given as indices, give the
+    selector's own sparse answer."""
+    rng = np.random.default_rng(14)
+    H_q, H_kv, N, D, B, Kt = 4, 2, 300, 32, 32, 3
+    Q = rng.standard_normal((H_q, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    hm = synth.default_head_map(H_q, H_kv)
+    Oa, La, sel, _ = orc.sparse_query(Q, K, V, hm, B, Kt)
+    rows = [np.concatenate([np.arange(b * B, min(N, (b + 1) * B)) for b in sel[h]]) for h in range(H_q)]
+    kmax = max(len(r) for r in rows)
+    idx = np.zeros((H_q, kmax), dtype=np.int64)
+    for h, r in enumerate(rows):
+        idx[h, :len(r)] = r
+    O, L = orc.sparse_query_indices(Q, K, V, idx, [len(r) for r in rows], hm)
+    assert np.allclose(O, Oa, atol=1e-12) and np.allclose(L, La, atol=1e-12)
+
+
+def test_warm_heads_lossless_on_grid_and_rounded_once():
+    """Groups that sit exactly on an fp16 grid b + k s come back bit-exact in both output types;
+    random groups come back in fp32 within half an fp32 ulp of the exact value."""
+    H_kv, N, D = 2, 5, 64
+    rng = np.random.default_rng(15)
+    b = np.float16(-3.5)
+    s = np.float16(0.25)
+    x = (np.float32(b) + np.float32(s) * rng.integers(0, 16, size=(N, H_kv * D)).astype(np.float32)).astype(np.float16)
+    x[:, ::32] = b                      # every group holds its minimum ...
+    x[:, 1::32] = np.float16(b + 15 * s)   # ... and its maximum, so the scale is s exactly
+    rec = orc.quantize_records(x)
+    want = x.reshape(N, H_kv, D).transpose(1, 0, 2)
+    assert np.array_equal(orc.warm_heads(rec, H_kv, D, np.float32), want.astype(np.float32))
+    assert np.array_equal(orc.warm_heads(rec, H_kv, D, np.float16), want)
+    y = (rng.standard_normal((N, H_kv * D)) * 40 + 200).astype(np.float16)
+    rec = orc.quantize_records(y)
+    exact = orc.records_to_heads(rec, H_kv, D)
+    w32 = orc.warm_heads(rec, H_kv, D, np.float32)
+    assert w32.dtype == np.float32
+    assert (np.abs(w32.astype(np.float64) - exact) <= np.spacing(np.abs(w32)) / 2).all()
+
+
 # ------------------------------------------------------------------ planted mistakes are caught
 
 def test_pins_catch_planted_mistakes(monkeypatch):
@@ -525,3 +593,29 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_records_to_heads_lossless_roundtrip()
     monkeypatch.setattr(mod, "records_to_heads", good_rh)
+
+    good_sqi = mod.sparse_query_indices
+
+    def counts_off_by_one(Q, K, V, indices, counts, head_map=None):
+        return good_sqi(Q, K, V, indices, np.asarray(counts) + 1, head_map)
+
+    def rows_of_next_head(Q, K, V, indices, counts, head_map=None):
+        return good_sqi(Q, K, V, np.roll(np.asarray(indices), 1, axis=0), np.roll(np.asarray(counts), 1), head_map)
+
+    for bad in (counts_off_by_one, rows_of_next_head):
+        monkeypatch.setattr(mod, "sparse_query_indices", bad)
+        with pytest.raises((AssertionError, IndexError)):
+            test_sparse_indices_hand_worked_two_heads()
+        monkeypatch.setattr(mod, "sparse_query_indices", good_sqi)
+
+    good_wh = mod.warm_heads
+
+    def warm_without_transpose(rec, H_kv, D, dtype=np.float32):
+        x = mod.dequantize_mlx4g32(*mod.unpack_records(rec, H_kv * D)).astype(np.float32)
+        x = x.reshape(H_kv, rec.shape[0], D)
+        return x if np.dtype(dtype) == np.float32 else x.astype(np.float16)
+
+    monkeypatch.setattr(mod, "warm_heads", warm_without_transpose)
+    with pytest.raises(AssertionError):
+        test_warm_heads_lossless_on_grid_and_rounded_once()
+    monkeypatch.setattr(mod, "warm_heads", good_wh)
