@@ -132,8 +132,10 @@ int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void 
 
 /* ATTEND.PREFIX.QUERY <sid> <layer> <H> <D> <top_k> <Q_blob> [<fa_window>].
  * Q: device [H_q, M, D] of q_dtype. M == 1: split-K decode over the slot (fp16 or mlx4g32).
- * M > 1: tiled tensor-core kernel; needs an fp16 slot and q_dtype F16 (PCK_EUNSUPPORTED
- * otherwise).
+ * M > 1: tiled tensor-core kernel; needs q_dtype F16 (PCK_EUNSUPPORTED otherwise). Over an
+ * mlx4g32 slot (D in {64, 128}) the call first dequantises the slot into a stream-ordered
+ * temporary of H_kv * N * 8 * D bytes, each value as an fp16 hi + lo pair, and attends to it
+ * with the same kernel at width 2D, so K and V keep ~22 bits.
  * top_k: 0 or >= N (dense). fa_window: 0. Other values are PCK_EUNSUPPORTED.
  * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
 int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
@@ -167,6 +169,25 @@ int pck_query_sparse_auto_fused(pck_ctx *ctx, const char *sid, int layer, int H_
                                 int fa_window, float *O, float *LSE, int32_t *idx_out,
                                 void *stream);
 
+/* ATTEND.PREFIX.QUERY_SPARSE <sid> <layer> <H> <D> <K_sparse_max> <Q> <indices> <counts>
+ * ("ATTEND.* and ATTEND.PREFIX.*", command table: M=1 attention restricted to caller-supplied
+ * per-head token indices, e.g. from a learned router). Q: device [H_q, D] of q_dtype; O: device
+ * fp32 [H_q, D]; LSE: device fp32 [H_q] or NULL. indices: HOST int32 [H_q, K_sparse_max], row h
+ * holding counts[h] prefix token positions (HOST int32 [H_q]) that q head h attends to, of kv
+ * head head_map[h] (NULL head_map: h / (H_q / H_kv)). Checked on the host before anything is
+ * launched: 1 <= counts[h] <= K_sparse_max, positions in [0, N) and strictly ascending (no
+ * duplicates), else PCK_EINVAL. fp16 slots, H_q <= 64, fa_window 0. The index lists are copied
+ * to the device with a pageable host-to-device copy (the host arrays may be reused once the call
+ * returns; the call cannot be captured in a CUDA graph); the selected tokens are gathered into a
+ * stream-ordered temporary and attended by the split-K decode. */
+int pck_query_sparse(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int K_sparse_max, int q_dtype,
+                     const void *Q, const int32_t *indices, const int32_t *counts, const int32_t *head_map,
+                     int fa_window, float *O, float *LSE, void *stream);
+
+/* Copy the slot's block means (fp32 [H_kv, ceil(N/B), D], built first when absent; see
+ * pck_build_block_means) into the device buffer `out`. */
+int pck_get_block_means(pck_ctx *ctx, const char *sid, int layer, int B, float *out, void *stream);
+
 /* n independent M=1 queries of one shape (H_q, H_kv, D, S_suf, q_dtype, head_map) in ONE
  * launch: the whole batch is split evenly over the GPU. 1 <= n <= PCK_MAX_BATCH. All slots
  * must have the same format. */
@@ -194,6 +215,16 @@ int pck_query_sparse_batch(pck_ctx *ctx, int n, const pck_sparse_desc *descs, in
  * finite and within the fp16 range. Needs no context. */
 int pck_quantize_mlx4g32(const void *X, int src_dtype, int64_t rows, int kv_dim,
                          void *out_records, void *stream);
+
+/* The KV.PREFIX.WARM / V.FETCH RANGE form of stored mlx4g32 records ("Shared KV Cache Serving
+ * -- Pion as LLM Memory", sections "KV.PREFIX.WARM" and "Cold-tier state machine"; "V.* -- the
+ * V-store", V.FETCH): records (device, token-major [N, rec] as in pck_store_records, 4-byte
+ * aligned) -> out (device, [H_kv, N, D], 16-byte aligned), the dequantised x = scale * code +
+ * bias rounded once to fp32 (out_dtype F32), or that fp32 value rounded to fp16 (F16): the
+ * dequantise and the [N, H*D] -> [H, N, D] transpose in one pass. H_kv * D % 32 == 0,
+ * D % 8 == 0. Needs no context. Errors: EINVAL, ECUDA. */
+int pck_dequantize_mlx4g32(const void *records, int64_t N, int H_kv, int D, int out_dtype, void *out,
+                           void *stream);
 
 /* Attention of M=1 queries over mlx4g32 records the caller holds, allocating nothing.
  * The pages have no counterpart: it exists for callers that cannot allocate device memory at

@@ -25,7 +25,8 @@ EXPORTS = (
     "pck_create", "pck_destroy", "pck_last_error", "pck_store", "pck_store_records", "pck_lookup",
     "pck_drop", "pck_build_block_means", "pck_query", "pck_query_fused", "pck_query_sparse_auto",
     "pck_query_sparse_auto_fused", "pck_query_batch", "pck_query_sparse_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
-    "pck_attend_records_noalloc", "pck_noalloc_status",
+    "pck_attend_records_noalloc", "pck_noalloc_status", "pck_query_sparse", "pck_get_block_means",
+    "pck_dequantize_mlx4g32",
 )
 
 
@@ -83,6 +84,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pck_sync": (i, [vp, vp]),
         "pck_attend_records_noalloc": (i, [i, i, i, vp, vp, i, i, vp, vp, i, vp, vp, vp, vp, vp]),
         "pck_noalloc_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
+        "pck_query_sparse": (i, [vp, cp, i, i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp]),
+        "pck_get_block_means": (i, [vp, cp, i, i, vp, vp]),
+        "pck_dequantize_mlx4g32": (i, [vp, i64, i, i, i, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -187,6 +191,21 @@ def quantize_mlx4g32(x: torch.Tensor, out: torch.Tensor | None = None, stream=No
     rc = lib.pck_quantize_mlx4g32(_ptr(x), _dt(x), rows, kv_dim, _ptr(out), _stream(stream))
     if rc != OK:
         raise PckError(rc, "pck_quantize_mlx4g32 rejected its arguments")
+    return out
+
+
+def dequantize_mlx4g32(records: torch.Tensor, N: int, H_kv: int, D: int, dtype=torch.float32, out=None,
+                       stream=None) -> torch.Tensor:
+    """Token-major mlx4g32 records [N, rec] -> [H_kv, N, D] in fp32 or fp16 (WARM / FETCH RANGE form)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty((H_kv, N, D), dtype=dtype, device=records.device)
+    kv = H_kv * D
+    _check_all(_spec(records, "records", nbytes=N * (kv // 2 + kv // 8)),
+               _spec(out, "out", (torch.float32, torch.float16), numel=H_kv * N * D))
+    rc = lib.pck_dequantize_mlx4g32(_ptr(records), N, H_kv, D, _dt(out), _ptr(out), _stream(stream))
+    if rc != OK:
+        raise PckError(rc, "pck_dequantize_mlx4g32 rejected its arguments")
     return out
 
 
@@ -307,6 +326,32 @@ class Context:
                                                       _stream(stream))
         self._rc(rc)
         return O, LSE, idx
+
+    def query_sparse(self, sid, layer, Q, indices, counts, head_map=None, fa_window=0, O=None, LSE=None,
+                     stream=None):
+        """QUERY_SPARSE: Q [H_q, D] (device); indices [H_q, K_sparse_max] and counts [H_q], host
+        integer arrays (positions in the prefix); returns (O [H_q, D], LSE [H_q])."""
+        import numpy as np
+        H_q, D = Q.shape[0], Q.shape[-1]
+        idx = np.ascontiguousarray(indices, dtype=np.int32)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        if idx.ndim != 2 or idx.shape[0] != H_q or cnt.shape != (H_q,):
+            raise ValueError("indices must be [H_q, K_sparse_max] and counts [H_q]")
+        O = torch.empty((H_q, D), dtype=torch.float32, device=Q.device) if O is None else O
+        LSE = torch.empty((H_q,), dtype=torch.float32, device=Q.device) if LSE is None else LSE
+        _check_all(_spec(Q, "Q", _FP, numel=H_q * D), _spec(O, "O", torch.float32, at_least=H_q * D),
+                   _spec(LSE, "LSE", torch.float32, at_least=H_q))
+        hm = _hm(head_map)
+        self._rc(self.lib.pck_query_sparse(self.h, sid.encode(), layer, H_q, D, idx.shape[1], _dt(Q), _ptr(Q),
+                                           idx.ctypes.data_as(ctypes.c_void_p), cnt.ctypes.data_as(ctypes.c_void_p),
+                                           hm[0] if hm else None, fa_window, _ptr(O), _ptr(LSE), _stream(stream)))
+        return O, LSE
+
+    def get_block_means(self, sid, layer, B, H_kv, N, D, stream=None):
+        """The slot's block means, fp32 [H_kv, ceil(N/B), D] (device)."""
+        out = torch.empty((H_kv, (N + B - 1) // B, D), dtype=torch.float32, device="cuda")
+        self._rc(self.lib.pck_get_block_means(self.h, sid.encode(), layer, B, _ptr(out), _stream(stream)))
+        return out
 
     def sparse_batch_caller(self, descs, H_q, H_kv, D, B, K_top, S_suf=0, q_dtype=DT_F32, head_map=None):
         """Prebuild a pck_query_sparse_batch call over descs (dicts with sid, layer, Q, O, and

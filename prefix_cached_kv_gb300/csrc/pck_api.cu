@@ -508,23 +508,41 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
         if (rc != PCK_OK) return rc;
         return check_async(c);
     }
-    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs an fp16 slot");
     if (q_dtype != PCK_DT_F16) return fail(c, PCK_EUNSUPPORTED, "M>1 needs fp16 Q");
     if (reinterpret_cast<uintptr_t>(Q) & 15) return fail(c, PCK_EINVAL, "Q must be 16-byte aligned");
     if (S_suf > 0 && ((reinterpret_cast<uintptr_t>(K_suf) | reinterpret_cast<uintptr_t>(V_suf)) & 15))
         return fail(c, PCK_EINVAL, "K_suf/V_suf must be 16-byte aligned when M > 1");
-    if (!prefill_supported(D)) return fail(c, PCK_EUNSUPPORTED, "M>1 kernel not available for D=%d", D);
-    if (S_suf > 0 && static_cast<size_t>(s->H_kv) * 2 * fp16_region_bytes((S_suf + TILE_TOK - 1) / TILE_TOK, D) >
+    // An mlx4g32 slot is attended as an fp16 slot of head dimension 2D holding [hi | lo] fp16 pairs
+    // of its dequantised values (S = [Q | Q] [K_hi | K_lo]^T, O = P V_hi + P V_lo): the tensor-core
+    // kernel runs at width DK = 2D.
+    const bool split = s->fmt == PCK_FMT_MLX4G32;
+    const int DK = split ? 2 * D : D;
+    if (!prefill_supported(DK))
+        return fail(c, PCK_EUNSUPPORTED, "M>1 kernel not available for D=%d%s", D, split ? " on an mlx4g32 slot" : "");
+    if (S_suf > 0 && static_cast<size_t>(s->H_kv) * 2 * fp16_region_bytes((S_suf + TILE_TOK - 1) / TILE_TOK, DK) >
                          WS_SUFFIX_BYTES)
         return fail(c, PCK_EUNSUPPORTED, "suffix of %d tokens exceeds the staging workspace", S_suf);
     const int suf_ntiles = (S_suf + TILE_TOK - 1) / TILE_TOK;
     if (S_suf > 0) {   // stage the suffix in the resident layout (the MMA operand layout)
-        cudaError_t e = launch_relayout_fp16(K_suf, V_suf, 1, s->H_kv, S_suf, D, suf_ntiles, c->suf_ws, st, c->sms);
+        cudaError_t e = launch_relayout_fp16(K_suf, V_suf, 1, s->H_kv, S_suf, D, suf_ntiles, c->suf_ws, st, c->sms, DK);
         if (e != cudaSuccess) return cuda_fail(c, e, "suffix staging launch");
+    }
+    uint8_t* kv = s->tiles;
+    if (split) {
+        const size_t bytes = static_cast<size_t>(s->H_kv) * 2 * fp16_region_bytes(s->ntiles, DK);
+        if (cudaMallocAsync(reinterpret_cast<void**>(&kv), bytes, st) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, PCK_ENOMEM, "cannot allocate %zu bytes for the dequantised slot", bytes);
+        }
+        cudaError_t e = launch_mlx4_split(s->tiles, s->H_kv, s->ntiles, D, kv, st);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(kv, st);
+            return cuda_fail(c, e, "dequantise launch");
+        }
     }
     PrefillParams pp{};
     pp.Q = static_cast<const __half*>(Q);
-    pp.kv = s->tiles;
+    pp.kv = kv;
     pp.O = O;
     pp.LSE = LSE;
     pp.H_q = H_q;
@@ -534,10 +552,12 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     pp.ntiles = s->ntiles;
     pp.S_suf = S_suf;
     pp.causal = causal;
+    pp.q_dup = split ? 1 : 0;
     pp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     pp.err = c->dev_err;
     cudaError_t e = launch_prefill(pp, grp, n_groups, S_suf > 0 ? c->suf_ws : nullptr, suf_ntiles, c->partials,
-                                   WS_PARTIAL_BYTES, c->sms, st, D);
+                                   WS_PARTIAL_BYTES, c->sms, st, DK);
+    if (split) cudaFreeAsync(kv, st);   // stream-ordered: after the kernels that read it
     if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
     ++c->queries;
     return check_async(c);
@@ -723,6 +743,121 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
                     static_cast<cudaStream_t>(stream));
     if (rc != PCK_OK) return rc;
     return check_async(c);
+}
+
+int pck_query_sparse(pck_ctx* c, const char* sid, int layer, int H_q, int D, int K_sparse_max, int q_dtype,
+                     const void* Q, const int32_t* indices, const int32_t* counts, const int32_t* head_map, int fa_window,
+                     float* O, float* LSE, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!Q || !O || !indices || !counts) return fail(c, PCK_EINVAL, "NULL Q, O, indices or counts");
+    if ((reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(Q)) & 15)
+        return fail(c, PCK_EINVAL, "Q and O must be 16-byte aligned");
+    if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
+    if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
+    if (K_sparse_max < 1) return fail(c, PCK_EINVAL, "K_sparse_max=%d", K_sparse_max);
+    if (H_q < 1 || H_q > MAX_DESC) return fail(c, PCK_EINVAL, "H_q=%d (1..%d)", H_q, MAX_DESC);
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "QUERY_SPARSE needs an fp16 slot");
+    if (D != s->D) return fail(c, PCK_EINVAL, "D=%d but the slot holds D=%d", D, s->D);
+    int8_t hm[PCK_MAX_HEADS];
+    WorkGroup grp_all[MAX_GROUPS];
+    int n_groups_all = 0;
+    rc = build_groups(c, H_q, s->H_kv, head_map, grp_all, &n_groups_all, hm, nullptr);
+    if (rc != PCK_OK) return rc;
+    // every head's list: 1 <= counts[h] <= K_sparse_max strictly ascending positions in [0, N)
+    int kmax = 0;
+    for (int h = 0; h < H_q; ++h) {
+        const int n = counts[h];
+        if (n < 1 || n > K_sparse_max) return fail(c, PCK_EINVAL, "counts[%d]=%d outside [1, %d]", h, n, K_sparse_max);
+        const int32_t* row = indices + static_cast<size_t>(h) * K_sparse_max;
+        for (int k = 0; k < n; ++k) {
+            if (row[k] < 0 || row[k] >= s->N)
+                return fail(c, PCK_EINVAL, "indices[%d][%d]=%d outside [0, %d)", h, k, row[k], s->N);
+            if (k > 0 && row[k] <= row[k - 1])
+                return fail(c, PCK_EINVAL, "indices[%d] not strictly ascending at %d (duplicate or unsorted)", h, k);
+        }
+        kmax = std::max(kmax, n);
+    }
+    // one device buffer: index rows [H_q][kmax], counts [H_q], head map [H_q] (int8), then one
+    // compact fp16 slot per q head holding its gathered tokens
+    const int ntmax = (kmax + TILE_TOK - 1) / TILE_TOK;
+    const size_t head_stride = 2 * fp16_region_bytes(ntmax, D);
+    const size_t meta = (static_cast<size_t>(H_q) * (kmax + 1) * sizeof(int32_t) + H_q + 255) & ~size_t(255);
+    std::vector<uint8_t> host(meta, 0);
+    int32_t* hidx = reinterpret_cast<int32_t*>(host.data());
+    for (int h = 0; h < H_q; ++h)
+        std::memcpy(hidx + static_cast<size_t>(h) * kmax, indices + static_cast<size_t>(h) * K_sparse_max,
+                    sizeof(int32_t) * counts[h]);
+    std::memcpy(hidx + static_cast<size_t>(H_q) * kmax, counts, sizeof(int32_t) * H_q);
+    std::memcpy(host.data() + static_cast<size_t>(H_q) * (kmax + 1) * sizeof(int32_t), hm, H_q);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* buf = nullptr;
+    const size_t bytes = meta + static_cast<size_t>(H_q) * head_stride;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate %zu bytes for the gathered tokens", bytes);
+    }
+    cudaError_t e = cudaMemcpyAsync(buf, host.data(), meta, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) {
+        const int32_t* didx = reinterpret_cast<const int32_t*>(buf);
+        e = launch_gather_fp16(s->tiles, s->ntiles, D, didx, didx + static_cast<size_t>(H_q) * kmax,
+                               reinterpret_cast<const int8_t*>(buf + static_cast<size_t>(H_q) * (kmax + 1) * sizeof(int32_t)),
+                               H_q, kmax, head_stride, buf + meta, st);
+    }
+    if (e != cudaSuccess) {
+        cudaFreeAsync(buf, st);
+        return cuda_fail(c, e, "gather launch");
+    }
+    // one dense decode over H_q single-head compact slots (one descriptor per q head)
+    Slot tmp[MAX_DESC];
+    DescIn d[MAX_DESC];
+    const size_t qbytes = static_cast<size_t>(D) * (q_dtype == PCK_DT_F16 ? 2 : 4);
+    for (int h = 0; h < H_q; ++h) {
+        tmp[h].fmt = PCK_FMT_FP16;
+        tmp[h].H_kv = 1;
+        tmp[h].N = counts[h];
+        tmp[h].D = D;
+        tmp[h].ntiles = (counts[h] + TILE_TOK - 1) / TILE_TOK;
+        tmp[h].tiles = buf + meta + static_cast<size_t>(h) * head_stride;
+        d[h] = DescIn{&tmp[h], static_cast<const uint8_t*>(Q) + h * qbytes, O + static_cast<size_t>(h) * D,
+                      LSE ? LSE + h : nullptr, nullptr, nullptr};
+    }
+    const WorkGroup one{0, 1, {0, -1, -1, -1, -1, -1, -1, -1}};
+    rc = run_decode(c, PCK_FMT_FP16, D, 1, 1, 0, q_dtype == PCK_DT_F16, &one, 1, d, H_q, 0, 0, 0, nullptr, st);
+    cudaFreeAsync(buf, st);   // stream-ordered: after the kernels that read it
+    if (rc != PCK_OK) return rc;
+    return check_async(c);
+}
+
+int pck_get_block_means(pck_ctx* c, const char* sid, int layer, int B, float* out, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (!out) return fail(c, PCK_EINVAL, "NULL out");
+    int rc = pck_build_block_means(c, sid, layer, B, stream);
+    if (rc != PCK_OK) return rc;
+    Slot* s = nullptr;
+    rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    const size_t bytes = static_cast<size_t>(s->H_kv) * ((s->N + B - 1) / B) * s->D * sizeof(float);
+    cudaError_t e = cudaMemcpyAsync(out, s->kmean[B], bytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(c, e, "block means copy");
+    return PCK_OK;
+}
+
+int pck_dequantize_mlx4g32(const void* records, int64_t N, int H_kv, int D, int out_dtype, void* out, void* stream) {
+    if (!records || !out || N < 0 || H_kv < 1 || H_kv > PCK_MAX_HEADS || D < 8 || D % 8 || (H_kv * D) % 32)
+        return PCK_EINVAL;
+    if (!dtype_ok(out_dtype)) return PCK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(records) & 3) return PCK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(out) & 15) return PCK_EINVAL;
+    if (N == 0) return PCK_OK;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = launch_dequant_records(records, N, H_kv, D, out_dtype == PCK_DT_F16, out,
+                                           static_cast<cudaStream_t>(stream), sms > 0 ? sms : 1);
+    return e == cudaSuccess ? PCK_OK : PCK_ECUDA;
 }
 
 int pck_quantize_mlx4g32(const void* X, int src_dtype, int64_t rows, int kv_dim, void* out_records, void* stream) {

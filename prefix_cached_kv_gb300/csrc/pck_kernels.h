@@ -12,10 +12,20 @@ constexpr int PCK_MAXH = 64;
 
 // store side
 cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim, void* out, cudaStream_t st, int sms);
+// DS: head dimension of the written layout (0 = D; DS > D pads every row with zero columns)
 cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
-                                 void* out, cudaStream_t st, int sms);
+                                 void* out, cudaStream_t st, int sms, int DS = 0);
 cudaError_t launch_relayout_mlx4(const void* Krec, const void* Vrec, int head_rows, int H_kv, int N, int D, int ntiles,
                                  void* out, cudaStream_t st, int sms);
+// QUERY_SPARSE: the tokens idx[h][0 .. counts[h]) of kv head head_map[h] of a resident fp16 slot,
+// gathered into one compact fp16 slot per q head h (at out + h * head_stride)
+cudaError_t launch_gather_fp16(const void* tiles, int ntiles, int D, const int* idx, const int* counts,
+                               const int8_t* head_map, int H_q, int kmax, size_t head_stride, void* out, cudaStream_t st);
+// mlx4g32 slot tiles -> an fp16 slot of head dimension 2D holding [hi | lo] fp16 pairs of the values
+cudaError_t launch_mlx4_split(const void* tiles, int H_kv, int ntiles, int D, void* out, cudaStream_t st);
+// token-major records [N, H_kv*D] -> [H_kv, N, D] fp32 or fp16
+cudaError_t launch_dequant_records(const void* rec, int64_t N, int H_kv, int D, int out_f16, void* out, cudaStream_t st,
+                                   int sms);
 
 // M=1 split-K decode (dense or sparse item sequences), fused suffix and merge
 struct DecodeLaunchInfo {
@@ -76,11 +86,15 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
 
 // batched-Q tensor-core prefill (tcgen05)
 struct PrefillParams {
-    const __half* Q;          // [H_q, M, D]
+    const __half* Q;          // [H_q, M, D] (q_dup: [H_q, M, D/2])
     const uint8_t* kv;        // resident fp16 slot
-    float* O;                 // [H_q, M, D]
+    float* O;                 // [H_q, M, D] (q_dup: [H_q, M, D/2])
     float* LSE;               // [H_q, M] or nullptr
     int H_q, H_kv, M, N, ntiles, S_suf, causal;
+    // q_dup: the slot holds [hi | lo] fp16 pairs of D/2-wide values (the suffix too); each Q row
+    // enters the tile twice, [q | q], so S sums both halves, and O is folded: O[c] = O'[c] +
+    // O'[c + D/2].
+    int q_dup;
     float scale_log2;
     int* err;
 };

@@ -348,10 +348,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         const int R = tid >> 3, rr = tid & 7;
         if (r < rows_total) {
             const int h = wg.qh[r / M], i = r % M;
-            const uint4* src = reinterpret_cast<const uint4*>(P.a.Q + ((size_t)h * M + i) * D);
+            const int qc = P.a.q_dup ? D / 16 : D / 8;   // 16-byte chunks of a source row
+            const uint4* src = reinterpret_cast<const uint4*>(P.a.Q + ((size_t)h * M + i) * (qc * 8));
 #pragma unroll 4
             for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4*>(qs + (R * (D / 8) + c) * 128 + rr * 16) = __ldg(src + c);
+                *reinterpret_cast<uint4*>(qs + (R * (D / 8) + c) * 128 + rr * 16) = __ldg(src + (c < qc ? c : c - qc));
         } else {
 #pragma unroll 4
             for (int c = 0; c < D / 8; ++c)
@@ -568,10 +569,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                         make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
                                     __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
             }
+            const int DO = P.a.q_dup ? D / 2 : D;   // columns of an output row
+            if (fin && P.a.q_dup)
+                for (int c = 0; c < D / 2; c += 4) {   // O = O_hi + O_lo
+                    const float4 a = *reinterpret_cast<const float4*>(srow + PARTIAL_O + c);
+                    const float4 b = *reinterpret_cast<const float4*>(srow + PARTIAL_O + D / 2 + c);
+                    *reinterpret_cast<float4*>(srow + PARTIAL_O + c) = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+                }
             if (row_ok) {
                 fence_proxy_async_smem();   // this thread's writes, before its own bulk copy reads them
                 if (fin) {   // O row, and LSE
-                    bulk_s2g(P.a.O + ((size_t)wg.qh[r / M] * M + i) * D, smem_u32(srow + PARTIAL_O), D * 4);
+                    bulk_s2g(P.a.O + ((size_t)wg.qh[r / M] * M + i) * DO, smem_u32(srow + PARTIAL_O), DO * 4);
                     if (P.a.LSE) P.a.LSE[(size_t)wg.qh[r / M] * M + i] = (m + log2f(lx)) * PF_LN2;
                 } else {     // partial [m, l_r, l_x, -, o unnormalised] of this key range, merged later
                     bulk_s2g(P.partials + ((size_t)(task * P.n_split + split) * PF_ROWS + tid) * RS, smem_u32(srow),
@@ -661,11 +669,28 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
         }
         const int h = wg.qh[r / M], i = r % M;
         const float inv = Lr > 0.f ? 1.0f / Lr : 0.f;
-        if (lane < LPP) {
+        if (!P.a.q_dup) {
+            if (lane < LPP) {
 #pragma unroll
-            for (int v = 0; v < V4; ++v)
-                reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane + v * LPP] =
-                    make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+                for (int v = 0; v < V4; ++v)
+                    reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane + v * LPP] =
+                        make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+            }
+        } else {   // O = O_hi + O_lo: float4 k and k + D/8 of the row
+            float4* orow = reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * (D / 2));
+            if constexpr (V4 == 2) {
+                orow[lane] = make_float4((acc[0].x + acc[1].x) * inv, (acc[0].y + acc[1].y) * inv,
+                                         (acc[0].z + acc[1].z) * inv, (acc[0].w + acc[1].w) * inv);
+            } else {
+                float4 b;
+                b.x = __shfl_down_sync(0xffffffffu, acc[0].x, LPP / 2);
+                b.y = __shfl_down_sync(0xffffffffu, acc[0].y, LPP / 2);
+                b.z = __shfl_down_sync(0xffffffffu, acc[0].z, LPP / 2);
+                b.w = __shfl_down_sync(0xffffffffu, acc[0].w, LPP / 2);
+                if (lane < LPP / 2)
+                    orow[lane] = make_float4((acc[0].x + b.x) * inv, (acc[0].y + b.y) * inv, (acc[0].z + b.z) * inv,
+                                             (acc[0].w + b.w) * inv);
+            }
         }
         if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lx > 0.f ? (Mx + log2f(Lx)) * PF_LN2 : -INFINITY;
     }
@@ -723,12 +748,24 @@ __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_con
         const float Lrq = __shfl_sync(0xffffffffu, Lr, 4 * q), Lxq = __shfl_sync(0xffffffffu, Lx, 4 * q);
         const float Mq = __shfl_sync(0xffffffffu, Mx, 4 * q);
         const int r = (tile - P.task_off[grp]) * PF_ROWS + rr0 + q;
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);   // q_dup: O_lo of this lane's columns
+        if (P.a.q_dup) {
+            b.x = __shfl_down_sync(0xffffffffu, acc.x, LPP / 2);
+            b.y = __shfl_down_sync(0xffffffffu, acc.y, LPP / 2);
+            b.z = __shfl_down_sync(0xffffffffu, acc.z, LPP / 2);
+            b.w = __shfl_down_sync(0xffffffffu, acc.w, LPP / 2);
+        }
         if (r >= wg.nq * M) continue;
         const int h = wg.qh[r / M], i = r % M;
         const float inv = Lrq > 0.f ? 1.0f / Lrq : 0.f;
-        if (lane < LPP)
-            reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (!P.a.q_dup) {
+            if (lane < LPP)
+                reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane] =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else if (lane < LPP / 2) {
+            reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * (D / 2))[lane] =
+                make_float4((acc.x + b.x) * inv, (acc.y + b.y) * inv, (acc.z + b.z) * inv, (acc.w + b.w) * inv);
+        }
         if (lane == 0 && P.a.LSE) P.a.LSE[(size_t)h * M + i] = Lxq > 0.f ? (Mq + log2f(Lxq)) * PF_LN2 : -INFINITY;
     }
 }

@@ -116,19 +116,45 @@ __global__ void __launch_bounds__(256, 6) quantize_mlx4g32_kernel(const SrcT* __
 
 // ------------------------------------------------------------------ fp16 re-layout
 
-// One CTA per (16-token tile j, kv head g). K and V rows t0..t0+15 are loaded coalesced into
-// shared memory (zeros past N; rows padded by 16 bytes so the column reads below spread over
-// the banks), then the tile's two 32*D-byte pieces of the resident layout are written with
-// consecutive 16-byte stores: the K piece as core matrices [token group][d chunk] (16 bytes =
-// 8 consecutive d of one token), the V piece as core matrices [d group][key chunk] (16 bytes =
-// 8 consecutive keys of one d).
+// The 16 tokens of one tile, K and V rows of DS halves each, staged in shared memory (rows padded
+// by 8 halves so that the column reads below spread over the banks) -> the tile's two 32*DS-byte
+// pieces of the resident layout, written with consecutive 16-byte stores: the K piece as core
+// matrices [token group][d chunk] (16 bytes = 8 consecutive d of one token), the V piece as core
+// matrices [d group][key chunk] (16 bytes = 8 consecutive keys of one d).
+template <int MAXD>
+__device__ __forceinline__ void write_fp16_tile(const __half (&sm)[2][TILE_TOK][MAXD + 8], int DS, uint4* kout,
+                                                uint4* vout) {
+    const int piece = 2 * DS;                                 // uint4 per tile piece (32 * DS bytes)
+    const int cpt = DS / 8;                                   // d chunks (K) / d groups (V)
+    for (int u = threadIdx.x; u < piece; u += blockDim.x) {
+        const int core = u >> 3, row = u & 7;
+        const int T = core / cpt, c = core - T * cpt;         // K core: token group T, d chunk c
+        kout[u] = *reinterpret_cast<const uint4*>(&sm[0][8 * T + row][8 * c]);
+        const int dg = core >> 1, tc = core & 1, d = 8 * dg + row;   // V core: d group, key chunk
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k][d])) |
+                   (static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k + 1][d])) << 16);
+        vout[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// One CTA per (16-token tile j, kv head g): K and V rows t0..t0+15 are loaded coalesced into
+// shared memory (zeros past N), then written in the resident layout of head dimension DS >= D
+// (columns D .. DS-1 zero: the [hi | lo] form of fp16 values, whose lo parts are 0).
 template <typename SrcT>
 __global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
-                                                            int N, int D, int ntiles, uint4* __restrict__ out) {
+                                                            int N, int D, int DS, int ntiles, uint4* __restrict__ out) {
     constexpr int MAXD = 256;
     __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
     const int j = blockIdx.x, g = blockIdx.y;
     const int t0 = j * TILE_TOK;
+    for (int q = threadIdx.x; q < 2 * TILE_TOK * (DS - D) / 8; q += blockDim.x) {
+        const int x = q / (TILE_TOK * (DS - D) / 8), r = q - x * (TILE_TOK * (DS - D) / 8);
+        const int tok = r / ((DS - D) / 8), c = r - tok * ((DS - D) / 8);
+        *reinterpret_cast<uint4*>(&sm[x][tok][D + 8 * c]) = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int x = 0; x < 2; ++x) {
         const SrcT* src = (x ? V : K) + (int64_t)g * N * D;
         if constexpr (sizeof(SrcT) == 2) {
@@ -146,21 +172,137 @@ __global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restri
         }
     }
     __syncthreads();
-    const int64_t piece = 2 * D;                              // uint4 per tile piece (32 * D bytes)
-    uint4* kout = out + ((int64_t)g * 2 * ntiles + j) * piece;
-    uint4* vout = out + ((int64_t)g * 2 * ntiles + ntiles + j) * piece;
-    const int cpt = D / 8;                                    // d chunks (K) / d groups (V)
-    for (int u = threadIdx.x; u < piece; u += blockDim.x) {
-        const int core = u >> 3, row = u & 7;
-        const int T = core / cpt, c = core - T * cpt;         // K core: token group T, d chunk c
-        kout[u] = *reinterpret_cast<const uint4*>(&sm[0][8 * T + row][8 * c]);
-        const int dg = core >> 1, tc = core & 1, d = 8 * dg + row;   // V core: d group, key chunk
-        uint32_t w[4];
+    const int64_t piece = 2 * DS;
+    write_fp16_tile<MAXD>(sm, DS, out + ((int64_t)g * 2 * ntiles + j) * piece, out + ((int64_t)g * 2 * ntiles + ntiles + j) * piece);
+}
+
+// ------------------------------------------------------------------ QUERY_SPARSE token gather
+
+// One CTA per (output tile j, q head h): the tokens idx[h][16j ..] (zeros past counts[h]) of kv
+// head head_map[h] are read from the resident fp16 slot (K: 16 bytes of 8 d per token and d
+// chunk; V: single values from the transposed tiles) into shared memory and written as tile j of
+// head h's compact slot: K region of ceil(counts[h] / 16) tiles, then its V region, at
+// out + h * head_stride bytes.
+__global__ void __launch_bounds__(128) gather_fp16_kernel(const uint8_t* __restrict__ tiles, int ntiles, int D,
+                                                          const int* __restrict__ idx, const int* __restrict__ counts,
+                                                          const int8_t* __restrict__ head_map, int kmax,
+                                                          size_t head_stride, uint8_t* __restrict__ out) {
+    constexpr int MAXD = 256;
+    __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
+    const int j = blockIdx.x, h = blockIdx.y;
+    const int cnt = counts[h];
+    const int nt = (cnt + TILE_TOK - 1) / TILE_TOK;
+    if (j >= nt) return;
+    const int g = head_map[h];
+    const uint8_t* kreg = tiles + (size_t)g * 2 * fp16_region_bytes(ntiles, D);
+    const uint8_t* vreg = kreg + fp16_region_bytes(ntiles, D);
+    const int* row = idx + (size_t)h * kmax;
+    for (int q = threadIdx.x; q < TILE_TOK * D / 8; q += blockDim.x) {
+        const int r = q / (D / 8), c = q - r * (D / 8);
+        const int k = j * TILE_TOK + r;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (k < cnt) {
+            const int t = row[k];
+            val = __ldg(reinterpret_cast<const uint4*>(kreg + ((size_t)(t >> 3) * (D / 8) + c) * 128 + (t & 7) * 16));
+        }
+        *reinterpret_cast<uint4*>(&sm[0][r][8 * c]) = val;
+    }
+    for (int q = threadIdx.x; q < TILE_TOK * D; q += blockDim.x) {
+        const int r = q / D, d = q - r * D;
+        const int k = j * TILE_TOK + r;
+        __half v = __float2half_rn(0.f);
+        if (k < cnt) {
+            const int t = row[k];
+            v = *reinterpret_cast<const __half*>(vreg + (size_t)(t >> 4) * 32 * D + ((d >> 3) * 2 + ((t & 15) >> 3)) * 128 +
+                                                 (d & 7) * 16 + (t & 7) * 2);
+        }
+        sm[1][r][d] = v;
+    }
+    __syncthreads();
+    uint8_t* base = out + (size_t)h * head_stride;
+    write_fp16_tile<MAXD>(sm, D, reinterpret_cast<uint4*>(base + (size_t)j * 32 * D),
+                          reinterpret_cast<uint4*>(base + fp16_region_bytes(nt, D) + (size_t)j * 32 * D));
+}
+
+// ------------------------------------------------------------------ mlx4g32 tiles -> fp16 hi/lo pairs
+
+// Code of (token tt, dimension d) of an mlx4g32 tile (layout in pck_common.cuh): K codes start at
+// the tile, V codes at 10 * D bytes.
+__device__ __forceinline__ uint32_t tile_k_code(const uint8_t* tile, int tt, int d) {
+    const int s = d >> 4, w = d & 15, hi8 = w >> 3, q = (w & 7) >> 1, odd = w & 1;
+    const int lane = 4 * (tt & 7) + q, n = (tt >> 3) + 2 * hi8 + 4 * odd;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(tile + ((s >> 2) * 32 + lane) * 16 + (s & 3) * 4);
+    return (word >> (4 * n)) & 0xFu;
+}
+__device__ __forceinline__ uint32_t tile_v_code(const uint8_t* vcodes, int tt, int d) {
+    const int i = d >> 4, w = d & 15, dhi = w >> 3, t = w & 7;
+    const int lane = 4 * t + ((tt & 7) >> 1), n = dhi + 2 * (tt >> 3) + 4 * (tt & 1);
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(vcodes + ((i >> 2) * 32 + lane) * 16 + (i & 3) * 4);
+    return (word >> (4 * n)) & 0xFu;
+}
+
+// One CTA per (tile j, kv head g) of an mlx4g32 slot: every value x = scale * code + bias (fp32,
+// one rounding) becomes an fp16 pair hi = fp16(x), lo = fp16(x - hi), and the tile is written as
+// tile j of an fp16 slot of head dimension 2D whose first D columns are the hi parts and the
+// last D the lo parts. Attention over that slot with Q' = [Q | Q] gives the scores of the
+// dequantised K to ~22 bits, and P [V_hi | V_lo] gives O in two halves that sum to P V.
+__global__ void __launch_bounds__(128) mlx4_tiles_split_kernel(const uint8_t* __restrict__ in, int ntiles, int D,
+                                                               uint4* __restrict__ out) {
+    constexpr int MAXD = 256;   // of the output (2D)
+    __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
+    const int j = blockIdx.x, g = blockIdx.y;
+    const uint8_t* tile = in + ((size_t)g * ntiles + j) * tile_bytes(FMT_I4, D);
+    const int ng = D / 32;
+    for (int q = threadIdx.x; q < 2 * TILE_TOK * D; q += blockDim.x) {
+        const int x = q / (TILE_TOK * D), r = q - x * TILE_TOK * D;
+        const int tt = r / D, d = r - tt * D;
+        const uint32_t c = x ? tile_v_code(tile + 10 * D, tt, d) : tile_k_code(tile, tt, d);
+        const __half2 sb = *reinterpret_cast<const __half2*>(tile + (x ? 18 : 8) * D + (tt * ng + (d >> 5)) * 4);
+        const float v = fmaf(__low2float(sb), static_cast<float>(c), __high2float(sb));
+        const __half hi = __float2half_rn(v);
+        sm[x][tt][d] = hi;
+        sm[x][tt][D + d] = __float2half_rn(v - __half2float(hi));
+    }
+    __syncthreads();
+    const int64_t piece = 2 * (2 * D);
+    write_fp16_tile<MAXD>(sm, 2 * D, out + ((int64_t)g * 2 * ntiles + j) * piece,
+                          out + ((int64_t)g * 2 * ntiles + ntiles + j) * piece);
+}
+
+// ------------------------------------------------------------------ records -> [H_kv, N, D] (WARM)
+
+// One thread per code word: 8 values of one token and one kv head, x = scale * code + bias in
+// fp32 (one rounding of the exact value), stored at out[g][t][d0 .. d0 + 8) as fp32 or as the
+// fp16 rounding of the fp32 value. Records are only 4-byte aligned (a record is kv_dim * 5/8 bytes).
+template <typename OutT>
+__global__ void __launch_bounds__(256) dequant_records_kernel(const uint8_t* __restrict__ rec, int64_t N, int H_kv,
+                                                              int D, OutT* __restrict__ out) {
+    const int kv_dim = H_kv * D, wpr = kv_dim / 8, rb = kv_dim / 2 + kv_dim / 8;
+    const int64_t total = N * wpr;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = w / wpr;
+        const int j = static_cast<int>(w - t * wpr);
+        const uint8_t* r = rec + t * rb;
+        const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(r) + j);
+        const int grp = j >> 2;   // 4 words per group of 32
+        const float sc = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(r + kv_dim / 2) + grp)));
+        const float bi = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(r + kv_dim / 2 + kv_dim / 16) + grp)));
+        float x[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            w[k] = static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k][d])) |
-                   (static_cast<uint32_t>(__half_as_ushort(sm[1][8 * tc + 2 * k + 1][d])) << 16);
-        vout[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < 8; ++k) x[k] = fmaf(sc, static_cast<float>((word >> (4 * k)) & 0xFu), bi);
+        const int e0 = 8 * j, g = e0 / D, d0 = e0 - g * D;
+        OutT* o = out + ((int64_t)g * N + t) * D + d0;
+        if constexpr (sizeof(OutT) == 4) {
+            reinterpret_cast<float4*>(o)[0] = make_float4(x[0], x[1], x[2], x[3]);
+            reinterpret_cast<float4*>(o)[1] = make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+            uint4 u;
+            u.x = h2_as_u32(__floats2half2_rn(x[0], x[1]));
+            u.y = h2_as_u32(__floats2half2_rn(x[2], x[3]));
+            u.z = h2_as_u32(__floats2half2_rn(x[4], x[5]));
+            u.w = h2_as_u32(__floats2half2_rn(x[6], x[7]));
+            *reinterpret_cast<uint4*>(o) = u;
+        }
     }
 }
 
@@ -279,16 +421,46 @@ cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim
 }
 
 cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
-                                 void* out, cudaStream_t st, int sms) {
+                                 void* out, cudaStream_t st, int sms, int DS) {
     (void)sms;
-    if (D > 256 || D % 8 != 0) return cudaErrorInvalidValue;
+    if (DS == 0) DS = D;
+    if (DS > 256 || D % 8 != 0 || DS % 8 != 0 || DS < D) return cudaErrorInvalidValue;
     const dim3 grid(ntiles, H_kv);
     if (src_f16)
         relayout_fp16_kernel<__half><<<grid, 128, 0, st>>>(static_cast<const __half*>(K), static_cast<const __half*>(V),
-                                                           N, D, ntiles, static_cast<uint4*>(out));
+                                                           N, D, DS, ntiles, static_cast<uint4*>(out));
     else
         relayout_fp16_kernel<float><<<grid, 128, 0, st>>>(static_cast<const float*>(K), static_cast<const float*>(V),
-                                                          N, D, ntiles, static_cast<uint4*>(out));
+                                                          N, D, DS, ntiles, static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_fp16(const void* tiles, int ntiles, int D, const int* idx, const int* counts,
+                               const int8_t* head_map, int H_q, int kmax, size_t head_stride, void* out, cudaStream_t st) {
+    if (D > 256 || D % 16 != 0) return cudaErrorInvalidValue;
+    const dim3 grid((kmax + TILE_TOK - 1) / TILE_TOK, H_q);
+    gather_fp16_kernel<<<grid, 128, 0, st>>>(static_cast<const uint8_t*>(tiles), ntiles, D, idx, counts, head_map, kmax,
+                                             head_stride, static_cast<uint8_t*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mlx4_split(const void* tiles, int H_kv, int ntiles, int D, void* out, cudaStream_t st) {
+    if (2 * D > 256 || D % 32 != 0) return cudaErrorInvalidValue;
+    const dim3 grid(ntiles, H_kv);
+    mlx4_tiles_split_kernel<<<grid, 128, 0, st>>>(static_cast<const uint8_t*>(tiles), ntiles, D, static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_records(const void* rec, int64_t N, int H_kv, int D, int out_f16, void* out, cudaStream_t st,
+                                   int sms) {
+    const int64_t words = N * (H_kv * D / 8);
+    const int blocks = grid_for(words, 256, sms);
+    if (out_f16)
+        dequant_records_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D,
+                                                                static_cast<__half*>(out));
+    else
+        dequant_records_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D,
+                                                               static_cast<float*>(out));
     return cudaGetLastError();
 }
 

@@ -93,3 +93,70 @@ def test_prefill_custom_head_map(ctx, H_q, H_kv, hm):
     ctx.sync()
     assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"batched-Q head_map {hm.tolist()}")
     ctx.drop("pfhm")
+
+
+MLX_CASES = [
+    # H_q, H_kv, N, M, S_suf, D, causal
+    (4, 2, 300, 130, 40, 64, True),
+    (3, 1, 256, 128, 128, 128, True),
+    (6, 2, 1000, 96, 200, 128, False),
+    (2, 1, 1, 2, 3, 64, True),
+    (1, 1, 4133, 16, 8, 128, True),     # 32 key-range splits: the general merge folds hi and lo
+    (1, 1, 4133, 16, 8, 64, True),
+    (12, 1, 200, 50, 30, 64, True),
+]
+
+
+@pytest.mark.parametrize("H_q,H_kv,N,M,S,D,causal", MLX_CASES)
+def test_prefill_over_mlx4g32_matches_oracle(ctx, H_q, H_kv, N, M, S, D, causal):
+    """M > 1 over an mlx4g32 slot: the oracle attends to the dequantised codes of the same fp16
+    K/V (the library quantised them itself)."""
+    seed = N + M + S + D + H_q + 1
+    K, V = synth.gen_kv(seed, H_kv, N, D)
+    Q = synth.gen_q(seed, H_q, M, D, dtype=np.float16)
+    hm = synth.default_head_map(H_q, H_kv)
+    Ko, Vo = [orc.dequantize_mlx4g32(*orc.quantize_mlx4g32(X.reshape(H_kv * N, D))).reshape(H_kv, N, D) for X in (K, V)]
+    sid = f"pfm{seed}"
+    ctx.store(sid, 0, dev(K), dev(V), fmt=1)
+    if S:
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        O, L = ctx.query_fused(sid, 0, dev(Q), dev(Ks), dev(Vs), causal=causal)
+        O_ref, L_ref = orc.prefix_query(Q, Ko, Vo, hm, Ks, Vs, causal=causal)
+    else:
+        O, L = ctx.query(sid, 0, dev(Q))
+        O_ref, L_ref = orc.prefix_query(Q, Ko, Vo, hm)
+    ctx.sync()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"mlx4g32 {(H_q, H_kv, N, M, S, D, causal)}")
+    ctx.drop(sid)
+
+
+@pytest.mark.parametrize("kind", ["bias_scale", "q100", "monotone", "dominant_suffix"])
+def test_prefill_over_mlx4g32_stress(ctx, kind):
+    H_q, H_kv, N, M, S, D = 6, 2, 300, 64, 64, 128
+    Q, K, V, Ks, Vs = synth.gen_stress(kind, 17, H_q, H_kv, N, D, M, S, rise=0.9, q_dtype=np.float16)
+    hm = synth.default_head_map(H_q, H_kv)
+    Ko, Vo = [orc.dequantize_mlx4g32(*orc.quantize_mlx4g32(X.reshape(H_kv * N, D))).reshape(H_kv, N, D) for X in (K, V)]
+    ctx.store("pfms", 0, dev(K), dev(V), fmt=1)
+    O, L = ctx.query_fused("pfms", 0, dev(Q), dev(Ks), dev(Vs), causal=True)
+    O_ref, L_ref = orc.prefix_query(Q, Ko, Vo, hm, Ks, Vs, causal=True)
+    ctx.sync()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"mlx4g32 prefill {kind}")
+    ctx.drop("pfms")
+
+
+def test_prefill_over_mlx4g32_workload_layer(ctx):
+    """One layer of the batched-Q workload (H_q=24, H_kv=8, D=128, N=4096, M=512, causal S_suf=512)
+    with the prefix stored as mlx4g32."""
+    w = synth.WORKLOADS["batched_q_prefill"]
+    H_q, H_kv, N, D, M, S = w["H_q"], w["H_kv"], w["N"], w["D"], w["M"], w["S_suf"]
+    K, V = synth.gen_kv(1, H_kv, N, D)
+    Q = synth.gen_q(1, H_q, M, D, dtype=np.float16)
+    Ks, Vs = synth.gen_suffix(1, H_kv, S, D)
+    hm = synth.default_head_map(H_q, H_kv)
+    Ko, Vo = [orc.dequantize_mlx4g32(*orc.quantize_mlx4g32(X.reshape(H_kv * N, D))).reshape(H_kv, N, D) for X in (K, V)]
+    ctx.store("pfm3", 0, dev(K), dev(V), fmt=1)
+    O, L = ctx.query_fused("pfm3", 0, dev(Q), dev(Ks), dev(Vs), causal=True)
+    O_ref, L_ref = orc.prefix_query(Q, Ko, Vo, hm, Ks, Vs, causal=True)
+    ctx.sync()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, "mlx4g32 batched-Q layer")
+    ctx.drop("pfm3")

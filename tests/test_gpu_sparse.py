@@ -226,3 +226,15 @@ def test_sparse_custom_head_map(ctx, H_q, H_kv, hm):
     near = orc.topk_margin(scores, K_top) < TIE_EPS
     assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], f"sparse head_map {hm.tolist()}")
     ctx.drop("sphm")
+
+
+@pytest.mark.parametrize("H_kv,N,D,B", [(2, 1000, 64, 64), (1, 777, 256, 32), (4, 4096, 128, 16), (1, 5, 64, 16)])
+def test_block_means_direct(ctx, H_kv, N, D, B):
+    """The slot's block means against the oracle's, value by value (the last block partial)."""
+    K, V = synth.gen_kv(N + B, H_kv, N, D)
+    ctx.store("bm", 0, dev(K), dev(V))
+    got = host(ctx.get_block_means("bm", 0, B, H_kv, N, D))
+    want = orc.block_means(K, B)
+    assert got.shape == want.shape
+    assert np.abs(got - want).max() <= 1e-5
+    ctx.drop("bm")
