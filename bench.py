@@ -5,18 +5,22 @@ Headline line (one JSON object on stdout): the GQA decode workload over an mlx4g
 16 layers, H_q=32, H_kv=8, D=64, N=8192, M=1, fused dense suffix S_suf=16. One step is one
 decode step of the model's attention: all 16 layers' prefix + suffix attention, issued as one
 batched launch of the split-K decode kernel. Inputs are resident in HBM when the timed region
-starts; the step rotates over 4 distinct prefix sets (4 x 84 MB > L2) so that no step reads
-data left in L2 by the previous three. ``value`` is prefix KV record bytes per second.
+starts; the step rotates over 4 distinct prefix sets (4 x 84 MB, more than the L2 size the
+device reports) so that no step reads data left in L2 by the previous three. ``value`` is
+prefix KV record bytes per second.
 
-Extra keys report the other rows of the hot path (fp16 M=1, batched-Q prefill, sparse top-K,
-cartridge quantise + 64-session attend), each with its own roofline fraction.
+Extra keys report the other rows of the hot path (the same workload as 16 dependent per-layer
+calls, fp16 M=1, batched-Q prefill over fp16 and mlx4g32 prefixes, sparse top-K, cartridge
+quantise + dequantise + 64-session attend), each with its own roofline fraction.
 
-``--impl reference`` times the CPU oracle (test infrastructure) on the host cores on the same
-workload and prints the same line with ``"impl": "reference"``.
+``--impl reference`` times the CPU oracle (test infrastructure) on all the host cores on the
+same workload and prints the same line with ``"impl": "reference"``. ``--profile ROW`` runs each
+kernel of one row once, at a size meant for an Nsight Compute capture, and prints nothing else.
 """
 import os
 
-# The CPU oracle (reference arm / cpu_baseline) runs single-threaded so its core count is known.
+# Each CPU oracle process (reference arm / cpu_baseline) runs single-threaded, one per host core,
+# so the core count is known.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -229,8 +233,35 @@ def run_main(args, ctx, torch, pk):
             "kernel": "decode_kernel<mlx4g32, D=64> + merge_kernel", "algorithmic_bytes_per_launch": ALG_BYTES_STEP,
             "duration": "per-step time of back-to-back graph-replayed steps (decode + merge, PDL-chained)",
             "peak_source": f"{pk['src']} hbm_gbs"}
+    latency = run_latency(args, ctx, torch, sets, pk)
     e2e = run_e2e(args, ctx, torch, sets, arenas)
-    return ms_step, steps, clocks, roof, e2e
+    return ms_step, steps, clocks, roof, e2e, latency
+
+
+def run_latency(args, ctx, torch, sets, pk):
+    """The same step as a model's decode runs it: 16 dependent per-layer pck_query_fused calls
+    (each a decode + merge), one CUDA graph per prefix set, rotating over the 4 sets."""
+    H_q, H_kv, D = W["H_q"], W["H_kv"], W["D"]
+
+    def step(r):
+        for d in sets[r]:
+            ctx.query_fused(d["sid"], d["layer"], d["Q"].view(H_q, 1, D), d["K_suf"], d["V_suf"],
+                            O=d["O"].view(H_q, 1, D), LSE=d["LSE"].view(H_q, 1))
+
+    for r in range(ROTATE):
+        step(r)
+    torch.cuda.synchronize()
+    g = graph_of(torch, lambda: [step(r) for r in range(ROTATE)])
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    reps = 50
+    ms = time_replays(torch, g, reps) / ROTATE
+    ctx.sync()
+    gbs = ALG_BYTES_STEP / (ms * 1e-3) / 1e9
+    return {"workload": WORKLOAD + " as 16 dependent per-layer fused calls (latency mode)",
+            "us_per_step": round(ms * 1e3, 2), "us_per_layer": round(ms * 1e3 / W["layers"], 3),
+            "record_gbs": round(KV_BYTES_STEP / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(gbs / pk["hbm"], 4),
+            "launches_per_step": 2 * W["layers"], "steps_timed": reps * ROTATE}
 
 
 def run_e2e(args, ctx, torch, sets, arenas):
@@ -312,12 +343,18 @@ def row_fp16_m1(ctx, torch, pk, reps=20):
             "kv_gbs_64_sessions_one_launch": round(gbs, 1), "frac_hbm_64_sessions": round(gbs / pk["hbm"], 4)}
 
 
-def row_sparse(ctx, torch, pk, reps=10):
+def row_sparse(ctx, torch, pk, reps=10, l2=None):
     """Sparse top-K (N=65,536, D=256, H_q=8, H_kv=2, B=64, K_top=8, S_suf=32) with the seeded
-    needles; 48 distinct sessions (their touched bytes exceed L2), one query call per session back
-    to back. Bytes counted: block means + selected K/V + suffix + Q/O (not the dense prefix)."""
+    needles. Single-query mode: one query call per session back to back over 48 sessions.
+    Throughput mode: 48 sessions per pck_query_sparse_batch call, rotating over enough distinct
+    48-session sets that the bytes one pass touches exceed 4x the L2 size. Bytes counted: block
+    means + selected K/V + suffix + Q/O (not the dense prefix)."""
     from prefix_cached_kv_gb300 import synth
     H_q, H_kv, N, D, B, Kt, S, R = 8, 2, 65536, 256, 64, 8, 32, 48
+    nbk = N // B
+    alg = H_kv * nbk * D * 4 + 8 * B * D * 2 * 2 * H_kv + 2 * H_kv * S * D * 2 + H_q * D * 4 * 2 + H_q * 4
+    l2 = l2 or (126 << 20)
+    n_sets = max(1, -(-4 * l2 // (R * alg)))         # ceil(4 L2 / bytes of one set)
     hm = synth.default_head_map(H_q, H_kv)
     K, V = synth.gen_kv(0, H_kv, N, D)
     Q = synth.gen_q(0, H_q, 1, D)[:, 0]
@@ -325,46 +362,54 @@ def row_sparse(ctx, torch, pk, reps=10):
     K = synth.plant_needles(K, Q, hm, needles, B)
     dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     Kd, Vd = dv(K), dv(V)
-    for r in range(R):
+    n_sess = n_sets * R
+    for r in range(n_sess):
         ctx.store(f"sparse{r}", 0, Kd, Vd)
         ctx.build_block_means(f"sparse{r}", 0, B)
     del Kd, Vd
+    # every session reads its own copy of Q (the needles were planted toward this Q) and its own suffix
     Qd = dv(Q)
-    Ks, Vs = [dv(a) for a in synth.gen_suffix(0, H_kv, S, D)]
-    Os = [torch.empty((H_q, D), device="cuda") for _ in range(R)]
-    Ls = [torch.empty((H_q,), device="cuda") for _ in range(R)]
-    idx = [torch.empty((H_q, Kt), dtype=torch.int32, device="cuda") for _ in range(R)]
-    calls = lambda: [ctx.query_sparse_auto(f"sparse{r}", 0, Qd, B, Kt, H_kv, K_suf=Ks, V_suf=Vs, O=Os[r], LSE=Ls[r],
-                                           idx=idx[r]) for r in range(R)]
+    Qs = [Qd.clone() for _ in range(n_sess)]
+    Kss = [torch.randn((H_kv, S, D), device="cuda").half() for _ in range(n_sess)]
+    Vss = [torch.randn((H_kv, S, D), device="cuda").half() for _ in range(n_sess)]
+    Os = [torch.empty((H_q, D), device="cuda") for _ in range(n_sess)]
+    Ls = [torch.empty((H_q,), device="cuda") for _ in range(n_sess)]
+    idx = [torch.empty((H_q, Kt), dtype=torch.int32, device="cuda") for _ in range(n_sess)]
+    calls = lambda: [ctx.query_sparse_auto(f"sparse{r}", 0, Qs[r], B, Kt, H_kv, K_suf=Kss[r], V_suf=Vss[r], O=Os[r],
+                                           LSE=Ls[r], idx=idx[r]) for r in range(R)]
     calls()
     g = graph_of(torch, calls)
     for _ in range(3):
         g.replay()
     ms = time_replays(torch, g, reps) / R
     ctx.sync()
-    ok = all(bool((t.cpu().numpy() == needles[None]).all()) for t in idx)
-    # throughput mode: the R sessions in one pck_query_sparse_batch call (one selector launch, one
-    # gather decode + merge), graph-replayed
+    ok = all(bool((t.cpu().numpy() == needles[None]).all()) for t in idx[:R])
+    del g
     for t in idx:
         t.fill_(-1)
-    descs = [dict(sid=f"sparse{r}", layer=0, Q=Qd, O=Os[r], LSE=Ls[r], K_suf=Ks, V_suf=Vs, idx=idx[r]) for r in range(R)]
-    bcall = ctx.sparse_batch_caller(descs, H_q, H_kv, D, B, Kt, S_suf=S)
-    bcall()
-    gb = graph_of(torch, bcall)
+    bcalls = []
+    for k in range(n_sets):
+        descs = [dict(sid=f"sparse{r}", layer=0, Q=Qs[r], O=Os[r], LSE=Ls[r], K_suf=Kss[r], V_suf=Vss[r], idx=idx[r])
+                 for r in range(k * R, (k + 1) * R)]
+        bcalls.append(ctx.sparse_batch_caller(descs, H_q, H_kv, D, B, Kt, S_suf=S))
+    for c in bcalls:
+        c()
+    gb = graph_of(torch, lambda: [c() for c in bcalls])
     for _ in range(3):
         gb.replay()
-    ms_b = time_replays(torch, gb, reps) / R
+    ms_b = time_replays(torch, gb, reps) / n_sess
     ctx.sync()
     ok_b = all(bool((t.cpu().numpy() == needles[None]).all()) for t in idx)
-    for r in range(R):
+    del gb
+    for r in range(n_sess):
         ctx.drop(f"sparse{r}")
-    nbk = N // B
-    alg = H_kv * nbk * D * 4 + 8 * B * D * 2 * 2 * H_kv + 2 * H_kv * S * D * 2 + H_q * D * 4 * 2 + H_q * 4
     gbs = lambda t_ms: alg / (t_ms * 1e-3) / 1e9
     return {"workload": "sparse_topk_64k", "us_per_call_back_to_back": round(ms * 1e3, 2),
             "alg_bytes_per_call": alg, "gbs": round(gbs(ms), 1), "frac_hbm": round(gbs(ms) / pk["hbm"], 4),
             "needles_selected": ok, "launches_per_call": 4,
-            "batched_sessions_per_call": R, "batched_us_per_session": round(ms_b * 1e3, 3),
+            "batched_sessions_per_call": R, "batched_sets_rotated": n_sets,
+            "batched_touched_mb_per_pass": round(n_sess * alg / 1e6, 1), "l2_mb": round(l2 / 1e6, 1),
+            "batched_us_per_session": round(ms_b * 1e3, 3),
             "batched_gbs": round(gbs(ms_b), 1), "batched_frac_hbm": round(gbs(ms_b) / pk["hbm"], 4),
             "batched_needles_selected": ok_b}
 
@@ -392,6 +437,18 @@ def row_cartridge(ctx, torch, pk, reps=10):
     qms = statistics.median(tm.ms())
     qbytes = rows * kv * 2 + rows * (kv // 2 + kv // 8)
     del X
+    # WARM / FETCH RANGE form of every stored record: [8, rows, 128] fp16 (dequantise + transpose)
+    Y = torch.empty((8, rows, kv // 8), dtype=torch.float16, device="cuda")
+    binding.dequantize_mlx4g32(rec, rows, 8, kv // 8, out=Y)
+    torch.cuda.synchronize()
+    tm = Timer(reps)
+    for k in range(reps):
+        tm.s[k].record()
+        binding.dequantize_mlx4g32(rec, rows, 8, kv // 8, out=Y)
+        tm.e[k].record()
+    wms = statistics.median(tm.ms())
+    wbytes = rows * (kv // 2 + kv // 8) + rows * kv * 2
+    del Y
     rb = kv // 2 + kv // 8
     descs = []
     for s in range(S):
@@ -417,21 +474,26 @@ def row_cartridge(ctx, torch, pk, reps=10):
             "quantize_ms": round(qms, 3), "quantize_gbs": round(qbytes / (qms * 1e-3) / 1e9, 1),
             "quantize_frac_hbm": round(qbytes / (qms * 1e-3) / 1e9 / pk["hbm"], 4),
             "quantize_tokens_per_s": round(N * L / (qms * 1e-3), 0),
+            "warm_dequantize_ms": round(wms, 3), "warm_dequantize_gbs": round(wbytes / (wms * 1e-3) / 1e9, 1),
+            "warm_dequantize_frac_hbm": round(wbytes / (wms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "warm_bytes": wbytes,
             "attend_us": round(ams * 1e3, 2), "attend_kv_gbs": round(abytes / (ams * 1e-3) / 1e9, 1),
             "attend_frac_hbm": round(abytes / (ams * 1e-3) / 1e9 / pk["hbm"], 4)}
 
 
-def row_prefill(ctx, torch, pk, reps=10):
-    """Batched-Q prefill: 28 layers, H_q=24, H_kv=8, D=128, N=4096 fp16 prefix, M=512 fp16 queries,
-    causal S_suf=512 suffix; algorithmic FLOPs count only unmasked scores."""
+def row_prefill(ctx, torch, pk, reps=10, fmt=0):
+    """Batched-Q prefill: 28 layers, H_q=24, H_kv=8, D=128, N=4096 prefix (fp16, or mlx4g32 with
+    fmt=1), M=512 fp16 queries, causal S_suf=512 suffix; algorithmic FLOPs count only unmasked
+    scores at head dimension D (the mlx4g32 form's hi/lo pairs double the tensor-core work)."""
     from prefix_cached_kv_gb300 import binding
     H_q, H_kv, D, N, M, S, L = 24, 8, 128, 4096, 512, 512, 28
     flops_layer = 4 * H_q * M * N * D + 4 * H_q * D * (M * (M + 1) // 2)
+    name = "batched_q_prefill" + ("" if fmt == 0 else " over an mlx4g32 prefix")
     try:
         for layer in range(L):
             K = torch.randn((H_kv, N, D), device="cuda").half()
             V = torch.randn((H_kv, N, D), device="cuda").half()
-            ctx.store("prefill", layer, K, V)
+            ctx.store("prefill", layer, K, V, fmt=fmt)
         Qs = [torch.randn((H_q, M, D), device="cuda").half() for _ in range(L)]
         Ks = [torch.randn((H_kv, S, D), device="cuda").half() for _ in range(L)]
         Vs = [torch.randn((H_kv, S, D), device="cuda").half() for _ in range(L)]
@@ -441,7 +503,7 @@ def row_prefill(ctx, torch, pk, reps=10):
     except binding.PckError as e:
         for layer in range(L):
             ctx.drop("prefill", layer)
-        return {"workload": "batched_q_prefill", "unavailable": str(e)}
+        return {"workload": name, "unavailable": str(e)}
     # one graph replay = the L layer calls back to back (staging + kernel + merge each), so the
     # GPU time is measured without the host's per-call launch cost in between
     g = graph_of(torch, lambda: [ctx.query_fused("prefill", l, Qs[l], Ks[l], Vs[l], O=O, LSE=LSE) for l in range(L)])
@@ -454,25 +516,84 @@ def row_prefill(ctx, torch, pk, reps=10):
     for layer in range(L):
         ctx.drop("prefill", layer)
     tf = flops_layer / (ms * 1e-3) / 1e12
-    return {"workload": "batched_q_prefill", "ms_per_layer": round(ms, 4), "tflops": round(tf, 1),
+    return {"workload": name, "ms_per_layer": round(ms, 4), "tflops": round(tf, 1),
             "frac_tensor_bf16_peak": round(tf / pk["bf16"], 4), "gflop_per_layer": round(flops_layer / 1e9, 3)}
+
+
+# ------------------------------------------------------------------ single launches for Nsight Compute
+
+def profile_row(row, ctx, torch):
+    """Run each kernel of one row twice (the first launch sets kernel attributes; capture the
+    second with -s / -c), at sizes that keep a capture to a few GB on the device: fp16 = the
+    64-session fp16 M=1 batch; sparse = a 16-session pck_query_sparse_batch (scoring, selection,
+    gather decode, merge); quant = one cartridge layer's K and V (354 MB in); warm = the same
+    layer's records dequantised to fp16; prefill = one batched-Q layer (fp16 prefix);
+    prefill_mlx = the same over an mlx4g32 prefix."""
+    from prefix_cached_kv_gb300 import binding, synth
+    if row == "fp16":
+        H, N, D, R = 8, 2048, 128, 64
+        descs = []
+        for r in range(R):
+            K, V = synth.torch_gen_kv_device(7 + r, H, N, D, "cuda", col_scale=True)
+            ctx.store(f"pf{r}", 0, K, V)
+            descs.append(dict(sid=f"pf{r}", layer=0, Q=torch.randn((H, D), device="cuda"),
+                              O=torch.empty((H, D), device="cuda"), LSE=torch.empty((H,), device="cuda")))
+        fn = lambda: ctx.query_batch(descs, H, H, D)
+    elif row == "sparse":
+        H_q, H_kv, N, D, B, Kt, S, R = 8, 2, 65536, 256, 64, 8, 32, 16
+        hm = synth.default_head_map(H_q, H_kv)
+        K, V = synth.gen_kv(0, H_kv, N, D)
+        Q = synth.gen_q(0, H_q, 1, D)[:, 0]
+        K = synth.plant_needles(K, Q, hm, synth.needle_blocks(0, N // B, Kt), B)
+        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        Kd, Vd, Qd = dv(K), dv(V), dv(Q)
+        Ks, Vs = [dv(a) for a in synth.gen_suffix(0, H_kv, S, D)]
+        descs = []
+        for r in range(R):
+            ctx.store(f"ps{r}", 0, Kd, Vd)
+            ctx.build_block_means(f"ps{r}", 0, B)
+            descs.append(dict(sid=f"ps{r}", layer=0, Q=Qd, O=torch.empty((H_q, D), device="cuda"),
+                              LSE=torch.empty((H_q,), device="cuda"), K_suf=Ks, V_suf=Vs,
+                              idx=torch.empty((H_q, Kt), dtype=torch.int32, device="cuda")))
+        fn = ctx.sparse_batch_caller(descs, H_q, H_kv, D, B, Kt, S_suf=S)
+    elif row in ("quant", "warm"):
+        N, kv = 86580, 1024
+        X = synth.torch_gen_rows_device(0, 2 * N, kv, "cuda", stream=1)
+        rec = binding.quantize_mlx4g32(X)
+        if row == "quant":
+            fn = lambda: binding.quantize_mlx4g32(X, rec)
+        else:
+            Y = torch.empty((8, 2 * N, 128), dtype=torch.float16, device="cuda")
+            fn = lambda: binding.dequantize_mlx4g32(rec, 2 * N, 8, 128, out=Y)
+    elif row in ("prefill", "prefill_mlx"):
+        H_q, H_kv, D, N, M, S = 24, 8, 128, 4096, 512, 512
+        ctx.store("pp", 0, torch.randn((H_kv, N, D), device="cuda").half(),
+                  torch.randn((H_kv, N, D), device="cuda").half(), fmt=0 if row == "prefill" else 1)
+        Q = torch.randn((H_q, M, D), device="cuda").half()
+        Ks = torch.randn((H_kv, S, D), device="cuda").half()
+        Vs = torch.randn((H_kv, S, D), device="cuda").half()
+        fn = lambda: ctx.query_fused("pp", 0, Q, Ks, Vs)
+    else:
+        raise SystemExit(f"unknown profile row {row}")
+    torch.cuda.synchronize()
+    for _ in range(2):
+        fn()
+        torch.cuda.synchronize()
+    ctx.sync()
 
 
 # ------------------------------------------------------------------ CPU oracle (reference arm, cpu_baseline)
 
-def oracle_step_inputs(n_layers, seed=0):
-    """Host inputs of n_layers of the headline workload, records built by the oracle's quantiser
+def oracle_layer_inputs(layer, seed=0):
+    """Host inputs of one layer of the headline workload, records built by the oracle's quantiser
     (store side, not timed)."""
     from oracle import pck_oracle as orc
     from prefix_cached_kv_gb300 import synth
     H_q, H_kv, N, D, S = W["H_q"], W["H_kv"], W["N"], W["D"], W["S_suf"]
-    layers = []
-    for layer in range(n_layers):
-        K, V = synth.gen_kv(seed, H_kv, N, D, layer=layer)
-        tok = lambda X: X.transpose(1, 0, 2).reshape(N, H_kv * D)
-        layers.append(dict(Krec=orc.quantize_records(tok(K)), Vrec=orc.quantize_records(tok(V)),
-                           Q=synth.gen_q(seed, H_q, 1, D, layer=layer), suf=synth.gen_suffix(seed, H_kv, S, D, layer=layer)))
-    return layers
+    K, V = synth.gen_kv(seed, H_kv, N, D, layer=layer)
+    tok = lambda X: X.transpose(1, 0, 2).reshape(N, H_kv * D)
+    return dict(Krec=orc.quantize_records(tok(K)), Vrec=orc.quantize_records(tok(V)),
+                Q=synth.gen_q(seed, H_q, 1, D, layer=layer), suf=synth.gen_suffix(seed, H_kv, S, D, layer=layer))
 
 
 def oracle_layer(inp):
@@ -485,47 +606,115 @@ def oracle_layer(inp):
     return orc.prefix_query(inp["Q"], Ko, Vo, None, Ks, Vs)
 
 
-def time_oracle(budget_s=12.0, n_layers=2):
-    layers = oracle_step_inputs(n_layers)
-    oracle_layer(layers[0])
-    t0 = time.perf_counter()
-    done = 0
+def _oracle_worker(wid, nw, inq, outq):
+    """One host core: builds the layers l with l % nw == wid once, then runs them once per step."""
+    mine = [l for l in range(W["layers"]) if l % nw == wid]
+    inputs = [oracle_layer_inputs(l) for l in mine]
+    outq.put(("ready", wid, 0.0))
     while True:
-        oracle_layer(layers[done % n_layers])
-        done += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    per_layer_s = dt / done
-    kv_layer = 2 * W["N"] * REC_BYTES
-    return {"value": round(kv_layer / per_layer_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} layer queries of {WORKLOAD} (dequantise records + prefix/suffix attention, "
-                      f"fp64 numpy, 1 thread), {dt:.1f} s; a 16-layer step is 16 such layer queries",
-            "s_per_layer": round(per_layer_s, 4)}
+        n = inq.get()
+        if n is None:
+            return
+        t0 = time.perf_counter()
+        for _ in range(n):
+            for inp in inputs:
+                oracle_layer(inp)
+        outq.put(("done", wid, time.perf_counter() - t0))
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+        for key in ("model name", "CPU part"):
+            for ln in info:
+                if ln.lower().startswith(key.lower()):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class OraclePool:
+    """The oracle's 16-layer step split over the host cores: one single-threaded process per core
+    (at most one per layer), started with `spawn` before any GPU work. run(n) times n steps on
+    all workers at once (wall clock from the start signal to the last worker's finish)."""
+
+    def __init__(self):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.nw = max(1, min(os.cpu_count() or 1, W["layers"]))
+        self.outq = ctx.Queue()
+        self.inqs = [ctx.Queue() for _ in range(self.nw)]
+        self.procs = [ctx.Process(target=_oracle_worker, args=(w, self.nw, self.inqs[w], self.outq), daemon=True)
+                      for w in range(self.nw)]
+        for p in self.procs:
+            p.start()
+        for _ in range(self.nw):
+            self.outq.get()
+
+    def run(self, n):
+        t0 = time.perf_counter()
+        for q in self.inqs:
+            q.put(n)
+        for _ in range(self.nw):
+            self.outq.get()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for q in self.inqs:
+            q.put(None)
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def time_oracle(budget_s=12.0):
+    """cpu_baseline: the oracle's 16-layer step on all host cores for about budget_s seconds."""
+    pool = OraclePool()
+    try:
+        t1 = pool.run(1)                                   # warm-up step, and its duration
+        n = max(1, int(budget_s / max(t1, 1e-3)))
+        dt = pool.run(n)
+    finally:
+        pool.close()
+    step_s = dt / n
+    kv_step = W["layers"] * 2 * W["N"] * REC_BYTES
+    return {"value": round(kv_step / step_s / 1e9, 4), "unit": "GB/s", "cores": pool.nw, "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cores": os.cpu_count(),
+            "sample": f"{n} full 16-layer steps of {WORKLOAD} (dequantise records + prefix/suffix attention, fp64 "
+                      f"numpy), layers split over {pool.nw} single-threaded processes, {dt:.1f} s",
+            "ms_per_step": round(step_s * 1e3, 2)}
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step = one layer query of the workload (a bounded
-    sample of the 16-layer step), value scaled to the same unit."""
+    """The CPU oracle as the reference arm: each step is the full 16-layer step of the workload,
+    its layers split over the host cores."""
     if rank() != 0:
         return
-    layers = oracle_step_inputs(2)
-    for k in range(args.warmup):
-        oracle_layer(layers[k % 2])
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        oracle_layer(layers[k % 2])
-    dt = time.perf_counter() - t0
-    kv_layer = 2 * W["N"] * REC_BYTES
-    val = kv_layer * args.steps / dt / 1e9
+    pool = OraclePool()
+    try:
+        if args.warmup:
+            pool.run(args.warmup)
+        dt = pool.run(args.steps)
+    finally:
+        pool.close()
+    kv_step = W["layers"] * 2 * W["N"] * REC_BYTES
+    val = kv_step * args.steps / dt / 1e9
+    sample = (f"{args.steps} timed full 16-layer steps (+{args.warmup} warm-up), layers over {pool.nw} "
+              f"single-threaded processes, fp64")
     line = {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-            "ms_per_16_layer_step_projected": round(dt / args.steps * 1e3 * W["layers"], 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": WORKLOAD, **W, "fmt": "mlx4g32", "step": "one layer query per step (sample)"},
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} timed layer queries (+{args.warmup} warm-up), 1 thread fp64"},
+            "config": {"workload": WORKLOAD, **W, "fmt": "mlx4g32", "step": "the full 16-layer step"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": pool.nw, "kind": "oracle",
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -544,34 +733,50 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="all | comma list of main,fp16,sparse,prefill,cartridge (main = the headline line)")
+                    help="all | comma list of main,fp16,sparse,prefill,prefill_mlx,cartridge (main = the headline line)")
+    ap.add_argument("--profile", default=None,
+                    help="fp16 | sparse | quant | warm | prefill | prefill_mlx: one capture-sized run of that row")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
         return
-    cpu = time_oracle() if rank() == 0 else None   # before any GPU work
+    if args.profile:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        from prefix_cached_kv_gb300 import binding
+        ctx = binding.Context(torch.cuda.current_device())
+        profile_row(args.profile, ctx, torch)
+        ctx.close()
+        return
+    want = {"main", "fp16", "sparse", "prefill", "prefill_mlx", "cartridge"} if args.rows == "all" \
+        else set(args.rows.split(","))
+    cpu = time_oracle() if rank() == 0 and "main" in want else None   # before any GPU work
     import torch
     dist_init()
     import __graft_entry__
     __graft_entry__.build()
     from prefix_cached_kv_gb300 import binding
     pk = peaks()
+    l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0)) or None
     ctx = binding.Context(torch.cuda.current_device())
-    want = {"main", "fp16", "sparse", "prefill", "cartridge"} if args.rows == "all" else set(args.rows.split(","))
-    ms_step = steps = clocks = roof = e2e = None
+    ms_step = steps = clocks = roof = e2e = latency = None
+    rows = {}
     if "main" in want:
-        ms_step, steps, clocks, roof, e2e = run_main(args, ctx, torch, pk)
+        ms_step, steps, clocks, roof, e2e, latency = run_main(args, ctx, torch, pk)
+        rows["A3_headline_latency_mode"] = latency
         for r in range(ROTATE):
             ctx.drop(f"bench{r}")
-    rows = {}
     if "fp16" in want:
         rows["A0_A2_fp16_m1"] = row_fp16_m1(ctx, torch, pk)
     if "sparse" in want:
-        rows["A6_A7_sparse"] = row_sparse(ctx, torch, pk)
+        rows["A6_A7_sparse"] = row_sparse(ctx, torch, pk, l2=l2)
     if "prefill" in want:
         rows["A4_A5_batched_q"] = row_prefill(ctx, torch, pk)
+    if "prefill_mlx" in want:
+        rows["N3_batched_q_mlx4g32"] = row_prefill(ctx, torch, pk, fmt=1)
     if "cartridge" in want:
-        rows["A1_A3_cartridge"] = row_cartridge(ctx, torch, pk)
+        rows["A1_A3_N2_cartridge"] = row_cartridge(ctx, torch, pk)
     ctx.close()
     if rank() != 0:
         return
@@ -580,12 +785,14 @@ def main():
         return
     ws = world()
     value = job_throughput(KV_BYTES_STEP, ms_step, ws) / 1e9
+    l2_txt = f"{l2 / 2**20:.0f} MiB L2 (device-reported)" if l2 else "L2 size not reported"
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u4/f16 in, f32 accumulate", "data": "synthetic",
             "config": {"workload": WORKLOAD, **W, "fmt": "mlx4g32",
                        "launch": "16 layers in one batched launch per step, CUDA-graph replayed",
-                       "l2": f"rotate {ROTATE} distinct 84 MB prefix sets (336 MB > L2)",
+                       "l2": f"rotate {ROTATE} distinct {KV_BYTES_STEP / 1e6:.0f} MB prefix sets "
+                             f"({ROTATE * KV_BYTES_STEP / 1e6:.0f} MB vs {l2_txt})",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": 2 * steps, "rows": rows}

@@ -43,6 +43,10 @@ constexpr int PF_THREADS = 192;       // 4 softmax warps + MMA warp + producer w
 constexpr int PF_MMA_WARP = 4, PF_LOAD_WARP = 5;
 constexpr int PF_ST = 2;              // K and V stages
 constexpr float PF_LN2 = 0.69314718055994530942f;
+// Launch-shape model of the key-range split, in units of one 64-key block of one CTA: a CTA's
+// set-up and epilogue, and the merge kernel that a split adds.
+constexpr double PF_CTA_COST = 2.0;
+constexpr double PF_MERGE_COST = 4.0;
 
 // Shared memory of one CTA: the Q tile and 2-stage K and V rings of 64-key blocks (two CTAs fit
 // on an SM up to D = 128). Tensor memory: two S buffers (64 fp32 columns each; P of a block is
@@ -826,15 +830,25 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
     P.suf_ntiles = suf_ntiles;
     P.partials = partials;
     if (off == 0) return cudaSuccess;
-    // key-range splits: enough CTAs to fill the SMs (two per SM up to D = 128, one at D = 256),
-    // never more splits than prefix blocks
+    // Key-range splits from a wave-cost model: with `slots` CTAs resident at once (two per SM up to
+    // D = 128, one at D = 256), a launch of off * ns CTAs takes ceil(off * ns / slots) waves of
+    // (nb / ns + PF_CTA_COST) block times, plus PF_MERGE_COST for the merge when ns > 1; never more
+    // splits than prefix blocks, nor than the partials workspace holds.
     const int nbp = (a.N + PF_BLOCK - 1) / PF_BLOCK;
+    const int nb = nbp + (a.S_suf + PF_BLOCK - 1) / PF_BLOCK;
     const int per_sm = D == 256 ? PCfg<256>::CTAS_PER_SM : PCfg<128>::CTAS_PER_SM;
-    int ns = (per_sm * sms) / off;
-    if (ns < 1) ns = 1;
-    if (ns > nbp) ns = nbp;
-    if (ns > 32) ns = 32;
-    while (ns > 1 && static_cast<size_t>(off) * ns * PF_ROWS * partial_stride(D) * sizeof(float) > partial_bytes) --ns;
+    const int slots = per_sm * sms;
+    int ns = 1;
+    double best = 1e30;
+    for (int k = 1; k <= 32 && k <= nbp; ++k) {
+        if (static_cast<size_t>(off) * k * PF_ROWS * partial_stride(D) * sizeof(float) > partial_bytes) break;
+        const double waves = static_cast<double>((static_cast<int64_t>(off) * k + slots - 1) / slots);
+        const double cost = waves * (static_cast<double>(nb) / k + PF_CTA_COST) + (k > 1 ? PF_MERGE_COST : 0.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            ns = k;
+        }
+    }
     P.n_split = ns;
     if (D == 64) return launch_prefill_t<64>(P, st);
     if (D == 128) return launch_prefill_t<128>(P, st);

@@ -39,3 +39,38 @@ def test_every_summary_names_its_command():
         text = open(os.path.join(PROFILES, f)).read()
         assert "ncu " in text and "--clock-control none" in text, f
         assert "python bench.py" in text, f
+
+
+L2_BYTES = 135_475_200   # the L2 size the GB300 reports (torch device properties), as in bench.py's line
+
+
+def _fields(name):
+    out = {}
+    for line in open(os.path.join(PROFILES, name)):
+        line = line.lstrip("# ").strip()
+        for key in ("algorithmic_read_bytes", "algorithmic_write_bytes", "dram_read_bytes", "dram_write_bytes",
+                    "traffic_bytes_per_launch"):
+            if line.startswith(key + ":"):
+                v = line.split(":", 1)[1].split()
+                if v and v[0].replace(".", "", 1).isdigit():
+                    out[key] = float(v[0])
+    return out
+
+
+def test_captured_dram_bytes_match_algorithmic_bytes():
+    """Every summary that records a DRAM capture: reads within 5 % of the algorithmic reads;
+    writes within 5 % above the algorithmic writes and at most one L2 below them (output still
+    dirty in L2 when the kernel ends is written back after it); traffic = reads + writes."""
+    seen = 0
+    for f in sorted(os.listdir(PROFILES)):
+        d = _fields(f)
+        if "dram_read_bytes" not in d:
+            continue
+        seen += 1
+        r, ar = d["dram_read_bytes"], d["algorithmic_read_bytes"]
+        assert 0.95 * ar <= r <= 1.05 * ar, (f, r, ar)
+        if "algorithmic_write_bytes" in d and d["algorithmic_write_bytes"] > 1e6:
+            w, aw = d["dram_write_bytes"], d["algorithmic_write_bytes"]
+            assert aw - L2_BYTES <= w <= 1.05 * aw + 8e6, (f, w, aw)
+        assert d["traffic_bytes_per_launch"] == d["dram_read_bytes"] + d["dram_write_bytes"], f
+    assert seen >= 4
