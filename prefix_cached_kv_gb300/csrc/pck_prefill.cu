@@ -354,9 +354,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             const int h = wg.qh[r / M], i = r % M;
             const int qc = P.a.q_dup ? D / 16 : D / 8;   // 16-byte chunks of a source row
             const uint4* src = reinterpret_cast<const uint4*>(P.a.Q + ((size_t)h * M + i) * (qc * 8));
-#pragma unroll 4
+            // every 16-byte piece of the row in flight at once, straight into shared memory
+            const uint32_t qs_s = smem_u32(qs);
+#pragma unroll 8
             for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4*>(qs + (R * (D / 8) + c) * 128 + rr * 16) = __ldg(src + (c < qc ? c : c - qc));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(qs_s + (R * (D / 8) + c) * 128 + rr * 16),
+                             "l"(src + (c < qc ? c : c - qc)) : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
         } else {
 #pragma unroll 4
             for (int c = 0; c < D / 8; ++c)

@@ -250,8 +250,11 @@ __global__ void __launch_bounds__(128) mlx4_tiles_split_kernel(const uint8_t* __
                                                                uint4* __restrict__ out) {
     constexpr int MAXD = 256;   // of the output (2D)
     __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
+    __shared__ __align__(16) uint8_t tile[20 * (MAXD / 2)];   // the input tile (20 * D bytes)
     const int j = blockIdx.x, g = blockIdx.y;
-    const uint8_t* tile = in + ((size_t)g * ntiles + j) * tile_bytes(FMT_I4, D);
+    const uint4* src = reinterpret_cast<const uint4*>(in + ((size_t)g * ntiles + j) * tile_bytes(FMT_I4, D));
+    for (int q = threadIdx.x; q < 20 * D / 16; q += blockDim.x) reinterpret_cast<uint4*>(tile)[q] = __ldg(src + q);
+    __syncthreads();
     const int ng = D / 32;
     for (int q = threadIdx.x; q < 2 * TILE_TOK * D; q += blockDim.x) {
         const int x = q / (TILE_TOK * D), r = q - x * TILE_TOK * D;

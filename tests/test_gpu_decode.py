@@ -178,3 +178,27 @@ def test_cartridge_attend_sampled(ctx):
         assert_close_o_lse(host(descs[s]["O"]), host(descs[s]["LSE"]), O_ref[:, 0], L_ref[:, 0], f"session {s}")
     for s in range(S):
         ctx.drop(f"cart{s}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_batch_suffix_computed_by_prefix_workers(ctx, fmt):
+    """A batch large enough that every resident warp streams prefix tiles: the suffix pieces (three
+    per item here, S_suf = 40) are computed by the prefix workers whose ranges hold the items'
+    first tiles. Descriptors of different prefix lengths, GQA 4, against the oracle."""
+    H_q, H_kv, D, S = 32, 8, 64, 40
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs = [], []
+    for r, N in enumerate((6000, 8192, 4099, 7001, 5555, 8192, 6500, 3001)):
+        K, V = synth.gen_kv(70 + r, H_kv, N, D)
+        Q = synth.gen_q(70 + r, H_q, 1, D)
+        Ks, Vs = synth.gen_suffix(70 + r, H_kv, S, D)
+        ctx.store(f"fold{r}", 0, dev(K), dev(V), fmt=fmt)
+        Ko, Vo = _oracle_kv(K, V, fmt)
+        refs.append(orc.prefix_query(Q, Ko, Vo, hm, Ks, Vs))
+        descs.append(dict(sid=f"fold{r}", layer=0, Q=dev(Q[:, 0]), O=torch.empty((H_q, D), device="cuda"),
+                          LSE=torch.empty((H_q,), device="cuda"), K_suf=dev(Ks), V_suf=dev(Vs)))
+    ctx.query_batch(descs, H_q, H_kv, D, S_suf=S)
+    ctx.sync()
+    for r, (O_ref, L_ref) in enumerate(refs):
+        assert_close_o_lse(host(descs[r]["O"]), host(descs[r]["LSE"]), O_ref[:, 0], L_ref[:, 0], f"fold {fmt} {r}")
+        ctx.drop(f"fold{r}")
