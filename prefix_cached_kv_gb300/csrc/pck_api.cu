@@ -265,7 +265,7 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
     const int64_t max_slots =
         static_cast<int64_t>(WS_PARTIAL_BYTES / (static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float)));
     DecodePlan plan;
-    if (!plan_decode(total, vmax, n_items, S_suf, sparse != 0, c->sms, li.ctas_per_sm, max_slots, &plan))
+    if (!plan_decode(&p, total, vmax, n_items, S_suf, c->sms, li.ctas_per_sm, max_slots, &plan))
         return fail(c, PCK_EUNSUPPORTED, "split-K workspace too small for %d items", n_items);
     p.total_tiles = static_cast<int>(total);
     p.tpw = plan.tpw;

@@ -83,7 +83,15 @@ struct DecodeParams {
     WorkGroup grp[MAX_GROUPS];
     int n_desc, n_groups, H_q, H_kv, S_suf, q_f16;
     int total_tiles;        // dense: sum over items of vtiles
-    int tpw;                // dense: tiles per prefix worker
+    int tpw;                // sparse: (unused) / dense: the target tiles per prefix worker
+    // dense, aligned != 0: every item of descriptor d is cut into ppi[d] pieces of
+    // ceil(vtiles / ppi[d]) tiles (the last one shorter), one per prefix worker; descriptor d's
+    // workers start at wbase[d] (item (d, grp)'s pieces are workers wbase[d] + grp * ppi[d] ..),
+    // wbase[n_desc] = n_workers. aligned == 0: worker w takes tiles [w tpw, (w+1) tpw) of the
+    // items laid end to end (a range may straddle two items).
+    int aligned;
+    int ppi[MAX_DESC];
+    int wbase[MAX_DESC + 1];
     int n_workers;          // prefix workers (warps)
     int n_suf;              // suffix pieces per item (ceil(S_suf / 16))
     int sparse;             // 1: item sequences come from sel_blocks

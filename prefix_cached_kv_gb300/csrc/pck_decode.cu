@@ -553,12 +553,16 @@ __device__ __forceinline__ int worker_units(const DecodeParams& p, int total) {
 // the item are those of workers w0 .. w0 + npref - 1 (npref = 0 when the item has no units).
 __device__ __forceinline__ void item_range(const DecodeParams& p, int item, int& w0, int& npref) {
     const int d = item / p.n_groups, grp = item - d * p.n_groups;
-    int s, e, tpw;
+    int s = 0, e = 0, tpw = 1;
     if (p.sparse) {
         const int n_items = p.n_desc * p.n_groups;
         s = min(max(__ldcg(p.item_base + item), 0), p.max_units);
         e = min(max(__ldcg(p.item_base + item + 1), s), p.max_units);
         tpw = worker_units(p, min(max(__ldcg(p.item_base + n_items), 0), p.max_units));
+    } else if (p.aligned) {   // the item's whole pieces
+        w0 = p.wbase[d] + grp * p.ppi[d];
+        npref = p.ppi[d];
+        return;
     } else {
         s = p.desc[d].tile_off + grp * p.desc[d].vtiles;
         e = s + p.desc[d].vtiles;
@@ -882,9 +886,20 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     using StateT = std::conditional_t<FMT == FMT_FP16, F16State<D, NCB>, I4State<D, NCB>>;
     Cursor cons;
     const int total = FMT == FMT_FP16 && p.sparse ? units_total(p) : p.total_tiles;
-    const int tpw = worker_units(p, total);
-    cons.t = w * tpw;
-    cons.t_end = min(total, cons.t + tpw);
+    if ((FMT == FMT_FP16 && p.sparse) || !p.aligned) {
+        const int tpw = worker_units(p, total);
+        cons.t = w * tpw;
+        cons.t_end = min(total, cons.t + tpw);
+    } else {   // dense, aligned: piece k of item (d, grp), found from the descriptors' first workers
+        int d = 0;
+        while (d + 1 < p.n_desc && p.wbase[d + 1] <= w) ++d;
+        const int r = w - p.wbase[d], ppi = p.ppi[d], vt = p.desc[d].vtiles;
+        const int grp = r / ppi, k = r - grp * ppi;
+        const int ps = (vt + ppi - 1) / ppi;
+        const int s0 = p.desc[d].tile_off + grp * vt;
+        cons.t = s0 + k * ps;
+        cons.t_end = min(s0 + vt, cons.t + ps);
+    }
     if (cons.t >= cons.t_end) return;
     cursor_seek<FMT, D>(p, cons);
     Cursor prod = cons;
@@ -1096,8 +1111,9 @@ DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb) {
     return info_t<FMT_I4, 256, 2>();
 }
 
-bool plan_decode(int64_t total, int vmax, int n_items, int S_suf, bool sparse, int sms, int ctas_per_sm,
+bool plan_decode(DecodeParams* p, int64_t total, int vmax, int n_items, int S_suf, int sms, int ctas_per_sm,
                  int64_t max_slots, DecodePlan* out) {
+    const bool sparse = p->sparse != 0;
     const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
     const int64_t n_suf_warps = static_cast<int64_t>(n_items) * n_suf;
     const int64_t fixed = n_items + n_suf_warps;            // item slots + suffix piece slots
@@ -1109,7 +1125,36 @@ bool plan_decode(int64_t total, int vmax, int n_items, int S_suf, bool sparse, i
     int64_t tpw = (total + max_warps - 1) / max_warps;
     tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);         // at most ~32 prefix pieces per item
     if (tpw < 2) tpw = 2;
-    const int64_t n_workers = sparse ? std::min<int64_t>(max_warps, total) : (total + tpw - 1) / tpw;
+    int64_t n_workers = 0;
+    p->aligned = 0;
+    if (sparse) {
+        n_workers = std::min<int64_t>(max_warps, total);
+    } else {
+        // whole pieces per item; grow the target size until the pieces fit the warps
+        const int64_t tpw0 = tpw;
+        for (;; ++tpw) {
+            n_workers = 0;
+            for (int d = 0; d < p->n_desc; ++d) {
+                const int vt = p->desc[d].vtiles;
+                const int ps = static_cast<int>(std::min<int64_t>(vt, (vt + ((vt + tpw - 1) / tpw) - 1) / ((vt + tpw - 1) / tpw)));
+                p->ppi[d] = (vt + ps - 1) / ps;                  // every piece non-empty
+                p->wbase[d] = static_cast<int>(n_workers);
+                n_workers += static_cast<int64_t>(p->n_groups) * p->ppi[d];
+            }
+            p->wbase[p->n_desc] = static_cast<int>(n_workers);
+            if (n_workers <= max_warps || tpw >= vmax) break;
+        }
+        int max_ps = 1;
+        for (int d = 0; d < p->n_desc; ++d)
+            max_ps = std::max(max_ps, (p->desc[d].vtiles + p->ppi[d] - 1) / p->ppi[d]);
+        if (n_workers <= max_warps && max_ps * 20 <= tpw0 * 21) {
+            p->aligned = 1;
+        } else {   // plain ranges of tpw0 tiles across the items
+            tpw = tpw0;
+            n_workers = (total + tpw - 1) / tpw;
+        }
+        if (n_workers + fixed > max_slots) return false;
+    }
     out->tpw = static_cast<int>(tpw);
     out->n_workers = static_cast<int>(n_workers);
     out->n_suf = n_suf;

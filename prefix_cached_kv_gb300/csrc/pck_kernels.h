@@ -50,7 +50,12 @@ struct DecodePlan {
     int64_t slots;        // partial slots written
 };
 // false when the launch cannot fit (the item and suffix slots alone exceed max_slots).
-bool plan_decode(int64_t total, int vmax, int n_items, int S_suf, bool sparse, int sms, int ctas_per_sm,
+// Dense launches (p->sparse == 0) cut every item into whole pieces of about tpw tiles (p->ppi,
+// p->wbase; one worker per piece, so that no worker's range straddles two items: a worker that
+// starts a second item finishes late) unless whole pieces would be over 5 % longer than the plain
+// split (items long against the warps' share), where p->aligned stays 0 and ranges of tpw tiles
+// run across item boundaries. p's descriptors, n_desc and n_groups must be set.
+bool plan_decode(DecodeParams* p, int64_t total, int vmax, int n_items, int S_suf, int sms, int ctas_per_sm,
                  int64_t max_slots, DecodePlan* out);
 int decode_ncb(const DecodeParams& p);   // 4-head column blocks the mlx4g32 kernel needs for p
 cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);

@@ -134,7 +134,10 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     const int64_t max_slots =
         static_cast<int64_t>(NA_PARTIAL_BYTES / (static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float)));
     DecodePlan plan;
-    if (!plan_decode(total, ntiles, n_groups, S_suf, false, sp->sms, sp->ctas_per_sm[di][ncb - 1], max_slots, &plan))
+    p.n_desc = 1;
+    p.n_groups = n_groups;
+    p.desc[0].vtiles = ntiles;
+    if (!plan_decode(&p, total, ntiles, n_groups, S_suf, sp->sms, sp->ctas_per_sm[di][ncb - 1], max_slots, &plan))
         return PCK_EUNSUPPORTED;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
