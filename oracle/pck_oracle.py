@@ -48,6 +48,10 @@ Readings taken where the pages are silent:
   block may be partial; its mean is over the tokens it has.
 * QUERY_SPARSE indices are prefix token positions; q head h attends to the first
   counts[h] entries of its row of indices (kv head head_map[h]).
+* fa_window (listed on every QUERY form, never defined): a sliding attention window.
+  Query row i sits at absolute position p_i = N + S_suf - M + i (prefix positions
+  0..N-1, then the suffix), the last key it may see; with fa_window = W > 0 it sees
+  only keys at positions p_i - W + 1 .. p_i. W = 0 means no window.
 * The dequantised values are fp32: the exact s*c + b rounded once to fp32. An fp16
   output is that fp32 value rounded to fp16.
 """
@@ -182,22 +186,28 @@ def attend_rows(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, tau: f
     return O, LSE
 
 
-def suffix_allowed(M: int, N: int, S: int, causal: bool) -> np.ndarray:
+def suffix_allowed(M: int, N: int, S: int, causal: bool, window: int = 0) -> np.ndarray:
     """[M, N + S] key mask of the fused forms: every row sees the N prefix keys; with causal, row
-    i (0-based, of M) sees suffix keys j <= S - M + i (bottom-right alignment), else all S."""
+    i (0-based, of M) sees suffix keys j <= S - M + i (bottom-right alignment), else all S. With
+    window = W > 0, row i sees only positions p_i - W + 1 .. p_i, p_i = N + S - M + i."""
     allowed = np.ones((M, N + S), dtype=bool)
     if S and causal:
         for i in range(M):
             jmax = S - M + i
             allowed[i, N + max(jmax + 1, 0):] = False
+    if window > 0:
+        for i in range(M):
+            p_i = N + S - M + i
+            allowed[i, :max(p_i - window + 1, 0)] = False
     return allowed
 
 
-def prefix_query(Q, K, V, head_map=None, K_suf=None, V_suf=None, causal: bool = True):
+def prefix_query(Q, K, V, head_map=None, K_suf=None, V_suf=None, causal: bool = True, window: int = 0):
     """Attention of Q [H_q, M, D] over the prefix K/V [H_kv, N, D] (+ optional suffix [H_kv, S, D]).
 
     Query row i (0-based, of M) sees all N prefix keys and, when causal, suffix keys
-    j <= S - M + i (bottom-right alignment); without causal it sees the whole suffix.
+    j <= S - M + i (bottom-right alignment); without causal it sees the whole suffix. A window
+    W > 0 keeps only the W positions up to p_i = N + S - M + i (see suffix_allowed).
     Returns (O [H_q, M, D] float64, LSE [H_q, M] float64).
     """
     Q = np.asarray(Q, dtype=np.float64)
@@ -209,7 +219,7 @@ def prefix_query(Q, K, V, head_map=None, K_suf=None, V_suf=None, causal: bool = 
     S = 0 if K_suf is None else K_suf.shape[1]
     O = np.zeros((H_q, M, D))
     LSE = np.zeros((H_q, M))
-    allowed = suffix_allowed(M, N, S, causal)
+    allowed = suffix_allowed(M, N, S, causal, window)
     for h in range(H_q):
         g = int(head_map[h])
         keys = np.asarray(K[g], dtype=np.float64)

@@ -455,6 +455,42 @@ def test_warm_heads_lossless_on_grid_and_rounded_once():
     assert (np.abs(w32.astype(np.float64) - exact) <= np.spacing(np.abs(w32)) / 2).all()
 
 
+def test_window_equals_attention_over_the_last_keys():
+    """A window of W keys at M = 1 equals plain attention over the last W positions of the
+    concatenated prefix and suffix, built by slicing (so prefix-only, suffix-only and mixed
+    windows are all covered); W = 0 and W >= N + S change nothing."""
+    rng = np.random.default_rng(16)
+    H_q, H_kv, N, S, D = 4, 2, 40, 9, 16
+    Q = rng.standard_normal((H_q, 1, D))
+    K, V = rng.standard_normal((H_kv, N, D)), rng.standard_normal((H_kv, N, D))
+    Ks, Vs = rng.standard_normal((H_kv, S, D)), rng.standard_normal((H_kv, S, D))
+    Kall, Vall = np.concatenate([K, Ks], axis=1), np.concatenate([V, Vs], axis=1)
+    full = orc.prefix_query(Q, K, V, None, Ks, Vs)
+    for W in (0, N + S, N + S + 7):
+        O, L = orc.prefix_query(Q, K, V, None, Ks, Vs, window=W)
+        assert np.allclose(O, full[0]) and np.allclose(L, full[1])
+    for W in (1, 3, S, S + 1, 25, N + S - 1):
+        O, L = orc.prefix_query(Q, K, V, None, Ks, Vs, window=W)
+        Or, Lr = orc.prefix_query(Q, Kall[:, -W:], Vall[:, -W:])
+        assert np.allclose(O, Or, atol=1e-12) and np.allclose(L, Lr, atol=1e-12)
+    # W = 1 at M = 1: the value row of the last suffix key, LSE = its score
+    O, L = orc.prefix_query(Q, K, V, None, Ks, Vs, window=1)
+    g = np.arange(H_q) // 2
+    assert np.allclose(O[:, 0], Vs[g, -1])
+    assert np.allclose(L[:, 0], np.einsum("hd,hd->h", Q[:, 0], Ks[g, -1]) / math.sqrt(D))
+
+
+def test_window_per_row_under_the_causal_mask():
+    """M > 1: row i sees positions p_i - W + 1 .. p_i with p_i = N + S - M + i: a hand-built mask
+    from positions, compared with suffix_allowed."""
+    N, S, M, W = 6, 4, 3, 4
+    allowed = orc.suffix_allowed(M, N, S, True, W)
+    for i in range(M):
+        p_i = N + S - M + i
+        want = np.array([(p_i - W + 1) <= t <= p_i for t in range(N + S)])
+        assert (allowed[i] == want).all()
+
+
 # ------------------------------------------------------------------ planted mistakes are caught
 
 def test_pins_catch_planted_mistakes(monkeypatch):
@@ -561,14 +597,14 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     good_mask = mod.suffix_allowed
 
-    def top_left_causal(M, N, S, causal):
+    def top_left_causal(M, N, S, causal, window=0):
         allowed = np.ones((M, N + S), dtype=bool)
         if S and causal:
             for i in range(M):
                 allowed[i, N + i + 1:] = False
         return allowed
 
-    def causal_one_short(M, N, S, causal):
+    def causal_one_short(M, N, S, causal, window=0):
         allowed = good_mask(M, N, S, causal)
         if S and causal:
             for i in range(M):
@@ -619,3 +655,17 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_warm_heads_lossless_on_grid_and_rounded_once()
     monkeypatch.setattr(mod, "warm_heads", good_wh)
+
+    def window_one_short(M, N, S, causal, window=0):
+        allowed = good_mask(M, N, S, causal, window)
+        if window > 0:
+            for i in range(M):
+                t = N + S - M + i - window + 1
+                if 0 <= t < N + S:
+                    allowed[i, t] = False
+        return allowed
+
+    monkeypatch.setattr(mod, "suffix_allowed", window_one_short)
+    with pytest.raises(AssertionError):
+        test_window_equals_attention_over_the_last_keys()
+    monkeypatch.setattr(mod, "suffix_allowed", good_mask)
