@@ -53,7 +53,9 @@ extern "C" {
 #define PCK_DT_F32       0
 #define PCK_DT_F16       1
 
-/* Head dimensions with kernels: 64, 128, 256. Larger H_q per kv head than 8 is split. */
+/* Head dimensions with kernels: fp16 slots 32, 64, 96, 128, 160, 192, 256 (M = 1 and M > 1);
+ * mlx4g32 slots 64, 128, 192, 256 (M > 1: 64, 128); sparse forms 64, 128, 256. D = 512 (listed by
+ * the pages) has none. More than 8 q heads per kv head are split into work groups. */
 #define PCK_MAX_BATCH    64   /* descriptors per pck_query_batch call */
 #define PCK_MAX_HEADS    64   /* H_q and H_kv limit */
 
@@ -108,7 +110,7 @@ const char *pck_last_error(const pck_ctx *ctx);
  * fmt MLX4G32 quantises both on the device (same arithmetic as pck_quantize_mlx4g32) and keeps
  * the codes/scales/biases resident. Replaces an existing slot with the same key. The library
  * copies K/V into its own memory: the caller may reuse K/V once the stream passes the call.
- * D in {64, 128, 256}, H_kv <= 64, N >= 1. Errors: EINVAL, EUNSUPPORTED, ENOMEM. */
+ * D: see above; H_kv <= 64, N >= 1. Errors: EINVAL, EUNSUPPORTED, ENOMEM. */
 int pck_store(pck_ctx *ctx, const char *sid, int layer, int H_kv, int N, int D, int fmt,
               const void *K, const void *V, int src_dtype, void *stream);
 
@@ -136,7 +138,12 @@ int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void 
  * mlx4g32 slot (D in {64, 128}) the call first dequantises the slot into a stream-ordered
  * temporary of H_kv * N * 8 * D bytes, each value as an fp16 hi + lo pair, and attends to it
  * with the same kernel at width 2D, so K and V keep ~22 bits.
- * top_k: 0 or >= N (dense). fa_window: 0. Other values are PCK_EUNSUPPORTED.
+ * top_k: 0 or >= N (dense); smaller values are PCK_EUNSUPPORTED.
+ * fa_window (listed on every QUERY form of the pages, never defined there; this library's reading):
+ * 0 = no window; W > 0 = a sliding attention window: query row i, at absolute position
+ * p_i = N + S_suf - M + i (prefix positions 0 .. N-1, then the suffix), sees only positions
+ * p_i - W + 1 .. p_i. Built for M = 1 (both formats, with or without a suffix); M > 1 with W > 0
+ * is PCK_EUNSUPPORTED, W < 0 PCK_EINVAL.
  * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
 int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
               const void *Q, const int32_t *head_map, int top_k, int fa_window,

@@ -61,8 +61,8 @@ struct pck_ctx {
     uint8_t* suf_ws = nullptr;
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
-    DecodeLaunchInfo dinfo[2][6];
-    bool dinfo_ok[2][6] = {};
+    DecodeLaunchInfo dinfo[2][14];   // [format][head dimension x column blocks]
+    bool dinfo_ok[2][14] = {};
 };
 
 namespace {
@@ -90,11 +90,23 @@ std::string key_of(const char* sid, int layer) {
     return k;
 }
 
-bool d_ok(int D) { return D == 64 || D == 128 || D == 256; }
-int d_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
+// head dimensions with kernels, per resident format (the M=1 kernels; M>1 and the sparse forms
+// check their own)
+bool d_ok(int D, int fmt) { return decode_dim_ok(fmt == PCK_FMT_FP16 ? FMT_FP16 : FMT_I4, D); }
+int d_index(int D) {
+    switch (D) {
+        case 32: return 0;
+        case 64: return 1;
+        case 96: return 2;
+        case 128: return 3;
+        case 160: return 4;
+        case 192: return 5;
+        default: return 6;
+    }
+}
 
 const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D, int ncb) {
-    const int i = d_index(D) + 3 * (ncb - 1);
+    const int i = d_index(D) + 7 * (ncb - 1);
     if (!c->dinfo_ok[fmt][i]) {
         c->dinfo[fmt][i] = decode_launch_info(fmt, D, ncb);
         c->dinfo_ok[fmt][i] = true;
@@ -219,6 +231,7 @@ struct DescIn {
     const void* Vsuf;
     const int* sel_blocks = nullptr;     // sparse: the query's [n_groups, sel_max] block lists
     const uint8_t* sel_mask = nullptr;   // sparse: per-block q-head masks
+    int window = 0;                      // dense M=1: fa_window (0: none)
 };
 
 // Plan and launch one decode over n descriptors (dense), or one sparse descriptor.
@@ -250,7 +263,14 @@ int run_decode(pck_ctx* c, int fmt, int D, int H_q, int H_kv, int S_suf, int q_f
         d.Vsuf = static_cast<const __half*>(dsc[i].Vsuf);
         d.N = dsc[i].slot->N;
         d.ntiles = dsc[i].slot->ntiles;
-        d.vtiles = sparse ? sel_max * tiles_per_block : d.ntiles;
+        d.t_lo = d.s_lo = d.tile0 = 0;
+        if (!sparse && dsc[i].window > 0) {   // the last `window` positions of prefix + suffix
+            const int first = d.N + S_suf - dsc[i].window;   // first visible position
+            d.t_lo = std::min(std::max(first, 0), d.N);      // == N: no prefix token is visible
+            d.s_lo = std::max(first - d.N, 0);
+            d.tile0 = std::min(d.t_lo, d.N - 1) / TILE_TOK;  // keep one (masked) tile
+        }
+        d.vtiles = sparse ? sel_max * tiles_per_block : d.ntiles - d.tile0;
         d.sel_blocks = dsc[i].sel_blocks;
         d.sel_mask = dsc[i].sel_mask;
         d.tile_off = static_cast<int>(total);
@@ -339,8 +359,9 @@ int pck_store(pck_ctx* c, const char* sid, int layer, int H_kv, int N, int D, in
     if (!c) return PCK_EINVAL;
     if (!sid || !K || !V) return fail(c, PCK_EINVAL, "NULL sid/K/V");
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || N < 1) return fail(c, PCK_EINVAL, "bad H_kv=%d or N=%d", H_kv, N);
-    if (!d_ok(D)) return fail(c, PCK_EUNSUPPORTED, "D=%d (kernels exist for 64, 128, 256)", D);
     if (fmt != PCK_FMT_FP16 && fmt != PCK_FMT_MLX4G32) return fail(c, PCK_EINVAL, "fmt=%d", fmt);
+    if (!d_ok(D, fmt))
+        return fail(c, PCK_EUNSUPPORTED, "D=%d (fp16 slots: 32, 64, 96, 128, 160, 192, 256; mlx4g32: 64, 128, 192, 256)", D);
     if (!dtype_ok(src_dtype)) return fail(c, PCK_EINVAL, "src_dtype=%d", src_dtype);
     if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) & 15)
         return fail(c, PCK_EINVAL, "K/V must be 16-byte aligned");
@@ -392,7 +413,7 @@ int pck_store_records(pck_ctx* c, const char* sid, int layer, int H_kv, int N, i
     if (!c) return PCK_EINVAL;
     if (!sid || !K_rec || !V_rec) return fail(c, PCK_EINVAL, "NULL sid/records");
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || N < 1) return fail(c, PCK_EINVAL, "bad H_kv=%d or N=%d", H_kv, N);
-    if (!d_ok(D)) return fail(c, PCK_EUNSUPPORTED, "D=%d (kernels exist for 64, 128, 256)", D);
+    if (!d_ok(D, PCK_FMT_MLX4G32)) return fail(c, PCK_EUNSUPPORTED, "D=%d (mlx4g32 slots: 64, 128, 192, 256)", D);
     if ((reinterpret_cast<uintptr_t>(K_rec) | reinterpret_cast<uintptr_t>(V_rec)) & 3)
         return fail(c, PCK_EINVAL, "records must be 4-byte aligned");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -486,7 +507,9 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     if (!c) return PCK_EINVAL;
     if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
     if (reinterpret_cast<uintptr_t>(O) & 15) return fail(c, PCK_EINVAL, "O must be 16-byte aligned");
-    if (fa_window != 0) return fail(c, PCK_EUNSUPPORTED, "fa_window=%d (only 0 is defined)", fa_window);
+    if (fa_window < 0) return fail(c, PCK_EINVAL, "fa_window=%d", fa_window);
+    if (fa_window > 0 && M > 1)
+        return fail(c, PCK_EUNSUPPORTED, "fa_window=%d with M=%d (windows are built for M = 1)", fa_window, M);
     if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
     if (M < 1) return fail(c, PCK_EINVAL, "M=%d", M);
     if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
@@ -504,6 +527,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M == 1) {
         DescIn d{s, Q, O, LSE, K_suf, V_suf};
+        d.window = fa_window;
         rc = run_decode(c, s->fmt, D, H_q, s->H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, &d, 1, 0, 0, 0, nullptr, st);
         if (rc != PCK_OK) return rc;
         return check_async(c);

@@ -68,8 +68,11 @@ struct DecodeDesc {
     const uint8_t* sel_mask;// sparse: [n_groups][sel_max] bit h = local q head h selected it
     int N;                  // prefix tokens
     int ntiles;             // ceil(N / 16)
-    int vtiles;             // tiles of one item's sequence (ntiles, or sel_max * tiles/block)
+    int vtiles;             // tiles of one item's sequence (ntiles - tile0, or sel_max * tiles/block)
     int tile_off;           // first global tile of this descriptor's items
+    // attention window (dense M=1): prefix tokens below t_lo and suffix tokens below s_lo are
+    // masked; an item's tiles start at resident tile tile0 = t_lo / 16 (0 without a window)
+    int t_lo, s_lo, tile0;
 };
 
 struct WorkGroup {

@@ -1,5 +1,7 @@
-// pck_decode.cu -- M=1 attention over a resident prefix: split-K ("stream-K") decode with the
-// dense suffix and the online-softmax merge fused into the same launch.
+// pck_decode_impl.cuh -- M=1 attention over a resident prefix: split-K ("stream-K") decode with
+// the dense suffix and the online-softmax merge fused into the same launch. The templates; they are
+// instantiated for D in {64, 128, 256} in pck_decode.cu and for D in {32, 96, 160, 192} in
+// pck_decode_xd.cu, so that the two compile in parallel.
 //
 // Follows "ATTEND.* and ATTEND.PREFIX.*", section "Wire forms": QUERY (M=1), QUERY_FUSED
 // (prefix + dense suffix + merge in one dispatch), QUERY_SPARSE_AUTO(_FUSED) (attention
@@ -29,6 +31,8 @@
 // Softmax runs in base 2 on log2(e)-prescaled scores; the running max is only moved when a
 // tile's max exceeds it by more than 8 (so stored weights stay <= 256), which keeps the
 // rescale of the accumulators off the common path and does not change the result.
+#pragma once
+
 #include <math.h>
 
 #include <algorithm>
@@ -45,7 +49,7 @@ struct DCfg {
     static constexpr int NG = D / 32;       // mlx4g32 groups per head
     static constexpr int NBV = D / 8;       // PV n-blocks over d
     static constexpr int TB = tile_bytes(FMT, D);
-    static constexpr int TPS = FMT == FMT_FP16 ? (D == 64 ? 2 : 1) : (D == 64 ? 4 : (D == 128 ? 4 : 1));
+    static constexpr int TPS = FMT == FMT_FP16 ? (D == 32 ? 4 : (D == 64 ? 2 : 1)) : (D == 64 ? 4 : (D == 128 ? 4 : 1));
     static constexpr int STAGE = TPS * TB;
     static constexpr int NSTAGE = FMT == FMT_FP16 ? 3 : 2;
     static constexpr int RING = NSTAGE * STAGE;
@@ -166,7 +170,7 @@ struct GlobalF16Tile {
 // step, then O^T += V^T P^T with P (hi / lo fp16 parts) moved into B fragments by movmatrix.
 template <int D, int NCB, typename Src>
 __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, int lane, int valid,
-                                         uint32_t head_mask, int nq) {
+                                         uint32_t head_mask, int nq, int lo = 0) {
     constexpr int KS = D / 16;
     const int q = lane & 3, t0 = lane >> 2;
     float acc[NCB][4];
@@ -185,15 +189,15 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
         z[cb][0] = acc[cb][0] + acc[cb][1];   // hi + lo columns
         z[cb][1] = acc[cb][2] + acc[cb][3];
     }
-    // masks (warp-uniform test): tokens past the end, heads the tile does not serve
+    // masks (warp-uniform test): tokens past the end or before a window, heads the tile does not serve
     const uint32_t heads = nq >= 32 ? 0xFFFFFFFFu : ((1u << nq) - 1u);
-    if (valid < 16 || (head_mask & heads) != heads || nq < 4 * NCB) {
+    if (valid < 16 || lo > 0 || (head_mask & heads) != heads || nq < 4 * NCB) {
 #pragma unroll
         for (int cb = 0; cb < NCB; ++cb) {
             const int h = cb * 4 + q;
             const bool hok = h < nq && ((head_mask >> h) & 1u);
-            if (!(hok && t0 < valid)) z[cb][0] = -INFINITY;
-            if (!(hok && t0 + 8 < valid)) z[cb][1] = -INFINITY;
+            if (!(hok && t0 < valid && t0 >= lo)) z[cb][0] = -INFINITY;
+            if (!(hok && t0 + 8 < valid && t0 + 8 >= lo)) z[cb][1] = -INFINITY;
         }
     }
     // Rescale test on each lane's own maximum: the head's maximum over its 8 lanes passes the
@@ -347,7 +351,7 @@ __device__ __forceinline__ void start_item_i4(I4State<D, NCB>& st, const DecodeP
 // softmax step, then O += P' V for each tile.
 template <int D, int NCB, int NT>
 __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile0, int lane, int valid0,
-                                        uint32_t head_mask, int nq) {
+                                        uint32_t head_mask, int nq, int lo0 = 0) {
     using S = I4State<D, NCB>;
     constexpr int NG = S::NG, KS = S::KS, TB = 20 * D;
     const int q = lane & 3, t0 = lane >> 2;
@@ -411,18 +415,19 @@ __device__ __forceinline__ void tile_i4(I4State<D, NCB>& st, const uint8_t* tile
             z[x][cb][1] = fmaf(zs1[cb], 1048576.0f, zb1[cb]);      // 2^20: rows t0+8 hold 16 c * 2^-24
         }
     }
-    // masks (warp-uniform test): tokens past the end of the prefix, heads the chunk does not serve
+    // masks (warp-uniform test): tokens past the end of the prefix or before a window, heads the
+    // chunk does not serve
     const uint32_t heads = nq >= 32 ? 0xFFFFFFFFu : ((1u << nq) - 1u);
-    if (valid0 < 16 * NT || (head_mask & heads) != heads || nq < 4 * NCB) {
+    if (valid0 < 16 * NT || lo0 > 0 || (head_mask & heads) != heads || nq < 4 * NCB) {
 #pragma unroll
         for (int x = 0; x < NT; ++x) {
-            const int va = valid0 - 16 * x;
+            const int va = valid0 - 16 * x, lx = lo0 - 16 * x;
 #pragma unroll
             for (int cb = 0; cb < NCB; ++cb) {
                 const int h = cb * 4 + q;
                 const bool hok = h < nq && ((head_mask >> h) & 1u);
-                if (!(hok && t0 < va)) z[x][cb][0] = -INFINITY;
-                if (!(hok && t0 + 8 < va)) z[x][cb][1] = -INFINITY;
+                if (!(hok && t0 < va && t0 >= lx)) z[x][cb][0] = -INFINITY;
+                if (!(hok && t0 + 8 < va && t0 + 8 >= lx)) z[x][cb][1] = -INFINITY;
             }
         }
     }
@@ -589,11 +594,12 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
         const int slot = k < npref ? (w0 + k + item) : (p.n_workers + n_items + item * p.n_suf + (k - npref));
         return p.partials + (size_t)slot * PSTR + h * partial_stride(D);
     };
-    constexpr int LPP = D / 4 > 32 ? 32 : D / 4;   // lanes per piece (one float4 of d each)
+    constexpr int F4 = D / 4;                      // float4 of o per piece
+    constexpr int LPP = F4 >= 32 ? 32 : (F4 > 16 ? 32 : (F4 > 8 ? 16 : 8));   // lanes per piece (a power of 2)
     constexpr int PPS = 32 / LPP;                  // pieces per warp-wide load
-    constexpr int V4 = D / 4 / LPP;                // float4 per lane per piece
-    constexpr int NB = D == 256 ? 16 : 16 / V4;    // warp-wide loads per batch
-    constexpr int BP = NB * PPS;                   // pieces per batch (32, 16, 16 for D = 64, 128, 256)
+    constexpr int V4 = (F4 + LPP - 1) / LPP;       // float4 per lane per piece
+    constexpr int NB = 32 / PPS < 16 ? 32 / PPS : 16;   // warp-wide loads per batch
+    constexpr int BP = NB * PPS;                   // pieces per batch (<= 32: one lane per piece's (m, l))
     const int sub = lane / LPP, dl = lane % LPP;
     float M = -INFINITY, L = 0.f;                  // L: this lane's share (lanes over pieces)
     float4 acc[V4];
@@ -614,7 +620,8 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
             if (jj < nk) {
                 const float4* ph = reinterpret_cast<const float4*>(piece(c + jj) + PARTIAL_O) + dl;
 #pragma unroll
-                for (int v = 0; v < V4; ++v) xs[b][v] = __ldcg(ph + v * LPP);
+                for (int v = 0; v < V4; ++v)
+                    xs[b][v] = dl + v * LPP < F4 ? __ldcg(ph + v * LPP) : make_float4(0.f, 0.f, 0.f, 0.f);
             } else {
 #pragma unroll
                 for (int v = 0; v < V4; ++v) xs[b][v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -662,8 +669,9 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
     if (sub == 0) {
 #pragma unroll
         for (int v = 0; v < V4; ++v)
-            reinterpret_cast<float4*>(ds.O + (size_t)qh * D)[dl + v * LPP] =
-                make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+            if (dl + v * LPP < F4)
+                reinterpret_cast<float4*>(ds.O + (size_t)qh * D)[dl + v * LPP] =
+                    make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
     }
     if (lane == 0 && ds.LSE) ds.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
 }
@@ -710,6 +718,7 @@ struct Cursor {
     int item, d, grp;        // current item (= d * n_groups + grp)
     int item_start, item_end;
     int ntiles, N, nq;
+    int tile0, t_lo;         // the item's first resident tile and first visible token (a window)
     const uint8_t* kbase;    // fp16: K region of the item's kv head; mlx4g32: the kv head's tiles
     size_t vofs;             // fp16: bytes from the K region to the V region
     int sel_blk, sel_msk;    // sparse, lists of <= 32 blocks: lane l holds entry l of the item's list
@@ -721,6 +730,7 @@ struct Chunk {
     int tile;     // first real tile (within the kv head) of the chunk
     int nreal;    // tiles to copy and compute
     int valid;    // tokens of the prefix from the chunk's first token on
+    int lo;       // tokens of the chunk's first tile below the window (<= 0: none)
     int nq;       // q heads of the item
     uint32_t mask;// bit h: local q head h attends to this chunk's tokens
     bool last;    // last chunk of this worker's piece of the item
@@ -751,6 +761,8 @@ __device__ __forceinline__ void cursor_set_item(const DecodeParams& p, Cursor& c
     c.ntiles = ds.ntiles;
     c.N = ds.N;
     c.nq = wg.nq;
+    c.tile0 = ds.tile0;
+    c.t_lo = ds.t_lo;
     if constexpr (FMT == FMT_FP16) {
         c.vofs = fp16_region_bytes(ds.ntiles, D);
         c.kbase = ds.kv + (size_t)wg.g * 2 * c.vofs;
@@ -839,7 +851,7 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
     int n;
     if (!CAN_SPARSE || !p.sparse) {
         n = min(TPS, lim);
-        ch.tile = local;
+        ch.tile = c.tile0 + local;
         ch.nreal = n;
         ch.mask = 0xFFu;
     } else {
@@ -866,6 +878,7 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
     ch.grp = c.grp;
     ch.nq = c.nq;
     ch.valid = c.N - ch.tile * TILE_TOK;
+    ch.lo = c.t_lo - ch.tile * TILE_TOK;
     if constexpr (FMT == FMT_FP16) {
         ch.src = c.kbase + (size_t)ch.tile * 32 * D;
         ch.src2 = c.kbase + c.vofs + (size_t)ch.tile * 32 * D;
@@ -960,20 +973,20 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         const uint32_t head_mask = c.mask;   // bit h: local q head h attends to this chunk's tokens
         const uint8_t* sbuf = ring + stage * C::STAGE;
         for (int k = 0; k < c.nreal; ++k) {
-            const int valid = c.valid - k * TILE_TOK;
+            const int valid = c.valid - k * TILE_TOK, lo = c.lo - k * TILE_TOK;
             if constexpr (FMT == FMT_FP16) {
                 const uint32_t sb = smem_u32(sbuf);
                 SmemF16Tile<D> tl{sb + k * 32 * D, sb + C::STAGE / 2 + k * 32 * D, lane};
-                tile_f16<D, NCB>(st, tl, lane, valid, head_mask, c.nq);
+                tile_f16<D, NCB>(st, tl, lane, valid, head_mask, c.nq, lo);
             } else {
                 if (D <= 128 && NCB == 1 && k + 3 < c.nreal) {   // four tiles per softmax step
-                    tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
+                    tile_i4<D, NCB, 4>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq, lo);
                     k += 3;
                 } else if (k + 1 < c.nreal) {   // two tiles per softmax step
-                    tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
+                    tile_i4<D, NCB, 2>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq, lo);
                     ++k;
                 } else {
-                    tile_i4<D, NCB, 1>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq);
+                    tile_i4<D, NCB, 1>(st, sbuf + k * C::TB, lane, valid, head_mask, c.nq, lo);
                 }
             }
         }
@@ -1007,7 +1020,7 @@ __device__ void suffix_worker(const DecodeParams& p, int sidx, int lane) {
     start_item_f16<D, NCB>(st, p, ds, wg, lane);
     const int t0 = 16 * k;
     GlobalF16Tile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
-    tile_f16<D, NCB>(st, tl, lane, p.S_suf - t0, 0xFFFFFFFFu, wg.nq);
+    tile_f16<D, NCB>(st, tl, lane, p.S_suf - t0, 0xFFFFFFFFu, wg.nq, ds.s_lo - t0);
     finish_piece_f16<D, NCB>(st, p, item, p.n_workers + n_items + item * p.n_suf + k, lane);
 }
 
@@ -1040,9 +1053,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __gr
 // ---------------------------------------------------------------- host side
 
 template <int FMT, int D, int NCB>
-static cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) {
+cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) {
     using C = DCfg<FMT, D>;
-    static bool attr_set = false;
+    static bool attr_set = false;   // per instantiation
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<FMT, D, NCB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
@@ -1077,7 +1090,7 @@ static cudaError_t launch_t(const DecodeParams& p, int n_ctas, cudaStream_t st) 
 }
 
 template <int FMT, int D, int NCB>
-static DecodeLaunchInfo info_t() {
+DecodeLaunchInfo info_t() {
     using C = DCfg<FMT, D>;
     DecodeLaunchInfo i{C::STAGE, C::NSTAGE, C::SMEM, 0};
     int n = 0;
@@ -1089,109 +1102,14 @@ static DecodeLaunchInfo info_t() {
     return i;
 }
 
-// ncb: 4-head column blocks of the mlx4g32 kernel (1 when every work group has <= 4 q heads).
-DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb) {
-    if (fmt == FMT_FP16) {
-        if (ncb == 1) {
-            if (D == 64) return info_t<FMT_FP16, 64, 1>();
-            if (D == 128) return info_t<FMT_FP16, 128, 1>();
-            return info_t<FMT_FP16, 256, 1>();
-        }
-        if (D == 64) return info_t<FMT_FP16, 64, 2>();
-        if (D == 128) return info_t<FMT_FP16, 128, 2>();
-        return info_t<FMT_FP16, 256, 2>();
-    }
-    if (ncb == 1) {
-        if (D == 64) return info_t<FMT_I4, 64, 1>();
-        if (D == 128) return info_t<FMT_I4, 128, 1>();
-        return info_t<FMT_I4, 256, 1>();
-    }
-    if (D == 64) return info_t<FMT_I4, 64, 2>();
-    if (D == 128) return info_t<FMT_I4, 128, 2>();
-    return info_t<FMT_I4, 256, 2>();
+// Launch and occupancy of one (format, D) pair; instantiated by the translation units that own D.
+template <int FMT, int D>
+cudaError_t launch_d(const DecodeParams& p, int ncb, int n_ctas, cudaStream_t st) {
+    return ncb == 1 ? launch_t<FMT, D, 1>(p, n_ctas, st) : launch_t<FMT, D, 2>(p, n_ctas, st);
 }
-
-bool plan_decode(DecodeParams* p, int64_t total, int vmax, int n_items, int S_suf, int sms, int ctas_per_sm,
-                 int64_t max_slots, DecodePlan* out) {
-    const bool sparse = p->sparse != 0;
-    const int n_suf = (S_suf + TILE_TOK - 1) / TILE_TOK;
-    const int64_t n_suf_warps = static_cast<int64_t>(n_items) * n_suf;
-    const int64_t fixed = n_items + n_suf_warps;            // item slots + suffix piece slots
-    if (fixed >= max_slots) return false;
-    // prefix workers and suffix warps together stay within one wave of resident warps
-    int64_t max_warps = static_cast<int64_t>(sms) * ctas_per_sm * DECODE_WARPS - n_suf_warps;
-    if (max_warps < 1) max_warps = 1;
-    if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;
-    int64_t tpw = (total + max_warps - 1) / max_warps;
-    tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);         // at most ~32 prefix pieces per item
-    if (tpw < 2) tpw = 2;
-    int64_t n_workers = 0;
-    p->aligned = 0;
-    if (sparse) {
-        n_workers = std::min<int64_t>(max_warps, total);
-    } else {
-        // whole pieces per item; grow the target size until the pieces fit the warps
-        const int64_t tpw0 = tpw;
-        for (;; ++tpw) {
-            n_workers = 0;
-            for (int d = 0; d < p->n_desc; ++d) {
-                const int vt = p->desc[d].vtiles;
-                const int ps = static_cast<int>(std::min<int64_t>(vt, (vt + ((vt + tpw - 1) / tpw) - 1) / ((vt + tpw - 1) / tpw)));
-                p->ppi[d] = (vt + ps - 1) / ps;                  // every piece non-empty
-                p->wbase[d] = static_cast<int>(n_workers);
-                n_workers += static_cast<int64_t>(p->n_groups) * p->ppi[d];
-            }
-            p->wbase[p->n_desc] = static_cast<int>(n_workers);
-            if (n_workers <= max_warps || tpw >= vmax) break;
-        }
-        int max_ps = 1;
-        for (int d = 0; d < p->n_desc; ++d)
-            max_ps = std::max(max_ps, (p->desc[d].vtiles + p->ppi[d] - 1) / p->ppi[d]);
-        if (n_workers <= max_warps && max_ps * 20 <= tpw0 * 21) {
-            p->aligned = 1;
-        } else {   // plain ranges of tpw0 tiles across the items
-            tpw = tpw0;
-            n_workers = (total + tpw - 1) / tpw;
-        }
-        if (n_workers + fixed > max_slots) return false;
-    }
-    out->tpw = static_cast<int>(tpw);
-    out->n_workers = static_cast<int>(n_workers);
-    out->n_suf = n_suf;
-    out->n_ctas = static_cast<int>((n_workers + n_suf_warps + DECODE_WARPS - 1) / DECODE_WARPS);
-    out->slots = n_workers + fixed;
-    return true;
-}
-
-int decode_ncb(const DecodeParams& p) {
-    int mx = 0;
-    for (int i = 0; i < p.n_groups; ++i) mx = p.grp[i].nq > mx ? p.grp[i].nq : mx;
-    return mx > 4 ? 2 : 1;
-}
-
-cudaError_t launch_decode(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st) {
-    if (fmt == FMT_FP16) {
-        if (decode_ncb(p) == 1) {
-            if (D == 64) return launch_t<FMT_FP16, 64, 1>(p, n_ctas, st);
-            if (D == 128) return launch_t<FMT_FP16, 128, 1>(p, n_ctas, st);
-            if (D == 256) return launch_t<FMT_FP16, 256, 1>(p, n_ctas, st);
-        } else {
-            if (D == 64) return launch_t<FMT_FP16, 64, 2>(p, n_ctas, st);
-            if (D == 128) return launch_t<FMT_FP16, 128, 2>(p, n_ctas, st);
-            if (D == 256) return launch_t<FMT_FP16, 256, 2>(p, n_ctas, st);
-        }
-        return cudaErrorInvalidValue;
-    }
-    if (decode_ncb(p) == 1) {
-        if (D == 64) return launch_t<FMT_I4, 64, 1>(p, n_ctas, st);
-        if (D == 128) return launch_t<FMT_I4, 128, 1>(p, n_ctas, st);
-        if (D == 256) return launch_t<FMT_I4, 256, 1>(p, n_ctas, st);
-    } else {
-        if (D == 64) return launch_t<FMT_I4, 64, 2>(p, n_ctas, st);
-        if (D == 128) return launch_t<FMT_I4, 128, 2>(p, n_ctas, st);
-        if (D == 256) return launch_t<FMT_I4, 256, 2>(p, n_ctas, st);
-    }
-    return cudaErrorInvalidValue;
+template <int FMT, int D>
+DecodeLaunchInfo info_d(int ncb) {
+    return ncb == 1 ? info_t<FMT, D, 1>() : info_t<FMT, D, 2>();
 }
 
 }  // namespace pck

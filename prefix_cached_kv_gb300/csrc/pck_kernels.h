@@ -35,6 +35,11 @@ struct DecodeLaunchInfo {
     int ctas_per_sm;
 };
 DecodeLaunchInfo decode_launch_info(int fmt, int D, int ncb);
+// the M=1 kernels' head dimensions: 32, 64, 96, 128, 160, 192, 256 for fp16 slots; 64, 128, 192,
+// 256 for mlx4g32 slots
+bool decode_dim_ok(int fmt, int D);
+DecodeLaunchInfo decode_launch_info_xd(int fmt, int D, int ncb);   // D in {32, 96, 160, 192}
+cudaError_t launch_decode_xd(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);
 // How one decode launch splits its work. Dense: `total` units (16-token tiles) over items of at
 // most `vmax` units each are cut into ranges of tpw units, one per prefix worker (a warp), with
 // at least ceil(vmax / 32) units per range so that an item has at most ~32 pieces to merge, and at

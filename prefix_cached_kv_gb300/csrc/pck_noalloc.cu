@@ -50,7 +50,7 @@ struct NaDevice {
     float* partials = nullptr;
     int* err = nullptr;
     int sms = 0;
-    int ctas_per_sm[3][2] = {};   // [D = 64, 128, 256][column blocks 1, 2]
+    int ctas_per_sm[4][2] = {};   // [D = 64, 128, 192, 256][column blocks 1, 2]
 };
 NaDevice g_na[NA_MAX_DEVICES];
 
@@ -63,8 +63,8 @@ void na_setup_once(NaDevice& s, int dev) {
         s.rc = PCK_ECUDA;
         return;
     }
-    const int Ds[3] = {64, 128, 256};
-    for (int i = 0; i < 3; ++i)
+    const int Ds[4] = {64, 128, 192, 256};
+    for (int i = 0; i < 4; ++i)
         for (int ncb = 1; ncb <= 2; ++ncb) s.ctas_per_sm[i][ncb - 1] = decode_launch_info(FMT_I4, Ds[i], ncb).ctas_per_sm;
     s.rc = cudaGetLastError() == cudaSuccess ? PCK_OK : PCK_ECUDA;
 }
@@ -88,7 +88,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     if (!K_rec || !V_rec || !Q || !O) return PCK_EINVAL;
     if ((reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(Q)) & 15) return PCK_EINVAL;
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || H_q < 1 || H_q > PCK_MAX_HEADS || N < 1 || S_suf < 0) return PCK_EINVAL;
-    if (D != 64 && D != 128 && D != 256) return PCK_EUNSUPPORTED;
+    if (D != 64 && D != 128 && D != 192 && D != 256) return PCK_EUNSUPPORTED;
     if (q_dtype != PCK_DT_F32 && q_dtype != PCK_DT_F16) return PCK_EINVAL;
     if (S_suf > 0 && (!K_suf || !V_suf)) return PCK_EINVAL;
     if ((reinterpret_cast<uintptr_t>(K_rec) | reinterpret_cast<uintptr_t>(V_rec)) & 3) return PCK_EINVAL;
@@ -129,7 +129,7 @@ extern "C" int pck_attend_records_noalloc(int H_kv, int N, int D, const void* K_
     NaDevice* sp = na_device();
     if (!sp) return PCK_ECUDA;
     const int ncb = max_nq > 4 ? 2 : 1;
-    const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
+    const int di = D == 64 ? 0 : (D == 128 ? 1 : (D == 192 ? 2 : 3));
     const int64_t total = static_cast<int64_t>(n_groups) * ntiles;
     const int64_t max_slots =
         static_cast<int64_t>(NA_PARTIAL_BYTES / (static_cast<size_t>(GMAX) * partial_stride(D) * sizeof(float)));

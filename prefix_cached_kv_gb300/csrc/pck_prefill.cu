@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
     const int lane = threadIdx.x & 31;
     const int rows = P.n_tiles * PF_ROWS;
     constexpr int LPP = D / 4 < 32 ? D / 4 : 32;   // lanes holding the row's d
-    constexpr int V4 = D / 4 / LPP;                  // float4 of d per lane
+    constexpr int V4 = (D / 4 + LPP - 1) / LPP;      // float4 of d per lane
     for (int R = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; R < rows; R += (gridDim.x * blockDim.x) >> 5) {
         const int tile = R / PF_ROWS, rr = R - tile * PF_ROWS;
         int grp = 0;
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
             for (int k = 0; k < NBS; ++k)
 #pragma unroll
                 for (int v = 0; v < V4; ++v)
-                    xs[k][v] = (k < nk && lane < LPP)
+                    xs[k][v] = (k < nk && lane < LPP && lane + v * LPP < D / 4)
                                    ? __ldcg(reinterpret_cast<const float4*>(base + (c + k) * sstride + PARTIAL_O) + lane + v * LPP)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             float Mb = ml.x;
@@ -682,8 +682,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
             if (lane < LPP) {
 #pragma unroll
                 for (int v = 0; v < V4; ++v)
-                    reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane + v * LPP] =
-                        make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+                    if (lane + v * LPP < D / 4)
+                        reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * D)[lane + v * LPP] =
+                            make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
             }
         } else {   // O = O_hi + O_lo: float4 k and k + D/8 of the row
             float4* orow = reinterpret_cast<float4*>(P.a.O + ((size_t)h * M + i) * (D / 2));
@@ -779,7 +780,9 @@ __global__ void __launch_bounds__(256, 3) prefill_merge4_kernel(const __grid_con
     }
 }
 
-bool prefill_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool prefill_supported(int D) {
+    return D == 32 || D == 64 || D == 96 || D == 128 || D == 160 || D == 192 || D == 256;
+}
 
 template <int D>
 static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
@@ -841,7 +844,7 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
     // splits than prefix blocks, nor than the partials workspace holds.
     const int nbp = (a.N + PF_BLOCK - 1) / PF_BLOCK;
     const int nb = nbp + (a.S_suf + PF_BLOCK - 1) / PF_BLOCK;
-    const int per_sm = D == 256 ? PCfg<256>::CTAS_PER_SM : PCfg<128>::CTAS_PER_SM;
+    const int per_sm = D > 128 ? PCfg<256>::CTAS_PER_SM : PCfg<128>::CTAS_PER_SM;   // 512 TMEM columns above 128
     const int slots = per_sm * sms;
     int ns = 1;
     double best = 1e30;
@@ -855,9 +858,16 @@ cudaError_t launch_prefill(const PrefillParams& a, const WorkGroup* grp, int n_g
         }
     }
     P.n_split = ns;
-    if (D == 64) return launch_prefill_t<64>(P, st);
-    if (D == 128) return launch_prefill_t<128>(P, st);
-    if (D == 256) return launch_prefill_t<256>(P, st);
+    switch (D) {
+        case 32: return launch_prefill_t<32>(P, st);
+        case 64: return launch_prefill_t<64>(P, st);
+        case 96: return launch_prefill_t<96>(P, st);
+        case 128: return launch_prefill_t<128>(P, st);
+        case 160: return launch_prefill_t<160>(P, st);
+        case 192: return launch_prefill_t<192>(P, st);
+        case 256: return launch_prefill_t<256>(P, st);
+        default: break;
+    }
     return cudaErrorInvalidValue;
 }
 

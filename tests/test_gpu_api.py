@@ -47,14 +47,18 @@ def test_argument_errors_before_launch():
         c.query("e", 0, Q, top_k=10)
     assert e.value.code == binding.EUNSUPPORTED
     with pytest.raises(binding.PckError) as e:
-        c.query("e", 0, Q, fa_window=128)
-    assert e.value.code == binding.EUNSUPPORTED
+        c.query("e", 0, Q, fa_window=-3)
+    assert e.value.code == binding.EINVAL
     with pytest.raises(binding.PckError) as e:
         c.query("e", 0, Q, head_map=[0, 1, 2, 0])
     assert e.value.code == binding.EINVAL
-    K96 = torch.zeros((1, 8, 96), dtype=torch.float16, device="cuda")
+    K80 = torch.zeros((1, 8, 80), dtype=torch.float16, device="cuda")
     with pytest.raises(binding.PckError) as e:
-        c.store("e", 1, K96, K96)
+        c.store("e", 1, K80, K80)
+    assert e.value.code == binding.EUNSUPPORTED
+    K96 = torch.zeros((1, 8, 96), dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.PckError) as e:   # 96 has fp16 kernels only
+        c.store("e", 1, K96, K96, fmt=binding.FMT_MLX4G32)
     assert e.value.code == binding.EUNSUPPORTED
     Q128 = dev(synth.gen_q(2, 4, 1, 128))
     with pytest.raises(binding.PckError) as e:
