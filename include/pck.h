@@ -243,7 +243,7 @@ int pck_dequantize_mlx4g32(const void *records, int64_t N, int H_kv, int D, int 
  * K_rec, V_rec: device token-major records [N, rec] as in pck_store_records. Q: device [H_q, D];
  * O: device fp32 [H_q, D]; LSE: device fp32 [H_q] or NULL; K_suf/V_suf: device fp16
  * [H_kv, S_suf, D] or NULL when S_suf == 0. Limits: H_kv * ceil(N/16) * 20*D bytes of resident
- * tiles <= 16 MiB, D in {64, 128, 256}; larger inputs return PCK_EUNSUPPORTED before any
+ * tiles <= 16 MiB, D in {64, 128, 192, 256}; larger inputs return PCK_EUNSUPPORTED before any
  * launch. The first call on a device (or the first pck_noalloc_status there) looks up the
  * scratch addresses and the kernels' occupancy: make it before any stream capture. All calls
  * share the scratch: calls that overlap on the GPU (other streams or host threads) race and
