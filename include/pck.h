@@ -53,9 +53,10 @@ extern "C" {
 #define PCK_DT_F32       0
 #define PCK_DT_F16       1
 
-/* Head dimensions with kernels: fp16 slots 32, 64, 96, 128, 160, 192, 256 (M = 1 and M > 1);
- * mlx4g32 slots 64, 128, 192, 256 (M > 1: 64, 128); sparse forms 64, 128, 256. D = 512 (listed by
- * the pages) has none. More than 8 q heads per kv head are split into work groups. */
+/* Head dimensions with kernels: fp16 slots 32, 64, 96, 128, 160, 192, 256 (M = 1 and M > 1) and
+ * 512 (M = 1 only: M > 1 returns PCK_EUNSUPPORTED); mlx4g32 slots 64, 128, 192, 256 (M > 1: 64,
+ * 128); QUERY_SPARSE_AUTO(_FUSED) 64, 128, 256; QUERY_SPARSE every fp16 slot. More than 8 q heads
+ * per kv head (4 at D = 512) are split into work groups, each of which reads the kv head. */
 #define PCK_MAX_BATCH    64   /* descriptors per pck_query_batch call */
 #define PCK_MAX_HEADS    64   /* H_q and H_kv limit */
 

@@ -61,8 +61,8 @@ struct pck_ctx {
     uint8_t* suf_ws = nullptr;
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
-    DecodeLaunchInfo dinfo[2][14];   // [format][head dimension x column blocks]
-    bool dinfo_ok[2][14] = {};
+    DecodeLaunchInfo dinfo[2][16];   // [format][head dimension x column blocks]
+    bool dinfo_ok[2][16] = {};
 };
 
 namespace {
@@ -101,12 +101,17 @@ int d_index(int D) {
         case 128: return 3;
         case 160: return 4;
         case 192: return 5;
-        default: return 6;
+        case 256: return 6;
+        default: return 7;
     }
 }
 
+// q heads per work group: D = 512 keeps one column block of 4 heads (its O accumulators fill a
+// lane's registers), so a kv head with more q heads is read once per 4 of them.
+int d_gmax(int D) { return D >= 512 ? 4 : GMAX; }
+
 const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D, int ncb) {
-    const int i = d_index(D) + 7 * (ncb - 1);
+    const int i = d_index(D) + 8 * (ncb - 1);
     if (!c->dinfo_ok[fmt][i]) {
         c->dinfo[fmt][i] = decode_launch_info(fmt, D, ncb);
         c->dinfo_ok[fmt][i] = true;
@@ -182,9 +187,9 @@ int check_async(pck_ctx* c) {
     return PCK_OK;
 }
 
-// q heads grouped by kv head, at most GMAX per work group.
+// q heads grouped by kv head, at most gmax (<= GMAX) per work group.
 int build_groups(pck_ctx* c, int H_q, int H_kv, const int32_t* head_map, WorkGroup* grp, int* n_groups,
-                 int8_t* hm_out, int* max_nq) {
+                 int8_t* hm_out, int* max_nq, int gmax = GMAX) {
     if (H_q < 1 || H_kv < 1 || H_q > PCK_MAX_HEADS || H_kv > PCK_MAX_HEADS)
         return fail(c, PCK_EINVAL, "H_q=%d H_kv=%d out of range [1, %d]", H_q, H_kv, PCK_MAX_HEADS);
     int hm[PCK_MAX_HEADS];
@@ -204,10 +209,10 @@ int build_groups(pck_ctx* c, int H_q, int H_kv, const int32_t* head_map, WorkGro
         for (int h = 0; h < H_q; ++h) {
             if (hm[h] != g) continue;
             cur.qh[cur.nq++] = static_cast<int8_t>(h);
-            if (cur.nq == GMAX) {
+            if (cur.nq == gmax) {
                 if (n == MAX_GROUPS) return fail(c, PCK_EUNSUPPORTED, "too many work groups");
                 grp[n++] = cur;
-                mx = GMAX;
+                mx = gmax;
                 cur = WorkGroup{g, 0, {-1, -1, -1, -1, -1, -1, -1, -1}};
             }
         }
@@ -361,7 +366,7 @@ int pck_store(pck_ctx* c, const char* sid, int layer, int H_kv, int N, int D, in
     if (H_kv < 1 || H_kv > PCK_MAX_HEADS || N < 1) return fail(c, PCK_EINVAL, "bad H_kv=%d or N=%d", H_kv, N);
     if (fmt != PCK_FMT_FP16 && fmt != PCK_FMT_MLX4G32) return fail(c, PCK_EINVAL, "fmt=%d", fmt);
     if (!d_ok(D, fmt))
-        return fail(c, PCK_EUNSUPPORTED, "D=%d (fp16 slots: 32, 64, 96, 128, 160, 192, 256; mlx4g32: 64, 128, 192, 256)", D);
+        return fail(c, PCK_EUNSUPPORTED, "D=%d (fp16 slots: 32, 64, 96, 128, 160, 192, 256, 512; mlx4g32: 64, 128, 192, 256)", D);
     if (!dtype_ok(src_dtype)) return fail(c, PCK_EINVAL, "src_dtype=%d", src_dtype);
     if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) & 15)
         return fail(c, PCK_EINVAL, "K/V must be 16-byte aligned");
@@ -522,7 +527,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
         return fail(c, PCK_EINVAL, "H_kv=%d but the slot holds H_kv=%d", H_kv_arg, s->H_kv);
     WorkGroup grp[MAX_GROUPS];
     int n_groups = 0;
-    rc = build_groups(c, H_q, s->H_kv, head_map, grp, &n_groups, nullptr, nullptr);
+    rc = build_groups(c, H_q, s->H_kv, head_map, grp, &n_groups, nullptr, nullptr, d_gmax(D));
     if (rc != PCK_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M == 1) {
@@ -761,7 +766,7 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
     }
     WorkGroup grp[MAX_GROUPS];
     int n_groups = 0;
-    int rc = build_groups(c, H_q, H_kv, head_map, grp, &n_groups, nullptr, nullptr);
+    int rc = build_groups(c, H_q, H_kv, head_map, grp, &n_groups, nullptr, nullptr, d_gmax(D));
     if (rc != PCK_OK) return rc;
     rc = run_decode(c, fmt, D, H_q, H_kv, S_suf, q_dtype == PCK_DT_F16, grp, n_groups, ds, n, 0, 0, 0, nullptr,
                     static_cast<cudaStream_t>(stream));

@@ -51,9 +51,15 @@ struct DCfg {
     static constexpr int TB = tile_bytes(FMT, D);
     static constexpr int TPS = FMT == FMT_FP16 ? (D == 32 ? 4 : (D == 64 ? 2 : 1)) : (D == 64 ? 4 : (D == 128 ? 4 : 1));
     static constexpr int STAGE = TPS * TB;
-    static constexpr int NSTAGE = FMT == FMT_FP16 ? 3 : 2;
+    // D = 512 (fp16): a 32 KB tile per stage, so one stage per warp; four warps' single stages
+    // still keep ~100 KB per SM in flight
+    static constexpr int NSTAGE = FMT == FMT_FP16 ? (D >= 512 ? 1 : 3) : 2;
     static constexpr int RING = NSTAGE * STAGE;
-    static constexpr int SMEM = DECODE_WARPS * RING + DECODE_WARPS * NSTAGE * 8;
+    // D = 512 (fp16): q's B fragments live in shared memory (KS x 32 lanes x 8 bytes per warp), so
+    // that the 128 O accumulators of a lane fit in its registers
+    static constexpr bool QS = FMT == FMT_FP16 && D >= 512;
+    static constexpr int QBYTES = QS ? (D / 16) * 256 : 0;
+    static constexpr int SMEM = DECODE_WARPS * RING + DECODE_WARPS * NSTAGE * 8 + DECODE_WARPS * QBYTES;
 };
 
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -70,7 +76,10 @@ constexpr float Q_LIMIT = 65504.0f;
 template <int D, int NCB>
 struct F16State {
     static constexpr int KS = D / 16;
-    uint32_t qb[NCB][KS][2];   // B fragments of the item's q (tau*log2e prescaled), hi or lo part
+    static constexpr bool QS = D >= 512;   // q fragments in shared memory (one column block)
+    static_assert(!QS || NCB == 1, "D = 512 takes at most 4 q heads per work group");
+    uint32_t qb[NCB][QS ? 1 : KS][2];   // B fragments of the item's q (tau*log2e prescaled), hi or lo part
+    uint32_t qsm;              // QS: shared-memory address of the warp's q fragments [KS][32 lanes][2]
     float oacc[NCB][KS][4];    // O^T m-tile mt: d = 16mt + l/4 in [0..1], d + 8 in [2..3]; columns
                                // 2q, 2q+1 = (hi, lo) of head cb*4 + q
     float m_ref[NCB];
@@ -109,8 +118,16 @@ __device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const Decod
                 bad |= !(fabsf(x0) < Q_LIMIT) || !(fabsf(x1) < Q_LIMIT);
                 uint32_t hi, lo;
                 split_hi_lo(x0, x1, hi, lo);
-                st.qb[cb][s][r] = part ? lo : hi;
+                if constexpr (F16State<D, NCB>::QS) xq[cb][s][r].x = __uint_as_float(part ? lo : hi);
+                else st.qb[cb][s][r] = part ? lo : hi;
             }
+        if constexpr (F16State<D, NCB>::QS) {   // each lane reads back only its own entries
+#pragma unroll
+            for (int s = 0; s < KS; ++s)
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(st.qsm + (s * 32 + lane) * 8),
+                             "r"(__float_as_uint(xq[cb][s][0].x)), "r"(__float_as_uint(xq[cb][s][1].x))
+                             : "memory");
+        }
         st.m_ref[cb] = -INFINITY;
         st.l_part[cb] = 0.f;
 #pragma unroll
@@ -180,8 +197,14 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
     for (int s = 0; s < KS; ++s) {
         uint32_t a[4];
         src.ka(s, a);
+        if constexpr (F16State<D, NCB>::QS) {
+            uint32_t b0, b1;
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(st.qsm + (s * 32 + lane) * 8) : "memory");
+            mma16816(acc[0], a, b0, b1);
+        } else {
 #pragma unroll
-        for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
+            for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
+        }
     }
     float z[NCB][2];
 #pragma unroll
@@ -598,7 +621,8 @@ __device__ void merge_item_head(const DecodeParams& p, int item, int h, int lane
     constexpr int LPP = F4 >= 32 ? 32 : (F4 > 16 ? 32 : (F4 > 8 ? 16 : 8));   // lanes per piece (a power of 2)
     constexpr int PPS = 32 / LPP;                  // pieces per warp-wide load
     constexpr int V4 = (F4 + LPP - 1) / LPP;       // float4 per lane per piece
-    constexpr int NB = 32 / PPS < 16 ? 32 / PPS : 16;   // warp-wide loads per batch
+    constexpr int NB0 = 32 / PPS < 16 ? 32 / PPS : 16;
+    constexpr int NB = V4 > 2 ? NB0 * 2 / V4 : NB0;     // warp-wide loads per batch (<= 32 float4 per lane)
     constexpr int BP = NB * PPS;                   // pieces per batch (<= 32: one lane per piece's (m, l))
     const int sub = lane / LPP, dl = lane % LPP;
     float M = -INFINITY, L = 0.f;                  // L: this lane's share (lanes over pieces)
@@ -894,7 +918,7 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
 // ---------------------------------------------------------------- workers
 
 template <int FMT, int D, int NCB>
-__device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars) {
+__device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars, uint8_t* qarea) {
     using C = DCfg<FMT, D>;
     using StateT = std::conditional_t<FMT == FMT_FP16, F16State<D, NCB>, I4State<D, NCB>>;
     Cursor cons;
@@ -951,6 +975,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     }
 
     StateT st;
+    if constexpr (FMT == FMT_FP16) st.qsm = smem_u32(qarea);
     int cur_item = -1;
     int stage = 0;
     uint32_t phase = 0;
@@ -1008,7 +1033,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
 }
 
 template <int D, int NCB>
-__device__ void suffix_worker(const DecodeParams& p, int sidx, int lane) {
+__device__ void suffix_worker(const DecodeParams& p, int sidx, int lane, uint8_t* qarea) {
     const int n_items = p.n_desc * p.n_groups;
     const int item = sidx / p.n_suf, k = sidx - item * p.n_suf;
     if (item >= n_items) return;
@@ -1017,6 +1042,7 @@ __device__ void suffix_worker(const DecodeParams& p, int sidx, int lane) {
     const WorkGroup& wg = p.grp[grp];
     // The suffix is fp16 whatever the prefix format: fp16-style q fragments (no 1/16 factor).
     F16State<D, NCB> st;
+    st.qsm = smem_u32(qarea);
     start_item_f16<D, NCB>(st, p, ds, wg, lane);
     const int t0 = 16 * k;
     GlobalF16Tile<D> tl{ds.Ksuf + (size_t)wg.g * p.S_suf * D, ds.Vsuf + (size_t)wg.g * p.S_suf * D, t0, p.S_suf, lane};
@@ -1043,10 +1069,11 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __gr
     const int gw = warp * gridDim.x + blockIdx.x;
     uint8_t* ring = smem + warp * C::RING;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * C::RING) + warp * C::NSTAGE;
+    uint8_t* qarea = smem + DECODE_WARPS * C::RING + DECODE_WARPS * C::NSTAGE * 8 + warp * C::QBYTES;
     if (gw < p.n_workers) {
-        prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars);
+        prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars, qarea);
     } else if (p.n_suf > 0) {
-        suffix_worker<D, NCB>(p, gw - p.n_workers, lane);
+        suffix_worker<D, NCB>(p, gw - p.n_workers, lane, qarea);
     }
 }
 
@@ -1103,13 +1130,16 @@ DecodeLaunchInfo info_t() {
 }
 
 // Launch and occupancy of one (format, D) pair; instantiated by the translation units that own D.
+// D = 512 has one column block only: its work groups hold at most 4 q heads.
 template <int FMT, int D>
 cudaError_t launch_d(const DecodeParams& p, int ncb, int n_ctas, cudaStream_t st) {
-    return ncb == 1 ? launch_t<FMT, D, 1>(p, n_ctas, st) : launch_t<FMT, D, 2>(p, n_ctas, st);
+    if constexpr (D >= 512) return ncb == 1 ? launch_t<FMT, D, 1>(p, n_ctas, st) : cudaErrorInvalidValue;
+    else return ncb == 1 ? launch_t<FMT, D, 1>(p, n_ctas, st) : launch_t<FMT, D, 2>(p, n_ctas, st);
 }
 template <int FMT, int D>
 DecodeLaunchInfo info_d(int ncb) {
-    return ncb == 1 ? info_t<FMT, D, 1>() : info_t<FMT, D, 2>();
+    if constexpr (D >= 512) return info_t<FMT, D, 1>();
+    else return ncb == 1 ? info_t<FMT, D, 1>() : info_t<FMT, D, 2>();
 }
 
 }  // namespace pck

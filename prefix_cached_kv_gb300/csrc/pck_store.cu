@@ -142,11 +142,11 @@ __device__ __forceinline__ void write_fp16_tile(const __half (&sm)[2][TILE_TOK][
 
 // One CTA per (16-token tile j, kv head g): K and V rows t0..t0+15 are loaded coalesced into
 // shared memory (zeros past N), then written in the resident layout of head dimension DS >= D
-// (columns D .. DS-1 zero: the [hi | lo] form of fp16 values, whose lo parts are 0).
-template <typename SrcT>
+// (columns D .. DS-1 zero: the [hi | lo] form of fp16 values, whose lo parts are 0). MAXD >= DS
+// sizes the staging (256, or 512 for the widest heads, which halves the CTAs an SM holds).
+template <typename SrcT, int MAXD>
 __global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
                                                             int N, int D, int DS, int ntiles, uint4* __restrict__ out) {
-    constexpr int MAXD = 256;
     __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
     const int j = blockIdx.x, g = blockIdx.y;
     const int t0 = j * TILE_TOK;
@@ -182,12 +182,12 @@ __global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restri
 // head head_map[h] are read from the resident fp16 slot (K: 16 bytes of 8 d per token and d
 // chunk; V: single values from the transposed tiles) into shared memory and written as tile j of
 // head h's compact slot: K region of ceil(counts[h] / 16) tiles, then its V region, at
-// out + h * head_stride bytes.
+// out + h * head_stride bytes. MAXD >= D sizes the staging.
+template <int MAXD>
 __global__ void __launch_bounds__(128) gather_fp16_kernel(const uint8_t* __restrict__ tiles, int ntiles, int D,
                                                           const int* __restrict__ idx, const int* __restrict__ counts,
                                                           const int8_t* __restrict__ head_map, int kmax,
                                                           size_t head_stride, uint8_t* __restrict__ out) {
-    constexpr int MAXD = 256;
     __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
     const int j = blockIdx.x, h = blockIdx.y;
     const int cnt = counts[h];
@@ -427,23 +427,31 @@ cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int 
                                  void* out, cudaStream_t st, int sms, int DS) {
     (void)sms;
     if (DS == 0) DS = D;
-    if (DS > 256 || D % 8 != 0 || DS % 8 != 0 || DS < D) return cudaErrorInvalidValue;
+    if (DS > 512 || D % 8 != 0 || DS % 8 != 0 || DS < D) return cudaErrorInvalidValue;
     const dim3 grid(ntiles, H_kv);
-    if (src_f16)
-        relayout_fp16_kernel<__half><<<grid, 128, 0, st>>>(static_cast<const __half*>(K), static_cast<const __half*>(V),
-                                                           N, D, DS, ntiles, static_cast<uint4*>(out));
-    else
-        relayout_fp16_kernel<float><<<grid, 128, 0, st>>>(static_cast<const float*>(K), static_cast<const float*>(V),
-                                                          N, D, DS, ntiles, static_cast<uint4*>(out));
+    const __half* kh = static_cast<const __half*>(K);
+    const __half* vh = static_cast<const __half*>(V);
+    const float* kf = static_cast<const float*>(K);
+    const float* vf = static_cast<const float*>(V);
+    uint4* o = static_cast<uint4*>(out);
+    if (DS <= 256) {
+        if (src_f16) relayout_fp16_kernel<__half, 256><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o);
+        else relayout_fp16_kernel<float, 256><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o);
+    } else {
+        if (src_f16) relayout_fp16_kernel<__half, 512><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o);
+        else relayout_fp16_kernel<float, 512><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_fp16(const void* tiles, int ntiles, int D, const int* idx, const int* counts,
                                const int8_t* head_map, int H_q, int kmax, size_t head_stride, void* out, cudaStream_t st) {
-    if (D > 256 || D % 16 != 0) return cudaErrorInvalidValue;
+    if (D > 512 || D % 16 != 0) return cudaErrorInvalidValue;
     const dim3 grid((kmax + TILE_TOK - 1) / TILE_TOK, H_q);
-    gather_fp16_kernel<<<grid, 128, 0, st>>>(static_cast<const uint8_t*>(tiles), ntiles, D, idx, counts, head_map, kmax,
-                                             head_stride, static_cast<uint8_t*>(out));
+    const uint8_t* t = static_cast<const uint8_t*>(tiles);
+    uint8_t* o = static_cast<uint8_t*>(out);
+    if (D <= 256) gather_fp16_kernel<256><<<grid, 128, 0, st>>>(t, ntiles, D, idx, counts, head_map, kmax, head_stride, o);
+    else gather_fp16_kernel<512><<<grid, 128, 0, st>>>(t, ntiles, D, idx, counts, head_map, kmax, head_stride, o);
     return cudaGetLastError();
 }
 

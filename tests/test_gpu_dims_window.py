@@ -1,6 +1,6 @@
-"""The head dimensions beyond 64/128/256 (fp16 M=1 decode and batched-Q at D = 32, 96, 160, 192;
-mlx4g32 M=1 at D = 192) and the attention window (fa_window, M = 1) on the GPU, against the
-oracle."""
+"""The head dimensions beyond 64/128/256 (fp16 M=1 decode at D = 32, 96, 160, 192, 512 and
+batched-Q at D = 32, 96, 160, 192; mlx4g32 M=1 at D = 192) and the attention window (fa_window,
+M = 1) on the GPU, against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -39,6 +39,11 @@ DIM_CASES = [
     (16, 2, 400, 192, 33, 0),
     (32, 8, 1000, 192, 16, 1),     # mlx4g32 at D = 192
     (16, 2, 257, 192, 5, 1),
+    (8, 8, 1000, 512, 0, 0),       # D = 512: q fragments in shared memory, one ring stage
+    (32, 8, 777, 512, 16, 0),      # GQA 4: one work group per kv head
+    (16, 2, 500, 512, 20, 0),      # GQA 8: two work groups of 4 per kv head
+    (12, 1, 2049, 512, 3, 0),      # GQA 12: three work groups, ragged tail
+    (2, 1, 1, 512, 0, 0),          # N = 1
 ]
 
 
@@ -61,6 +66,73 @@ def test_decode_other_head_dims(ctx, H_q, H_kv, N, D, S, fmt):
     ctx.sync()
     assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"D={D} {(H_q, H_kv, N, S, fmt)}")
     ctx.drop(sid)
+
+
+def test_decode_d512_fp16_q_and_custom_head_map(ctx):
+    """D = 512 with fp16 Q and q heads of a kv head that are not adjacent (5 of them: groups of
+    4 and 1)."""
+    H_q, H_kv, N, D, S = 10, 2, 640, 512, 9
+    K, V = synth.gen_kv(51, H_kv, N, D)
+    Q = synth.gen_q(51, H_q, 1, D, dtype=np.float16)
+    hm = np.array([h % 2 for h in range(H_q)], dtype=np.int32)
+    Ks, Vs = synth.gen_suffix(51, H_kv, S, D)
+    ctx.store("d512h", 0, dev(K), dev(V))
+    O, L = ctx.query_fused("d512h", 0, dev(Q), dev(Ks), dev(Vs), head_map=hm)
+    O_ref, L_ref = orc.prefix_query(Q, K, V, hm, Ks, Vs)
+    ctx.sync()
+    assert_close_o_lse(host(O), host(L), O_ref, L_ref, "D=512 fp16 Q, custom head_map")
+    ctx.drop("d512h")
+
+
+def test_decode_d512_batched(ctx):
+    """pck_query_batch at D = 512: 5 sessions of different lengths, GQA 8, with a suffix."""
+    H_q, H_kv, D, S = 16, 2, 512, 16
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs = [], []
+    for r, N in enumerate((1000, 3000, 17, 512, 1601)):
+        K, V = synth.gen_kv(90 + r, H_kv, N, D)
+        Q = synth.gen_q(90 + r, H_q, 1, D)
+        Ks, Vs = synth.gen_suffix(90 + r, H_kv, S, D)
+        ctx.store(f"d5b{r}", 0, dev(K), dev(V))
+        refs.append(orc.prefix_query(Q, K, V, hm, Ks, Vs))
+        descs.append(dict(sid=f"d5b{r}", layer=0, Q=dev(Q[:, 0]), O=torch.empty((H_q, D), device="cuda"),
+                          LSE=torch.empty((H_q,), device="cuda"), K_suf=dev(Ks), V_suf=dev(Vs)))
+    ctx.query_batch(descs, H_q, H_kv, D, S_suf=S)
+    ctx.sync()
+    for r, (O_ref, L_ref) in enumerate(refs):
+        assert_close_o_lse(host(descs[r]["O"]), host(descs[r]["LSE"]), O_ref[:, 0], L_ref[:, 0], f"D=512 batch {r}")
+        ctx.drop(f"d5b{r}")
+
+
+def test_d512_stress(ctx):
+    """Large logits, scores rising through prefix and suffix, and dominant keys at D = 512."""
+    for kind in ("q100", "monotone", "dominant_prefix", "dominant_suffix"):
+        Q, K, V, Ks, Vs = synth.gen_stress(kind, 512, 8, 2, 700, 512, 1, 16)
+        hm = synth.default_head_map(8, 2)
+        ctx.store("d5s", 0, dev(K), dev(V))
+        O, L = ctx.query_fused("d5s", 0, dev(Q), dev(Ks), dev(Vs))
+        O_ref, L_ref = orc.prefix_query(Q, K, V, hm, Ks, Vs)
+        ctx.sync()
+        assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"D=512 stress {kind}")
+    ctx.drop("d5s")
+
+
+def test_d512_rejections(ctx):
+    """D = 512 is built for fp16 slots at M = 1 only: M > 1, an mlx4g32 slot and the block-mean
+    sparse forms are refused before launch."""
+    from prefix_cached_kv_gb300 import binding
+    K, V = synth.gen_kv(4, 2, 300, 512)
+    ctx.store("d5r", 0, dev(K), dev(V))
+    with pytest.raises(binding.PckError) as e:
+        ctx.query("d5r", 0, dev(synth.gen_q(4, 4, 8, 512, dtype=np.float16)))
+    assert e.value.code == binding.EUNSUPPORTED
+    with pytest.raises(binding.PckError) as e:
+        ctx.query_sparse_auto("d5r", 0, dev(synth.gen_q(4, 4, 1, 512)[:, 0]), 64, 2, 2)
+    assert e.value.code == binding.EUNSUPPORTED
+    with pytest.raises(binding.PckError) as e:
+        ctx.store("d5q", 0, dev(K), dev(V), fmt=1)
+    assert e.value.code == binding.EUNSUPPORTED
+    ctx.drop("d5r")
 
 
 def test_decode_other_head_dims_batched(ctx):
@@ -134,6 +206,7 @@ WINDOW_SHAPES = [
     (8, 2, 777, 128, 0, 1),
     (16, 4, 300, 256, 40, 0),
     (8, 2, 500, 96, 24, 0),
+    (8, 2, 500, 512, 24, 0),
 ]
 
 

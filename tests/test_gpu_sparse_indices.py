@@ -36,6 +36,8 @@ def _lists(seed, H_q, N, K_max, min_count=1):
     (4, 1, 700, 256, 97, False, None),
     (3, 1, 50, 64, 1, False, None),           # a single token each
     (2, 2, 17, 64, 17, True, None),           # every token of a ragged prefix
+    (4, 2, 900, 512, 130, False, None),       # the widest head dim
+    (3, 1, 300, 96, 33, True, None),
 ])
 def test_query_sparse_matches_oracle(ctx, H_q, H_kv, N, D, K_max, q16, hm):
     K, V = synth.gen_kv(N + D, H_kv, N, D)
