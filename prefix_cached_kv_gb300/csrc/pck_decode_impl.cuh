@@ -710,6 +710,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     const int lane = threadIdx.x & 31;
     const int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int item = wi / GMAX, h = wi - item * GMAX;
+    // the next kernel of the stream may be scheduled now: a decode then sets up its workers from
+    // its launch parameters while this merge runs, and waits for it before reading memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool live = wi < p.n_desc * p.n_groups * GMAX && h < p.grp[item % p.n_groups].nq;   // warp-uniform
     int w0 = 0, npref = 0;
     if (live && !p.sparse) item_range(p, item, w0, npref);
@@ -917,11 +920,21 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, Cursor& c, Ch
 
 // ---------------------------------------------------------------- workers
 
+// This grid may be launched before the previous kernel of the stream has finished (programmatic
+// dependence): wait for it before reading anything it may have written, then let the merge
+// kernel be scheduled (it still waits for this whole grid before reading a partial).
+__device__ __forceinline__ void grid_dep_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int FMT, int D, int NCB>
 __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* ring, uint64_t* bars, uint8_t* qarea) {
     using C = DCfg<FMT, D>;
     using StateT = std::conditional_t<FMT == FMT_FP16, F16State<D, NCB>, I4State<D, NCB>>;
     Cursor cons;
+    const bool sparse = FMT == FMT_FP16 && p.sparse;
+    if (sparse) grid_dep_wait_then_release();   // the unit offsets come from the previous grid
     const int total = FMT == FMT_FP16 && p.sparse ? units_total(p) : p.total_tiles;
     if ((FMT == FMT_FP16 && p.sparse) || !p.aligned) {
         const int tpw = worker_units(p, total);
@@ -937,7 +950,10 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         cons.t = s0 + k * ps;
         cons.t_end = min(s0 + vt, cons.t + ps);
     }
-    if (cons.t >= cons.t_end) return;
+    if (cons.t >= cons.t_end) {
+        if (!sparse) grid_dep_wait_then_release();
+        return;
+    }
     cursor_seek<FMT, D>(p, cons);
     Cursor prod = cons;
 
@@ -948,6 +964,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         fence_mbar_init();
     }
     __syncwarp();
+    if (!sparse) grid_dep_wait_then_release();
 
     auto issue = [&](const Chunk& c, int s) {
         if (lane == 0) {
@@ -1057,12 +1074,6 @@ template <int FMT, int D, int NCB>
 __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<FMT, D>;
     extern __shared__ __align__(128) uint8_t smem[];
-    // the merge kernel (launched after this one with programmatic dependence) may be scheduled as
-    // this grid's CTAs retire; it still waits for the whole grid before reading any partial
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // this grid may itself be launched early (programmatic dependence on the previous kernel of
-    // the stream, e.g. the sparse selector): nothing is read before that kernel has completed
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // worker ids go round the CTAs first, so that the prefix workers (and the suffix warps after
     // them) spread evenly over the SMs however many of them have work
@@ -1072,8 +1083,9 @@ __global__ void __launch_bounds__(DECODE_WARPS * 32, 1) decode_kernel(const __gr
     uint8_t* qarea = smem + DECODE_WARPS * C::RING + DECODE_WARPS * C::NSTAGE * 8 + warp * C::QBYTES;
     if (gw < p.n_workers) {
         prefix_worker<FMT, D, NCB>(p, gw, lane, ring, bars, qarea);
-    } else if (p.n_suf > 0) {
-        suffix_worker<D, NCB>(p, gw - p.n_workers, lane, qarea);
+    } else {
+        grid_dep_wait_then_release();
+        if (p.n_suf > 0) suffix_worker<D, NCB>(p, gw - p.n_workers, lane, qarea);
     }
 }
 
