@@ -208,6 +208,50 @@ def test_sparse_batch_many_sessions_uneven_items(ctx):
         ctx.drop(f"spm{r}")
 
 
+def test_sparse_batch_in_a_cuda_graph(ctx):
+    """A batch of 9 sessions captured in a CUDA graph and replayed twice: the selector's
+    completion counter comes back to zero between replays, and every session matches the oracle
+    after each replay."""
+    H_q, H_kv, N, D, B, Kt, S = 4, 2, 2000, 128, 64, 3, 16
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs = [], []
+    for r in range(9):
+        seed = 700 + r
+        K, V = synth.gen_kv(seed, H_kv, N, D)
+        Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        sid = f"sph{r}"
+        ctx.store(sid, 0, dev(K), dev(V))
+        ctx.build_block_means(sid, 0, B)
+        descs.append(dict(sid=sid, layer=0, Q=dev(Q), O=torch.empty((H_q, D), device="cuda"),
+                          LSE=torch.empty((H_q,), device="cuda"), K_suf=dev(Ks), V_suf=dev(Vs),
+                          idx=torch.empty((H_q, Kt), dtype=torch.int32, device="cuda")))
+        refs.append(orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs))
+    call = ctx.sparse_batch_caller(descs, H_q, H_kv, D, B, Kt, S_suf=S)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=st):
+        call()
+    torch.cuda.current_stream().wait_stream(st)
+    for _ in range(2):
+        for d in descs:
+            d["O"].fill_(float("nan"))
+            d["idx"].fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        ctx.sync()
+        for r, (d, (O_ref, L_ref, idx_ref, scores)) in enumerate(zip(descs, refs)):
+            _check_idx(host(d["idx"]), scores, Kt)
+            near = orc.topk_margin(scores, Kt) < TIE_EPS
+            assert_close_o_lse(host(d["O"])[~near], host(d["LSE"])[~near], O_ref[~near], L_ref[~near], f"graph {r}")
+    del g
+    for r in range(9):
+        ctx.drop(f"sph{r}")
+
+
 @pytest.mark.parametrize("H_q,H_kv,hm", [
     (6, 3, [2, 0, 1, 1, 0, 2]),         # q heads of a kv head not adjacent
     (4, 2, [1, 1, 1, 1]),               # kv head 0 has no q heads: nothing scored or selected there
