@@ -205,9 +205,12 @@ int pck_query_batch(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, i
 /* n independent ATTEND.PREFIX.QUERY_SPARSE_AUTO(_FUSED) queries (page "ATTEND.* and
  * ATTEND.PREFIX.*", section "Wire forms"; batching them is this library's addition, as for
  * pck_query_batch) of one shape (H_q, H_kv, D, B, K_top, S_suf, q_dtype, head_map) over fp16
- * slots of the same N: the block scores of all of them run in one scoring launch, their top-K
- * selections in one selection launch, and their gathers (+ suffixes) in one split-K decode and
- * its merge (four launches whatever n). Each query is as pck_query_sparse_auto_fused
+ * slots of the same N. A batch of at least 32 work items (query x group of up to 8 q heads of a
+ * kv head, 4 at D = 256) over at most 1024 blocks per kv head, with 16-byte aligned suffixes,
+ * runs as ONE kernel with a CTA per work item (scores, top-K, union, gather decode of the union
+ * and the suffix, merge); otherwise the block scores of all queries run in one scoring launch,
+ * their top-K selections in one selection launch, and their gathers (+ suffixes) in one split-K
+ * decode and its merge (four launches). Each query is as pck_query_sparse_auto_fused
  * (S_suf > 0) or pck_query_sparse_auto (S_suf == 0) would compute it alone.
  * 1 <= n <= PCK_MAX_BATCH. Errors: EINVAL, EUNSUPPORTED (slots of different N, B not a multiple
  * of 16, K_top > 64, fa_window), MISS / COLDMISS for an absent slot. */

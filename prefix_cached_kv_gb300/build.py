@@ -17,8 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpck.so")
-SOURCES = ["pck_store.cu", "pck_decode.cu", "pck_decode_xd.cu", "pck_sparse.cu", "pck_prefill.cu", "pck_api.cu",
-           "pck_noalloc.cu"]
+SOURCES = ["pck_store.cu", "pck_decode.cu", "pck_decode_xd.cu", "pck_sparse.cu", "pck_sparse_fused.cu",
+           "pck_prefill.cu", "pck_api.cu", "pck_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

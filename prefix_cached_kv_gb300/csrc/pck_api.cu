@@ -660,6 +660,51 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
         int rc = pck_build_block_means(c, q[i].sid, q[i].layer, B, stream);
         if (rc != PCK_OK) return rc;
     }
+    bool suf_aligned = true;   // the fused kernel copies suffix rows with the bulk-copy engine
+    for (int i = 0; i < n && S_suf > 0; ++i)
+        suf_aligned = suf_aligned && !((reinterpret_cast<uintptr_t>(q[i].K_suf) | reinterpret_cast<uintptr_t>(q[i].V_suf)) & 15);
+    // The fused kernel runs a CTA per work item; with few items its per-CTA streaming rate bounds
+    // the call, and the four-kernel form (which spreads every phase over all SMs) is faster.
+    constexpr int FUSED_MIN_ITEMS = 32;
+    int n_items_est = 0;
+    {
+        int hm_cnt[PCK_MAX_HEADS] = {};
+        for (int h = 0; h < H_q; ++h) {
+            const int gk = head_map ? head_map[h] : (H_q % H_kv ? 0 : h / (H_q / H_kv));
+            if (gk >= 0 && gk < PCK_MAX_HEADS) ++hm_cnt[gk];
+        }
+        const int gm = sparse_fused_gmax(D);
+        for (int gk = 0; gk < H_kv && gk < PCK_MAX_HEADS; ++gk) n_items_est += n * ((hm_cnt[gk] + gm - 1) / gm);
+    }
+    if (suf_aligned && n_items_est >= FUSED_MIN_ITEMS && sparse_fused_ok(D, nb, K_eff)) {
+        // the whole query in one kernel, a CTA per work item
+        static thread_local FusedSparseParams fp;
+        std::memset(&fp, 0, sizeof fp);
+        int n_groups = 0, max_nq = 0;
+        int rc = build_groups(c, H_q, H_kv, head_map, fp.grp, &n_groups, nullptr, &max_nq, sparse_fused_gmax(D));
+        if (rc != PCK_OK) return rc;
+        fp.n_sess = n;
+        fp.n_groups = n_groups;
+        fp.H_q = H_q;
+        fp.D = D;
+        fp.N = slots[0]->N;
+        fp.ntiles = slots[0]->ntiles;
+        fp.nb = nb;
+        fp.tpb = B / 16;
+        fp.K_eff = K_eff;
+        fp.S_suf = S_suf;
+        fp.q_f16 = q_dtype == PCK_DT_F16;
+        fp.tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+        fp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+        fp.err = c->dev_err;
+        for (int i = 0; i < n; ++i)
+            fp.sess[i] = FusedSession{slots[i]->kmean[B], q[i].Q, slots[i]->tiles,
+                                      static_cast<const __half*>(q[i].K_suf), static_cast<const __half*>(q[i].V_suf),
+                                      q[i].O, q[i].LSE, q[i].idx_out};
+        const cudaError_t e = launch_sparse_fused(fp, max_nq, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "sparse launch");
+        return check_async(c);
+    }
     static thread_local SelectParams sp;
     std::memset(&sp, 0, sizeof sp);
     int n_groups = 0, max_nq = 0;

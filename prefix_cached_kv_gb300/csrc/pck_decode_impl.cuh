@@ -87,8 +87,9 @@ struct F16State {
 };
 
 // The item's q fragments: every load first (one round trip), then the hi / lo splits.
-template <int D, int NCB>
-__device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const DecodeParams& p, const DecodeDesc& ds,
+// (PP: any launch parameter block with q_f16, scale_log2 and err; DS: anything with Q)
+template <int D, int NCB, typename PP, typename DS>
+__device__ __forceinline__ void start_item_f16(F16State<D, NCB>& st, const PP& p, const DS& ds,
                                                const WorkGroup& wg, int lane) {
     constexpr int KS = D / 16;
     const int q = lane & 3, n = lane >> 2, hl = n >> 1, part = n & 1;
@@ -159,6 +160,25 @@ struct SmemF16Tile {
     }
 };
 
+// 16 rows of a dense suffix K_suf/V_suf [S_suf, D] copied as they are (row-major, 2 D bytes a
+// row) into shared memory: K fragments (tokens x d) by ldmatrix, V^T fragments (d x tokens) by
+// ldmatrix.trans of the same row-major 8 x 8 blocks.
+template <int D>
+struct SmemRowTile {
+    uint32_t kp, vp;   // shared-memory addresses of the K rows and the V rows
+    int lane;
+    __device__ __forceinline__ void ka(int s, uint32_t (&a)[4]) const {
+        const int j = lane >> 3;   // matrix j: tokens 8 (j & 1) .., d 16 s + 8 (j >> 1) ..
+        ldsm_x4(kp + ((j & 1) * 8 + (lane & 7)) * (2 * D) + (16 * s + 8 * (j >> 1)) * 2, a);
+    }
+    __device__ __forceinline__ void va(int mt, uint32_t (&a)[4]) const {
+        const int j = lane >> 3;   // matrix j: d 16 mt + 8 (j & 1) .., tokens 8 (j >> 1) ..
+        const uint32_t addr = vp + ((j >> 1) * 8 + (lane & 7)) * (2 * D) + (16 * mt + 8 * (j & 1)) * 2;
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(addr));
+    }
+};
+
 // Dense suffix K_suf/V_suf [S_suf, D] of one kv head, natural layout, read straight from global.
 template <int D>
 struct GlobalF16Tile {
@@ -189,10 +209,13 @@ template <int D, int NCB, typename Src>
 __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, int lane, int valid,
                                          uint32_t head_mask, int nq, int lo = 0) {
     constexpr int KS = D / 16;
+    // one column block over 8 or more k-steps: even and odd k-steps accumulate separately, which
+    // halves the chain of dependent MMAs a tile waits on
+    constexpr int NA = (KS >= 8 && NCB == 1) ? 2 : 1;
     const int q = lane & 3, t0 = lane >> 2;
-    float acc[NCB][4];
+    float acc[NCB * NA][4];
 #pragma unroll
-    for (int cb = 0; cb < NCB; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
+    for (int cb = 0; cb < NCB * NA; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
 #pragma unroll
     for (int s = 0; s < KS; ++s) {
         uint32_t a[4];
@@ -200,11 +223,17 @@ __device__ __forceinline__ void tile_f16(F16State<D, NCB>& st, const Src& src, i
         if constexpr (F16State<D, NCB>::QS) {
             uint32_t b0, b1;
             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(st.qsm + (s * 32 + lane) * 8) : "memory");
-            mma16816(acc[0], a, b0, b1);
+            mma16816(acc[s % NA], a, b0, b1);
+        } else if constexpr (NA == 2) {
+            mma16816(acc[s & 1], a, st.qb[0][s][0], st.qb[0][s][1]);
         } else {
 #pragma unroll
             for (int cb = 0; cb < NCB; ++cb) mma16816(acc[cb], a, st.qb[cb][s][0], st.qb[cb][s][1]);
         }
+    }
+    if constexpr (NA == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[0][i] += acc[1][i];
     }
     float z[NCB][2];
 #pragma unroll

@@ -94,6 +94,31 @@ struct SelectParams {
 };
 cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
 
+// The whole block-mean sparse query in one kernel (one CTA per (session, work group)): scores,
+// top-K and union in shared memory, gather decode of the union plus the dense suffix, and the
+// merge of the CTA's pieces. Work groups hold at most sparse_fused_gmax(D) q heads.
+struct FusedSession {
+    const float* kmean;      // [H_kv, nb, D]
+    const void* Q;           // [H_q, D]
+    const uint8_t* kv;       // resident fp16 slot
+    const __half* Ksuf;      // [H_kv, S_suf, D] or nullptr
+    const __half* Vsuf;
+    float* O;                // [H_q, D]
+    float* LSE;              // [H_q] or nullptr
+    int* idx_out;            // [H_q, K_eff] or nullptr
+};
+struct FusedSparseParams {
+    FusedSession sess[MAX_DESC];
+    WorkGroup grp[MAX_GROUPS];
+    int n_sess, n_groups, H_q, D, N, ntiles, nb, tpb, K_eff, S_suf, q_f16;
+    float tau;               // 1 / sqrt(D) (block scores)
+    float scale_log2;        // tau * log2(e) (attention)
+    int* err;
+};
+int sparse_fused_gmax(int D);
+bool sparse_fused_ok(int D, int nb, int K_eff);
+cudaError_t launch_sparse_fused(const FusedSparseParams& p, int max_nq, cudaStream_t st);
+
 // batched-Q tensor-core prefill (tcgen05)
 struct PrefillParams {
     const __half* Q;          // [H_q, M, D] (q_dup: [H_q, M, D/2])

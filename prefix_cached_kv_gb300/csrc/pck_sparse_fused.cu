@@ -1,0 +1,468 @@
+// pck_sparse_fused.cu -- the block-mean top-K sparse query ("ATTEND.* and ATTEND.PREFIX.*",
+// QUERY_SPARSE_AUTO(_FUSED)) as one kernel.
+//
+// One CTA per work item (session, group of q heads of one kv head g) runs every step of the
+// query in shared memory:
+//   1. scoring: each warp streams its own 8 KB slabs of the kv head's block means through its
+//      own ring of bulk copies and scores them for every q head of the group; the scores
+//      score[h, b] = tau * q_h . K_mean[g, b] stay in shared memory;
+//   2. selection: warp w takes the top-K of q heads w, w + W, ... (ties to the lower block),
+//      reports them sorted ascending, and the CTA forms the sorted union of the group's blocks
+//      with a mask of the q heads that chose each;
+//   3. gather decode: the union's resident 16-token tiles and the dense suffix's 16-row tiles
+//      (causal-free at M = 1; copied row-major, read by ldmatrix.trans for V) are split evenly
+//      over the warps, each streaming its tiles through its own ring with the split-K decode's
+//      tile step (each q head attends only to the blocks it chose);
+//   4. merge: the warps' partials [m, l, o] are combined by their LSE and O, LSE written.
+// Against the four-kernel form (scores, selection, gather decode, merge) this removes three
+// kernel boundaries and the round trips of the scores and unit offsets through global memory.
+// It needs the kv head's scores in shared memory (at most 1024 blocks) and K_top <= 64; larger
+// cases take the four-kernel form.
+#include "pck_decode_impl.cuh"
+#include "pck_select.cuh"
+
+namespace pck {
+
+namespace {
+
+constexpr int F_NBMAX = 1024;  // blocks per kv head whose scores fit in shared memory
+constexpr int F_KMAX = 64;     // K_top limit
+
+// Every warp streams its own copies: one warp's wait-and-reissue loop completes only a few
+// bulk copies per microsecond, and one warp per scheduler leaves the tile math's dependent
+// chains exposed, so a CTA runs as many warps as its rings fit in shared memory.
+template <int D, int NCB>
+struct FCfg {
+    static constexpr int W = D == 256 ? 6 : 8;                 // warps per CTA
+    static constexpr int HMAX = 4 * NCB;                       // q heads per group
+    static constexpr int SLAB = 8192 / (D * 4);                // blocks per scoring stage (8 KB)
+    static constexpr int SLAB_BYTES = SLAB * D * 4;
+    static constexpr int NSS = D == 256 ? 3 : 2;               // scoring stages per warp
+    static constexpr int SCORE_RING = W * NSS * SLAB_BYTES;
+    static constexpr int SCORES = HMAX * F_NBMAX * 4;
+    static constexpr int TB = 64 * D;                          // fp16 tile: K 32 D bytes, then V 32 D bytes
+    static constexpr int DST = D == 64 ? 4 : (D == 128 ? 3 : 2);   // decode ring stages per warp
+    static constexpr int DRING = W * DST * TB;
+    static constexpr int PART = W * HMAX * partial_stride(D) * 4;
+    static constexpr int A1 = SCORE_RING + SCORES;
+    static constexpr int REGION = A1 > DRING ? (A1 > PART ? A1 : PART) : (DRING > PART ? DRING : PART);
+    static constexpr int NBAR = W * NSS + W * DST;
+};
+
+template <int HMAX>
+struct FSel {
+    int picks[HMAX][F_KMAX];
+    int sorted[HMAX][F_KMAX];
+    uint64_t cand[HMAX][32];
+    int ublk[HMAX * F_KMAX];       // the union, ascending
+    int utile[HMAX * F_KMAX + 1];  // exclusive prefix of the union's tiles
+    uint8_t umask[HMAX * F_KMAX];
+    uint8_t first[HMAX * F_KMAX];
+    int nuniq, fail;
+};
+
+template <int D, int NCB>
+constexpr int fused_smem() {
+    using C = FCfg<D, NCB>;
+    return C::REGION + static_cast<int>(sizeof(FSel<C::HMAX>)) + C::NBAR * 8;
+}
+
+// Scores of blocks [b0, b0 + nbl) (nbl <= 8) of a stage for the group's q heads, 4 at a time:
+// lane products over 8 blocks x 4 heads summed by a reduce-scatter (lane l ends with block
+// l / 4, head l % 4), as in the scoring kernel of pck_sparse.cu.
+template <int D, int HMAX>
+__device__ __forceinline__ void fused_score(const float4 (&qv)[HMAX][D / 4 >= 32 ? D / 128 : 1], int nq, float tau,
+                                            const float* kslab, int nbl, float* sc, int b0, int lane) {
+    constexpr int F4 = D / 4;
+    constexpr int L4 = 8 * F4 / 32;
+    constexpr int QN = F4 >= 32 ? F4 / 32 : 1;
+    const float4* km = reinterpret_cast<const float4*>(kslab);
+#pragma unroll
+    for (int c4 = 0; c4 < HMAX / 4; ++c4) {
+        if (4 * c4 >= nq) break;
+        float acc[32];
+#pragma unroll
+        for (int v = 0; v < 32; ++v) acc[v] = 0.f;
+#pragma unroll
+        for (int k = 0; k < L4; ++k) {
+            const int e = lane + 32 * k;
+            const float4 kv = e / F4 < nbl ? km[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 q = qv[4 * c4 + j][F4 >= 32 ? k % QN : 0];
+                float x = kv.x * q.x;
+                x = fmaf(kv.y, q.y, x);
+                x = fmaf(kv.z, q.z, x);
+                x = fmaf(kv.w, q.w, x);
+                if constexpr (F4 >= 32) {
+                    acc[(k / (F4 / 32)) * 4 + j] += x;
+                } else {   // D = 64: lanes 0-15 hold block 2k, lanes 16-31 block 2k + 1
+                    const bool hi = lane >= 16;
+                    acc[(2 * k) * 4 + j] += hi ? 0.f : x;
+                    acc[(2 * k + 1) * 4 + j] += hi ? x : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < o; ++i) {
+                const float send = up ? acc[i] : acc[i + o];
+                const float keep = up ? acc[i + o] : acc[i];
+                acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        const int blk = lane >> 2, hl = 4 * c4 + (lane & 3);
+        if (hl < nq && blk < nbl) sc[hl * F_NBMAX + b0 + blk] = tau * acc[0];
+    }
+}
+
+template <int D, int NCB>
+__global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(const __grid_constant__ FusedSparseParams p) {
+    using C = FCfg<D, NCB>;
+    constexpr int FW = C::W;
+    constexpr int F_NSS = C::NSS;
+    constexpr int HMAX = C::HMAX;
+    constexpr int F4 = D / 4;
+    constexpr int QN = F4 >= 32 ? F4 / 32 : 1;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* regA = smem;
+    FSel<HMAX>& sm = *reinterpret_cast<FSel<HMAX>*>(smem + C::REGION);
+    const uint32_t bar0 = smem_u32(smem + C::REGION + sizeof(FSel<HMAX>));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int si = blockIdx.x / p.n_groups, grp = blockIdx.x - si * p.n_groups;
+    const FusedSession& ss = p.sess[si];
+    const WorkGroup& wg = p.grp[grp];
+    const int g = wg.g, nq = wg.nq;
+    auto sbar = [&](int s) { return bar0 + 8 * (warp * F_NSS + s); };
+    auto dbar = [&](int s) { return bar0 + 8 * (FW * F_NSS + warp * C::DST + s); };
+    if (tid == 0) {
+        for (int k = 0; k < C::NBAR; ++k) mbar_init(bar0 + 8 * k, 1);
+        fence_mbar_init();
+        sm.fail = 0;
+        sm.nuniq = 0;
+    }
+    __syncthreads();
+    // Q, the block means and the slot may come from the previous kernel of the stream
+    grid_dep_wait_then_release();
+
+    // ---------------------------------------------------------------- 1. scores
+    // Each warp streams its own slabs (w, w + FW, ...) through its own ring and scores them; the
+    // warps meet only once every score is in shared memory.
+    const int nb = p.nb;
+    constexpr int SLAB = C::SLAB;
+    const int nslabs = (nb + SLAB - 1) / SLAB;
+    const float* kmg = ss.kmean + (size_t)g * nb * D;
+    float* sc = reinterpret_cast<float*>(regA + C::SCORE_RING);   // [HMAX][F_NBMAX]
+    uint8_t* sring = regA + warp * F_NSS * C::SLAB_BYTES;
+    auto issue_slab = [&](int j, int st) {   // the warp's j-th slab (slab w + j FW) into stage st
+        const int b0 = (warp + j * FW) * SLAB;
+        const uint32_t bytes = static_cast<uint32_t>(min(SLAB, nb - b0)) * D * 4;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(sbar(st), bytes);
+            bulk_g2s(smem_u32(sring + st * C::SLAB_BYTES), kmg + (size_t)b0 * D, bytes, sbar(st));
+        }
+    };
+    const int mine = warp < nslabs ? (nslabs - warp + FW - 1) / FW : 0;   // slabs of this warp
+    for (int j = 0; j < min(F_NSS, mine); ++j) issue_slab(j, j);
+    float4 qv[HMAX][QN];   // the group's q heads (fp32), 4 per warp-wide score step
+#pragma unroll
+    for (int h = 0; h < HMAX; ++h)
+#pragma unroll
+        for (int i = 0; i < QN; ++i) {
+            const int d4 = F4 >= 32 ? lane + 32 * i : lane % F4;
+            if (h >= nq) {
+                qv[h][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (p.q_f16) {
+                const uint2 r = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(ss.Q) + (size_t)wg.qh[h] * D) + d4);
+                const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+                const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+                qv[h][i] = make_float4(x.x, x.y, y.x, y.y);
+            } else {
+                qv[h][i] = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ss.Q) + (size_t)wg.qh[h] * D) + d4);
+            }
+        }
+    for (int j = 0; j < mine; ++j) {
+        const int st = j % F_NSS;
+        if (!mbar_wait_bounded(sbar(st), (j / F_NSS) & 1)) {
+            set_err(p.err, 6);
+            sm.fail = 1;
+            for (int k = j + 1; k < min(mine, j + F_NSS); ++k)   // let the other copies land first
+                mbar_wait_bounded(sbar(k % F_NSS), (k / F_NSS) & 1);
+            break;
+        }
+        const int b0 = (warp + j * FW) * SLAB;
+        const float* slab = reinterpret_cast<const float*>(sring + st * C::SLAB_BYTES);
+#pragma unroll
+        for (int x = 0; x < SLAB / 8; ++x) {
+            const int nbl = min(8, nb - (b0 + 8 * x));
+            if (nbl > 0) fused_score<D, HMAX>(qv, nq, p.tau, slab + 8 * x * D, nbl, sc, b0 + 8 * x, lane);
+        }
+        __syncwarp();
+        if (j + F_NSS < mine) {
+            if (lane == 0) fence_proxy_async_smem();   // the reads of this stage precede the next copy into it
+            issue_slab(j + F_NSS, st);
+        }
+    }
+    __syncthreads();
+    if (sm.fail) return;
+
+    // ---------------------------------------------------------------- 2. top-K and union
+    const int K = p.K_eff;
+    for (int hw = warp; hw < nq; hw += FW) {
+        const float* sch = sc + hw * F_NBMAX;
+        uint64_t key[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int b = lane + 32 * i;
+            key[i] = b < nb ? score_key(sch[b], b) : 0ull;
+        }
+        const bool fast = K <= 32 && topk_by_threshold(key, K, lane, sm.cand[hw], sm.picks[hw]);
+        uint64_t prev = ~0ull;   // otherwise K rounds of arg-max below the previous pick
+        for (int r = 0; r < (fast ? 0 : K); ++r) {
+            uint64_t below[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) below[i] = key[i] < prev ? key[i] : 0ull;
+            uint64_t best = max32(below);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) best = umax64(best, shfl64_xor(best, o));
+            prev = best;
+            if (lane == 0) sm.picks[hw][r] = key_block(best);
+        }
+        __syncwarp();
+        const int h = wg.qh[hw];
+        for (int k = lane; k < K; k += 32) {   // ascending: a pick's place is the number below it
+            const int v = sm.picks[hw][k];
+            int r = 0;
+            for (int j = 0; j < K; ++j) r += sm.picks[hw][j] < v ? 1 : 0;
+            sm.sorted[hw][r] = v;
+            if (ss.idx_out) ss.idx_out[(size_t)h * K + r] = v;
+        }
+    }
+    __syncthreads();
+    // union: entry (w, k) = head w's k-th smallest pick; the first head holding a block stands for it
+    int nfirst = 0;
+    for (int e = tid; e < nq * F_KMAX; e += FW * 32) {
+        const int w = e / F_KMAX, k = e % F_KMAX;
+        bool f = false;
+        if (k < K) {
+            const int b = sm.sorted[w][k];
+            f = true;
+            for (int w2 = 0; w2 < w; ++w2)
+                for (int k2 = 0; k2 < K; ++k2) f = f && sm.sorted[w2][k2] != b;
+        }
+        sm.first[e] = f ? 1 : 0;
+        nfirst += f ? 1 : 0;
+    }
+    if (nfirst) atomicAdd(&sm.nuniq, nfirst);
+    __syncthreads();
+    const int nuniq = sm.nuniq;
+    for (int e = tid; e < nq * F_KMAX; e += FW * 32) {
+        if (!sm.first[e]) continue;
+        const int b = sm.sorted[e / F_KMAX][e % F_KMAX];
+        int rank = 0;   // distinct blocks below b
+        uint32_t m = 0;
+        for (int w2 = 0; w2 < nq; ++w2)
+            for (int k2 = 0; k2 < K; ++k2) {
+                const int v = sm.sorted[w2][k2];
+                rank += (sm.first[w2 * F_KMAX + k2] && v < b) ? 1 : 0;
+                m |= (v == b ? 1u : 0u) << w2;
+            }
+        sm.ublk[rank] = b;
+        sm.umask[rank] = static_cast<uint8_t>(m);
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive prefix of the union's tiles: a run of entries per lane, then a warp scan
+        const int per = (nuniq + 31) / 32, e0 = min(nuniq, lane * per), e1 = min(nuniq, e0 + per);
+        int sum = 0;
+        for (int e = e0; e < e1; ++e) sum += min(p.tpb, p.ntiles - sm.ublk[e] * p.tpb);
+        int x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int run = x - sum;
+        for (int e = e0; e < e1; ++e) {
+            sm.utile[e] = run;
+            run += min(p.tpb, p.ntiles - sm.ublk[e] * p.tpb);
+        }
+        if (lane == 31) sm.utile[nuniq] = x;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- 3. gather decode
+    const int upre = sm.utile[nuniq];
+    const int n_suf = (p.S_suf + TILE_TOK - 1) / TILE_TOK;
+    const int units = upre + n_suf;
+    const int per_w = (units + FW - 1) / FW;
+    const int u0 = min(units, warp * per_w), u1 = min(units, u0 + per_w);
+    F16State<D, NCB> st;
+    st.qsm = 0;
+    start_item_f16<D, NCB>(st, p, ss, wg, lane);
+    const size_t reg = fp16_region_bytes(p.ntiles, D);
+    const uint8_t* kreg = ss.kv + (size_t)g * 2 * reg;
+    const uint8_t* vreg = kreg + reg;
+    uint8_t* ring = regA + warp * C::DST * C::TB;
+    const uint32_t ring_s = smem_u32(ring);
+    const int pe = u1;   // the warp's units are [u0, u1)
+    // unit u -> (union entry, resident tile): entries are walked forward from the first one
+    int ek = 0;
+    {
+        int lo = 0, hi = nuniq;   // the last entry whose first unit is <= u0
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (sm.utile[mid] <= u0) lo = mid; else hi = mid;
+        }
+        ek = lo;
+    }
+    int pk = ek;   // producer's entry
+    auto tile_of = [&](int u, int& e) {
+        while (e + 1 < nuniq && sm.utile[e + 1] <= u) ++e;
+        return sm.ublk[e] * p.tpb + (u - sm.utile[e]);
+    };
+    // a unit below upre is a resident tile of the union; from upre on, 16 rows of the suffix,
+    // copied row-major (a short last tile's missing rows are zeroed first, so that their zero
+    // weights never meet stale bits)
+    auto issue_tile = [&](int u, int s) {
+        if (u < upre) {
+            const int T = tile_of(u, pk);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(dbar(s), C::TB);
+                bulk_g2s(ring_s + s * C::TB, kreg + (size_t)T * 32 * D, 32 * D, dbar(s));
+                bulk_g2s(ring_s + s * C::TB + 32 * D, vreg + (size_t)T * 32 * D, 32 * D, dbar(s));
+            }
+            return;
+        }
+        const int t0 = (u - upre) * TILE_TOK, rows = min(TILE_TOK, p.S_suf - t0);
+        if (rows < TILE_TOK) {
+            uint4* kz = reinterpret_cast<uint4*>(ring + s * C::TB + rows * 2 * D);
+            uint4* vz = reinterpret_cast<uint4*>(ring + s * C::TB + 32 * D + rows * 2 * D);
+            for (int i = lane; i < (TILE_TOK - rows) * D / 8; i += 32) {
+                kz[i] = make_uint4(0u, 0u, 0u, 0u);
+                vz[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(rows) * 2 * D;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(dbar(s), 2 * bytes);
+            bulk_g2s(ring_s + s * C::TB, ss.Ksuf + ((size_t)g * p.S_suf + t0) * D, bytes, dbar(s));
+            bulk_g2s(ring_s + s * C::TB + 32 * D, ss.Vsuf + ((size_t)g * p.S_suf + t0) * D, bytes, dbar(s));
+        }
+    };
+    // the rings reuse the memory of the scoring stages and the scores, which every warp has read
+    // (generic proxy) before the last barrier: order those reads before the copies into it
+    if (lane == 0) fence_proxy_async_smem();
+    int next = u0, inflight = 0;
+    for (int s = 0; s < C::DST && next < pe; ++s, ++next, ++inflight) issue_tile(next, s);
+    bool ok = true;
+    uint32_t phase = 0;
+    int stage = 0;
+    for (int u = u0; u < pe; ++u) {
+        const int T = u < upre ? tile_of(u, ek) : 0;
+        if (!mbar_wait_bounded(dbar(stage), (phase >> stage) & 1u)) {
+            set_err(p.err, 1);
+            for (int k = 1; k < inflight; ++k) {   // let the other copies land before giving up
+                const int s2 = (stage + k) % C::DST;
+                mbar_wait_bounded(dbar(s2), (phase >> s2) & 1u);
+            }
+            ok = false;
+            break;
+        }
+        --inflight;
+        const uint32_t sb = ring_s + stage * C::TB;
+        if (u < upre) {
+            SmemF16Tile<D> tl{sb, sb + 32 * D, lane};
+            tile_f16<D, NCB>(st, tl, lane, min(TILE_TOK, p.N - T * TILE_TOK), sm.umask[ek], nq);
+        } else {
+            const int t0 = (u - upre) * TILE_TOK;
+            SmemRowTile<D> tl{sb, sb + 32 * D, lane};
+            tile_f16<D, NCB>(st, tl, lane, p.S_suf - t0, 0xFFFFFFFFu, nq);
+        }
+        phase ^= 1u << stage;
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();   // our reads of this stage precede the next copy into it
+        if (next < pe) {
+            issue_tile(next, stage);
+            ++next;
+            ++inflight;
+        }
+        stage = stage + 1 == C::DST ? 0 : stage + 1;
+    }
+    (void)ok;
+
+    // ---------------------------------------------------------------- 4. merge of the warps' pieces
+    __syncthreads();   // every ring is drained: the partials may overwrite them
+    float* part = reinterpret_cast<float*>(regA);
+    constexpr int PS = partial_stride(D);
+    write_partial_f16<D, NCB>(st, part + warp * HMAX * PS, nq, lane);
+    __syncthreads();
+    constexpr int V = D / 32;   // o values per lane
+    for (int hl = warp; hl < nq; hl += FW) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < FW; ++w) M = fmaxf(M, part[(w * HMAX + hl) * PS]);
+        float L = 0.f, o[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) o[v] = 0.f;
+#pragma unroll
+        for (int w = 0; w < FW; ++w) {
+            const float* ph = part + (w * HMAX + hl) * PS;
+            const float mw = ph[0];
+            const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            L = fmaf(wt, ph[1], L);
+#pragma unroll
+            for (int v = 0; v < V; ++v) o[v] = fmaf(wt, ph[PARTIAL_O + lane * V + v], o[v]);
+        }
+        const int qh = wg.qh[hl];
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        float* orow = ss.O + (size_t)qh * D + lane * V;
+#pragma unroll
+        for (int v = 0; v < V; ++v) orow[v] = o[v] * inv;
+        if (lane == 0 && ss.LSE) ss.LSE[qh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+    }
+}
+
+template <int D, int NCB>
+cudaError_t launch_fused_t(const FusedSparseParams& p, cudaStream_t st) {
+    constexpr int SMEM = fused_smem<D, NCB>();
+    static_assert(SMEM <= 227 * 1024, "one CTA's shared memory");
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(sparse_fused_kernel<D, NCB>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_sess * p.n_groups));
+    cfg.blockDim = dim3(FCfg<D, NCB>::W * 32);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sparse_fused_kernel<D, NCB>, p);
+}
+
+}  // namespace
+
+int sparse_fused_gmax(int D) { return D >= 256 ? 4 : GMAX; }
+
+bool sparse_fused_ok(int D, int nb, int K_eff) {
+    return (D == 64 || D == 128 || D == 256) && nb >= 1 && nb <= F_NBMAX && K_eff >= 1 && K_eff <= F_KMAX;
+}
+
+cudaError_t launch_sparse_fused(const FusedSparseParams& p, int max_nq, cudaStream_t st) {
+    const int ncb = max_nq > 4 ? 2 : 1;
+    if (p.D == 64) return ncb == 1 ? launch_fused_t<64, 1>(p, st) : launch_fused_t<64, 2>(p, st);
+    if (p.D == 128) return ncb == 1 ? launch_fused_t<128, 1>(p, st) : launch_fused_t<128, 2>(p, st);
+    if (p.D == 256 && ncb == 1) return launch_fused_t<256, 1>(p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pck

@@ -282,3 +282,80 @@ def test_block_means_direct(ctx, H_kv, N, D, B):
     assert got.shape == want.shape
     assert np.abs(got - want).max() <= 1e-5
     ctx.drop("bm")
+
+
+# ---------------------------------------------------------------- the fused single-kernel form
+# pck_query_sparse_batch runs the whole query in one kernel (a CTA per (session, group of q
+# heads)) once a batch has at least 32 work items and every kv head has at most 1024 blocks;
+# these batches are sized to take that path.
+
+FUSED_CASES = [
+    # H_q, H_kv, head_map, N, D, B, K_top, S_suf, q fp16, sessions
+    (8, 2, None, 3000, 256, 64, 5, 24, False, 16),           # ragged last block, short last suffix tile
+    (16, 2, None, 2000, 128, 32, 40, 0, True, 16),           # 8 q heads per group, K_top > 32 (arg-max rounds)
+    (6, 3, [2, 0, 1, 1, 0, 2], 1500, 64, 64, 4, 9, False, 12),   # q heads of a kv head not adjacent
+    (4, 2, [1, 1, 1, 1], 777, 128, 16, 64, 16, False, 32),   # kv head 0 has no q heads; K_top = 64 > nb
+    (8, 1, None, 1100, 256, 64, 3, 32, True, 32),            # 8 q heads of one kv head at D = 256: two groups of 4
+]
+
+
+@pytest.mark.parametrize("H_q,H_kv,hm,N,D,B,Kt,S,q16,R", FUSED_CASES)
+def test_sparse_fused_batch_matches_oracle(ctx, H_q, H_kv, hm, N, D, B, Kt, S, q16, R):
+    hm = synth.default_head_map(H_q, H_kv) if hm is None else np.array(hm, dtype=np.int32)
+    nb = -(-N // B)
+    K_eff = min(Kt, nb)
+    descs, refs = [], []
+    for r in range(R):
+        seed = 5000 + 17 * r + D
+        K, V = synth.gen_kv(seed, H_kv, N, D)
+        Q = synth.gen_q(seed, H_q, 1, D, dtype=np.float16 if q16 else np.float32)[:, 0]
+        Ks = Vs = None
+        if S:
+            Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        sid = f"spf{r}"
+        ctx.store(sid, 0, dev(K), dev(V))
+        d = dict(sid=sid, layer=0, Q=dev(Q), O=torch.full((H_q, D), float("nan"), device="cuda"),
+                 LSE=torch.empty((H_q,), device="cuda"), idx=torch.full((H_q, K_eff), -1, dtype=torch.int32, device="cuda"))
+        if S:
+            d["K_suf"], d["V_suf"] = dev(Ks), dev(Vs)
+        descs.append(d)
+        refs.append(orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs))
+    ctx.query_sparse_batch(descs, H_q, H_kv, D, B, Kt, S_suf=S, q_dtype=binding_dt(q16), head_map=hm)
+    ctx.sync()
+    for r, (d, (O_ref, L_ref, idx_ref, scores)) in enumerate(zip(descs, refs)):
+        _check_idx(host(d["idx"]), scores, K_eff)
+        near = orc.topk_margin(scores, K_eff) < TIE_EPS
+        assert_close_o_lse(host(d["O"])[~near], host(d["LSE"])[~near], O_ref[~near], L_ref[~near],
+                           f"fused session {r} {(H_q, H_kv, N, D, B, Kt, S)}")
+    for r in range(R):
+        ctx.drop(f"spf{r}")
+
+
+def test_sparse_fused_batch_exact_ties(ctx):
+    """Bit-identical block means in every session (every score ties) through the fused form:
+    each head selects blocks 0..K_top-1 and attends uniformly over their tokens."""
+    H_q, H_kv, N, D, B, Kt, R = 4, 2, 2048, 64, 64, 6, 16
+    rng = np.random.default_rng(9)
+    row = rng.standard_normal(D).astype(np.float16)
+    K = np.broadcast_to(row, (H_kv, N, D)).copy()
+    hm = synth.default_head_map(H_q, H_kv)
+    descs, refs = [], []
+    for r in range(R):
+        _, V = synth.gen_kv(60 + r, H_kv, N, D)
+        Q = synth.gen_q(60 + r, H_q, 1, D)[:, 0]
+        ctx.store(f"spt{r}", 0, dev(K), dev(V))
+        descs.append(dict(sid=f"spt{r}", layer=0, Q=dev(Q), O=torch.empty((H_q, D), device="cuda"),
+                          LSE=torch.empty((H_q,), device="cuda"), idx=torch.empty((H_q, Kt), dtype=torch.int32, device="cuda")))
+        refs.append(orc.sparse_query(Q, K, V, hm, B, Kt))
+    ctx.query_sparse_batch(descs, H_q, H_kv, D, B, Kt)
+    ctx.sync()
+    for r, (d, (O_ref, L_ref, idx_ref, scores)) in enumerate(zip(descs, refs)):
+        assert (host(d["idx"]) == np.arange(Kt)[None]).all()
+        assert_close_o_lse(host(d["O"]), host(d["LSE"]), O_ref, L_ref, f"ties session {r}")
+    for r in range(R):
+        ctx.drop(f"spt{r}")
+
+
+def binding_dt(q16):
+    from prefix_cached_kv_gb300 import binding
+    return binding.DT_F16 if q16 else binding.DT_F32
