@@ -39,6 +39,9 @@ struct Slot {
     uint8_t* tiles = nullptr;
     size_t bytes = 0;
     std::unordered_map<int, float*> kmean;  // block size -> [H_kv, nb, D] fp32
+    // block size -> the same means as fp16 hi + lo pairs in the tensor-core tile layout (16 blocks
+    // a tile, [H_kv][ceil(nb / 16)][hi part | lo part]; see launch_block_means_split)
+    std::unordered_map<int, uint8_t*> kmean_split;
     std::list<std::string>::iterator lru;
 };
 
@@ -122,9 +125,11 @@ const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D, int ncb) {
 void free_slot(pck_ctx* c, Slot& s, cudaStream_t st) {
     if (s.tiles) cudaFreeAsync(s.tiles, st);
     for (auto& kv : s.kmean) cudaFreeAsync(kv.second, st);
+    for (auto& kv : s.kmean_split) cudaFreeAsync(kv.second, st);
     c->bytes_resident -= static_cast<int64_t>(s.bytes);
     s.tiles = nullptr;
     s.kmean.clear();
+    s.kmean_split.clear();
 }
 
 void remember_cold(pck_ctx* c, const std::string& k) {
@@ -506,6 +511,27 @@ int pck_build_block_means(pck_ctx* c, const char* sid, int layer, int B, void* s
     return PCK_OK;
 }
 
+// The split (fp16 hi + lo, tile layout) copy of a slot's block means, built from the fp32 ones.
+static int build_block_means_split(pck_ctx* c, Slot* s, int B, cudaStream_t st) {
+    if (s->kmean_split.count(B)) return PCK_OK;
+    const int nb = (s->N + B - 1) / B;
+    const size_t bytes = static_cast<size_t>(s->H_kv) * ((nb + 15) / 16) * 64 * s->D;
+    uint8_t* out = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&out), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate split block means");
+    }
+    const cudaError_t e = launch_block_means_split(s->kmean[B], s->H_kv, nb, s->D, out, st);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(out, st);
+        return cuda_fail(c, e, "split block means launch");
+    }
+    s->kmean_split[B] = out;
+    s->bytes += bytes;
+    c->bytes_resident += static_cast<int64_t>(bytes);
+    return PCK_OK;
+}
+
 static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, int M, int S_suf, int H_kv_arg,
                         int q_dtype, const void* Q, const void* K_suf, const void* V_suf, const int32_t* head_map,
                         int causal, int fa_window, float* O, float* LSE, void* stream) {
@@ -678,6 +704,10 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
     }
     if (suf_aligned && n_items_est >= FUSED_MIN_ITEMS && sparse_fused_ok(D, nb, K_eff)) {
         // the whole query in one kernel, a CTA per work item
+        for (int i = 0; i < n; ++i) {
+            const int rc = build_block_means_split(c, slots[i], B, st);
+            if (rc != PCK_OK) return rc;
+        }
         static thread_local FusedSparseParams fp;
         std::memset(&fp, 0, sizeof fp);
         int n_groups = 0, max_nq = 0;
@@ -698,7 +728,7 @@ static int sparse_run(pck_ctx* c, int n, const SparseIn* q, int H_q, int D, int 
         fp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
         fp.err = c->dev_err;
         for (int i = 0; i < n; ++i)
-            fp.sess[i] = FusedSession{slots[i]->kmean[B], q[i].Q, slots[i]->tiles,
+            fp.sess[i] = FusedSession{slots[i]->kmean_split[B], q[i].Q, slots[i]->tiles,
                                       static_cast<const __half*>(q[i].K_suf), static_cast<const __half*>(q[i].V_suf),
                                       q[i].O, q[i].LSE, q[i].idx_out};
         const cudaError_t e = launch_sparse_fused(fp, max_nq, st);

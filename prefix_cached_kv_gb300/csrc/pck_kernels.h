@@ -97,8 +97,12 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t st, int sms);
 // The whole block-mean sparse query in one kernel (one CTA per (session, work group)): scores,
 // top-K and union in shared memory, gather decode of the union plus the dense suffix, and the
 // merge of the CTA's pieces. Work groups hold at most sparse_fused_gmax(D) q heads.
+// fp32 block means [H_kv, nb, D] -> fp16 hi + lo pairs (x = hi + lo to ~22 bits) in the resident
+// K-tile layout with blocks as tokens: per kv head and group of 16 blocks, a hi part and a lo part
+// of 32 D bytes each (core matrices [block group][d chunk]); blocks past nb are zero.
+cudaError_t launch_block_means_split(const float* kmean, int H_kv, int nb, int D, uint8_t* out, cudaStream_t st);
 struct FusedSession {
-    const float* kmean;      // [H_kv, nb, D]
+    const uint8_t* kmean;    // split block means (launch_block_means_split) of the slot
     const void* Q;           // [H_q, D]
     const uint8_t* kv;       // resident fp16 slot
     const __half* Ksuf;      // [H_kv, S_suf, D] or nullptr

@@ -38,6 +38,31 @@ __global__ void block_means_kernel(const uint8_t* __restrict__ tiles, int N, int
     }
 }
 
+// Split copy of the block means for the tensor-core scoring of the fused sparse kernel: one CTA
+// per (group of 16 blocks, kv head); block r of the group and dimension d go to the core matrix
+// (r / 8, d / 8) of the group's hi part (fp16(x)) and lo part (fp16(x - hi)), zeros past nb.
+__global__ void __launch_bounds__(128) block_means_split_kernel(const float* __restrict__ kmean, int nb, int D,
+                                                                uint8_t* __restrict__ out) {
+    const int bg = blockIdx.x, g = blockIdx.y, nbg = gridDim.x;
+    uint8_t* hi = out + ((size_t)g * nbg + bg) * 64 * D;
+    uint8_t* lo = hi + 32 * D;
+    for (int e = threadIdx.x; e < 16 * D; e += blockDim.x) {
+        const int r = e / D, d = e - r * D, b = bg * 16 + r;
+        const float x = b < nb ? kmean[((size_t)g * nb + b) * D + d] : 0.f;
+        const __half h = __float2half_rn(x);
+        const __half l = __float2half_rn(x - __half2float(h));
+        const size_t off = ((size_t)(r >> 3) * (D / 8) + (d >> 3)) * 128 + (r & 7) * 16 + (d & 7) * 2;
+        *reinterpret_cast<__half*>(hi + off) = h;
+        *reinterpret_cast<__half*>(lo + off) = l;
+    }
+}
+
+cudaError_t launch_block_means_split(const float* kmean, int H_kv, int nb, int D, uint8_t* out, cudaStream_t st) {
+    if (D % 16 || nb < 1) return cudaErrorInvalidValue;
+    block_means_split_kernel<<<dim3((nb + 15) / 16, H_kv), 128, 0, st>>>(kmean, nb, D, out);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- block scoring
 
 // A scoring CTA takes a slab of SCORE_BPC consecutive blocks of one (session, kv head): one bulk

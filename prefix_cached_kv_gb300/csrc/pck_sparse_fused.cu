@@ -3,8 +3,9 @@
 //
 // One CTA per work item (session, group of q heads of one kv head g) runs every step of the
 // query in shared memory:
-//   1. scoring: each warp streams its own 8 KB slabs of the kv head's block means through its
-//      own ring of bulk copies and scores them for every q head of the group; the scores
+//   1. scoring: each warp streams its own tiles of 16 block means (kept per slot as fp16 hi + lo
+//      pairs, the same 4 bytes per value as fp32) through its own ring of bulk copies and scores
+//      them on the tensor cores for every q head of the group; the scores
 //      score[h, b] = tau * q_h . K_mean[g, b] stay in shared memory;
 //   2. selection: warp w takes the top-K of q heads w, w + W, ... (ties to the lower block),
 //      reports them sorted ascending, and the CTA forms the sorted union of the group's blocks
@@ -35,9 +36,9 @@ template <int D, int NCB>
 struct FCfg {
     static constexpr int W = D == 256 ? 6 : 8;                 // warps per CTA
     static constexpr int HMAX = 4 * NCB;                       // q heads per group
-    static constexpr int SLAB = 8192 / (D * 4);                // blocks per scoring stage (8 KB)
-    static constexpr int SLAB_BYTES = SLAB * D * 4;
-    static constexpr int NSS = D == 256 ? 3 : 2;               // scoring stages per warp
+    static constexpr int SLAB = 16;                            // blocks per scoring stage: one split tile
+    static constexpr int SLAB_BYTES = 64 * D;                  // its hi and lo parts
+    static constexpr int NSS = D == 64 ? 3 : 2;                // scoring stages per warp
     static constexpr int SCORE_RING = W * NSS * SLAB_BYTES;
     static constexpr int SCORES = HMAX * F_NBMAX * 4;
     static constexpr int TB = 64 * D;                          // fp16 tile: K 32 D bytes, then V 32 D bytes
@@ -67,65 +68,12 @@ constexpr int fused_smem() {
     return C::REGION + static_cast<int>(sizeof(FSel<C::HMAX>)) + C::NBAR * 8;
 }
 
-// Scores of blocks [b0, b0 + nbl) (nbl <= 8) of a stage for the group's q heads, 4 at a time:
-// lane products over 8 blocks x 4 heads summed by a reduce-scatter (lane l ends with block
-// l / 4, head l % 4), as in the scoring kernel of pck_sparse.cu.
-template <int D, int HMAX>
-__device__ __forceinline__ void fused_score(const float4 (&qv)[HMAX][D / 4 >= 32 ? D / 128 : 1], int nq, float tau,
-                                            const float* kslab, int nbl, float* sc, int b0, int lane) {
-    constexpr int F4 = D / 4;
-    constexpr int L4 = 8 * F4 / 32;
-    constexpr int QN = F4 >= 32 ? F4 / 32 : 1;
-    const float4* km = reinterpret_cast<const float4*>(kslab);
-#pragma unroll
-    for (int c4 = 0; c4 < HMAX / 4; ++c4) {
-        if (4 * c4 >= nq) break;
-        float acc[32];
-#pragma unroll
-        for (int v = 0; v < 32; ++v) acc[v] = 0.f;
-#pragma unroll
-        for (int k = 0; k < L4; ++k) {
-            const int e = lane + 32 * k;
-            const float4 kv = e / F4 < nbl ? km[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 q = qv[4 * c4 + j][F4 >= 32 ? k % QN : 0];
-                float x = kv.x * q.x;
-                x = fmaf(kv.y, q.y, x);
-                x = fmaf(kv.z, q.z, x);
-                x = fmaf(kv.w, q.w, x);
-                if constexpr (F4 >= 32) {
-                    acc[(k / (F4 / 32)) * 4 + j] += x;
-                } else {   // D = 64: lanes 0-15 hold block 2k, lanes 16-31 block 2k + 1
-                    const bool hi = lane >= 16;
-                    acc[(2 * k) * 4 + j] += hi ? 0.f : x;
-                    acc[(2 * k + 1) * 4 + j] += hi ? x : 0.f;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < o; ++i) {
-                const float send = up ? acc[i] : acc[i + o];
-                const float keep = up ? acc[i + o] : acc[i];
-                acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-        }
-        const int blk = lane >> 2, hl = 4 * c4 + (lane & 3);
-        if (hl < nq && blk < nbl) sc[hl * F_NBMAX + b0 + blk] = tau * acc[0];
-    }
-}
-
 template <int D, int NCB>
 __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(const __grid_constant__ FusedSparseParams p) {
     using C = FCfg<D, NCB>;
     constexpr int FW = C::W;
     constexpr int F_NSS = C::NSS;
     constexpr int HMAX = C::HMAX;
-    constexpr int F4 = D / 4;
-    constexpr int QN = F4 >= 32 ? F4 / 32 : 1;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* regA = smem;
     FSel<HMAX>& sm = *reinterpret_cast<FSel<HMAX>*>(smem + C::REGION);
@@ -148,41 +96,28 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
     grid_dep_wait_then_release();
 
     // ---------------------------------------------------------------- 1. scores
-    // Each warp streams its own slabs (w, w + FW, ...) through its own ring and scores them; the
-    // warps meet only once every score is in shared memory.
+    // Each warp streams its own groups of 16 blocks (w, w + W, ...) of the split block means
+    // through its own ring and scores them on the tensor cores, the blocks as MMA rows and the
+    // q heads' hi / lo parts as columns: score = (K_hi + K_lo) . (q_hi + q_lo) tau, every product
+    // exact and summed in fp32. The warps meet once every score is in shared memory.
     const int nb = p.nb;
-    constexpr int SLAB = C::SLAB;
-    const int nslabs = (nb + SLAB - 1) / SLAB;
-    const float* kmg = ss.kmean + (size_t)g * nb * D;
+    const int nbg = (nb + 15) / 16;
+    const uint8_t* kmg = ss.kmean + (size_t)g * nbg * C::SLAB_BYTES;
     float* sc = reinterpret_cast<float*>(regA + C::SCORE_RING);   // [HMAX][F_NBMAX]
     uint8_t* sring = regA + warp * F_NSS * C::SLAB_BYTES;
-    auto issue_slab = [&](int j, int st) {   // the warp's j-th slab (slab w + j FW) into stage st
-        const int b0 = (warp + j * FW) * SLAB;
-        const uint32_t bytes = static_cast<uint32_t>(min(SLAB, nb - b0)) * D * 4;
+    const uint32_t sring_s = smem_u32(sring);
+    auto issue_slab = [&](int j, int st) {   // the warp's j-th group (group w + j W) into stage st
         if (lane == 0) {
-            mbar_arrive_expect_tx(sbar(st), bytes);
-            bulk_g2s(smem_u32(sring + st * C::SLAB_BYTES), kmg + (size_t)b0 * D, bytes, sbar(st));
+            mbar_arrive_expect_tx(sbar(st), C::SLAB_BYTES);
+            bulk_g2s(sring_s + st * C::SLAB_BYTES, kmg + (size_t)(warp + j * FW) * C::SLAB_BYTES, C::SLAB_BYTES, sbar(st));
         }
     };
-    const int mine = warp < nslabs ? (nslabs - warp + FW - 1) / FW : 0;   // slabs of this warp
+    const int mine = warp < nbg ? (nbg - warp + FW - 1) / FW : 0;   // groups of this warp
     for (int j = 0; j < min(F_NSS, mine); ++j) issue_slab(j, j);
-    float4 qv[HMAX][QN];   // the group's q heads (fp32), 4 per warp-wide score step
-#pragma unroll
-    for (int h = 0; h < HMAX; ++h)
-#pragma unroll
-        for (int i = 0; i < QN; ++i) {
-            const int d4 = F4 >= 32 ? lane + 32 * i : lane % F4;
-            if (h >= nq) {
-                qv[h][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (p.q_f16) {
-                const uint2 r = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(ss.Q) + (size_t)wg.qh[h] * D) + d4);
-                const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
-                const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
-                qv[h][i] = make_float4(x.x, x.y, y.x, y.y);
-            } else {
-                qv[h][i] = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ss.Q) + (size_t)wg.qh[h] * D) + d4);
-            }
-        }
+    struct { int q_f16; float scale_log2; int* err; } qscale{p.q_f16, p.tau, p.err};
+    F16State<D, NCB> sq;   // B fragments of tau * q (hi / lo parts), as the decode builds them
+    sq.qsm = 0;
+    start_item_f16<D, NCB>(sq, qscale, ss, wg, lane);
     for (int j = 0; j < mine; ++j) {
         const int st = j % F_NSS;
         if (!mbar_wait_bounded(sbar(st), (j / F_NSS) & 1)) {
@@ -192,12 +127,32 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
                 mbar_wait_bounded(sbar(k % F_NSS), (k / F_NSS) & 1);
             break;
         }
-        const int b0 = (warp + j * FW) * SLAB;
-        const float* slab = reinterpret_cast<const float*>(sring + st * C::SLAB_BYTES);
+        const uint32_t sb = sring_s + st * C::SLAB_BYTES;
+        const SmemF16Tile<D> thi{sb, 0u, lane}, tlo{sb + 32 * D, 0u, lane};
+        float ah[NCB][4], al[NCB][4];
 #pragma unroll
-        for (int x = 0; x < SLAB / 8; ++x) {
-            const int nbl = min(8, nb - (b0 + 8 * x));
-            if (nbl > 0) fused_score<D, HMAX>(qv, nq, p.tau, slab + 8 * x * D, nbl, sc, b0 + 8 * x, lane);
+        for (int cb = 0; cb < NCB; ++cb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ah[cb][i] = al[cb][i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            uint32_t a[4], b[4];
+            thi.ka(k, a);
+            tlo.ka(k, b);
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+                mma16816(ah[cb], a, sq.qb[cb][k][0], sq.qb[cb][k][1]);
+                mma16816(al[cb], b, sq.qb[cb][k][0], sq.qb[cb][k][1]);
+            }
+        }
+        const int b0 = (warp + j * FW) * 16 + (lane >> 2);
+#pragma unroll
+        for (int cb = 0; cb < NCB; ++cb) {
+            const int hl = cb * 4 + (lane & 3);   // columns 2q, 2q + 1: head q's hi and lo parts
+            if (hl < nq) {
+                if (b0 < nb) sc[hl * F_NBMAX + b0] = (ah[cb][0] + al[cb][0]) + (ah[cb][1] + al[cb][1]);
+                if (b0 + 8 < nb) sc[hl * F_NBMAX + b0 + 8] = (ah[cb][2] + al[cb][2]) + (ah[cb][3] + al[cb][3]);
+            }
         }
         __syncwarp();
         if (j + F_NSS < mine) {
