@@ -36,8 +36,7 @@ template <int D, int NCB>
 struct FCfg {
     static constexpr int W = D == 256 ? 6 : 8;                 // warps per CTA
     static constexpr int HMAX = 4 * NCB;                       // q heads per group
-    static constexpr int SLAB = 16;                            // blocks per scoring stage: one split tile
-    static constexpr int SLAB_BYTES = 64 * D;                  // its hi and lo parts
+    static constexpr int SLAB_BYTES = 64 * D;                  // a scoring stage: 16 blocks, hi and lo parts
     static constexpr int NSS = D == 64 ? 3 : 2;                // scoring stages per warp
     static constexpr int SCORE_RING = W * NSS * SLAB_BYTES;
     static constexpr int SCORES = HMAX * F_NBMAX * 4;
