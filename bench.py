@@ -345,8 +345,8 @@ def row_fp16_m1(ctx, torch, pk, reps=20):
 
 def row_sparse(ctx, torch, pk, reps=10, l2=None):
     """Sparse top-K (N=65,536, D=256, H_q=8, H_kv=2, B=64, K_top=8, S_suf=32) with the seeded
-    needles. Single-query mode: one query call per session back to back over 48 sessions.
-    Throughput mode: 48 sessions per pck_query_sparse_batch call, rotating over enough distinct
+    needles. Single-query mode: one query call per session back to back over 48 sessions (four
+    kernels a call). Throughput mode: 48 sessions per pck_query_sparse_batch call (one fused kernel), rotating over enough distinct
     48-session sets that the bytes one pass touches exceed 4x the L2 size. Bytes counted: block
     means + selected K/V + suffix + Q/O (not the dense prefix)."""
     from prefix_cached_kv_gb300 import synth
@@ -406,7 +406,8 @@ def row_sparse(ctx, torch, pk, reps=10, l2=None):
     gbs = lambda t_ms: alg / (t_ms * 1e-3) / 1e9
     return {"workload": "sparse_topk_64k", "us_per_call_back_to_back": round(ms * 1e3, 2),
             "alg_bytes_per_call": alg, "gbs": round(gbs(ms), 1), "frac_hbm": round(gbs(ms) / pk["hbm"], 4),
-            "needles_selected": ok, "launches_per_call": 4,
+            "needles_selected": ok, "launches_per_call": 4, "batched_launches_per_call": 1,
+            "batched_form": "one fused kernel, a CTA per (session, kv head): scores on the tensor cores, top-K, union, gather decode, merge",
             "batched_sessions_per_call": R, "batched_sets_rotated": n_sets,
             "batched_touched_mb_per_pass": round(n_sess * alg / 1e6, 1), "l2_mb": round(l2 / 1e6, 1),
             "batched_us_per_session": round(ms_b * 1e3, 3),
