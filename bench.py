@@ -345,13 +345,13 @@ def row_fp16_m1(ctx, torch, pk, reps=20):
 
 def row_sparse(ctx, torch, pk, reps=10, l2=None):
     """Sparse top-K (N=65,536, D=256, H_q=8, H_kv=2, B=64, K_top=8, S_suf=32) with the seeded
-    needles. Single-query mode: one query call per session back to back over 48 sessions (four
-    kernels a call). Throughput mode: 48 sessions per pck_query_sparse_batch call (one fused
-    kernel), rotating over enough distinct 48-session sets that the bytes one pass touches exceed
-    4x the L2 size. Bytes counted: block means + selected K/V + suffix + Q/O (not the dense
+    needles. Single-query mode: one query call per session back to back over 64 sessions (four
+    kernels a call). Throughput mode: 64 sessions (the batch limit) per pck_query_sparse_batch
+    call (one fused kernel, 128 CTAs), rotating over enough distinct 64-session sets that the
+    bytes one pass touches exceed 4x the L2 size. Bytes counted: block means + selected K/V + suffix + Q/O (not the dense
     prefix)."""
     from prefix_cached_kv_gb300 import synth
-    H_q, H_kv, N, D, B, Kt, S, R = 8, 2, 65536, 256, 64, 8, 32, 48
+    H_q, H_kv, N, D, B, Kt, S, R = 8, 2, 65536, 256, 64, 8, 32, 64
     nbk = N // B
     alg = H_kv * nbk * D * 4 + 8 * B * D * 2 * 2 * H_kv + 2 * H_kv * S * D * 2 + H_q * D * 4 * 2 + H_q * 4
     l2 = l2 or (126 << 20)
