@@ -202,6 +202,18 @@ int pck_get_block_means(pck_ctx *ctx, const char *sid, int layer, int B, float *
 int pck_query_batch(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, int H_kv, int D,
                     int S_suf, int q_dtype, const int32_t *head_map, void *stream);
 
+/* pck_query_batch over HOST buffers: descs[i].Q, K_suf, V_suf (inputs) and O, LSE (outputs) are
+ * page-locked host pointers (cudaHostAlloc, cudaHostRegister or a pinned tensor), 16-byte
+ * aligned; everything else is as pck_query_batch. The call moves the bytes itself, on `stream`:
+ * a copy kernel reads the inputs over the host link into the context's staging memory (at most
+ * PCK_HOST_STAGE_BYTES per call), the batch runs on the staged copies, and its merge kernel
+ * writes O and LSE straight into the host buffers. The outputs are valid, and the inputs may be
+ * reused, once `stream` has been synchronised. Errors: as pck_query_batch; PCK_EINVAL for a
+ * pointer that is not page-locked host memory; PCK_EUNSUPPORTED above the staging size. */
+#define PCK_HOST_STAGE_BYTES (16u << 20)
+int pck_query_batch_host(pck_ctx *ctx, int n, const pck_query_desc *descs, int H_q, int H_kv, int D,
+                         int S_suf, int q_dtype, const int32_t *head_map, void *stream);
+
 /* n independent ATTEND.PREFIX.QUERY_SPARSE_AUTO(_FUSED) queries (page "ATTEND.* and
  * ATTEND.PREFIX.*", section "Wire forms"; batching them is this library's addition, as for
  * pck_query_batch) of one shape (H_q, H_kv, D, B, K_top, S_suf, q_dtype, head_map) over fp16

@@ -26,7 +26,7 @@ EXPORTS = (
     "pck_drop", "pck_build_block_means", "pck_query", "pck_query_fused", "pck_query_sparse_auto",
     "pck_query_sparse_auto_fused", "pck_query_batch", "pck_query_sparse_batch", "pck_quantize_mlx4g32", "pck_info", "pck_sync",
     "pck_attend_records_noalloc", "pck_noalloc_status", "pck_query_sparse", "pck_get_block_means",
-    "pck_dequantize_mlx4g32",
+    "pck_dequantize_mlx4g32", "pck_query_batch_host",
 )
 
 
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pck_query_sparse_auto": (i, [vp, cp, i, i, i, i, i, i, i, vp, vp, i, vp, vp, vp, vp]),
         "pck_query_sparse_auto_fused": (i, [vp, cp, i, i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp, vp]),
         "pck_query_batch": (i, [vp, i, ctypes.POINTER(QueryDesc), i, i, i, i, i, vp, vp]),
+        "pck_query_batch_host": (i, [vp, i, ctypes.POINTER(QueryDesc), i, i, i, i, i, vp, vp]),
         "pck_query_sparse_batch": (i, [vp, i, ctypes.POINTER(SparseDesc), i, i, i, i, i, i, i, vp, vp]),
         "pck_quantize_mlx4g32": (i, [vp, i, i64, i, vp, vp]),
         "pck_info": (i, [vp, ctypes.POINTER(InfoT)]),
@@ -127,9 +128,10 @@ def _spec(t, name, dtype=None, numel=None, at_least=None, nbytes=None):
     return (t, name, dtype, numel, at_least, nbytes)
 
 
-def _check_all(*specs):
+def _check_all(*specs, host=False):
     """Check caller tensors before their pointers reach the library, which trusts the sizes the
-    call implies: dtypes and sizes of every tensor first, then contiguity, then the device."""
+    call implies: dtypes and sizes of every tensor first, then contiguity, then the device (or,
+    for host-buffer calls, that every tensor is page-locked host memory)."""
     live = [sp for sp in specs if sp[0] is not None]
     for t, name, dtype, numel, at_least, nbytes in live:
         if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
@@ -144,7 +146,9 @@ def _check_all(*specs):
         if not t.is_contiguous():
             raise ValueError(f"{name}: must be contiguous")
     for t, name, *_ in live:
-        if not t.is_cuda:
+        if host and (t.is_cuda or not t.is_pinned()):
+            raise ValueError(f"{name}: must be a pinned host tensor")
+        if not host and not t.is_cuda:
             raise ValueError(f"{name}: must be on the CUDA device")
 
 
@@ -160,7 +164,7 @@ def _check_suffix(K_suf, V_suf, D, H_kv=None):
         raise ValueError(f"suffix shape {tuple(K_suf.shape)} does not match H_kv={H_kv}, D={D}")
 
 
-def _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, sparse=False):
+def _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, sparse=False, host=False):
     """Descriptor tensors of a batched call: Q [H_q, D] of q_dtype, O (fp32) and LSE (fp32) of at
     least H_q * D and H_q elements, the suffix [H_kv, S_suf, D] fp16, idx int32 (sparse)."""
     qt = {DT_F32: torch.float32, DT_F16: torch.float16}.get(q_dtype)
@@ -176,7 +180,7 @@ def _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, sparse=False):
                 specs.append(_spec(d.get(k), f"descs[{i}].{k}", torch.float16, numel=H_kv * S_suf * D))
         if sparse:
             specs.append(_spec(d.get("idx"), f"descs[{i}].idx", torch.int32, at_least=H_q))
-    _check_all(*specs)
+    _check_all(*specs, host=host)
 
 
 def quantize_mlx4g32(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -399,10 +403,12 @@ class Context:
         return self._rc(self.lib.pck_query_batch(self.h, n, arr, H_q, H_kv, D, S_suf, q_dtype, hm[0] if hm else None,
                                                  _stream(stream)))
 
-    def batch_caller(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None):
+    def batch_caller(self, descs, H_q, H_kv, D, S_suf=0, q_dtype=DT_F32, head_map=None, host=False):
         """Prebuild the descriptor array of a pck_query_batch call; returns a no-argument callable
-        that issues the call on the current stream (cheap enough to capture in a CUDA graph)."""
-        _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype)
+        that issues the call on the current stream (cheap enough to capture in a CUDA graph).
+        host=True: the descriptors' tensors are pinned host tensors and the call is
+        pck_query_batch_host (the library moves the bytes)."""
+        _check_descs(descs, H_q, H_kv, D, S_suf, q_dtype, host=host)
         n = len(descs)
         arr = (QueryDesc * n)()
         keep = []
@@ -414,7 +420,7 @@ class Context:
                                d["K_suf"].data_ptr() if d.get("K_suf") is not None else None,
                                d["V_suf"].data_ptr() if d.get("V_suf") is not None else None)
         hm = _hm(head_map)
-        fn, h = self.lib.pck_query_batch, self.h
+        fn, h = self.lib.pck_query_batch_host if host else self.lib.pck_query_batch, self.h
 
         def call():
             rc = fn(h, n, arr, H_q, H_kv, D, S_suf, q_dtype, hm[0] if hm else None, _stream(None))

@@ -62,6 +62,7 @@ struct pck_ctx {
     uint8_t* sel = nullptr;
     float* scores = nullptr;
     uint8_t* suf_ws = nullptr;
+    uint8_t* host_stage = nullptr;   // host-buffer calls: their inputs, copied in (PCK_HOST_STAGE_BYTES)
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
     DecodeLaunchInfo dinfo[2][16];   // [format][head dimension x column blocks]
@@ -332,7 +333,8 @@ int pck_create(pck_ctx** out, int device, int max_slots) {
         cudaMalloc(&c->counters, WS_COUNTERS * sizeof(int)) != cudaSuccess ||
         cudaMalloc(&c->dev_err, sizeof(int)) != cudaSuccess || cudaMalloc(&c->sel, WS_SEL_BYTES) != cudaSuccess ||
         cudaMalloc(&c->scores, WS_SCORES_BYTES) != cudaSuccess ||
-        cudaMalloc(&c->suf_ws, WS_SUFFIX_BYTES) != cudaSuccess) {
+        cudaMalloc(&c->suf_ws, WS_SUFFIX_BYTES) != cudaSuccess ||
+        cudaMalloc(&c->host_stage, PCK_HOST_STAGE_BYTES) != cudaSuccess) {
         cudaGetLastError();
         pck_destroy(c);
         return PCK_ENOMEM;
@@ -359,6 +361,7 @@ void pck_destroy(pck_ctx* c) {
     cudaFree(c->sel);
     cudaFree(c->scores);
     cudaFree(c->suf_ws);
+    cudaFree(c->host_stage);
     delete c;
 }
 
@@ -847,6 +850,70 @@ int pck_query_batch(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int
                     static_cast<cudaStream_t>(stream));
     if (rc != PCK_OK) return rc;
     return check_async(c);
+}
+
+// The device-side address of page-locked host memory (nullptr when p is not such memory).
+static void* host_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+int pck_query_batch_host(pck_ctx* c, int n, const pck_query_desc* descs, int H_q, int H_kv, int D, int S_suf,
+                         int q_dtype, const int32_t* head_map, void* stream) {
+    if (!c) return PCK_EINVAL;
+    if (n < 1 || n > PCK_MAX_BATCH || !descs) return fail(c, PCK_EINVAL, "n=%d (1..%d) or NULL descs", n, PCK_MAX_BATCH);
+    if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
+    if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
+    if (H_q < 1 || H_q > PCK_MAX_HEADS || H_kv < 1 || H_kv > PCK_MAX_HEADS || D < 1 || D > 512)
+        return fail(c, PCK_EINVAL, "H_q=%d H_kv=%d D=%d", H_q, H_kv, D);
+    const size_t q_bytes = static_cast<size_t>(H_q) * D * (q_dtype == PCK_DT_F16 ? 2 : 4);
+    const size_t s_bytes = static_cast<size_t>(H_kv) * S_suf * D * 2;
+    auto al16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+    const size_t per = al16(q_bytes) + 2 * al16(s_bytes);
+    if (per * n > PCK_HOST_STAGE_BYTES)
+        return fail(c, PCK_EUNSUPPORTED, "%zu bytes of inputs (the staging memory holds %u)", per * n, PCK_HOST_STAGE_BYTES);
+    if ((q_bytes | s_bytes) & 15) return fail(c, PCK_EINVAL, "Q and suffix sizes must be multiples of 16 bytes");
+    static thread_local CopySegs segs;
+    static thread_local pck_query_desc dd[PCK_MAX_BATCH];
+    segs.n = 0;
+    auto add = [&](const void* host, uint8_t* dst, size_t bytes, const char* what, int i) -> int {
+        void* src = host_device_ptr(host);
+        if (!src) return fail(c, PCK_EINVAL, "descriptor %d: %s is not page-locked host memory", i, what);
+        if (reinterpret_cast<uintptr_t>(src) & 15) return fail(c, PCK_EINVAL, "descriptor %d: %s not 16-byte aligned", i, what);
+        segs.src[segs.n] = src;
+        segs.dst[segs.n] = dst;
+        segs.n16[segs.n] = static_cast<int>(bytes / 16);
+        ++segs.n;
+        return PCK_OK;
+    };
+    for (int i = 0; i < n; ++i) {
+        uint8_t* base = c->host_stage + per * i;
+        dd[i] = descs[i];
+        int rc = add(descs[i].Q, base, q_bytes, "Q", i);
+        if (rc != PCK_OK) return rc;
+        dd[i].Q = base;
+        if (S_suf > 0) {
+            rc = add(descs[i].K_suf, base + al16(q_bytes), s_bytes, "K_suf", i);
+            if (rc != PCK_OK) return rc;
+            rc = add(descs[i].V_suf, base + al16(q_bytes) + al16(s_bytes), s_bytes, "V_suf", i);
+            if (rc != PCK_OK) return rc;
+            dd[i].K_suf = base + al16(q_bytes);
+            dd[i].V_suf = base + al16(q_bytes) + al16(s_bytes);
+        }
+        dd[i].O = static_cast<float*>(host_device_ptr(descs[i].O));
+        if (!dd[i].O) return fail(c, PCK_EINVAL, "descriptor %d: O is not page-locked host memory", i);
+        if (descs[i].LSE) {
+            dd[i].LSE = static_cast<float*>(host_device_ptr(descs[i].LSE));
+            if (!dd[i].LSE) return fail(c, PCK_EINVAL, "descriptor %d: LSE is not page-locked host memory", i);
+        }
+    }
+    const cudaError_t e = launch_copy_segments(segs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(c, e, "staging copy");
+    return pck_query_batch(c, n, dd, H_q, H_kv, D, S_suf, q_dtype, head_map, stream);
 }
 
 int pck_query_sparse(pck_ctx* c, const char* sid, int layer, int H_q, int D, int K_sparse_max, int q_dtype,

@@ -123,6 +123,17 @@ int sparse_fused_gmax(int D);
 bool sparse_fused_ok(int D, int nb, int K_eff);
 cudaError_t launch_sparse_fused(const FusedSparseParams& p, int max_nq, cudaStream_t st);
 
+// Contiguous byte ranges copied by one launch (host-buffer calls: page-locked host memory read
+// over the host link into device staging memory). Every address 16-byte aligned.
+constexpr int MAX_COPY_SEGS = 3 * 64;
+struct CopySegs {
+    const void* src[MAX_COPY_SEGS];
+    void* dst[MAX_COPY_SEGS];
+    int n16[MAX_COPY_SEGS];   // 16-byte units
+    int n;
+};
+cudaError_t launch_copy_segments(const CopySegs& p, cudaStream_t st);
+
 // batched-Q tensor-core prefill (tcgen05)
 struct PrefillParams {
     const __half* Q;          // [H_q, M, D] (q_dup: [H_q, M, D/2])

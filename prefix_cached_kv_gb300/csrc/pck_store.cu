@@ -486,3 +486,36 @@ cudaError_t launch_relayout_mlx4(const void* Krec, const void* Vrec, int head_ro
 }
 
 }  // namespace pck
+
+// ------------------------------------------------------------------ host-buffer staging copy
+
+namespace pck {
+
+// One CTA per segment, 16-byte loads and stores; launched with programmatic dependence, it waits
+// for the previous kernel of the stream before it overwrites the staging memory that kernel may
+// still be reading.
+__global__ void __launch_bounds__(256) copy_segments_kernel(const __grid_constant__ CopySegs p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int sgi = blockIdx.x;
+    if (sgi >= p.n) return;
+    const uint4* src = static_cast<const uint4*>(p.src[sgi]);
+    uint4* dst = static_cast<uint4*>(p.dst[sgi]);
+    for (int i = threadIdx.x; i < p.n16[sgi]; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_copy_segments(const CopySegs& p, cudaStream_t st) {
+    if (p.n < 1 || p.n > MAX_COPY_SEGS) return cudaErrorInvalidValue;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, copy_segments_kernel, p);
+}
+
+}  // namespace pck
