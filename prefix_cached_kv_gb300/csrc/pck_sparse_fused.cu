@@ -7,9 +7,9 @@
 //      pairs, the same 4 bytes per value as fp32) through its own ring of bulk copies and scores
 //      them on the tensor cores for every q head of the group; the scores
 //      score[h, b] = tau * q_h . K_mean[g, b] stay in shared memory;
-//   2. selection: warp w takes the top-K of q heads w, w + W, ... (ties to the lower block),
-//      reports them sorted ascending, and the CTA forms the sorted union of the group's blocks
-//      with a mask of the q heads that chose each;
+//   2. selection: warp w takes the top-K of q heads w, w + W, ... (ties to the lower block) and
+//      marks them in a per-head map of blocks, from which the picks come out ascending and one
+//      warp forms the union of the group's blocks with a mask of the q heads that chose each;
 //   3. gather decode: the union's resident 16-token tiles and the dense suffix's 16-row tiles
 //      (causal-free at M = 1; copied row-major, read by ldmatrix.trans for V) are split evenly
 //      over the warps, each streaming its tiles through its own ring with the split-K decode's
@@ -52,12 +52,11 @@ struct FCfg {
 template <int HMAX>
 struct FSel {
     int picks[HMAX][F_KMAX];
-    int sorted[HMAX][F_KMAX];
     uint64_t cand[HMAX][32];
+    uint32_t bmap[HMAX][F_NBMAX / 32];   // each head's picks as a map of blocks
     int ublk[HMAX * F_KMAX];       // the union, ascending
     int utile[HMAX * F_KMAX + 1];  // exclusive prefix of the union's tiles
     uint8_t umask[HMAX * F_KMAX];
-    uint8_t first[HMAX * F_KMAX];
     int nuniq, fail;
 };
 
@@ -163,6 +162,9 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
     if (sm.fail) return;
 
     // ---------------------------------------------------------------- 2. top-K and union
+    // Each head's picks become a 1024-bit map of blocks (lane l: word l, blocks 32 l .. 32 l + 31):
+    // the map read in lane order is the picks ascending, the OR of the maps is the union, a
+    // block's bit in each map is its head mask, and ranks are popcounts under a warp scan.
     const int K = p.K_eff;
     for (int hw = warp; hw < nq; hw += FW) {
         const float* sch = sc + hw * F_NBMAX;
@@ -184,67 +186,62 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
             prev = best;
             if (lane == 0) sm.picks[hw][r] = key_block(best);
         }
+        sm.bmap[hw][lane] = 0u;
         __syncwarp();
-        const int h = wg.qh[hw];
-        for (int k = lane; k < K; k += 32) {   // ascending: a pick's place is the number below it
+        for (int k = lane; k < K; k += 32) {
             const int v = sm.picks[hw][k];
-            int r = 0;
-            for (int j = 0; j < K; ++j) r += sm.picks[hw][j] < v ? 1 : 0;
-            sm.sorted[hw][r] = v;
-            if (ss.idx_out) ss.idx_out[(size_t)h * K + r] = v;
+            atomicOr(&sm.bmap[hw][v >> 5], 1u << (v & 31));
         }
-    }
-    __syncthreads();
-    // union: entry (w, k) = head w's k-th smallest pick; the first head holding a block stands for it
-    int nfirst = 0;
-    for (int e = tid; e < nq * F_KMAX; e += FW * 32) {
-        const int w = e / F_KMAX, k = e % F_KMAX;
-        bool f = false;
-        if (k < K) {
-            const int b = sm.sorted[w][k];
-            f = true;
-            for (int w2 = 0; w2 < w; ++w2)
-                for (int k2 = 0; k2 < K; ++k2) f = f && sm.sorted[w2][k2] != b;
-        }
-        sm.first[e] = f ? 1 : 0;
-        nfirst += f ? 1 : 0;
-    }
-    if (nfirst) atomicAdd(&sm.nuniq, nfirst);
-    __syncthreads();
-    const int nuniq = sm.nuniq;
-    for (int e = tid; e < nq * F_KMAX; e += FW * 32) {
-        if (!sm.first[e]) continue;
-        const int b = sm.sorted[e / F_KMAX][e % F_KMAX];
-        int rank = 0;   // distinct blocks below b
-        uint32_t m = 0;
-        for (int w2 = 0; w2 < nq; ++w2)
-            for (int k2 = 0; k2 < K; ++k2) {
-                const int v = sm.sorted[w2][k2];
-                rank += (sm.first[w2 * F_KMAX + k2] && v < b) ? 1 : 0;
-                m |= (v == b ? 1u : 0u) << w2;
-            }
-        sm.ublk[rank] = b;
-        sm.umask[rank] = static_cast<uint8_t>(m);
-    }
-    __syncthreads();
-    if (warp == 0) {   // exclusive prefix of the union's tiles: a run of entries per lane, then a warp scan
-        const int per = (nuniq + 31) / 32, e0 = min(nuniq, lane * per), e1 = min(nuniq, e0 + per);
-        int sum = 0;
-        for (int e = e0; e < e1; ++e) sum += min(p.tpb, p.ntiles - sm.ublk[e] * p.tpb);
-        int x = sum;
+        __syncwarp();
+        // ascending picks: a block's place is the picks in lower words plus the lower bits of its own
+        const uint32_t wbits = sm.bmap[hw][lane];
+        const int cnt = __popc(wbits);
+        int pre = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const int y = __shfl_up_sync(0xffffffffu, pre, o);
+            if (lane >= o) pre += y;
         }
-        int run = x - sum;
-        for (int e = e0; e < e1; ++e) {
-            sm.utile[e] = run;
-            run += min(p.tpb, p.ntiles - sm.ublk[e] * p.tpb);
+        if (ss.idx_out) {
+            const int h = wg.qh[hw];
+            uint32_t m = wbits;
+            for (int r = pre - cnt; m; ++r, m &= m - 1) ss.idx_out[(size_t)h * K + r] = 32 * lane + __ffs(m) - 1;
         }
-        if (lane == 31) sm.utile[nuniq] = x;
     }
     __syncthreads();
+    if (warp == 0) {   // the union, its head masks and its tiles' exclusive prefix, lane l over word l
+        uint32_t u = 0;
+        for (int w2 = 0; w2 < nq; ++w2) u |= sm.bmap[w2][lane];
+        const int cnt = __popc(u);
+        int tiles = 0;
+        for (uint32_t m = u; m; m &= m - 1) {
+            const int b = 32 * lane + __ffs(m) - 1;
+            tiles += min(p.tpb, p.ntiles - b * p.tpb);
+        }
+        int pre = cnt, tpre = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, pre, o);
+            const int z = __shfl_up_sync(0xffffffffu, tpre, o);
+            if (lane >= o) { pre += y; tpre += z; }
+        }
+        int r = pre - cnt, run = tpre - tiles;
+        for (uint32_t m = u; m; m &= m - 1, ++r) {
+            const int bit = __ffs(m) - 1, b = 32 * lane + bit;
+            uint32_t hm = 0;
+            for (int w2 = 0; w2 < nq; ++w2) hm |= ((sm.bmap[w2][lane] >> bit) & 1u) << w2;
+            sm.ublk[r] = b;
+            sm.umask[r] = static_cast<uint8_t>(hm);
+            sm.utile[r] = run;
+            run += min(p.tpb, p.ntiles - b * p.tpb);
+        }
+        if (lane == 31) {
+            sm.nuniq = pre;
+            sm.utile[pre] = tpre;
+        }
+    }
+    __syncthreads();
+    const int nuniq = sm.nuniq;
 
     // ---------------------------------------------------------------- 3. gather decode
     const int upre = sm.utile[nuniq];
