@@ -309,7 +309,6 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
     if (lane == 0) fence_proxy_async_smem();
     int next = u0, inflight = 0;
     for (int s = 0; s < C::DST && next < pe; ++s, ++next, ++inflight) issue_tile(next, s);
-    bool ok = true;
     uint32_t phase = 0;
     int stage = 0;
     for (int u = u0; u < pe; ++u) {
@@ -320,7 +319,6 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
                 const int s2 = (stage + k) % C::DST;
                 mbar_wait_bounded(dbar(s2), (phase >> s2) & 1u);
             }
-            ok = false;
             break;
         }
         --inflight;
@@ -343,7 +341,6 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
         }
         stage = stage + 1 == C::DST ? 0 : stage + 1;
     }
-    (void)ok;
 
     // ---------------------------------------------------------------- 4. merge of the warps' pieces
     __syncthreads();   // every ring is drained: the partials may overwrite them
