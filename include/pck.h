@@ -143,8 +143,9 @@ int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void 
  * fa_window (listed on every QUERY form of the pages, never defined there; this library's reading):
  * 0 = no window; W > 0 = a sliding attention window: query row i, at absolute position
  * p_i = N + S_suf - M + i (prefix positions 0 .. N-1, then the suffix), sees only positions
- * p_i - W + 1 .. p_i. Built for M = 1 (both formats, with or without a suffix); M > 1 with W > 0
- * is PCK_EUNSUPPORTED, W < 0 PCK_EINVAL.
+ * p_i - W + 1 .. p_i (and, with causal, no suffix key past its own). Built for every dense QUERY
+ * form (M = 1 and M > 1, both formats, with or without a suffix); the sparse forms take W = 0
+ * only (PCK_EUNSUPPORTED otherwise); W < 0 is PCK_EINVAL.
  * Writes O [H_q, M, D] and, if LSE != NULL, LSE [H_q, M]. */
 int pck_query(pck_ctx *ctx, const char *sid, int layer, int H_q, int D, int M, int q_dtype,
               const void *Q, const int32_t *head_map, int top_k, int fa_window,

@@ -542,8 +542,6 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     if (!Q || !O) return fail(c, PCK_EINVAL, "NULL Q or O");
     if (reinterpret_cast<uintptr_t>(O) & 15) return fail(c, PCK_EINVAL, "O must be 16-byte aligned");
     if (fa_window < 0) return fail(c, PCK_EINVAL, "fa_window=%d", fa_window);
-    if (fa_window > 0 && M > 1)
-        return fail(c, PCK_EUNSUPPORTED, "fa_window=%d with M=%d (windows are built for M = 1)", fa_window, M);
     if (!dtype_ok(q_dtype)) return fail(c, PCK_EINVAL, "q_dtype=%d", q_dtype);
     if (M < 1) return fail(c, PCK_EINVAL, "M=%d", M);
     if (S_suf < 0) return fail(c, PCK_EINVAL, "S_suf=%d", S_suf);
@@ -611,6 +609,7 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
     pp.S_suf = S_suf;
     pp.causal = causal;
     pp.q_dup = split ? 1 : 0;
+    pp.window = fa_window;
     pp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     pp.err = c->dev_err;
     cudaError_t e = launch_prefill(pp, grp, n_groups, S_suf > 0 ? c->suf_ws : nullptr, suf_ntiles, c->partials,

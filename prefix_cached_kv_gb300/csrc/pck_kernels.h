@@ -145,6 +145,9 @@ struct PrefillParams {
     // enters the tile twice, [q | q], so S sums both halves, and O is folded: O[c] = O'[c] +
     // O'[c + D/2].
     int q_dup;
+    // window > 0: row i sees only positions p_i - window + 1 .. p_i of the prefix and suffix laid
+    // end to end, p_i = N + S_suf - M + i (the causal bound, when set, still applies)
+    int window;
     float scale_log2;
     int* err;
 };

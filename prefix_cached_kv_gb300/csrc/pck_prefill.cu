@@ -183,7 +183,8 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // P of one 32-key chunk of a row: p_j = 2^(s_j sc - m) for the nv visible keys (0 for the
 // rest), packed as fp16 pairs into pk; returns (sum of the fp16-rounded p_j, sum of the fp32 p_j).
 template <bool FULL>
-__device__ __forceinline__ float2 chunk_exp(const uint32_t (&v)[32], int nv, uint64_t sc2, float m, uint32_t (&pk)[16]) {
+__device__ __forceinline__ float2 chunk_exp(const uint32_t (&v)[32], int lo, int nv, uint64_t sc2, float m,
+                                            uint32_t (&pk)[16]) {
     const uint64_t nm2 = f2_pack(-m, -m);
     uint64_t ax0 = 0, ax1 = 0, ar0 = 0, ar1 = 0;   // (0.f, 0.f)
 #pragma unroll
@@ -191,9 +192,9 @@ __device__ __forceinline__ float2 chunk_exp(const uint32_t (&v)[32], int nv, uin
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), sc2, nm2), x0, x1);
         float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        if (!FULL) {
-            p0 = 2 * j < nv ? p0 : 0.f;
-            p1 = 2 * j + 1 < nv ? p1 : 0.f;
+        if (!FULL) {   // keys [lo, nv) of the chunk are visible
+            p0 = 2 * j < nv && 2 * j >= lo ? p0 : 0.f;
+            p1 = 2 * j + 1 < nv && 2 * j + 1 >= lo ? p1 : 0.f;
         }
         const __half2 h = __floats2half2_rn(p0, p1);
         const float2 r = __half22float2(h);
@@ -472,6 +473,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         const bool row_ok = r < rows_total;
         const int i = row_ok ? r % M : 0;
         const int suf_lim = P.a.causal ? (S - M + i) : (S - 1);   // last visible suffix key
+        // first visible position of the prefix and suffix laid end to end (a window), else none
+        const int first_pos = P.a.window > 0 ? N + S - M + i - P.a.window + 1 : -(1 << 30);
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t o_tm = tmem + C::O_COL + lane_base;
         const float sc = P.a.scale_log2;
@@ -497,8 +500,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             for (int c = 0; c < PF_BLOCK / 32; ++c) {
                 if (c >= nch) break;
                 const int nv = nvalid - 32 * c;   // visible keys of this chunk (<= 0 .. >= 32)
+                // keys [lo, nv) of the chunk are visible: lo > 0 where a window starts inside it
+                const int lo = max(0, first_pos - ((kb.is_suf ? N : 0) + kb.key0 + 32 * c));
                 uint32_t pk[16];
-                float2 cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
+                float2 cs = nv >= 32 && lo == 0 ? chunk_exp<true>(v[c], 0, nv, sc2, m, pk)
+                                                : chunk_exp<false>(v[c], lo, nv, sc2, m, pk);
                 // A sum <= 2^15 bounds every p_j by 2^15: they fit fp16 and m may stay. Otherwise
                 // (or on the first chunk, where m = -inf and the sum is infinite) move m to the
                 // chunk's max, rescale what was summed or written with the old m, and redo.
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (j < nv) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(v[c][j]));
+                        if (j < nv && j >= lo) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(v[c][j]));
                     const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
                     const float mnew = need ? fmaxf(m, cm) : m;
                     const float alpha = need ? exp2f(m - mnew) : 1.0f;
@@ -540,7 +546,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                     lr *= alpha;
                     lx *= alpha;
                     m = mnew;
-                    cs = nv >= 32 ? chunk_exp<true>(v[c], nv, sc2, m, pk) : chunk_exp<false>(v[c], nv, sc2, m, pk);
+                    cs = nv >= 32 && lo == 0 ? chunk_exp<true>(v[c], 0, nv, sc2, m, pk)
+                                             : chunk_exp<false>(v[c], lo, nv, sc2, m, pk);
                 }
                 br += cs.x;
                 bx += cs.y;

@@ -243,9 +243,47 @@ def test_window_rejections(ctx):
         ctx.query("wr", 0, dev(synth.gen_q(3, 4, 1, 64)), fa_window=-1)
     assert e.value.code == binding.EINVAL
     with pytest.raises(binding.PckError) as e:
-        ctx.query("wr", 0, dev(synth.gen_q(3, 4, 8, 64, dtype=np.float16)), fa_window=16)
-    assert e.value.code == binding.EUNSUPPORTED
-    with pytest.raises(binding.PckError) as e:
         ctx.query_sparse_auto("wr", 0, dev(synth.gen_q(3, 4, 1, 64)[:, 0]), 64, 2, 2, fa_window=16)
     assert e.value.code == binding.EUNSUPPORTED
     ctx.drop("wr")
+
+
+@pytest.mark.parametrize("H_q,H_kv,N,M,S,D,fmt,causal", [
+    (4, 2, 1000, 130, 40, 64, 0, True),      # rows span several row tiles; windows end in the suffix
+    (6, 2, 700, 64, 64, 128, 0, True),
+    (3, 1, 4133, 16, 8, 128, 0, True),       # many key-range splits: whole splits before a row's window
+    (4, 2, 900, 96, 32, 64, 1, True),        # mlx4g32 slot (hi/lo pairs at width 2D)
+    (2, 2, 500, 40, 24, 96, 0, False),       # no causal bound: the window alone
+])
+def test_prefill_window_matches_oracle(ctx, H_q, H_kv, N, M, S, D, fmt, causal):
+    """fa_window at M > 1: row i sees positions p_i - W + 1 .. p_i (p_i = N + S - M + i), under the
+    causal bound when set; windows inside the suffix, across the prefix / suffix border, deep in
+    the prefix, wider than everything, and W = 1."""
+    seed = N + M + S + D + fmt
+    K, V = synth.gen_kv(seed, H_kv, N, D)
+    Q = synth.gen_q(seed, H_q, M, D, dtype=np.float16)
+    Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+    hm = synth.default_head_map(H_q, H_kv)
+    Ko, Vo = _oracle_kv(K, V, fmt)
+    sid = f"pw{seed}"
+    ctx.store(sid, 0, dev(K), dev(V), fmt=fmt)
+    for W in sorted({1, 17, S, S + 70, M + S, 300, N + S + 5}):
+        O, L = ctx.query_fused(sid, 0, dev(Q), dev(Ks), dev(Vs), causal=causal, fa_window=W)
+        O_ref, L_ref = orc.prefix_query(Q, Ko, Vo, hm, Ks, Vs, causal=causal, window=W)
+        ctx.sync()
+        assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"prefill window {W} {(H_q, H_kv, N, M, S, D, fmt, causal)}")
+    ctx.drop(sid)
+
+
+def test_prefill_window_without_suffix(ctx):
+    H_q, H_kv, N, M, D = 4, 2, 1500, 200, 128
+    K, V = synth.gen_kv(77, H_kv, N, D)
+    Q = synth.gen_q(77, H_q, M, D, dtype=np.float16)
+    hm = synth.default_head_map(H_q, H_kv)
+    ctx.store("pwn", 0, dev(K), dev(V))
+    for W in (1, 64, 250, 10 ** 6):
+        O, L = ctx.query("pwn", 0, dev(Q), fa_window=W)
+        O_ref, L_ref = orc.prefix_query(Q, K, V, hm, window=W)
+        ctx.sync()
+        assert_close_o_lse(host(O), host(L), O_ref, L_ref, f"prefill window {W}, no suffix")
+    ctx.drop("pwn")
