@@ -279,11 +279,13 @@ __global__ void __launch_bounds__(128) mlx4_tiles_split_kernel(const uint8_t* __
 // fp16 rounding of the fp32 value. Records are only 4-byte aligned (a record is kv_dim * 5/8 bytes).
 template <typename OutT>
 __global__ void __launch_bounds__(256) dequant_records_kernel(const uint8_t* __restrict__ rec, int64_t N, int H_kv,
-                                                              int D, OutT* __restrict__ out) {
+                                                              int D, int lw, int lD, OutT* __restrict__ out) {
+    // lw, lD: log2 of the words per record and of D when they are powers of two (shifts instead of
+    // 64-bit divisions on every word), else -1
     const int kv_dim = H_kv * D, wpr = kv_dim / 8, rb = kv_dim / 2 + kv_dim / 8;
     const int64_t total = N * wpr;
     for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = w / wpr;
+        const int64_t t = lw >= 0 ? w >> lw : w / wpr;
         const int j = static_cast<int>(w - t * wpr);
         const uint8_t* r = rec + t * rb;
         const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(r) + j);
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(256) dequant_records_kernel(const uint8_t* __r
         float x[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) x[k] = fmaf(sc, static_cast<float>((word >> (4 * k)) & 0xFu), bi);
-        const int e0 = 8 * j, g = e0 / D, d0 = e0 - g * D;
+        const int e0 = 8 * j, g = lD >= 0 ? e0 >> lD : e0 / D, d0 = e0 - g * D;
         OutT* o = out + ((int64_t)g * N + t) * D + d0;
         if constexpr (sizeof(OutT) == 4) {
             reinterpret_cast<float4*>(o)[0] = make_float4(x[0], x[1], x[2], x[3]);
@@ -466,11 +468,17 @@ cudaError_t launch_dequant_records(const void* rec, int64_t N, int H_kv, int D, 
                                    int sms) {
     const int64_t words = N * (H_kv * D / 8);
     const int blocks = grid_for(words, 256, sms);
+    auto log2_exact = [](int v) {
+        int l = 0;
+        while ((1 << l) < v) ++l;
+        return (1 << l) == v ? l : -1;
+    };
+    const int lw = log2_exact(H_kv * D / 8), lD = log2_exact(D);
     if (out_f16)
-        dequant_records_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D,
+        dequant_records_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D, lw, lD,
                                                                 static_cast<__half*>(out));
     else
-        dequant_records_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D,
+        dequant_records_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const uint8_t*>(rec), N, H_kv, D, lw, lD,
                                                                static_cast<float*>(out));
     return cudaGetLastError();
 }
