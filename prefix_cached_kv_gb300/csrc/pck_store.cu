@@ -63,7 +63,8 @@ __device__ __forceinline__ uint32_t codes_of(const float (&x)[8], float sf, floa
 // (measured: 107 us against 119 us for two pairs per iteration at four CTAs, 256 MB of input).
 template <typename SrcT>
 __global__ void __launch_bounds__(256, 6) quantize_mlx4g32_kernel(const SrcT* __restrict__ X, int64_t rows,
-                                                                   int kv_dim, uint8_t* __restrict__ out) {
+                                                                   int kv_dim, int lw, uint8_t* __restrict__ out) {
+    // lw: log2 of the words per row when a power of two (a shift instead of a 64-bit division), else -1
     const int wpr = kv_dim / 8;                 // words per row
     const int64_t total = rows * wpr / 2;       // word pairs; even per group, a warp never splits one
     const int rec = kv_dim / 2 + kv_dim / 8;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(256, 6) quantize_mlx4g32_kernel(const SrcT* __
         const uint32_t w1 = codes_of(x[1], sf, bf, rcp);
         if (live) {
             const int64_t wi = pi * 2;
-            const int64_t row = wi / wpr;
+            const int64_t row = lw >= 0 ? wi >> lw : wi / wpr;
             const int word = static_cast<int>(wi - row * wpr);
             uint8_t* r = out + row * rec;
             reinterpret_cast<uint32_t*>(r)[word] = w0;        // records are only 4-byte aligned
@@ -416,11 +417,14 @@ cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim
     int64_t total = rows * (kv_dim / 16);   // word pairs
     int threads = 256;
     int blocks = grid_for(total, threads, sms);
+    int lw = 0;
+    while ((1 << lw) < kv_dim / 8) ++lw;
+    if ((1 << lw) != kv_dim / 8) lw = -1;
     if (src_f16)
-        quantize_mlx4g32_kernel<__half><<<blocks, threads, 0, st>>>(static_cast<const __half*>(X), rows, kv_dim,
+        quantize_mlx4g32_kernel<__half><<<blocks, threads, 0, st>>>(static_cast<const __half*>(X), rows, kv_dim, lw,
                                                                      static_cast<uint8_t*>(out));
     else
-        quantize_mlx4g32_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float*>(X), rows, kv_dim,
+        quantize_mlx4g32_kernel<float><<<blocks, threads, 0, st>>>(static_cast<const float*>(X), rows, kv_dim, lw,
                                                                     static_cast<uint8_t*>(out));
     return cudaGetLastError();
 }
