@@ -32,7 +32,7 @@ bool plan_decode(DecodeParams* p, int64_t total, int vmax, int n_items, int S_su
     if (max_warps < 1) max_warps = 1;
     if (max_warps > max_slots - fixed) max_warps = max_slots - fixed;
     int64_t tpw = (total + max_warps - 1) / max_warps;
-    tpw = std::max<int64_t>(tpw, (vmax + 31) / 32);         // at most ~32 prefix pieces per item
+    tpw = std::max<int64_t>(tpw, std::max<int64_t>((vmax + 63) / 64, 4));   // at most ~64 pieces per item, at least 4 tiles each
     if (tpw < 2) tpw = 2;
     int64_t n_workers = 0;
     p->aligned = 0;
