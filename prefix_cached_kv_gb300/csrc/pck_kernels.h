@@ -42,9 +42,9 @@ DecodeLaunchInfo decode_launch_info_xd(int fmt, int D, int ncb);   // D in {32, 
 cudaError_t launch_decode_xd(int fmt, int D, const DecodeParams& p, int n_ctas, cudaStream_t st);
 // How one decode launch splits its work. Dense: `total` units (16-token tiles) over items of at
 // most `vmax` units each are cut into ranges of tpw units, one per prefix worker (a warp), with
-// at least max(ceil(vmax / 64), 4) units per range so that an item has at most ~64 pieces to merge, and at
-// most one wave of resident warps (ctas_per_sm CTAs of DECODE_WARPS warps on each of `sms` SMs)
-// together with the items' suffix warps. Sparse: `total` bounds the units, and every resident
+// at least max(ceil(vmax / 64), 4) units per range (an item has at most ~64 pieces to merge, and
+// a piece is worth its start-up), and at most one wave of resident warps (ctas_per_sm CTAs of
+// DECODE_WARPS warps on each of `sms` SMs) together with the items' suffix warps. Sparse: `total` bounds the units, and every resident
 // prefix warp takes a share on the device. The partial slots the launch writes (one per prefix
 // worker, per item, and per suffix piece) must fit `max_slots`; ranges grow until they do.
 struct DecodePlan {
