@@ -224,7 +224,10 @@ int pck_query_batch_host(pck_ctx *ctx, int n, const pck_query_desc *descs, int H
  * and the suffix, merge); otherwise the block scores of all queries run in one scoring launch,
  * their top-K selections in one selection launch, and their gathers (+ suffixes) in one split-K
  * decode and its merge (four launches). Each query is as pck_query_sparse_auto_fused
- * (S_suf > 0) or pck_query_sparse_auto (S_suf == 0) would compute it alone.
+ * (S_suf > 0) or pck_query_sparse_auto (S_suf == 0) would compute it alone. The first sparse
+ * call on a slot builds its block means (and, for the one-kernel form, their fp16 hi + lo copy)
+ * with stream-ordered allocations: make it, or pck_build_block_means, before capturing the call
+ * in a CUDA graph.
  * 1 <= n <= PCK_MAX_BATCH. Errors: EINVAL, EUNSUPPORTED (slots of different N, B not a multiple
  * of 16, K_top > 64, fa_window), MISS / COLDMISS for an absent slot. */
 int pck_query_sparse_batch(pck_ctx *ctx, int n, const pck_sparse_desc *descs, int H_q, int H_kv, int D,
