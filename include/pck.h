@@ -128,7 +128,8 @@ int pck_lookup(pck_ctx *ctx, const char *sid, int layer);
  * on `stream` (queued work on that stream still sees valid K/V). Returns the number dropped. */
 int pck_drop(pck_ctx *ctx, const char *sid, int layer, void *stream);
 
-/* Precompute the block means of K (fp32, [H_kv, ceil(N/B), D]) used by the sparse selector.
+/* Precompute the block means of K (fp32, [H_kv, ceil(N/B), D]) used by the sparse selector, and
+ * (at D in {64, 128, 256} with at most 1024 blocks) their fp16 hi + lo copy for the one-kernel form.
  * The sparse queries build them on first use per (slot, B); this lets a caller do it at store
  * time (e.g. before capturing a CUDA graph). Only fp16 slots. */
 int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void *stream);
@@ -225,9 +226,9 @@ int pck_query_batch_host(pck_ctx *ctx, int n, const pck_query_desc *descs, int H
  * their top-K selections in one selection launch, and their gathers (+ suffixes) in one split-K
  * decode and its merge (four launches). Each query is as pck_query_sparse_auto_fused
  * (S_suf > 0) or pck_query_sparse_auto (S_suf == 0) would compute it alone. The first sparse
- * call on a slot builds its block means (and, for the one-kernel form, their fp16 hi + lo copy)
- * with stream-ordered allocations: make it, or pck_build_block_means, before capturing the call
- * in a CUDA graph.
+ * call on a slot builds its block means (and their fp16 hi + lo copy, which the one-kernel form
+ * scores from) with stream-ordered allocations: call pck_build_block_means, or make a first
+ * call, before capturing the call in a CUDA graph.
  * 1 <= n <= PCK_MAX_BATCH. Errors: EINVAL, EUNSUPPORTED (slots of different N, B not a multiple
  * of 16, K_top > 64, fa_window), MISS / COLDMISS for an absent slot. */
 int pck_query_sparse_batch(pck_ctx *ctx, int n, const pck_sparse_desc *descs, int H_q, int H_kv, int D,

@@ -487,33 +487,6 @@ int pck_drop(pck_ctx* c, const char* sid, int layer, void* stream) {
     return dropped;
 }
 
-int pck_build_block_means(pck_ctx* c, const char* sid, int layer, int B, void* stream) {
-    if (!c) return PCK_EINVAL;
-    Slot* s = nullptr;
-    int rc = find_slot(c, sid, layer, &s);
-    if (rc != PCK_OK) return rc;
-    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "block means are built for fp16 slots only");
-    if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
-    if (s->kmean.count(B)) return PCK_OK;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int nb = (s->N + B - 1) / B;
-    float* km = nullptr;
-    const size_t bytes = static_cast<size_t>(s->H_kv) * nb * s->D * sizeof(float);
-    if (cudaMallocAsync(reinterpret_cast<void**>(&km), bytes, st) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(c, PCK_ENOMEM, "cannot allocate block means");
-    }
-    cudaError_t e = launch_block_means(s->tiles, s->H_kv, s->N, s->D, s->ntiles, B, km, st, c->sms);
-    if (e != cudaSuccess) {
-        cudaFreeAsync(km, st);
-        return cuda_fail(c, e, "block means launch");
-    }
-    s->kmean[B] = km;
-    s->bytes += bytes;
-    c->bytes_resident += static_cast<int64_t>(bytes);
-    return PCK_OK;
-}
-
 // The split (fp16 hi + lo, tile layout) copy of a slot's block means, built from the fp32 ones.
 static int build_block_means_split(pck_ctx* c, Slot* s, int B, cudaStream_t st) {
     if (s->kmean_split.count(B)) return PCK_OK;
@@ -532,6 +505,38 @@ static int build_block_means_split(pck_ctx* c, Slot* s, int B, cudaStream_t st) 
     s->kmean_split[B] = out;
     s->bytes += bytes;
     c->bytes_resident += static_cast<int64_t>(bytes);
+    return PCK_OK;
+}
+
+int pck_build_block_means(pck_ctx* c, const char* sid, int layer, int B, void* stream) {
+    if (!c) return PCK_EINVAL;
+    Slot* s = nullptr;
+    int rc = find_slot(c, sid, layer, &s);
+    if (rc != PCK_OK) return rc;
+    if (s->fmt != PCK_FMT_FP16) return fail(c, PCK_EUNSUPPORTED, "block means are built for fp16 slots only");
+    if (B < 16 || B % 16) return fail(c, PCK_EUNSUPPORTED, "B=%d (must be a positive multiple of 16)", B);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s->kmean.count(B)) {
+        const int nb0 = (s->N + B - 1) / B;
+        return sparse_fused_ok(s->D, nb0, 1) ? build_block_means_split(c, s, B, st) : PCK_OK;
+    }
+    const int nb = (s->N + B - 1) / B;
+    float* km = nullptr;
+    const size_t bytes = static_cast<size_t>(s->H_kv) * nb * s->D * sizeof(float);
+    if (cudaMallocAsync(reinterpret_cast<void**>(&km), bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, PCK_ENOMEM, "cannot allocate block means");
+    }
+    cudaError_t e = launch_block_means(s->tiles, s->H_kv, s->N, s->D, s->ntiles, B, km, st, c->sms);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(km, st);
+        return cuda_fail(c, e, "block means launch");
+    }
+    s->kmean[B] = km;
+    s->bytes += bytes;
+    c->bytes_resident += static_cast<int64_t>(bytes);
+    // the copy the one-kernel sparse form scores from, where that form applies
+    if (sparse_fused_ok(s->D, nb, 1)) return build_block_means_split(c, s, B, st);
     return PCK_OK;
 }
 
