@@ -131,7 +131,10 @@ int pck_drop(pck_ctx *ctx, const char *sid, int layer, void *stream);
 /* Precompute the block means of K (fp32, [H_kv, ceil(N/B), D]) used by the sparse selector, and
  * (at D in {64, 128, 256} with at most 1024 blocks) their fp16 hi + lo copy for the one-kernel form.
  * The sparse queries build them on first use per (slot, B); this lets a caller do it at store
- * time (e.g. before capturing a CUDA graph). Only fp16 slots. */
+ * time (e.g. before capturing a CUDA graph). Only fp16 slots. The means of all slots share
+ * device memory the context sets aside in large chunks (packed together, the batched sparse
+ * form reads them faster); a build that would allocate while `stream` is being captured
+ * returns PCK_EINVAL, so a captured sparse call needs its slots' means built beforehand. */
 int pck_build_block_means(pck_ctx *ctx, const char *sid, int layer, int B, void *stream);
 
 /* ATTEND.PREFIX.QUERY <sid> <layer> <H> <D> <top_k> <Q_blob> [<fa_window>].

@@ -33,12 +33,33 @@ constexpr int WS_COUNTERS = 1 << 16;
 constexpr int WS_SEL_BYTES = 1 << 20;                   // sparse selection lists
 constexpr size_t WS_SCORES_BYTES = size_t(16) << 20;
 constexpr size_t WS_SUFFIX_BYTES = size_t(32) << 20;    // batched-Q suffix staged in the slot layout
+constexpr size_t ARENA_CHUNK = size_t(256) << 20;      // block-means arena: chunk size
+constexpr size_t ARENA_ALIGN = 256;
+
+// The block means of every slot (fp32 and split), packed side by side into a few large chunks
+// instead of one pool allocation each between the slots' tiles: the batched sparse kernel
+// streams the means of many sessions at once, and packed together they read ~11 % faster
+// (0.65 against 0.73 us per session on the 64-session sparse batch). A freed range is reused
+// once the work its freeing stream had queued has completed (an event recorded there).
+struct MeansArena {
+    struct Chunk {
+        uint8_t* base;
+        size_t size, top;
+    };
+    struct Range {
+        uint8_t* p;
+        size_t bytes;
+        cudaEvent_t ready;   // nullptr: reusable now
+    };
+    std::vector<Chunk> chunks;
+    std::vector<Range> freed;
+};
 
 struct Slot {
     int fmt = 0, H_kv = 0, N = 0, D = 0, ntiles = 0;
     uint8_t* tiles = nullptr;
     size_t bytes = 0;
-    std::unordered_map<int, float*> kmean;  // block size -> [H_kv, nb, D] fp32
+    std::unordered_map<int, float*> kmean;  // block size -> [H_kv, nb, D] fp32 (in the means arena)
     // block size -> the same means as fp16 hi + lo pairs in the tensor-core tile layout (16 blocks
     // a tile, [H_kv][ceil(nb / 16)][hi part | lo part]; see launch_block_means_split)
     std::unordered_map<int, uint8_t*> kmean_split;
@@ -63,6 +84,7 @@ struct pck_ctx {
     float* scores = nullptr;
     uint8_t* suf_ws = nullptr;
     uint8_t* host_stage = nullptr;   // host-buffer calls: their inputs, copied in (PCK_HOST_STAGE_BYTES)
+    MeansArena means;
     int64_t queries = 0, stores = 0, evictions = 0;
     int64_t bytes_resident = 0;
     DecodeLaunchInfo dinfo[2][16];   // [format][head dimension x column blocks]
@@ -123,10 +145,80 @@ const DecodeLaunchInfo& dinfo(pck_ctx* c, int fmt, int D, int ncb) {
     return c->dinfo[fmt][i];
 }
 
+bool capturing(cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+size_t arena_round(size_t bytes) { return (bytes + ARENA_ALIGN - 1) & ~(ARENA_ALIGN - 1); }
+
+// A range of the means arena: a freed range whose stream work has completed, else the top of a
+// chunk, else a new chunk (nullptr when the device is out of memory).
+uint8_t* arena_alloc(pck_ctx* c, size_t bytes) {
+    bytes = arena_round(bytes);
+    MeansArena& A = c->means;
+    for (size_t i = 0; i < A.freed.size(); ++i) {
+        MeansArena::Range& r = A.freed[i];
+        if (r.bytes < bytes) continue;
+        if (r.ready) {
+            if (cudaEventQuery(r.ready) != cudaSuccess) {
+                cudaGetLastError();   // not ready yet (or a sticky error, reported by the next call)
+                continue;
+            }
+            cudaEventDestroy(r.ready);
+            r.ready = nullptr;
+        }
+        uint8_t* p = r.p;
+        if (r.bytes == bytes) {
+            A.freed.erase(A.freed.begin() + static_cast<std::ptrdiff_t>(i));
+        } else {
+            r.p += bytes;
+            r.bytes -= bytes;
+        }
+        return p;
+    }
+    for (MeansArena::Chunk& ch : A.chunks)
+        if (ch.size - ch.top >= bytes) {
+            uint8_t* p = ch.base + ch.top;
+            ch.top += bytes;
+            return p;
+        }
+    const size_t sz = std::max(ARENA_CHUNK, bytes);
+    uint8_t* base = nullptr;
+    if (cudaMalloc(reinterpret_cast<void**>(&base), sz) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    A.chunks.push_back({base, sz, bytes});
+    return base;
+}
+
+// Returns a range to the arena once the work queued on st so far (the last reads of it in stream
+// order) has completed. Without an event the range stays unused until the context ends.
+void arena_free(pck_ctx* c, void* p, size_t bytes, cudaStream_t st) {
+    cudaEvent_t ev = nullptr;
+    if (capturing(st) || cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(ev, st) != cudaSuccess) {
+        cudaGetLastError();
+        if (ev) cudaEventDestroy(ev);
+        return;
+    }
+    c->means.freed.push_back({static_cast<uint8_t*>(p), arena_round(bytes), ev});
+}
+
+size_t kmean_bytes(const Slot& s, int B) { return static_cast<size_t>(s.H_kv) * ((s.N + B - 1) / B) * s.D * sizeof(float); }
+size_t kmean_split_bytes(const Slot& s, int B) {
+    return static_cast<size_t>(s.H_kv) * (((s.N + B - 1) / B + 15) / 16) * 64 * s.D;
+}
+
 void free_slot(pck_ctx* c, Slot& s, cudaStream_t st) {
     if (s.tiles) cudaFreeAsync(s.tiles, st);
-    for (auto& kv : s.kmean) cudaFreeAsync(kv.second, st);
-    for (auto& kv : s.kmean_split) cudaFreeAsync(kv.second, st);
+    for (auto& kv : s.kmean) arena_free(c, kv.second, kmean_bytes(s, kv.first), st);
+    for (auto& kv : s.kmean_split) arena_free(c, kv.second, kmean_split_bytes(s, kv.first), st);
     c->bytes_resident -= static_cast<int64_t>(s.bytes);
     s.tiles = nullptr;
     s.kmean.clear();
@@ -355,6 +447,9 @@ void pck_destroy(pck_ctx* c) {
     cudaDeviceSynchronize();
     for (auto& kv : c->slots) free_slot(c, kv.second, nullptr);
     cudaDeviceSynchronize();
+    for (auto& r : c->means.freed)
+        if (r.ready) cudaEventDestroy(r.ready);
+    for (auto& ch : c->means.chunks) cudaFree(ch.base);
     cudaFree(c->partials);
     cudaFree(c->counters);
     cudaFree(c->dev_err);
@@ -490,16 +585,14 @@ int pck_drop(pck_ctx* c, const char* sid, int layer, void* stream) {
 // The split (fp16 hi + lo, tile layout) copy of a slot's block means, built from the fp32 ones.
 static int build_block_means_split(pck_ctx* c, Slot* s, int B, cudaStream_t st) {
     if (s->kmean_split.count(B)) return PCK_OK;
+    if (capturing(st)) return fail(c, PCK_EINVAL, "block means are built outside a stream capture");
     const int nb = (s->N + B - 1) / B;
-    const size_t bytes = static_cast<size_t>(s->H_kv) * ((nb + 15) / 16) * 64 * s->D;
-    uint8_t* out = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&out), bytes, st) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(c, PCK_ENOMEM, "cannot allocate split block means");
-    }
+    const size_t bytes = kmean_split_bytes(*s, B);
+    uint8_t* out = arena_alloc(c, bytes);
+    if (!out) return fail(c, PCK_ENOMEM, "cannot allocate split block means");
     const cudaError_t e = launch_block_means_split(s->kmean[B], s->H_kv, nb, s->D, out, st);
     if (e != cudaSuccess) {
-        cudaFreeAsync(out, st);
+        arena_free(c, out, bytes, st);
         return cuda_fail(c, e, "split block means launch");
     }
     s->kmean_split[B] = out;
@@ -520,16 +613,14 @@ int pck_build_block_means(pck_ctx* c, const char* sid, int layer, int B, void* s
         const int nb0 = (s->N + B - 1) / B;
         return sparse_fused_ok(s->D, nb0, 1) ? build_block_means_split(c, s, B, st) : PCK_OK;
     }
+    if (capturing(st)) return fail(c, PCK_EINVAL, "block means are built outside a stream capture");
     const int nb = (s->N + B - 1) / B;
-    float* km = nullptr;
-    const size_t bytes = static_cast<size_t>(s->H_kv) * nb * s->D * sizeof(float);
-    if (cudaMallocAsync(reinterpret_cast<void**>(&km), bytes, st) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(c, PCK_ENOMEM, "cannot allocate block means");
-    }
+    const size_t bytes = kmean_bytes(*s, B);
+    float* km = reinterpret_cast<float*>(arena_alloc(c, bytes));
+    if (!km) return fail(c, PCK_ENOMEM, "cannot allocate block means");
     cudaError_t e = launch_block_means(s->tiles, s->H_kv, s->N, s->D, s->ntiles, B, km, st, c->sms);
     if (e != cudaSuccess) {
-        cudaFreeAsync(km, st);
+        arena_free(c, km, bytes, st);
         return cuda_fail(c, e, "block means launch");
     }
     s->kmean[B] = km;

@@ -252,6 +252,67 @@ def test_sparse_batch_in_a_cuda_graph(ctx):
         ctx.drop(f"sph{r}")
 
 
+def test_block_means_arena_reuse(ctx):
+    """The block means live in the context's arena: a dropped slot's means are reused by a later
+    slot (after the drop's stream work), a replaced slot gets fresh means, and the slots that stay
+    keep theirs. Every query is checked against the oracle."""
+    H_q, H_kv, N, D, B, Kt, S = 4, 2, 3000, 128, 64, 4, 8
+    hm = synth.default_head_map(H_q, H_kv)
+
+    def put(sid, seed):
+        K, V = synth.gen_kv(seed, H_kv, N, D)
+        ctx.store(sid, 0, dev(K), dev(V))
+        ctx.build_block_means(sid, 0, B)
+        return K, V
+
+    def check(sid, seed, K, V):
+        Q = synth.gen_q(seed, H_q, 1, D)[:, 0]
+        Ks, Vs = synth.gen_suffix(seed, H_kv, S, D)
+        O, L, idx = ctx.query_sparse_auto(sid, 0, dev(Q), B, Kt, H_kv, K_suf=dev(Ks), V_suf=dev(Vs))
+        O_ref, L_ref, _, scores = orc.sparse_query(Q, K, V, hm, B, Kt, Ks, Vs)
+        _check_idx(host(idx), scores, Kt)
+        near = orc.topk_margin(scores, Kt) < TIE_EPS
+        assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], sid)
+
+    kv = {r: put(f"ar{r}", 900 + r) for r in range(3)}
+    ctx.drop("ar1")
+    torch.cuda.synchronize()
+    kv[3] = put("ar3", 903)                       # takes the range ar1 freed
+    kv[0] = put("ar0", 910)                       # replaced: old means freed, new ones built
+    for r, seed in ((0, 910), (2, 902), (3, 903)):
+        check(f"ar{r}", seed, *kv[r])
+    for r in (0, 2, 3):
+        ctx.drop(f"ar{r}")
+
+
+def test_block_means_not_built_during_capture(ctx):
+    """A sparse call whose block means are missing cannot build them while its stream is being
+    captured: it returns PCK_EINVAL before launching anything, and works once they are built."""
+    from prefix_cached_kv_gb300 import binding
+    H_q, H_kv, N, D, B, Kt = 4, 2, 1000, 64, 64, 2
+    K, V = synth.gen_kv(950, H_kv, N, D)
+    Q = dev(synth.gen_q(950, H_q, 1, D)[:, 0])
+    ctx.store("cap", 0, dev(K), dev(V))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        g.capture_begin()
+        try:
+            with pytest.raises(binding.PckError) as e:
+                ctx.query_sparse_auto("cap", 0, Q, B, Kt, H_kv)
+        finally:
+            g.capture_end()
+    assert e.value.code == binding.EINVAL
+    del g
+    ctx.build_block_means("cap", 0, B)
+    O, L, idx = ctx.query_sparse_auto("cap", 0, Q, B, Kt, H_kv)
+    O_ref, L_ref, _, scores = orc.sparse_query(host(Q), K, V, synth.default_head_map(H_q, H_kv), B, Kt)
+    near = orc.topk_margin(scores, Kt) < TIE_EPS
+    assert_close_o_lse(host(O)[~near], host(L)[~near], O_ref[~near], L_ref[~near], "after capture")
+    ctx.drop("cap")
+
+
 @pytest.mark.parametrize("H_q,H_kv,hm", [
     (6, 3, [2, 0, 1, 1, 0, 2]),         # q heads of a kv head not adjacent
     (4, 2, [1, 1, 1, 1]),               # kv head 0 has no q heads: nothing scored or selected there
