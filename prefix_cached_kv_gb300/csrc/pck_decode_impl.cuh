@@ -993,7 +993,6 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         fence_mbar_init();
     }
     __syncwarp();
-    if (!sparse) grid_dep_wait_then_release();
 
     auto issue = [&](const Chunk& c, int s) {
         if (lane == 0) {
@@ -1012,6 +1011,10 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         }
     };
 
+    // The first stages of a dense launch are filled before the wait for the previous kernel: they
+    // read only resident slot tiles, which no kernel that lets its dependents start early writes
+    // (the store-side kernels run to completion before the next launch), so the first bytes
+    // stream in while the previous merge finishes. Q, the suffix and the partials come after it.
     int inflight = 0;
     for (int s = 0; s < C::NSTAGE; ++s) {
         Chunk c;
@@ -1019,6 +1022,7 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
         issue(c, s);
         ++inflight;
     }
+    if (!sparse) grid_dep_wait_then_release();
 
     StateT st;
     if constexpr (FMT == FMT_FP16) st.qsm = smem_u32(qarea);
