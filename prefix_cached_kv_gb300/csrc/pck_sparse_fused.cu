@@ -90,8 +90,6 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
         sm.nuniq = 0;
     }
     __syncthreads();
-    // Q, the block means and the slot may come from the previous kernel of the stream
-    grid_dep_wait_then_release();
 
     // ---------------------------------------------------------------- 1. scores
     // Each warp streams its own groups of 16 blocks (w, w + W, ...) of the split block means
@@ -112,6 +110,10 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
     };
     const int mine = warp < nbg ? (nbg - warp + FW - 1) / FW : 0;   // groups of this warp
     for (int j = 0; j < min(F_NSS, mine); ++j) issue_slab(j, j);
+    // The first stages above read only block means, which no kernel that lets its dependents start
+    // early writes (they are built by kernels that run to completion); Q, the suffix and the
+    // outputs may belong to the previous kernel of the stream, so wait for it from here on.
+    grid_dep_wait_then_release();
     struct { int q_f16; float scale_log2; int* err; } qscale{p.q_f16, p.tau, p.err};
     F16State<D, NCB> sq;   // B fragments of tau * q (hi / lo parts), as the decode builds them
     sq.qsm = 0;
