@@ -676,7 +676,9 @@ static int query_common(pck_ctx* c, const char* sid, int layer, int H_q, int D, 
         return fail(c, PCK_EUNSUPPORTED, "suffix of %d tokens exceeds the staging workspace", S_suf);
     const int suf_ntiles = (S_suf + TILE_TOK - 1) / TILE_TOK;
     if (S_suf > 0) {   // stage the suffix in the resident layout (the MMA operand layout)
-        cudaError_t e = launch_relayout_fp16(K_suf, V_suf, 1, s->H_kv, S_suf, D, suf_ntiles, c->suf_ws, st, c->sms, DK);
+        // released early: the attention kernel fetches its first resident prefix blocks while this
+        // runs, and waits for it before touching the staged suffix
+        cudaError_t e = launch_relayout_fp16(K_suf, V_suf, 1, s->H_kv, S_suf, D, suf_ntiles, c->suf_ws, st, c->sms, DK, 1);
         if (e != cudaSuccess) return cuda_fail(c, e, "suffix staging launch");
     }
     uint8_t* kv = s->tiles;

@@ -12,9 +12,10 @@ constexpr int PCK_MAXH = 64;
 
 // store side
 cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim, void* out, cudaStream_t st, int sms);
-// DS: head dimension of the written layout (0 = D; DS > D pads every row with zero columns)
+// DS: head dimension of the written layout (0 = D; DS > D pads every row with zero columns);
+// release: 1 lets the next kernel start before this one ends (only for a reader that waits for it)
 cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
-                                 void* out, cudaStream_t st, int sms, int DS = 0);
+                                 void* out, cudaStream_t st, int sms, int DS = 0, int release = 0);
 cudaError_t launch_relayout_mlx4(const void* Krec, const void* Vrec, int head_rows, int H_kv, int N, int D, int ntiles,
                                  void* out, cudaStream_t st, int sms);
 // QUERY_SPARSE: the tokens idx[h][0 .. counts[h]) of kv head head_map[h] of a resident fp16 slot,

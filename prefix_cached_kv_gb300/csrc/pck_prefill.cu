@@ -347,6 +347,27 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                      ::"r"(smem_u32(tmem_slot)), "r"(C::TMEM_COLS) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    tc_fence_before();
+    __syncthreads();   // barriers and the tensor-memory address visible to every warp
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // This grid may start before the previous kernel of the stream has finished (programmatic
+    // dependence): the producer fetches the first stages of resident prefix blocks at once (no
+    // kernel that releases its dependents early writes a slot's tiles, and a dequantised mlx4g32
+    // copy is written by a kernel that runs to completion first); Q, the staged suffix and every
+    // output wait for the previous grid.
+    int pre = 0;   // stages issued before the wait (producer lane)
+    if (warp == PF_LOAD_WARP && lane == 0) {
+        for (; pre < PF_ST && pre < nbl && kb0 + pre < nbp; ++pre) {
+            const KeyBlock kb = key_block(P, g, kb0 + pre, nbp, D);
+            const uint32_t bytes = kb.ntile * 32 * D;
+            mbar_arrive_expect_tx(bar + B_KF + 8 * pre, bytes);
+            bulk_g2s(s_base + C::OFF_K + pre * C::KV_BYTES, kb.k, bytes, bar + B_KF + 8 * pre);
+            mbar_arrive_expect_tx(bar + B_VF + 8 * pre, bytes);
+            bulk_g2s(s_base + C::OFF_V + pre * C::KV_BYTES, kb.v, bytes, bar + B_VF + 8 * pre);
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid < PF_ROWS) {   // Q row -> core-matrix layout (zeros for rows past the end)
         const int r = row0 + tid;
         uint8_t* qs = smem + C::OFF_Q;
@@ -370,10 +391,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         }
         fence_proxy_async_smem();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    __syncthreads();   // the Q tile
     bool failed = false;
 
     if (warp == PF_LOAD_WARP) {
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         // needs P(j-2).V done, and whichever stage frees first is refilled first (V never runs
         // ahead of K). Idle polls back off and are bounded like every other wait.
         if (lane == 0) {
-            int jk = 0, jv = 0;
+            int jk = pre, jv = pre;
             uint32_t idle = 0;
             while (jv < nbl) {
                 bool moved = false;
@@ -801,7 +819,9 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    // The merge is launched programmatically (PDL) and waits for the attention grid as a whole.
+    // Both launches are programmatic (PDL): the attention kernel may start while the suffix staging
+    // runs (its prologue says what it reads before waiting), and the merge waits for the attention
+    // grid as a whole.
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
@@ -811,7 +831,7 @@ static cudaError_t launch_prefill_t(const PfParams& P, cudaStream_t st) {
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = at;
-    cfg.numAttrs = 0;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, P);
     if (e != cudaSuccess || P.n_split == 1) return e;
     const int rows = P.n_tiles * PF_ROWS;

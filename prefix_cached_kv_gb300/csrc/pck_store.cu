@@ -145,9 +145,14 @@ __device__ __forceinline__ void write_fp16_tile(const __half (&sm)[2][TILE_TOK][
 // shared memory (zeros past N), then written in the resident layout of head dimension DS >= D
 // (columns D .. DS-1 zero: the [hi | lo] form of fp16 values, whose lo parts are 0). MAXD >= DS
 // sizes the staging (256, or 512 for the widest heads, which halves the CTAs an SM holds).
+// release: let the next kernel of the stream be scheduled at once (the batched-Q suffix staging,
+// whose reader waits for this grid before it touches the staged suffix); the store path never
+// does, so a slot's tiles are complete before any later kernel starts.
 template <typename SrcT, int MAXD>
 __global__ void __launch_bounds__(128) relayout_fp16_kernel(const SrcT* __restrict__ K, const SrcT* __restrict__ V,
-                                                            int N, int D, int DS, int ntiles, uint4* __restrict__ out) {
+                                                            int N, int D, int DS, int ntiles, uint4* __restrict__ out,
+                                                            int release) {
+    if (release) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ __align__(16) __half sm[2][TILE_TOK][MAXD + 8];
     const int j = blockIdx.x, g = blockIdx.y;
     const int t0 = j * TILE_TOK;
@@ -430,7 +435,7 @@ cudaError_t launch_quantize(const void* X, int src_f16, int64_t rows, int kv_dim
 }
 
 cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int H_kv, int N, int D, int ntiles,
-                                 void* out, cudaStream_t st, int sms, int DS) {
+                                 void* out, cudaStream_t st, int sms, int DS, int release) {
     (void)sms;
     if (DS == 0) DS = D;
     if (DS > 512 || D % 8 != 0 || DS % 8 != 0 || DS < D) return cudaErrorInvalidValue;
@@ -441,11 +446,11 @@ cudaError_t launch_relayout_fp16(const void* K, const void* V, int src_f16, int 
     const float* vf = static_cast<const float*>(V);
     uint4* o = static_cast<uint4*>(out);
     if (DS <= 256) {
-        if (src_f16) relayout_fp16_kernel<__half, 256><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o);
-        else relayout_fp16_kernel<float, 256><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o);
+        if (src_f16) relayout_fp16_kernel<__half, 256><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o, release);
+        else relayout_fp16_kernel<float, 256><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o, release);
     } else {
-        if (src_f16) relayout_fp16_kernel<__half, 512><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o);
-        else relayout_fp16_kernel<float, 512><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o);
+        if (src_f16) relayout_fp16_kernel<__half, 512><<<grid, 128, 0, st>>>(kh, vh, N, D, DS, ntiles, o, release);
+        else relayout_fp16_kernel<float, 512><<<grid, 128, 0, st>>>(kf, vf, N, D, DS, ntiles, o, release);
     }
     return cudaGetLastError();
 }
