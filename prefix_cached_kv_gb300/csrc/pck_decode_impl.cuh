@@ -994,16 +994,18 @@ __device__ void prefix_worker(const DecodeParams& p, int w, int lane, uint8_t* r
     }
     __syncwarp();
 
+    // the slot's tiles are read once per launch: first out of L2
+    const uint64_t pol = l2_evict_first();
     auto issue = [&](const Chunk& c, int s) {
         if (lane == 0) {
             if (c.nreal > 0) {
                 mbar_arrive_expect_tx(bar_s + 8 * s, c.nreal * C::TB);
                 if constexpr (FMT == FMT_FP16) {
                     const uint32_t half = c.nreal * 32 * D;
-                    bulk_g2s(ring_s + s * C::STAGE, c.src, half, bar_s + 8 * s);
-                    bulk_g2s(ring_s + s * C::STAGE + C::STAGE / 2, c.src2, half, bar_s + 8 * s);
+                    bulk_g2s_hint(ring_s + s * C::STAGE, c.src, half, bar_s + 8 * s, pol);
+                    bulk_g2s_hint(ring_s + s * C::STAGE + C::STAGE / 2, c.src2, half, bar_s + 8 * s, pol);
                 } else {
-                    bulk_g2s(ring_s + s * C::STAGE, c.src, c.nreal * C::TB, bar_s + 8 * s);
+                    bulk_g2s_hint(ring_s + s * C::STAGE, c.src, c.nreal * C::TB, bar_s + 8 * s, pol);
                 }
             } else {
                 mbar_arrive(bar_s + 8 * s);
