@@ -102,10 +102,11 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
     float* sc = reinterpret_cast<float*>(regA + C::SCORE_RING);   // [HMAX][F_NBMAX]
     uint8_t* sring = regA + warp * F_NSS * C::SLAB_BYTES;
     const uint32_t sring_s = smem_u32(sring);
+    const uint64_t pol = l2_evict_first();   // block means and union tiles are read once per call
     auto issue_slab = [&](int j, int st) {   // the warp's j-th group (group w + j W) into stage st
         if (lane == 0) {
             mbar_arrive_expect_tx(sbar(st), C::SLAB_BYTES);
-            bulk_g2s(sring_s + st * C::SLAB_BYTES, kmg + (size_t)(warp + j * FW) * C::SLAB_BYTES, C::SLAB_BYTES, sbar(st));
+            bulk_g2s_hint(sring_s + st * C::SLAB_BYTES, kmg + (size_t)(warp + j * FW) * C::SLAB_BYTES, C::SLAB_BYTES, sbar(st), pol);
         }
     };
     const int mine = warp < nbg ? (nbg - warp + FW - 1) / FW : 0;   // groups of this warp
@@ -283,8 +284,8 @@ __global__ void __launch_bounds__(FCfg<D, NCB>::W * 32, 1) sparse_fused_kernel(c
             const int T = tile_of(u, pk);
             if (lane == 0) {
                 mbar_arrive_expect_tx(dbar(s), C::TB);
-                bulk_g2s(ring_s + s * C::TB, kreg + (size_t)T * 32 * D, 32 * D, dbar(s));
-                bulk_g2s(ring_s + s * C::TB + 32 * D, vreg + (size_t)T * 32 * D, 32 * D, dbar(s));
+                bulk_g2s_hint(ring_s + s * C::TB, kreg + (size_t)T * 32 * D, 32 * D, dbar(s), pol);
+                bulk_g2s_hint(ring_s + s * C::TB + 32 * D, vreg + (size_t)T * 32 * D, 32 * D, dbar(s), pol);
             }
             return;
         }
