@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(256) dequant_records_kernel(const uint8_t* __r
         const int64_t t = lw >= 0 ? w >> lw : w / wpr;
         const int j = static_cast<int>(w - t * wpr);
         const uint8_t* r = rec + t * rb;
-        const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(r) + j);
+        const uint32_t word = __ldcs(reinterpret_cast<const uint32_t*>(r) + j);   // read once: streaming
         const int grp = j >> 2;   // 4 words per group of 32
         const float sc = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(r + kv_dim / 2) + grp)));
         const float bi = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(r + kv_dim / 2 + kv_dim / 16) + grp)));
@@ -303,16 +303,17 @@ __global__ void __launch_bounds__(256) dequant_records_kernel(const uint8_t* __r
         for (int k = 0; k < 8; ++k) x[k] = fmaf(sc, static_cast<float>((word >> (4 * k)) & 0xFu), bi);
         const int e0 = 8 * j, g = lD >= 0 ? e0 >> lD : e0 / D, d0 = e0 - g * D;
         OutT* o = out + ((int64_t)g * N + t) * D + d0;
+        // written once and not read back by this kernel: streaming (evict-first) stores
         if constexpr (sizeof(OutT) == 4) {
-            reinterpret_cast<float4*>(o)[0] = make_float4(x[0], x[1], x[2], x[3]);
-            reinterpret_cast<float4*>(o)[1] = make_float4(x[4], x[5], x[6], x[7]);
+            __stcs(reinterpret_cast<float4*>(o), make_float4(x[0], x[1], x[2], x[3]));
+            __stcs(reinterpret_cast<float4*>(o) + 1, make_float4(x[4], x[5], x[6], x[7]));
         } else {
             uint4 u;
             u.x = h2_as_u32(__floats2half2_rn(x[0], x[1]));
             u.y = h2_as_u32(__floats2half2_rn(x[2], x[3]));
             u.z = h2_as_u32(__floats2half2_rn(x[4], x[5]));
             u.w = h2_as_u32(__floats2half2_rn(x[6], x[7]));
-            *reinterpret_cast<uint4*>(o) = u;
+            __stcs(reinterpret_cast<uint4*>(o), u);
         }
     }
 }
