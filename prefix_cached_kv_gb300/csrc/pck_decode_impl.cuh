@@ -740,7 +740,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     const int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int item = wi / GMAX, h = wi - item * GMAX;
     // the next kernel of the stream may be scheduled now: a decode then sets up its workers from
-    // its launch parameters while this merge runs, and waits for it before reading memory
+    // its launch parameters and fills its first ring stages with resident tiles while this merge
+    // runs, and waits for it before reading anything else
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool live = wi < p.n_desc * p.n_groups * GMAX && h < p.grp[item % p.n_groups].nq;   // warp-uniform
     int w0 = 0, npref = 0;
