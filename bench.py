@@ -10,8 +10,9 @@ device reports) so that no step reads data left in L2 by the previous three. ``v
 prefix KV record bytes per second.
 
 Extra keys report the other rows of the hot path (the same workload as 16 dependent per-layer
-calls, fp16 M=1, batched-Q prefill over fp16 and mlx4g32 prefixes, sparse top-K, cartridge
-quantise + dequantise + 64-session attend), each with its own roofline fraction.
+calls, fp16 M=1 at D=128 and at the other head dimensions, batched-Q prefill over fp16 and
+mlx4g32 prefixes, sparse top-K, cartridge quantise + dequantise + 64-session attend), each with
+its own roofline fraction.
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on all the host cores on the
 same workload and prints the same line with ``"impl": "reference"``. ``--profile ROW`` runs each
@@ -349,6 +350,38 @@ def row_fp16_m1(ctx, torch, pk, reps=20):
             "kv_gbs_single_calls": round(kv / (lat * 1e-3) / 1e9, 1),
             "frac_hbm_single_calls": round(kv / (lat * 1e-3) / 1e9 / pk["hbm"], 4),
             "kv_gbs_64_sessions_one_launch": round(gbs, 1), "frac_hbm_64_sessions": round(gbs / pk["hbm"], 4)}
+
+
+def row_dims(ctx, torch, pk, reps=20):
+    """fp16 M=1 at the other head dimensions (D = 32, 96, 160, 192, 256, 512): 64 sessions of H=8
+    in one batched launch, N = 262,144 / D tokens so every session holds 8.4 MB of K/V whatever D
+    (537 MB per pass, over 4x L2)."""
+    from prefix_cached_kv_gb300 import synth
+    H, R = 8, 64
+    out = {"workload": "prefix_m1_fp16 at other head dims, 64 sessions x H=8 in one launch"}
+    for D in (32, 96, 160, 192, 256, 512):
+        N = 262144 // D
+        for r in range(R):
+            K, V = synth.torch_gen_kv_device(11 + r, H, N, D, "cuda", col_scale=True)
+            ctx.store(f"dims_{r}", 0, K, V)
+        Qs = [torch.randn((H, D), device="cuda") for _ in range(R)]
+        Os = [torch.empty((H, D), device="cuda") for _ in range(R)]
+        Ls = [torch.empty((H,), device="cuda") for _ in range(R)]
+        descs = [dict(sid=f"dims_{r}", layer=0, Q=Qs[r], O=Os[r], LSE=Ls[r]) for r in range(R)]
+        call = ctx.batch_caller(descs, H, H, D)
+        call()
+        g = graph_of(torch, call)
+        for _ in range(3):
+            g.replay()
+        ms = time_replays(torch, g, reps)
+        ctx.sync()
+        del g
+        for r in range(R):
+            ctx.drop(f"dims_{r}")
+        gbs = R * 2 * H * N * D * 2 / (ms * 1e-3) / 1e9
+        out[f"D{D}_kv_gbs"] = round(gbs, 1)
+        out[f"D{D}_frac_hbm"] = round(gbs / pk["hbm"], 4)
+    return out
 
 
 def row_sparse(ctx, torch, pk, reps=10, l2=None):
@@ -743,7 +776,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="all | comma list of main,fp16,sparse,prefill,prefill_mlx,cartridge (main = the headline line)")
+                    help="all | comma list of main,fp16,dims,sparse,prefill,prefill_mlx,cartridge (main = the headline line)")
     ap.add_argument("--profile", default=None,
                     help="fp16 | sparse | quant | warm | prefill | prefill_mlx: one capture-sized run of that row")
     args = ap.parse_args()
@@ -759,7 +792,7 @@ def main():
         profile_row(args.profile, ctx, torch)
         ctx.close()
         return
-    want = {"main", "fp16", "sparse", "prefill", "prefill_mlx", "cartridge"} if args.rows == "all" \
+    want = {"main", "fp16", "dims", "sparse", "prefill", "prefill_mlx", "cartridge"} if args.rows == "all" \
         else set(args.rows.split(","))
     cpu = time_oracle() if rank() == 0 and "main" in want else None   # before any GPU work
     import torch
@@ -779,6 +812,8 @@ def main():
             ctx.drop(f"bench{r}")
     if "fp16" in want:
         rows["A0_A2_fp16_m1"] = row_fp16_m1(ctx, torch, pk)
+    if "dims" in want:
+        rows["N4_other_head_dims"] = row_dims(ctx, torch, pk)
     if "sparse" in want:
         rows["A6_A7_sparse"] = row_sparse(ctx, torch, pk, l2=l2)
     if "prefill" in want:
