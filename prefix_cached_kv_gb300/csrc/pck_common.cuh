@@ -223,15 +223,9 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return d;
 }
 
-// x -> half2(fp16(x), fp16(x - fp16(x))): the hi and lo fp16 parts of x in one register.
-__device__ __forceinline__ uint32_t pack_hilo(float x) {
-    const __half h = __float2half_rn(x);
-    const __half l = __float2half_rn(x - __half2float(h));
-    return static_cast<uint32_t>(__half_as_ushort(h)) | (static_cast<uint32_t>(__half_as_ushort(l)) << 16);
-}
-
-// pack_hilo of two values at once (bit-identical): a = half2(fp16(x0), fp16(x0 - fp16(x0))),
-// b = the same for x1; the hi parts and the lo parts each take one paired conversion.
+// The hi and lo fp16 parts of two values, each pair in one register: a = half2(fp16(x0),
+// fp16(x0 - fp16(x0))), b = the same for x1; the hi parts and the lo parts each take one paired
+// conversion.
 __device__ __forceinline__ void pack_hilo2(float x0, float x1, uint32_t& a, uint32_t& b) {
     const __half2 h = __floats2half2_rn(x0, x1);
     const float2 hf = __half22float2(h);
